@@ -1,0 +1,411 @@
+"""Benchmark: paged GQA decode step (RoPE + KV append, then decode attention)
+on Llama-3.2-1B attention shapes, one JSON line on stdout.
+
+Default workload: batch 32 x 16 layers x 2048-token contexts, 65536 shuffled
+16-token pages (2 GiB bf16 pool).  One step = for every layer: kv_append_rope
+(one new token per sequence, K rotated and appended, q rotated) followed by
+paged_gqa_decode.  The pool (2 GiB per step) is larger than L2, so no flush is
+needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                    [--workload batch32|stress256]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(replicas, weak scaling, no collective on the data path); rank 0 prints the
+line with the max elapsed time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")   # the CPU oracle baseline runs on one core
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged GQA decode: KV-read GB/s (% of HBM peak), decode tokens/s, µs/layer"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", choices=["batch32", "stress256"], default="batch32")
+    ap.add_argument("--compute", choices=["tensor", "fma"], default="tensor")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def make_case(name):
+    return W.case_batch32() if name == "batch32" else W.case_stress()
+
+
+# ------------------------------------------------------------- distributed --
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms; summarised over a wall-clock window."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"pkv_clocks_{os.getpid()}.csv")
+        try:
+            uuid = None
+            try:
+                uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+                if uuid and not uuid.startswith("GPU-"):
+                    uuid = "GPU-" + uuid
+            except Exception:
+                uuid = None
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "200"]
+            if uuid:
+                cmd += ["-i", uuid]
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 - 0.25 <= r[0] <= t1 + 0.25] or rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside)}
+
+
+# ------------------------------------------------------------- roofline ----
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(kernel_tag):
+    """dram bytes per launch recorded by ncu for this kernel source, else None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    src = os.path.join(ROOT, "paged_kv_gqa_append_gb300", "csrc", "paged_decode.cu")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for line in open(path):
+            f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+            if f.get("kernel") == kernel_tag and f.get("source_sha") == sha:
+                return float(f["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------ CPU oracle ---
+
+class OracleSample:
+    """The FP64 oracle on one (layer, sequence) pair of the workload.
+
+    One run: append the sequence's new token into its pages (K rotated, q
+    rotated), then decode its 32 heads over the full context.
+    """
+
+    def __init__(self, case):
+        from oracle import paged_kv as OP, rope as OR
+        self.OP = OP
+        self.case = case
+        self.cos, self.sin = OR.table(OR.inv_freq_llama3(), W.MAX_CONTEXT)
+        self.n = int(case.seq_lens[0])
+        pages_per = (self.n + 15) // 16
+        gen = W.cpu_gen(case.seed + 99)
+        self.pool = W.bf16_bits(W.normal_bf16((pages_per, 2, 8, 16, 64), gen))
+        self.bt = np.full((1, W.MAX_BLOCKS), -1, np.int32)
+        self.bt[0, :pages_per] = np.arange(pages_per)
+        self.k = W.bf16_bits(W.normal_bf16((1, 8, 64), gen))
+        self.v = W.bf16_bits(W.normal_bf16((1, 8, 64), gen))
+        self.q = W.bf16_bits(W.normal_bf16((1, 32, 64), gen))
+        self.kv_bytes = self.n * W.NUM_KV_HEADS * W.HEAD_DIM * 2 * 2
+
+    def run_one(self):
+        p2, qr, _ = self.OP.append_rope(self.pool, self.k, self.v, np.array([self.n - 1]), None,
+                                        self.bt, self.cos, self.sin, self.q)
+        self.OP.decode(qr, p2, self.bt, np.array([self.n]), self.case.scale)
+
+    def timed(self, budget_s):
+        """Run pairs until budget_s has passed; returns (GB/s, pairs, seconds)."""
+        done, t0 = 0, time.perf_counter()
+        while True:
+            self.run_one()
+            done += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                return done * self.kv_bytes / el / 1e9, done, el
+
+
+def cpu_cores_used():
+    return 1  # the oracle is single-threaded NumPy (BLAS pinned to one thread)
+
+
+# ------------------------------------------------------------------- arms ---
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    case = make_case(args.workload)
+    ora = OracleSample(case)
+    # warm-up steps, then K timed steps; each step = one (layer, seq) pair
+    for _ in range(args.warmup):
+        ora.run_one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ora.run_one()
+    el = time.perf_counter() - t0
+    pairs = args.steps
+    n_tok = ora.n
+    value = pairs * ora.kv_bytes / el / 1e9
+    sample = (f"{pairs} (layer, sequence) pairs of {case.name}: append 1 token + decode 32 heads "
+              f"over {n_tok} tokens each")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": case.name, "batch": case.num_seqs, "layers": case.num_layers,
+                   "ctx": n_tok, "sample": "one (layer, seq) pair per step"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cpu_cores_used(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_gb300(args, world, rank, local):
+    import paged_kv_gqa_append_gb300 as pkv
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    case = make_case(args.workload)
+    L, S = case.num_layers, case.num_seqs
+    compute = pkv.COMPUTE_TENSOR if args.compute == "tensor" else pkv.COMPUTE_FMA
+
+    pool = W.fill_pool(case, device=dev)
+    q_raw = W.fill_queries(case, device=dev)
+    k_new, v_new = W.fill_new_kv(case, device=dev)
+    bt = torch.from_numpy(case.block_tables).to(dev)
+    lens = torch.from_numpy(case.seq_lens).to(dev)
+    pos = torch.from_numpy(W.new_positions(case)).to(dev)
+    cos, sin = pkv.rope_tables_device(dev, W.MAX_CONTEXT)
+    q_rot = torch.empty_like(q_raw)
+    out = torch.empty_like(q_raw)
+    ws = pkv.alloc_workspace(S, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kv_bytes_layer = case.kv_bytes_per_layer()
+    kw = dict(workspace=ws, max_seq_len=case.max_seq_len, d_err=err,
+              compute=None if compute == pkv.COMPUTE_TENSOR else compute)
+
+    def step(ev=None):
+        for l in range(L):
+            pkv.kv_append_rope(k_new[l], v_new[l], pos, bt[l], pool, cos, sin,
+                               q_in=q_raw[l], q_out=q_rot[l], d_err=err)
+            if ev is not None:
+                ev[l][0].record(stream)
+            pkv.paged_gqa_decode(q_rot[l], pool, bt[l], lens, out[l], case.scale, **kw)
+            if ev is not None:
+                ev[l][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    code = pkv.pkv_read_device_error(err)
+    if code != 0:
+        raise RuntimeError(f"device error {pkv.status_string(code)} during warm-up")
+
+    # ---- headline: K steps, device-timed, inputs resident in HBM ----------
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.5 if clocks else 0)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dec_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(L)] for _ in range(args.steps)]
+    e0.record(stream)
+    for i in range(args.steps):
+        step(dec_ev[i])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    ms_local = e0.elapsed_time(e1)
+    dec_ms = [a.elapsed_time(b) for row in dec_ev for (a, b) in row]
+    ms = max_over_ranks(ms_local, world, dev)
+    code = pkv.pkv_read_device_error(err)
+    if code != 0:
+        raise RuntimeError(f"device error {pkv.status_string(code)} in the timed region")
+    clk = clocks.summary(t_wall0, t_wall1) if clocks else None
+    if clocks:
+        clocks.stop()
+
+    steps = args.steps
+    sec = ms / 1e3
+    total_kv = kv_bytes_layer * L * steps * world
+    value = total_kv / sec / 1e9
+    tokens_per_s = S * steps * world / sec
+    us_per_layer = ms * 1e3 / (steps * L)
+
+    # ---- e2e: same step through the public API with host buffers ----------
+    e2e = None
+    if not args.no_e2e:
+        q_h = q_raw.cpu().pin_memory()
+        k_h, v_h = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
+        pos_h, lens_h = pos.cpu().pin_memory(), lens.cpu().pin_memory()
+        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, pos_h, lens_h))
+        d2h = out_h.numel() * out_h.element_size()
+        k_e2e = max(1, min(steps, 500))
+        barrier(world)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        a.record(stream)
+        for _ in range(k_e2e):
+            q_raw.copy_(q_h, non_blocking=True)
+            k_new.copy_(k_h, non_blocking=True)
+            v_new.copy_(v_h, non_blocking=True)
+            pos.copy_(pos_h, non_blocking=True)
+            lens.copy_(lens_h, non_blocking=True)
+            step()
+            out_h.copy_(out, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        host_s = time.perf_counter() - t0
+        e2e_s = max_over_ranks(max(a.elapsed_time(b) / 1e3, host_s), world, dev)
+        e2e = {"value": kv_bytes_layer * L * k_e2e * world / e2e_s / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": k_e2e, "tokens_per_s": S * k_e2e * world / e2e_s}
+
+    # ---- roofline of the dominant kernel (decode: split + combine) --------
+    peak, peak_kind = hbm_peak()
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    achieved = kv_bytes_layer / (dec_avg_ms / 1e3) / 1e9
+    tag = "paged_decode_split_" + ("mma" if compute == pkv.COMPUTE_TENSOR else "fma")
+    traffic = ncu_traffic(f"{tag}:{case.name}")
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
+            "kernel": "paged_gqa_decode (split + combine), avg of %d launches" % len(dec_ms),
+            "algorithmic_bytes_per_launch": kv_bytes_layer,
+            "avg_launch_us": dec_avg_ms * 1e3}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, pairs, el = OracleSample(case).timed(10.0)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": cpu_cores_used(), "kind": "oracle",
+               "sample": f"{pairs} (layer, sequence) pairs of {case.name} (append 1 token + "
+                         f"decode 32 heads over {int(case.seq_lens[0])} tokens), {el:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": ms / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": case.name, "batch": S, "layers": L,
+                       "ctx": int(case.seq_lens[0]), "pool_pages": case.num_pages,
+                       "pool_bytes": case.num_pages * W.PAGE_ELEMS * 2,
+                       "l2": "inputs larger than L2 (pool read per step exceeds 129 MB L2)",
+                       "parallelism": f"replicas x{world}", "compute": args.compute},
+            "tokens_per_s": tokens_per_s, "us_per_layer": us_per_layer,
+            "kv_bytes_per_step": kv_bytes_layer * L,
+            "hbm_frac_step": value / world / peak,
+            "clocks": clk, "e2e": e2e, "gpu_launches": 3 * L * steps,
+            "roofline": roof, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_gb300(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

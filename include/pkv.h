@@ -1,0 +1,256 @@
+/*
+ * pkv.h - paged GQA decode attention and fused RoPE + paged KV append
+ *         for NVIDIA GB300 (sm_103a).  Plain C ABI.
+ *
+ * What the calls compute comes from the samir-vllm article (techfi24,
+ * "samir-vllm implemente l'inference Llama 3.2 1B en C++/CUDA"):
+ *   - section "Gestion de la KV cache et strategies de batching": a shared KV
+ *     pool of 16-token physical pages, one block table per sequence and per
+ *     layer, each new token's K/V written at its absolute RoPE position, and
+ *     paged attention that reads only the sequence's own pages, accumulating
+ *     weighted V without a contiguous prefix or stored scores; admission
+ *     credit and explicit rejection of oversize requests;
+ *   - section "Architecture et flux d'inference": grouped-query attention,
+ *     BF16 storage with FP32 reductions.
+ * Shapes are Llama-3.2-1B's ("2. Weight Loading and GPU Buffer Design",
+ * section "Preallocating the 16 compute buffers": 32 query heads,
+ * KV_DIM 512, hidden 2048), i.e. 8 KV heads of dimension 64, group size 4.
+ *
+ * Conventions shared by every call
+ *   - Ownership: the caller owns every buffer (pool, tables, q/k/v, outputs,
+ *     workspace, error word, stream).  No call allocates device memory or
+ *     keeps per-call state; the library holds only a per-thread cache of TMA
+ *     descriptors (host memory).  Model-owned vs caller-owned memory follows
+ *     the split of "Lifecycle and Memory Model" (TinyLoop C++ API), sections
+ *     "Model-owned memory" and "Per-request / handle-owned memory".
+ *   - Pointers named d_* or documented as "device" are device addresses;
+ *     "host" pointers are ordinary CPU memory.  bf16 tensors are passed as
+ *     void* to keep CUDA headers out of this file.
+ *   - Asynchrony: GPU calls only enqueue work on `stream` (a cudaStream_t,
+ *     NULL = legacy default stream) and return at once.  The return value
+ *     reports host-side checks (null pointers, alignment, sizes, launch
+ *     errors) only.  Problems the kernels find in the data (a page id
+ *     outside the pool, a position beyond the table) are written to the
+ *     caller's device error word *d_err: the first code wins (atomic
+ *     compare-and-swap from 0), the offending token or sequence is skipped
+ *     (its output rows are written as zeros) and no kernel ever traps.
+ *   - Thread safety: calls are re-entrant; concurrent calls on different
+ *     streams need distinct workspaces and outputs ("Lifecycle and Memory
+ *     Model", section "Mutable state and thread-safety implications").
+ *     The scheduler object (pkv_sched_*) is not thread-safe.
+ *   - Device selection: a call runs on the device that owns `stream`
+ *     (the current device for the default stream).
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Fixed layer topology (compile-time in the kernels). */
+#define PKV_NUM_Q_HEADS 32
+#define PKV_NUM_KV_HEADS 8
+#define PKV_GROUP 4
+#define PKV_HEAD_DIM 64
+#define PKV_ROPE_PAIRS 32
+#define PKV_PAGE_TOKENS 16
+#define PKV_PAGE_ELEMS (2 * PKV_NUM_KV_HEADS * PKV_PAGE_TOKENS * PKV_HEAD_DIM)
+#define PKV_PAGE_BYTES (2 * PKV_PAGE_ELEMS) /* 32768 */
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARGUMENT = 1,   /* null pointer, negative size, bad stride  */
+  PKV_ERR_MISALIGNED = 2,         /* a buffer is not 16-byte aligned          */
+  PKV_ERR_UNSUPPORTED_SHAPE = 3,  /* size outside what the kernels support    */
+  PKV_ERR_WORKSPACE_TOO_SMALL = 4,
+  PKV_ERR_CUDA = 5,               /* CUDA runtime/launch error                 */
+  PKV_ERR_DEVICE_INDEX = 6,       /* device word: bad page id / position / row */
+  PKV_ERR_POOL_EXHAUSTED = 7,     /* scheduler: not enough free pages now      */
+  PKV_ERR_REQUEST_TOO_LARGE = 8,  /* scheduler: credit exceeds the whole pool  */
+  PKV_ERR_TIMEOUT = 9             /* device word: a bounded wait gave up       */
+} pkv_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* pkv_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int pkv_version(void);
+
+/* ------------------------------------------------------------------------
+ * RoPE tables (host-side set-up, run once, like the frequency table the
+ * tiny-vllm engine builds at start-up: "2. Weight Loading and GPU Buffer
+ * Design", section "What else is set up in the initialization block").
+ * ---------------------------------------------------------------------- */
+
+/* inv_freq[i] = theta^(-2i/64), i < 32.  inv_freq: host double[32] (out). */
+int pkv_rope_inv_freq_plain(double* inv_freq, double theta);
+
+/* Llama 3 frequency scaling of the plain table: components with wavelength
+ * 2*pi/f below original_max_pos/high_freq_factor are kept, above
+ * original_max_pos/low_freq_factor divided by `factor`, blended linearly in
+ * between.  inv_freq: host double[32] (out). */
+int pkv_rope_inv_freq_llama3(double* inv_freq, double theta, double factor,
+                             double low_freq_factor, double high_freq_factor,
+                             int original_max_pos);
+
+/* host_cos/host_sin: host float[max_pos][32] (out);
+ * cos[p][i] = (float)cos((double)p * inv_freq[i]), same for sin.
+ * The caller copies the tables to the device for kv_append_rope. */
+int pkv_rope_table_fill(float* host_cos, float* host_sin, int max_pos, const double* inv_freq);
+
+/* ------------------------------------------------------------------------
+ * kv_append_rope - write T new tokens' K/V into their pages.
+ *
+ * For token t of block-table row s = token_seq[t] (or t when token_seq is
+ * NULL) at absolute position p = positions[t]: K of every KV head g is
+ * rotated by RoPE at position p (pairs (i, i+32), fp32 operations in the
+ * order r0 = x0*c - x1*s, r1 = x0*s + x1*c, each rounded to nearest, then
+ * rounded to bf16 nearest-even) and written to slot p % 16 of page
+ * block_tables[s * bt_row_stride + p / 16]; V is copied bit for bit.
+ * If q_in is given, the 32 query heads of token t are rotated the same way
+ * into q_out (q_out may equal q_in).  Tokens of one call must address
+ * distinct (row, position) pairs.
+ *
+ *   k, v          device bf16 [T][8][64]
+ *   positions     device int32 [T]
+ *   token_seq     device int32 [T] or NULL
+ *   block_tables  device int32 [num_seqs][bt_row_stride], first max_blocks
+ *                 entries of each row used; -1 = no page
+ *   kv_pool       device bf16 [num_pages][2 (K,V)][8][16][64], 32 KiB/page
+ *   rope_cos/sin  device float [max_pos][32] (see pkv_rope_table_fill)
+ *   q_in, q_out   device bf16 [T][32][64], or both NULL
+ *   d_err         device int32, first device-detected error code (or NULL)
+ * A token whose row, position or page id is out of range writes nothing,
+ * gets a zero q_out row and sets *d_err = PKV_ERR_DEVICE_INDEX.
+ * Returns PKV_OK or a host-side error (nothing is launched then).
+ * ---------------------------------------------------------------------- */
+int kv_append_rope(const void* k, const void* v, const int32_t* positions,
+                   const int32_t* token_seq, int T,
+                   const int32_t* block_tables, int num_seqs, int bt_row_stride, int max_blocks,
+                   void* kv_pool, int num_pages,
+                   const float* rope_cos, const float* rope_sin, int max_pos,
+                   const void* q_in, void* q_out,
+                   int* d_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * paged_gqa_decode - one decode step of grouped-query attention over
+ * each sequence's own pages.
+ *
+ * For sequence s with n = seq_lens[s] tokens (positions [0, n), including
+ * the token just appended) and query head h (KV head g = h / 4):
+ *     x_j = scale * q[s][h] . K_j[g],   out[s][h] = sum_j softmax(x)_j V_j[g]
+ * K_j/V_j are read from slot j % 16 of page block_tables[s][j / 16].
+ * Loads are bf16, all arithmetic fp32 (exponentials in base 2), output
+ * rounded to bf16 nearest-even.  Work is split into page ranges spread
+ * evenly over the GPU (flash-decoding); partial (o, m, l) triples go to the
+ * workspace and a second kernel merges them with a log-sum-exp combine.
+ *
+ *   q             device bf16 [num_seqs][32][64] (already rotated)
+ *   kv_pool       device bf16 pool as in kv_append_rope, 16-byte aligned
+ *   block_tables  device int32 [num_seqs][bt_row_stride]
+ *   seq_lens      device int32 [num_seqs]
+ *   max_seq_len   host upper bound of seq_lens (sizes the grid; a larger
+ *                 actual length is still handled correctly)
+ *   out           device bf16 [num_seqs][32][64]
+ *   workspace     device memory of at least
+ *                 paged_gqa_decode_workspace_bytes(num_seqs) bytes,
+ *                 16-byte aligned, contents need not be initialised
+ * seq_len 0 gives a zero output.  A negative seq_len, seq_len above
+ * 16 * max_blocks, or a needed page id outside [0, num_pages) gives a zero
+ * output for that sequence and sets *d_err = PKV_ERR_DEVICE_INDEX.
+ * ---------------------------------------------------------------------- */
+size_t paged_gqa_decode_workspace_bytes(int num_seqs);
+
+int paged_gqa_decode(const void* q, const void* kv_pool, int num_pages,
+                     const int32_t* block_tables, int bt_row_stride, int max_blocks,
+                     const int32_t* seq_lens, int num_seqs, int max_seq_len,
+                     void* out, float scale,
+                     void* workspace, size_t workspace_bytes,
+                     int* d_err, void* stream);
+
+/* Tuning / comparison knobs for paged_gqa_decode_ex (NULL = defaults). */
+typedef enum pkv_compute {
+  PKV_COMPUTE_TENSOR = 0, /* scores and P*V on the tensor cores (bf16 mma, fp32 accumulate) */
+  PKV_COMPUTE_FMA = 1     /* same pipeline, fp32 FMA on the CUDA cores (comparison arm)     */
+} pkv_compute;
+
+typedef struct pkv_decode_opts {
+  int compute;            /* pkv_compute                                             */
+  int min_units_per_warp; /* 0 = default (2): fewer warps for small batches          */
+  int ctas_per_sm;        /* 0 = as many as fit (at most 4)                          */
+} pkv_decode_opts;
+
+/* paged_gqa_decode with explicit options; same contract otherwise. */
+int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_pages,
+                        const int32_t* block_tables, int bt_row_stride, int max_blocks,
+                        const int32_t* seq_lens, int num_seqs, int max_seq_len,
+                        void* out, float scale,
+                        void* workspace, size_t workspace_bytes,
+                        int* d_err, void* stream, const pkv_decode_opts* opts);
+
+/* Wait for `stream`, then copy the device error word to *code_out (host).
+ * If `clear` is non-zero the word is reset to 0 afterwards. */
+int pkv_read_device_error(int* d_err, void* stream, int clear, int* code_out);
+
+/* ------------------------------------------------------------------------
+ * Continuous-batching scheduler (host only): FIFO admission by credit and
+ * on-demand page allocation.  From the samir-vllm article, section
+ * "Gestion de la KV cache et strategies de batching": a request is admitted
+ * once its page budget is available; credit = prompt_tokens +
+ * allowed_new_tokens - 1 tokens rounded up to 16-token pages, per layer; a
+ * request whose budget exceeds the pool is rejected with an explicit error.
+ * Rules the article leaves open: strict FIFO (the head blocks the queue);
+ * a request fits when credit <= free pages - pages still reserved by running
+ * requests; pages come from a LIFO free stack that starts [N-1 ... 0] (page
+ * 0 first); a finished request pushes back its pages layer by layer in
+ * logical order; a new request takes the lowest free slot (block-table row).
+ * ---------------------------------------------------------------------- */
+typedef struct pkv_sched pkv_sched;
+
+/* Pages reserved for a request: num_layers * ceil((prompt + new - 1) / 16). */
+int pkv_credit_pages(int prompt_tokens, int allowed_new_tokens, int num_layers);
+
+/* NULL on invalid sizes or allocation failure (fail closed, as load_model
+ * does in "Lifecycle and Memory Model", section "Internal allocation
+ * phases"). */
+pkv_sched* pkv_sched_create(int num_pages, int num_layers, int max_blocks, int max_slots);
+void pkv_sched_destroy(pkv_sched* s);
+
+/* Queue a request; *req_id (host, out) gets its id.  Returns
+ * PKV_ERR_REQUEST_TOO_LARGE (not queued) if its credit exceeds the pool or
+ * its length exceeds max_blocks pages. */
+int pkv_sched_submit(pkv_sched* s, int prompt_tokens, int allowed_new_tokens, int* req_id);
+
+/* Admit queued requests in FIFO order while the head fits.  Writes up to
+ * max_out admitted ids to admitted (host) and their count to *n_admitted. */
+int pkv_sched_admit(pkv_sched* s, int* admitted, int max_out, int* n_admitted);
+
+/* Make every layer of a running request hold pages for positions
+ * [0, new_len).  PKV_ERR_POOL_EXHAUSTED if that would exceed its credit. */
+int pkv_sched_grow(pkv_sched* s, int req_id, int new_len);
+
+/* Release a running request's pages and slot. */
+int pkv_sched_finish(pkv_sched* s, int req_id);
+
+/* Copy one request's block table for `layer` (host int32[max_blocks], -1
+ * padded) and report its slot (may be NULL). */
+int pkv_sched_block_table(const pkv_sched* s, int req_id, int layer, int32_t* row, int* slot);
+
+/* Counters: free pages, pages still reserved by running requests, queued
+ * requests, running requests (any may be NULL). */
+int pkv_sched_stats(const pkv_sched* s, int* free_pages, int* reserved_pages,
+                    int* queued, int* running);
+
+/* Allocation log: number of page grants so far, and grant i as
+ * (request, layer, logical page, page id). */
+int pkv_sched_event_count(const pkv_sched* s);
+int pkv_sched_event(const pkv_sched* s, int i, int* req_id, int* layer, int* logical, int* page);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H */

@@ -1,0 +1,331 @@
+"""Python binding of libpkv.so: paged GQA decode and fused RoPE + paged KV append.
+
+The functions carry the C-ABI names and only marshal arguments: they check
+dtypes, devices and shapes of torch tensors, pass raw pointers, sizes and the
+current CUDA stream to the library, and raise ``PkvError`` on a non-zero
+status.  Every step of the computation runs in the library's sm_103a kernels;
+there is no fallback.  Importing this package fails loudly when libpkv.so is
+missing (build it with ``python -m paged_kv_gqa_append_gb300.build``).
+
+Tensor layouts (see include/pkv.h):
+    kv_pool       [num_pages, 2, 8, 16, 64] bf16   (K = 0, V = 1), 32 KiB/page
+    block_tables  [num_seqs, >= max_blocks] int32  (-1 = no page)
+    q / out       [num_seqs, 32, 64] bf16
+    k / v         [T, 8, 64] bf16;  positions / token_seq [T] int32
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+NUM_Q_HEADS = 32
+NUM_KV_HEADS = 8
+HEAD_DIM = 64
+PAGE_TOKENS = 16
+ROPE_PAIRS = 32
+
+COMPUTE_TENSOR = 0
+COMPUTE_FMA = 1
+
+STATUS = {
+    0: "PKV_OK", 1: "PKV_ERR_INVALID_ARGUMENT", 2: "PKV_ERR_MISALIGNED",
+    3: "PKV_ERR_UNSUPPORTED_SHAPE", 4: "PKV_ERR_WORKSPACE_TOO_SMALL", 5: "PKV_ERR_CUDA",
+    6: "PKV_ERR_DEVICE_INDEX", 7: "PKV_ERR_POOL_EXHAUSTED", 8: "PKV_ERR_REQUEST_TOO_LARGE",
+    9: "PKV_ERR_TIMEOUT",
+}
+OK, ERR_DEVICE_INDEX, ERR_POOL_EXHAUSTED, ERR_REQUEST_TOO_LARGE, ERR_TIMEOUT = 0, 6, 7, 8, 9
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libpkv.so not found at {LIB_PATH}; build it with "
+                      "`python -m paged_kv_gqa_append_gb300.build` (nvcc for sm_103a)")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_p, _i, _f, _d, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_size_t
+_ip = ctypes.POINTER(ctypes.c_int)
+
+
+class DecodeOpts(ctypes.Structure):
+    _fields_ = [("compute", _i), ("min_units_per_warp", _i), ("ctas_per_sm", _i)]
+
+
+_SIGS = {
+    "pkv_status_string": (ctypes.c_char_p, [_i]),
+    "pkv_version": (_i, []),
+    "pkv_rope_inv_freq_plain": (_i, [_p, _d]),
+    "pkv_rope_inv_freq_llama3": (_i, [_p, _d, _d, _d, _d, _i]),
+    "pkv_rope_table_fill": (_i, [_p, _p, _i, _p]),
+    "kv_append_rope": (_i, [_p, _p, _p, _p, _i, _p, _i, _i, _i, _p, _i, _p, _p, _i, _p, _p, _p, _p]),
+    "paged_gqa_decode_workspace_bytes": (_sz, [_i]),
+    "paged_gqa_decode": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p, _p]),
+    "paged_gqa_decode_ex": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p, _p,
+                                 ctypes.POINTER(DecodeOpts)]),
+    "pkv_read_device_error": (_i, [_p, _p, _i, _ip]),
+    "pkv_credit_pages": (_i, [_i, _i, _i]),
+    "pkv_sched_create": (_p, [_i, _i, _i, _i]),
+    "pkv_sched_destroy": (None, [_p]),
+    "pkv_sched_submit": (_i, [_p, _i, _i, _ip]),
+    "pkv_sched_admit": (_i, [_p, _p, _i, _ip]),
+    "pkv_sched_grow": (_i, [_p, _i, _i]),
+    "pkv_sched_finish": (_i, [_p, _i]),
+    "pkv_sched_block_table": (_i, [_p, _i, _i, _p, _ip]),
+    "pkv_sched_stats": (_i, [_p, _ip, _ip, _ip, _ip]),
+    "pkv_sched_event_count": (_i, [_p]),
+    "pkv_sched_event": (_i, [_p, _i, _ip, _ip, _ip, _ip]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise PkvError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtype, device=None, shape_tail=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if shape_tail is not None and tuple(t.shape[-len(shape_tail):]) != tuple(shape_tail):
+        raise ValueError(f"{name} must end in shape {shape_tail}, got {tuple(t.shape)}")
+
+
+def status_string(status: int) -> str:
+    return lib.pkv_status_string(status).decode()
+
+
+# --------------------------------------------------------------- RoPE set-up --
+
+def pkv_rope_inv_freq_plain(theta: float = 500000.0) -> np.ndarray:
+    out = np.zeros(ROPE_PAIRS, np.float64)
+    _check(lib.pkv_rope_inv_freq_plain(out.ctypes.data, theta), "pkv_rope_inv_freq_plain")
+    return out
+
+
+def pkv_rope_inv_freq_llama3(theta=500000.0, factor=32.0, low_freq_factor=1.0,
+                             high_freq_factor=4.0, original_max_pos=8192) -> np.ndarray:
+    out = np.zeros(ROPE_PAIRS, np.float64)
+    _check(lib.pkv_rope_inv_freq_llama3(out.ctypes.data, theta, factor, low_freq_factor,
+                                        high_freq_factor, original_max_pos),
+           "pkv_rope_inv_freq_llama3")
+    return out
+
+
+def pkv_rope_table_fill(inv_freq, max_pos: int):
+    """Host fp32 cos/sin tables [max_pos][32] (numpy)."""
+    f = np.ascontiguousarray(inv_freq, dtype=np.float64)
+    if f.shape != (ROPE_PAIRS,):
+        raise ValueError("inv_freq must have 32 entries")
+    cos = np.empty((max_pos, ROPE_PAIRS), np.float32)
+    sin = np.empty_like(cos)
+    _check(lib.pkv_rope_table_fill(cos.ctypes.data, sin.ctypes.data, max_pos, f.ctypes.data),
+           "pkv_rope_table_fill")
+    return cos, sin
+
+
+def rope_tables_device(device, max_pos: int = 2048, inv_freq=None):
+    """cos/sin tables on `device` (Llama-3.2 frequencies by default)."""
+    if inv_freq is None:
+        inv_freq = pkv_rope_inv_freq_llama3()
+    cos, sin = pkv_rope_table_fill(inv_freq, max_pos)
+    return torch.from_numpy(cos).to(device), torch.from_numpy(sin).to(device)
+
+
+# ------------------------------------------------------------------- append --
+
+def kv_append_rope(k, v, positions, block_tables, kv_pool, rope_cos, rope_sin,
+                   token_seq=None, q_in=None, q_out=None, d_err=None, max_blocks=None,
+                   stream=None):
+    """Rotate K (and optionally q) at `positions` and write K/V into pool pages."""
+    dev = kv_pool.device
+    _need(kv_pool, "kv_pool", torch.bfloat16, dev, (2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM))
+    _need(k, "k", torch.bfloat16, dev, (NUM_KV_HEADS, HEAD_DIM))
+    _need(v, "v", torch.bfloat16, dev, (NUM_KV_HEADS, HEAD_DIM))
+    T = k.numel() // (NUM_KV_HEADS * HEAD_DIM)
+    if v.numel() != k.numel():
+        raise ValueError("k and v must have the same shape")
+    _need(positions, "positions", torch.int32, dev)
+    if positions.numel() != T:
+        raise ValueError("positions must have one entry per token")
+    if token_seq is not None:
+        _need(token_seq, "token_seq", torch.int32, dev)
+        if token_seq.numel() != T:
+            raise ValueError("token_seq must have one entry per token")
+    _need(block_tables, "block_tables", torch.int32, dev)
+    if block_tables.dim() != 2:
+        raise ValueError("block_tables must be [num_seqs, row_stride]")
+    _need(rope_cos, "rope_cos", torch.float32, dev, (ROPE_PAIRS,))
+    _need(rope_sin, "rope_sin", torch.float32, dev, (ROPE_PAIRS,))
+    if (q_in is None) != (q_out is None):
+        raise ValueError("q_in and q_out go together")
+    if q_in is not None:
+        _need(q_in, "q_in", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
+        _need(q_out, "q_out", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
+        if q_in.numel() != T * NUM_Q_HEADS * HEAD_DIM or q_out.numel() != q_in.numel():
+            raise ValueError("q_in/q_out must be [T, 32, 64]")
+    if d_err is not None:
+        _need(d_err, "d_err", torch.int32, dev)
+    S, stride = block_tables.shape
+    mb = stride if max_blocks is None else max_blocks
+    st = lib.kv_append_rope(_ptr(k), _ptr(v), _ptr(positions), _ptr(token_seq), T,
+                            _ptr(block_tables), S, stride, mb, _ptr(kv_pool), kv_pool.shape[0],
+                            _ptr(rope_cos), _ptr(rope_sin), rope_cos.shape[0],
+                            _ptr(q_in), _ptr(q_out), _ptr(d_err), _stream(stream))
+    _check(st, "kv_append_rope")
+
+
+# ------------------------------------------------------------------- decode --
+
+def paged_gqa_decode_workspace_bytes(num_seqs: int) -> int:
+    return int(lib.paged_gqa_decode_workspace_bytes(num_seqs))
+
+
+def alloc_workspace(num_seqs: int, device) -> torch.Tensor:
+    """Caller-owned workspace for paged_gqa_decode (uninitialised bytes)."""
+    with torch.cuda.device(device):
+        n = paged_gqa_decode_workspace_bytes(num_seqs)
+    if n <= 0:
+        raise PkvError(5, "paged_gqa_decode_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def paged_gqa_decode(q, kv_pool, block_tables, seq_lens, out, scale, workspace=None,
+                     max_seq_len=None, d_err=None, max_blocks=None, compute=None,
+                     min_units_per_warp=0, ctas_per_sm=0, stream=None):
+    """out[s, h] = softmax(scale * q[s, h] . K) V over sequence s's own pages."""
+    dev = kv_pool.device
+    _need(kv_pool, "kv_pool", torch.bfloat16, dev, (2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM))
+    _need(q, "q", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
+    _need(out, "out", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
+    S = q.numel() // (NUM_Q_HEADS * HEAD_DIM)
+    if out.numel() != q.numel():
+        raise ValueError("out must match q")
+    _need(block_tables, "block_tables", torch.int32, dev)
+    if block_tables.dim() != 2 or block_tables.shape[0] < S:
+        raise ValueError("block_tables must be [>= num_seqs, row_stride]")
+    _need(seq_lens, "seq_lens", torch.int32, dev)
+    if seq_lens.numel() != S:
+        raise ValueError("seq_lens must have num_seqs entries")
+    stride = block_tables.shape[1]
+    mb = stride if max_blocks is None else max_blocks
+    if max_seq_len is None:
+        max_seq_len = PAGE_TOKENS * mb
+    if workspace is None:
+        workspace = alloc_workspace(S, dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    if d_err is not None:
+        _need(d_err, "d_err", torch.int32, dev)
+    args = (_ptr(q), _ptr(kv_pool), kv_pool.shape[0], _ptr(block_tables), stride, mb,
+            _ptr(seq_lens), S, int(max_seq_len), _ptr(out), float(scale), _ptr(workspace),
+            workspace.numel(), _ptr(d_err), _stream(stream))
+    if compute is None and not min_units_per_warp and not ctas_per_sm:
+        st = lib.paged_gqa_decode(*args)
+    else:
+        opts = DecodeOpts(COMPUTE_TENSOR if compute is None else compute,
+                          min_units_per_warp, ctas_per_sm)
+        st = lib.paged_gqa_decode_ex(*args, ctypes.byref(opts))
+    _check(st, "paged_gqa_decode")
+
+
+def pkv_read_device_error(d_err, clear: bool = True, stream=None) -> int:
+    """Synchronise the stream and return the device error word (optionally reset it)."""
+    code = ctypes.c_int(0)
+    _check(lib.pkv_read_device_error(_ptr(d_err), _stream(stream), int(clear), ctypes.byref(code)),
+           "pkv_read_device_error")
+    return code.value
+
+
+# ---------------------------------------------------------------- scheduler --
+
+def pkv_credit_pages(prompt_tokens: int, allowed_new_tokens: int, num_layers: int) -> int:
+    return int(lib.pkv_credit_pages(prompt_tokens, allowed_new_tokens, num_layers))
+
+
+class Scheduler:
+    """Continuous-batching admission and page allocation (C++ pkv_sched)."""
+
+    def __init__(self, num_pages: int, num_layers: int, max_blocks: int = 128, max_slots: int = 256):
+        self._h = lib.pkv_sched_create(num_pages, num_layers, max_blocks, max_slots)
+        if not self._h:
+            raise PkvError(1, "pkv_sched_create")
+        self.num_layers, self.max_blocks, self.max_slots = num_layers, max_blocks, max_slots
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            lib.pkv_sched_destroy(h)
+            self._h = None
+
+    def submit(self, prompt_tokens: int, allowed_new_tokens: int):
+        """Returns (status, request id); oversize requests give ERR_REQUEST_TOO_LARGE."""
+        rid = ctypes.c_int(-1)
+        st = lib.pkv_sched_submit(self._h, prompt_tokens, allowed_new_tokens, ctypes.byref(rid))
+        if st not in (OK, ERR_REQUEST_TOO_LARGE):
+            raise PkvError(st, "pkv_sched_submit")
+        return st, rid.value
+
+    def admit(self):
+        buf = (ctypes.c_int * self.max_slots)()
+        n = ctypes.c_int(0)
+        _check(lib.pkv_sched_admit(self._h, buf, self.max_slots, ctypes.byref(n)), "pkv_sched_admit")
+        return list(buf[:n.value])
+
+    def grow(self, rid: int, new_len: int) -> int:
+        st = lib.pkv_sched_grow(self._h, rid, new_len)
+        if st not in (OK, ERR_POOL_EXHAUSTED):
+            raise PkvError(st, "pkv_sched_grow")
+        return st
+
+    def finish(self, rid: int):
+        _check(lib.pkv_sched_finish(self._h, rid), "pkv_sched_finish")
+
+    def block_table(self, rid: int, layer: int):
+        row = np.empty(self.max_blocks, np.int32)
+        slot = ctypes.c_int(-1)
+        _check(lib.pkv_sched_block_table(self._h, rid, layer, row.ctypes.data, ctypes.byref(slot)),
+               "pkv_sched_block_table")
+        return row, slot.value
+
+    def stats(self):
+        v = [ctypes.c_int(0) for _ in range(4)]
+        _check(lib.pkv_sched_stats(self._h, *[ctypes.byref(x) for x in v]), "pkv_sched_stats")
+        return dict(free=v[0].value, reserved=v[1].value, queued=v[2].value, running=v[3].value)
+
+    def events(self):
+        n = lib.pkv_sched_event_count(self._h)
+        out = []
+        v = [ctypes.c_int(0) for _ in range(4)]
+        for i in range(n):
+            _check(lib.pkv_sched_event(self._h, i, *[ctypes.byref(x) for x in v]), "pkv_sched_event")
+            out.append(tuple(x.value for x in v))
+        return out

@@ -1,0 +1,28 @@
+// Host-side helpers shared by the C-ABI entry points (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// Make the device that owns `stream` current for this thread (the current
+// device is kept for the legacy default stream).  Returns PKV_OK or
+// PKV_ERR_CUDA.
+int bind_stream_device(void* stream, int* device_out);
+
+// Number of SMs of `device` (cached after the first query).
+int sm_count(int device);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return PKV_OK;
+  (void)cudaGetLastError();  // clear the sticky-free error state for the next call
+  return PKV_ERR_CUDA;
+}
+
+}  // namespace pkv

@@ -1,0 +1,795 @@
+// Paged GQA decode attention for sm_103a: a balanced split phase that streams
+// each (sequence, KV head, page) unit through TMA into shared memory, and a
+// log-sum-exp combine.
+//
+// Source of the computation: samir-vllm article, section "Gestion de la KV
+// cache et strategies de batching" (paged attention reads only the current
+// sequence's pages and accumulates weighted V without a contiguous prefix or
+// stored scores) and section "Architecture et flux d'inference" (grouped-query
+// attention, BF16 tensors, FP32 reductions).
+//
+// Work decomposition (GB300-specific, not from the pages):
+//   * A unit is one (sequence s, KV head g, logical page j): 2 KiB of K plus
+//     2 KiB of V, contiguous in the head-major page layout.  Units are ordered
+//     (s, g, j); the U = 8 * sum_s ceil(len_s / 16) units are cut into NW equal
+//     contiguous ranges, one per warp: warp w owns [w*U/NW, (w+1)*U/NW).  Every
+//     CTA rebuilds the per-sequence page prefix from seq_lens in shared memory,
+//     so no host synchronisation is needed for variable lengths.
+//   * Each warp is an independent pipeline: lane 0 issues TMA loads of K and V
+//     tiles (128-byte swizzle) for up to kStages units ahead, one mbarrier per
+//     stage; the warp consumes them in order.
+//   * Per unit, the 4 query heads of the group share the page: scores
+//     S = Q K^T and O += P V run on the tensor cores as bf16 mma.sync
+//     m16n8k16 with fp32 accumulation (heads padded 4 -> 16 rows), or, in the
+//     comparison variant, as fp32 FMA on the CUDA cores.  Online softmax in
+//     base 2 with the scale folded in.
+//   * A warp writes one partial (o[4][64], m[4], l[4]) per segment (s, g) it
+//     touches, at index 8*s + g + w, which is unique because both terms grow
+//     along the unit order.  The combine kernel merges the partials of each
+//     segment and writes bf16.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <mutex>
+#include <stdint.h>
+#include <string.h>
+
+#include "internal.h"
+#include "pkv.h"
+#include "ptx.cuh"
+
+namespace pkv {
+
+constexpr int kWarps = 4;            // warps per CTA
+constexpr int kStages = 4;           // units in flight per warp
+constexpr int kTileBytes = 2048;     // 16 tokens x 64 dims bf16
+constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kMaxCtasPerSm = 4;     // workspace is sized for this many
+constexpr int kMaxSeqs = 4096;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per stage wait
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DecodeParams {
+  const uint16_t* q;              // [S][32][64] bf16
+  const int32_t* block_tables;    // [S][bt_stride]
+  const int32_t* seq_lens;        // [S]
+  uint16_t* out;                  // [S][32][64] bf16
+  int bt_stride, max_blocks, num_pages, num_seqs;
+  float sl2;                      // scale * log2(e)
+  int* d_err;
+  int32_t* ws_prefix;             // [S + 1] page prefix, written by CTA 0
+  float2* ws_ml;                  // [npart][4] (m, l); l < 0 marks a bad segment
+  float* ws_o;                    // [npart][4][64]
+};
+
+struct SmemLayout {
+  static constexpr int kTiles = kWarps * kStages * kStageBytes;
+  static constexpr int kBars = kTiles;                                // uint64 [kWarps][kStages]
+  static constexpr int kPid = kBars + kWarps * kStages * 8;           // int [kWarps][kStages]
+  static constexpr int kPrefix = kPid + kWarps * kStages * 4;         // int [S + 1]
+  static size_t bytes(int num_seqs) { return 1024 + kPrefix + 4 * (size_t)(num_seqs + 1); }
+};
+
+// ---------------------------------------------------------------------------
+// Unit cursor: walks (s, g, j) in unit order, skipping empty sequences.
+// ---------------------------------------------------------------------------
+struct Cursor {
+  int s, g, j, np;
+};
+
+__device__ __forceinline__ void cursor_seek(Cursor& c, uint32_t u, const int32_t* prefix, int S) {
+  int lo = 0, hi = S - 1;  // largest s with 8 * prefix[s] <= u
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (8u * (uint32_t)prefix[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  c.s = lo;
+  c.np = prefix[lo + 1] - prefix[lo];
+  const uint32_t r = u - 8u * (uint32_t)prefix[lo];
+  c.g = (int)(r / (uint32_t)c.np);
+  c.j = (int)(r % (uint32_t)c.np);
+}
+
+__device__ __forceinline__ void cursor_next(Cursor& c, const int32_t* prefix, int S) {
+  if (++c.j < c.np) return;
+  c.j = 0;
+  if (++c.g < 8) return;
+  c.g = 0;
+  do { ++c.s; } while (c.s < S && prefix[c.s + 1] == prefix[c.s]);
+  if (c.s < S) c.np = prefix[c.s + 1] - prefix[c.s];
+}
+
+// Page id of unit u (or -1 if the table entry is outside the pool, -2 if u is
+// past the end of this warp's range).
+__device__ __forceinline__ int unit_page(uint32_t u, uint32_t u_end, const int32_t* prefix,
+                                         const DecodeParams& p) {
+  if (u >= u_end) return -2;
+  Cursor c;
+  cursor_seek(c, u, prefix, p.num_seqs);
+  const int pid = __ldg(p.block_tables + (size_t)c.s * p.bt_stride + c.j);
+  return (pid >= 0 && pid < p.num_pages) ? pid : -1;
+}
+
+// Pages of sequence s, or 0 (and an error) for a length outside [0, 16*max_blocks].
+__device__ __forceinline__ int seq_pages(int n, int max_blocks, bool* bad) {
+  if (n < 0 || n > PKV_PAGE_TOKENS * max_blocks) {
+    *bad = true;
+    return 0;
+  }
+  return (n + PKV_PAGE_TOKENS - 1) / PKV_PAGE_TOKENS;
+}
+
+// Block-wide exclusive prefix of pages over all sequences into prefix[0..S].
+__device__ void build_prefix(const DecodeParams& p, int32_t* prefix) {
+  __shared__ int warp_tot[kWarps];
+  const int S = p.num_seqs;
+  const int nthr = kWarps * 32;
+  const int per = (S + nthr - 1) / nthr;
+  const int lo = threadIdx.x * per, hi = min(S, lo + per);
+  bool bad = false;
+  int sum = 0;
+  for (int s = lo; s < hi; ++s) sum += seq_pages(__ldg(p.seq_lens + s), p.max_blocks, &bad);
+  if (bad && blockIdx.x == 0) report_error(p.d_err, PKV_ERR_DEVICE_INDEX);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int base = 0;
+  for (int w = 0; w < warp; ++w) base += warp_tot[w];
+  int run = base + incl - sum;
+  for (int s = lo; s < hi; ++s) {
+    prefix[s] = run;
+    run += seq_pages(__ldg(p.seq_lens + s), p.max_blocks, &bad);
+  }
+  if (threadIdx.x == nthr - 1) prefix[S] = run;
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-core page compute (bf16 mma.sync m16n8k16, fp32 accumulate).
+// Lane (gq = lane/4, tig = lane%4).  Rows of A are query heads (rows 0..3 real,
+// 4..15 zero), so only lanes 0..15 carry results.  S = Q K^T has N = tokens
+// (two 8-token tiles per page, K = 64 dims in 4 chunks); O += P V has N = dims
+// (8 tiles), K = 16 tokens.  The C layout of S is the A layout of P, so the
+// probabilities never leave registers.
+// ---------------------------------------------------------------------------
+struct MmaState {
+  uint32_t qa[4][2];  // Q A-fragments per 16-dim chunk: (row gq, k 2tig..) and (k 8+2tig..)
+  float o[8][4];      // O accumulators per 8-dim tile
+  float m, l;         // running max (log2 units) and per-lane partial denominator
+
+  __device__ __forceinline__ void load_q(const DecodeParams& p, int s, int g, int lane) {
+    const int gq = lane >> 2, tig = lane & 3;
+    if (gq < 4) {
+      const uint32_t* qrow =
+          reinterpret_cast<const uint32_t*>(p.q + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + gq) * 64);
+#pragma unroll
+      for (int kc = 0; kc < 4; ++kc) {
+        qa[kc][0] = __ldg(qrow + kc * 8 + tig);
+        qa[kc][1] = __ldg(qrow + kc * 8 + 4 + tig);
+      }
+    } else {
+#pragma unroll
+      for (int kc = 0; kc < 4; ++kc) qa[kc][0] = qa[kc][1] = 0u;
+    }
+  }
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int n = 0; n < 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    m = -INFINITY;
+    l = 0.f;
+  }
+
+  __device__ __forceinline__ void page(uint32_t sK, uint32_t sV, int valid, float sl2, int lane) {
+    const int tig = lane & 3, mi = lane >> 3, r = lane & 7;
+    // ---- S = Q K^T -------------------------------------------------------
+    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint32_t krow = sK + (uint32_t)((8 * (mi >> 1) + r) * 128);
+#pragma unroll
+    for (int kc = 0; kc < 4; ++kc) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(krow + ((((2 * kc) + (mi & 1)) ^ r) << 4), b0, b1, b2, b3);
+      mma_bf16_16816(s0, qa[kc][0], qa[kc][1], b0, b1);
+      mma_bf16_16816(s1, qa[kc][0], qa[kc][1], b2, b3);
+    }
+    // ---- online softmax (base 2) ------------------------------------------
+    const int t0 = 2 * tig;
+    float x0 = s0[0] * sl2, x1 = s0[1] * sl2, x2 = s1[0] * sl2, x3 = s1[1] * sl2;
+    if (valid < PKV_PAGE_TOKENS) {
+      x0 = (t0 < valid) ? x0 : -INFINITY;
+      x1 = (t0 + 1 < valid) ? x1 : -INFINITY;
+      x2 = (t0 + 8 < valid) ? x2 : -INFINITY;
+      x3 = (t0 + 9 < valid) ? x3 : -INFINITY;
+    }
+    float pm = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
+    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
+    const float mn = fmaxf(m, pm);
+    const float alpha = (m == mn) ? 1.f : exp2f(m - mn);
+    const float p0 = (x0 == mn) ? 1.f : exp2f(x0 - mn);
+    const float p1 = (x1 == mn) ? 1.f : exp2f(x1 - mn);
+    const float p2 = (x2 == mn) ? 1.f : exp2f(x2 - mn);
+    const float p3 = (x3 == mn) ? 1.f : exp2f(x3 - mn);
+    m = mn;
+    const uint32_t pa0 = pack_bf16x2(p0, p1);  // P[gq][2tig, 2tig+1]
+    const uint32_t pa2 = pack_bf16x2(p2, p3);  // P[gq][8+2tig, 9+2tig]
+    // the denominator uses the same bf16-rounded weights as the PV product
+    l = l * alpha + ((bf16lo_to_f32(pa0) + bf16hi_to_f32(pa0)) +
+                     (bf16lo_to_f32(pa2) + bf16hi_to_f32(pa2)));
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+      o[n][0] *= alpha;
+      o[n][1] *= alpha;
+    }
+    // ---- O += P V ----------------------------------------------------------
+    uint32_t m01 = 0xFFFFFFFFu, m89 = 0xFFFFFFFFu;
+    if (valid < PKV_PAGE_TOKENS) {  // zero V rows past the end (they may hold NaN bits)
+      m01 = ((t0 < valid) ? 0x0000FFFFu : 0u) | ((t0 + 1 < valid) ? 0xFFFF0000u : 0u);
+      m89 = ((t0 + 8 < valid) ? 0x0000FFFFu : 0u) | ((t0 + 9 < valid) ? 0xFFFF0000u : 0u);
+    }
+    const uint32_t vrow = sV + (uint32_t)((8 * (mi & 1) + r) * 128);
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) {
+      uint32_t v0, v1, v2, v3;
+      ldsm_x4_t(vrow + ((((2 * pp) + (mi >> 1)) ^ r) << 4), v0, v1, v2, v3);
+      v0 &= m01; v2 &= m01; v1 &= m89; v3 &= m89;
+      mma_bf16_16816(o[2 * pp], pa0, pa2, v0, v1);
+      mma_bf16_16816(o[2 * pp + 1], pa0, pa2, v2, v3);
+    }
+  }
+
+  __device__ __forceinline__ void write_partial(const DecodeParams& p, uint32_t pidx, bool bad,
+                                                int lane) {
+    const int gq = lane >> 2, tig = lane & 3;
+    float lt = l;
+    lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+    if (gq < 4) {
+      float* o_dst = p.ws_o + ((size_t)pidx * 4 + gq) * 64 + 2 * tig;
+#pragma unroll
+      for (int n = 0; n < 8; ++n)
+        *reinterpret_cast<float2*>(o_dst + 8 * n) = make_float2(o[n][0], o[n][1]);
+      if (tig == 0) p.ws_ml[(size_t)pidx * 4 + gq] = make_float2(m, bad ? -1.f : lt);
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// CUDA-core page compute (fp32 FMA), the comparison variant.
+// Lane (t8 = lane/4, qd = lane%4): tokens t8 and t8+8 of the page, dims
+// [16 qd, 16 qd + 16).  Scores are reduced over the 4 lanes of a quad; the
+// output accumulates per lane and is reduced over t8 once per segment.
+// ---------------------------------------------------------------------------
+struct FmaState {
+  float qf[4][16];
+  float o[4][16];
+  float m[4], l[4];
+
+  __device__ __forceinline__ void load_q(const DecodeParams& p, int s, int g, int lane) {
+    const int qd = lane & 3;
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + hh) * 64 + 16 * qd);
+      const uint4 a = __ldg(src), b = __ldg(src + 1);
+      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        qf[hh][2 * i] = bf16lo_to_f32(w[i]);
+        qf[hh][2 * i + 1] = bf16hi_to_f32(w[i]);
+      }
+    }
+  }
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) {
+#pragma unroll
+      for (int d = 0; d < 16; ++d) o[hh][d] = 0.f;
+      m[hh] = -INFINITY;
+      l[hh] = 0.f;
+    }
+  }
+
+  __device__ __forceinline__ static void load_row16(uint32_t tile, int t, int qd, float (&f)[16]) {
+    uint4 a, b;
+    const uint32_t row = tile + (uint32_t)(t * 128);
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w)
+                 : "r"(row + (((2 * qd) ^ (t & 7)) << 4)));
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                 : "r"(row + (((2 * qd + 1) ^ (t & 7)) << 4)));
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      f[2 * i] = bf16lo_to_f32(w[i]);
+      f[2 * i + 1] = bf16hi_to_f32(w[i]);
+    }
+  }
+
+  __device__ __forceinline__ void page(uint32_t sK, uint32_t sV, int valid, float sl2, int lane) {
+    const int t8 = lane >> 2, qd = lane & 3;
+    float x[2][4];
+#pragma unroll
+    for (int ps = 0; ps < 2; ++ps) {
+      float kf[16];
+      load_row16(sK, t8 + 8 * ps, qd, kf);
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) {
+        float acc = 0.f;
+#pragma unroll
+        for (int d = 0; d < 16; ++d) acc = fmaf(qf[hh][d], kf[d], acc);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        x[ps][hh] = (t8 + 8 * ps < valid) ? acc * sl2 : -INFINITY;
+      }
+    }
+    float pr[2][4];
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) {
+      float pm = fmaxf(x[0][hh], x[1][hh]);
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+      const float mn = fmaxf(m[hh], pm);
+      const float alpha = (m[hh] == mn) ? 1.f : exp2f(m[hh] - mn);
+      pr[0][hh] = (x[0][hh] == mn) ? 1.f : exp2f(x[0][hh] - mn);
+      pr[1][hh] = (x[1][hh] == mn) ? 1.f : exp2f(x[1][hh] - mn);
+      m[hh] = mn;
+      l[hh] = l[hh] * alpha + (pr[0][hh] + pr[1][hh]);
+#pragma unroll
+      for (int d = 0; d < 16; ++d) o[hh][d] *= alpha;
+    }
+#pragma unroll
+    for (int ps = 0; ps < 2; ++ps) {
+      if (t8 + 8 * ps < valid) {  // rows past the end may hold NaN bits: never touch them
+        float vf[16];
+        load_row16(sV, t8 + 8 * ps, qd, vf);
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh)
+#pragma unroll
+          for (int d = 0; d < 16; ++d) o[hh][d] = fmaf(pr[ps][hh], vf[d], o[hh][d]);
+      }
+    }
+  }
+
+  __device__ __forceinline__ void write_partial(const DecodeParams& p, uint32_t pidx, bool bad,
+                                                int lane) {
+    const int t8 = lane >> 2, qd = lane & 3;
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) {
+      float lt = l[hh];
+      lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+      lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+      lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+#pragma unroll
+      for (int d = 0; d < 16; ++d) {
+        float v = o[hh][d];
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 16);
+        o[hh][d] = v;
+      }
+      if (t8 == 0) {
+        float4* dst = reinterpret_cast<float4*>(p.ws_o + ((size_t)pidx * 4 + hh) * 64 + 16 * qd);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_float4(o[hh][4 * i], o[hh][4 * i + 1], o[hh][4 * i + 2], o[hh][4 * i + 3]);
+        if (qd == 0) p.ws_ml[(size_t)pidx * 4 + hh] = make_float2(m[hh], bad ? -1.f : lt);
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Split phase.
+// ---------------------------------------------------------------------------
+template <class State>
+__global__ void __launch_bounds__(kWarps * 32)
+    paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  int32_t* prefix = reinterpret_cast<int32_t*>(smem + SmemLayout::kPrefix);
+  int* spid = reinterpret_cast<int*>(smem + SmemLayout::kPid);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = p.num_seqs;
+
+  pdl_wait();
+  build_prefix(p, prefix);
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i <= S; i += blockDim.x) p.ws_prefix[i] = prefix[i];
+  pdl_launch_dependents();
+
+  const uint32_t U = 8u * (uint32_t)prefix[S];
+  const uint32_t NW = gridDim.x * kWarps;
+  const uint32_t w = blockIdx.x * kWarps + warp;
+  const uint32_t u0 = (uint32_t)(((uint64_t)w * U) / NW);
+  const uint32_t u1 = (uint32_t)(((uint64_t)(w + 1) * U) / NW);
+  if (u0 >= u1) return;
+  const int n_units = (int)(u1 - u0);
+
+  const uint32_t tiles = smem_u32(smem) + warp * kStages * kStageBytes;
+  const uint32_t bars = smem_u32(smem + SmemLayout::kBars) + warp * kStages * 8;
+  int* my_pid = spid + warp * kStages;
+  if (lane == 0) {
+    for (int st = 0; st < kStages; ++st) mbar_init(bars + 8 * st, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  // Page ids of the next 64 units, one per lane in two chunks.
+  int pidA = unit_page(u0 + lane, u1, prefix, p);
+  int pidB = unit_page(u0 + 32 + lane, u1, prefix, p);
+  int chunk_base = 0;
+  Cursor ci;
+  cursor_seek(ci, u0, prefix, S);
+  int iv = 0;
+  bool timed_out = false;
+
+  auto issue = [&](int stage) {
+    const int rel = iv - chunk_base;
+    const int pid = __shfl_sync(0xffffffffu, rel < 32 ? pidA : pidB, rel & 31);
+    if (lane == 0) {
+      my_pid[stage] = pid;
+      const uint32_t bar = bars + 8 * stage;
+      if (pid >= 0) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, kStageBytes);
+        const uint32_t dst = tiles + stage * kStageBytes;
+        const int zk = (pid * 2 + 0) * PKV_NUM_KV_HEADS + ci.g;
+        const int zv = (pid * 2 + 1) * PKV_NUM_KV_HEADS + ci.g;
+        tma_load_3d(dst, &tmap, 0, 0, zk, bar);
+        tma_load_3d(dst + kTileBytes, &tmap, 0, 0, zv, bar);
+      } else {
+        mbar_arrive(bar);  // keep the phase sequence of this stage intact
+      }
+    }
+    cursor_next(ci, prefix, S);
+    ++iv;
+    if (iv - chunk_base == 32) {
+      pidA = pidB;
+      chunk_base += 32;
+      pidB = unit_page(u0 + chunk_base + 32 + lane, u1, prefix, p);
+    }
+  };
+
+  for (int st = 0; st < kStages && iv < n_units; ++st) issue(st);
+  __syncwarp();
+
+  State st;
+  Cursor cc;
+  cursor_seek(cc, u0, prefix, S);
+  st.reset();
+  st.load_q(p, cc.s, cc.g, lane);
+  int seg_len = __ldg(p.seq_lens + cc.s);
+  bool seg_bad = false;
+
+  for (int uc = 0; uc < n_units; ++uc) {
+    const int stage = uc % kStages;
+    const uint32_t parity = (uint32_t)(uc / kStages) & 1u;
+    const int pid = my_pid[stage];
+    if (!timed_out) {
+      if (!mbar_wait_bounded(bars + 8 * stage, parity, kWaitLimitNs)) {
+        timed_out = true;
+        if (lane == 0) report_error(p.d_err, PKV_ERR_TIMEOUT);
+      }
+    }
+    if (timed_out) {
+      seg_bad = true;
+    } else if (pid >= 0) {
+      const int valid = min(PKV_PAGE_TOKENS, seg_len - PKV_PAGE_TOKENS * cc.j);
+      const uint32_t sK = tiles + stage * kStageBytes;
+      st.page(sK, sK + kTileBytes, valid, p.sl2, lane);
+    } else {
+      seg_bad = true;
+      if (lane == 0) report_error(p.d_err, PKV_ERR_DEVICE_INDEX);
+    }
+    __syncwarp();
+    if (!timed_out && iv < n_units) issue(stage);
+    const bool seg_end = (cc.j == cc.np - 1) || (uc == n_units - 1);
+    if (seg_end) {
+      st.write_partial(p, (uint32_t)(8 * cc.s + cc.g) + w, seg_bad, lane);
+      st.reset();
+      seg_bad = false;
+    }
+    cursor_next(cc, prefix, S);
+    if (seg_end && uc + 1 < n_units) {
+      st.load_q(p, cc.s, cc.g, lane);
+      seg_len = __ldg(p.seq_lens + cc.s);
+    }
+    __syncwarp();
+  }
+  if (timed_out) {
+    // Drain whatever this warp still has in flight before leaving (bounded).
+    for (int u = max(0, iv - kStages); u < iv; ++u) {
+      const int stage = u % kStages;
+      (void)mbar_wait_bounded(bars + 8 * stage, (uint32_t)(u / kStages) & 1u, kWaitLimitNs);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Combine: one CTA per sequence, one warp per KV head.  Lane (hh = lane/8,
+// 8 dims at 8*(lane%8)) merges the partials of segment (s, g) with
+//   M = max m_r, o = sum e^(m_r - M) o_r / sum e^(m_r - M) l_r.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) paged_decode_combine_kernel(const DecodeParams p, int nw) {
+  pdl_wait();
+  const int s = blockIdx.x, g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hh = lane >> 3, d0 = (lane & 7) * 8;
+  uint16_t* dst = p.out + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + hh) * 64 + d0;
+  const uint32_t P0 = (uint32_t)p.ws_prefix[s], P1 = (uint32_t)p.ws_prefix[s + 1];
+  const uint32_t U = 8u * (uint32_t)p.ws_prefix[p.num_seqs];
+  const uint32_t np = P1 - P0;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  float M = -INFINITY, L = 0.f;
+  bool bad = (np == 0);
+  if (np > 0) {
+    const uint32_t base = 8u * P0 + (uint32_t)g * np, last = base + np - 1;
+    const uint32_t w0 = (uint32_t)((((uint64_t)base + 1) * nw - 1) / U);
+    const uint32_t w1 = (uint32_t)((((uint64_t)last + 1) * nw - 1) / U);
+    const uint32_t sg = 8u * s + g;
+    for (uint32_t w = w0; w <= w1; ++w) {
+      const uint64_t st0 = ((uint64_t)w * U) / nw, st1 = ((uint64_t)(w + 1) * U) / nw;
+      if (st0 == st1) continue;  // this warp had no units and wrote nothing
+      const size_t r = sg + w;
+      const float2 ml = p.ws_ml[r * 4 + hh];
+      if (ml.y < 0.f) {
+        bad = true;
+        continue;
+      }
+      const float Mn = fmaxf(M, ml.x);
+      const float a = (M == Mn) ? 1.f : exp2f(M - Mn);
+      const float b = (ml.x == Mn) ? 1.f : exp2f(ml.x - Mn);
+      const float4* src = reinterpret_cast<const float4*>(p.ws_o + (r * 4 + hh) * 64 + d0);
+      const float4 o0 = src[0], o1 = src[1];
+      const float ov[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = acc[i] * a + b * ov[i];
+      L = L * a + b * ml.y;
+      M = Mn;
+    }
+  }
+  uint32_t packed[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float lo = 0.f, hi = 0.f;
+    if (!bad && L > 0.f) {
+      lo = __fdiv_rn(acc[2 * i], L);
+      hi = __fdiv_rn(acc[2 * i + 1], L);
+    }
+    packed[i] = pack_bf16x2(lo, hi);
+  }
+  *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+    else
+      (void)cudaGetLastError();
+  });
+  return fn;
+}
+
+// Pool viewed as a 3-D tensor: x = dim (64), y = token slot (16),
+// z = (page * 2 + kv) * 8 + head.  One box = one 2 KiB (page, kv, head) tile,
+// stored in shared memory with the 128-byte swizzle.
+static int make_pool_map(CUtensorMap* map, const void* pool, int num_pages) {
+  struct Cached {
+    const void* ptr = nullptr;
+    int pages = 0;
+    CUtensorMap map;
+  };
+  static thread_local Cached cache;
+  if (cache.ptr == pool && cache.pages == num_pages) {
+    *map = cache.map;
+    return PKV_OK;
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return PKV_ERR_CUDA;
+  const cuuint64_t dims[3] = {64, 16, (cuuint64_t)num_pages * 16};
+  const cuuint64_t strides[2] = {128, 2048};
+  const cuuint32_t box[3] = {64, 16, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return PKV_ERR_CUDA;
+  cache.ptr = pool;
+  cache.pages = num_pages;
+  cache.map = *map;
+  return PKV_OK;
+}
+
+struct WorkspaceLayout {
+  size_t prefix, ml, o, total;
+  int npart;
+};
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static WorkspaceLayout workspace_layout(int num_seqs, int num_sms) {
+  WorkspaceLayout w;
+  w.npart = 8 * num_seqs + num_sms * kMaxCtasPerSm * kWarps;
+  w.prefix = 0;
+  w.ml = align256(4 * (size_t)(num_seqs + 1));
+  w.o = w.ml + align256((size_t)w.npart * 4 * sizeof(float2));
+  w.total = w.o + (size_t)w.npart * 4 * 64 * sizeof(float);
+  return w;
+}
+
+template <class State>
+static int setup_split_kernel(int device, size_t smem, int* occ) {
+  static std::mutex mu;
+  static int configured[64] = {0};
+  static int cached_occ[64] = {0};
+  static size_t cached_smem[64] = {0};
+  std::lock_guard<std::mutex> lock(mu);
+  auto kern = paged_decode_split_kernel<State>;
+  if (device < 0 || device >= 64) return PKV_ERR_CUDA;
+  if (!configured[device]) {
+    const int max_smem = 227 * 1024;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e != cudaSuccess) return cuda_status(e);
+    configured[device] = 1;
+  }
+  if (cached_smem[device] != smem) {
+    int n = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kWarps * 32, smem);
+    if (e != cudaSuccess) return cuda_status(e);
+    cached_smem[device] = smem;
+    cached_occ[device] = n;
+  }
+  *occ = cached_occ[device];
+  return PKV_OK;
+}
+
+template <class State>
+static int launch_decode(const DecodeParams& prm, const CUtensorMap& map, int device, int num_sms,
+                         int max_seq_len, int min_units, int ctas_per_sm, cudaStream_t stream,
+                         int* nw_out) {
+  const size_t smem = SmemLayout::bytes(prm.num_seqs);
+  int occ = 0;
+  int rc = setup_split_kernel<State>(device, smem, &occ);
+  if (rc != PKV_OK) return rc;
+  if (occ < 1) return PKV_ERR_UNSUPPORTED_SHAPE;
+  occ = min(occ, kMaxCtasPerSm);
+  if (ctas_per_sm > 0) occ = min(occ, ctas_per_sm);
+  const long long pages_bound = max_seq_len > 0 ? (max_seq_len + 15) / 16 : 0;
+  const long long u_bound = 8ll * prm.num_seqs * pages_bound;
+  long long nw = (long long)num_sms * occ * kWarps;
+  const long long want = (u_bound + min_units - 1) / min_units;
+  if (want < nw) nw = want;
+  int ctas = (int)((nw + kWarps - 1) / kWarps);
+  if (ctas < 1) ctas = 1;
+  *nw_out = ctas * kWarps;
+
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_split_kernel<State>, map, prm);
+  if (e != cudaSuccess) return cuda_status(e);
+
+  cfg.gridDim = dim3(prm.num_seqs);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, paged_decode_combine_kernel, prm, *nw_out);
+  return cuda_status(e);
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" size_t paged_gqa_decode_workspace_bytes(int num_seqs) {
+  if (num_seqs < 0) return 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  const int sms = sm_count(dev);
+  if (sms <= 0) return 0;
+  return workspace_layout(num_seqs, sms).total;
+}
+
+extern "C" int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_pages,
+                                   const int32_t* block_tables, int bt_row_stride, int max_blocks,
+                                   const int32_t* seq_lens, int num_seqs, int max_seq_len,
+                                   void* out, float scale, void* workspace,
+                                   size_t workspace_bytes, int* d_err, void* stream,
+                                   const pkv_decode_opts* opts) {
+  if (num_seqs < 0 || num_pages < 1 || max_blocks < 1 || bt_row_stride < max_blocks)
+    return PKV_ERR_INVALID_ARGUMENT;
+  if (num_seqs == 0) return PKV_OK;
+  if (!q || !kv_pool || !block_tables || !seq_lens || !out || !workspace)
+    return PKV_ERR_INVALID_ARGUMENT;
+  if (!isfinite(scale)) return PKV_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return PKV_ERR_MISALIGNED;
+  if (num_seqs > kMaxSeqs || (long long)num_pages * 16 * 8 * 2 >= (1ll << 31) ||
+      (long long)max_blocks * PKV_PAGE_TOKENS >= (1ll << 24))
+    return PKV_ERR_UNSUPPORTED_SHAPE;
+  const int compute = opts ? opts->compute : PKV_COMPUTE_TENSOR;
+  const int min_units = (opts && opts->min_units_per_warp > 0) ? opts->min_units_per_warp : 2;
+  const int ctas_per_sm = opts ? opts->ctas_per_sm : 0;
+  if (compute != PKV_COMPUTE_TENSOR && compute != PKV_COMPUTE_FMA) return PKV_ERR_INVALID_ARGUMENT;
+
+  int dev = 0;
+  int rc = bind_stream_device(stream, &dev);
+  if (rc != PKV_OK) return rc;
+  const int sms = sm_count(dev);
+  if (sms <= 0) return PKV_ERR_CUDA;
+  const WorkspaceLayout wl = workspace_layout(num_seqs, sms);
+  if (workspace_bytes < wl.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
+
+  CUtensorMap map;
+  rc = make_pool_map(&map, kv_pool, num_pages);
+  if (rc != PKV_OK) return rc;
+
+  DecodeParams prm;
+  prm.q = static_cast<const uint16_t*>(q);
+  prm.block_tables = block_tables;
+  prm.seq_lens = seq_lens;
+  prm.out = static_cast<uint16_t*>(out);
+  prm.bt_stride = bt_row_stride;
+  prm.max_blocks = max_blocks;
+  prm.num_pages = num_pages;
+  prm.num_seqs = num_seqs;
+  prm.sl2 = scale * kLog2e;
+  prm.d_err = d_err;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  prm.ws_prefix = reinterpret_cast<int32_t*>(ws + wl.prefix);
+  prm.ws_ml = reinterpret_cast<float2*>(ws + wl.ml);
+  prm.ws_o = reinterpret_cast<float*>(ws + wl.o);
+
+  int nw = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (compute == PKV_COMPUTE_TENSOR)
+    return launch_decode<MmaState>(prm, map, dev, sms, max_seq_len, min_units, ctas_per_sm, st, &nw);
+  return launch_decode<FmaState>(prm, map, dev, sms, max_seq_len, min_units, ctas_per_sm, st, &nw);
+}
+
+extern "C" int paged_gqa_decode(const void* q, const void* kv_pool, int num_pages,
+                                const int32_t* block_tables, int bt_row_stride, int max_blocks,
+                                const int32_t* seq_lens, int num_seqs, int max_seq_len, void* out,
+                                float scale, void* workspace, size_t workspace_bytes, int* d_err,
+                                void* stream) {
+  return paged_gqa_decode_ex(q, kv_pool, num_pages, block_tables, bt_row_stride, max_blocks,
+                             seq_lens, num_seqs, max_seq_len, out, scale, workspace,
+                             workspace_bytes, d_err, stream, nullptr);
+}

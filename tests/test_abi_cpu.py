@@ -1,0 +1,152 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol that
+include/pkv.h declares, rejects bad arguments before launching anything, and
+its host-side RoPE tables and scheduler agree with the FP64 oracle exactly."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from paged_kv_gqa_append_gb300 import build as B
+
+B.build()  # no-op when libpkv.so is up to date
+import paged_kv_gqa_append_gb300 as pkv  # noqa: E402
+import workloads as W  # noqa: E402
+from oracle import admission as A, rope  # noqa: E402
+
+HEADER = os.path.join(B.ROOT, "include", "pkv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)
+    keywords = {"if", "sizeof", "return", "defined"}
+    return sorted({n for n in names if n not in keywords and not n.startswith("__")})
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert "kv_append_rope" in names and "paged_gqa_decode" in names
+    missing = [n for n in names if not hasattr(pkv.lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings():
+    assert pkv.status_string(0) == "PKV_OK"
+    assert pkv.status_string(6) == "PKV_ERR_DEVICE_INDEX"
+    assert pkv.status_string(99) == "PKV_ERR_UNKNOWN"
+    assert pkv.lib.pkv_version() >= 100
+
+
+def test_inv_freq_bit_exact_vs_oracle():
+    assert np.array_equal(pkv.pkv_rope_inv_freq_plain(500000.0), rope.inv_freq_plain(500000.0))
+    assert np.array_equal(pkv.pkv_rope_inv_freq_plain(10000.0), rope.inv_freq_plain(10000.0))
+    assert np.array_equal(pkv.pkv_rope_inv_freq_llama3(), rope.inv_freq_llama3())
+
+
+def test_rope_table_bit_exact_vs_oracle():
+    f = rope.inv_freq_llama3()
+    cos_c, sin_c = pkv.pkv_rope_table_fill(pkv.pkv_rope_inv_freq_llama3(), 2048)
+    cos_o, sin_o = rope.table(f, 2048)
+    assert np.array_equal(cos_c.view(np.uint32), cos_o.view(np.uint32))
+    assert np.array_equal(sin_c.view(np.uint32), sin_o.view(np.uint32))
+
+
+def test_credit_matches_oracle():
+    for p, n, l in [(10, 7, 2), (16, 1, 2), (17, 1, 2), (30, 129, 2), (1920, 129, 16), (1, 1, 16)]:
+        assert pkv.pkv_credit_pages(p, n, l) == A.credit_pages(p, n, l)
+
+
+def test_host_side_validation_returns_before_launch():
+    L = pkv.lib
+    null = None
+    # append: null pointers, bad sizes
+    assert L.kv_append_rope(null, null, null, null, 4, null, 1, 128, 128, null, 8, null, null,
+                            2048, null, null, null, null) == 1
+    assert L.kv_append_rope(null, null, null, null, -1, null, 1, 128, 128, null, 8, null, null,
+                            2048, null, null, null, null) == 1
+    assert L.kv_append_rope(null, null, null, null, 0, null, 1, 128, 128, null, 8, null, null,
+                            2048, null, null, null, null) == 0      # nothing to do
+    # append: q_in without q_out
+    fake = ctypes.c_void_p(0x10000)
+    assert L.kv_append_rope(fake, fake, fake, null, 1, fake, 1, 128, 128, fake, 8, fake, fake,
+                            2048, fake, null, null, null) == 1
+    # append: misaligned k
+    odd = ctypes.c_void_p(0x10002)
+    assert L.kv_append_rope(odd, fake, fake, null, 1, fake, 1, 128, 128, fake, 8, fake, fake,
+                            2048, null, null, null, null) == 2
+    # decode: zero sequences is a no-op; nulls; stride < max_blocks; misaligned pool
+    assert L.paged_gqa_decode(null, null, 8, null, 128, 128, null, 0, 0, null, 0.125, null, 0,
+                              null, null) == 0
+    assert L.paged_gqa_decode(null, null, 8, null, 128, 128, null, 1, 16, null, 0.125, null, 0,
+                              null, null) == 1
+    assert L.paged_gqa_decode(fake, fake, 8, fake, 64, 128, fake, 1, 16, fake, 0.125, fake, 1 << 20,
+                              null, null) == 1
+    assert L.paged_gqa_decode(fake, odd, 8, fake, 128, 128, fake, 1, 16, fake, 0.125, fake, 1 << 20,
+                              null, null) == 2
+    assert L.paged_gqa_decode(fake, fake, 8, fake, 128, 128, fake, 5000, 16, fake, 0.125, fake,
+                              1 << 30, null, null) == 3
+    assert L.paged_gqa_decode(fake, fake, 8, fake, 128, 128, fake, 1, 16, fake, float("nan"), fake,
+                              1 << 20, null, null) == 1
+
+
+def _run_cpp_schedule(case):
+    """Drive the C++ scheduler with the oracle's step loop; return its log."""
+    s = pkv.Scheduler(case.num_pages, case.num_layers, W.MAX_BLOCKS, 256)
+    ids = [s.submit(int(p), case.allowed_new_tokens) for p in case.prompt_lens]
+    running, length, done, log = [], {}, {}, []
+    while s.stats()["queued"] or running:
+        admitted = s.admit()
+        for rid in admitted:
+            assert s.grow(rid, int(case.prompt_lens[rid])) == pkv.OK
+            length[rid], done[rid] = int(case.prompt_lens[rid]), 0
+        running += admitted
+        lens = []
+        for rid in running:
+            assert s.grow(rid, length[rid] + 1) == pkv.OK
+            length[rid] += 1
+            done[rid] += 1
+            lens.append(length[rid])
+        finished = [r for r in running if done[r] == case.decode_steps]
+        log.append(dict(admitted=admitted, running=list(running), lens=lens, finished=finished))
+        for rid in finished:
+            s.finish(rid)
+        running = [r for r in running if r not in finished]
+    return ids, log, s
+
+
+def test_scheduler_matches_oracle_on_continuous_mix():
+    case = W.case_continuous()
+    ids_o, log_o, sch_o = A.simulate(case.prompt_lens, case.decode_steps, case.num_pages,
+                                     case.num_layers)
+    ids_c, log_c, sch_c = _run_cpp_schedule(case)
+    assert [r for _, r in ids_c] == [r for _, r in ids_o]
+    assert len(log_c) == len(log_o)
+    for a, b in zip(log_c, log_o):
+        for key in ("admitted", "running", "lens", "finished"):
+            assert a[key] == b[key], key
+    assert sch_c.events() == sch_o.events
+    assert sch_c.stats()["free"] == case.num_pages and sch_c.stats()["reserved"] == 0
+
+
+def test_scheduler_rejects_and_blocks():
+    s = pkv.Scheduler(num_pages=20, num_layers=2, max_blocks=10, max_slots=4)
+    assert s.submit(10, 7) == (pkv.OK, 0)
+    assert s.submit(30, 129) == (pkv.OK, 1)
+    assert s.submit(1, 1) == (pkv.OK, 2)
+    assert s.submit(200, 1) == (pkv.ERR_REQUEST_TOO_LARGE, -1)
+    assert s.submit(40, 129) == (pkv.ERR_REQUEST_TOO_LARGE, -1)
+    assert s.admit() == [0]
+    assert s.grow(0, 10) == pkv.OK
+    assert s.admit() == []
+    assert s.grow(0, 17) == pkv.ERR_POOL_EXHAUSTED
+    s.finish(0)
+    assert s.admit() == [1]
+    assert s.grow(1, 30) == pkv.OK
+    assert s.events() == [(0, 0, 0, 0), (0, 1, 0, 1), (1, 0, 0, 1), (1, 0, 1, 0), (1, 1, 0, 2),
+                          (1, 1, 1, 3)]
+    row, slot = s.block_table(1, 1)
+    assert list(row[:3]) == [2, 3, -1] and slot == 0
+    assert s.stats() == dict(free=16, reserved=16, queued=1, running=1)

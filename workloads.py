@@ -152,8 +152,9 @@ def fill_pool(case: DecodeCase, device="cpu", chunk_pages: int = 8192) -> torch.
         n_vec = case.num_pages * NUM_KV_HEADS * PAGE_TOKENS
         n_out = int(round(case.outlier_frac * n_vec))
         idx = torch.randperm(n_vec, generator=gen, device=device)[:n_out]
-        keys = pool[:, 0].reshape(n_vec, HEAD_DIM)          # view into K halves
-        keys[idx] = keys[idx] * 8                           # x8 is exact in bf16
+        page, vec = idx // (NUM_KV_HEADS * PAGE_TOKENS), idx % (NUM_KV_HEADS * PAGE_TOKENS)
+        kv = pool.view(case.num_pages, 2, NUM_KV_HEADS * PAGE_TOKENS, HEAD_DIM)
+        kv[page, 0, vec] = kv[page, 0, vec] * 8              # x8 is exact in bf16
     return pool
 
 
