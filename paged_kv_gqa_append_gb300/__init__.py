@@ -4,8 +4,8 @@ The functions carry the C-ABI names and only marshal arguments: they check
 dtypes, devices and shapes of torch tensors, pass raw pointers, sizes and the
 current CUDA stream to the library, and raise ``PkvError`` on a non-zero
 status.  Every step of the computation runs in the library's sm_103a kernels;
-there is no fallback.  Importing this package fails loudly when libpkv.so is
-missing (build it with ``python -m paged_kv_gqa_append_gb300.build``).
+there is no fallback: the first call raises when libpkv.so is missing (build
+it with ``python -m paged_kv_gqa_append_gb300.build``).
 
 Tensor layouts (see include/pkv.h):
     kv_pool       [num_pages, 2, 8, 16, 64] bf16   (K = 0, V = 1), 32 KiB/page
@@ -48,12 +48,6 @@ class PkvError(RuntimeError):
         super().__init__(f"{where}: {STATUS.get(status, status)}")
 
 
-if not os.path.exists(LIB_PATH):
-    raise ImportError(f"libpkv.so not found at {LIB_PATH}; build it with "
-                      "`python -m paged_kv_gqa_append_gb300.build` (nvcc for sm_103a)")
-
-lib = ctypes.CDLL(LIB_PATH)
-
 _p, _i, _f, _d, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_size_t
 _ip = ctypes.POINTER(ctypes.c_int)
 
@@ -86,10 +80,30 @@ _SIGS = {
     "pkv_sched_event_count": (_i, [_p]),
     "pkv_sched_event": (_i, [_p, _i, _ip, _ip, _ip, _ip]),
 }
-for _name, (_res, _args) in _SIGS.items():
-    _fn = getattr(lib, _name)
-    _fn.restype = _res
-    _fn.argtypes = _args
+
+_LIB = None
+
+
+def _L():
+    """The loaded libpkv.so; raises if it has not been built (no fallback exists)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libpkv.so not found at {LIB_PATH}; build it with "
+                               "`python -m paged_kv_gqa_append_gb300.build` (nvcc, sm_103a)")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def __getattr__(name):
+    if name == "lib":
+        return _L()
+    raise AttributeError(name)
 
 
 def _check(status: int, where: str):
@@ -121,21 +135,21 @@ def _need(t, name, dtype, device=None, shape_tail=None):
 
 
 def status_string(status: int) -> str:
-    return lib.pkv_status_string(status).decode()
+    return _L().pkv_status_string(status).decode()
 
 
 # --------------------------------------------------------------- RoPE set-up --
 
 def pkv_rope_inv_freq_plain(theta: float = 500000.0) -> np.ndarray:
     out = np.zeros(ROPE_PAIRS, np.float64)
-    _check(lib.pkv_rope_inv_freq_plain(out.ctypes.data, theta), "pkv_rope_inv_freq_plain")
+    _check(_L().pkv_rope_inv_freq_plain(out.ctypes.data, theta), "pkv_rope_inv_freq_plain")
     return out
 
 
 def pkv_rope_inv_freq_llama3(theta=500000.0, factor=32.0, low_freq_factor=1.0,
                              high_freq_factor=4.0, original_max_pos=8192) -> np.ndarray:
     out = np.zeros(ROPE_PAIRS, np.float64)
-    _check(lib.pkv_rope_inv_freq_llama3(out.ctypes.data, theta, factor, low_freq_factor,
+    _check(_L().pkv_rope_inv_freq_llama3(out.ctypes.data, theta, factor, low_freq_factor,
                                         high_freq_factor, original_max_pos),
            "pkv_rope_inv_freq_llama3")
     return out
@@ -148,7 +162,7 @@ def pkv_rope_table_fill(inv_freq, max_pos: int):
         raise ValueError("inv_freq must have 32 entries")
     cos = np.empty((max_pos, ROPE_PAIRS), np.float32)
     sin = np.empty_like(cos)
-    _check(lib.pkv_rope_table_fill(cos.ctypes.data, sin.ctypes.data, max_pos, f.ctypes.data),
+    _check(_L().pkv_rope_table_fill(cos.ctypes.data, sin.ctypes.data, max_pos, f.ctypes.data),
            "pkv_rope_table_fill")
     return cos, sin
 
@@ -197,7 +211,7 @@ def kv_append_rope(k, v, positions, block_tables, kv_pool, rope_cos, rope_sin,
         _need(d_err, "d_err", torch.int32, dev)
     S, stride = block_tables.shape
     mb = stride if max_blocks is None else max_blocks
-    st = lib.kv_append_rope(_ptr(k), _ptr(v), _ptr(positions), _ptr(token_seq), T,
+    st = _L().kv_append_rope(_ptr(k), _ptr(v), _ptr(positions), _ptr(token_seq), T,
                             _ptr(block_tables), S, stride, mb, _ptr(kv_pool), kv_pool.shape[0],
                             _ptr(rope_cos), _ptr(rope_sin), rope_cos.shape[0],
                             _ptr(q_in), _ptr(q_out), _ptr(d_err), _stream(stream))
@@ -207,7 +221,7 @@ def kv_append_rope(k, v, positions, block_tables, kv_pool, rope_cos, rope_sin,
 # ------------------------------------------------------------------- decode --
 
 def paged_gqa_decode_workspace_bytes(num_seqs: int) -> int:
-    return int(lib.paged_gqa_decode_workspace_bytes(num_seqs))
+    return int(_L().paged_gqa_decode_workspace_bytes(num_seqs))
 
 
 def alloc_workspace(num_seqs: int, device) -> torch.Tensor:
@@ -249,18 +263,18 @@ def paged_gqa_decode(q, kv_pool, block_tables, seq_lens, out, scale, workspace=N
             _ptr(seq_lens), S, int(max_seq_len), _ptr(out), float(scale), _ptr(workspace),
             workspace.numel(), _ptr(d_err), _stream(stream))
     if compute is None and not min_units_per_warp and not ctas_per_sm:
-        st = lib.paged_gqa_decode(*args)
+        st = _L().paged_gqa_decode(*args)
     else:
         opts = DecodeOpts(COMPUTE_TENSOR if compute is None else compute,
                           min_units_per_warp, ctas_per_sm)
-        st = lib.paged_gqa_decode_ex(*args, ctypes.byref(opts))
+        st = _L().paged_gqa_decode_ex(*args, ctypes.byref(opts))
     _check(st, "paged_gqa_decode")
 
 
 def pkv_read_device_error(d_err, clear: bool = True, stream=None) -> int:
     """Synchronise the stream and return the device error word (optionally reset it)."""
     code = ctypes.c_int(0)
-    _check(lib.pkv_read_device_error(_ptr(d_err), _stream(stream), int(clear), ctypes.byref(code)),
+    _check(_L().pkv_read_device_error(_ptr(d_err), _stream(stream), int(clear), ctypes.byref(code)),
            "pkv_read_device_error")
     return code.value
 
@@ -268,14 +282,14 @@ def pkv_read_device_error(d_err, clear: bool = True, stream=None) -> int:
 # ---------------------------------------------------------------- scheduler --
 
 def pkv_credit_pages(prompt_tokens: int, allowed_new_tokens: int, num_layers: int) -> int:
-    return int(lib.pkv_credit_pages(prompt_tokens, allowed_new_tokens, num_layers))
+    return int(_L().pkv_credit_pages(prompt_tokens, allowed_new_tokens, num_layers))
 
 
 class Scheduler:
     """Continuous-batching admission and page allocation (C++ pkv_sched)."""
 
     def __init__(self, num_pages: int, num_layers: int, max_blocks: int = 128, max_slots: int = 256):
-        self._h = lib.pkv_sched_create(num_pages, num_layers, max_blocks, max_slots)
+        self._h = _L().pkv_sched_create(num_pages, num_layers, max_blocks, max_slots)
         if not self._h:
             raise PkvError(1, "pkv_sched_create")
         self.num_layers, self.max_blocks, self.max_slots = num_layers, max_blocks, max_slots
@@ -283,13 +297,13 @@ class Scheduler:
     def __del__(self):
         h = getattr(self, "_h", None)
         if h:
-            lib.pkv_sched_destroy(h)
+            _L().pkv_sched_destroy(h)
             self._h = None
 
     def submit(self, prompt_tokens: int, allowed_new_tokens: int):
         """Returns (status, request id); oversize requests give ERR_REQUEST_TOO_LARGE."""
         rid = ctypes.c_int(-1)
-        st = lib.pkv_sched_submit(self._h, prompt_tokens, allowed_new_tokens, ctypes.byref(rid))
+        st = _L().pkv_sched_submit(self._h, prompt_tokens, allowed_new_tokens, ctypes.byref(rid))
         if st not in (OK, ERR_REQUEST_TOO_LARGE):
             raise PkvError(st, "pkv_sched_submit")
         return st, rid.value
@@ -297,35 +311,35 @@ class Scheduler:
     def admit(self):
         buf = (ctypes.c_int * self.max_slots)()
         n = ctypes.c_int(0)
-        _check(lib.pkv_sched_admit(self._h, buf, self.max_slots, ctypes.byref(n)), "pkv_sched_admit")
+        _check(_L().pkv_sched_admit(self._h, buf, self.max_slots, ctypes.byref(n)), "pkv_sched_admit")
         return list(buf[:n.value])
 
     def grow(self, rid: int, new_len: int) -> int:
-        st = lib.pkv_sched_grow(self._h, rid, new_len)
+        st = _L().pkv_sched_grow(self._h, rid, new_len)
         if st not in (OK, ERR_POOL_EXHAUSTED):
             raise PkvError(st, "pkv_sched_grow")
         return st
 
     def finish(self, rid: int):
-        _check(lib.pkv_sched_finish(self._h, rid), "pkv_sched_finish")
+        _check(_L().pkv_sched_finish(self._h, rid), "pkv_sched_finish")
 
     def block_table(self, rid: int, layer: int):
         row = np.empty(self.max_blocks, np.int32)
         slot = ctypes.c_int(-1)
-        _check(lib.pkv_sched_block_table(self._h, rid, layer, row.ctypes.data, ctypes.byref(slot)),
+        _check(_L().pkv_sched_block_table(self._h, rid, layer, row.ctypes.data, ctypes.byref(slot)),
                "pkv_sched_block_table")
         return row, slot.value
 
     def stats(self):
         v = [ctypes.c_int(0) for _ in range(4)]
-        _check(lib.pkv_sched_stats(self._h, *[ctypes.byref(x) for x in v]), "pkv_sched_stats")
+        _check(_L().pkv_sched_stats(self._h, *[ctypes.byref(x) for x in v]), "pkv_sched_stats")
         return dict(free=v[0].value, reserved=v[1].value, queued=v[2].value, running=v[3].value)
 
     def events(self):
-        n = lib.pkv_sched_event_count(self._h)
+        n = _L().pkv_sched_event_count(self._h)
         out = []
         v = [ctypes.c_int(0) for _ in range(4)]
         for i in range(n):
-            _check(lib.pkv_sched_event(self._h, i, *[ctypes.byref(x) for x in v]), "pkv_sched_event")
+            _check(_L().pkv_sched_event(self._h, i, *[ctypes.byref(x) for x in v]), "pkv_sched_event")
             out.append(tuple(x.value for x in v))
         return out
