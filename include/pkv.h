@@ -77,6 +77,11 @@ typedef enum pkv_status {
 /* Human-readable name of a status code (static string, never NULL). */
 const char* pkv_status_string(int status);
 
+/* Description of the last PKV_ERR_CUDA raised on the calling thread (the
+ * failing CUDA call and its error string); "" if none.  Static per-thread
+ * storage, valid until the next failing call on that thread. */
+const char* pkv_last_error(void);
+
 /* Library version as 10000*major + 100*minor + patch. */
 int pkv_version(void);
 

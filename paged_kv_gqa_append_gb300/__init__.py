@@ -43,9 +43,10 @@ OK, ERR_DEVICE_INDEX, ERR_POOL_EXHAUSTED, ERR_REQUEST_TOO_LARGE, ERR_TIMEOUT = 0
 
 
 class PkvError(RuntimeError):
-    def __init__(self, status: int, where: str):
+    def __init__(self, status: int, where: str, detail: str = ""):
         self.status = status
-        super().__init__(f"{where}: {STATUS.get(status, status)}")
+        msg = f"{where}: {STATUS.get(status, status)}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
 
 
 _p, _i, _f, _d, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_size_t
@@ -59,6 +60,7 @@ class DecodeOpts(ctypes.Structure):
 _SIGS = {
     "pkv_status_string": (ctypes.c_char_p, [_i]),
     "pkv_version": (_i, []),
+    "pkv_last_error": (ctypes.c_char_p, []),
     "pkv_rope_inv_freq_plain": (_i, [_p, _d]),
     "pkv_rope_inv_freq_llama3": (_i, [_p, _d, _d, _d, _d, _i]),
     "pkv_rope_table_fill": (_i, [_p, _p, _i, _p]),
@@ -108,7 +110,8 @@ def __getattr__(name):
 
 def _check(status: int, where: str):
     if status != OK:
-        raise PkvError(status, where)
+        detail = _L().pkv_last_error().decode() if status == 5 else ""
+        raise PkvError(status, where, detail)
 
 
 def _ptr(t):

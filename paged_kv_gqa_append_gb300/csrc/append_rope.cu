@@ -160,5 +160,5 @@ extern "C" int kv_append_rope(const void* k, const void* v, const int32_t* posit
   cfg.stream = static_cast<cudaStream_t>(stream);
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_status(cudaLaunchKernelEx(&cfg, kv_append_rope_kernel, p));
+  return cuda_status(cudaLaunchKernelEx(&cfg, kv_append_rope_kernel, p), "cudaLaunchKernelEx(append)");
 }

@@ -8,28 +8,35 @@
 #include <math.h>
 #include <mutex>
 #include <stdint.h>
+#include <stdio.h>
 
 #include "internal.h"
 #include "pkv.h"
 
 namespace pkv {
 
+static thread_local char g_last_error[256] = "";
+
+void set_last_error(const char* where, const char* what) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where ? where : "?", what ? what : "?");
+}
+
 int bind_stream_device(void* stream, int* device_out) {
   int dev = 0;
   cudaError_t e;
   if (stream != nullptr) {
     e = cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &dev);
-    if (e != cudaSuccess) return cuda_status(e);
+    if (e != cudaSuccess) return cuda_status(e, "cudaStreamGetDevice");
     int cur = -1;
     e = cudaGetDevice(&cur);
-    if (e != cudaSuccess) return cuda_status(e);
+    if (e != cudaSuccess) return cuda_status(e, "cudaGetDevice");
     if (cur != dev) {
       e = cudaSetDevice(dev);
-      if (e != cudaSuccess) return cuda_status(e);
+      if (e != cudaSuccess) return cuda_status(e, "cudaSetDevice");
     }
   } else {
     e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_status(e);
+    if (e != cudaSuccess) return cuda_status(e, "cudaGetDevice");
   }
   *device_out = dev;
   return PKV_OK;
@@ -70,6 +77,8 @@ extern "C" const char* pkv_status_string(int status) {
     default: return "PKV_ERR_UNKNOWN";
   }
 }
+
+extern "C" const char* pkv_last_error(void) { return g_last_error; }
 
 extern "C" int pkv_version(void) { return 10000 * 0 + 100 * 1 + 0; }
 
@@ -129,11 +138,11 @@ extern "C" int pkv_read_device_error(int* d_err, void* stream, int clear, int* c
   int host = 0;
   cudaError_t e = cudaMemcpyAsync(&host, d_err, sizeof(int), cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-  if (e != cudaSuccess) return cuda_status(e);
+  if (e != cudaSuccess) return cuda_status(e, "pkv_read_device_error");
   *code_out = host;
   if (clear) {
     e = cudaMemsetAsync(d_err, 0, sizeof(int), st);
-    if (e != cudaSuccess) return cuda_status(e);
+    if (e != cudaSuccess) return cuda_status(e, "pkv_read_device_error clear");
   }
   return PKV_OK;
 }

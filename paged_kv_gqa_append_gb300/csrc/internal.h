@@ -19,9 +19,13 @@ int sm_count(int device);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-inline int cuda_status(cudaError_t e) {
+// Remember a failure description for pkv_last_error() (per thread).
+void set_last_error(const char* where, const char* what);
+
+inline int cuda_status(cudaError_t e, const char* where = "cuda") {
   if (e == cudaSuccess) return PKV_OK;
-  (void)cudaGetLastError();  // clear the sticky-free error state for the next call
+  set_last_error(where, cudaGetErrorString(e));
+  (void)cudaGetLastError();  // clear the non-sticky error state for the next call
   return PKV_ERR_CUDA;
 }
 

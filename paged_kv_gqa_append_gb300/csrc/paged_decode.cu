@@ -32,6 +32,7 @@
 #include <math.h>
 #include <mutex>
 #include <stdint.h>
+#include <stdio.h>
 #include <string.h>
 
 #include "internal.h"
@@ -612,7 +613,10 @@ static int make_pool_map(CUtensorMap* map, const void* pool, int num_pages) {
     return PKV_OK;
   }
   EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return PKV_ERR_CUDA;
+  if (fn == nullptr) {
+    set_last_error("cudaGetDriverEntryPointByVersion", "cuTensorMapEncodeTiled unavailable");
+    return PKV_ERR_CUDA;
+  }
   const cuuint64_t dims[3] = {64, 16, (cuuint64_t)num_pages * 16};
   const cuuint64_t strides[2] = {128, 2048};
   const cuuint32_t box[3] = {64, 16, 1};
@@ -620,7 +624,12 @@ static int make_pool_map(CUtensorMap* map, const void* pool, int num_pages) {
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return PKV_ERR_CUDA;
+  if (r != CUDA_SUCCESS) {
+    char msg[64];
+    snprintf(msg, sizeof(msg), "CUresult %d", (int)r);
+    set_last_error("cuTensorMapEncodeTiled", msg);
+    return PKV_ERR_CUDA;
+  }
   cache.ptr = pool;
   cache.pages = num_pages;
   cache.map = *map;
@@ -652,17 +661,20 @@ static int setup_split_kernel(int device, size_t smem, int* occ) {
   static size_t cached_smem[64] = {0};
   std::lock_guard<std::mutex> lock(mu);
   auto kern = paged_decode_split_kernel<State>;
-  if (device < 0 || device >= 64) return PKV_ERR_CUDA;
+  if (device < 0 || device >= 64) {
+    set_last_error("setup_split_kernel", "device index out of range");
+    return PKV_ERR_CUDA;
+  }
   if (!configured[device]) {
     const int max_smem = 227 * 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-    if (e != cudaSuccess) return cuda_status(e);
+    if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(split)");
     configured[device] = 1;
   }
   if (cached_smem[device] != smem) {
     int n = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kWarps * 32, smem);
-    if (e != cudaSuccess) return cuda_status(e);
+    if (e != cudaSuccess) return cuda_status(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
     cached_smem[device] = smem;
     cached_occ[device] = n;
   }
@@ -701,13 +713,13 @@ static int launch_decode(const DecodeParams& prm, const CUtensorMap& map, int de
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_split_kernel<State>, map, prm);
-  if (e != cudaSuccess) return cuda_status(e);
+  if (e != cudaSuccess) return cuda_status(e, "cudaLaunchKernelEx(split)");
 
   cfg.gridDim = dim3(prm.num_seqs);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   e = cudaLaunchKernelEx(&cfg, paged_decode_combine_kernel, prm, *nw_out);
-  return cuda_status(e);
+  return cuda_status(e, "cudaLaunchKernelEx(combine)");
 }
 
 }  // namespace pkv
