@@ -659,6 +659,7 @@ static int setup_split_kernel(int device, size_t smem, int* occ) {
   static int configured[64] = {0};
   static int cached_occ[64] = {0};
   static size_t cached_smem[64] = {0};
+  static int max_dyn_smem[64] = {0};
   std::lock_guard<std::mutex> lock(mu);
   auto kern = paged_decode_split_kernel<State>;
   if (device < 0 || device >= 64) {
@@ -666,11 +667,20 @@ static int setup_split_kernel(int device, size_t smem, int* occ) {
     return PKV_ERR_CUDA;
   }
   if (!configured[device]) {
-    const int max_smem = 227 * 1024;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    // opt-in limit per block minus this kernel's static shared memory
+    int optin = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+    if (e != cudaSuccess) return cuda_status(e, "cudaDeviceGetAttribute(smem optin)");
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return cuda_status(e, "cudaFuncGetAttributes(split)");
+    const int max_dyn = optin - (int)fa.sharedSizeBytes;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
     if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(split)");
+    max_dyn_smem[device] = max_dyn;
     configured[device] = 1;
   }
+  if ((long long)smem > max_dyn_smem[device]) return PKV_ERR_UNSUPPORTED_SHAPE;
   if (cached_smem[device] != smem) {
     int n = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kWarps * 32, smem);
