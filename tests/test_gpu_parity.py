@@ -81,11 +81,12 @@ def test_append_single_sequence_bit_exact(lib, cuda_device, tables):
 def test_append_many_sequences_bit_exact_inplace_q(lib, cuda_device, tables):
     cos_d, sin_d, cos_o, sin_o = tables
     rng = np.random.default_rng(11)
-    S, N, T = 6, 64, 700
+    S, N, T = 6, 64, 500
     pool0 = OP.new_pool(N, 0x1234)
     perm = rng.permutation(N).astype(np.int32)
     bt = np.full((S, 128), -1, np.int32)
-    caps = [160, 16, 33, 300, 1, 129]
+    caps = [160, 16, 33, 300, 1, 129]     # 639 distinct (row, position) pairs >= T
+    assert sum(caps) >= T
     cur = 0
     for s, c in enumerate(caps):
         n = (c + 15) // 16
