@@ -265,55 +265,53 @@ def run_gb300(args, world, rank, local):
     lens = torch.from_numpy(case.seq_lens).to(dev)
     pos = torch.from_numpy(W.new_positions(case)).to(dev)
     cos, sin = pkv.rope_tables_device(dev, W.MAX_CONTEXT)
-    q_rot = torch.empty_like(q_raw)
     out = torch.empty_like(q_raw)
-    ws = pkv.alloc_workspace(S, dev)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
     kv_bytes_layer = case.kv_bytes_per_layer()
-    kw = dict(workspace=ws, max_seq_len=case.max_seq_len, d_err=err,
-              compute=None if compute == pkv.COMPUTE_TENSOR else compute)
-
-    def step(ev=None):
-        for l in range(L):
-            pkv.kv_append_rope(k_new[l], v_new[l], pos, bt[l], pool, cos, sin,
-                               q_in=q_raw[l], q_out=q_rot[l], d_err=err)
-            if ev is not None:
-                ev[l][0].record(stream)
-            pkv.paged_gqa_decode(q_rot[l], pool, bt[l], lens, out[l], case.scale, **kw)
-            if ev is not None:
-                ev[l][1].record(stream)
+    step = pkv.DecodeStep(pool, bt, lens, pos, k_new, v_new, q_raw, out, cos, sin, case.scale,
+                          max_seq_len=case.max_seq_len,
+                          compute=None if compute == pkv.COMPUTE_TENSOR else compute)
+    stream = torch.cuda.current_stream(dev)
 
     for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    code = pkv.pkv_read_device_error(err)
+        step.run()
+    code = step.error()
     if code != 0:
         raise RuntimeError(f"device error {pkv.status_string(code)} during warm-up")
 
-    # ---- headline: K steps, device-timed, inputs resident in HBM ----------
+    # ---- headline: K graph replays of the step, inputs resident in HBM -----
     clocks = ClockSampler(dev.index) if rank == 0 else None
     time.sleep(0.5 if clocks else 0)
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.time()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    dec_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(L)] for _ in range(args.steps)]
     e0.record(stream)
-    for i in range(args.steps):
-        step(dec_ev[i])
+    for _ in range(args.steps):
+        step.run()
     e1.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     barrier(world)
-    ms_local = e0.elapsed_time(e1)
-    dec_ms = [a.elapsed_time(b) for row in dec_ev for (a, b) in row]
-    ms = max_over_ranks(ms_local, world, dev)
-    code = pkv.pkv_read_device_error(err)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    code = step.error()
     if code != 0:
         raise RuntimeError(f"device error {pkv.status_string(code)} in the timed region")
-    clk = clocks.summary(t_wall0, t_wall1) if clocks else None
+
+    # ---- roofline: the decode kernel alone, L launches per graph replay ----
+    g_dec = step.decode_only_graph()
+    for _ in range(3):
+        g_dec.replay()
+    k_roof = max(10, args.steps // 4)
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    r0.record(stream)
+    for _ in range(k_roof):
+        g_dec.replay()
+    r1.record(stream)
+    torch.cuda.synchronize()
+    dec_avg_ms = r0.elapsed_time(r1) / (k_roof * L)
+    t_wall2 = time.time()
+    clk = clocks.summary(t_wall0, t_wall2) if clocks else None
     if clocks:
         clocks.stop()
 
@@ -324,14 +322,15 @@ def run_gb300(args, world, rank, local):
     tokens_per_s = S * steps * world / sec
     us_per_layer = ms * 1e3 / (steps * L)
 
-    # ---- e2e: same step through the public API with host buffers ----------
+    # ---- e2e: the same step with its inputs uploaded and output read back --
     e2e = None
     if not args.no_e2e:
         q_h = q_raw.cpu().pin_memory()
         k_h, v_h = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
         pos_h, lens_h = pos.cpu().pin_memory(), lens.cpu().pin_memory()
+        bt_h = bt.cpu().pin_memory()
         out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, pos_h, lens_h))
+        h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, pos_h, lens_h, bt_h))
         d2h = out_h.numel() * out_h.element_size()
         k_e2e = max(1, min(steps, 500))
         barrier(world)
@@ -345,7 +344,8 @@ def run_gb300(args, world, rank, local):
             v_new.copy_(v_h, non_blocking=True)
             pos.copy_(pos_h, non_blocking=True)
             lens.copy_(lens_h, non_blocking=True)
-            step()
+            bt.copy_(bt_h, non_blocking=True)
+            step.run()
             out_h.copy_(out, non_blocking=True)
         b.record(stream)
         torch.cuda.synchronize()
@@ -353,17 +353,20 @@ def run_gb300(args, world, rank, local):
         e2e_s = max_over_ranks(max(a.elapsed_time(b) / 1e3, host_s), world, dev)
         e2e = {"value": kv_bytes_layer * L * k_e2e * world / e2e_s / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps": k_e2e, "tokens_per_s": S * k_e2e * world / e2e_s}
+               "steps": k_e2e, "tokens_per_s": S * k_e2e * world / e2e_s,
+               "path": "DecodeStep graph replay + pinned H2D/D2H copies"}
+        if step.error() != 0:
+            raise RuntimeError("device error in the e2e region")
 
-    # ---- roofline of the dominant kernel (decode: split + combine) --------
+    # ---- roofline of the dominant kernel -----------------------------------
     peak, peak_kind = hbm_peak()
-    dec_avg_ms = sum(dec_ms) / len(dec_ms)
     achieved = kv_bytes_layer / (dec_avg_ms / 1e3) / 1e9
     tag = "paged_decode_split_" + ("mma" if compute == pkv.COMPUTE_TENSOR else "fma")
     traffic = ncu_traffic(f"{tag}:{case.name}")
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
-            "kernel": "paged_gqa_decode (split + combine), avg of %d launches" % len(dec_ms),
+            "kernel": f"{tag} (paged_gqa_decode: one launch per layer)",
+            "launches_timed": k_roof * L,
             "algorithmic_bytes_per_launch": kv_bytes_layer,
             "avg_launch_us": dec_avg_ms * 1e3}
 
@@ -383,11 +386,12 @@ def run_gb300(args, world, rank, local):
                        "ctx": int(case.seq_lens[0]), "pool_pages": case.num_pages,
                        "pool_bytes": case.num_pages * W.PAGE_ELEMS * 2,
                        "l2": "inputs larger than L2 (pool read per step exceeds 129 MB L2)",
-                       "parallelism": f"replicas x{world}", "compute": args.compute},
+                       "parallelism": f"replicas x{world}", "compute": args.compute,
+                       "launch": "CUDA graph of the step (append + decode per layer)"},
             "tokens_per_s": tokens_per_s, "us_per_layer": us_per_layer,
             "kv_bytes_per_step": kv_bytes_layer * L,
             "hbm_frac_step": value / world / peak,
-            "clocks": clk, "e2e": e2e, "gpu_launches": 3 * L * steps,
+            "clocks": clk, "e2e": e2e, "gpu_launches": step.launches_per_step * steps,
             "roofline": roof, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -151,8 +151,9 @@ int kv_append_rope(const void* k, const void* v, const int32_t* positions,
  * K_j/V_j are read from slot j % 16 of page block_tables[s][j / 16].
  * Loads are bf16, all arithmetic fp32 (exponentials in base 2), output
  * rounded to bf16 nearest-even.  Work is split into page ranges spread
- * evenly over the GPU (flash-decoding); partial (o, m, l) triples go to the
- * workspace and a second kernel merges them with a log-sum-exp combine.
+ * evenly over the GPU (flash-decoding); the partial (o, m, l) triples of a
+ * sequence split across warps go to the workspace and the last warp to
+ * finish merges them with a log-sum-exp combine (one kernel launch).
  *
  *   q             device bf16 [num_seqs][32][64] (already rotated)
  *   kv_pool       device bf16 pool as in kv_append_rope, 16-byte aligned
@@ -162,8 +163,13 @@ int kv_append_rope(const void* k, const void* v, const int32_t* positions,
  *                 actual length is still handled correctly)
  *   out           device bf16 [num_seqs][32][64]
  *   workspace     device memory of at least
- *                 paged_gqa_decode_workspace_bytes(num_seqs) bytes,
- *                 16-byte aligned, contents need not be initialised
+ *                 paged_gqa_decode_workspace_bytes(num_seqs) bytes, 16-byte
+ *                 aligned and zero-filled before its first use.  Each call
+ *                 leaves it zero-filled again (per-segment arrival counters
+ *                 are reset by the warp that merges the segment), so one
+ *                 workspace serves any number of calls in stream order;
+ *                 calls that may run at the same time need distinct
+ *                 workspaces.  After a PKV_ERR_TIMEOUT, zero it again.
  * seq_len 0 gives a zero output.  A negative seq_len, seq_len above
  * 16 * max_blocks, or a needed page id outside [0, num_pages) gives a zero
  * output for that sequence and sets *d_err = PKV_ERR_DEVICE_INDEX.

@@ -228,12 +228,12 @@ def paged_gqa_decode_workspace_bytes(num_seqs: int) -> int:
 
 
 def alloc_workspace(num_seqs: int, device) -> torch.Tensor:
-    """Caller-owned workspace for paged_gqa_decode (uninitialised bytes)."""
+    """Caller-owned workspace for paged_gqa_decode, zero-filled as the call requires."""
     with torch.cuda.device(device):
         n = paged_gqa_decode_workspace_bytes(num_seqs)
     if n <= 0:
         raise PkvError(5, "paged_gqa_decode_workspace_bytes")
-    return torch.empty(n, dtype=torch.uint8, device=device)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
 def paged_gqa_decode(q, kv_pool, block_tables, seq_lens, out, scale, workspace=None,
@@ -346,3 +346,75 @@ class Scheduler:
             _check(_L().pkv_sched_event(self._h, i, *[ctypes.byref(x) for x in v]), "pkv_sched_event")
             out.append(tuple(x.value for x in v))
         return out
+
+
+# --------------------------------------------------------------- decode step --
+
+class DecodeStep:
+    """One decode step over every layer, captured once into a CUDA graph.
+
+    Per layer l (in order, as a model runs them):
+        kv_append_rope(k[l], v[l], positions, block_tables[l], pool, cos, sin,
+                       q_in=q[l], q_out=q_rot[l])
+        paged_gqa_decode(q_rot[l], pool, block_tables[l], seq_lens, out[l], scale)
+    so token s of layer l is written at positions[s] of row s and attended
+    with seq_lens[s] tokens.  The tensors are bound at construction: refresh
+    their contents in place (new K/V/q, positions, lengths, tables) and call
+    run().  Replaying the graph removes the per-call host cost, and the
+    kernels' programmatic-dependent-launch edges overlap each launch with
+    the previous kernel's tail.
+
+        pool          [num_pages, 2, 8, 16, 64] bf16
+        block_tables  [L, S, max_blocks] int32
+        seq_lens      [S] int32;  positions [S] int32
+        k, v          [L, S, 8, 64] bf16;  q, out [L, S, 32, 64] bf16
+    """
+
+    def __init__(self, pool, block_tables, seq_lens, positions, k, v, q, out, rope_cos, rope_sin,
+                 scale, max_seq_len=None, workspace=None, d_err=None, q_rot=None, compute=None,
+                 use_graph=True, stream=None):
+        self.L, self.S = block_tables.shape[0], block_tables.shape[1]
+        self.t = dict(pool=pool, bt=block_tables, lens=seq_lens, pos=positions, k=k, v=v, q=q,
+                      out=out, cos=rope_cos, sin=rope_sin)
+        dev = pool.device
+        self.q_rot = torch.empty_like(q) if q_rot is None else q_rot
+        self.workspace = alloc_workspace(self.S, dev) if workspace is None else workspace
+        self.d_err = torch.zeros(1, dtype=torch.int32, device=dev) if d_err is None else d_err
+        self.scale = float(scale)
+        self.max_seq_len = max_seq_len
+        self.compute = compute
+        self.launches_per_step = 2 * self.L
+        self._launch()                      # eager run: sets up kernels and descriptors
+        torch.cuda.synchronize(dev)
+        self.graph = None
+        if use_graph:
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph, stream=stream):
+                self._launch()
+
+    def _launch(self, decode_only=False):
+        t = self.t
+        for l in range(self.L):
+            if not decode_only:
+                kv_append_rope(t["k"][l], t["v"][l], t["pos"], t["bt"][l], t["pool"], t["cos"],
+                               t["sin"], q_in=t["q"][l], q_out=self.q_rot[l], d_err=self.d_err)
+            paged_gqa_decode(self.q_rot[l], t["pool"], t["bt"][l], t["lens"], t["out"][l],
+                             self.scale, workspace=self.workspace, max_seq_len=self.max_seq_len,
+                             d_err=self.d_err, compute=self.compute)
+
+    def run(self):
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self._launch()
+
+    def decode_only_graph(self):
+        """A graph of just the L decode calls (for timing the decode kernel)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self._launch(decode_only=True)
+        return g
+
+    def error(self) -> int:
+        """Synchronise and return (and clear) the device error word."""
+        return pkv_read_device_error(self.d_err)

@@ -1,6 +1,7 @@
-// Paged GQA decode attention for sm_103a: a balanced split phase that streams
-// each (sequence, KV head, page) unit through TMA into shared memory, and a
-// log-sum-exp combine.
+// Paged GQA decode attention for sm_103a: one kernel that streams each
+// (sequence, KV head, page) unit through TMA into shared memory, splits the
+// work evenly over all warps of the GPU, and merges split segments with a
+// log-sum-exp combine done by the last warp to finish each segment.
 //
 // Source of the computation: samir-vllm article, section "Gestion de la KV
 // cache et strategies de batching" (paged attention reads only the current
@@ -23,10 +24,12 @@
 //     m16n8k16 with fp32 accumulation (heads padded 4 -> 16 rows), or, in the
 //     comparison variant, as fp32 FMA on the CUDA cores.  Online softmax in
 //     base 2 with the scale folded in.
-//   * A warp writes one partial (o[4][64], m[4], l[4]) per segment (s, g) it
-//     touches, at index 8*s + g + w, which is unique because both terms grow
-//     along the unit order.  The combine kernel merges the partials of each
-//     segment and writes bf16.
+//   * A segment (s, g) that one warp covers alone is normalised and stored as
+//     bf16 by that warp.  Otherwise each warp writes a partial (o[4][64],
+//     m[4], l[4]) at index 8*s + g + w (unique: both terms grow along the unit
+//     order), counts itself in with an atomic, and the warp that arrives last
+//     merges the partials with a log-sum-exp combine and resets the counter,
+//     so the whole decode is one kernel with no inter-CTA waiting.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -58,7 +61,7 @@ struct DecodeParams {
   int bt_stride, max_blocks, num_pages, num_seqs;
   float sl2;                      // scale * log2(e)
   int* d_err;
-  int32_t* ws_prefix;             // [S + 1] page prefix, written by CTA 0
+  uint32_t* ws_cnt;               // [8 S] arrivals per segment; zero between calls
   float2* ws_ml;                  // [npart][4] (m, l); l < 0 marks a bad segment
   float* ws_o;                    // [npart][4][64]
 };
@@ -120,9 +123,12 @@ __device__ __forceinline__ int seq_pages(int n, int max_blocks, bool* bad) {
   return (n + PKV_PAGE_TOKENS - 1) / PKV_PAGE_TOKENS;
 }
 
-// Block-wide exclusive prefix of pages over all sequences into prefix[0..S].
-__device__ void build_prefix(const DecodeParams& p, int32_t* prefix) {
+// Block-wide exclusive prefix of pages over all sequences into prefix[0..S];
+// returns the number of sequences without pages (empty or invalid length).
+__device__ int build_prefix(const DecodeParams& p, int32_t* prefix) {
   __shared__ int warp_tot[kWarps];
+  __shared__ int n_empty;
+  if (threadIdx.x == 0) n_empty = 0;
   const int S = p.num_seqs;
   const int nthr = kWarps * 32;
   const int per = (S + nthr - 1) / nthr;
@@ -143,12 +149,23 @@ __device__ void build_prefix(const DecodeParams& p, int32_t* prefix) {
   int base = 0;
   for (int w = 0; w < warp; ++w) base += warp_tot[w];
   int run = base + incl - sum;
+  int empties = 0;
   for (int s = lo; s < hi; ++s) {
     prefix[s] = run;
-    run += seq_pages(__ldg(p.seq_lens + s), p.max_blocks, &bad);
+    const int np = seq_pages(__ldg(p.seq_lens + s), p.max_blocks, &bad);
+    empties += (np == 0);
+    run += np;
   }
   if (threadIdx.x == nthr - 1) prefix[S] = run;
+  if (empties) atomicAdd(&n_empty, empties);
   __syncthreads();
+  return n_empty;
+}
+
+// Warp owning unit u when U units are cut into NW ranges [w*U/NW, (w+1)*U/NW):
+// the largest w with floor(w*U/NW) <= u.
+__device__ __forceinline__ uint32_t warp_of(uint32_t u, uint32_t U, uint32_t NW) {
+  return (uint32_t)((((uint64_t)u + 1) * NW - 1) / U);
 }
 
 // ---------------------------------------------------------------------------
@@ -259,6 +276,26 @@ struct MmaState {
       if (tig == 0) p.ws_ml[(size_t)pidx * 4 + gq] = make_float2(m, bad ? -1.f : lt);
     }
   }
+
+  // A segment that one warp covers alone: normalise and store bf16 directly.
+  __device__ __forceinline__ void write_output(const DecodeParams& p, int s, int g, bool bad,
+                                               int lane) {
+    const int gq = lane >> 2, tig = lane & 3;
+    float lt = l;
+    lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+    if (gq < 4) {
+      const bool ok = !bad && lt > 0.f;
+      uint32_t* dst =
+          reinterpret_cast<uint32_t*>(p.out + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + gq) * 64) + tig;
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        const float lo = ok ? __fdiv_rn(o[n][0], lt) : 0.f;
+        const float hi = ok ? __fdiv_rn(o[n][1], lt) : 0.f;
+        dst[4 * n] = pack_bf16x2(lo, hi);
+      }
+    }
+  }
 };
 
 // ---------------------------------------------------------------------------
@@ -361,33 +398,146 @@ struct FmaState {
     }
   }
 
+  // Sum o and l over the 8 token lanes (t8) that share a dim quarter.
+  __device__ __forceinline__ void reduce_tokens(float (&lt)[4]) {
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) {
+      float v = l[hh];
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 16);
+      lt[hh] = v;
+#pragma unroll
+      for (int d = 0; d < 16; ++d) {
+        float x = o[hh][d];
+        x += __shfl_xor_sync(0xffffffffu, x, 4);
+        x += __shfl_xor_sync(0xffffffffu, x, 8);
+        x += __shfl_xor_sync(0xffffffffu, x, 16);
+        o[hh][d] = x;
+      }
+    }
+  }
+
   __device__ __forceinline__ void write_partial(const DecodeParams& p, uint32_t pidx, bool bad,
                                                 int lane) {
     const int t8 = lane >> 2, qd = lane & 3;
+    float lt[4];
+    reduce_tokens(lt);
+    if (t8 == 0) {
 #pragma unroll
-    for (int hh = 0; hh < 4; ++hh) {
-      float lt = l[hh];
-      lt += __shfl_xor_sync(0xffffffffu, lt, 4);
-      lt += __shfl_xor_sync(0xffffffffu, lt, 8);
-      lt += __shfl_xor_sync(0xffffffffu, lt, 16);
-#pragma unroll
-      for (int d = 0; d < 16; ++d) {
-        float v = o[hh][d];
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        v += __shfl_xor_sync(0xffffffffu, v, 8);
-        v += __shfl_xor_sync(0xffffffffu, v, 16);
-        o[hh][d] = v;
-      }
-      if (t8 == 0) {
+      for (int hh = 0; hh < 4; ++hh) {
         float4* dst = reinterpret_cast<float4*>(p.ws_o + ((size_t)pidx * 4 + hh) * 64 + 16 * qd);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           dst[i] = make_float4(o[hh][4 * i], o[hh][4 * i + 1], o[hh][4 * i + 2], o[hh][4 * i + 3]);
-        if (qd == 0) p.ws_ml[(size_t)pidx * 4 + hh] = make_float2(m[hh], bad ? -1.f : lt);
+        if (qd == 0) p.ws_ml[(size_t)pidx * 4 + hh] = make_float2(m[hh], bad ? -1.f : lt[hh]);
+      }
+    }
+  }
+
+  __device__ __forceinline__ void write_output(const DecodeParams& p, int s, int g, bool bad,
+                                               int lane) {
+    const int t8 = lane >> 2, qd = lane & 3;
+    float lt[4];
+    reduce_tokens(lt);
+    if (t8 == 0) {
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) {
+        const bool ok = !bad && lt[hh] > 0.f;
+        uint32_t* dst = reinterpret_cast<uint32_t*>(
+                            p.out + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + hh) * 64 + 16 * qd);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float lo = ok ? __fdiv_rn(o[hh][2 * i], lt[hh]) : 0.f;
+          const float hi = ok ? __fdiv_rn(o[hh][2 * i + 1], lt[hh]) : 0.f;
+          dst[i] = pack_bf16x2(lo, hi);
+        }
       }
     }
   }
 };
+
+// ---------------------------------------------------------------------------
+// Merge the P partials of segment (s, g) and store bf16, run by the warp that
+// arrives last.  Partial k was written by warp w0 + k when every warp owns
+// units (U >= NW), else by the owner of unit base + k (one unit per warp).
+//   M = max_k m_k,   o = sum_k e^(m_k - M) o_k / sum_k e^(m_k - M) l_k.
+// Lane (hh = lane/8, dims 8*(lane%8)..+8) produces 8 outputs; partial loads
+// are independent across k, so they overlap.
+// ---------------------------------------------------------------------------
+__device__ __noinline__ void combine_segment(const DecodeParams& p, int s, int g, uint32_t base,
+                                             uint32_t w0, uint32_t P, bool dense, uint32_t U,
+                                             uint32_t NW, int lane) {
+  const uint32_t sg = 8u * (uint32_t)s + (uint32_t)g;
+  const int hh = lane >> 3, d0 = (lane & 7) * 8;
+  float M[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  bool bad = false;
+  for (uint32_t k0 = 0; k0 < P; k0 += 32) {
+    const uint32_t k = k0 + lane;
+    if (k < P) {
+      const uint32_t wk = dense ? w0 + k : warp_of(base + k, U, NW);
+      const float4* ml = reinterpret_cast<const float4*>(p.ws_ml + (size_t)(sg + wk) * 4);
+      const float4 a = __ldcg(ml), b = __ldcg(ml + 1);  // (m0 l0 m1 l1) (m2 l2 m3 l3)
+      M[0] = fmaxf(M[0], a.x);
+      M[1] = fmaxf(M[1], a.z);
+      M[2] = fmaxf(M[2], b.x);
+      M[3] = fmaxf(M[3], b.z);
+      bad |= (a.y < 0.f) || (a.w < 0.f) || (b.y < 0.f) || (b.w < 0.f);
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < 4; ++h)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M[h] = fmaxf(M[h], __shfl_xor_sync(0xffffffffu, M[h], o));
+  bad = __any_sync(0xffffffffu, bad);
+
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float Lp[4] = {0.f, 0.f, 0.f, 0.f};
+  if (!bad) {
+    for (uint32_t k0 = 0; k0 < P; k0 += 32) {
+      const uint32_t k = k0 + lane;
+      float wt[4] = {0.f, 0.f, 0.f, 0.f};
+      if (k < P) {
+        const uint32_t wk = dense ? w0 + k : warp_of(base + k, U, NW);
+        const float4* ml = reinterpret_cast<const float4*>(p.ws_ml + (size_t)(sg + wk) * 4);
+        const float4 a = __ldcg(ml), b = __ldcg(ml + 1);
+        const float mk[4] = {a.x, a.z, b.x, b.z}, lk[4] = {a.y, a.w, b.y, b.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          wt[h] = (mk[h] == M[h]) ? 1.f : exp2f(mk[h] - M[h]);
+          Lp[h] += wt[h] * lk[h];
+        }
+      }
+      const uint32_t n = min(32u, P - k0);
+#pragma unroll 4
+      for (uint32_t i = 0; i < n; ++i) {
+        const float x0 = __shfl_sync(0xffffffffu, wt[0], i);
+        const float x1 = __shfl_sync(0xffffffffu, wt[1], i);
+        const float x2 = __shfl_sync(0xffffffffu, wt[2], i);
+        const float x3 = __shfl_sync(0xffffffffu, wt[3], i);
+        const float wi = hh == 0 ? x0 : hh == 1 ? x1 : hh == 2 ? x2 : x3;
+        const uint32_t wk = dense ? w0 + k0 + i : warp_of(base + k0 + i, U, NW);
+        const float4* src =
+            reinterpret_cast<const float4*>(p.ws_o + ((size_t)(sg + wk) * 4 + hh) * 64 + d0);
+        const float4 o0 = __ldcg(src), o1 = __ldcg(src + 1);
+        acc[0] += wi * o0.x; acc[1] += wi * o0.y; acc[2] += wi * o0.z; acc[3] += wi * o0.w;
+        acc[4] += wi * o1.x; acc[5] += wi * o1.y; acc[6] += wi * o1.z; acc[7] += wi * o1.w;
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < 4; ++h)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Lp[h] += __shfl_xor_sync(0xffffffffu, Lp[h], o);
+  const float L = hh == 0 ? Lp[0] : hh == 1 ? Lp[1] : hh == 2 ? Lp[2] : Lp[3];
+  const bool ok = !bad && L > 0.f;
+  uint32_t packed[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    packed[i] = pack_bf16x2(ok ? __fdiv_rn(acc[2 * i], L) : 0.f, ok ? __fdiv_rn(acc[2 * i + 1], L) : 0.f);
+  uint16_t* dst = p.out + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + hh) * 64 + d0;
+  *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+}
 
 // ---------------------------------------------------------------------------
 // Split phase.
@@ -404,13 +554,20 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int S = p.num_seqs;
 
   pdl_wait();
-  build_prefix(p, prefix);
-  if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i <= S; i += blockDim.x) p.ws_prefix[i] = prefix[i];
+  const int n_empty = build_prefix(p, prefix);
   pdl_launch_dependents();
+  const uint32_t NW = gridDim.x * kWarps;
+  if (n_empty > 0) {
+    // Sequences without pages get a zero output (16-byte stores, grid-strided).
+    const uint32_t total = (uint32_t)S * (PKV_NUM_Q_HEADS * 64 / 8);
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += NW * 32) {
+      const int s = (int)(i / (PKV_NUM_Q_HEADS * 64 / 8));
+      if (prefix[s + 1] == prefix[s])
+        reinterpret_cast<uint4*>(p.out)[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
 
   const uint32_t U = 8u * (uint32_t)prefix[S];
-  const uint32_t NW = gridDim.x * kWarps;
   const uint32_t w = blockIdx.x * kWarps + warp;
   const uint32_t u0 = (uint32_t)(((uint64_t)w * U) / NW);
   const uint32_t u1 = (uint32_t)(((uint64_t)(w + 1) * U) / NW);
@@ -497,7 +654,27 @@ __global__ void __launch_bounds__(kWarps * 32)
     if (!timed_out && iv < n_units) issue(stage);
     const bool seg_end = (cc.j == cc.np - 1) || (uc == n_units - 1);
     if (seg_end) {
-      st.write_partial(p, (uint32_t)(8 * cc.s + cc.g) + w, seg_bad, lane);
+      const uint32_t np = (uint32_t)cc.np;
+      const uint32_t base = 8u * (uint32_t)prefix[cc.s] + (uint32_t)cc.g * np;
+      const uint32_t w0 = warp_of(base, U, NW);
+      const bool dense = U >= NW;
+      const uint32_t nparts = dense ? warp_of(base + np - 1, U, NW) - w0 + 1 : np;
+      if (nparts == 1) {
+        st.write_output(p, cc.s, cc.g, seg_bad, lane);
+      } else {
+        const uint32_t sg = 8u * (uint32_t)cc.s + (uint32_t)cc.g;
+        st.write_partial(p, sg + w, seg_bad, lane);
+        __threadfence();
+        __syncwarp();
+        uint32_t old = 0;
+        if (lane == 0) old = atomicAdd(p.ws_cnt + sg, 1u);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old == nparts - 1) {  // every other partial of this segment is visible
+          __threadfence();
+          combine_segment(p, cc.s, cc.g, base, w0, nparts, dense, U, NW, lane);
+          if (lane == 0) p.ws_cnt[sg] = 0u;  // ready for the next call
+        }
+      }
       st.reset();
       seg_bad = false;
     }
@@ -515,63 +692,6 @@ __global__ void __launch_bounds__(kWarps * 32)
       (void)mbar_wait_bounded(bars + 8 * stage, (uint32_t)(u / kStages) & 1u, kWaitLimitNs);
     }
   }
-}
-
-// ---------------------------------------------------------------------------
-// Combine: one CTA per sequence, one warp per KV head.  Lane (hh = lane/8,
-// 8 dims at 8*(lane%8)) merges the partials of segment (s, g) with
-//   M = max m_r, o = sum e^(m_r - M) o_r / sum e^(m_r - M) l_r.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) paged_decode_combine_kernel(const DecodeParams p, int nw) {
-  pdl_wait();
-  const int s = blockIdx.x, g = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hh = lane >> 3, d0 = (lane & 7) * 8;
-  uint16_t* dst = p.out + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + hh) * 64 + d0;
-  const uint32_t P0 = (uint32_t)p.ws_prefix[s], P1 = (uint32_t)p.ws_prefix[s + 1];
-  const uint32_t U = 8u * (uint32_t)p.ws_prefix[p.num_seqs];
-  const uint32_t np = P1 - P0;
-  float acc[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  float M = -INFINITY, L = 0.f;
-  bool bad = (np == 0);
-  if (np > 0) {
-    const uint32_t base = 8u * P0 + (uint32_t)g * np, last = base + np - 1;
-    const uint32_t w0 = (uint32_t)((((uint64_t)base + 1) * nw - 1) / U);
-    const uint32_t w1 = (uint32_t)((((uint64_t)last + 1) * nw - 1) / U);
-    const uint32_t sg = 8u * s + g;
-    for (uint32_t w = w0; w <= w1; ++w) {
-      const uint64_t st0 = ((uint64_t)w * U) / nw, st1 = ((uint64_t)(w + 1) * U) / nw;
-      if (st0 == st1) continue;  // this warp had no units and wrote nothing
-      const size_t r = sg + w;
-      const float2 ml = p.ws_ml[r * 4 + hh];
-      if (ml.y < 0.f) {
-        bad = true;
-        continue;
-      }
-      const float Mn = fmaxf(M, ml.x);
-      const float a = (M == Mn) ? 1.f : exp2f(M - Mn);
-      const float b = (ml.x == Mn) ? 1.f : exp2f(ml.x - Mn);
-      const float4* src = reinterpret_cast<const float4*>(p.ws_o + (r * 4 + hh) * 64 + d0);
-      const float4 o0 = src[0], o1 = src[1];
-      const float ov[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = acc[i] * a + b * ov[i];
-      L = L * a + b * ml.y;
-      M = Mn;
-    }
-  }
-  uint32_t packed[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float lo = 0.f, hi = 0.f;
-    if (!bad && L > 0.f) {
-      lo = __fdiv_rn(acc[2 * i], L);
-      hi = __fdiv_rn(acc[2 * i + 1], L);
-    }
-    packed[i] = pack_bf16x2(lo, hi);
-  }
-  *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
 }
 
 // ---------------------------------------------------------------------------
@@ -637,17 +757,19 @@ static int make_pool_map(CUtensorMap* map, const void* pool, int num_pages) {
 }
 
 struct WorkspaceLayout {
-  size_t prefix, ml, o, total;
+  size_t cnt, ml, o, total;
   int npart;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// [cnt: u32 x 8S][ml: float2 x 4 x npart][o: float x 256 x npart], npart =
+// 8S + the most warps a launch can use (partial index 8s + g + warp).
 static WorkspaceLayout workspace_layout(int num_seqs, int num_sms) {
   WorkspaceLayout w;
   w.npart = 8 * num_seqs + num_sms * kMaxCtasPerSm * kWarps;
-  w.prefix = 0;
-  w.ml = align256(4 * (size_t)(num_seqs + 1));
+  w.cnt = 0;
+  w.ml = align256(4 * (size_t)8 * num_seqs);
   w.o = w.ml + align256((size_t)w.npart * 4 * sizeof(float2));
   w.total = w.o + (size_t)w.npart * 4 * 64 * sizeof(float);
   return w;
@@ -723,13 +845,7 @@ static int launch_decode(const DecodeParams& prm, const CUtensorMap& map, int de
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_split_kernel<State>, map, prm);
-  if (e != cudaSuccess) return cuda_status(e, "cudaLaunchKernelEx(split)");
-
-  cfg.gridDim = dim3(prm.num_seqs);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  e = cudaLaunchKernelEx(&cfg, paged_decode_combine_kernel, prm, *nw_out);
-  return cuda_status(e, "cudaLaunchKernelEx(combine)");
+  return cuda_status(e, "cudaLaunchKernelEx(split)");
 }
 
 }  // namespace pkv
@@ -795,7 +911,7 @@ extern "C" int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_p
   prm.sl2 = scale * kLog2e;
   prm.d_err = d_err;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  prm.ws_prefix = reinterpret_cast<int32_t*>(ws + wl.prefix);
+  prm.ws_cnt = reinterpret_cast<uint32_t*>(ws + wl.cnt);
   prm.ws_ml = reinterpret_cast<float2*>(ws + wl.ml);
   prm.ws_o = reinterpret_cast<float*>(ws + wl.o);
 

@@ -309,3 +309,56 @@ def test_full_size_stress256_sampled(lib, cuda_device, tables):
     samples = [(0, 0), (3, 200), (9, 77), (15, 255)]
     full_size_step_check(lib, cuda_device, case, samples, tables)
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------- step graph, fused --
+
+def test_workspace_counters_return_to_zero(lib, cuda_device):
+    """Segments split across warps are merged by the last warp, which resets its counter."""
+    case = make_case([700, 1, 1500, 33, 2048], seed=31, extra_pages=3)
+    pool = W.bf16_bits(W.fill_pool(case))
+    q = W.bf16_bits(W.fill_queries(case))[0]
+    bt = case.block_tables[0]
+    ws = lib.alloc_workspace(case.num_seqs, cuda_device)
+    ref, _ = OP.decode(q, pool, bt, case.seq_lens, case.scale)
+    for mu in (1, 3, 1000):          # many splits, some, none
+        out, code = run_decode(lib, cuda_device, q, pool, bt, case.seq_lens, workspace=ws,
+                               min_units_per_warp=mu)
+        assert code == 0
+        check_close(bf16_to_f64(out), ref, f"min_units_per_warp={mu}")
+        cnt = ws[:8 * case.num_seqs * 4].view(torch.int32)
+        assert int(cnt.abs().sum()) == 0
+
+
+def test_decode_step_graph_matches_eager_and_oracle(lib, cuda_device, tables):
+    cos_d, sin_d, cos_o, sin_o = tables
+    case = W.case_uniform(6, batch=4, layers=3, ctx=300, name="step_small")
+    case.seq_lens[:] = [300, 17, 129, 256]
+    dev = cuda_device
+    pool0 = W.fill_pool(case, device=dev)
+    q = W.fill_queries(case, device=dev)
+    k, v = W.fill_new_kv(case, device=dev)
+    pos = torch.from_numpy(W.new_positions(case)).to(dev)
+    bt = torch.from_numpy(case.block_tables).to(dev)
+    lens = torch.from_numpy(case.seq_lens).to(dev)
+    outs = []
+    for use_graph in (False, True):
+        pool = pool0.clone()
+        out = torch.empty_like(q)
+        step = lib.DecodeStep(pool, bt, lens, pos, k, v, q, out, cos_d, sin_d, case.scale,
+                              max_seq_len=300, use_graph=use_graph)
+        step.run()
+        assert step.error() == 0
+        outs.append((bits(out), bits(pool), bits(step.q_rot)))
+    assert all(np.array_equal(a, b) for a, b in zip(outs[0], outs[1]))
+    out_b, pool_b, qrot_b = outs[1]
+    pool_in = bits(pool0)
+    for l in range(case.num_layers):
+        want_pool, want_q, e = OP.append_rope(pool_in, bits(k[l]), bits(v[l]), W.new_positions(case),
+                                              None, case.block_tables[l], cos_o, sin_o, bits(q[l]))
+        assert not e
+        pool_in = want_pool
+        assert np.array_equal(qrot_b[l], want_q)
+        ref, _ = OP.decode(want_q, want_pool, case.block_tables[l], case.seq_lens, case.scale)
+        check_close(OB.to_f64(out_b[l]), ref, f"step layer {l}")
+    assert np.array_equal(pool_b, pool_in)
