@@ -39,7 +39,11 @@
  *     Model", section "Mutable state and thread-safety implications").
  *     The scheduler object (pkv_sched_*) is not thread-safe.
  *   - Device selection: a call runs on the device that owns `stream`
- *     (the current device for the default stream).
+ *     (the current device for the default stream).  While `stream` is being
+ *     captured into a CUDA graph the stream cannot be queried, so the device
+ *     made current by the last uncaptured call on this thread is used: run
+ *     each call once before capturing it (which also does the one-time
+ *     kernel set-up outside the capture).
  */
 #ifndef PKV_H
 #define PKV_H

@@ -24,7 +24,12 @@ void set_last_error(const char* where, const char* what) {
 int bind_stream_device(void* stream, int* device_out) {
   int dev = 0;
   cudaError_t e;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (stream != nullptr) {
+    e = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cap);
+    if (e != cudaSuccess) return cuda_status(e, "cudaStreamIsCapturing");
+  }
+  if (stream != nullptr && cap == cudaStreamCaptureStatusNone) {
     e = cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &dev);
     if (e != cudaSuccess) return cuda_status(e, "cudaStreamGetDevice");
     int cur = -1;
