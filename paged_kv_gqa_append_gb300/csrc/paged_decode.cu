@@ -45,7 +45,7 @@
 namespace pkv {
 
 constexpr int kWarps = 4;            // warps per CTA
-constexpr int kStages = 4;           // units in flight per warp
+constexpr int kDefaultStages = 4;    // units in flight per warp (template kSt)
 constexpr int kTileBytes = 2048;     // 16 tokens x 64 dims bf16
 constexpr int kStageBytes = 2 * kTileBytes;
 constexpr int kMaxCtasPerSm = 4;     // workspace is sized for this many
@@ -66,6 +66,7 @@ struct DecodeParams {
   float* ws_o;                    // [npart][4][64]
 };
 
+template <int kStages>
 struct SmemLayout {
   static constexpr int kTiles = kWarps * kStages * kStageBytes;
   static constexpr int kBars = kTiles;                                // uint64 [kWarps][kStages]
@@ -542,9 +543,10 @@ __device__ __noinline__ void combine_segment(const DecodeParams& p, int s, int g
 // ---------------------------------------------------------------------------
 // Split phase.
 // ---------------------------------------------------------------------------
-template <class State>
+template <class State, int kStages>
 __global__ void __launch_bounds__(kWarps * 32)
     paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
+  using SmemLayout = pkv::SmemLayout<kStages>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -775,7 +777,7 @@ static WorkspaceLayout workspace_layout(int num_seqs, int num_sms) {
   return w;
 }
 
-template <class State>
+template <class State, int kStages>
 static int setup_split_kernel(int device, size_t smem, int* occ) {
   static std::mutex mu;
   static int configured[64] = {0};
@@ -783,7 +785,7 @@ static int setup_split_kernel(int device, size_t smem, int* occ) {
   static size_t cached_smem[64] = {0};
   static int max_dyn_smem[64] = {0};
   std::lock_guard<std::mutex> lock(mu);
-  auto kern = paged_decode_split_kernel<State>;
+  auto kern = paged_decode_split_kernel<State, kStages>;
   if (device < 0 || device >= 64) {
     set_last_error("setup_split_kernel", "device index out of range");
     return PKV_ERR_CUDA;
@@ -814,13 +816,13 @@ static int setup_split_kernel(int device, size_t smem, int* occ) {
   return PKV_OK;
 }
 
-template <class State>
+template <class State, int kStages>
 static int launch_decode(const DecodeParams& prm, const CUtensorMap& map, int device, int num_sms,
                          int max_seq_len, int min_units, int ctas_per_sm, cudaStream_t stream,
                          int* nw_out) {
-  const size_t smem = SmemLayout::bytes(prm.num_seqs);
+  const size_t smem = SmemLayout<kStages>::bytes(prm.num_seqs);
   int occ = 0;
-  int rc = setup_split_kernel<State>(device, smem, &occ);
+  int rc = setup_split_kernel<State, kStages>(device, smem, &occ);
   if (rc != PKV_OK) return rc;
   if (occ < 1) return PKV_ERR_UNSUPPORTED_SHAPE;
   occ = min(occ, kMaxCtasPerSm);
@@ -844,7 +846,7 @@ static int launch_decode(const DecodeParams& prm, const CUtensorMap& map, int de
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_split_kernel<State>, map, prm);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_split_kernel<State, kStages>, map, prm);
   return cuda_status(e, "cudaLaunchKernelEx(split)");
 }
 
@@ -885,6 +887,8 @@ extern "C" int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_p
   const int compute = opts ? opts->compute : PKV_COMPUTE_TENSOR;
   const int min_units = (opts && opts->min_units_per_warp > 0) ? opts->min_units_per_warp : 2;
   const int ctas_per_sm = opts ? opts->ctas_per_sm : 0;
+  const int stages = (opts && opts->stages > 0) ? opts->stages : kDefaultStages;
+  if (stages != 2 && stages != 4 && stages != 8) return PKV_ERR_INVALID_ARGUMENT;
   if (compute != PKV_COMPUTE_TENSOR && compute != PKV_COMPUTE_FMA) return PKV_ERR_INVALID_ARGUMENT;
 
   int dev = 0;
@@ -917,9 +921,14 @@ extern "C" int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_p
 
   int nw = 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (compute == PKV_COMPUTE_TENSOR)
-    return launch_decode<MmaState>(prm, map, dev, sms, max_seq_len, min_units, ctas_per_sm, st, &nw);
-  return launch_decode<FmaState>(prm, map, dev, sms, max_seq_len, min_units, ctas_per_sm, st, &nw);
+  if (compute == PKV_COMPUTE_FMA)
+    return launch_decode<FmaState, 4>(prm, map, dev, sms, max_seq_len, min_units, ctas_per_sm, st,
+                                      &nw);
+  switch (stages) {
+    case 2: return launch_decode<MmaState, 2>(prm, map, dev, sms, max_seq_len, min_units, ctas_per_sm, st, &nw);
+    case 8: return launch_decode<MmaState, 8>(prm, map, dev, sms, max_seq_len, min_units, ctas_per_sm, st, &nw);
+    default: return launch_decode<MmaState, 4>(prm, map, dev, sms, max_seq_len, min_units, ctas_per_sm, st, &nw);
+  }
 }
 
 extern "C" int paged_gqa_decode(const void* q, const void* kv_pool, int num_pages,
