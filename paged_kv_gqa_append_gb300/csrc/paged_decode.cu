@@ -48,7 +48,7 @@ constexpr int kWarps = 4;            // warps per CTA
 constexpr int kDefaultStages = 4;    // units in flight per warp (template kSt)
 constexpr int kTileBytes = 2048;     // 16 tokens x 64 dims bf16
 constexpr int kStageBytes = 2 * kTileBytes;
-constexpr int kMaxCtasPerSm = 4;     // workspace is sized for this many
+constexpr int kMaxCtasPerSm = 6;     // workspace is sized for this many
 constexpr int kMaxSeqs = 4096;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per stage wait
 constexpr float kLog2e = 1.4426950408889634f;
@@ -178,6 +178,7 @@ __device__ __forceinline__ uint32_t warp_of(uint32_t u, uint32_t U, uint32_t NW)
 // probabilities never leave registers.
 // ---------------------------------------------------------------------------
 struct MmaState {
+  static constexpr int kMinBlocks = 4;  // <= 128 registers: four CTAs per SM
   uint32_t qa[4][2];  // Q A-fragments per 16-dim chunk: (row gq, k 2tig..) and (k 8+2tig..)
   float o[8][4];      // O accumulators per 8-dim tile
   float m, l;         // running max (log2 units) and per-lane partial denominator
@@ -306,6 +307,7 @@ struct MmaState {
 // output accumulates per lane and is reduced over t8 once per segment.
 // ---------------------------------------------------------------------------
 struct FmaState {
+  static constexpr int kMinBlocks = 1;
   float qf[4][16];
   float o[4][16];
   float m[4], l[4];
@@ -544,7 +546,7 @@ __device__ __noinline__ void combine_segment(const DecodeParams& p, int s, int g
 // Split phase.
 // ---------------------------------------------------------------------------
 template <class State, int kStages>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, State::kMinBlocks)
     paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
   using SmemLayout = pkv::SmemLayout<kStages>;
   extern __shared__ uint8_t smem_raw[];
@@ -888,7 +890,7 @@ extern "C" int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_p
   const int min_units = (opts && opts->min_units_per_warp > 0) ? opts->min_units_per_warp : 2;
   const int ctas_per_sm = opts ? opts->ctas_per_sm : 0;
   const int stages = (opts && opts->stages > 0) ? opts->stages : kDefaultStages;
-  if (stages != 2 && stages != 4 && stages != 8) return PKV_ERR_INVALID_ARGUMENT;
+  if (stages != 2 && stages != 3 && stages != 4 && stages != 8) return PKV_ERR_INVALID_ARGUMENT;
   if (compute != PKV_COMPUTE_TENSOR && compute != PKV_COMPUTE_FMA) return PKV_ERR_INVALID_ARGUMENT;
 
   int dev = 0;
@@ -926,6 +928,7 @@ extern "C" int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_p
                                       &nw);
   switch (stages) {
     case 2: return launch_decode<MmaState, 2>(prm, map, dev, sms, max_seq_len, min_units, ctas_per_sm, st, &nw);
+    case 3: return launch_decode<MmaState, 3>(prm, map, dev, sms, max_seq_len, min_units, ctas_per_sm, st, &nw);
     case 8: return launch_decode<MmaState, 8>(prm, map, dev, sms, max_seq_len, min_units, ctas_per_sm, st, &nw);
     default: return launch_decode<MmaState, 4>(prm, map, dev, sms, max_seq_len, min_units, ctas_per_sm, st, &nw);
   }
