@@ -195,9 +195,10 @@ typedef enum pkv_compute {
 
 typedef struct pkv_decode_opts {
   int compute;            /* pkv_compute                                             */
-  int min_units_per_warp; /* 0 = default (2): fewer warps for small batches          */
-  int ctas_per_sm;        /* 0 = as many as fit (at most 6)                          */
-  int stages;             /* pages in flight per warp: 0 = default, or 2, 3, 4, 8    */
+  int min_units_per_warp; /* 0 = default (2): fewer CTAs for small batches           */
+  int ctas_per_sm;        /* 0 = as many as fit (at most 8)                          */
+  int stages;             /* pages in flight per warp: 0 = default (2), 2 or 4       */
+  int warps_per_cta;      /* 0 = default (16); 16 (2 stages), 8 or 4                 */
 } pkv_decode_opts;
 
 /* paged_gqa_decode with explicit options; same contract otherwise. */

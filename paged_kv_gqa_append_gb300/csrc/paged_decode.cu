@@ -1,7 +1,4 @@
-// Paged GQA decode attention for sm_103a: one kernel that streams each
-// (sequence, KV head, page) unit through TMA into shared memory, splits the
-// work evenly over all warps of the GPU, and merges split segments with a
-// log-sum-exp combine done by the last warp to finish each segment.
+// Paged GQA decode attention for sm_103a, one kernel per call.
 //
 // Source of the computation: samir-vllm article, section "Gestion de la KV
 // cache et strategies de batching" (paged attention reads only the current
@@ -12,24 +9,26 @@
 // Work decomposition (GB300-specific, not from the pages):
 //   * A unit is one (sequence s, KV head g, logical page j): 2 KiB of K plus
 //     2 KiB of V, contiguous in the head-major page layout.  Units are ordered
-//     (s, g, j); the U = 8 * sum_s ceil(len_s / 16) units are cut into NW equal
-//     contiguous ranges, one per warp: warp w owns [w*U/NW, (w+1)*U/NW).  Every
-//     CTA rebuilds the per-sequence page prefix from seq_lens in shared memory,
-//     so no host synchronisation is needed for variable lengths.
-//   * Each warp is an independent pipeline: lane 0 issues TMA loads of K and V
-//     tiles (128-byte swizzle) for up to kStages units ahead, one mbarrier per
-//     stage; the warp consumes them in order.
-//   * Per unit, the 4 query heads of the group share the page: scores
+//     (s, g, j); a segment is the run of units of one (s, g).  Every CTA
+//     rebuilds the per-sequence page prefix from seq_lens in shared memory (no
+//     host synchronisation for variable lengths), takes the contiguous unit
+//     range [c*U/NC, (c+1)*U/NC) and cuts it into kWarps contiguous warp
+//     ranges, so the load is even for any length mix.
+//   * Each warp is an independent pipeline: lane 0 issues TMA loads of the K
+//     and V tiles (128-byte swizzle) kStages units ahead, one mbarrier per
+//     stage.  Per unit the 4 query heads of the group share the page: scores
 //     S = Q K^T and O += P V run on the tensor cores as bf16 mma.sync
 //     m16n8k16 with fp32 accumulation (heads padded 4 -> 16 rows), or, in the
-//     comparison variant, as fp32 FMA on the CUDA cores.  Online softmax in
-//     base 2 with the scale folded in.
-//   * A segment (s, g) that one warp covers alone is normalised and stored as
-//     bf16 by that warp.  Otherwise each warp writes a partial (o[4][64],
-//     m[4], l[4]) at index 8*s + g + w (unique: both terms grow along the unit
-//     order), counts itself in with an atomic, and the warp that arrives last
-//     merges the partials with a log-sum-exp combine and resets the counter,
-//     so the whole decode is one kernel with no inter-CTA waiting.
+//     comparison variant, as fp32 FMA.  Online softmax in base 2, scale folded.
+//   * Segment ends: a segment inside one warp range is normalised and stored
+//     as bf16 by that warp.  Otherwise the warps deposit (o, m, l) records in
+//     shared memory and, after one CTA barrier, the first warp of the segment
+//     merges them.  A segment that lies inside the CTA range is then stored;
+//     one that crosses CTA ranges is written as a CTA partial at index
+//     8*s + g + c (unique: both terms grow along the unit order), counted in
+//     with an atomic, and the CTA that arrives last merges the partials with a
+//     log-sum-exp combine and resets the counter.  No CTA ever waits on
+//     another.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -44,11 +43,10 @@
 
 namespace pkv {
 
-constexpr int kWarps = 4;            // warps per CTA
-constexpr int kDefaultStages = 4;    // units in flight per warp (template kSt)
 constexpr int kTileBytes = 2048;     // 16 tokens x 64 dims bf16
 constexpr int kStageBytes = 2 * kTileBytes;
-constexpr int kMaxCtasPerSm = 6;     // workspace is sized for this many
+constexpr int kRecordBytes = 4 * 64 * 4 + 4 * 8;  // o[4][64] fp32 + (m, l)[4]
+constexpr int kMaxCtasPerSm = 8;     // workspace is sized for this many CTAs per SM
 constexpr int kMaxSeqs = 4096;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per stage wait
 constexpr float kLog2e = 1.4426950408889634f;
@@ -61,19 +59,35 @@ struct DecodeParams {
   int bt_stride, max_blocks, num_pages, num_seqs;
   float sl2;                      // scale * log2(e)
   int* d_err;
-  uint32_t* ws_cnt;               // [8 S] arrivals per segment; zero between calls
+  uint32_t* ws_cnt;               // [8 S] CTA arrivals per segment; zero between calls
   float2* ws_ml;                  // [npart][4] (m, l); l < 0 marks a bad segment
   float* ws_o;                    // [npart][4][64]
 };
 
-template <int kStages>
+// One (o, m, l) record: unnormalised o[4][64] and (m, l) for the 4 heads of a
+// KV group; l < 0 marks a segment that touched a bad page.
+struct Record {
+  float* o;
+  float2* ml;
+};
+
+template <int kWarps, int kStages>
 struct SmemLayout {
   static constexpr int kTiles = kWarps * kStages * kStageBytes;
-  static constexpr int kBars = kTiles;                                // uint64 [kWarps][kStages]
-  static constexpr int kPid = kBars + kWarps * kStages * 8;           // int [kWarps][kStages]
-  static constexpr int kPrefix = kPid + kWarps * kStages * 4;         // int [S + 1]
+  static constexpr int kBars = kTiles;                                 // u64 [kWarps][kStages]
+  static constexpr int kPid = kBars + kWarps * kStages * 8;            // int [kWarps][kStages]
+  static constexpr int kSlots = kPid + kWarps * kStages * 4;           // Record [kWarps][2]
+  static constexpr int kPrefix = kSlots + kWarps * 2 * kRecordBytes;   // int [S + 1]
   static size_t bytes(int num_seqs) { return 1024 + kPrefix + 4 * (size_t)(num_seqs + 1); }
+  __device__ static Record slot(uint8_t* smem, int warp, int which) {
+    uint8_t* base = smem + kSlots + (warp * 2 + which) * kRecordBytes;
+    return Record{reinterpret_cast<float*>(base), reinterpret_cast<float2*>(base + 1024)};
+  }
 };
+
+__device__ __forceinline__ Record global_record(const struct DecodeParams& p, uint32_t idx) {
+  return Record{p.ws_o + (size_t)idx * 256, p.ws_ml + (size_t)idx * 4};
+}
 
 // ---------------------------------------------------------------------------
 // Unit cursor: walks (s, g, j) in unit order, skipping empty sequences.
@@ -104,6 +118,11 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const int32_t* prefix, in
   if (c.s < S) c.np = prefix[c.s + 1] - prefix[c.s];
 }
 
+// First unit of the segment that contains the cursor's unit.
+__device__ __forceinline__ uint32_t seg_base(const Cursor& c, const int32_t* prefix) {
+  return 8u * (uint32_t)prefix[c.s] + (uint32_t)c.g * (uint32_t)c.np;
+}
+
 // Page id of unit u (or -1 if the table entry is outside the pool, -2 if u is
 // past the end of this warp's range).
 __device__ __forceinline__ int unit_page(uint32_t u, uint32_t u_end, const int32_t* prefix,
@@ -115,7 +134,7 @@ __device__ __forceinline__ int unit_page(uint32_t u, uint32_t u_end, const int32
   return (pid >= 0 && pid < p.num_pages) ? pid : -1;
 }
 
-// Pages of sequence s, or 0 (and an error) for a length outside [0, 16*max_blocks].
+// Pages of a sequence, or 0 (and an error) for a length outside [0, 16*max_blocks].
 __device__ __forceinline__ int seq_pages(int n, int max_blocks, bool* bad) {
   if (n < 0 || n > PKV_PAGE_TOKENS * max_blocks) {
     *bad = true;
@@ -126,6 +145,7 @@ __device__ __forceinline__ int seq_pages(int n, int max_blocks, bool* bad) {
 
 // Block-wide exclusive prefix of pages over all sequences into prefix[0..S];
 // returns the number of sequences without pages (empty or invalid length).
+template <int kWarps>
 __device__ int build_prefix(const DecodeParams& p, int32_t* prefix) {
   __shared__ int warp_tot[kWarps];
   __shared__ int n_empty;
@@ -163,11 +183,83 @@ __device__ int build_prefix(const DecodeParams& p, int32_t* prefix) {
   return n_empty;
 }
 
-// Warp owning unit u when U units are cut into NW ranges [w*U/NW, (w+1)*U/NW):
-// the largest w with floor(w*U/NW) <= u.
-__device__ __forceinline__ uint32_t warp_of(uint32_t u, uint32_t U, uint32_t NW) {
-  return (uint32_t)((((uint64_t)u + 1) * NW - 1) / U);
+// Owner of unit u when U units are cut into N ranges [k*U/N, (k+1)*U/N): the
+// largest k with floor(k*U/N) <= u.
+__device__ __forceinline__ uint32_t owner_of(uint32_t u, uint32_t U, uint32_t N) {
+  return (uint32_t)((((uint64_t)u + 1) * N - 1) / U);
 }
+__device__ __forceinline__ uint32_t range_start(uint32_t k, uint32_t U, uint32_t N) {
+  return (uint32_t)(((uint64_t)k * U) / N);
+}
+
+// ---------------------------------------------------------------------------
+// Merging records.  Lane (hh = lane/8, dims d0 = 8*(lane%8) .. d0+8) keeps an
+// online log-sum-exp merge of the records it is given:
+//   M' = max(M, m_k);  acc = acc e^(M - M') + o_k e^(m_k - M');
+//   L = L e^(M - M') + l_k e^(m_k - M').
+// ---------------------------------------------------------------------------
+struct MergeAcc {
+  float acc[8];
+  float M, L;
+  bool bad;
+
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    M = -INFINITY;
+    L = 0.f;
+    bad = false;
+  }
+
+  __device__ __forceinline__ void add(float2 ml, float4 o0, float4 o1) {
+    if (ml.y < 0.f) {
+      bad = true;
+      return;
+    }
+    const float Mn = fmaxf(M, ml.x);
+    const float a = (M == Mn) ? 1.f : exp2f(M - Mn);
+    const float b = (ml.x == Mn) ? 1.f : exp2f(ml.x - Mn);
+    const float ov[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = acc[i] * a + b * ov[i];
+    L = L * a + b * ml.y;
+    M = Mn;
+  }
+
+  // record in shared memory
+  __device__ __forceinline__ void add_shared(const Record& r, int lane) {
+    const int hh = lane >> 3, d0 = (lane & 7) * 8;
+    const float4* src = reinterpret_cast<const float4*>(r.o + hh * 64 + d0);
+    add(r.ml[hh], src[0], src[1]);
+  }
+
+  // record in global memory written by another CTA: read through L2 only
+  __device__ __forceinline__ void add_global(const Record& r, int lane) {
+    const int hh = lane >> 3, d0 = (lane & 7) * 8;
+    const float4* src = reinterpret_cast<const float4*>(r.o + hh * 64 + d0);
+    add(__ldcg(r.ml + hh), __ldcg(src), __ldcg(src + 1));
+  }
+
+  __device__ __forceinline__ void store_record(const Record& r, int lane) const {
+    const int hh = lane >> 3, d0 = (lane & 7) * 8;
+    float4* dst = reinterpret_cast<float4*>(r.o + hh * 64 + d0);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if ((lane & 7) == 0) r.ml[hh] = make_float2(M, bad ? -1.f : L);
+  }
+
+  __device__ __forceinline__ void store_output(const DecodeParams& p, int s, int g, int lane) const {
+    const int hh = lane >> 3, d0 = (lane & 7) * 8;
+    const bool ok = !bad && L > 0.f;
+    uint32_t packed[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      packed[i] = pack_bf16x2(ok ? __fdiv_rn(acc[2 * i], L) : 0.f,
+                              ok ? __fdiv_rn(acc[2 * i + 1], L) : 0.f);
+    uint16_t* dst = p.out + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + hh) * 64 + d0;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  }
+};
 
 // ---------------------------------------------------------------------------
 // Tensor-core page compute (bf16 mma.sync m16n8k16, fp32 accumulate).
@@ -178,7 +270,8 @@ __device__ __forceinline__ uint32_t warp_of(uint32_t u, uint32_t U, uint32_t NW)
 // probabilities never leave registers.
 // ---------------------------------------------------------------------------
 struct MmaState {
-  static constexpr int kMinBlocks = 4;  // <= 128 registers: four CTAs per SM
+  // at most 128 registers per thread: 16 warps of work per SM
+  __host__ __device__ static constexpr int min_blocks(int warps) { return warps >= 16 ? 1 : 16 / warps; }
   uint32_t qa[4][2];  // Q A-fragments per 16-dim chunk: (row gq, k 2tig..) and (k 8+2tig..)
   float o[8][4];      // O accumulators per 8-dim tile
   float m, l;         // running max (log2 units) and per-lane partial denominator
@@ -264,18 +357,22 @@ struct MmaState {
     }
   }
 
-  __device__ __forceinline__ void write_partial(const DecodeParams& p, uint32_t pidx, bool bad,
-                                                int lane) {
-    const int gq = lane >> 2, tig = lane & 3;
+  __device__ __forceinline__ float total_l() const {
     float lt = l;
     lt += __shfl_xor_sync(0xffffffffu, lt, 1);
     lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+    return lt;
+  }
+
+  __device__ __forceinline__ void write_record(const Record& r, bool bad, int lane) {
+    const int gq = lane >> 2, tig = lane & 3;
+    const float lt = total_l();
     if (gq < 4) {
-      float* o_dst = p.ws_o + ((size_t)pidx * 4 + gq) * 64 + 2 * tig;
+      float* o_dst = r.o + gq * 64 + 2 * tig;
 #pragma unroll
       for (int n = 0; n < 8; ++n)
         *reinterpret_cast<float2*>(o_dst + 8 * n) = make_float2(o[n][0], o[n][1]);
-      if (tig == 0) p.ws_ml[(size_t)pidx * 4 + gq] = make_float2(m, bad ? -1.f : lt);
+      if (tig == 0) r.ml[gq] = make_float2(m, bad ? -1.f : lt);
     }
   }
 
@@ -283,9 +380,7 @@ struct MmaState {
   __device__ __forceinline__ void write_output(const DecodeParams& p, int s, int g, bool bad,
                                                int lane) {
     const int gq = lane >> 2, tig = lane & 3;
-    float lt = l;
-    lt += __shfl_xor_sync(0xffffffffu, lt, 1);
-    lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+    const float lt = total_l();
     if (gq < 4) {
       const bool ok = !bad && lt > 0.f;
       uint32_t* dst =
@@ -307,7 +402,7 @@ struct MmaState {
 // output accumulates per lane and is reduced over t8 once per segment.
 // ---------------------------------------------------------------------------
 struct FmaState {
-  static constexpr int kMinBlocks = 1;
+  __host__ __device__ static constexpr int min_blocks(int) { return 1; }
   float qf[4][16];
   float o[4][16];
   float m[4], l[4];
@@ -421,19 +516,18 @@ struct FmaState {
     }
   }
 
-  __device__ __forceinline__ void write_partial(const DecodeParams& p, uint32_t pidx, bool bad,
-                                                int lane) {
+  __device__ __forceinline__ void write_record(const Record& r, bool bad, int lane) {
     const int t8 = lane >> 2, qd = lane & 3;
     float lt[4];
     reduce_tokens(lt);
     if (t8 == 0) {
 #pragma unroll
       for (int hh = 0; hh < 4; ++hh) {
-        float4* dst = reinterpret_cast<float4*>(p.ws_o + ((size_t)pidx * 4 + hh) * 64 + 16 * qd);
+        float4* dst = reinterpret_cast<float4*>(r.o + hh * 64 + 16 * qd);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           dst[i] = make_float4(o[hh][4 * i], o[hh][4 * i + 1], o[hh][4 * i + 2], o[hh][4 * i + 3]);
-        if (qd == 0) p.ws_ml[(size_t)pidx * 4 + hh] = make_float2(m[hh], bad ? -1.f : lt[hh]);
+        if (qd == 0) r.ml[hh] = make_float2(m[hh], bad ? -1.f : lt[hh]);
       }
     }
   }
@@ -448,7 +542,7 @@ struct FmaState {
       for (int hh = 0; hh < 4; ++hh) {
         const bool ok = !bad && lt[hh] > 0.f;
         uint32_t* dst = reinterpret_cast<uint32_t*>(
-                            p.out + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + hh) * 64 + 16 * qd);
+            p.out + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + hh) * 64 + 16 * qd);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float lo = ok ? __fdiv_rn(o[hh][2 * i], lt[hh]) : 0.f;
@@ -461,239 +555,208 @@ struct FmaState {
 };
 
 // ---------------------------------------------------------------------------
-// Merge the P partials of segment (s, g) and store bf16, run by the warp that
-// arrives last.  Partial k was written by warp w0 + k when every warp owns
-// units (U >= NW), else by the owner of unit base + k (one unit per warp).
-//   M = max_k m_k,   o = sum_k e^(m_k - M) o_k / sum_k e^(m_k - M) l_k.
-// Lane (hh = lane/8, dims 8*(lane%8)..+8) produces 8 outputs; partial loads
-// are independent across k, so they overlap.
+// A segment whose records come from several CTAs: store this CTA's merged
+// record, count it in, and let the CTA that arrives last merge all of them.
+// CTA c owns units [c*U/NC, (c+1)*U/NC); when U >= NC every CTA owns some
+// units, so the CTAs touching the segment are c0..c1, else each owns at most
+// one unit and the record of unit base + k comes from owner_of(base + k).
 // ---------------------------------------------------------------------------
-__device__ __noinline__ void combine_segment(const DecodeParams& p, int s, int g, uint32_t base,
-                                             uint32_t w0, uint32_t P, bool dense, uint32_t U,
-                                             uint32_t NW, int lane) {
+__device__ __noinline__ void cross_cta_merge(const DecodeParams& p, const MergeAcc& mine, int s,
+                                             int g, uint32_t base, uint32_t np, uint32_t U,
+                                             uint32_t NC, uint32_t c, int lane) {
   const uint32_t sg = 8u * (uint32_t)s + (uint32_t)g;
-  const int hh = lane >> 3, d0 = (lane & 7) * 8;
-  float M[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-  bool bad = false;
-  for (uint32_t k0 = 0; k0 < P; k0 += 32) {
-    const uint32_t k = k0 + lane;
-    if (k < P) {
-      const uint32_t wk = dense ? w0 + k : warp_of(base + k, U, NW);
-      const float4* ml = reinterpret_cast<const float4*>(p.ws_ml + (size_t)(sg + wk) * 4);
-      const float4 a = __ldcg(ml), b = __ldcg(ml + 1);  // (m0 l0 m1 l1) (m2 l2 m3 l3)
-      M[0] = fmaxf(M[0], a.x);
-      M[1] = fmaxf(M[1], a.z);
-      M[2] = fmaxf(M[2], b.x);
-      M[3] = fmaxf(M[3], b.z);
-      bad |= (a.y < 0.f) || (a.w < 0.f) || (b.y < 0.f) || (b.w < 0.f);
-    }
-  }
-#pragma unroll
-  for (int h = 0; h < 4; ++h)
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M[h] = fmaxf(M[h], __shfl_xor_sync(0xffffffffu, M[h], o));
-  bad = __any_sync(0xffffffffu, bad);
-
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float Lp[4] = {0.f, 0.f, 0.f, 0.f};
-  if (!bad) {
-    for (uint32_t k0 = 0; k0 < P; k0 += 32) {
-      const uint32_t k = k0 + lane;
-      float wt[4] = {0.f, 0.f, 0.f, 0.f};
-      if (k < P) {
-        const uint32_t wk = dense ? w0 + k : warp_of(base + k, U, NW);
-        const float4* ml = reinterpret_cast<const float4*>(p.ws_ml + (size_t)(sg + wk) * 4);
-        const float4 a = __ldcg(ml), b = __ldcg(ml + 1);
-        const float mk[4] = {a.x, a.z, b.x, b.z}, lk[4] = {a.y, a.w, b.y, b.w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          wt[h] = (mk[h] == M[h]) ? 1.f : exp2f(mk[h] - M[h]);
-          Lp[h] += wt[h] * lk[h];
-        }
-      }
-      const uint32_t n = min(32u, P - k0);
+  mine.store_record(global_record(p, sg + c), lane);
+  __threadfence();
+  __syncwarp();
+  uint32_t old = 0;
+  if (lane == 0) old = atomicAdd(p.ws_cnt + sg, 1u);
+  old = __shfl_sync(0xffffffffu, old, 0);
+  const bool dense = U >= NC;
+  const uint32_t c0 = owner_of(base, U, NC);
+  const uint32_t P = dense ? owner_of(base + np - 1, U, NC) - c0 + 1 : np;
+  if (old != P - 1) return;
+  __threadfence();  // every other record of this segment is now visible
+  MergeAcc t;
+  t.init();
 #pragma unroll 4
-      for (uint32_t i = 0; i < n; ++i) {
-        const float x0 = __shfl_sync(0xffffffffu, wt[0], i);
-        const float x1 = __shfl_sync(0xffffffffu, wt[1], i);
-        const float x2 = __shfl_sync(0xffffffffu, wt[2], i);
-        const float x3 = __shfl_sync(0xffffffffu, wt[3], i);
-        const float wi = hh == 0 ? x0 : hh == 1 ? x1 : hh == 2 ? x2 : x3;
-        const uint32_t wk = dense ? w0 + k0 + i : warp_of(base + k0 + i, U, NW);
-        const float4* src =
-            reinterpret_cast<const float4*>(p.ws_o + ((size_t)(sg + wk) * 4 + hh) * 64 + d0);
-        const float4 o0 = __ldcg(src), o1 = __ldcg(src + 1);
-        acc[0] += wi * o0.x; acc[1] += wi * o0.y; acc[2] += wi * o0.z; acc[3] += wi * o0.w;
-        acc[4] += wi * o1.x; acc[5] += wi * o1.y; acc[6] += wi * o1.z; acc[7] += wi * o1.w;
-      }
-    }
+  for (uint32_t k = 0; k < P; ++k) {
+    const uint32_t ck = dense ? c0 + k : owner_of(base + k, U, NC);
+    t.add_global(global_record(p, sg + ck), lane);
   }
-#pragma unroll
-  for (int h = 0; h < 4; ++h)
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) Lp[h] += __shfl_xor_sync(0xffffffffu, Lp[h], o);
-  const float L = hh == 0 ? Lp[0] : hh == 1 ? Lp[1] : hh == 2 ? Lp[2] : Lp[3];
-  const bool ok = !bad && L > 0.f;
-  uint32_t packed[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    packed[i] = pack_bf16x2(ok ? __fdiv_rn(acc[2 * i], L) : 0.f, ok ? __fdiv_rn(acc[2 * i + 1], L) : 0.f);
-  uint16_t* dst = p.out + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + hh) * 64 + d0;
-  *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  t.store_output(p, s, g, lane);
+  if (lane == 0) p.ws_cnt[sg] = 0u;  // ready for the next call
 }
 
 // ---------------------------------------------------------------------------
-// Split phase.
+// The decode kernel.
 // ---------------------------------------------------------------------------
-template <class State, int kStages>
-__global__ void __launch_bounds__(kWarps * 32, State::kMinBlocks)
-    paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
-  using SmemLayout = pkv::SmemLayout<kStages>;
+template <class State, int kWarps, int kStages>
+__global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
+  using Smem = SmemLayout<kWarps, kStages>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  int32_t* prefix = reinterpret_cast<int32_t*>(smem + SmemLayout::kPrefix);
-  int* spid = reinterpret_cast<int*>(smem + SmemLayout::kPid);
+  int32_t* prefix = reinterpret_cast<int32_t*>(smem + Smem::kPrefix);
+  int* spid = reinterpret_cast<int*>(smem + Smem::kPid);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.num_seqs;
 
   pdl_wait();
-  const int n_empty = build_prefix(p, prefix);
+  const int n_empty = build_prefix<kWarps>(p, prefix);
   pdl_launch_dependents();
-  const uint32_t NW = gridDim.x * kWarps;
   if (n_empty > 0) {
     // Sequences without pages get a zero output (16-byte stores, grid-strided).
-    const uint32_t total = (uint32_t)S * (PKV_NUM_Q_HEADS * 64 / 8);
-    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += NW * 32) {
-      const int s = (int)(i / (PKV_NUM_Q_HEADS * 64 / 8));
-      if (prefix[s + 1] == prefix[s])
-        reinterpret_cast<uint4*>(p.out)[i] = make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t per_seq = PKV_NUM_Q_HEADS * 64 / 8;
+    const uint32_t total = (uint32_t)S * per_seq;
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += gridDim.x * blockDim.x) {
+      const int s = (int)(i / per_seq);
+      if (prefix[s + 1] == prefix[s]) reinterpret_cast<uint4*>(p.out)[i] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
 
   const uint32_t U = 8u * (uint32_t)prefix[S];
-  const uint32_t w = blockIdx.x * kWarps + warp;
-  const uint32_t u0 = (uint32_t)(((uint64_t)w * U) / NW);
-  const uint32_t u1 = (uint32_t)(((uint64_t)(w + 1) * U) / NW);
-  if (u0 >= u1) return;
+  const uint32_t NC = gridDim.x, c = blockIdx.x;
+  const uint32_t a = range_start(c, U, NC), b = range_start(c + 1, U, NC);
+  const uint32_t u0 = a + range_start(warp, b - a, kWarps);
+  const uint32_t u1 = a + range_start(warp + 1, b - a, kWarps);
   const int n_units = (int)(u1 - u0);
 
-  const uint32_t tiles = smem_u32(smem) + warp * kStages * kStageBytes;
-  const uint32_t bars = smem_u32(smem + SmemLayout::kBars) + warp * kStages * 8;
-  int* my_pid = spid + warp * kStages;
-  if (lane == 0) {
-    for (int st = 0; st < kStages; ++st) mbar_init(bars + 8 * st, 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-
-  // Page ids of the next 64 units, one per lane in two chunks.
-  int pidA = unit_page(u0 + lane, u1, prefix, p);
-  int pidB = unit_page(u0 + 32 + lane, u1, prefix, p);
-  int chunk_base = 0;
-  Cursor ci;
-  cursor_seek(ci, u0, prefix, S);
-  int iv = 0;
-  bool timed_out = false;
-
-  auto issue = [&](int stage) {
-    const int rel = iv - chunk_base;
-    const int pid = __shfl_sync(0xffffffffu, rel < 32 ? pidA : pidB, rel & 31);
+  if (n_units > 0) {
+    const uint32_t tiles = smem_u32(smem) + warp * kStages * kStageBytes;
+    const uint32_t bars = smem_u32(smem + Smem::kBars) + warp * kStages * 8;
+    int* my_pid = spid + warp * kStages;
     if (lane == 0) {
-      my_pid[stage] = pid;
-      const uint32_t bar = bars + 8 * stage;
-      if (pid >= 0) {
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar, kStageBytes);
-        const uint32_t dst = tiles + stage * kStageBytes;
-        const int zk = (pid * 2 + 0) * PKV_NUM_KV_HEADS + ci.g;
-        const int zv = (pid * 2 + 1) * PKV_NUM_KV_HEADS + ci.g;
-        tma_load_3d(dst, &tmap, 0, 0, zk, bar);
-        tma_load_3d(dst + kTileBytes, &tmap, 0, 0, zv, bar);
-      } else {
-        mbar_arrive(bar);  // keep the phase sequence of this stage intact
-      }
-    }
-    cursor_next(ci, prefix, S);
-    ++iv;
-    if (iv - chunk_base == 32) {
-      pidA = pidB;
-      chunk_base += 32;
-      pidB = unit_page(u0 + chunk_base + 32 + lane, u1, prefix, p);
-    }
-  };
-
-  for (int st = 0; st < kStages && iv < n_units; ++st) issue(st);
-  __syncwarp();
-
-  State st;
-  Cursor cc;
-  cursor_seek(cc, u0, prefix, S);
-  st.reset();
-  st.load_q(p, cc.s, cc.g, lane);
-  int seg_len = __ldg(p.seq_lens + cc.s);
-  bool seg_bad = false;
-
-  for (int uc = 0; uc < n_units; ++uc) {
-    const int stage = uc % kStages;
-    const uint32_t parity = (uint32_t)(uc / kStages) & 1u;
-    const int pid = my_pid[stage];
-    if (!timed_out) {
-      if (!mbar_wait_bounded(bars + 8 * stage, parity, kWaitLimitNs)) {
-        timed_out = true;
-        if (lane == 0) report_error(p.d_err, PKV_ERR_TIMEOUT);
-      }
-    }
-    if (timed_out) {
-      seg_bad = true;
-    } else if (pid >= 0) {
-      const int valid = min(PKV_PAGE_TOKENS, seg_len - PKV_PAGE_TOKENS * cc.j);
-      const uint32_t sK = tiles + stage * kStageBytes;
-      st.page(sK, sK + kTileBytes, valid, p.sl2, lane);
-    } else {
-      seg_bad = true;
-      if (lane == 0) report_error(p.d_err, PKV_ERR_DEVICE_INDEX);
+      for (int st = 0; st < kStages; ++st) mbar_init(bars + 8 * st, 1);
+      fence_mbar_init();
     }
     __syncwarp();
-    if (!timed_out && iv < n_units) issue(stage);
-    const bool seg_end = (cc.j == cc.np - 1) || (uc == n_units - 1);
-    if (seg_end) {
-      const uint32_t np = (uint32_t)cc.np;
-      const uint32_t base = 8u * (uint32_t)prefix[cc.s] + (uint32_t)cc.g * np;
-      const uint32_t w0 = warp_of(base, U, NW);
-      const bool dense = U >= NW;
-      const uint32_t nparts = dense ? warp_of(base + np - 1, U, NW) - w0 + 1 : np;
-      if (nparts == 1) {
-        st.write_output(p, cc.s, cc.g, seg_bad, lane);
-      } else {
-        const uint32_t sg = 8u * (uint32_t)cc.s + (uint32_t)cc.g;
-        st.write_partial(p, sg + w, seg_bad, lane);
-        __threadfence();
-        __syncwarp();
-        uint32_t old = 0;
-        if (lane == 0) old = atomicAdd(p.ws_cnt + sg, 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old == nparts - 1) {  // every other partial of this segment is visible
-          __threadfence();
-          combine_segment(p, cc.s, cc.g, base, w0, nparts, dense, U, NW, lane);
-          if (lane == 0) p.ws_cnt[sg] = 0u;  // ready for the next call
+
+    // Page ids of the next 64 units, one per lane in two chunks.
+    int pidA = unit_page(u0 + lane, u1, prefix, p);
+    int pidB = unit_page(u0 + 32 + lane, u1, prefix, p);
+    int chunk_base = 0;
+    Cursor ci;
+    cursor_seek(ci, u0, prefix, S);
+    int iv = 0;
+    bool timed_out = false;
+
+    auto issue = [&](int stage) {
+      const int rel = iv - chunk_base;
+      const int pid = __shfl_sync(0xffffffffu, rel < 32 ? pidA : pidB, rel & 31);
+      if (lane == 0) {
+        my_pid[stage] = pid;
+        const uint32_t bar = bars + 8 * stage;
+        if (pid >= 0) {
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(bar, kStageBytes);
+          const uint32_t dst = tiles + stage * kStageBytes;
+          const int zk = (pid * 2 + 0) * PKV_NUM_KV_HEADS + ci.g;
+          const int zv = (pid * 2 + 1) * PKV_NUM_KV_HEADS + ci.g;
+          tma_load_3d(dst, &tmap, 0, 0, zk, bar);
+          tma_load_3d(dst + kTileBytes, &tmap, 0, 0, zv, bar);
+        } else {
+          mbar_arrive(bar);  // keep the phase sequence of this stage intact
         }
       }
-      st.reset();
-      seg_bad = false;
-    }
-    cursor_next(cc, prefix, S);
-    if (seg_end && uc + 1 < n_units) {
-      st.load_q(p, cc.s, cc.g, lane);
-      seg_len = __ldg(p.seq_lens + cc.s);
-    }
+      cursor_next(ci, prefix, S);
+      ++iv;
+      if (iv - chunk_base == 32) {
+        pidA = pidB;
+        chunk_base += 32;
+        pidB = unit_page(u0 + chunk_base + 32 + lane, u1, prefix, p);
+      }
+    };
+
+    for (int st = 0; st < kStages && iv < n_units; ++st) issue(st);
     __syncwarp();
+
+    State st;
+    Cursor cc;
+    cursor_seek(cc, u0, prefix, S);
+    st.reset();
+    st.load_q(p, cc.s, cc.g, lane);
+    int seg_len = __ldg(p.seq_lens + cc.s);
+    bool seg_bad = false;
+
+    for (int uc = 0; uc < n_units; ++uc) {
+      const int stage = uc % kStages;
+      const uint32_t parity = (uint32_t)(uc / kStages) & 1u;
+      const int pid = my_pid[stage];
+      if (!timed_out) {
+        if (!mbar_wait_bounded(bars + 8 * stage, parity, kWaitLimitNs)) {
+          timed_out = true;
+          if (lane == 0) report_error(p.d_err, PKV_ERR_TIMEOUT);
+        }
+      }
+      if (timed_out) {
+        seg_bad = true;
+      } else if (pid >= 0) {
+        const int valid = min(PKV_PAGE_TOKENS, seg_len - PKV_PAGE_TOKENS * cc.j);
+        const uint32_t sK = tiles + stage * kStageBytes;
+        st.page(sK, sK + kTileBytes, valid, p.sl2, lane);
+      } else {
+        seg_bad = true;
+        if (lane == 0) report_error(p.d_err, PKV_ERR_DEVICE_INDEX);
+      }
+      __syncwarp();
+      if (!timed_out && iv < n_units) issue(stage);
+      const bool seg_end = (cc.j == cc.np - 1) || (uc == n_units - 1);
+      if (seg_end) {
+        const uint32_t base = seg_base(cc, prefix), last = base + (uint32_t)cc.np - 1;
+        const bool before = base < u0, after = last >= u1;
+        if (!before && !after)
+          st.write_output(p, cc.s, cc.g, seg_bad, lane);
+        else
+          st.write_record(Smem::slot(smem, warp, before ? 0 : 1), seg_bad, lane);
+        st.reset();
+        seg_bad = false;
+      }
+      cursor_next(cc, prefix, S);
+      if (seg_end && uc + 1 < n_units) {
+        st.load_q(p, cc.s, cc.g, lane);
+        seg_len = __ldg(p.seq_lens + cc.s);
+      }
+      __syncwarp();
+    }
+    if (timed_out) {
+      // Drain whatever this warp still has in flight before leaving (bounded).
+      for (int u = max(0, iv - kStages); u < iv; ++u) {
+        const int stage = u % kStages;
+        (void)mbar_wait_bounded(bars + 8 * stage, (uint32_t)(u / kStages) & 1u, kWaitLimitNs);
+      }
+    }
   }
-  if (timed_out) {
-    // Drain whatever this warp still has in flight before leaving (bounded).
-    for (int u = max(0, iv - kStages); u < iv; ++u) {
-      const int stage = u % kStages;
-      (void)mbar_wait_bounded(bars + 8 * stage, (uint32_t)(u / kStages) & 1u, kWaitLimitNs);
+  __syncthreads();
+
+  // Merge the segments that cross warp ranges.  A warp merges (A) its last
+  // segment when that one starts inside its range and runs past it, and the
+  // CTA's first non-empty warp also merges (B) a segment that started before
+  // the CTA range.  Records of the following warps are in their slot 0.
+  if (n_units > 0) {
+    const uint32_t first_warp = owner_of(0, b - a, kWarps);
+    for (int which = 0; which < 2; ++which) {
+      if (which == 0 && (uint32_t)warp != first_warp) continue;
+      Cursor cs;
+      cursor_seek(cs, which == 0 ? u0 : u1 - 1, prefix, S);
+      const uint32_t base = seg_base(cs, prefix), last = base + (uint32_t)cs.np - 1;
+      if (which == 0 && !(base < a)) continue;
+      if (which == 1 && !(base >= u0 && last >= u1)) continue;
+      MergeAcc m;
+      m.init();
+      m.add_shared(Smem::slot(smem, warp, which == 0 ? 0 : 1), lane);
+      for (int j = warp + 1; j < kWarps; ++j) {
+        const uint32_t v0 = a + range_start(j, b - a, kWarps);
+        const uint32_t v1 = a + range_start(j + 1, b - a, kWarps);
+        if (v0 >= v1) continue;  // empty warp range
+        if (v0 > last) break;
+        m.add_shared(Smem::slot(smem, j, 0), lane);
+      }
+      if (base >= a && last < b)
+        m.store_output(p, cs.s, cs.g, lane);
+      else
+        cross_cta_merge(p, m, cs.s, cs.g, base, (uint32_t)cs.np, U, NC, c, lane);
     }
   }
 }
@@ -767,11 +830,11 @@ struct WorkspaceLayout {
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// [cnt: u32 x 8S][ml: float2 x 4 x npart][o: float x 256 x npart], npart =
-// 8S + the most warps a launch can use (partial index 8s + g + warp).
+// [cnt: u32 x 8S][ml: float2 x 4 x npart][o: float x 256 x npart] with
+// npart = 8S + the most CTAs a launch can use (record index 8s + g + c).
 static WorkspaceLayout workspace_layout(int num_seqs, int num_sms) {
   WorkspaceLayout w;
-  w.npart = 8 * num_seqs + num_sms * kMaxCtasPerSm * kWarps;
+  w.npart = 8 * num_seqs + num_sms * kMaxCtasPerSm;
   w.cnt = 0;
   w.ml = align256(4 * (size_t)8 * num_seqs);
   w.o = w.ml + align256((size_t)w.npart * 4 * sizeof(float2));
@@ -779,17 +842,17 @@ static WorkspaceLayout workspace_layout(int num_seqs, int num_sms) {
   return w;
 }
 
-template <class State, int kStages>
-static int setup_split_kernel(int device, size_t smem, int* occ) {
+template <class State, int kWarps, int kStages>
+static int setup_kernel(int device, size_t smem, int* occ) {
   static std::mutex mu;
   static int configured[64] = {0};
   static int cached_occ[64] = {0};
   static size_t cached_smem[64] = {0};
   static int max_dyn_smem[64] = {0};
   std::lock_guard<std::mutex> lock(mu);
-  auto kern = paged_decode_split_kernel<State, kStages>;
+  auto kern = paged_decode_kernel<State, kWarps, kStages>;
   if (device < 0 || device >= 64) {
-    set_last_error("setup_split_kernel", "device index out of range");
+    set_last_error("paged_gqa_decode", "device index out of range");
     return PKV_ERR_CUDA;
   }
   if (!configured[device]) {
@@ -799,10 +862,10 @@ static int setup_split_kernel(int device, size_t smem, int* occ) {
     if (e != cudaSuccess) return cuda_status(e, "cudaDeviceGetAttribute(smem optin)");
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, kern);
-    if (e != cudaSuccess) return cuda_status(e, "cudaFuncGetAttributes(split)");
+    if (e != cudaSuccess) return cuda_status(e, "cudaFuncGetAttributes(decode)");
     const int max_dyn = optin - (int)fa.sharedSizeBytes;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
-    if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(split)");
+    if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(decode)");
     max_dyn_smem[device] = max_dyn;
     configured[device] = 1;
   }
@@ -818,38 +881,35 @@ static int setup_split_kernel(int device, size_t smem, int* occ) {
   return PKV_OK;
 }
 
-template <class State, int kStages>
+template <class State, int kWarps, int kStages>
 static int launch_decode(const DecodeParams& prm, const CUtensorMap& map, int device, int num_sms,
-                         int max_seq_len, int min_units, int ctas_per_sm, cudaStream_t stream,
-                         int* nw_out) {
-  const size_t smem = SmemLayout<kStages>::bytes(prm.num_seqs);
+                         int max_seq_len, int min_units, int ctas_per_sm, cudaStream_t stream) {
+  const size_t smem = SmemLayout<kWarps, kStages>::bytes(prm.num_seqs);
   int occ = 0;
-  int rc = setup_split_kernel<State, kStages>(device, smem, &occ);
+  int rc = setup_kernel<State, kWarps, kStages>(device, smem, &occ);
   if (rc != PKV_OK) return rc;
   if (occ < 1) return PKV_ERR_UNSUPPORTED_SHAPE;
   occ = min(occ, kMaxCtasPerSm);
   if (ctas_per_sm > 0) occ = min(occ, ctas_per_sm);
   const long long pages_bound = max_seq_len > 0 ? (max_seq_len + 15) / 16 : 0;
   const long long u_bound = 8ll * prm.num_seqs * pages_bound;
-  long long nw = (long long)num_sms * occ * kWarps;
-  const long long want = (u_bound + min_units - 1) / min_units;
-  if (want < nw) nw = want;
-  int ctas = (int)((nw + kWarps - 1) / kWarps);
-  if (ctas < 1) ctas = 1;
-  *nw_out = ctas * kWarps;
+  long long nc = (long long)num_sms * occ;
+  const long long want = (u_bound + (long long)kWarps * min_units - 1) / ((long long)kWarps * min_units);
+  if (want < nc) nc = want;
+  if (nc < 1) nc = 1;
 
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ctas);
+  cfg.gridDim = dim3((unsigned)nc);
   cfg.blockDim = dim3(kWarps * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_split_kernel<State, kStages>, map, prm);
-  return cuda_status(e, "cudaLaunchKernelEx(split)");
+  cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<State, kWarps, kStages>, map, prm);
+  return cuda_status(e, "cudaLaunchKernelEx(decode)");
 }
 
 }  // namespace pkv
@@ -889,9 +949,13 @@ extern "C" int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_p
   const int compute = opts ? opts->compute : PKV_COMPUTE_TENSOR;
   const int min_units = (opts && opts->min_units_per_warp > 0) ? opts->min_units_per_warp : 2;
   const int ctas_per_sm = opts ? opts->ctas_per_sm : 0;
-  const int stages = (opts && opts->stages > 0) ? opts->stages : kDefaultStages;
-  if (stages != 2 && stages != 3 && stages != 4 && stages != 8) return PKV_ERR_INVALID_ARGUMENT;
+  const int stages = (opts && opts->stages > 0) ? opts->stages : 2;
+  const int warps = (opts && opts->warps_per_cta > 0) ? opts->warps_per_cta : 16;
   if (compute != PKV_COMPUTE_TENSOR && compute != PKV_COMPUTE_FMA) return PKV_ERR_INVALID_ARGUMENT;
+  const int cfg = warps * 100 + stages;
+  if (compute == PKV_COMPUTE_TENSOR && cfg != 1602 && cfg != 802 && cfg != 804 && cfg != 402 &&
+      cfg != 404)
+    return PKV_ERR_INVALID_ARGUMENT;
 
   int dev = 0;
   int rc = bind_stream_device(stream, &dev);
@@ -921,16 +985,16 @@ extern "C" int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_p
   prm.ws_ml = reinterpret_cast<float2*>(ws + wl.ml);
   prm.ws_o = reinterpret_cast<float*>(ws + wl.o);
 
-  int nw = 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int ms = max_seq_len;
   if (compute == PKV_COMPUTE_FMA)
-    return launch_decode<FmaState, 4>(prm, map, dev, sms, max_seq_len, min_units, ctas_per_sm, st,
-                                      &nw);
-  switch (stages) {
-    case 2: return launch_decode<MmaState, 2>(prm, map, dev, sms, max_seq_len, min_units, ctas_per_sm, st, &nw);
-    case 3: return launch_decode<MmaState, 3>(prm, map, dev, sms, max_seq_len, min_units, ctas_per_sm, st, &nw);
-    case 8: return launch_decode<MmaState, 8>(prm, map, dev, sms, max_seq_len, min_units, ctas_per_sm, st, &nw);
-    default: return launch_decode<MmaState, 4>(prm, map, dev, sms, max_seq_len, min_units, ctas_per_sm, st, &nw);
+    return launch_decode<FmaState, 4, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
+  switch (cfg) {
+    case 802: return launch_decode<MmaState, 8, 2>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
+    case 804: return launch_decode<MmaState, 8, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
+    case 402: return launch_decode<MmaState, 4, 2>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
+    case 404: return launch_decode<MmaState, 4, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
+    default: return launch_decode<MmaState, 16, 2>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
   }
 }
 
