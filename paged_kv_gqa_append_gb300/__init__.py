@@ -55,7 +55,7 @@ _ip = ctypes.POINTER(ctypes.c_int)
 
 class DecodeOpts(ctypes.Structure):
     _fields_ = [("compute", _i), ("min_units_per_warp", _i), ("ctas_per_sm", _i), ("stages", _i),
-                ("warps_per_cta", _i)]
+                ("warps_per_cta", _i), ("combine", _i)]
 
 
 _SIGS = {
@@ -240,7 +240,7 @@ def alloc_workspace(num_seqs: int, device) -> torch.Tensor:
 def paged_gqa_decode(q, kv_pool, block_tables, seq_lens, out, scale, workspace=None,
                      max_seq_len=None, d_err=None, max_blocks=None, compute=None,
                      min_units_per_warp=0, ctas_per_sm=0, stages=0, warps_per_cta=0,
-                     stream=None):
+                     combine=0, stream=None):
     """out[s, h] = softmax(scale * q[s, h] . K) V over sequence s's own pages."""
     dev = kv_pool.device
     _need(kv_pool, "kv_pool", torch.bfloat16, dev, (2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM))
@@ -267,11 +267,12 @@ def paged_gqa_decode(q, kv_pool, block_tables, seq_lens, out, scale, workspace=N
     args = (_ptr(q), _ptr(kv_pool), kv_pool.shape[0], _ptr(block_tables), stride, mb,
             _ptr(seq_lens), S, int(max_seq_len), _ptr(out), float(scale), _ptr(workspace),
             workspace.numel(), _ptr(d_err), _stream(stream))
-    if compute is None and not (min_units_per_warp or ctas_per_sm or stages or warps_per_cta):
+    if compute is None and not (min_units_per_warp or ctas_per_sm or stages or warps_per_cta
+                                or combine):
         st = _L().paged_gqa_decode(*args)
     else:
         opts = DecodeOpts(COMPUTE_TENSOR if compute is None else compute,
-                          min_units_per_warp, ctas_per_sm, stages, warps_per_cta)
+                          min_units_per_warp, ctas_per_sm, stages, warps_per_cta, combine)
         st = _L().paged_gqa_decode_ex(*args, ctypes.byref(opts))
     _check(st, "paged_gqa_decode")
 

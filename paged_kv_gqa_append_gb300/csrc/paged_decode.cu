@@ -60,6 +60,8 @@ struct DecodeParams {
   float sl2;                      // scale * log2(e)
   int* d_err;
   uint32_t* ws_cnt;               // [8 S] CTA arrivals per segment; zero between calls
+  int32_t* ws_prefix;             // [S + 1] page prefix (separate-combine mode)
+  int combine_mode;               // 0: last CTA merges; 1: boundary kernel merges
   float2* ws_ml;                  // [npart][4] (m, l); l < 0 marks a bad segment
   float* ws_o;                    // [npart][4][64]
 };
@@ -76,11 +78,16 @@ struct SmemLayout {
   static constexpr int kTiles = kWarps * kStages * kStageBytes;
   static constexpr int kBars = kTiles;                                 // u64 [kWarps][kStages]
   static constexpr int kPid = kBars + kWarps * kStages * 8;            // int [kWarps][kStages]
-  static constexpr int kSlots = kPid + kWarps * kStages * 4;           // Record [kWarps][2]
-  static constexpr int kPrefix = kSlots + kWarps * 2 * kRecordBytes;   // int [S + 1]
+  static constexpr int kBad = kPid + kWarps * kStages * 4;             // int [kWarps]
+  static constexpr int kSlots = kBad + ((kWarps * 4 + 15) / 16) * 16;  // Record [kWarps]
+  static constexpr int kPrefix = kSlots + kWarps * kRecordBytes;       // int [S + 1]
   static size_t bytes(int num_seqs) { return 1024 + kPrefix + 4 * (size_t)(num_seqs + 1); }
+  // Slot 0 (dedicated) holds the warp's record for a segment that began
+  // before its range; slot 1 holds the record for a segment that runs past
+  // its range, written after the warp's last page, in its own idle tiles.
   __device__ static Record slot(uint8_t* smem, int warp, int which) {
-    uint8_t* base = smem + kSlots + (warp * 2 + which) * kRecordBytes;
+    uint8_t* base = which == 0 ? smem + kSlots + warp * kRecordBytes
+                               : smem + warp * kStages * kStageBytes;
     return Record{reinterpret_cast<float*>(base), reinterpret_cast<float2*>(base + 1024)};
   }
 };
@@ -566,6 +573,7 @@ __device__ __noinline__ void cross_cta_merge(const DecodeParams& p, const MergeA
                                              uint32_t NC, uint32_t c, int lane) {
   const uint32_t sg = 8u * (uint32_t)s + (uint32_t)g;
   mine.store_record(global_record(p, sg + c), lane);
+  if (p.combine_mode == 1) return;  // merged by the boundary kernel after this grid
   __threadfence();
   __syncwarp();
   uint32_t old = 0;
@@ -604,6 +612,8 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
 
   pdl_wait();
   const int n_empty = build_prefix<kWarps>(p, prefix);
+  if (p.combine_mode == 1 && blockIdx.x == 0)
+    for (int i = threadIdx.x; i <= S; i += blockDim.x) p.ws_prefix[i] = prefix[i];
   pdl_launch_dependents();
   if (n_empty > 0) {
     // Sequences without pages get a zero output (16-byte stores, grid-strided).
@@ -623,6 +633,8 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
   const uint32_t u1 = a + range_start(warp + 1, b - a, kWarps);
   const int n_units = (int)(u1 - u0);
 
+  int* warp_bad = reinterpret_cast<int*>(smem + Smem::kBad);
+  if (lane == 0) warp_bad[warp] = 0;
   if (n_units > 0) {
     const uint32_t tiles = smem_u32(smem) + warp * kStages * kStageBytes;
     const uint32_t bars = smem_u32(smem + Smem::kBars) + warp * kStages * 8;
@@ -708,7 +720,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
         const bool before = base < u0, after = last >= u1;
         if (!before && !after)
           st.write_output(p, cc.s, cc.g, seg_bad, lane);
-        else
+        else if (before || !timed_out)  // tiles may still be receiving after a timeout
           st.write_record(Smem::slot(smem, warp, before ? 0 : 1), seg_bad, lane);
         st.reset();
         seg_bad = false;
@@ -721,6 +733,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
       __syncwarp();
     }
     if (timed_out) {
+      if (lane == 0) warp_bad[warp] = 1;
       // Drain whatever this warp still has in flight before leaving (bounded).
       for (int u = max(0, iv - kStages); u < iv; ++u) {
         const int stage = u % kStages;
@@ -746,12 +759,14 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
       MergeAcc m;
       m.init();
       m.add_shared(Smem::slot(smem, warp, which == 0 ? 0 : 1), lane);
+      m.bad |= warp_bad[warp] != 0;
       for (int j = warp + 1; j < kWarps; ++j) {
         const uint32_t v0 = a + range_start(j, b - a, kWarps);
         const uint32_t v1 = a + range_start(j + 1, b - a, kWarps);
         if (v0 >= v1) continue;  // empty warp range
         if (v0 > last) break;
         m.add_shared(Smem::slot(smem, j, 0), lane);
+        m.bad |= warp_bad[j] != 0;
       }
       if (base >= a && last < b)
         m.store_output(p, cs.s, cs.g, lane);
@@ -759,6 +774,40 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
         cross_cta_merge(p, m, cs.s, cs.g, base, (uint32_t)cs.np, U, NC, c, lane);
     }
   }
+}
+
+// ---------------------------------------------------------------------------
+// Separate-combine mode: one warp per CTA boundary c (1 <= c < NC) merges the
+// segment that first crosses it, after the decode grid has finished.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) paged_decode_boundary_kernel(const DecodeParams p,
+                                                                    uint32_t NC) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const uint32_t c = blockIdx.x * 8u + (threadIdx.x >> 5) + 1u;
+  if (c >= NC) return;
+  const int S = p.num_seqs;
+  const int32_t* prefix = p.ws_prefix;
+  const uint32_t U = 8u * (uint32_t)prefix[S];
+  if (U == 0) return;
+  const uint32_t bc = range_start(c, U, NC);
+  if (bc == 0 || bc >= U) return;
+  Cursor cs;
+  cursor_seek(cs, bc, prefix, S);
+  const uint32_t base = seg_base(cs, prefix), np = (uint32_t)cs.np;
+  if (!(base < bc) || c != owner_of(base, U, NC) + 1u) return;
+  const uint32_t sg = 8u * (uint32_t)cs.s + (uint32_t)cs.g;
+  const bool dense = U >= NC;
+  const uint32_t c0 = owner_of(base, U, NC);
+  const uint32_t P = dense ? owner_of(base + np - 1, U, NC) - c0 + 1 : np;
+  MergeAcc t;
+  t.init();
+#pragma unroll 4
+  for (uint32_t k = 0; k < P; ++k) {
+    const uint32_t ck = dense ? c0 + k : owner_of(base + k, U, NC);
+    t.add_global(global_record(p, sg + ck), lane);
+  }
+  t.store_output(p, cs.s, cs.g, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -824,19 +873,20 @@ static int make_pool_map(CUtensorMap* map, const void* pool, int num_pages) {
 }
 
 struct WorkspaceLayout {
-  size_t cnt, ml, o, total;
+  size_t cnt, prefix, ml, o, total;
   int npart;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// [cnt: u32 x 8S][ml: float2 x 4 x npart][o: float x 256 x npart] with
+// [cnt: u32 x 8S][prefix: i32 x (S+1)][ml: float2 x 4 x npart][o: float x 256 x npart] with
 // npart = 8S + the most CTAs a launch can use (record index 8s + g + c).
 static WorkspaceLayout workspace_layout(int num_seqs, int num_sms) {
   WorkspaceLayout w;
   w.npart = 8 * num_seqs + num_sms * kMaxCtasPerSm;
   w.cnt = 0;
-  w.ml = align256(4 * (size_t)8 * num_seqs);
+  w.prefix = align256(4 * (size_t)8 * num_seqs);
+  w.ml = w.prefix + align256(4 * (size_t)(num_seqs + 1));
   w.o = w.ml + align256((size_t)w.npart * 4 * sizeof(float2));
   w.total = w.o + (size_t)w.npart * 4 * 64 * sizeof(float);
   return w;
@@ -909,7 +959,12 @@ static int launch_decode(const DecodeParams& prm, const CUtensorMap& map, int de
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<State, kWarps, kStages>, map, prm);
-  return cuda_status(e, "cudaLaunchKernelEx(decode)");
+  if (e != cudaSuccess || prm.combine_mode != 1 || nc < 2) return cuda_status(e, "cudaLaunchKernelEx(decode)");
+  cfg.gridDim = dim3((unsigned)((nc - 1 + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, paged_decode_boundary_kernel, prm, (uint32_t)nc);
+  return cuda_status(e, "cudaLaunchKernelEx(boundary)");
 }
 
 }  // namespace pkv
@@ -953,8 +1008,8 @@ extern "C" int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_p
   const int warps = (opts && opts->warps_per_cta > 0) ? opts->warps_per_cta : 16;
   if (compute != PKV_COMPUTE_TENSOR && compute != PKV_COMPUTE_FMA) return PKV_ERR_INVALID_ARGUMENT;
   const int cfg = warps * 100 + stages;
-  if (compute == PKV_COMPUTE_TENSOR && cfg != 1602 && cfg != 802 && cfg != 804 && cfg != 402 &&
-      cfg != 404)
+  if (compute == PKV_COMPUTE_TENSOR && cfg != 1602 && cfg != 1603 && cfg != 802 && cfg != 804 &&
+      cfg != 402 && cfg != 404)
     return PKV_ERR_INVALID_ARGUMENT;
 
   int dev = 0;
@@ -982,6 +1037,8 @@ extern "C" int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_p
   prm.d_err = d_err;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   prm.ws_cnt = reinterpret_cast<uint32_t*>(ws + wl.cnt);
+  prm.ws_prefix = reinterpret_cast<int32_t*>(ws + wl.prefix);
+  prm.combine_mode = (opts && opts->combine == 1) ? 1 : 0;
   prm.ws_ml = reinterpret_cast<float2*>(ws + wl.ml);
   prm.ws_o = reinterpret_cast<float*>(ws + wl.o);
 
@@ -990,6 +1047,7 @@ extern "C" int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_p
   if (compute == PKV_COMPUTE_FMA)
     return launch_decode<FmaState, 4, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
   switch (cfg) {
+    case 1603: return launch_decode<MmaState, 16, 3>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
     case 802: return launch_decode<MmaState, 8, 2>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
     case 804: return launch_decode<MmaState, 8, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
     case 402: return launch_decode<MmaState, 4, 2>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);

@@ -240,7 +240,10 @@ def test_decode_mixed_batch8(lib, cuda_device, compute):
                                   dict(ctas_per_sm=1), dict(max_seq_len=2048),
                                   dict(warps_per_cta=8, stages=2), dict(warps_per_cta=8, stages=4),
                                   dict(warps_per_cta=4, stages=2), dict(warps_per_cta=4, stages=4),
-                                  dict(warps_per_cta=4, stages=2, min_units_per_warp=1)])
+                                  dict(warps_per_cta=4, stages=2, min_units_per_warp=1),
+                                  dict(warps_per_cta=16, stages=3), dict(combine=1),
+                                  dict(combine=1, warps_per_cta=4, stages=2, min_units_per_warp=1),
+                                  dict(combine=1, ctas_per_sm=1, min_units_per_warp=1)])
 def test_decode_work_split_variants(lib, cuda_device, opts):
     """Different warp counts (including more warps than units) give the same answer."""
     case = make_case([3, 40, 17, 700, 1, 129, 2048, 16], seed=9, extra_pages=5)
