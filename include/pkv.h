@@ -212,6 +212,36 @@ int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_pages,
                         void* workspace, size_t workspace_bytes,
                         int* d_err, void* stream, const pkv_decode_opts* opts);
 
+/* ------------------------------------------------------------------------
+ * paged_gqa_decode_noalloc - paged_gqa_decode for callers that cannot
+ * allocate device memory.  (No counterpart on the source pages: it exists
+ * for integration, not for the method.)
+ *
+ * Some callers cannot call cudaMalloc at all: a plug-in inside a host
+ * program that owns the whole device-memory budget, or a serving loop that
+ * may not allocate after start-up.  This entry point takes the same inputs
+ * and outputs as paged_gqa_decode but no workspace: it uses a fixed array of
+ * PKV_NOALLOC_WORKSPACE_BYTES in the library's own device memory, which each
+ * GPU that loads the library holds until the process exits.  It allocates
+ * nothing and calls no allocating routine.
+ *   - Limit: paged_gqa_decode_workspace_bytes(num_seqs) must fit in the
+ *     array (on a 152-SM GB300: up to 343 sequences per call); larger
+ *     batches return PKV_ERR_WORKSPACE_TOO_SMALL and pkv_last_error() says
+ *     why.
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the array: calls whose kernels may run
+ *     at the same time on the GPU race with each other.  Each call clears the
+ *     part that must start at zero (on `stream`) before its kernel runs.
+ * ---------------------------------------------------------------------- */
+#define PKV_NOALLOC_WORKSPACE_BYTES (4 * 1024 * 1024)
+
+int paged_gqa_decode_noalloc(const void* q, const void* kv_pool, int num_pages,
+                             const int32_t* block_tables, int bt_row_stride, int max_blocks,
+                             const int32_t* seq_lens, int num_seqs, int max_seq_len,
+                             void* out, float scale, int* d_err, void* stream);
+
 /* Wait for `stream`, then copy the device error word to *code_out (host).
  * If `clear` is non-zero the word is reset to 0 afterwards. */
 int pkv_read_device_error(int* d_err, void* stream, int clear, int* code_out);
