@@ -242,6 +242,42 @@ int paged_gqa_decode_noalloc(const void* q, const void* kv_pool, int num_pages,
                              const int32_t* seq_lens, int num_seqs, int max_seq_len,
                              void* out, float scale, int* d_err, void* stream);
 
+/* ------------------------------------------------------------------------
+ * paged_gqa_decode_append - one decode step with the KV append fused in.
+ *
+ * Same result as kv_append_rope(k_new, v_new, positions = seq_lens - 1,
+ * token_seq = NULL, ..., q_in = q, q_out) followed by
+ * paged_gqa_decode(q_out, ...), in one kernel: for every sequence s with
+ * n = seq_lens[s] >= 1, the new token sits at position p = n - 1; its K is
+ * rotated at p and written with its V into slot p % 16 of page
+ * block_tables[s][p / 16] (bytes identical to kv_append_rope), q[s] is
+ * rotated at p into q_out (if q_out is not NULL), and attention runs over
+ * positions [0, n) with the rotated query.  The warp that owns the page of
+ * the new token inserts it into its staged copy of that page, so no second
+ * pass over memory is needed ("Gestion de la KV cache et strategies de
+ * batching": each new token is written at its absolute RoPE position and
+ * attention reads only the sequence's pages).
+ *
+ *   q             device bf16 [num_seqs][32][64], NOT rotated
+ *   k_new, v_new  device bf16 [num_seqs][8][64]
+ *   rope_cos/sin  device float [max_pos][32]
+ *   kv_pool       device bf16 pool, written (the new token) and read
+ *   q_out         device bf16 [num_seqs][32][64] or NULL
+ * Other arguments as paged_gqa_decode.  seq_len 0 appends nothing and gives
+ * zero outputs; seq_len above max_pos or 16 * max_blocks, or a bad page id,
+ * gives zero outputs for that sequence and sets *d_err.  Tensor-core path
+ * only (opts->compute must be PKV_COMPUTE_TENSOR); warps_per_cta 16, 8 or 4
+ * with 2 stages.
+ * ---------------------------------------------------------------------- */
+int paged_gqa_decode_append(const void* q, const void* k_new, const void* v_new,
+                            const float* rope_cos, const float* rope_sin, int max_pos,
+                            void* kv_pool, int num_pages,
+                            const int32_t* block_tables, int bt_row_stride, int max_blocks,
+                            const int32_t* seq_lens, int num_seqs, int max_seq_len,
+                            void* q_out, void* out, float scale,
+                            void* workspace, size_t workspace_bytes,
+                            int* d_err, void* stream, const pkv_decode_opts* opts);
+
 /* Wait for `stream`, then copy the device error word to *code_out (host).
  * If `clear` is non-zero the word is reset to 0 afterwards. */
 int pkv_read_device_error(int* d_err, void* stream, int clear, int* code_out);

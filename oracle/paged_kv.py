@@ -151,6 +151,48 @@ def decode(q_bits, pool, block_tables, seq_lens, scale: float):
     return out, err
 
 
+def decode_step(pool, q_bits, k_bits, v_bits, block_tables, seq_lens, cos, sin, scale: float):
+    """One decode step: append each sequence's new token, then attend.
+
+    For sequence s with n = seq_lens[s]:
+      * n == 0: nothing is appended; output and rotated query are zero;
+      * n < 0, or n beyond the RoPE table or 16 * max_blocks: the same, and
+        the error flag is raised;
+      * otherwise q_bits[s] is rotated at position n - 1 (returned in q_rot);
+        the new token (k_bits[s], v_bits[s]) is appended at n - 1 through
+        append_rope, which raises the flag and writes nothing if the page for
+        n - 1 is outside the pool; attention over [0, n) uses the rotated
+        query, and a needed page outside the pool gives a zero output and
+        raises the flag (decode's rule).
+    Returns (pool', q_rot [S][32][64] bits, out float64 [S][32][64], err).
+    """
+    S = q_bits.shape[0]
+    lens = np.asarray(seq_lens)
+    max_len = min(cos.shape[0], PAGE_TOKENS * block_tables.shape[1])
+    q_rot = np.zeros_like(q_bits)
+    out = np.zeros((S, NUM_Q_HEADS, HEAD_DIM))
+    err = False
+    valid = []
+    for s in range(S):
+        n = int(lens[s])
+        if n == 0:
+            continue
+        if n < 0 or n > max_len:
+            err = True
+            continue
+        valid.append(s)
+        for h in range(NUM_Q_HEADS):
+            q_rot[s, h] = rope.rotate_bf16(q_bits[s, h], cos[n - 1], sin[n - 1])
+        pool, _, e = append_rope(pool, k_bits[s:s + 1], v_bits[s:s + 1], [n - 1], [s],
+                                 block_tables, cos, sin)
+        err |= e
+    for s in valid:
+        o, e = decode(q_rot[s:s + 1], pool, block_tables[s:s + 1], [int(lens[s])], scale)
+        err |= e
+        out[s] = o[0]
+    return pool, q_rot, out, err
+
+
 def decode_one(q_bits_sh, pool, block_table_row, n: int, scale: float, h: int):
     """One (sequence, query head) output, for sampled checks at full size."""
     kv = gather(pool, block_table_row, n)

@@ -70,6 +70,8 @@ _SIGS = {
     "paged_gqa_decode": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p, _p]),
     "paged_gqa_decode_ex": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p, _p,
                                  ctypes.POINTER(DecodeOpts)]),
+    "paged_gqa_decode_append": (_i, [_p, _p, _p, _p, _p, _i, _p, _i, _p, _i, _i, _p, _i, _i, _p, _p,
+                                     _f, _p, _sz, _p, _p, ctypes.POINTER(DecodeOpts)]),
     "paged_gqa_decode_noalloc": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _p]),
     "pkv_read_device_error": (_i, [_p, _p, _i, _ip]),
     "pkv_credit_pages": (_i, [_i, _i, _i]),
@@ -278,6 +280,52 @@ def paged_gqa_decode(q, kv_pool, block_tables, seq_lens, out, scale, workspace=N
     _check(st, "paged_gqa_decode")
 
 
+def paged_gqa_decode_append(q, k_new, v_new, kv_pool, block_tables, seq_lens, out, rope_cos,
+                            rope_sin, scale, q_out=None, workspace=None, max_seq_len=None,
+                            d_err=None, max_blocks=None, warps_per_cta=0, min_units_per_warp=0,
+                            ctas_per_sm=0, stream=None):
+    """One decode step: append each sequence's new token at seq_lens-1, then attend."""
+    dev = kv_pool.device
+    _need(kv_pool, "kv_pool", torch.bfloat16, dev, (2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM))
+    _need(q, "q", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
+    _need(out, "out", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
+    S = q.numel() // (NUM_Q_HEADS * HEAD_DIM)
+    if out.numel() != q.numel():
+        raise ValueError("out must match q")
+    for t, name in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, name, torch.bfloat16, dev, (NUM_KV_HEADS, HEAD_DIM))
+        if t.numel() != S * NUM_KV_HEADS * HEAD_DIM:
+            raise ValueError(f"{name} must be [num_seqs, 8, 64]")
+    if q_out is not None:
+        _need(q_out, "q_out", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
+        if q_out.numel() != q.numel():
+            raise ValueError("q_out must match q")
+    _need(rope_cos, "rope_cos", torch.float32, dev, (ROPE_PAIRS,))
+    _need(rope_sin, "rope_sin", torch.float32, dev, (ROPE_PAIRS,))
+    _need(block_tables, "block_tables", torch.int32, dev)
+    if block_tables.dim() != 2 or block_tables.shape[0] < S:
+        raise ValueError("block_tables must be [>= num_seqs, row_stride]")
+    _need(seq_lens, "seq_lens", torch.int32, dev)
+    if seq_lens.numel() != S:
+        raise ValueError("seq_lens must have num_seqs entries")
+    stride = block_tables.shape[1]
+    mb = stride if max_blocks is None else max_blocks
+    if max_seq_len is None:
+        max_seq_len = PAGE_TOKENS * mb
+    if workspace is None:
+        workspace = alloc_workspace(S, dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    if d_err is not None:
+        _need(d_err, "d_err", torch.int32, dev)
+    opts = DecodeOpts(COMPUTE_TENSOR, min_units_per_warp, ctas_per_sm, 0, warps_per_cta, 0)
+    st = _L().paged_gqa_decode_append(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(rope_cos), _ptr(rope_sin), rope_cos.shape[0],
+        _ptr(kv_pool), kv_pool.shape[0], _ptr(block_tables), stride, mb, _ptr(seq_lens), S,
+        int(max_seq_len), _ptr(q_out), _ptr(out), float(scale), _ptr(workspace),
+        workspace.numel(), _ptr(d_err), _stream(stream), ctypes.byref(opts))
+    _check(st, "paged_gqa_decode_append")
+
+
 def pkv_read_device_error(d_err, clear: bool = True, stream=None) -> int:
     """Synchronise the stream and return the device error word (optionally reset it)."""
     code = ctypes.c_int(0)
@@ -357,12 +405,15 @@ class Scheduler:
 class DecodeStep:
     """One decode step over every layer, captured once into a CUDA graph.
 
-    Per layer l (in order, as a model runs them):
+    Per layer l (in order, as a model runs them), by default one fused call
+        paged_gqa_decode_append(q[l], k[l], v[l], pool, block_tables[l],
+                                seq_lens, out[l], cos, sin, q_out=q_rot[l])
+    which appends token s of layer l at position seq_lens[s] - 1 and attends
+    over seq_lens[s] tokens; with fused=False the same step runs as
         kv_append_rope(k[l], v[l], positions, block_tables[l], pool, cos, sin,
                        q_in=q[l], q_out=q_rot[l])
         paged_gqa_decode(q_rot[l], pool, block_tables[l], seq_lens, out[l], scale)
-    so token s of layer l is written at positions[s] of row s and attended
-    with seq_lens[s] tokens.  The tensors are bound at construction: refresh
+    (token s written at positions[s]).  The tensors are bound at construction: refresh
     their contents in place (new K/V/q, positions, lengths, tables) and call
     run().  Replaying the graph removes the per-call host cost, and the
     kernels' programmatic-dependent-launch edges overlap each launch with
@@ -376,7 +427,7 @@ class DecodeStep:
 
     def __init__(self, pool, block_tables, seq_lens, positions, k, v, q, out, rope_cos, rope_sin,
                  scale, max_seq_len=None, workspace=None, d_err=None, q_rot=None, compute=None,
-                 use_graph=True, stream=None):
+                 use_graph=True, stream=None, fused=True):
         self.L, self.S = block_tables.shape[0], block_tables.shape[1]
         self.t = dict(pool=pool, bt=block_tables, lens=seq_lens, pos=positions, k=k, v=v, q=q,
                       out=out, cos=rope_cos, sin=rope_sin)
@@ -387,7 +438,9 @@ class DecodeStep:
         self.scale = float(scale)
         self.max_seq_len = max_seq_len
         self.compute = compute
-        self.launches_per_step = 2 * self.L
+        # the fused kernel places each new token at seq_lens - 1 (positions unused)
+        self.fused = fused and compute in (None, COMPUTE_TENSOR)
+        self.launches_per_step = (1 if self.fused else 2) * self.L
         self._launch()                      # eager run: sets up kernels and descriptors
         torch.cuda.synchronize(dev)
         self.graph = None
@@ -398,6 +451,13 @@ class DecodeStep:
 
     def _launch(self, decode_only=False):
         t = self.t
+        if self.fused and not decode_only:
+            for l in range(self.L):
+                paged_gqa_decode_append(t["q"][l], t["k"][l], t["v"][l], t["pool"], t["bt"][l],
+                                        t["lens"], t["out"][l], t["cos"], t["sin"], self.scale,
+                                        q_out=self.q_rot[l], workspace=self.workspace,
+                                        max_seq_len=self.max_seq_len, d_err=self.d_err)
+            return
         for l in range(self.L):
             if not decode_only:
                 kv_append_rope(t["k"][l], t["v"][l], t["pos"], t["bt"][l], t["pool"], t["cos"],

@@ -17,6 +17,7 @@
 #include "internal.h"
 #include "pkv.h"
 #include "ptx.cuh"
+#include "rope.cuh"
 
 namespace pkv {
 
@@ -34,18 +35,6 @@ struct AppendParams {
   int T, num_seqs, bt_stride, max_blocks, num_pages, max_pos;
   int* d_err;
 };
-
-// r0 = x0*c - x1*s, r1 = x0*s + x1*c, every operation rounded to nearest in
-// fp32 (no contraction into FMA), then rounded to bf16 nearest-even.
-__device__ __forceinline__ void rope_pair(uint16_t x0b, uint16_t x1b, float c, float s,
-                                          uint16_t& r0b, uint16_t& r1b) {
-  const float x0 = __uint_as_float((uint32_t)x0b << 16);
-  const float x1 = __uint_as_float((uint32_t)x1b << 16);
-  const float r0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s));
-  const float r1 = __fadd_rn(__fmul_rn(x0, s), __fmul_rn(x1, c));
-  r0b = __bfloat16_as_ushort(__float2bfloat16_rn(r0));
-  r1b = __bfloat16_as_ushort(__float2bfloat16_rn(r1));
-}
 
 __global__ void __launch_bounds__(256) kv_append_rope_kernel(const AppendParams p) {
   pdl_wait();

@@ -40,6 +40,7 @@
 #include "internal.h"
 #include "pkv.h"
 #include "ptx.cuh"
+#include "rope.cuh"
 
 namespace pkv {
 
@@ -64,6 +65,15 @@ struct DecodeParams {
   int combine_mode;               // 0: last CTA merges; 1: boundary kernel merges
   float2* ws_ml;                  // [npart][4] (m, l); l < 0 marks a bad segment
   float* ws_o;                    // [npart][4][64]
+  // Fused decode step (paged_gqa_decode_append): sequence s's new token sits
+  // at position seq_lens[s] - 1; q holds the un-rotated query.
+  const uint16_t* k_new;          // [S][8][64] bf16
+  const uint16_t* v_new;          // [S][8][64] bf16
+  const float* rope_cos;          // [max_pos][32]
+  const float* rope_sin;          // [max_pos][32]
+  uint16_t* q_out;                // [S][32][64] rotated q, or null
+  uint16_t* pool;                 // the pool, writable (same memory as the TMA map)
+  int max_pos;
 };
 
 // One (o, m, l) record: unnormalised o[4][64] and (m, l) for the 4 heads of a
@@ -141,9 +151,9 @@ __device__ __forceinline__ int unit_page(uint32_t u, uint32_t u_end, const int32
   return (pid >= 0 && pid < p.num_pages) ? pid : -1;
 }
 
-// Pages of a sequence, or 0 (and an error) for a length outside [0, 16*max_blocks].
-__device__ __forceinline__ int seq_pages(int n, int max_blocks, bool* bad) {
-  if (n < 0 || n > PKV_PAGE_TOKENS * max_blocks) {
+// Pages of a sequence, or 0 (and an error) for a length outside [0, max_len].
+__device__ __forceinline__ int seq_pages(int n, int max_len, bool* bad) {
+  if (n < 0 || n > max_len) {
     *bad = true;
     return 0;
   }
@@ -152,8 +162,11 @@ __device__ __forceinline__ int seq_pages(int n, int max_blocks, bool* bad) {
 
 // Block-wide exclusive prefix of pages over all sequences into prefix[0..S];
 // returns the number of sequences without pages (empty or invalid length).
-template <int kWarps>
+template <int kWarps, bool kAppend>
 __device__ int build_prefix(const DecodeParams& p, int32_t* prefix) {
+  // with a fused append the new token's position must also lie in the table
+  const int max_len = kAppend ? min(PKV_PAGE_TOKENS * p.max_blocks, p.max_pos)
+                              : PKV_PAGE_TOKENS * p.max_blocks;
   __shared__ int warp_tot[kWarps];
   __shared__ int n_empty;
   if (threadIdx.x == 0) n_empty = 0;
@@ -163,7 +176,7 @@ __device__ int build_prefix(const DecodeParams& p, int32_t* prefix) {
   const int lo = threadIdx.x * per, hi = min(S, lo + per);
   bool bad = false;
   int sum = 0;
-  for (int s = lo; s < hi; ++s) sum += seq_pages(__ldg(p.seq_lens + s), p.max_blocks, &bad);
+  for (int s = lo; s < hi; ++s) sum += seq_pages(__ldg(p.seq_lens + s), max_len, &bad);
   if (bad && blockIdx.x == 0) report_error(p.d_err, PKV_ERR_DEVICE_INDEX);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = sum;
@@ -180,7 +193,7 @@ __device__ int build_prefix(const DecodeParams& p, int32_t* prefix) {
   int empties = 0;
   for (int s = lo; s < hi; ++s) {
     prefix[s] = run;
-    const int np = seq_pages(__ldg(p.seq_lens + s), p.max_blocks, &bad);
+    const int np = seq_pages(__ldg(p.seq_lens + s), max_len, &bad);
     empties += (np == 0);
     run += np;
   }
@@ -283,15 +296,47 @@ struct MmaState {
   float o[8][4];      // O accumulators per 8-dim tile
   float m, l;         // running max (log2 units) and per-lane partial denominator
 
-  __device__ __forceinline__ void load_q(const DecodeParams& p, int s, int g, int lane) {
+  // Q fragments of query heads 4g..4g+3.  With kAppend the query is rotated
+  // here at position `pos` (dims d < 32 and d + 32 sit in the same lane:
+  // fragments kc and kc + 2), and written to q_out when `write_q`.
+  template <bool kAppend>
+  __device__ __forceinline__ void load_q(const DecodeParams& p, int s, int g, int pos,
+                                         bool write_q, int lane) {
     const int gq = lane >> 2, tig = lane & 3;
     if (gq < 4) {
-      const uint32_t* qrow =
-          reinterpret_cast<const uint32_t*>(p.q + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + gq) * 64);
+      const size_t row = ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + gq) * 64;
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + row);
 #pragma unroll
       for (int kc = 0; kc < 4; ++kc) {
         qa[kc][0] = __ldg(qrow + kc * 8 + tig);
         qa[kc][1] = __ldg(qrow + kc * 8 + 4 + tig);
+      }
+      if (kAppend) {
+        const float* cr = p.rope_cos + (size_t)pos * PKV_ROPE_PAIRS;
+        const float* sr = p.rope_sin + (size_t)pos * PKV_ROPE_PAIRS;
+#pragma unroll
+        for (int kc = 0; kc < 2; ++kc) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int d = 16 * kc + 8 * h + 2 * tig;
+            const float2 c = __ldg(reinterpret_cast<const float2*>(cr + d));
+            const float2 sn = __ldg(reinterpret_cast<const float2*>(sr + d));
+            const uint32_t lo = qa[kc][h], hi = qa[kc + 2][h];
+            uint16_t a0, b0, a1, b1;
+            rope_pair((uint16_t)(lo & 0xFFFFu), (uint16_t)(hi & 0xFFFFu), c.x, sn.x, a0, b0);
+            rope_pair((uint16_t)(lo >> 16), (uint16_t)(hi >> 16), c.y, sn.y, a1, b1);
+            qa[kc][h] = (uint32_t)a0 | ((uint32_t)a1 << 16);
+            qa[kc + 2][h] = (uint32_t)b0 | ((uint32_t)b1 << 16);
+          }
+        }
+        if (write_q && p.q_out != nullptr) {
+          uint32_t* qo = reinterpret_cast<uint32_t*>(p.q_out + row);
+#pragma unroll
+          for (int kc = 0; kc < 4; ++kc) {
+            qo[kc * 8 + tig] = qa[kc][0];
+            qo[kc * 8 + 4 + tig] = qa[kc][1];
+          }
+        }
       }
     } else {
 #pragma unroll
@@ -414,7 +459,9 @@ struct FmaState {
   float o[4][16];
   float m[4], l[4];
 
-  __device__ __forceinline__ void load_q(const DecodeParams& p, int s, int g, int lane) {
+  template <bool kAppend>
+  __device__ __forceinline__ void load_q(const DecodeParams& p, int s, int g, int, bool, int lane) {
+    static_assert(!kAppend, "the fused append runs on the tensor-core path only");
     const int qd = lane & 3;
 #pragma unroll
     for (int hh = 0; hh < 4; ++hh) {
@@ -562,6 +609,51 @@ struct FmaState {
 };
 
 // ---------------------------------------------------------------------------
+// Fused append: the warp that owns a sequence's last page writes the new
+// token's rotated K row and its V row into the staged tiles (so its own
+// attention sees them) and into the pool.  Lane l rotates the pair
+// (l, l + 32) and moves V dims (2l, 2l + 1).  Shared-memory element (row, d)
+// of a tile is at row*128 + (((d / 8) ^ (row % 8)) * 16) + (d % 8) * 2.
+// ---------------------------------------------------------------------------
+struct NewToken {
+  uint16_t k0, k1;
+  uint32_t v;
+  float c, s;
+
+  __device__ __forceinline__ void load(const DecodeParams& p, int seq, int g, int pos, int lane) {
+    const uint16_t* kr = p.k_new + ((size_t)seq * PKV_NUM_KV_HEADS + g) * 64;
+    k0 = __ldg(kr + lane);
+    k1 = __ldg(kr + lane + 32);
+    v = __ldg(reinterpret_cast<const uint32_t*>(p.v_new + ((size_t)seq * PKV_NUM_KV_HEADS + g) * 64) +
+              lane);
+    c = __ldg(p.rope_cos + (size_t)pos * PKV_ROPE_PAIRS + lane);
+    s = __ldg(p.rope_sin + (size_t)pos * PKV_ROPE_PAIRS + lane);
+  }
+
+  __device__ __forceinline__ void insert(const DecodeParams& p, uint32_t sK, uint32_t sV, int pid,
+                                         int g, int slot, int lane) const {
+    uint16_t r0, r1;
+    rope_pair(k0, k1, c, s, r0, r1);
+    const uint32_t sw = (uint32_t)(slot & 7), low = (uint32_t)(lane & 7) * 2;
+    const uint32_t rk = sK + (uint32_t)slot * 128;
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(rk + ((((uint32_t)lane >> 3) ^ sw) << 4) + low),
+                 "h"(r0) : "memory");
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(rk + (((((uint32_t)lane >> 3) + 4) ^ sw) << 4) + low),
+                 "h"(r1) : "memory");
+    const uint32_t dv = 2u * (uint32_t)lane;
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(sV + (uint32_t)slot * 128 + (((dv >> 3) ^ sw) << 4) +
+                                                  (dv & 7) * 2),
+                 "r"(v) : "memory");
+    uint16_t* kg = p.pool + ((((size_t)pid * 2 + 0) * PKV_NUM_KV_HEADS + g) * PKV_PAGE_TOKENS + slot) * 64;
+    kg[lane] = r0;
+    kg[lane + 32] = r1;
+    uint32_t* vg = reinterpret_cast<uint32_t*>(
+        p.pool + ((((size_t)pid * 2 + 1) * PKV_NUM_KV_HEADS + g) * PKV_PAGE_TOKENS + slot) * 64);
+    vg[lane] = v;
+  }
+};
+
+// ---------------------------------------------------------------------------
 // A segment whose records come from several CTAs: store this CTA's merged
 // record, count it in, and let the CTA that arrives last merge all of them.
 // CTA c owns units [c*U/NC, (c+1)*U/NC); when U >= NC every CTA owns some
@@ -598,7 +690,7 @@ __device__ __noinline__ void cross_cta_merge(const DecodeParams& p, const MergeA
 // ---------------------------------------------------------------------------
 // The decode kernel.
 // ---------------------------------------------------------------------------
-template <class State, int kWarps, int kStages>
+template <class State, int kWarps, int kStages, bool kAppend>
 __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
   using Smem = SmemLayout<kWarps, kStages>;
@@ -611,7 +703,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
   const int S = p.num_seqs;
 
   pdl_wait();
-  const int n_empty = build_prefix<kWarps>(p, prefix);
+  const int n_empty = build_prefix<kWarps, kAppend>(p, prefix);
   if (p.combine_mode == 1 && blockIdx.x == 0)
     for (int i = threadIdx.x; i <= S; i += blockDim.x) p.ws_prefix[i] = prefix[i];
   pdl_launch_dependents();
@@ -622,7 +714,11 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += gridDim.x * blockDim.x) {
       const int s = (int)(i / per_seq);
-      if (prefix[s + 1] == prefix[s]) reinterpret_cast<uint4*>(p.out)[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (prefix[s + 1] == prefix[s]) {
+        reinterpret_cast<uint4*>(p.out)[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (kAppend && p.q_out != nullptr)
+          reinterpret_cast<uint4*>(p.q_out)[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
   }
 
@@ -688,8 +784,16 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
     Cursor cc;
     cursor_seek(cc, u0, prefix, S);
     st.reset();
-    st.load_q(p, cc.s, cc.g, lane);
     int seg_len = __ldg(p.seq_lens + cc.s);
+    NewToken tok;
+    auto enter_segment = [&]() {
+      const uint32_t base = seg_base(cc, prefix);
+      // this warp rotates q (and stores it if it owns the segment's first
+      // page) and, if it owns the last page, brings in the new token
+      st.template load_q<kAppend>(p, cc.s, cc.g, seg_len - 1, base >= u0, lane);
+      if (kAppend && base + (uint32_t)cc.np - 1 < u1) tok.load(p, cc.s, cc.g, seg_len - 1, lane);
+    };
+    enter_segment();
     bool seg_bad = false;
 
     for (int uc = 0; uc < n_units; ++uc) {
@@ -707,6 +811,10 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
       } else if (pid >= 0) {
         const int valid = min(PKV_PAGE_TOKENS, seg_len - PKV_PAGE_TOKENS * cc.j);
         const uint32_t sK = tiles + stage * kStageBytes;
+        if (kAppend && cc.j == cc.np - 1) {  // the page that receives the new token
+          tok.insert(p, sK, sK + kTileBytes, pid, cc.g, (seg_len - 1) % PKV_PAGE_TOKENS, lane);
+          __syncwarp();
+        }
         st.page(sK, sK + kTileBytes, valid, p.sl2, lane);
       } else {
         seg_bad = true;
@@ -727,8 +835,8 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
       }
       cursor_next(cc, prefix, S);
       if (seg_end && uc + 1 < n_units) {
-        st.load_q(p, cc.s, cc.g, lane);
         seg_len = __ldg(p.seq_lens + cc.s);
+        enter_segment();
       }
       __syncwarp();
     }
@@ -892,7 +1000,7 @@ static WorkspaceLayout workspace_layout(int num_seqs, int num_sms) {
   return w;
 }
 
-template <class State, int kWarps, int kStages>
+template <class State, int kWarps, int kStages, bool kAppend>
 static int setup_kernel(int device, size_t smem, int* occ) {
   static std::mutex mu;
   static int configured[64] = {0};
@@ -900,7 +1008,7 @@ static int setup_kernel(int device, size_t smem, int* occ) {
   static size_t cached_smem[64] = {0};
   static int max_dyn_smem[64] = {0};
   std::lock_guard<std::mutex> lock(mu);
-  auto kern = paged_decode_kernel<State, kWarps, kStages>;
+  auto kern = paged_decode_kernel<State, kWarps, kStages, kAppend>;
   if (device < 0 || device >= 64) {
     set_last_error("paged_gqa_decode", "device index out of range");
     return PKV_ERR_CUDA;
@@ -931,12 +1039,12 @@ static int setup_kernel(int device, size_t smem, int* occ) {
   return PKV_OK;
 }
 
-template <class State, int kWarps, int kStages>
+template <class State, int kWarps, int kStages, bool kAppend = false>
 static int launch_decode(const DecodeParams& prm, const CUtensorMap& map, int device, int num_sms,
                          int max_seq_len, int min_units, int ctas_per_sm, cudaStream_t stream) {
   const size_t smem = SmemLayout<kWarps, kStages>::bytes(prm.num_seqs);
   int occ = 0;
-  int rc = setup_kernel<State, kWarps, kStages>(device, smem, &occ);
+  int rc = setup_kernel<State, kWarps, kStages, kAppend>(device, smem, &occ);
   if (rc != PKV_OK) return rc;
   if (occ < 1) return PKV_ERR_UNSUPPORTED_SHAPE;
   occ = min(occ, kMaxCtasPerSm);
@@ -958,7 +1066,8 @@ static int launch_decode(const DecodeParams& prm, const CUtensorMap& map, int de
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<State, kWarps, kStages>, map, prm);
+  cudaError_t e =
+      cudaLaunchKernelEx(&cfg, paged_decode_kernel<State, kWarps, kStages, kAppend>, map, prm);
   if (e != cudaSuccess || prm.combine_mode != 1 || nc < 2) return cuda_status(e, "cudaLaunchKernelEx(decode)");
   cfg.gridDim = dim3((unsigned)((nc - 1 + 7) / 8));
   cfg.blockDim = dim3(256);
@@ -983,12 +1092,23 @@ extern "C" size_t paged_gqa_decode_workspace_bytes(int num_seqs) {
   return workspace_layout(num_seqs, sms).total;
 }
 
-extern "C" int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_pages,
-                                   const int32_t* block_tables, int bt_row_stride, int max_blocks,
-                                   const int32_t* seq_lens, int num_seqs, int max_seq_len,
-                                   void* out, float scale, void* workspace,
-                                   size_t workspace_bytes, int* d_err, void* stream,
-                                   const pkv_decode_opts* opts) {
+namespace pkv {
+
+// New-token inputs of the fused decode step.
+struct AppendArgs {
+  const void* k_new;
+  const void* v_new;
+  const float* rope_cos;
+  const float* rope_sin;
+  int max_pos;
+  void* q_out;
+};
+
+static int decode_entry(const void* q, const void* kv_pool, int num_pages,
+                        const int32_t* block_tables, int bt_row_stride, int max_blocks,
+                        const int32_t* seq_lens, int num_seqs, int max_seq_len, void* out,
+                        float scale, void* workspace, size_t workspace_bytes, int* d_err,
+                        void* stream, const pkv_decode_opts* opts, const AppendArgs* app) {
   if (num_seqs < 0 || num_pages < 1 || max_blocks < 1 || bt_row_stride < max_blocks)
     return PKV_ERR_INVALID_ARGUMENT;
   if (num_seqs == 0) return PKV_OK;
@@ -998,6 +1118,14 @@ extern "C" int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_p
   if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out) || !aligned16(workspace) ||
       (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
     return PKV_ERR_MISALIGNED;
+  if (app) {
+    if (!app->k_new || !app->v_new || !app->rope_cos || !app->rope_sin || app->max_pos < 1)
+      return PKV_ERR_INVALID_ARGUMENT;
+    if (((reinterpret_cast<uintptr_t>(app->k_new) | reinterpret_cast<uintptr_t>(app->v_new) |
+          reinterpret_cast<uintptr_t>(app->rope_cos) | reinterpret_cast<uintptr_t>(app->rope_sin)) & 7u) ||
+        !aligned16(app->q_out))
+      return PKV_ERR_MISALIGNED;
+  }
   if (num_seqs > kMaxSeqs || (long long)num_pages * 16 * 8 * 2 >= (1ll << 31) ||
       (long long)max_blocks * PKV_PAGE_TOKENS >= (1ll << 24))
     return PKV_ERR_UNSUPPORTED_SHAPE;
@@ -1007,10 +1135,12 @@ extern "C" int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_p
   const int stages = (opts && opts->stages > 0) ? opts->stages : 2;
   const int warps = (opts && opts->warps_per_cta > 0) ? opts->warps_per_cta : 16;
   if (compute != PKV_COMPUTE_TENSOR && compute != PKV_COMPUTE_FMA) return PKV_ERR_INVALID_ARGUMENT;
+  if (app && compute != PKV_COMPUTE_TENSOR) return PKV_ERR_INVALID_ARGUMENT;
   const int cfg = warps * 100 + stages;
   if (compute == PKV_COMPUTE_TENSOR && cfg != 1602 && cfg != 1603 && cfg != 802 && cfg != 804 &&
       cfg != 402 && cfg != 404)
     return PKV_ERR_INVALID_ARGUMENT;
+  if (app && cfg != 1602 && cfg != 802 && cfg != 402) return PKV_ERR_INVALID_ARGUMENT;
 
   int dev = 0;
   int rc = bind_stream_device(stream, &dev);
@@ -1025,6 +1155,7 @@ extern "C" int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_p
   if (rc != PKV_OK) return rc;
 
   DecodeParams prm;
+  memset(&prm, 0, sizeof(prm));
   prm.q = static_cast<const uint16_t*>(q);
   prm.block_tables = block_tables;
   prm.seq_lens = seq_lens;
@@ -1041,9 +1172,25 @@ extern "C" int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_p
   prm.combine_mode = (opts && opts->combine == 1) ? 1 : 0;
   prm.ws_ml = reinterpret_cast<float2*>(ws + wl.ml);
   prm.ws_o = reinterpret_cast<float*>(ws + wl.o);
+  if (app) {
+    prm.k_new = static_cast<const uint16_t*>(app->k_new);
+    prm.v_new = static_cast<const uint16_t*>(app->v_new);
+    prm.rope_cos = app->rope_cos;
+    prm.rope_sin = app->rope_sin;
+    prm.max_pos = app->max_pos;
+    prm.q_out = static_cast<uint16_t*>(app->q_out);
+    prm.pool = static_cast<uint16_t*>(const_cast<void*>(kv_pool));
+  }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int ms = max_seq_len;
+  if (app) {
+    switch (cfg) {
+      case 802: return launch_decode<MmaState, 8, 2, true>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
+      case 402: return launch_decode<MmaState, 4, 2, true>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
+      default: return launch_decode<MmaState, 16, 2, true>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
+    }
+  }
   if (compute == PKV_COMPUTE_FMA)
     return launch_decode<FmaState, 4, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
   switch (cfg) {
@@ -1054,6 +1201,32 @@ extern "C" int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_p
     case 404: return launch_decode<MmaState, 4, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
     default: return launch_decode<MmaState, 16, 2>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
   }
+}
+
+}  // namespace pkv
+
+extern "C" int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_pages,
+                                   const int32_t* block_tables, int bt_row_stride, int max_blocks,
+                                   const int32_t* seq_lens, int num_seqs, int max_seq_len,
+                                   void* out, float scale, void* workspace,
+                                   size_t workspace_bytes, int* d_err, void* stream,
+                                   const pkv_decode_opts* opts) {
+  return decode_entry(q, kv_pool, num_pages, block_tables, bt_row_stride, max_blocks, seq_lens,
+                      num_seqs, max_seq_len, out, scale, workspace, workspace_bytes, d_err, stream,
+                      opts, nullptr);
+}
+
+extern "C" int paged_gqa_decode_append(const void* q, const void* k_new, const void* v_new,
+                                       const float* rope_cos, const float* rope_sin, int max_pos,
+                                       void* kv_pool, int num_pages, const int32_t* block_tables,
+                                       int bt_row_stride, int max_blocks, const int32_t* seq_lens,
+                                       int num_seqs, int max_seq_len, void* q_out, void* out,
+                                       float scale, void* workspace, size_t workspace_bytes,
+                                       int* d_err, void* stream, const pkv_decode_opts* opts) {
+  const AppendArgs app{k_new, v_new, rope_cos, rope_sin, max_pos, q_out};
+  return decode_entry(q, kv_pool, num_pages, block_tables, bt_row_stride, max_blocks, seq_lens,
+                      num_seqs, max_seq_len, out, scale, workspace, workspace_bytes, d_err, stream,
+                      opts, &app);
 }
 
 extern "C" int paged_gqa_decode(const void* q, const void* kv_pool, int num_pages,

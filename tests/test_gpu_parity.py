@@ -258,9 +258,10 @@ def test_decode_work_split_variants(lib, cuda_device, opts):
 
 # ------------------------------------------------- full-size, sampled -------
 
-def full_size_step_check(lib, dev, case, samples, tables):
+def full_size_step_check(lib, dev, case, samples, tables, fused=True):
     """Run one bench-shaped step (append new token with q rotation, then decode,
-    on every layer) and compare sampled (layer, seq) outputs with the oracle."""
+    on every layer; fused into one call or as two calls) and compare sampled
+    (layer, seq) outputs with the oracle."""
     cos_d, sin_d, cos_o, sin_o = tables
     pool = W.fill_pool(case, device=dev)
     q_raw = W.fill_queries(case, device=dev)
@@ -279,10 +280,15 @@ def full_size_step_check(lib, dev, case, samples, tables):
     ws = lib.alloc_workspace(case.num_seqs, dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     for l in range(case.num_layers):
-        lib.kv_append_rope(k_new[l], v_new[l], posd, bt_all[l], pool, cos_d, sin_d,
-                           q_in=q_raw[l], q_out=q_rot[l], d_err=err)
-        lib.paged_gqa_decode(q_rot[l], pool, bt_all[l], lens, out[l], case.scale, workspace=ws,
-                             max_seq_len=case.max_seq_len, d_err=err)
+        if fused:
+            lib.paged_gqa_decode_append(q_raw[l], k_new[l], v_new[l], pool, bt_all[l], lens, out[l],
+                                        cos_d, sin_d, case.scale, q_out=q_rot[l], workspace=ws,
+                                        max_seq_len=case.max_seq_len, d_err=err)
+        else:
+            lib.kv_append_rope(k_new[l], v_new[l], posd, bt_all[l], pool, cos_d, sin_d,
+                               q_in=q_raw[l], q_out=q_rot[l], d_err=err)
+            lib.paged_gqa_decode(q_rot[l], pool, bt_all[l], lens, out[l], case.scale,
+                                 workspace=ws, max_seq_len=case.max_seq_len, d_err=err)
     assert lib.pkv_read_device_error(err) == 0
     worst = 0.0
     for (l, s) in samples:
@@ -304,10 +310,11 @@ def full_size_step_check(lib, dev, case, samples, tables):
     return worst
 
 
-def test_full_size_batch32_sampled(lib, cuda_device, tables):
+@pytest.mark.parametrize("fused", [True, False])
+def test_full_size_batch32_sampled(lib, cuda_device, tables, fused):
     case = W.case_batch32()
     samples = [(0, 0), (0, 31), (7, 13), (15, 5), (15, 31)]
-    full_size_step_check(lib, cuda_device, case, samples, tables)
+    full_size_step_check(lib, cuda_device, case, samples, tables, fused=fused)
 
 
 def test_full_size_stress256_sampled(lib, cuda_device, tables):
@@ -336,7 +343,8 @@ def test_workspace_counters_return_to_zero(lib, cuda_device):
         assert int(cnt.abs().sum()) == 0
 
 
-def test_decode_step_graph_matches_eager_and_oracle(lib, cuda_device, tables):
+@pytest.mark.parametrize("fused", [True, False])
+def test_decode_step_graph_matches_eager_and_oracle(lib, cuda_device, tables, fused):
     cos_d, sin_d, cos_o, sin_o = tables
     case = W.case_uniform(6, batch=4, layers=3, ctx=300, name="step_small")
     case.seq_lens[:] = [300, 17, 129, 256]
@@ -352,7 +360,7 @@ def test_decode_step_graph_matches_eager_and_oracle(lib, cuda_device, tables):
         pool = pool0.clone()
         out = torch.empty_like(q)
         step = lib.DecodeStep(pool, bt, lens, pos, k, v, q, out, cos_d, sin_d, case.scale,
-                              max_seq_len=300, use_graph=use_graph)
+                              max_seq_len=300, use_graph=use_graph, fused=fused)
         step.run()
         assert step.error() == 0
         outs.append((bits(out), bits(pool), bits(step.q_rot)))
@@ -368,3 +376,81 @@ def test_decode_step_graph_matches_eager_and_oracle(lib, cuda_device, tables):
         ref, _ = OP.decode(want_q, want_pool, case.block_tables[l], case.seq_lens, case.scale)
         check_close(OB.to_f64(out_b[l]), ref, f"step layer {l}")
     assert np.array_equal(pool_b, pool_in)
+
+
+# ------------------------------------------------------- fused decode step --
+
+def fused_case(lens, seed, layers=2):
+    case = make_case(lens, seed=seed, extra_pages=6)
+    # same lengths for every layer, separate pages per layer
+    bt = case.block_tables[0]
+    L = layers
+    N = case.num_pages
+    tables = np.full((L, len(lens), 128), -1, np.int32)
+    for l in range(L):
+        tables[l] = np.where(bt >= 0, bt + l * N, -1)
+    return W.DecodeCase(case.name, seed, L, case.seq_lens, N * L, tables)
+
+
+@pytest.mark.parametrize("warps", [0, 8, 4])
+def test_fused_append_decode_matches_oracle(lib, cuda_device, tables, warps):
+    cos_d, sin_d, cos_o, sin_o = tables
+    case = fused_case([1, 16, 17, 0, 2048, 333, 1500, 2], seed=41)
+    dev = cuda_device
+    pool0 = W.fill_pool(case)
+    q = W.fill_queries(case)
+    k, v = W.fill_new_kv(case)
+    pool = pool0.to(dev)
+    q_out = torch.full(q.shape, 3.0, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lens = torch.from_numpy(case.seq_lens).to(dev)
+    for l in range(case.num_layers):
+        lib.paged_gqa_decode_append(q[l].to(dev), k[l].to(dev), v[l].to(dev), pool,
+                                    torch.from_numpy(case.block_tables[l]).to(dev), lens, out[l],
+                                    cos_d, sin_d, case.scale, q_out=q_out[l], d_err=err,
+                                    warps_per_cta=warps, max_seq_len=2048)
+    assert lib.pkv_read_device_error(err) == 0
+    want_pool = bits(pool0)
+    for l in range(case.num_layers):
+        want_pool, want_q, ref, e = OP.decode_step(want_pool, bits(q[l]), bits(k[l]), bits(v[l]),
+                                                   case.block_tables[l], case.seq_lens, cos_o,
+                                                   sin_o, case.scale)
+        assert not e
+        assert np.array_equal(bits(q_out[l]), want_q)
+        check_close(bf16_to_f64(out[l]), ref, f"fused layer {l} warps {warps}")
+    assert np.array_equal(bits(pool), want_pool)
+
+
+@pytest.mark.parametrize("bad", ["last_page", "middle_page", "past_table"])
+def test_fused_append_decode_error_contract(lib, cuda_device, tables, bad):
+    cos_d, sin_d, cos_o, sin_o = tables
+    case = fused_case([40, 70, 17], seed=43, layers=1)
+    dev = cuda_device
+    pool0 = W.fill_pool(case)
+    q, (k, v) = W.fill_queries(case), W.fill_new_kv(case)
+    bt = case.block_tables[0].copy()
+    lens = case.seq_lens.copy()
+    if bad == "last_page":
+        bt[1, 4] = case.num_pages + 5      # the page that should receive seq 1's new token
+    elif bad == "middle_page":
+        bt[1, 1] = -1
+    else:
+        lens[1] = 65                       # position 64 is past the 64-entry rope table
+        bt[1, 4] = bt[1, 3]
+    pool = pool0.to(dev)
+    out = torch.empty(q[0].shape, dtype=torch.bfloat16, device=dev)
+    q_out = torch.full(q[0].shape, 3.0, dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lib.paged_gqa_decode_append(q[0].to(dev), k[0].to(dev), v[0].to(dev), pool,
+                                torch.from_numpy(bt).to(dev), torch.from_numpy(lens).to(dev), out,
+                                cos_d[:64].contiguous(), sin_d[:64].contiguous(), case.scale,
+                                q_out=q_out, d_err=err)
+    assert lib.pkv_read_device_error(err) == lib.ERR_DEVICE_INDEX
+    want_pool, want_q, ref, e = OP.decode_step(bits(pool0), bits(q[0]), bits(k[0]), bits(v[0]),
+                                               bt, lens, cos_o[:64], sin_o[:64], case.scale)
+    assert e
+    assert np.array_equal(bits(pool), want_pool)
+    assert np.array_equal(bits(q_out), want_q)
+    assert np.all(bits(out)[1] == 0)
+    check_close(bf16_to_f64(out), ref, f"fused with a bad sequence ({bad})")

@@ -302,3 +302,31 @@ def test_workload_shapes():
     assert ids.size == 65536 and np.unique(ids).size == 65536
     c5 = W.case_stress()
     assert c5.num_pages * W.PAGE_ELEMS * 2 == 16 * 2 ** 30
+
+
+def test_decode_step_is_append_then_decode():
+    """The step equals the two-call composition when every index is valid,
+    and isolates a bad sequence (zero output, flag) when one is not."""
+    rng = np.random.default_rng(15)
+    lens = np.array([1, 16, 17, 0, 50], np.int32)
+    pool, bt, q = random_paged(rng, lens, extra_pages=4)
+    k, v = rand_bits(rng, (5, 8, 64)), rand_bits(rng, (5, 8, 64))
+    cos, sin = rope.table(rope.inv_freq_llama3(), 64)
+    p1, qr, out, err = P.decode_step(pool, q, k, v, bt, lens, cos, sin, 0.125)
+    assert not err
+    live = np.nonzero(lens)[0]
+    p2, qr2, e2 = P.append_rope(pool, k[live], v[live], lens[live] - 1, live, bt, cos, sin, q[live])
+    assert not e2 and np.array_equal(p1, p2) and np.array_equal(qr[live], qr2)
+    assert np.all(qr[3] == 0) and np.all(out[3] == 0)
+    qf = np.zeros_like(q)
+    qf[live] = qr2
+    ref, _ = P.decode(qf, p2, bt, lens, 0.125)
+    assert np.array_equal(out, ref)
+    # a length past the 64-entry table: that sequence only is rejected
+    lens_bad = lens.copy()
+    lens_bad[4] = 65
+    bt_big = bt.copy()
+    bt_big[4, 4] = bt[4, 3]
+    _, qr3, out3, err3 = P.decode_step(pool, q, k, v, bt_big, lens_bad, cos, sin, 0.125)
+    assert err3 and np.all(out3[4] == 0) and np.all(qr3[4] == 0)
+    assert np.array_equal(out3[:3], out[:3])
