@@ -59,10 +59,11 @@ def locate(block_table_row, pos: int, num_pages: int, max_blocks: int):
 
 
 def append_rope(pool, k_bits, v_bits, positions, token_seq, block_tables, cos, sin,
-                q_bits=None):
+                q_bits=None, inplace=False):
     """Write T new tokens into the pool.  Returns (pool', q_rot or None, error_flag).
 
-    pool:          uint16 [N][2][8][16][64] (not modified; a copy is returned)
+    pool:          uint16 [N][2][8][16][64] (a copy is returned, or the pool
+                   itself is written when inplace=True)
     k_bits/v_bits: uint16 [T][8][64]
     positions:     [T] absolute positions; token_seq: [T] rows of block_tables
                    (None: token t belongs to row t)
@@ -72,7 +73,7 @@ def append_rope(pool, k_bits, v_bits, positions, token_seq, block_tables, cos, s
     Tokens are applied in order, so a later duplicate (same row and position)
     would overwrite an earlier one.
     """
-    out = np.array(pool, copy=True)
+    out = pool if inplace else np.array(pool, copy=True)
     num_pages = out.shape[0]
     S, max_blocks = block_tables.shape
     max_pos = cos.shape[0]
@@ -90,9 +91,8 @@ def append_rope(pool, k_bits, v_bits, positions, token_seq, block_tables, cos, s
             err = True
             continue
         page, slot = where
-        for g in range(NUM_KV_HEADS):
-            out[page, 0, g, slot, :] = rope.rotate_bf16(k_bits[t, g], cos[p], sin[p])
-            out[page, 1, g, slot, :] = v_bits[t, g]
+        out[page, 0, :, slot, :] = rope.rotate_bf16(k_bits[t], cos[p], sin[p])   # all 8 heads
+        out[page, 1, :, slot, :] = v_bits[t]
         if q_bits is not None:
             for h in range(NUM_Q_HEADS):
                 q_rot[t, h] = rope.rotate_bf16(q_bits[t, h], cos[p], sin[p])

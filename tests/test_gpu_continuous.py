@@ -1,0 +1,133 @@
+"""Continuous-batching mix on the GPU, step for step against the oracle.
+
+64 requests (prompts geometric, mean 300, clipped to [1, 1920]) run 128
+decode steps each on 16 layers in a 128 MiB pool, admitted by the
+admission-credit rule.  The C++ scheduler (driving the kernels) and the
+oracle's scheduler must take identical decisions; every decode output of
+layers 0 and 15 at every 16th step must match the FP64 oracle; the final pool
+must equal the oracle's bit for bit.  The same run is made with the fused
+decode step and with kv_append_rope followed by paged_gqa_decode.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import admission as OA, paged_kv as OP, rope as OR
+from tests._util import bf16_to_f64, bits, check_close
+
+pytestmark = pytest.mark.gpu
+
+SAMPLE_EVERY = 16
+SAMPLE_LAYERS = (0, 15)
+
+
+@pytest.fixture(scope="module")
+def lib(cuda_device):
+    from paged_kv_gqa_append_gb300 import build
+    build.build()
+    import paged_kv_gqa_append_gb300 as m
+    return m
+
+
+class Source:
+    """Seeded K/V/q of the mix, memoised per (request, layer, position)."""
+
+    def __init__(self, case):
+        self.case = case
+        self.q_cache = {}
+        self.kv_cache = {}
+
+    def prompt_kv(self, rid, layer):
+        return W.request_kv(self.case.seed, rid, layer, 0, int(self.case.prompt_lens[rid]))
+
+    def token_kv(self, rid, layer, pos):
+        key = (rid, layer, pos)
+        if key not in self.kv_cache:
+            k, v = W.request_kv(self.case.seed, rid, layer, pos, 1)
+            self.kv_cache[key] = (k[0], v[0])
+        return self.kv_cache[key]
+
+    def token_q(self, rid, layer, pos):
+        key = (rid, layer, pos)
+        if key not in self.q_cache:
+            self.q_cache[key] = W.request_q(self.case.seed, rid, layer, pos)
+        return self.q_cache[key]
+
+
+def run_mix(lib, dev, case, fused, cos_d, sin_d):
+    from paged_kv_gqa_append_gb300.serving import ContinuousBatcher
+    src = Source(case)
+    pool = torch.zeros((case.num_pages, 2, 8, 16, 64), dtype=torch.bfloat16, device=dev)
+    cb = ContinuousBatcher(pool, case.num_layers, cos_d, sin_d, W.DEFAULT_SCALE,
+                           max_slots=64, fused=fused)
+    for p in case.prompt_lens:
+        assert cb.submit(int(p), case.allowed_new_tokens) >= 0
+    # oracle side
+    osch = OA.Scheduler(case.num_pages, case.num_layers, W.MAX_BLOCKS, 64)
+    for p in case.prompt_lens:
+        assert osch.submit(int(p), case.allowed_new_tokens)[0] == OA.Scheduler.OK
+    opool = OP.new_pool(case.num_pages)
+    cos_o, sin_o = OR.table(OR.inv_freq_llama3(), W.MAX_CONTEXT)
+    orun, olen, odone = [], {}, {}
+    step = 0
+    checked = 0
+    while cb.sched.stats()["queued"] or cb.running:
+        adm = cb.admit(src.prompt_kv)
+        oadm = osch.admit()
+        assert adm == oadm, (step, adm, oadm)
+        for rid in oadm:
+            P = int(case.prompt_lens[rid])
+            assert osch.grow(rid, P) == osch.OK
+            for l in range(case.num_layers):
+                k, v = src.prompt_kv(rid, l)
+                row = np.array([osch.block_table_row(rid, l)], np.int32)
+                _, _, e = OP.append_rope(opool, bits(k), bits(v), np.arange(P), np.zeros(P, np.int32),
+                                         row, cos_o, sin_o, inplace=True)
+                assert not e
+            olen[rid], odone[rid] = P, 0
+        orun += oadm
+        ids, lens, out = cb.step(src.token_kv, src.token_q)
+        assert ids == orun
+        sample = step % SAMPLE_EVERY == 0
+        outs = out[list(SAMPLE_LAYERS)].cpu() if sample else None
+        for rid in orun:
+            assert osch.grow(rid, olen[rid] + 1) == osch.OK
+        for l in range(case.num_layers):
+            for b, rid in enumerate(orun):
+                pos = olen[rid]
+                k, v = src.token_kv(rid, l, pos)
+                row = np.array([osch.block_table_row(rid, l)], np.int32)
+                q = src.token_q(rid, l, pos)
+                _, qr, e = OP.append_rope(opool, bits(k[None]), bits(v[None]), [pos], [0], row,
+                                          cos_o, sin_o, bits(q[None]), inplace=True)
+                assert not e
+                if sample and l in SAMPLE_LAYERS:
+                    ref, e2 = OP.decode(qr, opool, row, [pos + 1], W.DEFAULT_SCALE)
+                    assert not e2
+                    got = bf16_to_f64(outs[SAMPLE_LAYERS.index(l), b])[None]
+                    check_close(got, ref, f"step {step} layer {l} request {rid}")
+                    checked += 1
+        for rid in orun:
+            olen[rid] += 1
+            odone[rid] += 1
+        done = cb.retire(case.decode_steps)
+        odone_ids = [r for r in orun if odone[r] == case.decode_steps]
+        assert done == odone_ids
+        for rid in odone_ids:
+            osch.finish(rid)
+        orun = [r for r in orun if r not in odone_ids]
+        step += 1
+    assert cb.error() == 0
+    assert cb.sched.events() == osch.events
+    assert np.array_equal(bits(pool), opool)
+    assert checked >= len(case.prompt_lens)     # every request sampled at least once
+    return step
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_continuous_batching_mix_matches_oracle(lib, cuda_device, fused):
+    case = W.case_continuous()
+    cos_d, sin_d = lib.rope_tables_device(cuda_device, W.MAX_CONTEXT)
+    steps = run_mix(lib, cuda_device, case, fused, cos_d, sin_d)
+    assert steps > case.decode_steps          # requests really overlapped in time
