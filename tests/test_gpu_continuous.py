@@ -127,7 +127,9 @@ def run_mix(lib, dev, case, fused, cos_d, sin_d):
 
 @pytest.mark.parametrize("fused", [True, False])
 def test_continuous_batching_mix_matches_oracle(lib, cuda_device, fused):
-    case = W.case_continuous()
+    # the full 64-request mix on the fused step; the two-call path on its
+    # first 16 requests (same scheduler, same pool size)
+    case = W.case_continuous() if fused else W.case_continuous(requests=16)
     cos_d, sin_d = lib.rope_tables_device(cuda_device, W.MAX_CONTEXT)
     steps = run_mix(lib, cuda_device, case, fused, cos_d, sin_d)
     assert steps > case.decode_steps          # requests really overlapped in time
