@@ -55,7 +55,7 @@ _ip = ctypes.POINTER(ctypes.c_int)
 
 class DecodeOpts(ctypes.Structure):
     _fields_ = [("compute", _i), ("min_units_per_warp", _i), ("ctas_per_sm", _i), ("stages", _i),
-                ("warps_per_cta", _i), ("combine", _i)]
+                ("warps_per_cta", _i), ("combine", _i), ("schedule", _i), ("early_kv", _i)]
 
 
 _SIGS = {
@@ -243,8 +243,13 @@ def alloc_workspace(num_seqs: int, device) -> torch.Tensor:
 def paged_gqa_decode(q, kv_pool, block_tables, seq_lens, out, scale, workspace=None,
                      max_seq_len=None, d_err=None, max_blocks=None, compute=None,
                      min_units_per_warp=0, ctas_per_sm=0, stages=0, warps_per_cta=0,
-                     combine=0, stream=None):
-    """out[s, h] = softmax(scale * q[s, h] . K) V over sequence s's own pages."""
+                     combine=0, schedule=0, early_kv=0, stream=None):
+    """out[s, h] = softmax(scale * q[s, h] . K) V over sequence s's own pages.
+
+    early_kv=1 promises that the kernel enqueued just before this call on the
+    stream writes neither block_tables, seq_lens nor the pages read here; the
+    call then starts on them while that kernel finishes.
+    """
     dev = kv_pool.device
     _need(kv_pool, "kv_pool", torch.bfloat16, dev, (2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM))
     _need(q, "q", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
@@ -271,11 +276,12 @@ def paged_gqa_decode(q, kv_pool, block_tables, seq_lens, out, scale, workspace=N
             _ptr(seq_lens), S, int(max_seq_len), _ptr(out), float(scale), _ptr(workspace),
             workspace.numel(), _ptr(d_err), _stream(stream))
     if compute is None and not (min_units_per_warp or ctas_per_sm or stages or warps_per_cta
-                                or combine):
+                                or combine or schedule or early_kv):
         st = _L().paged_gqa_decode(*args)
     else:
         opts = DecodeOpts(COMPUTE_TENSOR if compute is None else compute,
-                          min_units_per_warp, ctas_per_sm, stages, warps_per_cta, combine)
+                          min_units_per_warp, ctas_per_sm, stages, warps_per_cta, combine,
+                          schedule, early_kv)
         st = _L().paged_gqa_decode_ex(*args, ctypes.byref(opts))
     _check(st, "paged_gqa_decode")
 
@@ -283,8 +289,12 @@ def paged_gqa_decode(q, kv_pool, block_tables, seq_lens, out, scale, workspace=N
 def paged_gqa_decode_append(q, k_new, v_new, kv_pool, block_tables, seq_lens, out, rope_cos,
                             rope_sin, scale, q_out=None, workspace=None, max_seq_len=None,
                             d_err=None, max_blocks=None, warps_per_cta=0, min_units_per_warp=0,
-                            ctas_per_sm=0, stream=None):
-    """One decode step: append each sequence's new token at seq_lens-1, then attend."""
+                            ctas_per_sm=0, schedule=0, early_kv=0, stream=None):
+    """One decode step: append each sequence's new token at seq_lens-1, then attend.
+
+    early_kv as for paged_gqa_decode (the pages meant are the ones this call
+    reads and appends to).
+    """
     dev = kv_pool.device
     _need(kv_pool, "kv_pool", torch.bfloat16, dev, (2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM))
     _need(q, "q", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
@@ -317,7 +327,8 @@ def paged_gqa_decode_append(q, k_new, v_new, kv_pool, block_tables, seq_lens, ou
     _need(workspace, "workspace", torch.uint8, dev)
     if d_err is not None:
         _need(d_err, "d_err", torch.int32, dev)
-    opts = DecodeOpts(COMPUTE_TENSOR, min_units_per_warp, ctas_per_sm, 0, warps_per_cta, 0)
+    opts = DecodeOpts(COMPUTE_TENSOR, min_units_per_warp, ctas_per_sm, 0, warps_per_cta, 0,
+                      schedule, early_kv)
     st = _L().paged_gqa_decode_append(
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(rope_cos), _ptr(rope_sin), rope_cos.shape[0],
         _ptr(kv_pool), kv_pool.shape[0], _ptr(block_tables), stride, mb, _ptr(seq_lens), S,
@@ -417,7 +428,11 @@ class DecodeStep:
     their contents in place (new K/V/q, positions, lengths, tables) and call
     run().  Replaying the graph removes the per-call host cost, and the
     kernels' programmatic-dependent-launch edges overlap each launch with
-    the previous kernel's tail.
+    the previous kernel's tail.  With overlap_layers (the default) the decode
+    kernel of layer l >= 1 also reads its tables and stages its first pages
+    before layer l - 1's kernel has finished (early_kv), which requires the
+    layers' block tables to name disjoint pages, as separate layers' caches
+    do.  Layer 0 always waits for whatever ran before the step.
 
         pool          [num_pages, 2, 8, 16, 64] bf16
         block_tables  [L, S, max_blocks] int32
@@ -427,7 +442,7 @@ class DecodeStep:
 
     def __init__(self, pool, block_tables, seq_lens, positions, k, v, q, out, rope_cos, rope_sin,
                  scale, max_seq_len=None, workspace=None, d_err=None, q_rot=None, compute=None,
-                 use_graph=True, stream=None, fused=True):
+                 use_graph=True, stream=None, fused=True, overlap_layers=True):
         self.L, self.S = block_tables.shape[0], block_tables.shape[1]
         self.t = dict(pool=pool, bt=block_tables, lens=seq_lens, pos=positions, k=k, v=v, q=q,
                       out=out, cos=rope_cos, sin=rope_sin)
@@ -438,6 +453,7 @@ class DecodeStep:
         self.scale = float(scale)
         self.max_seq_len = max_seq_len
         self.compute = compute
+        self.overlap = bool(overlap_layers)
         # the fused kernel places each new token at seq_lens - 1 (positions unused)
         self.fused = fused and compute in (None, COMPUTE_TENSOR)
         self.launches_per_step = (1 if self.fused else 2) * self.L
@@ -456,15 +472,18 @@ class DecodeStep:
                 paged_gqa_decode_append(t["q"][l], t["k"][l], t["v"][l], t["pool"], t["bt"][l],
                                         t["lens"], t["out"][l], t["cos"], t["sin"], self.scale,
                                         q_out=self.q_rot[l], workspace=self.workspace,
-                                        max_seq_len=self.max_seq_len, d_err=self.d_err)
+                                        max_seq_len=self.max_seq_len, d_err=self.d_err,
+                                        early_kv=int(self.overlap and l > 0))
             return
         for l in range(self.L):
             if not decode_only:
                 kv_append_rope(t["k"][l], t["v"][l], t["pos"], t["bt"][l], t["pool"], t["cos"],
                                t["sin"], q_in=t["q"][l], q_out=self.q_rot[l], d_err=self.d_err)
+            # after kv_append_rope of the same layer the pages are not ready early
             paged_gqa_decode(self.q_rot[l], t["pool"], t["bt"][l], t["lens"], t["out"][l],
                              self.scale, workspace=self.workspace, max_seq_len=self.max_seq_len,
-                             d_err=self.d_err, compute=self.compute)
+                             d_err=self.d_err, compute=self.compute,
+                             early_kv=int(self.overlap and decode_only and l > 0))
 
     def run(self):
         if self.graph is not None:

@@ -74,6 +74,10 @@ struct DecodeParams {
   uint16_t* q_out;                // [S][32][64] rotated q, or null
   uint16_t* pool;                 // the pool, writable (same memory as the TMA map)
   int max_pos;
+  // 1: block tables, lengths and K/V pages are not written by the previous
+  // kernel in the stream, so they are read (and the first pages staged)
+  // before waiting for it; everything else still waits.
+  int early;
 };
 
 // One (o, m, l) record: unnormalised o[4][64] and (m, l) for the 4 heads of a
@@ -160,14 +164,15 @@ __device__ __forceinline__ int seq_pages(int n, int max_len, bool* bad) {
   return (n + PKV_PAGE_TOKENS - 1) / PKV_PAGE_TOKENS;
 }
 
-// Block-wide exclusive prefix of pages over all sequences into prefix[0..S];
-// returns the number of sequences without pages (empty or invalid length).
+// Block-wide exclusive prefix of pages over all sequences into prefix[0..S]
+// and, if `nz` is given, of non-empty sequences into nz[0..S]; returns the
+// number of sequences without pages (empty or invalid length).
 template <int kWarps, bool kAppend>
-__device__ int build_prefix(const DecodeParams& p, int32_t* prefix) {
+__device__ int build_prefix(const DecodeParams& p, int32_t* prefix, int32_t* nz = nullptr) {
   // with a fused append the new token's position must also lie in the table
   const int max_len = kAppend ? min(PKV_PAGE_TOKENS * p.max_blocks, p.max_pos)
                               : PKV_PAGE_TOKENS * p.max_blocks;
-  __shared__ int warp_tot[kWarps];
+  __shared__ int warp_tot[kWarps], warp_nz[kWarps];
   __shared__ int n_empty;
   if (threadIdx.x == 0) n_empty = 0;
   const int S = p.num_seqs;
@@ -175,29 +180,48 @@ __device__ int build_prefix(const DecodeParams& p, int32_t* prefix) {
   const int per = (S + nthr - 1) / nthr;
   const int lo = threadIdx.x * per, hi = min(S, lo + per);
   bool bad = false;
-  int sum = 0;
-  for (int s = lo; s < hi; ++s) sum += seq_pages(__ldg(p.seq_lens + s), max_len, &bad);
+  int sum = 0, cnt = 0;
+  for (int s = lo; s < hi; ++s) {
+    const int np = seq_pages(__ldg(p.seq_lens + s), max_len, &bad);
+    sum += np;
+    cnt += (np > 0);
+  }
   if (bad && blockIdx.x == 0) report_error(p.d_err, PKV_ERR_DEVICE_INDEX);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = sum;
+  int incl = sum, incl_nz = cnt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
+    const int w = __shfl_up_sync(0xffffffffu, incl_nz, o);
+    if (lane >= o) {
+      incl += v;
+      incl_nz += w;
+    }
   }
-  if (lane == 31) warp_tot[warp] = incl;
+  if (lane == 31) {
+    warp_tot[warp] = incl;
+    warp_nz[warp] = incl_nz;
+  }
   __syncthreads();
-  int base = 0;
-  for (int w = 0; w < warp; ++w) base += warp_tot[w];
-  int run = base + incl - sum;
+  int base = 0, base_nz = 0;
+  for (int w = 0; w < warp; ++w) {
+    base += warp_tot[w];
+    base_nz += warp_nz[w];
+  }
+  int run = base + incl - sum, run_nz = base_nz + incl_nz - cnt;
   int empties = 0;
   for (int s = lo; s < hi; ++s) {
     prefix[s] = run;
+    if (nz) nz[s] = run_nz;
     const int np = seq_pages(__ldg(p.seq_lens + s), max_len, &bad);
     empties += (np == 0);
     run += np;
+    run_nz += (np > 0);
   }
-  if (threadIdx.x == nthr - 1) prefix[S] = run;
+  if (threadIdx.x == nthr - 1) {
+    prefix[S] = run;
+    if (nz) nz[S] = run_nz;
+  }
   if (empties) atomicAdd(&n_empty, empties);
   __syncthreads();
   return n_empty;
@@ -660,11 +684,11 @@ struct NewToken {
 // units, so the CTAs touching the segment are c0..c1, else each owns at most
 // one unit and the record of unit base + k comes from owner_of(base + k).
 // ---------------------------------------------------------------------------
-__device__ __noinline__ void cross_cta_merge(const DecodeParams& p, const MergeAcc& mine, int s,
-                                             int g, uint32_t base, uint32_t np, uint32_t U,
-                                             uint32_t NC, uint32_t c, int lane) {
+// Count this CTA's record of segment (s, g) in (it is already stored at
+// record 8s + g + c) and, if it is the last one, merge all of them.
+__device__ __noinline__ void cross_cta_arrive(const DecodeParams& p, int s, int g, uint32_t base,
+                                              uint32_t np, uint32_t U, uint32_t NC, int lane) {
   const uint32_t sg = 8u * (uint32_t)s + (uint32_t)g;
-  mine.store_record(global_record(p, sg + c), lane);
   if (p.combine_mode == 1) return;  // merged by the boundary kernel after this grid
   __threadfence();
   __syncwarp();
@@ -687,6 +711,13 @@ __device__ __noinline__ void cross_cta_merge(const DecodeParams& p, const MergeA
   if (lane == 0) p.ws_cnt[sg] = 0u;  // ready for the next call
 }
 
+__device__ __forceinline__ void cross_cta_merge(const DecodeParams& p, const MergeAcc& mine, int s,
+                                                int g, uint32_t base, uint32_t np, uint32_t U,
+                                                uint32_t NC, uint32_t c, int lane) {
+  mine.store_record(global_record(p, 8u * (uint32_t)s + (uint32_t)g + c), lane);
+  cross_cta_arrive(p, s, g, base, np, U, NC, lane);
+}
+
 // ---------------------------------------------------------------------------
 // The decode kernel.
 // ---------------------------------------------------------------------------
@@ -702,25 +733,11 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.num_seqs;
 
-  pdl_wait();
+  // Without `early` everything waits for the previous kernel here.  With it,
+  // only reads of q and the new token, and every global write, wait (below).
+  if (!p.early) pdl_wait();
   const int n_empty = build_prefix<kWarps, kAppend>(p, prefix);
-  if (p.combine_mode == 1 && blockIdx.x == 0)
-    for (int i = threadIdx.x; i <= S; i += blockDim.x) p.ws_prefix[i] = prefix[i];
   pdl_launch_dependents();
-  if (n_empty > 0) {
-    // Sequences without pages get a zero output (16-byte stores, grid-strided).
-    const uint32_t per_seq = PKV_NUM_Q_HEADS * 64 / 8;
-    const uint32_t total = (uint32_t)S * per_seq;
-    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += gridDim.x * blockDim.x) {
-      const int s = (int)(i / per_seq);
-      if (prefix[s + 1] == prefix[s]) {
-        reinterpret_cast<uint4*>(p.out)[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (kAppend && p.q_out != nullptr)
-          reinterpret_cast<uint4*>(p.q_out)[i] = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-  }
 
   const uint32_t U = 8u * (uint32_t)prefix[S];
   const uint32_t NC = gridDim.x, c = blockIdx.x;
@@ -779,6 +796,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
 
     for (int st = 0; st < kStages && iv < n_units; ++st) issue(st);
     __syncwarp();
+    if (p.early) pdl_wait();
 
     State st;
     Cursor cc;
@@ -848,6 +866,24 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
         (void)mbar_wait_bounded(bars + 8 * stage, (uint32_t)(u / kStages) & 1u, kWaitLimitNs);
       }
     }
+  } else if (p.early) {
+    pdl_wait();
+  }
+  if (p.combine_mode == 1 && blockIdx.x == 0)
+    for (int i = threadIdx.x; i <= S; i += blockDim.x) p.ws_prefix[i] = prefix[i];
+  if (n_empty > 0) {
+    // Sequences without pages get a zero output (16-byte stores, grid-strided).
+    const uint32_t per_seq = PKV_NUM_Q_HEADS * 64 / 8;
+    const uint32_t total = (uint32_t)S * per_seq;
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += gridDim.x * blockDim.x) {
+      const int s = (int)(i / per_seq);
+      if (prefix[s + 1] == prefix[s]) {
+        reinterpret_cast<uint4*>(p.out)[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (kAppend && p.q_out != nullptr)
+          reinterpret_cast<uint4*>(p.q_out)[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
   }
   __syncthreads();
 
@@ -881,6 +917,417 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
       else
         cross_cta_merge(p, m, cs.s, cs.g, base, (uint32_t)cs.np, U, NC, c, lane);
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Dynamic schedule.  One CTA per SM.  A producer warp streams the CTA's unit
+// range, in order, through a ring of kRing staged pages (the K and V tiles,
+// plus the new token's rows on the fused step's last pages), and
+// kDynConsumers warps take the staged units one at a time from a shared
+// counter, so the CTA's units go to whichever warp is free, however unevenly
+// the memory system serves them.
+//
+// A consumer keeps one online-softmax state while the units it takes stay in
+// one segment (s, g).  When it moves past the segment it stores it (it took
+// all of the CTA's units of that segment) or merges it, under a short lock,
+// into the segment's shared-memory accumulator; the contributor that brings
+// the accumulator's unit count to the CTA's count finalises it (store, or CTA
+// record + cross-CTA arrival) and hands the entry on to the segment kAcc
+// places later.  Entry e serves the CTA's segments e, e + kAcc, ... (counted
+// from the CTA's first segment) in that order -- a segment that one warp
+// covers alone takes its turn too -- so a merge only ever waits for an older
+// segment, and the oldest open segment never waits.
+//
+// Ring protocol (pos = position in the CTA's range, slot = pos % kRing,
+// round = pos / kRing):
+//   producer  wait empty[slot] phase round - 1 (pos >= kRing), write meta and
+//             seq[slot] = pos, arm full[slot] with the bytes, start the copies;
+//   consumer  claim pos, wait until seq[slot] == pos (so full[slot] is in
+//             phase `round`: a parity wait alone cannot tell round from
+//             round - 2), wait full[slot] phase round, compute, arrive on
+//             empty[slot].
+// ---------------------------------------------------------------------------
+constexpr int kDynConsumers = 15;
+constexpr int kRing = 32;
+constexpr int kAcc = 48;
+constexpr int kSideBytes = 512;  // k_new row, v_new row, cos row, sin row (128 B each)
+
+struct AccEntry {
+  float o[4][64];  // unnormalised output of query heads 4g..4g+3
+  float M[4], L[4];
+  int tag;   // local rank of the one segment that may merge here now
+  int done;  // units merged for it so far
+  int lock, bad;
+};
+
+struct DynSmem {
+  static constexpr int kThreads = (kDynConsumers + 1) * 32;
+  static constexpr int kTiles = kRing * kStageBytes;
+  static constexpr int kSide = kTiles;
+  static constexpr int kFull = kSide + kRing * kSideBytes;
+  static constexpr int kEmpty = kFull + kRing * 8;
+  static constexpr int kMeta = kEmpty + kRing * 8;
+  static constexpr int kSeq = kMeta + kRing * 16;
+  static constexpr int kAccOff = kSeq + kRing * 4;
+  static constexpr int kCtl = kAccOff + kAcc * (int)sizeof(AccEntry);
+  static constexpr int kPrefix = kCtl + 64;
+  static size_t bytes(int S) { return 1024 + kPrefix + 8 * (size_t)(S + 1); }
+};
+static_assert(DynSmem::kAccOff % 16 == 0 && sizeof(AccEntry) % 16 == 0, "float4 access");
+
+__device__ __forceinline__ void acc_clear(AccEntry& A, int lane) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) (&A.o[0][0])[lane + 32 * i] = 0.f;
+  if (lane < 4) {
+    A.M[lane] = -INFINITY;
+    A.L[lane] = 0.f;
+  }
+  if (lane == 0) {
+    A.done = 0;
+    A.bad = 0;
+  }
+}
+
+// Merge a consumer's state into a shared accumulator (caller holds the lock).
+__device__ __forceinline__ void mma_state_merge_into(const MmaState& st, AccEntry& A, bool bad,
+                                                     int lane) {
+  const int gq = lane >> 2, tig = lane & 3;
+  const float lt = st.total_l();
+  float Mold = 0.f, Lold = 0.f;
+  if (gq < 4) {
+    Mold = A.M[gq];
+    Lold = A.L[gq];
+  }
+  __syncwarp();
+  if (gq < 4) {
+    const float Mn = fmaxf(Mold, st.m);
+    const float a = (Mold == Mn) ? 1.f : exp2f(Mold - Mn);
+    const float b = (st.m == Mn) ? 1.f : exp2f(st.m - Mn);
+    float* dst = &A.o[gq][2 * tig];
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+      const float2 old = *reinterpret_cast<float2*>(dst + 8 * n);
+      *reinterpret_cast<float2*>(dst + 8 * n) =
+          make_float2(old.x * a + st.o[n][0] * b, old.y * a + st.o[n][1] * b);
+    }
+    if (tig == 0) {
+      A.M[gq] = Mn;
+      A.L[gq] = Lold * a + lt * b;
+    }
+  }
+  if (lane == 0 && bad) A.bad = 1;
+  __syncwarp();
+}
+
+template <bool kAppend>
+__global__ void __launch_bounds__(DynSmem::kThreads, 1)
+    paged_decode_dyn_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int S = p.num_seqs;
+  int32_t* prefix = reinterpret_cast<int32_t*>(smem + DynSmem::kPrefix);
+  int32_t* nz = prefix + (S + 1);
+  int* ctl = reinterpret_cast<int*>(smem + DynSmem::kCtl);  // [0] next claim, [1] error, [2] issued
+  volatile int* vctl = ctl;
+  volatile int* seqs = reinterpret_cast<volatile int*>(smem + DynSmem::kSeq);
+  AccEntry* acc = reinterpret_cast<AccEntry*>(smem + DynSmem::kAccOff);
+  int4* meta = reinterpret_cast<int4*>(smem + DynSmem::kMeta);
+  const uint32_t tiles = smem_u32(smem), side = smem_u32(smem + DynSmem::kSide);
+  const uint32_t full0 = smem_u32(smem + DynSmem::kFull), empty0 = smem_u32(smem + DynSmem::kEmpty);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // shared-memory set-up (touches nothing the previous kernel writes; made
+  // visible by the barriers inside build_prefix)
+  if (threadIdx.x < kRing) {
+    mbar_init(full0 + 8 * threadIdx.x, 1);
+    mbar_init(empty0 + 8 * threadIdx.x, 1);
+    seqs[threadIdx.x] = -1;
+    fence_mbar_init();
+  }
+  for (int e = warp; e < kAcc; e += kDynConsumers + 1) {
+    acc_clear(acc[e], lane);
+    if (lane == 0) {
+      acc[e].tag = e;
+      acc[e].lock = 0;
+    }
+  }
+  if (threadIdx.x == 0) ctl[0] = ctl[1] = ctl[2] = 0;
+
+  pdl_wait();
+  const int n_empty = build_prefix<kDynConsumers + 1, kAppend>(p, prefix, nz);
+  pdl_launch_dependents();
+  if (n_empty > 0) {
+    const uint32_t per_seq = PKV_NUM_Q_HEADS * 64 / 8;
+    const uint32_t total = (uint32_t)S * per_seq;
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += gridDim.x * blockDim.x) {
+      const int s = (int)(i / per_seq);
+      if (prefix[s + 1] == prefix[s]) {
+        reinterpret_cast<uint4*>(p.out)[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (kAppend && p.q_out != nullptr)
+          reinterpret_cast<uint4*>(p.q_out)[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  }
+  const uint32_t U = 8u * (uint32_t)prefix[S];
+  const uint32_t NC = gridDim.x, c = blockIdx.x;
+  const uint32_t a = range_start(c, U, NC), b = range_start(c + 1, U, NC);
+  const int n = (int)(b - a);
+
+  if (warp == 0) {
+    // ---------------- producer ---------------------------------------------
+    auto unit_meta = [&](int pos) -> int4 {
+      if (pos >= n) return make_int4(-1, 0, -1, 0);
+      Cursor cu;
+      cursor_seek(cu, a + (uint32_t)pos, prefix, S);
+      int pid = __ldg(p.block_tables + (size_t)cu.s * p.bt_stride + cu.j);
+      if (pid < 0 || pid >= p.num_pages) pid = -1;
+      return make_int4(cu.s, cu.g | (cu.j << 3), pid, __ldg(p.seq_lens + cu.s));
+    };
+    int4 cur = unit_meta(lane), nxt = unit_meta(32 + lane);
+    bool stop = false;
+    int issued = 0;
+    for (int batch = 0; batch < n && !stop; batch += 32) {
+      for (int grp = 0; grp < 32 && batch + grp < n; grp += 8) {
+        const int pos = batch + lane;
+        const bool mine = lane >= grp && lane < grp + 8 && pos < n;
+        const int slot = lane;  // pos % kRing
+        bool ok = vctl[1] == 0;
+        if (ok && mine && pos >= kRing)
+          ok = mbar_wait_bounded(empty0 + 8 * slot, (uint32_t)(pos / kRing - 1) & 1u, kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (lane == 0 && vctl[1] == 0) {
+            atomicOr(ctl + 1, 1);
+            report_error(p.d_err, PKV_ERR_TIMEOUT);
+          }
+          stop = true;
+          break;
+        }
+        if (mine) {
+          meta[slot] = cur;
+          seqs[slot] = pos;
+          const uint32_t bar = full0 + 8 * slot;
+          if (cur.z >= 0) {
+            const int g = cur.y & 7, j = cur.y >> 3, len = cur.w;
+            const bool last = kAppend && j == (len - 1) / PKV_PAGE_TOKENS;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar, kStageBytes + (last ? kSideBytes : 0));
+            const uint32_t dst = tiles + slot * kStageBytes;
+            tma_load_3d(dst, &tmap, 0, 0, (cur.z * 2 + 0) * PKV_NUM_KV_HEADS + g, bar);
+            tma_load_3d(dst + kTileBytes, &tmap, 0, 0, (cur.z * 2 + 1) * PKV_NUM_KV_HEADS + g, bar);
+            if (last) {
+              const uint32_t sd = side + slot * kSideBytes;
+              const size_t row = ((size_t)cur.x * PKV_NUM_KV_HEADS + g) * 64;
+              bulk_load(sd, p.k_new + row, 128, bar);
+              bulk_load(sd + 128, p.v_new + row, 128, bar);
+              bulk_load(sd + 256, p.rope_cos + (size_t)(len - 1) * PKV_ROPE_PAIRS, 128, bar);
+              bulk_load(sd + 384, p.rope_sin + (size_t)(len - 1) * PKV_ROPE_PAIRS, 128, bar);
+            }
+          } else {
+            mbar_arrive(bar);
+          }
+        }
+        __syncwarp();
+        issued = min(n, batch + grp + 8);
+      }
+      cur = nxt;
+      nxt = unit_meta(batch + 64 + lane);
+    }
+    if (lane == 0) ctl[2] = issued;
+  } else {
+    // ---------------- consumers --------------------------------------------
+    MmaState st;
+    st.reset();
+    int cs = 0, cg = 0, clen = 0, m_units = 0, seg_last = -1, lrank = 0, rank0 = 0;
+    uint32_t sbase = 0, snp = 1;
+    bool seg_bad = false, failed = false;
+    if (n > 0) {
+      Cursor cu;
+      cursor_seek(cu, a, prefix, S);
+      rank0 = 8 * nz[cu.s] + cu.g;
+    }
+    auto give_up = [&]() {
+      if (lane == 0 && vctl[1] == 0) {
+        atomicOr(ctl + 1, 1);
+        report_error(p.d_err, PKV_ERR_TIMEOUT);
+      }
+      failed = true;
+    };
+
+    // Leave the current segment; false if a bounded wait gave up.
+    auto flush = [&]() -> bool {
+      if (m_units == 0) return true;
+      const uint32_t last = sbase + snp - 1;
+      const int n_x = (int)(min(last, b - 1) - max(sbase, a) + 1);
+      const bool inside = sbase >= a && last < b;
+      const int units = m_units;
+      const bool bad = seg_bad;
+      m_units = 0;
+      seg_bad = false;
+      AccEntry& A = acc[lrank % kAcc];
+      int got = 0;
+      if (units == n_x) {
+        // this warp took every unit the CTA has of the segment: no merge, but
+        // the entry still passes through this segment's turn, in order
+        if (lane == 0) {
+          volatile int* tag = &A.tag;
+          const uint64_t t0 = global_timer_ns();
+          for (;;) {
+            if (*tag == lrank) {
+              got = 1;
+              break;
+            }
+            if (global_timer_ns() - t0 > kWaitLimitNs) break;
+            __nanosleep(32);
+          }
+          if (got) *tag = lrank + kAcc;
+        }
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (got) {
+          if (inside) {
+            st.write_output(p, cs, cg, bad, lane);
+          } else {
+            st.write_record(global_record(p, 8u * (uint32_t)cs + (uint32_t)cg + c), bad, lane);
+            cross_cta_arrive(p, cs, cg, sbase, snp, U, NC, lane);
+          }
+        }
+        st.reset();
+        return got != 0;
+      }
+      if (lane == 0) {  // the lock, held only while this segment owns the entry
+        const uint64_t t0 = global_timer_ns();
+        for (;;) {
+          if (atomicCAS(&A.lock, 0, 1) == 0) {
+            __threadfence_block();
+            if (*reinterpret_cast<volatile int*>(&A.tag) == lrank) {
+              got = 1;
+              break;
+            }
+            atomicExch(&A.lock, 0);
+          }
+          if (global_timer_ns() - t0 > kWaitLimitNs) break;
+          __nanosleep(32);
+        }
+      }
+      got = __shfl_sync(0xffffffffu, got, 0);
+      __syncwarp();
+      if (!got) {
+        st.reset();
+        return false;
+      }
+      mma_state_merge_into(st, A, bad, lane);
+      st.reset();
+      int complete = 0;
+      if (lane == 0) {
+        A.done += units;
+        complete = A.done == n_x;
+      }
+      complete = __shfl_sync(0xffffffffu, complete, 0);
+      MergeAcc t;
+      if (complete) {  // take the result, then hand the entry on
+        const int hh = lane >> 3, d0 = (lane & 7) * 8;
+        const float4* src = reinterpret_cast<const float4*>(&A.o[hh][d0]);
+        const float4 o0 = src[0], o1 = src[1];
+        t.acc[0] = o0.x; t.acc[1] = o0.y; t.acc[2] = o0.z; t.acc[3] = o0.w;
+        t.acc[4] = o1.x; t.acc[5] = o1.y; t.acc[6] = o1.z; t.acc[7] = o1.w;
+        t.M = A.M[hh];
+        t.L = A.L[hh];
+        t.bad = A.bad != 0;
+        __syncwarp();
+        acc_clear(A, lane);
+        if (lane == 0) A.tag = lrank + kAcc;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        atomicExch(&A.lock, 0);
+      }
+      if (complete) {
+        if (inside) {
+          t.store_output(p, cs, cg, lane);
+        } else {
+          t.store_record(global_record(p, 8u * (uint32_t)cs + (uint32_t)cg + c), lane);
+          cross_cta_arrive(p, cs, cg, sbase, snp, U, NC, lane);
+        }
+      }
+      return true;
+    };
+
+    for (;;) {
+      int pos = 0;
+      if (lane == 0) pos = atomicAdd(ctl, 1);
+      pos = __shfl_sync(0xffffffffu, pos, 0);
+      if (pos >= n || vctl[1] != 0) break;
+      const bool fresh = pos > seg_last;  // past the held segment
+      if (fresh && !flush()) {
+        give_up();
+        break;
+      }
+      const int slot = pos % kRing;
+      int ok = 1;
+      if (lane == 0 && seqs[slot] != pos) {
+        const uint64_t t0 = global_timer_ns();
+        while (seqs[slot] != pos) {
+          if (vctl[1] != 0 || global_timer_ns() - t0 > kWaitLimitNs) {
+            ok = 0;
+            break;
+          }
+          __nanosleep(20);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      __syncwarp();
+      if (ok) ok = mbar_wait_bounded(full0 + 8 * slot, (uint32_t)(pos / kRing) & 1u, kWaitLimitNs);
+      if (!__all_sync(0xffffffffu, ok)) {
+        give_up();
+        break;
+      }
+      const int4 mt = meta[slot];
+      const int s = mt.x, g = mt.y & 7, j = mt.y >> 3, pid = mt.z, len = mt.w;
+      if (fresh) {
+        cs = s;
+        cg = g;
+        clen = len;
+        snp = (uint32_t)(prefix[s + 1] - prefix[s]);
+        sbase = 8u * (uint32_t)prefix[s] + (uint32_t)g * snp;
+        seg_last = (int)(min(sbase + snp - 1, b - 1) - a);
+        lrank = 8 * nz[s] + g - rank0;
+        st.template load_q<kAppend>(p, s, g, len - 1, j == 0, lane);
+      }
+      if (pid >= 0) {
+        const int valid = min(PKV_PAGE_TOKENS, clen - PKV_PAGE_TOKENS * j);
+        const uint32_t sK = tiles + slot * kStageBytes;
+        if (kAppend && j == (clen - 1) / PKV_PAGE_TOKENS) {
+          // the new token: rows staged by the producer next to the tiles
+          const uint8_t* sd = smem + DynSmem::kSide + slot * kSideBytes;
+          NewToken tok;
+          tok.k0 = reinterpret_cast<const uint16_t*>(sd)[lane];
+          tok.k1 = reinterpret_cast<const uint16_t*>(sd)[lane + 32];
+          tok.v = reinterpret_cast<const uint32_t*>(sd + 128)[lane];
+          tok.c = reinterpret_cast<const float*>(sd + 256)[lane];
+          tok.s = reinterpret_cast<const float*>(sd + 384)[lane];
+          tok.insert(p, sK, sK + kTileBytes, pid, g, (clen - 1) % PKV_PAGE_TOKENS, lane);
+          __syncwarp();
+        }
+        st.page(sK, sK + kTileBytes, valid, p.sl2, lane);
+      } else {
+        seg_bad = true;
+        if (lane == 0) report_error(p.d_err, PKV_ERR_DEVICE_INDEX);
+      }
+      ++m_units;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+    }
+    if (!failed && !flush()) give_up();
+  }
+  __syncthreads();
+  if (warp == 0 && vctl[1] != 0) {
+    // after a timeout: wait (bounded) for every copy still in flight
+    const int issued = ctl[2];
+    for (int pos = max(0, issued - kRing) + lane; pos < issued; pos += 32)
+      (void)mbar_wait_bounded(full0 + 8 * (pos % kRing), (uint32_t)(pos / kRing) & 1u, kWaitLimitNs);
   }
 }
 
@@ -1076,6 +1523,50 @@ static int launch_decode(const DecodeParams& prm, const CUtensorMap& map, int de
   return cuda_status(e, "cudaLaunchKernelEx(boundary)");
 }
 
+template <bool kAppend>
+static int launch_decode_dyn(const DecodeParams& prm, const CUtensorMap& map, int device,
+                             int num_sms, int max_seq_len, int min_units, cudaStream_t stream) {
+  static std::mutex mu;
+  static int max_dyn[64] = {0};
+  auto kern = paged_decode_dyn_kernel<kAppend>;
+  const size_t smem = DynSmem::bytes(prm.num_seqs);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (device < 0 || device >= 64) return PKV_ERR_CUDA;
+    if (max_dyn[device] == 0) {
+      int optin = 0;
+      cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+      if (e != cudaSuccess) return cuda_status(e, "cudaDeviceGetAttribute(smem optin)");
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return cuda_status(e, "cudaFuncGetAttributes(dyn)");
+      const int m = optin - (int)fa.sharedSizeBytes;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, m);
+      if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(dyn)");
+      max_dyn[device] = m;
+    }
+    if ((long long)smem > max_dyn[device]) return PKV_ERR_UNSUPPORTED_SHAPE;
+  }
+  const long long pages_bound = max_seq_len > 0 ? (max_seq_len + 15) / 16 : 0;
+  const long long u_bound = 8ll * prm.num_seqs * pages_bound;
+  long long nc = num_sms;
+  const long long per = (long long)kDynConsumers * min_units;
+  const long long want = (u_bound + per - 1) / per;
+  if (want < nc) nc = want;
+  if (nc < 1) nc = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)nc);
+  cfg.blockDim = dim3(DynSmem::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, map, prm), "cudaLaunchKernelEx(dyn)");
+}
+
 }  // namespace pkv
 
 using namespace pkv;
@@ -1121,9 +1612,8 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   if (app) {
     if (!app->k_new || !app->v_new || !app->rope_cos || !app->rope_sin || app->max_pos < 1)
       return PKV_ERR_INVALID_ARGUMENT;
-    if (((reinterpret_cast<uintptr_t>(app->k_new) | reinterpret_cast<uintptr_t>(app->v_new) |
-          reinterpret_cast<uintptr_t>(app->rope_cos) | reinterpret_cast<uintptr_t>(app->rope_sin)) & 7u) ||
-        !aligned16(app->q_out))
+    if (!aligned16(app->k_new) || !aligned16(app->v_new) || !aligned16(app->rope_cos) ||
+        !aligned16(app->rope_sin) || !aligned16(app->q_out))
       return PKV_ERR_MISALIGNED;
   }
   if (num_seqs > kMaxSeqs || (long long)num_pages * 16 * 8 * 2 >= (1ll << 31) ||
@@ -1170,6 +1660,7 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   prm.ws_cnt = reinterpret_cast<uint32_t*>(ws + wl.cnt);
   prm.ws_prefix = reinterpret_cast<int32_t*>(ws + wl.prefix);
   prm.combine_mode = (opts && opts->combine == 1) ? 1 : 0;
+  prm.early = (opts && opts->early_kv == 1) ? 1 : 0;
   prm.ws_ml = reinterpret_cast<float2*>(ws + wl.ml);
   prm.ws_o = reinterpret_cast<float*>(ws + wl.o);
   if (app) {
@@ -1184,6 +1675,12 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int ms = max_seq_len;
+  const int schedule = opts ? opts->schedule : 0;
+  if (schedule == 1 && compute == PKV_COMPUTE_TENSOR && prm.combine_mode == 0) {
+    const int rc2 = app ? launch_decode_dyn<true>(prm, map, dev, sms, ms, min_units, st)
+                        : launch_decode_dyn<false>(prm, map, dev, sms, ms, min_units, st);
+    if (rc2 != PKV_ERR_UNSUPPORTED_SHAPE) return rc2;  // too many sequences: static schedule
+  }
   if (app) {
     switch (cfg) {
       case 802: return launch_decode<MmaState, 8, 2, true>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);

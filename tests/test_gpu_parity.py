@@ -243,7 +243,10 @@ def test_decode_mixed_batch8(lib, cuda_device, compute):
                                   dict(warps_per_cta=4, stages=2, min_units_per_warp=1),
                                   dict(warps_per_cta=16, stages=3), dict(combine=1),
                                   dict(combine=1, warps_per_cta=4, stages=2, min_units_per_warp=1),
-                                  dict(combine=1, ctas_per_sm=1, min_units_per_warp=1)])
+                                  dict(combine=1, ctas_per_sm=1, min_units_per_warp=1),
+                                  dict(schedule=1), dict(schedule=1, min_units_per_warp=1),
+                                  dict(early_kv=1), dict(early_kv=1, max_seq_len=2048),
+                                  dict(schedule=1, max_seq_len=2048)])
 def test_decode_work_split_variants(lib, cuda_device, opts):
     """Different warp counts (including more warps than units) give the same answer."""
     case = make_case([3, 40, 17, 700, 1, 129, 2048, 16], seed=9, extra_pages=5)
@@ -258,7 +261,7 @@ def test_decode_work_split_variants(lib, cuda_device, opts):
 
 # ------------------------------------------------- full-size, sampled -------
 
-def full_size_step_check(lib, dev, case, samples, tables, fused=True):
+def full_size_step_check(lib, dev, case, samples, tables, fused=True, schedule=0):
     """Run one bench-shaped step (append new token with q rotation, then decode,
     on every layer; fused into one call or as two calls) and compare sampled
     (layer, seq) outputs with the oracle."""
@@ -283,12 +286,13 @@ def full_size_step_check(lib, dev, case, samples, tables, fused=True):
         if fused:
             lib.paged_gqa_decode_append(q_raw[l], k_new[l], v_new[l], pool, bt_all[l], lens, out[l],
                                         cos_d, sin_d, case.scale, q_out=q_rot[l], workspace=ws,
-                                        max_seq_len=case.max_seq_len, d_err=err)
+                                        max_seq_len=case.max_seq_len, d_err=err, schedule=schedule)
         else:
             lib.kv_append_rope(k_new[l], v_new[l], posd, bt_all[l], pool, cos_d, sin_d,
                                q_in=q_raw[l], q_out=q_rot[l], d_err=err)
             lib.paged_gqa_decode(q_rot[l], pool, bt_all[l], lens, out[l], case.scale,
-                                 workspace=ws, max_seq_len=case.max_seq_len, d_err=err)
+                                 workspace=ws, max_seq_len=case.max_seq_len, d_err=err,
+                                 schedule=schedule)
     assert lib.pkv_read_device_error(err) == 0
     worst = 0.0
     for (l, s) in samples:
@@ -310,17 +314,18 @@ def full_size_step_check(lib, dev, case, samples, tables, fused=True):
     return worst
 
 
-@pytest.mark.parametrize("fused", [True, False])
-def test_full_size_batch32_sampled(lib, cuda_device, tables, fused):
+@pytest.mark.parametrize("fused,schedule", [(True, 0), (False, 0), (True, 1), (False, 1)])
+def test_full_size_batch32_sampled(lib, cuda_device, tables, fused, schedule):
     case = W.case_batch32()
     samples = [(0, 0), (0, 31), (7, 13), (15, 5), (15, 31)]
-    full_size_step_check(lib, cuda_device, case, samples, tables, fused=fused)
+    full_size_step_check(lib, cuda_device, case, samples, tables, fused=fused, schedule=schedule)
 
 
-def test_full_size_stress256_sampled(lib, cuda_device, tables):
+@pytest.mark.parametrize("schedule", [0, 1])
+def test_full_size_stress256_sampled(lib, cuda_device, tables, schedule):
     case = W.case_stress()
     samples = [(0, 0), (3, 200), (9, 77), (15, 255)]
-    full_size_step_check(lib, cuda_device, case, samples, tables)
+    full_size_step_check(lib, cuda_device, case, samples, tables, schedule=schedule)
     torch.cuda.empty_cache()
 
 
@@ -392,8 +397,8 @@ def fused_case(lens, seed, layers=2):
     return W.DecodeCase(case.name, seed, L, case.seq_lens, N * L, tables)
 
 
-@pytest.mark.parametrize("warps", [0, 8, 4])
-def test_fused_append_decode_matches_oracle(lib, cuda_device, tables, warps):
+@pytest.mark.parametrize("warps,schedule", [(0, 0), (8, 0), (4, 0), (0, 1)])
+def test_fused_append_decode_matches_oracle(lib, cuda_device, tables, warps, schedule):
     cos_d, sin_d, cos_o, sin_o = tables
     case = fused_case([1, 16, 17, 0, 2048, 333, 1500, 2], seed=41)
     dev = cuda_device
@@ -409,7 +414,7 @@ def test_fused_append_decode_matches_oracle(lib, cuda_device, tables, warps):
         lib.paged_gqa_decode_append(q[l].to(dev), k[l].to(dev), v[l].to(dev), pool,
                                     torch.from_numpy(case.block_tables[l]).to(dev), lens, out[l],
                                     cos_d, sin_d, case.scale, q_out=q_out[l], d_err=err,
-                                    warps_per_cta=warps, max_seq_len=2048)
+                                    warps_per_cta=warps, max_seq_len=2048, schedule=schedule)
     assert lib.pkv_read_device_error(err) == 0
     want_pool = bits(pool0)
     for l in range(case.num_layers):
@@ -422,8 +427,9 @@ def test_fused_append_decode_matches_oracle(lib, cuda_device, tables, warps):
     assert np.array_equal(bits(pool), want_pool)
 
 
+@pytest.mark.parametrize("schedule", [0, 1])
 @pytest.mark.parametrize("bad", ["last_page", "middle_page", "past_table"])
-def test_fused_append_decode_error_contract(lib, cuda_device, tables, bad):
+def test_fused_append_decode_error_contract(lib, cuda_device, tables, bad, schedule):
     cos_d, sin_d, cos_o, sin_o = tables
     case = fused_case([40, 70, 17], seed=43, layers=1)
     dev = cuda_device
@@ -445,7 +451,7 @@ def test_fused_append_decode_error_contract(lib, cuda_device, tables, bad):
     lib.paged_gqa_decode_append(q[0].to(dev), k[0].to(dev), v[0].to(dev), pool,
                                 torch.from_numpy(bt).to(dev), torch.from_numpy(lens).to(dev), out,
                                 cos_d[:64].contiguous(), sin_d[:64].contiguous(), case.scale,
-                                q_out=q_out, d_err=err)
+                                q_out=q_out, d_err=err, schedule=schedule)
     assert lib.pkv_read_device_error(err) == lib.ERR_DEVICE_INDEX
     want_pool, want_q, ref, e = OP.decode_step(bits(pool0), bits(q[0]), bits(k[0]), bits(v[0]),
                                                bt, lens, cos_o[:64], sin_o[:64], case.scale)
