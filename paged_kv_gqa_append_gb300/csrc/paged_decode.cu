@@ -32,6 +32,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
+#include <algorithm>
 #include <mutex>
 #include <stdint.h>
 #include <stdio.h>
@@ -317,7 +318,7 @@ struct MmaState {
   // at most 128 registers per thread: 16 warps of work per SM
   __host__ __device__ static constexpr int min_blocks(int warps) { return warps >= 16 ? 1 : 16 / warps; }
   uint32_t qa[4][2];  // Q A-fragments per 16-dim chunk: (row gq, k 2tig..) and (k 8+2tig..)
-  float o[8][4];      // O accumulators per 8-dim tile
+  float o[8][2];      // O accumulators per 8-dim tile (row lane/4; rows 8..15 are padding)
   float m, l;         // running max (log2 units) and per-lane partial denominator
 
   // Q fragments of query heads 4g..4g+3.  With kAppend the query is rotated
@@ -326,25 +327,36 @@ struct MmaState {
   template <bool kAppend>
   __device__ __forceinline__ void load_q(const DecodeParams& p, int s, int g, int pos,
                                          bool write_q, int lane) {
+    const size_t row0 = ((size_t)s * PKV_NUM_Q_HEADS + g * 4) * 64;
+    load_q_rows<kAppend, false>(p, p.q + row0, p.rope_cos + (size_t)pos * PKV_ROPE_PAIRS,
+                                p.rope_sin + (size_t)pos * PKV_ROPE_PAIRS, row0, write_q, lane);
+  }
+
+  // The same from rows at `qsrc` (4 heads x 64, global or, with kStaged,
+  // shared memory) and the cos/sin rows `cr`, `sr` of the new position;
+  // q_out rows start at element `row0`.
+  template <bool kAppend, bool kStaged>
+  __device__ __forceinline__ void load_q_rows(const DecodeParams& p, const uint16_t* qsrc,
+                                              const float* cr, const float* sr, size_t row0,
+                                              bool write_q, int lane) {
     const int gq = lane >> 2, tig = lane & 3;
     if (gq < 4) {
-      const size_t row = ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + gq) * 64;
-      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + row);
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qsrc + gq * 64);
 #pragma unroll
       for (int kc = 0; kc < 4; ++kc) {
-        qa[kc][0] = __ldg(qrow + kc * 8 + tig);
-        qa[kc][1] = __ldg(qrow + kc * 8 + 4 + tig);
+        qa[kc][0] = kStaged ? qrow[kc * 8 + tig] : __ldg(qrow + kc * 8 + tig);
+        qa[kc][1] = kStaged ? qrow[kc * 8 + 4 + tig] : __ldg(qrow + kc * 8 + 4 + tig);
       }
       if (kAppend) {
-        const float* cr = p.rope_cos + (size_t)pos * PKV_ROPE_PAIRS;
-        const float* sr = p.rope_sin + (size_t)pos * PKV_ROPE_PAIRS;
 #pragma unroll
         for (int kc = 0; kc < 2; ++kc) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int d = 16 * kc + 8 * h + 2 * tig;
-            const float2 c = __ldg(reinterpret_cast<const float2*>(cr + d));
-            const float2 sn = __ldg(reinterpret_cast<const float2*>(sr + d));
+            const float2* cp = reinterpret_cast<const float2*>(cr + d);
+            const float2* sp = reinterpret_cast<const float2*>(sr + d);
+            const float2 c = kStaged ? *cp : __ldg(cp);
+            const float2 sn = kStaged ? *sp : __ldg(sp);
             const uint32_t lo = qa[kc][h], hi = qa[kc + 2][h];
             uint16_t a0, b0, a1, b1;
             rope_pair((uint16_t)(lo & 0xFFFFu), (uint16_t)(hi & 0xFFFFu), c.x, sn.x, a0, b0);
@@ -354,7 +366,7 @@ struct MmaState {
           }
         }
         if (write_q && p.q_out != nullptr) {
-          uint32_t* qo = reinterpret_cast<uint32_t*>(p.q_out + row);
+          uint32_t* qo = reinterpret_cast<uint32_t*>(p.q_out + row0 + gq * 64);
 #pragma unroll
           for (int kc = 0; kc < 4; ++kc) {
             qo[kc * 8 + tig] = qa[kc][0];
@@ -370,7 +382,7 @@ struct MmaState {
 
   __device__ __forceinline__ void reset() {
 #pragma unroll
-    for (int n = 0; n < 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    for (int n = 0; n < 8; ++n) o[n][0] = o[n][1] = 0.f;
     m = -INFINITY;
     l = 0.f;
   }
@@ -378,7 +390,7 @@ struct MmaState {
   __device__ __forceinline__ void page(uint32_t sK, uint32_t sV, int valid, float sl2, int lane) {
     const int tig = lane & 3, mi = lane >> 3, r = lane & 7;
     // ---- S = Q K^T -------------------------------------------------------
-    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+    float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
     const uint32_t krow = sK + (uint32_t)((8 * (mi >> 1) + r) * 128);
 #pragma unroll
     for (int kc = 0; kc < 4; ++kc) {
@@ -921,143 +933,429 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
 }
 
 // ---------------------------------------------------------------------------
-// Dynamic schedule.  One CTA per SM.  A producer warp streams the CTA's unit
-// range, in order, through a ring of kRing staged pages (the K and V tiles,
-// plus the new token's rows on the fused step's last pages), and
-// kDynConsumers warps take the staged units one at a time from a shared
-// counter, so the CTA's units go to whichever warp is free, however unevenly
-// the memory system serves them.
+// Dynamic schedule (opts.schedule = 1).  CTA c owns the unit range [a, b) as
+// in the static schedule, but its warps take units one at a time from a
+// shared counter, each through its own two-stage TMA pipeline, instead of
+// fixed sub-ranges: the warps of a CTA finish together however unevenly
+// memory serves them.  Units are taken in this order: the part of the
+// segment that began in the previous CTA (block F), the part of the segment
+// that runs on into the next CTA (block E), then the inner segments.  The
+// records of the two shared segments are therefore complete, and merged
+// across CTAs, while the inner segments still stream.
 //
-// A consumer keeps one online-softmax state while the units it takes stay in
-// one segment (s, g).  When it moves past the segment it stores it (it took
-// all of the CTA's units of that segment) or merges it, under a short lock,
-// into the segment's shared-memory accumulator; the contributor that brings
-// the accumulator's unit count to the CTA's count finalises it (store, or CTA
-// record + cross-CTA arrival) and hands the entry on to the segment kAcc
-// places later.  Entry e serves the CTA's segments e, e + kAcc, ... (counted
-// from the CTA's first segment) in that order -- a segment that one warp
-// covers alone takes its turn too -- so a merge only ever waits for an older
-// segment, and the oldest open segment never waits.
+// A warp keeps one online-softmax state while the units it takes stay in one
+// segment.  When it moves on it stores the segment (it took all of the CTA's
+// units of it) or writes its (o, m, l) record into one of its two
+// shared-memory record slots and counts it in with one 64-bit atomic add on
+// the segment's word (units in the low half, the slot's bit in the high
+// half); the record that completes the count makes its writer merge every
+// listed record, free their slots and finalise the segment (store, or record
+// + cross-CTA arrival).  No warp waits for another's merge.  Word e serves
+// the segments of order e, e + kSeg, ... in turn -- a segment one warp
+// covers alone takes its turn too -- and a slot is reused only once its last
+// record has been merged, so a warp only ever waits for an older segment,
+// and the oldest open segment never waits.
 //
-// Ring protocol (pos = position in the CTA's range, slot = pos % kRing,
-// round = pos / kRing):
-//   producer  wait empty[slot] phase round - 1 (pos >= kRing), write meta and
-//             seq[slot] = pos, arm full[slot] with the bytes, start the copies;
-//   consumer  claim pos, wait until seq[slot] == pos (so full[slot] is in
-//             phase `round`: a parity wait alone cannot tell round from
-//             round - 2), wait full[slot] phase round, compute, arrive on
-//             empty[slot].
+// Warps claim chunks of consecutive units, large first and shrinking to single
+// units at the end (guided self-scheduling: remaining / (2 x warps)), so a
+// segment gets few contributors and the CTA still ends evenly.  Per warp and
+// stage one mbarrier covers the K and V tiles (TMA), the q rows of the KV
+// group when the unit starts a new segment for that warp, and, for the fused
+// append, the cos/sin rows of the new position and (on the page that
+// receives it) the new token's K and V rows.  Page ids and (s, g) of the
+// CTA's units are resolved once, into shared memory, before the pipeline
+// starts.
 // ---------------------------------------------------------------------------
-constexpr int kDynConsumers = 15;
-constexpr int kRing = 32;
-constexpr int kAcc = 48;
-constexpr int kSideBytes = 512;  // k_new row, v_new row, cos row, sin row (128 B each)
+constexpr int kDynWarps = 16;
+constexpr int kDynStages = 2;
+constexpr int kSeg = 64;  // segment words, reused in segment order
+// staged rows per warp and stage: q (4 heads, 512 B) | k_new | v_new | cos | sin
+constexpr int kSideQ = 0, kSideK = 512, kSideV = 640, kSideCos = 768, kSideSin = 896;
+constexpr int kSideBytes = 1024;
 
-struct AccEntry {
-  float o[4][64];  // unnormalised output of query heads 4g..4g+3
-  float M[4], L[4];
-  int tag;   // local rank of the one segment that may merge here now
-  int done;  // units merged for it so far
-  int lock, bad;
+struct SegWord {
+  unsigned long long word;  // units counted in (low 32 bits) | record-slot bits (high 32)
+  int tag;                  // order of the one segment that may use the word now
+  int pad;
 };
 
 struct DynSmem {
-  static constexpr int kThreads = (kDynConsumers + 1) * 32;
-  static constexpr int kTiles = kRing * kStageBytes;
-  static constexpr int kSide = kTiles;
-  static constexpr int kFull = kSide + kRing * kSideBytes;
-  static constexpr int kEmpty = kFull + kRing * 8;
-  static constexpr int kMeta = kEmpty + kRing * 8;
-  static constexpr int kSeq = kMeta + kRing * 16;
-  static constexpr int kAccOff = kSeq + kRing * 4;
-  static constexpr int kCtl = kAccOff + kAcc * (int)sizeof(AccEntry);
-  static constexpr int kPrefix = kCtl + 64;
-  static size_t bytes(int S) { return 1024 + kPrefix + 8 * (size_t)(S + 1); }
+  static constexpr int kThreads = kDynWarps * 32;
+  static constexpr int kSlots = kDynWarps * kDynStages;
+  static constexpr int kSide = kSlots * kStageBytes;  // tiles first (1024-aligned)
+  static constexpr int kBars = kSide + kSlots * kSideBytes;
+  static constexpr int kMeta = kBars + kSlots * 8;
+  static constexpr int kRecs = kMeta + kSlots * 16;             // Record [2][kDynWarps]
+  static constexpr int kBusy = kRecs + 2 * kDynWarps * kRecordBytes;  // int [2 kDynWarps]
+  static constexpr int kSegs = kBusy + 2 * kDynWarps * 4;
+  static constexpr int kCtl = kSegs + kSeg * (int)sizeof(SegWord);
+  static constexpr int kPrefix = kCtl + 64;  // prefix[S + 1] | nz[S + 1] | len[S]
+  __host__ __device__ static size_t table_off(int S) { return ((size_t)kPrefix + 4 * (3 * (size_t)S + 2) + 15) & ~(size_t)15; }
+  __host__ __device__ static size_t bytes(int S, int n_cap) { return 1024 + table_off(S) + 8 * (size_t)n_cap; }
+  // record slot `bit` = warp + kDynWarps * slot
+  __device__ static Record rec(uint8_t* smem, int bit) {
+    uint8_t* base = smem + kRecs + bit * kRecordBytes;
+    return Record{reinterpret_cast<float*>(base), reinterpret_cast<float2*>(base + 1024)};
+  }
 };
-static_assert(DynSmem::kAccOff % 16 == 0 && sizeof(AccEntry) % 16 == 0, "float4 access");
+static_assert(DynSmem::kRecs % 16 == 0 && kRecordBytes % 16 == 0 && DynSmem::kSegs % 16 == 0,
+              "aligned records");
 
-__device__ __forceinline__ void acc_clear(AccEntry& A, int lane) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) (&A.o[0][0])[lane + 32 * i] = 0.f;
-  if (lane < 4) {
-    A.M[lane] = -INFINITY;
-    A.L[lane] = 0.f;
-  }
-  if (lane == 0) {
-    A.done = 0;
-    A.bad = 0;
-  }
-}
-
-// Merge a consumer's state into a shared accumulator (caller holds the lock).
-__device__ __forceinline__ void mma_state_merge_into(const MmaState& st, AccEntry& A, bool bad,
-                                                     int lane) {
-  const int gq = lane >> 2, tig = lane & 3;
-  const float lt = st.total_l();
-  float Mold = 0.f, Lold = 0.f;
-  if (gq < 4) {
-    Mold = A.M[gq];
-    Lold = A.L[gq];
-  }
-  __syncwarp();
-  if (gq < 4) {
-    const float Mn = fmaxf(Mold, st.m);
-    const float a = (Mold == Mn) ? 1.f : exp2f(Mold - Mn);
-    const float b = (st.m == Mn) ? 1.f : exp2f(st.m - Mn);
-    float* dst = &A.o[gq][2 * tig];
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      const float2 old = *reinterpret_cast<float2*>(dst + 8 * n);
-      *reinterpret_cast<float2*>(dst + 8 * n) =
-          make_float2(old.x * a + st.o[n][0] * b, old.y * a + st.o[n][1] * b);
-    }
-    if (tig == 0) {
-      A.M[gq] = Mn;
-      A.L[gq] = Lold * a + lt * b;
+// Spin (one lane, bounded) until `pred()`; false on timeout.
+template <class Pred>
+__device__ __forceinline__ bool spin_until(Pred pred) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (pred()) return true;
+    if ((it & 255u) == 255u) {
+      const uint64_t now = global_timer_ns();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > kWaitLimitNs) return false;
     }
   }
-  if (lane == 0 && bad) A.bad = 1;
-  __syncwarp();
 }
 
 template <bool kAppend>
 __global__ void __launch_bounds__(DynSmem::kThreads, 1)
-    paged_decode_dyn_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
+    paged_decode_dyn_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p,
+                            int n_cap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int S = p.num_seqs;
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + DynSmem::kPrefix);
   int32_t* nz = prefix + (S + 1);
-  int* ctl = reinterpret_cast<int*>(smem + DynSmem::kCtl);  // [0] next claim, [1] error, [2] issued
+  int32_t* slen = nz + (S + 1);
+  int2* ptab = reinterpret_cast<int2*>(smem + DynSmem::table_off(S));  // {page id, 8 s + g}
+  int* ctl = reinterpret_cast<int*>(smem + DynSmem::kCtl);  // [0] next unit, [1] error
+  const uint32_t ctl_addr = smem_u32(ctl);
   volatile int* vctl = ctl;
-  volatile int* seqs = reinterpret_cast<volatile int*>(smem + DynSmem::kSeq);
-  AccEntry* acc = reinterpret_cast<AccEntry*>(smem + DynSmem::kAccOff);
-  int4* meta = reinterpret_cast<int4*>(smem + DynSmem::kMeta);
-  const uint32_t tiles = smem_u32(smem), side = smem_u32(smem + DynSmem::kSide);
-  const uint32_t full0 = smem_u32(smem + DynSmem::kFull), empty0 = smem_u32(smem + DynSmem::kEmpty);
+  SegWord* segw = reinterpret_cast<SegWord*>(smem + DynSmem::kSegs);
+  volatile int* busy = reinterpret_cast<volatile int*>(smem + DynSmem::kBusy);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slot0 = warp * kDynStages;
+  int4* my_meta = reinterpret_cast<int4*>(smem + DynSmem::kMeta) + slot0;
+  const uint32_t tiles0 = smem_u32(smem) + slot0 * kStageBytes;
+  uint8_t* side0 = smem + DynSmem::kSide + slot0 * kSideBytes;
+  const uint32_t bars0 = smem_u32(smem + DynSmem::kBars) + slot0 * 8;
 
-  // shared-memory set-up (touches nothing the previous kernel writes; made
-  // visible by the barriers inside build_prefix)
-  if (threadIdx.x < kRing) {
-    mbar_init(full0 + 8 * threadIdx.x, 1);
-    mbar_init(empty0 + 8 * threadIdx.x, 1);
-    seqs[threadIdx.x] = -1;
+  // shared-memory set-up (made visible by the barriers inside build_prefix)
+  if (lane == 0) {
+    for (int st = 0; st < kDynStages; ++st) mbar_init(bars0 + 8 * st, 1);
     fence_mbar_init();
   }
-  for (int e = warp; e < kAcc; e += kDynConsumers + 1) {
-    acc_clear(acc[e], lane);
-    if (lane == 0) {
-      acc[e].tag = e;
-      acc[e].lock = 0;
-    }
+  for (int e = threadIdx.x; e < kSeg; e += blockDim.x) {
+    segw[e].word = 0ull;
+    segw[e].tag = e;
   }
-  if (threadIdx.x == 0) ctl[0] = ctl[1] = ctl[2] = 0;
+  if (threadIdx.x < 2 * kDynWarps) busy[threadIdx.x] = 0;
+  if (threadIdx.x == 0) ctl[0] = ctl[1] = 0;
 
-  pdl_wait();
-  const int n_empty = build_prefix<kDynConsumers + 1, kAppend>(p, prefix, nz);
+  // Without `early` everything waits for the previous kernel here; with it,
+  // reads of q and the new token, and every global write, wait (below).
+  if (!p.early) pdl_wait();
+  const int n_empty = build_prefix<kDynWarps, kAppend>(p, prefix, nz);
   pdl_launch_dependents();
+  for (int s = threadIdx.x; s < S; s += blockDim.x) slen[s] = __ldg(p.seq_lens + s);
+
+  const uint32_t U = 8u * (uint32_t)prefix[S];
+  const uint32_t NC = gridDim.x, c = blockIdx.x;
+  const uint32_t a = range_start(c, U, NC), b = range_start(c + 1, U, NC);
+  int n = (int)(b - a);
+  if (n > n_cap) {  // cannot happen for lengths the prefix accepts; never index past the table
+    if (threadIdx.x == 0) report_error(p.d_err, PKV_ERR_DEVICE_INDEX);
+    n = 0;
+  }
+  // blocks F and E (the segments shared with the neighbouring CTAs) first
+  int F = 0, E = 0, rank0 = 0, rlast = 0;
+  if (n > 0) {
+    Cursor ca, cb;
+    cursor_seek(ca, a, prefix, S);
+    cursor_seek(cb, b - 1, prefix, S);
+    const uint32_t base_a = seg_base(ca, prefix), last_a = base_a + (uint32_t)ca.np - 1;
+    const uint32_t base_b = seg_base(cb, prefix), last_b = base_b + (uint32_t)cb.np - 1;
+    if (base_a < a) F = (int)(min(last_a, b - 1) - a + 1);
+    if (last_b >= b && base_b >= a) E = (int)(b - base_b);
+    rank0 = 8 * nz[ca.s] + ca.g;
+    rlast = 8 * nz[cb.s] + cb.g - rank0;
+  }
+  auto unit_of = [&](int q) -> uint32_t {
+    if (q < F) return a + (uint32_t)q;
+    if (q < F + E) return b - (uint32_t)E + (uint32_t)(q - F);
+    return a + (uint32_t)(q - E);
+  };
+  // order of segment (s, g) among the CTA's segments as they are taken
+  auto order_of = [&](int s, int g) -> int {
+    const int nat = 8 * nz[s] + g - rank0;
+    if (E > 0 && nat == rlast) return F > 0 ? 1 : 0;
+    if (F > 0 && nat == 0) return 0;
+    return nat + (E > 0 ? 1 : 0);
+  };
+  for (int q = threadIdx.x; q < n; q += blockDim.x) {
+    Cursor cu;
+    cursor_seek(cu, unit_of(q), prefix, S);
+    const int pid = __ldg(p.block_tables + (size_t)cu.s * p.bt_stride + cu.j);
+    ptab[q] = make_int2((pid >= 0 && pid < p.num_pages) ? pid : -1, (cu.s << 3) | cu.g);
+  }
+  __syncthreads();
+
+  // ---- per-warp pipeline ----------------------------------------------------
+  int last_seg = -1;   // 8 s + g of the last unit this warp staged
+  uint32_t ph = 0;     // bit st: parity of the next phase of stage st
+  uint32_t armed = 0;  // bit st: stage st has been armed at least once
+  bool failed = false;
+  int cq = 0, ce = 0;  // rest of the warp's current chunk: [cq, ce)
+
+  // next unit for this warp: from its chunk, else a new chunk of
+  // max(1, remaining / (2 x warps)) units (n when none is left)
+  auto claim = [&]() -> int {
+    if (cq < ce) return cq++;
+    int q0 = n, sz = 0;
+    if (lane == 0) {
+      for (int it = 0; it < (1 << 16); ++it) {
+        const int cur = ld_shared_volatile(ctl_addr);
+        if (cur >= n) break;
+        const int want = max(1, (n - cur) / (2 * kDynWarps));
+        if (atom_cas_shared(ctl_addr, cur, cur + want) == cur) {
+          q0 = cur;
+          sz = want;
+          break;
+        }
+      }
+    }
+    q0 = __shfl_sync(0xffffffffu, q0, 0);
+    sz = __shfl_sync(0xffffffffu, sz, 0);
+    cq = q0 + 1;
+    ce = q0 + sz;
+    return q0;
+  };
+  // Stage unit q: the tiles now; the q / new-token / rope rows now unless
+  // `defer` (they may depend on the previous kernel).
+  auto stage_rows = [&](int stage) {
+    const int4 mt = my_meta[stage];
+    const int s = mt.y, g = mt.z & 7;
+    const bool need_q = (mt.z >> 3) & 1, is_last = (mt.z >> 4) & 1;
+    const uint32_t sd = smem_u32(side0 + stage * kSideBytes), bar = bars0 + 8 * stage;
+    if (need_q)
+      bulk_load(sd + kSideQ, p.q + ((size_t)s * PKV_NUM_Q_HEADS + g * 4) * 64, 512, bar);
+    if (kAppend && (need_q || is_last)) {
+      const size_t r = (size_t)(slen[s] - 1) * PKV_ROPE_PAIRS;
+      bulk_load(sd + kSideCos, p.rope_cos + r, 128, bar);
+      bulk_load(sd + kSideSin, p.rope_sin + r, 128, bar);
+    }
+    if (kAppend && is_last && mt.w >= 0) {
+      const size_t r = ((size_t)s * PKV_NUM_KV_HEADS + g) * 64;
+      bulk_load(sd + kSideK, p.k_new + r, 128, bar);
+      bulk_load(sd + kSideV, p.v_new + r, 128, bar);
+    }
+  };
+  auto stage_unit = [&](int stage, int q, bool defer) {
+    if (q >= n) {
+      if (lane == 0) my_meta[stage] = make_int4(-1, 0, 0, -1);
+      __syncwarp();
+      return;
+    }
+    const int2 te = ptab[q];
+    const int pid = te.x, seg = te.y, ss = te.y >> 3, gg = te.y & 7;
+    const int np = prefix[ss + 1] - prefix[ss];
+    const int jj = (int)(unit_of(q) - (8u * (uint32_t)prefix[ss] + (uint32_t)(gg * np)));
+    const bool need_q = seg != last_seg;
+    last_seg = seg;
+    const bool is_last = kAppend && jj == np - 1;
+    const uint32_t bytes = (pid >= 0 ? kStageBytes : 0) + (need_q ? 512 : 0) +
+                           (kAppend && (need_q || is_last) ? 256 : 0) +
+                           (kAppend && is_last && pid >= 0 ? 256 : 0);
+    if (lane == 0) {
+      my_meta[stage] = make_int4(q, ss, gg | (need_q << 3) | (is_last << 4) | (jj << 5), pid);
+      const uint32_t bar = bars0 + 8 * stage;
+      fence_proxy_async_smem();  // the stage was last read (and patched) by generic accesses
+      if (bytes == 0) {
+        mbar_arrive(bar);
+      } else {
+        mbar_arrive_expect_tx(bar, bytes);
+        if (pid >= 0) {
+          const uint32_t dst = tiles0 + stage * kStageBytes;
+          tma_load_3d(dst, &tmap, 0, 0, (pid * 2 + 0) * PKV_NUM_KV_HEADS + gg, bar);
+          tma_load_3d(dst + kTileBytes, &tmap, 0, 0, (pid * 2 + 1) * PKV_NUM_KV_HEADS + gg, bar);
+        }
+        if (!defer) stage_rows(stage);
+      }
+    }
+    ph ^= 1u << stage;
+    armed |= 1u << stage;
+    __syncwarp();
+  };
+
+  MmaState st;
+  st.reset();
+  int cs = 0, cg = 0, clen = 0, m_units = 0, lorder = 0;
+  uint32_t sbase = 0, snp = 1;
+  bool seg_bad = false;
+
+  int next_slot = 0;
+  // Leave the current segment; false if a bounded wait gave up.
+  auto flush = [&]() -> bool {
+    if (m_units == 0) return true;
+    const uint32_t last = sbase + snp - 1;
+    const int n_x = (int)(min(last, b - 1) - max(sbase, a) + 1);
+    const bool inside = sbase >= a && last < b;
+    const int units = m_units;
+    const bool bad = seg_bad;
+    m_units = 0;
+    seg_bad = false;
+    SegWord& E = segw[lorder % kSeg];
+    volatile int* tag = &E.tag;
+    int got = 0;
+    if (units == n_x) {
+      // this warp took every unit the CTA has of the segment: no record, but
+      // the word still passes through this segment's turn, in order
+      if (lane == 0) {
+        got = spin_until([&] { return *tag == lorder; });
+        if (got) *tag = lorder + kSeg;
+      }
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (got) {
+        if (inside) {
+          st.write_output(p, cs, cg, bad, lane);
+        } else {
+          st.write_record(global_record(p, 8u * (uint32_t)cs + (uint32_t)cg + c), bad, lane);
+          cross_cta_arrive(p, cs, cg, sbase, snp, U, NC, lane);
+        }
+      }
+      st.reset();
+      return got != 0;
+    }
+    // a record slot of this warp whose last record has been merged
+    const int bit = warp + kDynWarps * next_slot;
+    next_slot ^= 1;
+    if (lane == 0) got = spin_until([&] { return busy[bit] == 0; });
+    got = __shfl_sync(0xffffffffu, got, 0);
+    if (!got) {
+      st.reset();
+      return false;
+    }
+    st.write_record(DynSmem::rec(smem, bit), bad, lane);
+    st.reset();
+    __syncwarp();
+    uint32_t lo = 0, hi = 0;
+    if (lane == 0) {
+      busy[bit] = 1;
+      got = spin_until([&] { return *tag == lorder; });
+      if (got) {
+        __threadfence_block();  // the record before the count
+        const unsigned long long old = atom_add_shared_u64(
+            smem_u32(&E.word), (unsigned long long)units | (1ull << (32 + bit)));
+        lo = (uint32_t)old;
+        hi = (uint32_t)(old >> 32);
+      }
+    }
+    got = __shfl_sync(0xffffffffu, got, 0);
+    if (!got) return false;
+    lo = __shfl_sync(0xffffffffu, lo, 0) + (uint32_t)units;
+    hi = __shfl_sync(0xffffffffu, hi, 0) | (1u << bit);
+    if ((int)lo != n_x) return true;
+    // this record completes the segment: merge every record listed
+    __threadfence_block();
+    MergeAcc t;
+    t.init();
+    for (uint32_t mm = hi; mm != 0; mm &= mm - 1) t.add_shared(DynSmem::rec(smem, __ffs(mm) - 1), lane);
+    __syncwarp();
+    __threadfence_block();  // the reads before the slots are handed back
+    if ((hi >> lane) & 1u) busy[lane] = 0;
+    if (lane == 0) {
+      E.word = 0ull;
+      __threadfence_block();
+      *tag = lorder + kSeg;
+    }
+    if (inside) {
+      t.store_output(p, cs, cg, lane);
+    } else {
+      t.store_record(global_record(p, 8u * (uint32_t)cs + (uint32_t)cg + c), lane);
+      cross_cta_arrive(p, cs, cg, sbase, snp, U, NC, lane);
+    }
+    return true;
+  };
+
+  // prologue: two units in flight (tiles only before the wait with `early`)
+  for (int stg = 0; stg < kDynStages; ++stg) stage_unit(stg, claim(), p.early != 0);
+  if (p.early) {
+    pdl_wait();
+    if (lane == 0)
+      for (int stg = 0; stg < kDynStages; ++stg)
+        if (my_meta[stg].x >= 0) stage_rows(stg);
+    __syncwarp();
+  }
+
+  for (int k = 0;; ++k) {
+    const int stage = k % kDynStages;
+    const int4 mt = my_meta[stage];
+    if (mt.x < 0 || vctl[1] != 0) break;
+    if (!mbar_wait_bounded(bars0 + 8 * stage, ((ph >> stage) & 1u) ^ 1u, kWaitLimitNs)) {
+      failed = true;
+      if (lane == 0) {
+        atomicOr(ctl + 1, 1);
+        report_error(p.d_err, PKV_ERR_TIMEOUT);
+      }
+      break;
+    }
+    const int s = mt.y, g = mt.z & 7, j = mt.z >> 5, pid = mt.w;
+    const bool need_q = (mt.z >> 3) & 1, is_last = (mt.z >> 4) & 1;
+    const uint8_t* sd = side0 + stage * kSideBytes;
+    if (need_q) {  // a new segment for this warp
+      if (!flush()) {
+        failed = true;
+        if (lane == 0) {
+          atomicOr(ctl + 1, 1);
+          report_error(p.d_err, PKV_ERR_TIMEOUT);
+        }
+        break;
+      }
+      cs = s;
+      cg = g;
+      clen = slen[s];
+      snp = (uint32_t)(prefix[s + 1] - prefix[s]);
+      sbase = 8u * (uint32_t)prefix[s] + (uint32_t)g * snp;
+      lorder = order_of(s, g);
+      st.template load_q_rows<kAppend, true>(
+          p, reinterpret_cast<const uint16_t*>(sd + kSideQ),
+          reinterpret_cast<const float*>(sd + kSideCos), reinterpret_cast<const float*>(sd + kSideSin),
+          ((size_t)s * PKV_NUM_Q_HEADS + g * 4) * 64, j == 0, lane);
+    }
+    if (pid >= 0) {
+      const uint32_t sK = tiles0 + stage * kStageBytes;
+      if (kAppend && is_last) {  // the new token, staged next to the tiles
+        NewToken tok;
+        tok.k0 = reinterpret_cast<const uint16_t*>(sd + kSideK)[lane];
+        tok.k1 = reinterpret_cast<const uint16_t*>(sd + kSideK)[lane + 32];
+        tok.v = reinterpret_cast<const uint32_t*>(sd + kSideV)[lane];
+        tok.c = reinterpret_cast<const float*>(sd + kSideCos)[lane];
+        tok.s = reinterpret_cast<const float*>(sd + kSideSin)[lane];
+        tok.insert(p, sK, sK + kTileBytes, pid, g, (clen - 1) % PKV_PAGE_TOKENS, lane);
+        __syncwarp();
+      }
+      st.page(sK, sK + kTileBytes, min(PKV_PAGE_TOKENS, clen - PKV_PAGE_TOKENS * j), p.sl2, lane);
+    } else {
+      seg_bad = true;
+      if (lane == 0) report_error(p.d_err, PKV_ERR_DEVICE_INDEX);
+    }
+    ++m_units;
+    __syncwarp();
+    stage_unit(stage, claim(), false);
+  }
+  if (!failed && vctl[1] == 0) {
+    if (!flush() && lane == 0) {
+      atomicOr(ctl + 1, 1);
+      report_error(p.d_err, PKV_ERR_TIMEOUT);
+    }
+  } else {
+    // after a timeout: wait (bounded) for this warp's copies still in flight
+    for (int stg = 0; stg < kDynStages; ++stg)
+      if ((armed >> stg) & 1u)
+        (void)mbar_wait_bounded(bars0 + 8 * stg, ((ph >> stg) & 1u) ^ 1u, kWaitLimitNs);
+  }
+
+  if (p.combine_mode == 1 && blockIdx.x == 0)
+    for (int i = threadIdx.x; i <= S; i += blockDim.x) p.ws_prefix[i] = prefix[i];
   if (n_empty > 0) {
     const uint32_t per_seq = PKV_NUM_Q_HEADS * 64 / 8;
     const uint32_t total = (uint32_t)S * per_seq;
@@ -1070,264 +1368,6 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
           reinterpret_cast<uint4*>(p.q_out)[i] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-  }
-  const uint32_t U = 8u * (uint32_t)prefix[S];
-  const uint32_t NC = gridDim.x, c = blockIdx.x;
-  const uint32_t a = range_start(c, U, NC), b = range_start(c + 1, U, NC);
-  const int n = (int)(b - a);
-
-  if (warp == 0) {
-    // ---------------- producer ---------------------------------------------
-    auto unit_meta = [&](int pos) -> int4 {
-      if (pos >= n) return make_int4(-1, 0, -1, 0);
-      Cursor cu;
-      cursor_seek(cu, a + (uint32_t)pos, prefix, S);
-      int pid = __ldg(p.block_tables + (size_t)cu.s * p.bt_stride + cu.j);
-      if (pid < 0 || pid >= p.num_pages) pid = -1;
-      return make_int4(cu.s, cu.g | (cu.j << 3), pid, __ldg(p.seq_lens + cu.s));
-    };
-    int4 cur = unit_meta(lane), nxt = unit_meta(32 + lane);
-    bool stop = false;
-    int issued = 0;
-    for (int batch = 0; batch < n && !stop; batch += 32) {
-      for (int grp = 0; grp < 32 && batch + grp < n; grp += 8) {
-        const int pos = batch + lane;
-        const bool mine = lane >= grp && lane < grp + 8 && pos < n;
-        const int slot = lane;  // pos % kRing
-        bool ok = vctl[1] == 0;
-        if (ok && mine && pos >= kRing)
-          ok = mbar_wait_bounded(empty0 + 8 * slot, (uint32_t)(pos / kRing - 1) & 1u, kWaitLimitNs);
-        if (!__all_sync(0xffffffffu, ok)) {
-          if (lane == 0 && vctl[1] == 0) {
-            atomicOr(ctl + 1, 1);
-            report_error(p.d_err, PKV_ERR_TIMEOUT);
-          }
-          stop = true;
-          break;
-        }
-        if (mine) {
-          meta[slot] = cur;
-          seqs[slot] = pos;
-          const uint32_t bar = full0 + 8 * slot;
-          if (cur.z >= 0) {
-            const int g = cur.y & 7, j = cur.y >> 3, len = cur.w;
-            const bool last = kAppend && j == (len - 1) / PKV_PAGE_TOKENS;
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar, kStageBytes + (last ? kSideBytes : 0));
-            const uint32_t dst = tiles + slot * kStageBytes;
-            tma_load_3d(dst, &tmap, 0, 0, (cur.z * 2 + 0) * PKV_NUM_KV_HEADS + g, bar);
-            tma_load_3d(dst + kTileBytes, &tmap, 0, 0, (cur.z * 2 + 1) * PKV_NUM_KV_HEADS + g, bar);
-            if (last) {
-              const uint32_t sd = side + slot * kSideBytes;
-              const size_t row = ((size_t)cur.x * PKV_NUM_KV_HEADS + g) * 64;
-              bulk_load(sd, p.k_new + row, 128, bar);
-              bulk_load(sd + 128, p.v_new + row, 128, bar);
-              bulk_load(sd + 256, p.rope_cos + (size_t)(len - 1) * PKV_ROPE_PAIRS, 128, bar);
-              bulk_load(sd + 384, p.rope_sin + (size_t)(len - 1) * PKV_ROPE_PAIRS, 128, bar);
-            }
-          } else {
-            mbar_arrive(bar);
-          }
-        }
-        __syncwarp();
-        issued = min(n, batch + grp + 8);
-      }
-      cur = nxt;
-      nxt = unit_meta(batch + 64 + lane);
-    }
-    if (lane == 0) ctl[2] = issued;
-  } else {
-    // ---------------- consumers --------------------------------------------
-    MmaState st;
-    st.reset();
-    int cs = 0, cg = 0, clen = 0, m_units = 0, seg_last = -1, lrank = 0, rank0 = 0;
-    uint32_t sbase = 0, snp = 1;
-    bool seg_bad = false, failed = false;
-    if (n > 0) {
-      Cursor cu;
-      cursor_seek(cu, a, prefix, S);
-      rank0 = 8 * nz[cu.s] + cu.g;
-    }
-    auto give_up = [&]() {
-      if (lane == 0 && vctl[1] == 0) {
-        atomicOr(ctl + 1, 1);
-        report_error(p.d_err, PKV_ERR_TIMEOUT);
-      }
-      failed = true;
-    };
-
-    // Leave the current segment; false if a bounded wait gave up.
-    auto flush = [&]() -> bool {
-      if (m_units == 0) return true;
-      const uint32_t last = sbase + snp - 1;
-      const int n_x = (int)(min(last, b - 1) - max(sbase, a) + 1);
-      const bool inside = sbase >= a && last < b;
-      const int units = m_units;
-      const bool bad = seg_bad;
-      m_units = 0;
-      seg_bad = false;
-      AccEntry& A = acc[lrank % kAcc];
-      int got = 0;
-      if (units == n_x) {
-        // this warp took every unit the CTA has of the segment: no merge, but
-        // the entry still passes through this segment's turn, in order
-        if (lane == 0) {
-          volatile int* tag = &A.tag;
-          const uint64_t t0 = global_timer_ns();
-          for (;;) {
-            if (*tag == lrank) {
-              got = 1;
-              break;
-            }
-            if (global_timer_ns() - t0 > kWaitLimitNs) break;
-            __nanosleep(32);
-          }
-          if (got) *tag = lrank + kAcc;
-        }
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (got) {
-          if (inside) {
-            st.write_output(p, cs, cg, bad, lane);
-          } else {
-            st.write_record(global_record(p, 8u * (uint32_t)cs + (uint32_t)cg + c), bad, lane);
-            cross_cta_arrive(p, cs, cg, sbase, snp, U, NC, lane);
-          }
-        }
-        st.reset();
-        return got != 0;
-      }
-      if (lane == 0) {  // the lock, held only while this segment owns the entry
-        const uint64_t t0 = global_timer_ns();
-        for (;;) {
-          if (atomicCAS(&A.lock, 0, 1) == 0) {
-            __threadfence_block();
-            if (*reinterpret_cast<volatile int*>(&A.tag) == lrank) {
-              got = 1;
-              break;
-            }
-            atomicExch(&A.lock, 0);
-          }
-          if (global_timer_ns() - t0 > kWaitLimitNs) break;
-          __nanosleep(32);
-        }
-      }
-      got = __shfl_sync(0xffffffffu, got, 0);
-      __syncwarp();
-      if (!got) {
-        st.reset();
-        return false;
-      }
-      mma_state_merge_into(st, A, bad, lane);
-      st.reset();
-      int complete = 0;
-      if (lane == 0) {
-        A.done += units;
-        complete = A.done == n_x;
-      }
-      complete = __shfl_sync(0xffffffffu, complete, 0);
-      MergeAcc t;
-      if (complete) {  // take the result, then hand the entry on
-        const int hh = lane >> 3, d0 = (lane & 7) * 8;
-        const float4* src = reinterpret_cast<const float4*>(&A.o[hh][d0]);
-        const float4 o0 = src[0], o1 = src[1];
-        t.acc[0] = o0.x; t.acc[1] = o0.y; t.acc[2] = o0.z; t.acc[3] = o0.w;
-        t.acc[4] = o1.x; t.acc[5] = o1.y; t.acc[6] = o1.z; t.acc[7] = o1.w;
-        t.M = A.M[hh];
-        t.L = A.L[hh];
-        t.bad = A.bad != 0;
-        __syncwarp();
-        acc_clear(A, lane);
-        if (lane == 0) A.tag = lrank + kAcc;
-      }
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence_block();
-        atomicExch(&A.lock, 0);
-      }
-      if (complete) {
-        if (inside) {
-          t.store_output(p, cs, cg, lane);
-        } else {
-          t.store_record(global_record(p, 8u * (uint32_t)cs + (uint32_t)cg + c), lane);
-          cross_cta_arrive(p, cs, cg, sbase, snp, U, NC, lane);
-        }
-      }
-      return true;
-    };
-
-    for (;;) {
-      int pos = 0;
-      if (lane == 0) pos = atomicAdd(ctl, 1);
-      pos = __shfl_sync(0xffffffffu, pos, 0);
-      if (pos >= n || vctl[1] != 0) break;
-      const bool fresh = pos > seg_last;  // past the held segment
-      if (fresh && !flush()) {
-        give_up();
-        break;
-      }
-      const int slot = pos % kRing;
-      int ok = 1;
-      if (lane == 0 && seqs[slot] != pos) {
-        const uint64_t t0 = global_timer_ns();
-        while (seqs[slot] != pos) {
-          if (vctl[1] != 0 || global_timer_ns() - t0 > kWaitLimitNs) {
-            ok = 0;
-            break;
-          }
-          __nanosleep(20);
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      __syncwarp();
-      if (ok) ok = mbar_wait_bounded(full0 + 8 * slot, (uint32_t)(pos / kRing) & 1u, kWaitLimitNs);
-      if (!__all_sync(0xffffffffu, ok)) {
-        give_up();
-        break;
-      }
-      const int4 mt = meta[slot];
-      const int s = mt.x, g = mt.y & 7, j = mt.y >> 3, pid = mt.z, len = mt.w;
-      if (fresh) {
-        cs = s;
-        cg = g;
-        clen = len;
-        snp = (uint32_t)(prefix[s + 1] - prefix[s]);
-        sbase = 8u * (uint32_t)prefix[s] + (uint32_t)g * snp;
-        seg_last = (int)(min(sbase + snp - 1, b - 1) - a);
-        lrank = 8 * nz[s] + g - rank0;
-        st.template load_q<kAppend>(p, s, g, len - 1, j == 0, lane);
-      }
-      if (pid >= 0) {
-        const int valid = min(PKV_PAGE_TOKENS, clen - PKV_PAGE_TOKENS * j);
-        const uint32_t sK = tiles + slot * kStageBytes;
-        if (kAppend && j == (clen - 1) / PKV_PAGE_TOKENS) {
-          // the new token: rows staged by the producer next to the tiles
-          const uint8_t* sd = smem + DynSmem::kSide + slot * kSideBytes;
-          NewToken tok;
-          tok.k0 = reinterpret_cast<const uint16_t*>(sd)[lane];
-          tok.k1 = reinterpret_cast<const uint16_t*>(sd)[lane + 32];
-          tok.v = reinterpret_cast<const uint32_t*>(sd + 128)[lane];
-          tok.c = reinterpret_cast<const float*>(sd + 256)[lane];
-          tok.s = reinterpret_cast<const float*>(sd + 384)[lane];
-          tok.insert(p, sK, sK + kTileBytes, pid, g, (clen - 1) % PKV_PAGE_TOKENS, lane);
-          __syncwarp();
-        }
-        st.page(sK, sK + kTileBytes, valid, p.sl2, lane);
-      } else {
-        seg_bad = true;
-        if (lane == 0) report_error(p.d_err, PKV_ERR_DEVICE_INDEX);
-      }
-      ++m_units;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * slot);
-    }
-    if (!failed && !flush()) give_up();
-  }
-  __syncthreads();
-  if (warp == 0 && vctl[1] != 0) {
-    // after a timeout: wait (bounded) for every copy still in flight
-    const int issued = ctl[2];
-    for (int pos = max(0, issued - kRing) + lane; pos < issued; pos += 32)
-      (void)mbar_wait_bounded(full0 + 8 * (pos % kRing), (uint32_t)(pos / kRing) & 1u, kWaitLimitNs);
   }
 }
 
@@ -1529,7 +1569,6 @@ static int launch_decode_dyn(const DecodeParams& prm, const CUtensorMap& map, in
   static std::mutex mu;
   static int max_dyn[64] = {0};
   auto kern = paged_decode_dyn_kernel<kAppend>;
-  const size_t smem = DynSmem::bytes(prm.num_seqs);
   {
     std::lock_guard<std::mutex> lock(mu);
     if (device < 0 || device >= 64) return PKV_ERR_CUDA;
@@ -1545,26 +1584,32 @@ static int launch_decode_dyn(const DecodeParams& prm, const CUtensorMap& map, in
       if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(dyn)");
       max_dyn[device] = m;
     }
-    if ((long long)smem > max_dyn[device]) return PKV_ERR_UNSUPPORTED_SHAPE;
   }
   const long long pages_bound = max_seq_len > 0 ? (max_seq_len + 15) / 16 : 0;
   const long long u_bound = 8ll * prm.num_seqs * pages_bound;
   long long nc = num_sms;
-  const long long per = (long long)kDynConsumers * min_units;
+  const long long per = (long long)kDynWarps * (min_units > 0 ? min_units : 1);
   const long long want = (u_bound + per - 1) / per;
   if (want < nc) nc = want;
   if (nc < 1) nc = 1;
+  // page-id table: the most units any CTA can own for lengths the kernel accepts
+  const long long max_len = kAppend ? std::min<long long>(16ll * prm.max_blocks, prm.max_pos)
+                                    : 16ll * prm.max_blocks;
+  const long long units_max = 8ll * prm.num_seqs * ((max_len + 15) / 16);
+  const long long n_cap = (units_max + nc - 1) / nc + 1;
+  const long long smem = (long long)DynSmem::bytes(prm.num_seqs, 0) + 8 * n_cap;
+  if (smem > max_dyn[device]) return PKV_ERR_UNSUPPORTED_SHAPE;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)nc);
   cfg.blockDim = dim3(DynSmem::kThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_status(cudaLaunchKernelEx(&cfg, kern, map, prm), "cudaLaunchKernelEx(dyn)");
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, map, prm, (int)n_cap), "cudaLaunchKernelEx(dyn)");
 }
 
 }  // namespace pkv
@@ -1676,7 +1721,7 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int ms = max_seq_len;
   const int schedule = opts ? opts->schedule : 0;
-  if (schedule == 1 && compute == PKV_COMPUTE_TENSOR && prm.combine_mode == 0) {
+  if (schedule == 1 && compute == PKV_COMPUTE_TENSOR) {
     const int rc2 = app ? launch_decode_dyn<true>(prm, map, dev, sms, ms, min_units, st)
                         : launch_decode_dyn<false>(prm, map, dev, sms, ms, min_units, st);
     if (rc2 != PKV_ERR_UNSUPPORTED_SHAPE) return rc2;  // too many sequences: static schedule

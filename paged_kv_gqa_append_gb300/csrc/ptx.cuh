@@ -104,14 +104,20 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr));
 }
 // D(16x8, fp32) += A(16x16, bf16, row) * B(16x8, bf16, col).  Rows 8..15 of A
-// are zero in every use here, so a1 = a3 = 0 are passed as constants.
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0,
+// are zero in every use here, so a1 = a3 = 0 are passed as constants, and so
+// are rows 8..15 of C: those rows of D stay zero and are not kept -- `d`
+// holds this lane's two entries of row lane/4 only.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0,
                                                uint32_t b1) {
+  float z0, z1;
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %11, %12, %13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(z0), "=f"(z1)
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(d[0]), "f"(d[1]), "f"(0.f),
+        "f"(0.f));
+  (void)z0;
+  (void)z1;
 }
 
 // ---- bf16 helpers ----------------------------------------------------------
@@ -124,6 +130,25 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t x) {
   return __uint_as_float(x & 0xFFFF0000u);
+}
+
+// shared-memory word access by 32-bit shared address
+__device__ __forceinline__ int atom_cas_shared(uint32_t addr, int cmp, int val) {
+  int old;
+  asm volatile("atom.shared.cas.b32 %0, [%1], %2, %3;" : "=r"(old) : "r"(addr), "r"(cmp), "r"(val)
+               : "memory");
+  return old;
+}
+__device__ __forceinline__ unsigned long long atom_add_shared_u64(uint32_t addr,
+                                                                  unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.shared.add.u64 %0, [%1], %2;" : "=l"(old) : "r"(addr), "l"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ int ld_shared_volatile(uint32_t addr) {
+  int v;
+  asm volatile("ld.volatile.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ void report_error(int* d_err, int code) {
