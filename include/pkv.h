@@ -202,17 +202,19 @@ typedef struct pkv_decode_opts {
   int combine;            /* segments split across CTAs: 0 = the last CTA merges
                              them in the same kernel, 1 = a second kernel merges
                              them after the first (programmatic dependent launch) */
-  int schedule;           /* 0 = static warp ranges; 1 = dynamic: a producer warp
-                             streams pages through a shared ring and 15 consumer
-                             warps claim work as they free up (tensor path)      */
+  int schedule;           /* 0 = static: each warp a fixed contiguous sub-range;
+                             1 = dynamic: warps claim chunks of the CTA's range
+                             from a shared counter (large first, single pages at
+                             the end) and the CTA's shared segments go first.
+                             Falls back to 0 when its page table does not fit in
+                             shared memory (tensor path only)                   */
   int early_kv;           /* 1 = the caller guarantees that block_tables, seq_lens
                              and the K/V pages this call reads are not written by
                              the kernel enqueued just before it on the stream:
                              the call then reads them, and stages its first pages,
                              while that kernel is still finishing (programmatic
                              dependent launch); q, the new token and all writes
-                             still wait for it.  0 = everything waits (default).
-                             Static schedule only.                                 */
+                             still wait for it.  0 = everything waits (default). */
 } pkv_decode_opts;
 
 /* paged_gqa_decode with explicit options; same contract otherwise. */
