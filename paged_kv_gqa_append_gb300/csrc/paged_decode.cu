@@ -95,8 +95,8 @@ struct SmemLayout {
   static constexpr int kPid = kBars + kWarps * kStages * 8;            // int [kWarps][kStages]
   static constexpr int kBad = kPid + kWarps * kStages * 4;             // int [kWarps]
   static constexpr int kSlots = kBad + ((kWarps * 4 + 15) / 16) * 16;  // Record [kWarps]
-  static constexpr int kPrefix = kSlots + kWarps * kRecordBytes;       // int [S + 1]
-  static size_t bytes(int num_seqs) { return 1024 + kPrefix + 4 * (size_t)(num_seqs + 1); }
+  static constexpr int kPrefix = kSlots + kWarps * kRecordBytes;       // int [S + 1], then len [S]
+  static size_t bytes(int num_seqs) { return 1024 + kPrefix + 4 * (size_t)(2 * num_seqs + 1); }
   // Slot 0 (dedicated) holds the warp's record for a segment that began
   // before its range; slot 1 holds the record for a segment that runs past
   // its range, written after the warp's last page, in its own idle tiles.
@@ -165,11 +165,13 @@ __device__ __forceinline__ int seq_pages(int n, int max_len, bool* bad) {
   return (n + PKV_PAGE_TOKENS - 1) / PKV_PAGE_TOKENS;
 }
 
-// Block-wide exclusive prefix of pages over all sequences into prefix[0..S]
-// and, if `nz` is given, of non-empty sequences into nz[0..S]; returns the
-// number of sequences without pages (empty or invalid length).
+// Block-wide exclusive prefix of pages over all sequences into prefix[0..S],
+// if `nz` is given of non-empty sequences into nz[0..S], and if `lens` is
+// given a copy of seq_lens[0..S); returns the number of sequences without
+// pages (empty or invalid length).
 template <int kWarps, bool kAppend>
-__device__ int build_prefix(const DecodeParams& p, int32_t* prefix, int32_t* nz = nullptr) {
+__device__ int build_prefix(const DecodeParams& p, int32_t* prefix, int32_t* nz = nullptr,
+                            int32_t* lens = nullptr) {
   // with a fused append the new token's position must also lie in the table
   const int max_len = kAppend ? min(PKV_PAGE_TOKENS * p.max_blocks, p.max_pos)
                               : PKV_PAGE_TOKENS * p.max_blocks;
@@ -183,7 +185,9 @@ __device__ int build_prefix(const DecodeParams& p, int32_t* prefix, int32_t* nz 
   bool bad = false;
   int sum = 0, cnt = 0;
   for (int s = lo; s < hi; ++s) {
-    const int np = seq_pages(__ldg(p.seq_lens + s), max_len, &bad);
+    const int len = __ldg(p.seq_lens + s);
+    if (lens) lens[s] = len;
+    const int np = seq_pages(len, max_len, &bad);
     sum += np;
     cnt += (np > 0);
   }
@@ -214,7 +218,7 @@ __device__ int build_prefix(const DecodeParams& p, int32_t* prefix, int32_t* nz 
   for (int s = lo; s < hi; ++s) {
     prefix[s] = run;
     if (nz) nz[s] = run_nz;
-    const int np = seq_pages(__ldg(p.seq_lens + s), max_len, &bad);
+    const int np = seq_pages(lens ? lens[s] : __ldg(p.seq_lens + s), max_len, &bad);
     empties += (np == 0);
     run += np;
     run_nz += (np > 0);
@@ -741,6 +745,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + Smem::kPrefix);
+  int32_t* slen = prefix + (p.num_seqs + 1);
   int* spid = reinterpret_cast<int*>(smem + Smem::kPid);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.num_seqs;
@@ -748,7 +753,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
   // Without `early` everything waits for the previous kernel here.  With it,
   // only reads of q and the new token, and every global write, wait (below).
   if (!p.early) pdl_wait();
-  const int n_empty = build_prefix<kWarps, kAppend>(p, prefix);
+  const int n_empty = build_prefix<kWarps, kAppend>(p, prefix, nullptr, slen);
   pdl_launch_dependents();
 
   const uint32_t U = 8u * (uint32_t)prefix[S];
@@ -789,10 +794,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
           fence_proxy_async_smem();
           mbar_arrive_expect_tx(bar, kStageBytes);
           const uint32_t dst = tiles + stage * kStageBytes;
-          const int zk = (pid * 2 + 0) * PKV_NUM_KV_HEADS + ci.g;
-          const int zv = (pid * 2 + 1) * PKV_NUM_KV_HEADS + ci.g;
-          tma_load_3d(dst, &tmap, 0, 0, zk, bar);
-          tma_load_3d(dst + kTileBytes, &tmap, 0, 0, zv, bar);
+          tma_load_4d(dst, &tmap, 0, 0, ci.g, pid * 2, bar);  // K tile, then V tile
         } else {
           mbar_arrive(bar);  // keep the phase sequence of this stage intact
         }
@@ -814,7 +816,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
     Cursor cc;
     cursor_seek(cc, u0, prefix, S);
     st.reset();
-    int seg_len = __ldg(p.seq_lens + cc.s);
+    int seg_len = slen[cc.s];
     NewToken tok;
     auto enter_segment = [&]() {
       const uint32_t base = seg_base(cc, prefix);
@@ -865,7 +867,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
       }
       cursor_next(cc, prefix, S);
       if (seg_end && uc + 1 < n_units) {
-        seg_len = __ldg(p.seq_lens + cc.s);
+        seg_len = slen[cc.s];
         enter_segment();
       }
       __syncwarp();
@@ -1054,9 +1056,8 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
   // Without `early` everything waits for the previous kernel here; with it,
   // reads of q and the new token, and every global write, wait (below).
   if (!p.early) pdl_wait();
-  const int n_empty = build_prefix<kDynWarps, kAppend>(p, prefix, nz);
+  const int n_empty = build_prefix<kDynWarps, kAppend>(p, prefix, nz, slen);
   pdl_launch_dependents();
-  for (int s = threadIdx.x; s < S; s += blockDim.x) slen[s] = __ldg(p.seq_lens + s);
 
   const uint32_t U = 8u * (uint32_t)prefix[S];
   const uint32_t NC = gridDim.x, c = blockIdx.x;
@@ -1129,12 +1130,8 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
     ce = q0 + sz;
     return q0;
   };
-  // Stage unit q: the tiles now; the q / new-token / rope rows now unless
-  // `defer` (they may depend on the previous kernel).
-  auto stage_rows = [&](int stage) {
-    const int4 mt = my_meta[stage];
-    const int s = mt.y, g = mt.z & 7;
-    const bool need_q = (mt.z >> 3) & 1, is_last = (mt.z >> 4) & 1;
+  // The q / new-token / rope rows of a staged unit (lane 0).
+  auto stage_rows = [&](int stage, int s, int g, bool need_q, bool is_last, int pid) {
     const uint32_t sd = smem_u32(side0 + stage * kSideBytes), bar = bars0 + 8 * stage;
     if (need_q)
       bulk_load(sd + kSideQ, p.q + ((size_t)s * PKV_NUM_Q_HEADS + g * 4) * 64, 512, bar);
@@ -1143,22 +1140,41 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
       bulk_load(sd + kSideCos, p.rope_cos + r, 128, bar);
       bulk_load(sd + kSideSin, p.rope_sin + r, 128, bar);
     }
-    if (kAppend && is_last && mt.w >= 0) {
+    if (kAppend && is_last && pid >= 0) {
       const size_t r = ((size_t)s * PKV_NUM_KV_HEADS + g) * 64;
       bulk_load(sd + kSideK, p.k_new + r, 128, bar);
       bulk_load(sd + kSideV, p.v_new + r, 128, bar);
     }
   };
-  auto stage_unit = [&](int stage, int q, bool defer) {
-    if (q >= n) {
+  // Table entry of unit q and its sequence's page prefix, read ahead of use.
+  struct Ahead {
+    int q, pid, seg, p0, p1;
+  };
+  auto look_ahead = [&](int q) -> Ahead {
+    Ahead h;
+    h.q = q;
+    h.pid = -1;
+    h.seg = h.p0 = h.p1 = 0;
+    if (q < n) {  // entries past n were never written
+      const int2 te = ptab[q];
+      h.pid = te.x;
+      h.seg = te.y;
+      h.p0 = prefix[te.y >> 3];
+      h.p1 = prefix[(te.y >> 3) + 1];
+    }
+    return h;
+  };
+  // Stage a unit: the tiles now; the q / new-token / rope rows now unless
+  // `defer` (they may depend on the previous kernel).
+  auto stage_unit = [&](int stage, const Ahead& h, bool defer) {
+    if (h.q >= n) {
       if (lane == 0) my_meta[stage] = make_int4(-1, 0, 0, -1);
       __syncwarp();
       return;
     }
-    const int2 te = ptab[q];
-    const int pid = te.x, seg = te.y, ss = te.y >> 3, gg = te.y & 7;
-    const int np = prefix[ss + 1] - prefix[ss];
-    const int jj = (int)(unit_of(q) - (8u * (uint32_t)prefix[ss] + (uint32_t)(gg * np)));
+    const int q = h.q, pid = h.pid, seg = h.seg, ss = h.seg >> 3, gg = h.seg & 7;
+    const int np = h.p1 - h.p0;
+    const int jj = (int)(unit_of(q) - (8u * (uint32_t)h.p0 + (uint32_t)(gg * np)));
     const bool need_q = seg != last_seg;
     last_seg = seg;
     const bool is_last = kAppend && jj == np - 1;
@@ -1175,10 +1191,9 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
         mbar_arrive_expect_tx(bar, bytes);
         if (pid >= 0) {
           const uint32_t dst = tiles0 + stage * kStageBytes;
-          tma_load_3d(dst, &tmap, 0, 0, (pid * 2 + 0) * PKV_NUM_KV_HEADS + gg, bar);
-          tma_load_3d(dst + kTileBytes, &tmap, 0, 0, (pid * 2 + 1) * PKV_NUM_KV_HEADS + gg, bar);
+          tma_load_4d(dst, &tmap, 0, 0, gg, pid * 2, bar);  // K tile, then V tile
         }
-        if (!defer) stage_rows(stage);
+        if (!defer) stage_rows(stage, ss, gg, need_q, is_last, pid);
       }
     }
     ph ^= 1u << stage;
@@ -1277,12 +1292,14 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
   };
 
   // prologue: two units in flight (tiles only before the wait with `early`)
-  for (int stg = 0; stg < kDynStages; ++stg) stage_unit(stg, claim(), p.early != 0);
+  for (int stg = 0; stg < kDynStages; ++stg) stage_unit(stg, look_ahead(claim()), p.early != 0);
   if (p.early) {
     pdl_wait();
     if (lane == 0)
-      for (int stg = 0; stg < kDynStages; ++stg)
-        if (my_meta[stg].x >= 0) stage_rows(stg);
+      for (int stg = 0; stg < kDynStages; ++stg) {
+        const int4 mt = my_meta[stg];
+        if (mt.x >= 0) stage_rows(stg, mt.y, mt.z & 7, (mt.z >> 3) & 1, (mt.z >> 4) & 1, mt.w);
+      }
     __syncwarp();
   }
 
@@ -1290,6 +1307,10 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
     const int stage = k % kDynStages;
     const int4 mt = my_meta[stage];
     if (mt.x < 0 || vctl[1] != 0) break;
+    // the next unit of this warp's chunk, read before the page is computed (a
+    // new chunk is claimed only after it, so claims do not run ahead)
+    const bool in_chunk = cq < ce;
+    const Ahead nxt = look_ahead(in_chunk ? cq++ : n);
     if (!mbar_wait_bounded(bars0 + 8 * stage, ((ph >> stage) & 1u) ^ 1u, kWaitLimitNs)) {
       failed = true;
       if (lane == 0) {
@@ -1340,7 +1361,7 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
     }
     ++m_units;
     __syncwarp();
-    stage_unit(stage, claim(), false);
+    stage_unit(stage, in_chunk ? nxt : look_ahead(claim()), false);
   }
   if (!failed && vctl[1] == 0) {
     if (!flush() && lane == 0) {
@@ -1429,9 +1450,10 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Pool viewed as a 3-D tensor: x = dim (64), y = token slot (16),
-// z = (page * 2 + kv) * 8 + head.  One box = one 2 KiB (page, kv, head) tile,
-// stored in shared memory with the 128-byte swizzle.
+// Pool viewed as a 4-D tensor: dim (64), token slot (16), head (8),
+// page * 2 + kv.  One box {64, 16, 1, 2} = the K and V tiles of one (page,
+// head), 2 x 2 KiB, stored in shared memory with the 128-byte swizzle (16
+// rows of 128 bytes each, so the V tile starts a fresh swizzle period).
 static int make_pool_map(CUtensorMap* map, const void* pool, int num_pages) {
   struct Cached {
     const void* ptr = nullptr;
@@ -1448,11 +1470,13 @@ static int make_pool_map(CUtensorMap* map, const void* pool, int num_pages) {
     set_last_error("cudaGetDriverEntryPointByVersion", "cuTensorMapEncodeTiled unavailable");
     return PKV_ERR_CUDA;
   }
-  const cuuint64_t dims[3] = {64, 16, (cuuint64_t)num_pages * 16};
-  const cuuint64_t strides[2] = {128, 2048};
-  const cuuint32_t box[3] = {64, 16, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides,
+  // (dim, token, head, 2 page + K/V): one box {64, 16, 1, 2} is the K tile and
+  // then the V tile of one (page, head), 4 KiB, in a single copy
+  const cuuint64_t dims[4] = {64, 16, PKV_NUM_KV_HEADS, (cuuint64_t)num_pages * 2};
+  const cuuint64_t strides[3] = {128, 2048, 2048 * PKV_NUM_KV_HEADS};
+  const cuuint32_t box[4] = {64, 16, 1, 2};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
