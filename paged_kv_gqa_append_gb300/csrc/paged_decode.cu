@@ -93,8 +93,8 @@ struct SmemLayout {
   static constexpr int kTiles = kWarps * kStages * kStageBytes;
   static constexpr int kBars = kTiles;                                 // u64 [kWarps][kStages]
   static constexpr int kPid = kBars + kWarps * kStages * 8;            // int [kWarps][kStages]
-  static constexpr int kBad = kPid + kWarps * kStages * 4;             // int [kWarps]
-  static constexpr int kSlots = kBad + ((kWarps * 4 + 15) / 16) * 16;  // Record [kWarps]
+  static constexpr int kCnt = kPid + kWarps * kStages * 4;             // int [kWarps + 1]
+  static constexpr int kSlots = kCnt + (((kWarps + 1) * 4 + 15) / 16) * 16;  // Record [kWarps]
   static constexpr int kPrefix = kSlots + kWarps * kRecordBytes;       // int [S + 1], then len [S]
   static size_t bytes(int num_seqs) { return 1024 + kPrefix + 4 * (size_t)(2 * num_seqs + 1); }
   // Slot 0 (dedicated) holds the warp's record for a segment that began
@@ -280,6 +280,32 @@ struct MergeAcc {
     const int hh = lane >> 3, d0 = (lane & 7) * 8;
     const float4* src = reinterpret_cast<const float4*>(r.o + hh * 64 + d0);
     add(r.ml[hh], src[0], src[1]);
+  }
+
+  // Merge of records in shared memory in two passes: the largest m first, then
+  // the sum of the rescaled records (independent terms, no rescale chain).
+  // `each(f)` calls f(record) for every record to merge.
+  template <class Each>
+  __device__ __forceinline__ void merge_shared(Each each, int lane) {
+    const int hh = lane >> 3, d0 = (lane & 7) * 8;
+    float Mx = -INFINITY;
+    each([&](const Record& r) {
+      const float2 ml = r.ml[hh];
+      if (ml.y < 0.f) bad = true;
+      else Mx = fmaxf(Mx, ml.x);
+    });
+    each([&](const Record& r) {
+      const float2 ml = r.ml[hh];
+      if (ml.y >= 0.f) {
+        const float w = (ml.x == Mx) ? 1.f : exp2f(ml.x - Mx);
+        const float4* src = reinterpret_cast<const float4*>(r.o + hh * 64 + d0);
+        const float4 o0 = src[0], o1 = src[1];
+        acc[0] += w * o0.x; acc[1] += w * o0.y; acc[2] += w * o0.z; acc[3] += w * o0.w;
+        acc[4] += w * o1.x; acc[5] += w * o1.y; acc[6] += w * o1.z; acc[7] += w * o1.w;
+        L += w * ml.y;
+      }
+    });
+    M = Mx;
   }
 
   // record in global memory written by another CTA: read through L2 only
@@ -747,8 +773,12 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + Smem::kPrefix);
   int32_t* slen = prefix + (p.num_seqs + 1);
   int* spid = reinterpret_cast<int*>(smem + Smem::kPid);
+  // per crossing segment: covering warps counted in (key: the warp where it
+  // starts, or kWarps for the one that began before the CTA's range)
+  int* seg_cnt = reinterpret_cast<int*>(smem + Smem::kCnt);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.num_seqs;
+  if (threadIdx.x <= kWarps) seg_cnt[threadIdx.x] = 0;  // ordered by build_prefix's barriers
 
   // Without `early` everything waits for the previous kernel here.  With it,
   // only reads of q and the new token, and every global write, wait (below).
@@ -763,8 +793,6 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
   const uint32_t u1 = a + range_start(warp + 1, b - a, kWarps);
   const int n_units = (int)(u1 - u0);
 
-  int* warp_bad = reinterpret_cast<int*>(smem + Smem::kBad);
-  if (lane == 0) warp_bad[warp] = 0;
   if (n_units > 0) {
     const uint32_t tiles = smem_u32(smem) + warp * kStages * kStageBytes;
     const uint32_t bars = smem_u32(smem + Smem::kBars) + warp * kStages * 8;
@@ -828,6 +856,58 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
     enter_segment();
     bool seg_bad = false;
 
+    // A segment that crosses warp ranges: this warp's record is in its slot;
+    // count it in, and the last of the CTA's covering warps merges them all
+    // at once (no CTA-wide barrier) and finalises the segment -- after its own
+    // last page, if it still has pages to stream (fin_* below).
+    int fin_s = -1, fin_g = 0;
+    uint32_t fin_base = 0, fin_np = 0;
+    auto finalise = [&](int s, int g, uint32_t base, uint32_t np) {
+      const uint32_t last = base + np - 1;
+      const uint32_t lo = max(base, a), hi = min(last, b - 1), n_cta = b - a;
+      const int j0 = (int)owner_of(lo - a, n_cta, kWarps), j1 = (int)owner_of(hi - a, n_cta, kWarps);
+      // the records of the covering warps with non-empty ranges
+      auto each = [&](auto f) {
+        uint32_t v0 = range_start(j0, n_cta, kWarps);
+        for (int j = j0; j <= j1; ++j) {
+          const uint32_t v1 = range_start(j + 1, n_cta, kWarps);
+          if (v1 > v0) f(Smem::slot(smem, j, base < a + v0 ? 0 : 1));
+          v0 = v1;
+        }
+      };
+      MergeAcc m;
+      m.init();
+      m.merge_shared(each, lane);
+      if (base >= a && last < b)
+        m.store_output(p, s, g, lane);
+      else
+        cross_cta_merge(p, m, s, g, base, np, U, NC, c, lane);
+    };
+    auto count_in = [&](int s, int g, uint32_t base, uint32_t np, bool more) {
+      const uint32_t last = base + np - 1;
+      const uint32_t lo = max(base, a), hi = min(last, b - 1), n_cta = b - a;
+      const int j0 = (int)owner_of(lo - a, n_cta, kWarps), j1 = (int)owner_of(hi - a, n_cta, kWarps);
+      int total = 0;
+      for (int j = j0; j <= j1; ++j) total += range_start(j + 1, n_cta, kWarps) > range_start(j, n_cta, kWarps);
+      int old = 0;
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();  // the record before the count
+        old = atomicAdd(seg_cnt + (base < a ? kWarps : j0), 1);
+      }
+      old = __shfl_sync(0xffffffffu, old, 0);
+      if (old + 1 != total) return;
+      __threadfence_block();
+      if (more) {  // keep streaming; finalise after this warp's last page
+        fin_s = s;
+        fin_g = g;
+        fin_base = base;
+        fin_np = np;
+      } else {
+        finalise(s, g, base, np);
+      }
+    };
+
     for (int uc = 0; uc < n_units; ++uc) {
       const int stage = uc % kStages;
       const uint32_t parity = (uint32_t)(uc / kStages) & 1u;
@@ -858,10 +938,12 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
       if (seg_end) {
         const uint32_t base = seg_base(cc, prefix), last = base + (uint32_t)cc.np - 1;
         const bool before = base < u0, after = last >= u1;
-        if (!before && !after)
+        if (!before && !after) {
           st.write_output(p, cc.s, cc.g, seg_bad, lane);
-        else if (before || !timed_out)  // tiles may still be receiving after a timeout
+        } else if (!timed_out) {  // after a timeout the segment is left unfinished
           st.write_record(Smem::slot(smem, warp, before ? 0 : 1), seg_bad, lane);
+          count_in(cc.s, cc.g, base, (uint32_t)cc.np, uc + 1 < n_units);
+        }
         st.reset();
         seg_bad = false;
       }
@@ -872,8 +954,8 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
       }
       __syncwarp();
     }
+    if (fin_s >= 0 && !timed_out) finalise(fin_s, fin_g, fin_base, fin_np);
     if (timed_out) {
-      if (lane == 0) warp_bad[warp] = 1;
       // Drain whatever this warp still has in flight before leaving (bounded).
       for (int u = max(0, iv - kStages); u < iv; ++u) {
         const int stage = u % kStages;
@@ -897,39 +979,6 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
         if (kAppend && p.q_out != nullptr)
           reinterpret_cast<uint4*>(p.q_out)[i] = make_uint4(0u, 0u, 0u, 0u);
       }
-    }
-  }
-  __syncthreads();
-
-  // Merge the segments that cross warp ranges.  A warp merges (A) its last
-  // segment when that one starts inside its range and runs past it, and the
-  // CTA's first non-empty warp also merges (B) a segment that started before
-  // the CTA range.  Records of the following warps are in their slot 0.
-  if (n_units > 0) {
-    const uint32_t first_warp = owner_of(0, b - a, kWarps);
-    for (int which = 0; which < 2; ++which) {
-      if (which == 0 && (uint32_t)warp != first_warp) continue;
-      Cursor cs;
-      cursor_seek(cs, which == 0 ? u0 : u1 - 1, prefix, S);
-      const uint32_t base = seg_base(cs, prefix), last = base + (uint32_t)cs.np - 1;
-      if (which == 0 && !(base < a)) continue;
-      if (which == 1 && !(base >= u0 && last >= u1)) continue;
-      MergeAcc m;
-      m.init();
-      m.add_shared(Smem::slot(smem, warp, which == 0 ? 0 : 1), lane);
-      m.bad |= warp_bad[warp] != 0;
-      for (int j = warp + 1; j < kWarps; ++j) {
-        const uint32_t v0 = a + range_start(j, b - a, kWarps);
-        const uint32_t v1 = a + range_start(j + 1, b - a, kWarps);
-        if (v0 >= v1) continue;  // empty warp range
-        if (v0 > last) break;
-        m.add_shared(Smem::slot(smem, j, 0), lane);
-        m.bad |= warp_bad[j] != 0;
-      }
-      if (base >= a && last < b)
-        m.store_output(p, cs.s, cs.g, lane);
-      else
-        cross_cta_merge(p, m, cs.s, cs.g, base, (uint32_t)cs.np, U, NC, c, lane);
     }
   }
 }
