@@ -1599,6 +1599,22 @@ static int setup_kernel(int device, size_t smem, int* occ) {
   return PKV_OK;
 }
 
+// A segment split between two CTAs costs a record hand-off through global
+// memory at the end of the launch: about as long as streaming kCrossUnits
+// more units per CTA (measured on the 32 x 2048 batch).  With every sequence
+// at the length bound there are 8 S segments of `pages_bound` units each; if
+// the CTAs can hold k whole segments each (k dividing 8 S) at a load within
+// kCrossUnits of the even split, take that grid of 8 S / k CTAs instead.
+constexpr long long kCrossUnits = 64;
+static long long whole_segment_grid(long long nc, int num_seqs, long long pages_bound) {
+  const long long n_seg = 8ll * num_seqs;
+  if (nc < 2 || pages_bound < 1 || n_seg <= nc) return nc;
+  const long long k = (n_seg + nc - 1) / nc;
+  if (n_seg % k != 0) return nc;
+  if (k * pages_bound * nc > n_seg * pages_bound + kCrossUnits * nc) return nc;
+  return n_seg / k;
+}
+
 template <class State, int kWarps, int kStages, bool kAppend = false>
 static int launch_decode(const DecodeParams& prm, const CUtensorMap& map, int device, int num_sms,
                          int max_seq_len, int min_units, int ctas_per_sm, cudaStream_t stream) {
@@ -1615,6 +1631,7 @@ static int launch_decode(const DecodeParams& prm, const CUtensorMap& map, int de
   const long long want = (u_bound + (long long)kWarps * min_units - 1) / ((long long)kWarps * min_units);
   if (want < nc) nc = want;
   if (nc < 1) nc = 1;
+  if (occ == 1) nc = whole_segment_grid(nc, prm.num_seqs, pages_bound);
 
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1665,6 +1682,7 @@ static int launch_decode_dyn(const DecodeParams& prm, const CUtensorMap& map, in
   const long long want = (u_bound + per - 1) / per;
   if (want < nc) nc = want;
   if (nc < 1) nc = 1;
+  nc = whole_segment_grid(nc, prm.num_seqs, pages_bound);
   // page-id table: the most units any CTA can own for lengths the kernel accepts
   const long long max_len = kAppend ? std::min<long long>(16ll * prm.max_blocks, prm.max_pos)
                                     : 16ll * prm.max_blocks;
