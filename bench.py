@@ -49,6 +49,11 @@ def parse():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", choices=["batch32", "stress256"], default="batch32")
     ap.add_argument("--compute", choices=["tensor", "fma"], default="tensor")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layers of the workload (0 = its own: 16); fewer layers shrink the pool "
+                         "for a profiler capture of the same kernel shape")
+    ap.add_argument("--schedule", choices=["static", "dynamic"], default="static",
+                    help="decode schedule (opts.schedule 0 or 1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--unfused", action="store_true",
@@ -56,8 +61,13 @@ def parse():
     return ap.parse_args()
 
 
-def make_case(name):
-    return W.case_batch32() if name == "batch32" else W.case_stress()
+def make_case(name, layers=0):
+    case = W.case_batch32() if name == "batch32" else W.case_stress()
+    if layers and layers != case.num_layers:  # same batch, context and seed, fewer layers
+        case = W.case_uniform(case.seed, case.num_seqs, layers, int(case.seq_lens[0]),
+                              outlier_frac=case.outlier_frac,
+                              name=case.name.replace(f"_l{case.num_layers}_", f"_l{layers}_"))
+    return case
 
 
 # ------------------------------------------------------------- distributed --
@@ -226,7 +236,7 @@ def cpu_cores_used():
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    case = make_case(args.workload)
+    case = make_case(args.workload, args.layers)
     ora = OracleSample(case)
     # warm-up steps, then K timed steps; each step = one (layer, seq) pair
     for _ in range(args.warmup):
@@ -258,7 +268,7 @@ def run_gb300(args, world, rank, local):
     import paged_kv_gqa_append_gb300 as pkv
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    case = make_case(args.workload)
+    case = make_case(args.workload, args.layers)
     L, S = case.num_layers, case.num_seqs
     compute = pkv.COMPUTE_TENSOR if args.compute == "tensor" else pkv.COMPUTE_FMA
 
@@ -274,7 +284,8 @@ def run_gb300(args, world, rank, local):
     step = pkv.DecodeStep(pool, bt, lens, pos, k_new, v_new, q_raw, out, cos, sin, case.scale,
                           max_seq_len=case.max_seq_len,
                           compute=None if compute == pkv.COMPUTE_TENSOR else compute,
-                          fused=not args.unfused)
+                          fused=not args.unfused,
+                          schedule=1 if args.schedule == "dynamic" else 0)
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(args.warmup):
@@ -321,6 +332,21 @@ def run_gb300(args, world, rank, local):
         r1.record(stream)
         torch.cuda.synchronize()
         dec_avg_ms = r0.elapsed_time(r1) / (k_roof * L)
+    # ---- the append kernel alone (kv_append_rope of the step's tokens) -----
+    g_app = step.append_only_graph()
+    for _ in range(3):
+        g_app.replay()
+    k_app = max(10, args.steps // 4)
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    p0.record(stream)
+    for _ in range(k_app):
+        g_app.replay()
+    p1.record(stream)
+    torch.cuda.synchronize()
+    append_us = p0.elapsed_time(p1) * 1e3 / (k_app * L)
+    if step.error() != 0:
+        raise RuntimeError("device error in the append timing")
     t_wall2 = time.time()
     clk = clocks.summary(t_wall0, t_wall2) if clocks else None
     if clocks:
@@ -374,6 +400,8 @@ def run_gb300(args, world, rank, local):
     achieved = kv_bytes_layer / (dec_avg_ms / 1e3) / 1e9
     tag = ("paged_decode_append" if step.fused else
            "paged_decode_" + ("mma" if compute == pkv.COMPUTE_TENSOR else "fma"))
+    if args.schedule == "dynamic":
+        tag += "_dyn"
     traffic = ncu_traffic(f"{tag}:{case.name}")
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
@@ -401,10 +429,12 @@ def run_gb300(args, world, rank, local):
                        "pool_bytes": case.num_pages * W.PAGE_ELEMS * 2,
                        "l2": "inputs larger than L2 (pool read per step exceeds 129 MB L2)",
                        "parallelism": f"replicas x{world}", "compute": args.compute,
+                       "schedule": args.schedule,
                        "launch": ("CUDA graph of the step: one fused append+decode kernel per layer"
                                   if step.fused else
                                   "CUDA graph of the step: append kernel + decode kernel per layer")},
             "tokens_per_s": tokens_per_s, "us_per_layer": us_per_layer,
+            "append_us_per_layer": append_us,
             "kv_bytes_per_step": kv_bytes_layer * L,
             "hbm_frac_step": value / world / peak,
             "clocks": clk, "e2e": e2e, "gpu_launches": step.launches_per_step * steps,

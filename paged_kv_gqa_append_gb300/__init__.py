@@ -442,7 +442,7 @@ class DecodeStep:
 
     def __init__(self, pool, block_tables, seq_lens, positions, k, v, q, out, rope_cos, rope_sin,
                  scale, max_seq_len=None, workspace=None, d_err=None, q_rot=None, compute=None,
-                 use_graph=True, stream=None, fused=True, overlap_layers=True):
+                 use_graph=True, stream=None, fused=True, overlap_layers=True, schedule=0):
         self.L, self.S = block_tables.shape[0], block_tables.shape[1]
         self.t = dict(pool=pool, bt=block_tables, lens=seq_lens, pos=positions, k=k, v=v, q=q,
                       out=out, cos=rope_cos, sin=rope_sin)
@@ -454,6 +454,7 @@ class DecodeStep:
         self.max_seq_len = max_seq_len
         self.compute = compute
         self.overlap = bool(overlap_layers)
+        self.schedule = int(schedule)
         # the fused kernel places each new token at seq_lens - 1 (positions unused)
         self.fused = fused and compute in (None, COMPUTE_TENSOR)
         self.launches_per_step = (1 if self.fused else 2) * self.L
@@ -473,7 +474,8 @@ class DecodeStep:
                                         t["lens"], t["out"][l], t["cos"], t["sin"], self.scale,
                                         q_out=self.q_rot[l], workspace=self.workspace,
                                         max_seq_len=self.max_seq_len, d_err=self.d_err,
-                                        early_kv=int(self.overlap and l > 0))
+                                        early_kv=int(self.overlap and l > 0),
+                                        schedule=self.schedule)
             return
         for l in range(self.L):
             if not decode_only:
@@ -483,13 +485,25 @@ class DecodeStep:
             paged_gqa_decode(self.q_rot[l], t["pool"], t["bt"][l], t["lens"], t["out"][l],
                              self.scale, workspace=self.workspace, max_seq_len=self.max_seq_len,
                              d_err=self.d_err, compute=self.compute,
-                             early_kv=int(self.overlap and decode_only and l > 0))
+                             early_kv=int(self.overlap and decode_only and l > 0),
+                             schedule=self.schedule)
 
     def run(self):
         if self.graph is not None:
             self.graph.replay()
         else:
             self._launch()
+
+    def append_only_graph(self):
+        """A graph of just the L kv_append_rope calls of the step (tokens at
+        `positions`, q rotated into the step's q_rot buffer)."""
+        t = self.t
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for l in range(self.L):
+                kv_append_rope(t["k"][l], t["v"][l], t["pos"], t["bt"][l], t["pool"], t["cos"],
+                               t["sin"], q_in=t["q"][l], q_out=self.q_rot[l], d_err=self.d_err)
+        return g
 
     def decode_only_graph(self):
         """A graph of just the L decode calls (for timing the decode kernel)."""
