@@ -151,6 +151,51 @@ def decode(q_bits, pool, block_tables, seq_lens, scale: float):
     return out, err
 
 
+def prefill(q_bits, cu_q, pool, block_tables, seq_lens, scale: float):
+    """Causal GQA attention of each sequence's newest tokens over its own pages.
+
+    From the samir-vllm article ("Gestion de la KV cache et strategies de
+    batching"): attention reads only the sequence's pages; a token at
+    absolute position p sees the positions up to its own.  Sequence s holds
+    n = seq_lens[s] tokens in its pages; its queries are the last
+    q_len = cu_q[s+1] - cu_q[s] of them, at positions n - q_len .. n - 1,
+    rows cu_q[s] .. cu_q[s+1] - 1 of q (a whole prompt is q_len == n; a chunk
+    after a cached prefix has q_len < n).
+
+    q_bits: uint16 [T][32][64] (rotated); cu_q: [S + 1]; block_tables:
+    [S][max_blocks]; seq_lens: [S].  Returns (out float64 [T][32][64],
+    error_flag).  The rows of a sequence with q_len < 0 or q_len > n, an n
+    outside [0, 16 * max_blocks] or a bad needed page id stay zero and raise
+    the flag.
+    """
+    T = q_bits.shape[0]
+    S = len(seq_lens)
+    max_blocks = block_tables.shape[1]
+    out = np.zeros((T, NUM_Q_HEADS, HEAD_DIM))
+    err = False
+    q = bf16.to_f64(q_bits)
+    for s in range(S):
+        n = int(seq_lens[s])
+        r0, r1 = int(cu_q[s]), int(cu_q[s + 1])
+        q_len = r1 - r0
+        if q_len < 0 or q_len > n or n > PAGE_TOKENS * max_blocks:
+            err = True
+            continue
+        if q_len == 0:
+            continue
+        kv = gather(pool, block_tables[s], n)
+        if kv is None:
+            err = True
+            continue
+        K, V = kv
+        for i in range(q_len):
+            p = n - q_len + i
+            for h in range(NUM_Q_HEADS):
+                g = h // GROUP
+                out[r0 + i, h] = attend(q[r0 + i, h], K[:p + 1, g, :], V[:p + 1, g, :], scale)
+    return out, err
+
+
 def decode_step(pool, q_bits, k_bits, v_bits, block_tables, seq_lens, cos, sin, scale: float):
     """One decode step: append each sequence's new token, then attend.
 
