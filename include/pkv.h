@@ -291,6 +291,38 @@ int paged_gqa_decode_append(const void* q, const void* k_new, const void* v_new,
                             void* workspace, size_t workspace_bytes,
                             int* d_err, void* stream, const pkv_decode_opts* opts);
 
+/* ------------------------------------------------------------------------
+ * paged_gqa_prefill - causal GQA attention of each sequence's newest tokens
+ * over its own pages: a whole prompt, or a chunk of one after a cached
+ * prefix ("Gestion de la KV cache et strategies de batching": attention
+ * reads only the sequence's pages; a token at position p sees positions
+ * up to its own).
+ *
+ * Sequence s holds n = seq_lens[s] tokens in its pages (already written,
+ * e.g. by kv_append_rope earlier on the stream); its queries are the last
+ * q_len = cu_q[s+1] - cu_q[s] of them, at positions n - q_len .. n - 1, and
+ * are rows cu_q[s] .. cu_q[s+1] - 1 of q and out:
+ *   out[t][h] = sum_{j <= p_t} softmax_j(scale * q[t][h] . K_j[h/4]) V_j[h/4].
+ *
+ *   q           device bf16 [num_tokens][32][64], rotated
+ *   cu_q        device int32 [num_seqs + 1], row offsets (cu_q[0] = 0)
+ *   kv_pool     device bf16 pool (read only), num_pages pages
+ *   block_tables, bt_row_stride, max_blocks, seq_lens: as paged_gqa_decode
+ *   max_q_len   host upper bound of every q_len (sizes the grid)
+ *   out         device bf16 [num_tokens][32][64]
+ * bf16 mma.sync with fp32 accumulation and an online softmax, one CTA per
+ * (32 query tokens, KV head, sequence); deterministic.  A sequence whose
+ * rows fall outside [0, num_tokens) or whose q_len is negative is left
+ * untouched; one with q_len > n, q_len > max_q_len, n above
+ * 16 * max_blocks or a needed page id outside [0, num_pages) gets zero
+ * rows; both set *d_err = PKV_ERR_DEVICE_INDEX.  No workspace.
+ * ---------------------------------------------------------------------- */
+int paged_gqa_prefill(const void* q, int num_tokens, const int32_t* cu_q,
+                      const void* kv_pool, int num_pages,
+                      const int32_t* block_tables, int bt_row_stride, int max_blocks,
+                      const int32_t* seq_lens, int num_seqs, int max_q_len,
+                      void* out, float scale, int* d_err, void* stream);
+
 /* Wait for `stream`, then copy the device error word to *code_out (host).
  * If `clear` is non-zero the word is reset to 0 afterwards. */
 int pkv_read_device_error(int* d_err, void* stream, int clear, int* code_out);

@@ -67,6 +67,7 @@ _SIGS = {
     "pkv_rope_table_fill": (_i, [_p, _p, _i, _p]),
     "kv_append_rope": (_i, [_p, _p, _p, _p, _i, _p, _i, _i, _i, _p, _i, _p, _p, _i, _p, _p, _p, _p]),
     "paged_gqa_decode_workspace_bytes": (_sz, [_i]),
+    "paged_gqa_prefill": (_i, [_p, _i, _p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _p]),
     "paged_gqa_decode": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p, _p]),
     "paged_gqa_decode_ex": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p, _p,
                                  ctypes.POINTER(DecodeOpts)]),
@@ -335,6 +336,41 @@ def paged_gqa_decode_append(q, k_new, v_new, kv_pool, block_tables, seq_lens, ou
         int(max_seq_len), _ptr(q_out), _ptr(out), float(scale), _ptr(workspace),
         workspace.numel(), _ptr(d_err), _stream(stream), ctypes.byref(opts))
     _check(st, "paged_gqa_decode_append")
+
+
+def paged_gqa_prefill(q, cu_q, kv_pool, block_tables, seq_lens, out, scale, max_q_len=None,
+                      d_err=None, max_blocks=None, stream=None):
+    """Causal attention of each sequence's last q_len tokens over its own pages.
+
+    q, out: [T, 32, 64] bf16 (q rotated); cu_q: [S + 1] int32 row offsets on
+    the device; seq_lens: [S] int32 tokens held (the queries are the last
+    cu_q[s+1] - cu_q[s] of them).  max_q_len: host bound of every q_len
+    (default T).
+    """
+    dev = kv_pool.device
+    _need(kv_pool, "kv_pool", torch.bfloat16, dev, (2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM))
+    _need(q, "q", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
+    _need(out, "out", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
+    T = q.numel() // (NUM_Q_HEADS * HEAD_DIM)
+    if out.numel() != q.numel():
+        raise ValueError("out must match q")
+    _need(cu_q, "cu_q", torch.int32, dev)
+    _need(seq_lens, "seq_lens", torch.int32, dev)
+    S = seq_lens.numel()
+    if cu_q.numel() != S + 1:
+        raise ValueError("cu_q must have num_seqs + 1 entries")
+    _need(block_tables, "block_tables", torch.int32, dev)
+    if block_tables.dim() != 2 or block_tables.shape[0] < S:
+        raise ValueError("block_tables must be [>= num_seqs, row_stride]")
+    stride = block_tables.shape[1]
+    mb = stride if max_blocks is None else max_blocks
+    if d_err is not None:
+        _need(d_err, "d_err", torch.int32, dev)
+    st = _L().paged_gqa_prefill(_ptr(q), T, _ptr(cu_q), _ptr(kv_pool), kv_pool.shape[0],
+                                _ptr(block_tables), stride, mb, _ptr(seq_lens), S,
+                                int(T if max_q_len is None else max_q_len), _ptr(out),
+                                float(scale), _ptr(d_err), _stream(stream))
+    _check(st, "paged_gqa_prefill")
 
 
 def pkv_read_device_error(d_err, clear: bool = True, stream=None) -> int:

@@ -1,6 +1,7 @@
 // Host-side helpers shared by the C-ABI entry points (not part of the ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -28,5 +29,11 @@ inline int cuda_status(cudaError_t e, const char* where = "cuda") {
   (void)cudaGetLastError();  // clear the non-sticky error state for the next call
   return PKV_ERR_CUDA;
 }
+
+// TMA tensor map of the pool [num_pages][2][8][16][64] bf16 viewed as
+// (dim 64, slot 16, head 8, page * 2 + kv), box {64, 16, 1, 2} (the K then V
+// tile of one (page, head)), 128-byte swizzle; cached per thread for the
+// last (pool, num_pages).  Returns PKV_OK or PKV_ERR_CUDA.
+int make_pool_map(CUtensorMap* map, const void* pool, int num_pages);
 
 }  // namespace pkv

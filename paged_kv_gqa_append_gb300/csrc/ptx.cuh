@@ -109,15 +109,26 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 // holds this lane's two entries of row lane/4 only.
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0,
                                                uint32_t b1) {
-  float z0, z1;
+  float t[4] = {d[0], d[1], 0.f, 0.f};
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %11, %12, %13};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(z0), "=f"(z1)
-      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(d[0]), "f"(d[1]), "f"(0.f),
-        "f"(0.f));
-  (void)z0;
-  (void)z1;
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(t[0]), "+f"(t[1]), "+f"(t[2]), "+f"(t[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+  d[0] = t[0];
+  d[1] = t[1];
+}
+
+// D(16x8, fp32) += A(16x16, bf16, row) * B(16x8, bf16, col), all 16 rows real:
+// d = {row lane/4: cols 2 (lane%4), +1; row lane/4 + 8: the same cols}.
+__device__ __forceinline__ void mma_bf16_16816_full(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                    uint32_t a2, uint32_t a3, uint32_t b0,
+                                                    uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // ---- bf16 helpers ----------------------------------------------------------

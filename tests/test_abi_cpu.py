@@ -90,6 +90,16 @@ def test_host_side_validation_returns_before_launch():
                               1 << 30, null, null) == 3
     assert L.paged_gqa_decode(fake, fake, 8, fake, 128, 128, fake, 1, 16, fake, float("nan"), fake,
                               1 << 20, null, null) == 1
+    # prefill: nothing to do; nulls; stride < max_blocks; misaligned q; NaN scale; too many seqs
+    PF = L.paged_gqa_prefill
+    assert PF(null, 0, null, null, 8, null, 128, 128, null, 0, 16, null, 0.125, null, null) == 0
+    assert PF(null, 16, null, null, 8, null, 128, 128, null, 1, 16, null, 0.125, null, null) == 1
+    assert PF(fake, 16, fake, fake, 8, fake, 64, 128, fake, 1, 16, fake, 0.125, null, null) == 1
+    assert PF(odd, 16, fake, fake, 8, fake, 128, 128, fake, 1, 16, fake, 0.125, null, null) == 2
+    assert PF(fake, 16, fake, fake, 8, fake, 128, 128, fake, 1, 16, fake, float("nan"), null,
+              null) == 1
+    assert PF(fake, 16, fake, fake, 8, fake, 128, 128, fake, 70000, 16, fake, 0.125, null,
+              null) == 3
 
 
 def _run_cpp_schedule(case):
