@@ -351,6 +351,12 @@ int pkv_credit_pages(int prompt_tokens, int allowed_new_tokens, int num_layers);
 pkv_sched* pkv_sched_create(int num_pages, int num_layers, int max_blocks, int max_slots);
 void pkv_sched_destroy(pkv_sched* s);
 
+/* Batching mode ("Gestion de la KV cache et strategies de batching": two
+ * modes): 0 = continuous (default), admit whenever the head of the queue
+ * fits; 1 = static, admit only when no request is running, i.e. wait for
+ * the current group to finish, then admit the FIFO prefix that fits. */
+int pkv_sched_set_mode(pkv_sched* s, int mode);
+
 /* Queue a request; *req_id (host, out) gets its id.  Returns
  * PKV_ERR_REQUEST_TOO_LARGE (not queued) if its credit exceeds the pool or
  * its length exceeds max_blocks pages. */

@@ -2,7 +2,7 @@
 
 From the samir-vllm article, "Gestion de la KV cache et strategies de batching":
   * continuous batching admits a request as soon as its page budget is
-    available;
+    available; static batching waits for the current group to finish;
   * the admission credit is prompt_tokens + allowed_new_tokens - 1 tokens,
     rounded up to 16-token pages, for each layer;
   * a request whose budget exceeds the whole pool is rejected with an explicit
@@ -20,7 +20,10 @@ Readings where the article is silent (the C++ scheduler follows the same rules):
     0 comes first);
   * a finished request returns its pages layer by layer in logical order,
     pushed onto the stack in that order; its slot (block-table row) is freed;
-  * a new request takes the lowest free slot.
+  * a new request takes the lowest free slot;
+  * static batching: no request is admitted while any request of the
+    current group is still running; once all have finished, the next group
+    is the FIFO prefix admitted by the same fit rule.
 """
 from __future__ import annotations
 
@@ -39,8 +42,12 @@ class Scheduler:
     """FIFO admission with credit reservation and on-demand page allocation."""
 
     OK, EXHAUSTED, TOO_LARGE, INVALID = "ok", "exhausted", "too_large", "invalid"
+    CONTINUOUS, STATIC = "continuous", "static"
 
-    def __init__(self, num_pages: int, num_layers: int, max_blocks: int, max_slots: int):
+    def __init__(self, num_pages: int, num_layers: int, max_blocks: int, max_slots: int,
+                 mode: str = CONTINUOUS):
+        assert mode in (self.CONTINUOUS, self.STATIC)
+        self.mode = mode
         self.num_pages = num_pages
         self.num_layers = num_layers
         self.max_blocks = max_blocks
@@ -72,8 +79,12 @@ class Scheduler:
         return self.OK, rid
 
     def admit(self):
-        """Admit queued requests in FIFO order while the head fits.  Returns ids."""
+        """Admit queued requests in FIFO order while the head fits.  Returns ids.
+
+        In static mode nothing is admitted while a request is running."""
         admitted = []
+        if self.mode == self.STATIC and any(r["state"] == "running" for r in self.req.values()):
+            return admitted
         while self.queue:
             rid = self.queue[0]
             r = self.req[rid]
@@ -126,7 +137,7 @@ class Scheduler:
 
 
 def simulate(prompt_lens, decode_steps: int, num_pages: int, num_layers: int,
-             max_blocks: int = 128, max_slots: int = 256):
+             max_blocks: int = 128, max_slots: int = 256, mode: str = Scheduler.CONTINUOUS):
     """Run the continuous-batching schedule; return the per-step event log.
 
     Step loop: admit (FIFO) -> allocate prompt pages for the newly admitted ->
@@ -137,7 +148,7 @@ def simulate(prompt_lens, decode_steps: int, num_pages: int, num_layers: int,
     Returns (submit results, log, scheduler); ``scheduler.events`` lists every
     page allocation as (request, layer, logical page, page id) in order.
     """
-    sch = Scheduler(num_pages, num_layers, max_blocks, max_slots)
+    sch = Scheduler(num_pages, num_layers, max_blocks, max_slots, mode)
     ids = []
     for p in prompt_lens:
         st, rid = sch.submit(int(p), decode_steps + 1)

@@ -77,6 +77,7 @@ _SIGS = {
     "pkv_read_device_error": (_i, [_p, _p, _i, _ip]),
     "pkv_credit_pages": (_i, [_i, _i, _i]),
     "pkv_sched_create": (_p, [_i, _i, _i, _i]),
+    "pkv_sched_set_mode": (_i, [_p, _i]),
     "pkv_sched_destroy": (None, [_p]),
     "pkv_sched_submit": (_i, [_p, _i, _i, _ip]),
     "pkv_sched_admit": (_i, [_p, _p, _i, _ip]),
@@ -388,13 +389,18 @@ def pkv_credit_pages(prompt_tokens: int, allowed_new_tokens: int, num_layers: in
 
 
 class Scheduler:
-    """Continuous-batching admission and page allocation (C++ pkv_sched)."""
+    """Admission and page allocation (C++ pkv_sched): continuous batching, or
+    static batching (static=True: a new group only once the current one has
+    finished)."""
 
-    def __init__(self, num_pages: int, num_layers: int, max_blocks: int = 128, max_slots: int = 256):
+    def __init__(self, num_pages: int, num_layers: int, max_blocks: int = 128, max_slots: int = 256,
+                 static: bool = False):
         self._h = _L().pkv_sched_create(num_pages, num_layers, max_blocks, max_slots)
         if not self._h:
             raise PkvError(1, "pkv_sched_create")
         self.num_layers, self.max_blocks, self.max_slots = num_layers, max_blocks, max_slots
+        if static:
+            _check(_L().pkv_sched_set_mode(self._h, 1), "pkv_sched_set_mode")
 
     def __del__(self):
         h = getattr(self, "_h", None)

@@ -50,6 +50,7 @@ struct pkv_sched {
   std::vector<Event> events;
   long long reserved = 0;  // sum over running requests of credit - held
   int running = 0;
+  int mode = 0;            // 0 continuous, 1 static (admit only when nothing runs)
 };
 
 extern "C" int pkv_credit_pages(int prompt_tokens, int allowed_new_tokens, int num_layers) {
@@ -81,6 +82,12 @@ extern "C" pkv_sched* pkv_sched_create(int num_pages, int num_layers, int max_bl
 
 extern "C" void pkv_sched_destroy(pkv_sched* s) { delete s; }
 
+extern "C" int pkv_sched_set_mode(pkv_sched* s, int mode) {
+  if (!s || (mode != 0 && mode != 1)) return PKV_ERR_INVALID_ARGUMENT;
+  s->mode = mode;
+  return PKV_OK;
+}
+
 extern "C" int pkv_sched_submit(pkv_sched* s, int prompt_tokens, int allowed_new_tokens,
                                 int* req_id) {
   if (!s || !req_id || prompt_tokens < 1 || allowed_new_tokens < 1)
@@ -104,6 +111,10 @@ extern "C" int pkv_sched_admit(pkv_sched* s, int* admitted, int max_out, int* n_
   if (!s || !n_admitted || max_out < 0 || (max_out > 0 && !admitted))
     return PKV_ERR_INVALID_ARGUMENT;
   int n = 0;
+  if (s->mode == 1 && s->running > 0) {  // static batching: the group is still running
+    *n_admitted = 0;
+    return PKV_OK;
+  }
   while (!s->queue.empty() && n < max_out) {
     Request& r = s->reqs[s->queue.front()];
     if ((long long)r.credit > (long long)s->free_stack.size() - s->reserved) break;

@@ -32,10 +32,12 @@ class ContinuousBatcher:
     rope_cos/sin [max_pos, 32] fp32 device tables
     fused:       decode steps as one fused append+decode kernel per layer
                  (else kv_append_rope followed by paged_gqa_decode)
+    static:      static batching: a new group is admitted only once every
+                 request of the current one has finished
     """
 
     def __init__(self, pool, num_layers, rope_cos, rope_sin, scale, max_blocks=128,
-                 max_slots=256, fused=True):
+                 max_slots=256, fused=True, static=False):
         self.pool = pool
         self.dev = pool.device
         self.L = num_layers
@@ -43,7 +45,7 @@ class ContinuousBatcher:
         self.cos, self.sin = rope_cos, rope_sin
         self.scale = float(scale)
         self.fused = fused
-        self.sched = Scheduler(pool.shape[0], num_layers, max_blocks, max_slots)
+        self.sched = Scheduler(pool.shape[0], num_layers, max_blocks, max_slots, static=static)
         self.max_slots = max_slots
         self.tables = torch.full((num_layers, max_slots, max_blocks), -1, dtype=torch.int32,
                                  device=self.dev)

@@ -102,9 +102,9 @@ def test_host_side_validation_returns_before_launch():
               null) == 3
 
 
-def _run_cpp_schedule(case):
+def _run_cpp_schedule(case, static=False):
     """Drive the C++ scheduler with the oracle's step loop; return its log."""
-    s = pkv.Scheduler(case.num_pages, case.num_layers, W.MAX_BLOCKS, 256)
+    s = pkv.Scheduler(case.num_pages, case.num_layers, W.MAX_BLOCKS, 256, static=static)
     ids = [s.submit(int(p), case.allowed_new_tokens) for p in case.prompt_lens]
     running, length, done, log = [], {}, {}, []
     while s.stats()["queued"] or running:
@@ -127,11 +127,13 @@ def _run_cpp_schedule(case):
     return ids, log, s
 
 
-def test_scheduler_matches_oracle_on_continuous_mix():
+@pytest.mark.parametrize("static", [False, True])
+def test_scheduler_matches_oracle_on_continuous_mix(static):
     case = W.case_continuous()
     ids_o, log_o, sch_o = A.simulate(case.prompt_lens, case.decode_steps, case.num_pages,
-                                     case.num_layers)
-    ids_c, log_c, sch_c = _run_cpp_schedule(case)
+                                     case.num_layers,
+                                     mode=A.Scheduler.STATIC if static else A.Scheduler.CONTINUOUS)
+    ids_c, log_c, sch_c = _run_cpp_schedule(case, static)
     assert [r for _, r in ids_c] == [r for _, r in ids_o]
     assert len(log_c) == len(log_o)
     for a, b in zip(log_c, log_o):

@@ -55,16 +55,17 @@ class Source:
         return self.q_cache[key]
 
 
-def run_mix(lib, dev, case, fused, cos_d, sin_d):
+def run_mix(lib, dev, case, fused, cos_d, sin_d, static=False):
     from paged_kv_gqa_append_gb300.serving import ContinuousBatcher
     src = Source(case)
     pool = torch.zeros((case.num_pages, 2, 8, 16, 64), dtype=torch.bfloat16, device=dev)
     cb = ContinuousBatcher(pool, case.num_layers, cos_d, sin_d, W.DEFAULT_SCALE,
-                           max_slots=64, fused=fused)
+                           max_slots=64, fused=fused, static=static)
     for p in case.prompt_lens:
         assert cb.submit(int(p), case.allowed_new_tokens) >= 0
     # oracle side
-    osch = OA.Scheduler(case.num_pages, case.num_layers, W.MAX_BLOCKS, 64)
+    osch = OA.Scheduler(case.num_pages, case.num_layers, W.MAX_BLOCKS, 64,
+                        OA.Scheduler.STATIC if static else OA.Scheduler.CONTINUOUS)
     for p in case.prompt_lens:
         assert osch.submit(int(p), case.allowed_new_tokens)[0] == OA.Scheduler.OK
     opool = OP.new_pool(case.num_pages)
@@ -125,11 +126,11 @@ def run_mix(lib, dev, case, fused, cos_d, sin_d):
     return step
 
 
-@pytest.mark.parametrize("fused", [True, False])
-def test_continuous_batching_mix_matches_oracle(lib, cuda_device, fused):
-    # the full 64-request mix on the fused step; the two-call path on its
-    # first 16 requests (same scheduler, same pool size)
-    case = W.case_continuous() if fused else W.case_continuous(requests=16)
+@pytest.mark.parametrize("fused,static", [(True, False), (False, False), (True, True)])
+def test_continuous_batching_mix_matches_oracle(lib, cuda_device, fused, static):
+    # the full 64-request mix on the fused step; the two-call path and static
+    # batching on its first 16 requests (same scheduler, same pool size)
+    case = W.case_continuous() if fused and not static else W.case_continuous(requests=16)
     cos_d, sin_d = lib.rope_tables_device(cuda_device, W.MAX_CONTEXT)
-    steps = run_mix(lib, cuda_device, case, fused, cos_d, sin_d)
+    steps = run_mix(lib, cuda_device, case, fused, cos_d, sin_d, static)
     assert steps > case.decode_steps          # requests really overlapped in time

@@ -80,3 +80,39 @@ def test_simulation_pages_disjoint_over_time():
         running_sets = [held[r] for r in e["running"]]
         allp = [p for st in running_sets for p in st]
         assert len(allp) == len(set(allp))
+
+
+def test_static_batching_waits_for_the_group():
+    """Hand-worked: pool of 20 pages, 2 layers; requests of credit 6, 6, 4
+    (prompt + new - 1 = 48 / 48 / 32 tokens -> 3 / 3 / 2 pages per layer).
+    All three fit at once; a fourth of credit 6 does not (16 + 6 > 20).
+    Continuous admits the fourth as soon as one of the first three frees
+    its pages; static waits until all three have finished."""
+    for mode, expect_after_one in ((A.Scheduler.CONTINUOUS, [3]), (A.Scheduler.STATIC, [])):
+        s = A.Scheduler(num_pages=20, num_layers=2, max_blocks=10, max_slots=8, mode=mode)
+        for prompt, new in ((40, 9), (40, 9), (30, 3), (40, 9)):
+            assert s.submit(prompt, new)[0] == s.OK
+        assert s.admit() == [0, 1, 2]                # credits 6 + 6 + 4 = 16 <= 20
+        assert s.admit() == []                        # 6 > 20 - 16
+        assert s.finish(2) == s.OK                    # 4 pages of credit come back
+        assert s.admit() == expect_after_one          # 6 <= 20 - 12 only for continuous
+        if mode == A.Scheduler.STATIC:
+            assert s.finish(0) == s.OK
+            assert s.admit() == []                    # request 1 still running
+            assert s.finish(1) == s.OK
+            assert s.admit() == [3]                   # the group has finished
+
+
+def test_static_simulation_groups_do_not_overlap():
+    case = W.case_continuous()
+    ids, log, _ = A.simulate(case.prompt_lens, case.decode_steps, case.num_pages,
+                             case.num_layers, mode=A.Scheduler.STATIC)
+    assert all(st == A.Scheduler.OK for st, _ in ids)
+    running = set()
+    for e in log:
+        if e["admitted"]:
+            assert not (running - set(e["admitted"])), "admitted while a group was running"
+        running |= set(e["admitted"])
+        running -= set(e["finished"])
+    admitted = [r for e in log for r in e["admitted"]]
+    assert admitted == sorted(admitted) and len(admitted) == len(case.prompt_lens)
