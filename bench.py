@@ -39,6 +39,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "paged GQA decode: KV-read GB/s (% of HBM peak), decode tokens/s, µs/layer"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0   # one earlier burst measurement on a GB300
 
 
 def parse():
@@ -47,7 +48,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--workload", choices=["batch32", "stress256"], default="batch32")
+    ap.add_argument("--workload", choices=["batch32", "stress256", "prefill", "argmax"],
+                    default="batch32",
+                    help="batch32 / stress256: the decode step; prefill: causal prefill of 8 "
+                         "prompts x 1920 tokens; argmax: next-token argmax of 32 x 128256 logits")
     ap.add_argument("--compute", choices=["tensor", "fma"], default="tensor")
     ap.add_argument("--layers", type=int, default=0,
                     help="layers of the workload (0 = its own: 16); fewer layers shrink the pool "
@@ -233,8 +237,49 @@ def cpu_cores_used():
 
 # ------------------------------------------------------------------- arms ---
 
+def run_reference_other(args):
+    """The oracle on the prefill or argmax workload (one bounded sample per step)."""
+    if args.workload == "prefill":
+        from oracle import paged_kv as OP
+        pool_h, bt_h, q_h, _, lens_h = prefill_inputs(None)
+        P, rows = PREFILL_P, 4
+        q_s, cu_s, pool_bits = W.bf16_bits(q_h[P - rows:P]), np.array([0, rows], np.int32), W.bf16_bits(pool_h)
+        one = lambda: OP.prefill(q_s, cu_s, pool_bits, bt_h[:1], lens_h[:1], W.DEFAULT_SCALE)
+        work, unit, metric = rows * P * W.NUM_Q_HEADS * W.HEAD_DIM * 4 / 1e12, "TFLOP/s", \
+            "paged causal prefill TFLOP/s (causal attention FLOPs)"
+        sample = f"{rows} query rows at the end of a {P}-token prompt per step"
+        workload = f"prefill_b{PREFILL_S}_p{P}"
+    else:
+        from oracle import argmax as OA
+        x = torch.randn(ARGMAX_ROWS, ARGMAX_VOCAB, generator=torch.Generator().manual_seed(6)).numpy()
+        one = lambda: OA.argmax_rows(x)
+        work, unit, metric = ARGMAX_ROWS * ARGMAX_VOCAB * 4 / 1e9, "GB/s", \
+            "next-token argmax GB/s (FP32 logits read)"
+        sample = f"{ARGMAX_ROWS} rows of {ARGMAX_VOCAB} per step"
+        workload = f"argmax_b{ARGMAX_ROWS}_v{ARGMAX_VOCAB}"
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    el = time.perf_counter() - t0
+    value = work * args.steps / el
+    print(json.dumps({
+        "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": workload, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cpu_cores_used(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+        flush=True)
+
+
 def run_reference(args, world, rank):
     if rank != 0:
+        return
+    if args.workload in ("prefill", "argmax"):
+        run_reference_other(args)
         return
     case = make_case(args.workload, args.layers)
     ora = OracleSample(case)
@@ -443,12 +488,221 @@ def run_gb300(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------ prefill and argmax lines --
+
+def tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (bf16 burst)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+PREFILL_S, PREFILL_P = 8, 1920   # prompts x tokens (the longest prompts of the mix)
+
+
+def prefill_flops(S, P):
+    """Causal attention FLOPs: sum over queries of (keys seen) x 32 heads x 64 x 4."""
+    return S * (P * (P + 1) // 2) * W.NUM_Q_HEADS * W.HEAD_DIM * 4
+
+
+def prefill_inputs(dev):
+    S, P = PREFILL_S, PREFILL_P
+    pages_per = (P + W.PAGE_TOKENS - 1) // W.PAGE_TOKENS
+    num_pages = S * pages_per
+    gen = W.cpu_gen(5)
+    pool = W.normal_bf16((num_pages, 2, 8, 16, 64), gen)
+    perm = np.random.default_rng(5).permutation(num_pages).astype(np.int32)
+    bt = np.full((S, W.MAX_BLOCKS), -1, np.int32)
+    for s in range(S):
+        bt[s, :pages_per] = perm[s * pages_per:(s + 1) * pages_per]
+    q = W.normal_bf16((S * P, W.NUM_Q_HEADS, W.HEAD_DIM), gen)
+    cu = np.arange(0, S * P + 1, P, dtype=np.int32)
+    lens = np.full(S, P, np.int32)
+    return pool, bt, q, cu, lens
+
+
+def run_prefill_line(args, world, rank, local):
+    import paged_kv_gqa_append_gb300 as pkv
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    S, P = PREFILL_S, PREFILL_P
+    pool_h, bt_h, q_h, cu_h, lens_h = prefill_inputs(dev)
+    pool, q = pool_h.to(dev), q_h.to(dev)
+    bt, cu, lens = (torch.from_numpy(a).to(dev) for a in (bt_h, cu_h, lens_h))
+    out = torch.empty_like(q)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    run = lambda: pkv.paged_gqa_prefill(q, cu, pool, bt, lens, out, W.DEFAULT_SCALE, max_q_len=P,
+                                        d_err=err)
+    for _ in range(args.warmup):
+        run()
+    if pkv.pkv_read_device_error(err):
+        raise RuntimeError("device error in prefill warm-up")
+    steps = max(1, min(args.steps, 200))
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.5 if clocks else 0)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    clk = clocks.summary(t_wall0, t_wall1) if clocks else None
+    if clocks:
+        clocks.stop()
+    if pkv.pkv_read_device_error(err):
+        raise RuntimeError("device error in the prefill timed region")
+    flops = prefill_flops(S, P)
+    value = flops * steps * world / (ms / 1e3) / 1e12
+    # e2e: q uploaded from pinned memory and out read back every step
+    q_pin, out_pin = q_h.pin_memory(), torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    k_e2e = max(1, min(steps, 50))
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    a.record(stream)
+    for _ in range(k_e2e):
+        q.copy_(q_pin, non_blocking=True)
+        run()
+        out_pin.copy_(out, non_blocking=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(max(a.elapsed_time(b) / 1e3, time.perf_counter() - t0), world, dev)
+    peak, kind = tensor_peak()
+    avg_us = ms * 1e3 / steps
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle import paged_kv as OP
+        rows = 4   # the last 4 queries of the first prompt (each sees ~1920 keys)
+        q_s = W.bf16_bits(q_h[P - rows:P])
+        cu_s = np.array([0, rows], np.int32)
+        pool_bits = W.bf16_bits(pool_h)
+        done, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < 10.0:
+            OP.prefill(q_s, cu_s, pool_bits, bt_h[:1], lens_h[:1], W.DEFAULT_SCALE)
+            done += 1
+        el = time.perf_counter() - t0
+        cpu_flops = done * rows * P * W.NUM_Q_HEADS * W.HEAD_DIM * 4
+        cpu = {"value": cpu_flops / el / 1e12, "unit": "TFLOP/s", "cores": cpu_cores_used(),
+               "kind": "oracle", "sample": f"{done} x {rows} query rows at positions "
+                                           f"{P - rows}..{P - 1} of a {P}-token prompt, {el:.1f} s"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": "paged causal prefill TFLOP/s (causal attention FLOPs)", "value": value,
+            "unit": "TFLOP/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"prefill_b{S}_p{P}", "prompts": S, "prompt_tokens": P,
+                       "l2": "pool 240 MiB > 129 MB L2 and every page read by 32 query blocks",
+                       "parallelism": f"replicas x{world}"},
+            "clocks": clk, "gpu_launches": steps,
+            "e2e": {"value": flops * k_e2e * world / e2e_s / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": q_pin.numel() * 2, "d2h_bytes_per_step": out_pin.numel() * 2,
+                    "steps": k_e2e},
+            "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak,
+                         "unit": "TFLOP/s", "frac": value / world / peak, "traffic": None,
+                         "peak_source": kind, "kernel": "paged_prefill_kernel (mma.sync bf16)",
+                         "avg_launch_us": avg_us, "algorithmic_flops_per_launch": flops},
+            "cpu_baseline": cpu}), flush=True)
+
+
+ARGMAX_ROWS, ARGMAX_VOCAB, ARGMAX_BUFS = 32, 128256, 12   # 12 x 16.4 MB > L2
+
+
+def run_argmax_line(args, world, rank, local):
+    import paged_kv_gqa_append_gb300 as pkv
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    gen = torch.Generator().manual_seed(6)
+    host = [torch.randn(ARGMAX_ROWS, ARGMAX_VOCAB, generator=gen) for _ in range(ARGMAX_BUFS)]
+    bufs = [h.to(dev) for h in host]
+    out = torch.empty(ARGMAX_ROWS, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for i in range(max(args.warmup, 3)):
+        pkv.argmax_rows(bufs[i % ARGMAX_BUFS], out)
+    steps = max(ARGMAX_BUFS, min(args.steps, 2000))
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.5 if clocks else 0)
+    barrier(world)
+    t_wall0 = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        pkv.argmax_rows(bufs[i % ARGMAX_BUFS], out)   # inputs rotate through > L2 of buffers
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    clk = clocks.summary(t_wall0, time.time()) if clocks else None
+    if clocks:
+        clocks.stop()
+    nbytes = ARGMAX_ROWS * ARGMAX_VOCAB * 4
+    value = nbytes * steps * world / (ms / 1e3) / 1e9
+    peak, kind = hbm_peak()
+    # e2e: logits uploaded from pinned memory, ids read back, every step
+    pin = host[0].pin_memory()
+    ids = torch.empty(ARGMAX_ROWS, dtype=torch.int32, pin_memory=True)
+    k_e2e = 200
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    a.record(stream)
+    for _ in range(k_e2e):
+        bufs[0].copy_(pin, non_blocking=True)
+        pkv.argmax_rows(bufs[0], out)
+        ids.copy_(out, non_blocking=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(max(a.elapsed_time(b) / 1e3, time.perf_counter() - t0), world, dev)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle import argmax as OA
+        x = host[0].numpy()
+        done, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < 5.0:
+            OA.argmax_rows(x)
+            done += 1
+        el = time.perf_counter() - t0
+        cpu = {"value": nbytes * done / el / 1e9, "unit": "GB/s", "cores": cpu_cores_used(),
+               "kind": "oracle", "sample": f"{done} x {ARGMAX_ROWS} rows of {ARGMAX_VOCAB}, {el:.1f} s"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": "next-token argmax GB/s (FP32 logits read)", "value": value, "unit": "GB/s",
+            "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": ms / steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": f"argmax_b{ARGMAX_ROWS}_v{ARGMAX_VOCAB}", "rows": ARGMAX_ROWS,
+                       "vocab": ARGMAX_VOCAB,
+                       "l2": f"{ARGMAX_BUFS} input buffers rotated, {ARGMAX_BUFS * nbytes >> 20} MiB > L2",
+                       "parallelism": f"replicas x{world}"},
+            "us_per_step": ms * 1e3 / steps, "clocks": clk, "gpu_launches": steps,
+            "e2e": {"value": nbytes * k_e2e * world / e2e_s / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": ARGMAX_ROWS * 4,
+                    "steps": k_e2e},
+            "roofline": {"bound": "hbm", "achieved": value / world, "peak": peak, "unit": "GB/s",
+                         "frac": value / world / peak, "traffic": None, "peak_source": kind,
+                         "kernel": "argmax_kernel", "avg_launch_us": ms * 1e3 / steps,
+                         "algorithmic_bytes_per_launch": nbytes},
+            "cpu_baseline": cpu}), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args.gpus)
     try:
         if args.impl == "reference":
             run_reference(args, world, rank)
+        elif args.workload == "prefill":
+            run_prefill_line(args, world, rank, local)
+        elif args.workload == "argmax":
+            run_argmax_line(args, world, rank, local)
         else:
             run_gb300(args, world, rank, local)
     finally:

@@ -323,6 +323,19 @@ int paged_gqa_prefill(const void* q, int num_tokens, const int32_t* cu_q,
                       const int32_t* seq_lens, int num_seqs, int max_q_len,
                       void* out, float scale, int* d_err, void* stream);
 
+/* ------------------------------------------------------------------------
+ * pkv_argmax_f32 - next-token selection ("Architecture et flux
+ * d'inference": the final logits are FP32 and a GPU argmax selects the next
+ * token).  out_ids[r] = the first index of the largest non-NaN value of row
+ * r (NaN orders below every number, -inf included); 0 when every value of
+ * the row is NaN.
+ *   logits      device float [rows][row_stride], vocab <= row_stride used
+ *   out_ids     device int32 [rows]
+ * One CTA per row; deterministic.  Host-side checks only (no device error).
+ * ---------------------------------------------------------------------- */
+int pkv_argmax_f32(const float* logits, int rows, int vocab, long long row_stride,
+                   int32_t* out_ids, void* stream);
+
 /* Wait for `stream`, then copy the device error word to *code_out (host).
  * If `clear` is non-zero the word is reset to 0 afterwards. */
 int pkv_read_device_error(int* d_err, void* stream, int clear, int* code_out);

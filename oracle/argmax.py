@@ -6,10 +6,9 @@ logits are produced in FP32 and a GPU argmax selects the next token.
 Readings where the article is silent (the CUDA kernel follows the same rule):
   * the result is the smallest index of the row's largest value (ties go to
     the lowest token id);
-  * a NaN never wins: it orders below every number, -inf included, so a row
-    of only NaN and -inf (or only NaN) selects index 0 only when nothing
-    larger exists -- concretely, the first index holding the row's largest
-    non-NaN value, or 0 when every value is NaN.
+  * a NaN never wins: it orders below every number, -inf included; the
+    result is the first index holding the row's largest non-NaN value, and
+    0 when every value of the row is NaN.
 """
 from __future__ import annotations
 

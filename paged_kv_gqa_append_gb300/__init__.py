@@ -68,6 +68,7 @@ _SIGS = {
     "kv_append_rope": (_i, [_p, _p, _p, _p, _i, _p, _i, _i, _i, _p, _i, _p, _p, _i, _p, _p, _p, _p]),
     "paged_gqa_decode_workspace_bytes": (_sz, [_i]),
     "paged_gqa_prefill": (_i, [_p, _i, _p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _p]),
+    "pkv_argmax_f32": (_i, [_p, _i, _i, ctypes.c_longlong, _p, _p]),
     "paged_gqa_decode": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p, _p]),
     "paged_gqa_decode_ex": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p, _p,
                                  ctypes.POINTER(DecodeOpts)]),
@@ -372,6 +373,22 @@ def paged_gqa_prefill(q, cu_q, kv_pool, block_tables, seq_lens, out, scale, max_
                                 int(T if max_q_len is None else max_q_len), _ptr(out),
                                 float(scale), _ptr(d_err), _stream(stream))
     _check(st, "paged_gqa_prefill")
+
+
+def argmax_rows(logits, out=None, stream=None):
+    """Next-token ids: per row of FP32 logits [rows, vocab] (row stride may
+    exceed vocab), the first index of the largest non-NaN value."""
+    if logits.dtype != torch.float32 or not logits.is_cuda or logits.dim() != 2:
+        raise ValueError("logits must be a 2-D float32 CUDA tensor")
+    if logits.stride(1) != 1:
+        raise ValueError("logits rows must be contiguous")
+    rows, vocab = logits.shape
+    if out is None:
+        out = torch.empty(rows, dtype=torch.int32, device=logits.device)
+    _need(out, "out", torch.int32, logits.device)
+    _check(_L().pkv_argmax_f32(_ptr(logits), rows, vocab, logits.stride(0), _ptr(out),
+                               _stream(stream)), "pkv_argmax_f32")
+    return out
 
 
 def pkv_read_device_error(d_err, clear: bool = True, stream=None) -> int:

@@ -100,6 +100,13 @@ def test_host_side_validation_returns_before_launch():
               null) == 1
     assert PF(fake, 16, fake, fake, 8, fake, 128, 128, fake, 70000, 16, fake, 0.125, null,
               null) == 3
+    # argmax: nothing to do; bad sizes; nulls; misaligned
+    AM = L.pkv_argmax_f32
+    assert AM(null, 0, 10, 10, null, null) == 0
+    assert AM(fake, 4, 0, 10, fake, null) == 1
+    assert AM(fake, 4, 10, 9, fake, null) == 1
+    assert AM(null, 4, 10, 10, fake, null) == 1
+    assert AM(ctypes.c_void_p(0x10001), 4, 10, 10, fake, null) == 2
 
 
 def _run_cpp_schedule(case, static=False):
