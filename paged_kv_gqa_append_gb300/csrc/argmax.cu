@@ -3,12 +3,16 @@
 // the next token).  Result per row: the first index of the largest non-NaN
 // value; 0 when every value is NaN.
 //
-// One CTA per row.  Each thread keeps the best (value, index) of a strided
-// share of the row (16-byte streaming loads when the row is 16-byte aligned);
-// warp shuffles, then one shared-memory round, reduce the pairs under the
-// same total order (larger value first, then lower index, NaN last), which
-// is associative and commutative, so the result does not depend on the
-// reduction order.
+// Few rows (fewer than two per SM): a cluster of kClusterCtas CTAs per row,
+// each reducing one contiguous part; the parts' results meet in the first
+// CTA's shared memory (distributed shared memory) after a cluster barrier.
+// Many rows: one CTA per row.  Inside a CTA each thread keeps the best
+// (value, index) of a strided share (16-byte streaming loads when the part is
+// 16-byte aligned); warp shuffles, then one shared-memory round, reduce the
+// pairs under the same total order (larger value first, then lower index,
+// NaN last), which is associative and commutative, so the result does not
+// depend on the reduction order.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -20,6 +24,7 @@ namespace pkv {
 namespace {
 
 constexpr int kArgThreads = 256;
+constexpr int kClusterCtas = 8;
 
 // (v, i) before (bv, bi)?  bi < 0 marks "nothing yet"; a NaN never wins.
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
@@ -35,26 +40,27 @@ __device__ __forceinline__ void take(float v, int i, float& bv, int& bi) {
   }
 }
 
-__global__ void __launch_bounds__(kArgThreads) argmax_kernel(const float* __restrict__ x, int vocab,
-                                                             long long stride,
-                                                             int32_t* __restrict__ out) {
-  const float* row = x + (size_t)blockIdx.x * (size_t)stride;
-  float bv = 0.f;
-  int bi = -1;
-  if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
-    const int n4 = vocab / 4;
-    const float4* r4 = reinterpret_cast<const float4*>(row);
+// Best (value, index) of elements [lo, hi) of `row`, reduced over the CTA;
+// valid in thread 0.
+__device__ void cta_best(const float* __restrict__ row, int lo, int hi, float& bv, int& bi) {
+  bv = 0.f;
+  bi = -1;
+  int i = lo + threadIdx.x;
+  if (((reinterpret_cast<uintptr_t>(row + lo)) & 15u) == 0) {
+    const int n4 = (hi - lo) / 4;
+    const float4* r4 = reinterpret_cast<const float4*>(row + lo);
+#pragma unroll 4
     for (int k = threadIdx.x; k < n4; k += kArgThreads) {
       const float4 v = __ldcs(r4 + k);
-      take(v.x, 4 * k, bv, bi);
-      take(v.y, 4 * k + 1, bv, bi);
-      take(v.z, 4 * k + 2, bv, bi);
-      take(v.w, 4 * k + 3, bv, bi);
+      const int base = lo + 4 * k;
+      take(v.x, base, bv, bi);
+      take(v.y, base + 1, bv, bi);
+      take(v.z, base + 2, bv, bi);
+      take(v.w, base + 3, bv, bi);
     }
-    for (int i = 4 * n4 + threadIdx.x; i < vocab; i += kArgThreads) take(__ldcs(row + i), i, bv, bi);
-  } else {
-    for (int i = threadIdx.x; i < vocab; i += kArgThreads) take(__ldcs(row + i), i, bv, bi);
+    i = lo + 4 * n4 + threadIdx.x;
   }
+  for (; i < hi; i += kArgThreads) take(__ldcs(row + i), i, bv, bi);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float ov = __shfl_down_sync(0xffffffffu, bv, o);
@@ -78,7 +84,46 @@ __global__ void __launch_bounds__(kArgThreads) argmax_kernel(const float* __rest
       const int oi = __shfl_down_sync(0xffffffffu, bi, o);
       take(ov, oi, bv, bi);
     }
-    if (lane == 0) out[blockIdx.x] = bi < 0 ? 0 : bi;
+  }
+}
+
+__global__ void __launch_bounds__(kArgThreads) argmax_kernel(const float* __restrict__ x, int vocab,
+                                                             long long stride,
+                                                             int32_t* __restrict__ out) {
+  float bv;
+  int bi;
+  cta_best(x + (size_t)blockIdx.x * (size_t)stride, 0, vocab, bv, bi);
+  if (threadIdx.x == 0) out[blockIdx.x] = bi < 0 ? 0 : bi;
+}
+
+// Cluster of kClusterCtas CTAs per row (cluster dimension set at launch).
+__global__ void __launch_bounds__(kArgThreads) argmax_cluster_kernel(const float* __restrict__ x,
+                                                                     int vocab, long long stride,
+                                                                     int32_t* __restrict__ out) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  __shared__ float part_v[kClusterCtas];
+  __shared__ int part_i[kClusterCtas];
+  const int rank = (int)cluster.block_rank();
+  const int row = blockIdx.x / kClusterCtas;
+  // part boundaries on multiples of 4 elements
+  const int per = ((vocab + kClusterCtas - 1) / kClusterCtas + 3) & ~3;
+  const int lo = min(vocab, rank * per), hi = min(vocab, lo + per);
+  float bv;
+  int bi;
+  cta_best(x + (size_t)row * (size_t)stride, lo, hi, bv, bi);
+  if (threadIdx.x == 0) {
+    float* rv = cluster.map_shared_rank(part_v, 0);
+    int* ri = cluster.map_shared_rank(part_i, 0);
+    rv[rank] = bv;
+    ri[rank] = bi;
+  }
+  cluster.sync();  // every part is in the first CTA's shared memory
+  if (rank == 0 && threadIdx.x == 0) {
+    float v = 0.f;
+    int i = -1;
+    for (int r = 0; r < kClusterCtas; ++r) take(part_v[r], part_i[r], v, i);
+    out[row] = i < 0 ? 0 : i;
   }
 }
 
@@ -95,7 +140,24 @@ extern "C" int pkv_argmax_f32(const float* logits, int rows, int vocab, long lon
   int dev = 0;
   const int rc = pkv::bind_stream_device(stream, &dev);
   if (rc != PKV_OK) return rc;
-  pkv::argmax_kernel<<<rows, pkv::kArgThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      logits, vocab, row_stride, out_ids);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (rows < 2 * pkv::sm_count(dev) && vocab >= 64 * pkv::kClusterCtas &&
+      (long long)rows * pkv::kClusterCtas <= 0x7fffffffll) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = pkv::kClusterCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(rows * pkv::kClusterCtas));
+    cfg.blockDim = dim3(pkv::kArgThreads);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return pkv::cuda_status(cudaLaunchKernelEx(&cfg, pkv::argmax_cluster_kernel, logits, vocab,
+                                               row_stride, out_ids),
+                            "cudaLaunchKernelEx(argmax cluster)");
+  }
+  pkv::argmax_kernel<<<rows, pkv::kArgThreads, 0, st>>>(logits, vocab, row_stride, out_ids);
   return pkv::cuda_status(cudaGetLastError(), "argmax_kernel");
 }
