@@ -310,8 +310,9 @@ int paged_gqa_decode_append(const void* q, const void* k_new, const void* v_new,
  *   block_tables, bt_row_stride, max_blocks, seq_lens: as paged_gqa_decode
  *   max_q_len   host upper bound of every q_len (sizes the grid)
  *   out         device bf16 [num_tokens][32][64]
- * bf16 mma.sync with fp32 accumulation and an online softmax, one CTA per
- * (32 query tokens, KV head, sequence); deterministic.  A sequence whose
+ * tcgen05 MMAs (bf16 operands, fp32 accumulation in tensor memory) and an
+ * online softmax, one CTA per (32 query tokens, KV head, sequence);
+ * deterministic.  A sequence whose
  * rows fall outside [0, num_tokens) or whose q_len is negative is left
  * untouched; one with q_len > n, q_len > max_q_len, n above
  * 16 * max_blocks or a needed page id outside [0, num_pages) gets zero
@@ -322,6 +323,17 @@ int paged_gqa_prefill(const void* q, int num_tokens, const int32_t* cu_q,
                       const int32_t* block_tables, int bt_row_stride, int max_blocks,
                       const int32_t* seq_lens, int num_seqs, int max_q_len,
                       void* out, float scale, int* d_err, void* stream);
+
+/* paged_gqa_prefill with the compute path chosen: PKV_COMPUTE_TENSOR (the
+ * default: tcgen05 MMAs with S and O in tensor memory, 64-key blocks) or
+ * PKV_PREFILL_MMA_SYNC (bf16 mma.sync with register accumulators, the
+ * comparison arm).  Same contract and results within the same tolerance. */
+#define PKV_PREFILL_MMA_SYNC 2
+int paged_gqa_prefill_ex(const void* q, int num_tokens, const int32_t* cu_q,
+                         const void* kv_pool, int num_pages,
+                         const int32_t* block_tables, int bt_row_stride, int max_blocks,
+                         const int32_t* seq_lens, int num_seqs, int max_q_len,
+                         void* out, float scale, int* d_err, void* stream, int compute);
 
 /* ------------------------------------------------------------------------
  * pkv_argmax_f32 - next-token selection ("Architecture et flux

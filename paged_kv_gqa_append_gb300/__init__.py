@@ -68,6 +68,7 @@ _SIGS = {
     "kv_append_rope": (_i, [_p, _p, _p, _p, _i, _p, _i, _i, _i, _p, _i, _p, _p, _i, _p, _p, _p, _p]),
     "paged_gqa_decode_workspace_bytes": (_sz, [_i]),
     "paged_gqa_prefill": (_i, [_p, _i, _p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _p]),
+    "paged_gqa_prefill_ex": (_i, [_p, _i, _p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _p, _i]),
     "pkv_argmax_f32": (_i, [_p, _i, _i, ctypes.c_longlong, _p, _p]),
     "paged_gqa_decode": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p, _p]),
     "paged_gqa_decode_ex": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p, _p,
@@ -340,14 +341,18 @@ def paged_gqa_decode_append(q, k_new, v_new, kv_pool, block_tables, seq_lens, ou
     _check(st, "paged_gqa_decode_append")
 
 
+PREFILL_MMA_SYNC = 2  # comparison arm of paged_gqa_prefill (legacy bf16 mma.sync)
+
+
 def paged_gqa_prefill(q, cu_q, kv_pool, block_tables, seq_lens, out, scale, max_q_len=None,
-                      d_err=None, max_blocks=None, stream=None):
+                      d_err=None, max_blocks=None, compute=None, stream=None):
     """Causal attention of each sequence's last q_len tokens over its own pages.
 
     q, out: [T, 32, 64] bf16 (q rotated); cu_q: [S + 1] int32 row offsets on
     the device; seq_lens: [S] int32 tokens held (the queries are the last
     cu_q[s+1] - cu_q[s] of them).  max_q_len: host bound of every q_len
-    (default T).
+    (default T).  compute: None / COMPUTE_TENSOR (tcgen05, tensor memory) or
+    PREFILL_MMA_SYNC.
     """
     dev = kv_pool.device
     _need(kv_pool, "kv_pool", torch.bfloat16, dev, (2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM))
@@ -368,10 +373,11 @@ def paged_gqa_prefill(q, cu_q, kv_pool, block_tables, seq_lens, out, scale, max_
     mb = stride if max_blocks is None else max_blocks
     if d_err is not None:
         _need(d_err, "d_err", torch.int32, dev)
-    st = _L().paged_gqa_prefill(_ptr(q), T, _ptr(cu_q), _ptr(kv_pool), kv_pool.shape[0],
-                                _ptr(block_tables), stride, mb, _ptr(seq_lens), S,
-                                int(T if max_q_len is None else max_q_len), _ptr(out),
-                                float(scale), _ptr(d_err), _stream(stream))
+    st = _L().paged_gqa_prefill_ex(_ptr(q), T, _ptr(cu_q), _ptr(kv_pool), kv_pool.shape[0],
+                                   _ptr(block_tables), stride, mb, _ptr(seq_lens), S,
+                                   int(T if max_q_len is None else max_q_len), _ptr(out),
+                                   float(scale), _ptr(d_err), _stream(stream),
+                                   COMPUTE_TENSOR if compute is None else int(compute))
     _check(st, "paged_gqa_prefill")
 
 

@@ -35,5 +35,7 @@ inline int cuda_status(cudaError_t e, const char* where = "cuda") {
 // tile of one (page, head)), 128-byte swizzle; cached per thread for the
 // last (pool, num_pages).  Returns PKV_OK or PKV_ERR_CUDA.
 int make_pool_map(CUtensorMap* map, const void* pool, int num_pages);
+// The same view with a one-tile box {64, 16, 1, 1}.
+int make_pool_tile_map(CUtensorMap* map, const void* pool, int num_pages);
 
 }  // namespace pkv

@@ -8,7 +8,22 @@
 // n = seq_lens[s] tokens; its queries are the last q_len = cu_q[s+1] - cu_q[s]
 // of them, at positions n - q_len .. n - 1.
 //
-// Work unit = (query block of 32 tokens, KV head g, sequence s), one CTA.
+// Two implementations of the same contract:
+//  * tcgen05 (default): one CTA per (32 query tokens, KV head, sequence) =
+//    an M = 128 tile of query rows (token-major, the 4 query heads of the
+//    group inside); keys in blocks of 64 (4 pages).  S = Q K^T and O += P V
+//    run on the 5th-generation tensor cores with S and O in tensor memory,
+//    operands in 128-byte-swizzled shared memory (Q and P written by
+//    threads, K and V tiles by TMA; V is the MN-major B operand as stored).
+//    A producer warp streams K and V through two stages, one thread issues
+//    the MMAs, and a warpgroup runs the softmax with one thread per row
+//    (the row max and sum need no shuffles); O is rescaled in tensor memory
+//    only when a row's running max grows by more than 8 (in log2 units) --
+//    softmax does not depend on the subtracted constant, and the weights
+//    stay below 2^8.
+//  * mma.sync (comparison arm, below): the same units on the legacy tensor path.
+//
+// mma.sync arm: work unit = (query block of 32 tokens, KV head g, sequence s), one CTA.
 // Its 128 query rows (32 tokens x the 4 query heads of g) share every K/V
 // page they read: a producer warp streams the pages [0, last position / 16]
 // through a 4-stage TMA ring (one {64, 16, 1, 2} box = K then V tile), and
@@ -285,16 +300,294 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   }
 }
 
+// ---------------------------------------------------------------------------
+// tcgen05 prefill.
+// ---------------------------------------------------------------------------
+constexpr int kTcRows = 128;                   // 32 tokens x 4 query heads
+constexpr int kTcKeys = 64;                    // keys per block (4 pages)
+constexpr int kTcPages = kTcKeys / PKV_PAGE_TOKENS;
+constexpr int kTcStages = 2;
+constexpr int kTcThreads = 256;                // w0 TMA, w1 MMA, w2-3 Q, w4-7 softmax
+constexpr uint32_t kTmemCols = 128;            // S: [0, 64), O: [64, 128)
+constexpr uint32_t kTmemO = 64;
+constexpr float kLazyRescale = 8.f;            // log2 units
+
+struct TcSmem {
+  static constexpr int kQ = 0;                          // [128][64] bf16, swizzled
+  static constexpr int kP = kQ + kTcRows * 128;         // [128][64 keys] bf16, swizzled
+  static constexpr int kK = kP + kTcRows * 128;         // [stage][64 keys][64] bf16
+  static constexpr int kV = kK + kTcStages * kTcKeys * 128;
+  static constexpr int kBars = kV + kTcStages * kTcKeys * 128;
+  // barriers: kv_full[2], kv_empty[2], s_full, p_full, o_done, q_ready
+  static constexpr int kTmemSlot = kBars + 8 * 8;
+  static constexpr int kBytes = kTmemSlot + 16;
+};
+
+__device__ __forceinline__ uint32_t sw128_chunk(int row, int chunk) {
+  return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__global__ void __launch_bounds__(kTcThreads, 2)
+    paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap, const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ int bad_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = blockIdx.z, g = blockIdx.y;
+  const int qb = (int)gridDim.x - 1 - (int)blockIdx.x;  // latest (longest) blocks first
+
+  pdl_wait();
+  pdl_launch_dependents();
+  const int r0 = __ldg(p.cu_q + s), r1 = __ldg(p.cu_q + s + 1), q_len = r1 - r0;
+  const int n = __ldg(p.seq_lens + s);
+  if (r0 < 0 || r1 > p.num_tokens || q_len < 0) {  // rows outside q/out: touch nothing
+    if (blockIdx.x == 0 && g == 0 && threadIdx.x == 0) report_error(p.d_err, PKV_ERR_DEVICE_INDEX);
+    return;
+  }
+  if (q_len == 0) return;
+  const int n_pages_seq = (n + PKV_PAGE_TOKENS - 1) / PKV_PAGE_TOKENS;
+  bool bad = q_len > n || n > PKV_PAGE_TOKENS * p.max_blocks || q_len > (int)gridDim.x * kPfTokens;
+  if (threadIdx.x == 0) bad_flag = 0;
+  __syncthreads();
+  if (!bad && warp == 0) {
+    int any = 0;
+    for (int j = lane; j < n_pages_seq; j += 32) {
+      const int pid = __ldg(p.block_tables + (size_t)s * p.bt_stride + j);
+      any |= (pid < 0 || pid >= p.num_pages);
+    }
+    if (__any_sync(0xffffffffu, any) && lane == 0) bad_flag = 1;
+  }
+  __syncthreads();
+  if (bad || bad_flag) {
+    if (blockIdx.x == 0 && g == 0 && threadIdx.x == 0) report_error(p.d_err, PKV_ERR_DEVICE_INDEX);
+    zero_rows(p, r0, q_len, g);
+    return;
+  }
+  const int t0 = qb * kPfTokens;
+  if (t0 >= q_len) return;
+  const int t_end = min(t0 + kPfTokens, q_len);
+  const int pos0 = n - q_len;
+  const int p_last = pos0 + t_end - 1;
+  const int nb = p_last / kTcKeys + 1;           // key blocks [0, nb)
+
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + TcSmem::kQ, sP = sbase + TcSmem::kP;
+  const uint32_t bars = sbase + TcSmem::kBars;
+  const uint32_t kv_full = bars, kv_empty = bars + 16, s_full = bars + 32, p_full = bars + 40,
+                 o_done = bars + 48, q_ready = bars + 56;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TcSmem::kTmemSlot);
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kTcStages; ++st) {
+      mbar_init(kv_full + 8 * st, 1);
+      mbar_init(kv_empty + 8 * st, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, kTcRows);
+    mbar_init(o_done, 1);
+    mbar_init(q_ready, 64);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool failed = false;
+
+  if (warp == 0) {
+    // ---------------- K / V producer --------------------------------------
+    if (lane == 0) {
+      const int32_t* row = p.block_tables + (size_t)s * p.bt_stride;
+      for (int b = 0; b < nb && !failed; ++b) {
+        const int st = b & 1;
+        if (b >= kTcStages &&
+            !mbar_wait_bounded(kv_empty + 8 * st, (uint32_t)((b / kTcStages - 1) & 1), kPfWaitNs)) {
+          report_error(p.d_err, PKV_ERR_TIMEOUT);
+          failed = true;
+          break;
+        }
+        const int j0 = b * kTcPages, jn = min(kTcPages, n_pages_seq - j0);
+        mbar_arrive_expect_tx(kv_full + 8 * st, (uint32_t)(jn * 2 * 2048));
+        const uint32_t dK = sbase + TcSmem::kK + st * kTcKeys * 128;
+        const uint32_t dV = sbase + TcSmem::kV + st * kTcKeys * 128;
+        for (int pg = 0; pg < jn; ++pg) {
+          const int pid = __ldg(row + j0 + pg);
+          tma_load_4d(dK + pg * 2048, &tmap, 0, 0, g, pid * 2, kv_full + 8 * st);
+          tma_load_4d(dV + pg * 2048, &tmap, 0, 0, g, pid * 2 + 1, kv_full + 8 * st);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ------------------------------------------
+    if (lane == 0) {
+      const uint32_t id_s = umma_idesc_bf16(kTcRows, kTcKeys, 0);
+      const uint32_t id_o = umma_idesc_bf16(kTcRows, 64, 1);
+      if (!mbar_wait_bounded(q_ready, 0, kPfWaitNs)) failed = true;
+      for (int b = 0; b < nb && !failed; ++b) {
+        const int st = b & 1;
+        if (!mbar_wait_bounded(kv_full + 8 * st, (uint32_t)((b / kTcStages) & 1), kPfWaitNs)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sK = sbase + TcSmem::kK + st * kTcKeys * 128;
+        const uint32_t sV = sbase + TcSmem::kV + st * kTcKeys * 128;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // S = Q K^T, 16 dims per step
+          umma_bf16(tmem, umma_desc_sw128(sQ + 32 * k, 16, 1024), umma_desc_sw128(sK + 32 * k, 16, 1024),
+                    id_s, k > 0);
+        umma_commit(s_full);
+        if (!mbar_wait_bounded(p_full, (uint32_t)(b & 1), kPfWaitNs)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // O += P V, 16 keys per step (V is MN-major: 16 rows = 2048 B)
+          umma_bf16(tmem + kTmemO, umma_desc_sw128(sP + 32 * k, 16, 1024),
+                    umma_desc_sw128(sV + 2048 * k, 8192, 1024), id_o, (b > 0 || k > 0));
+        umma_commit(o_done);
+        umma_commit(kv_empty + 8 * st);
+      }
+      if (failed) report_error(p.d_err, PKV_ERR_TIMEOUT);
+    }
+  } else if (warp < 4) {
+    // ---------------- Q tile (row i = token i / 4, head 4 g + i % 4) -------
+    const int t = threadIdx.x - 64;
+    for (int idx = t; idx < kTcRows * 8; idx += 64) {
+      const int row = idx >> 3, c = idx & 7;
+      const int tok = t0 + (row >> 2);
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (tok < t_end)
+        v = __ldg(reinterpret_cast<const uint4*>(
+                      p.q + ((size_t)(r0 + tok) * PKV_NUM_Q_HEADS + g * 4 + (row & 3)) * 64) + c);
+      *reinterpret_cast<uint4*>(smem + TcSmem::kQ + sw128_chunk(row, c)) = v;
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(q_ready);
+  } else {
+    // ---------------- softmax: thread = row ------------------------------
+    const int i = threadIdx.x - 128;               // TMEM lane = query row
+    const uint32_t lane_base = (uint32_t)(32 * (warp - 4)) << 16;
+    const int tok = t0 + (i >> 2);
+    const bool valid = tok < t_end;
+    const int p_i = valid ? pos0 + tok : -1;
+    float m_used = -INFINITY, l = 0.f;
+    // every wait is decided warp-wide: the tensor-memory loads below are
+    // warp-collective
+    auto wait_all = [&](uint32_t bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, kPfWaitNs));
+    };
+    for (int b = 0; b < nb; ++b) {
+      if (!wait_all(s_full, (uint32_t)(b & 1))) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      const int k0 = b * kTcKeys;
+      // pass 1: row max of the block's scores (masked keys excluded)
+      float mx = -INFINITY;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float v[32];
+        tmem_ld32(tmem + lane_base + 32 * h, v);
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (k0 + 32 * h + c <= p_i) mx = fmaxf(mx, v[c] * p.sl2);
+      }
+      // the previous block's P V must be done before P and O are touched
+      if (b > 0 && !wait_all(o_done, (uint32_t)((b - 1) & 1))) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      if (mx > m_used + kLazyRescale || (m_used == -INFINITY && mx > -INFINITY)) {
+        if (m_used > -INFINITY) {  // rescale O (and l) to the new reference
+          const float alpha = exp2f(m_used - mx);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float v[32];
+            tmem_ld32(tmem + lane_base + kTmemO + 32 * h, v);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) v[c] *= alpha;
+            tmem_st32(tmem + lane_base + kTmemO + 32 * h, v);
+          }
+          l *= alpha;
+        }
+        m_used = mx;
+      }
+      // pass 2: weights, rounded to bf16 (the denominator sums the same values)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float v[32];
+        tmem_ld32(tmem + lane_base + 32 * h, v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const int k = k0 + 32 * h + c;
+          const float w0 = (k <= p_i && m_used > -INFINITY) ? exp2f(v[c] * p.sl2 - m_used) : 0.f;
+          const float w1 = (k + 1 <= p_i && m_used > -INFINITY) ? exp2f(v[c + 1] * p.sl2 - m_used) : 0.f;
+          pk[c / 2] = pack_bf16x2(w0, w1);
+          l += bf16lo_to_f32(pk[c / 2]) + bf16hi_to_f32(pk[c / 2]);
+        }
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8)
+          *reinterpret_cast<uint4*>(smem + TcSmem::kP + sw128_chunk(i, 4 * h + c8)) =
+              make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+      }
+      // keys past the sequence's end: their V rows may hold any bits; zero them
+      const int zero_from = max(0, n - k0);
+      if (zero_from < kTcKeys) {
+        uint8_t* vst = smem + TcSmem::kV + (b & 1) * kTcKeys * 128;
+        for (int idx = i; idx < (kTcKeys - zero_from) * 8; idx += kTcRows)
+          *reinterpret_cast<uint4*>(vst + (zero_from + idx / 8) * 128 + (idx & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (!failed && wait_all(o_done, (uint32_t)((nb - 1) & 1))) {
+      tc_fence_after();
+      uint32_t* dst = reinterpret_cast<uint32_t*>(
+          p.out + ((size_t)(r0 + (valid ? tok : 0)) * PKV_NUM_Q_HEADS + g * 4 + (i & 3)) * 64);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float v[32];
+        tmem_ld32(tmem + lane_base + kTmemO + 32 * h, v);  // every lane: warp-collective
+        if (valid) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 2)
+            dst[16 * h + c / 2] = pack_bf16x2(__fdiv_rn(v[c], l), __fdiv_rn(v[c + 1], l));
+        }
+      }
+    } else if (!failed) {
+      failed = true;
+    }
+    if (failed && i == 0) report_error(p.d_err, PKV_ERR_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 }  // namespace
 }  // namespace pkv
 
 using namespace pkv;
 
-extern "C" int paged_gqa_prefill(const void* q, int num_tokens, const int32_t* cu_q,
-                                 const void* kv_pool, int num_pages, const int32_t* block_tables,
-                                 int bt_row_stride, int max_blocks, const int32_t* seq_lens,
-                                 int num_seqs, int max_q_len, void* out, float scale, int* d_err,
-                                 void* stream) {
+extern "C" int paged_gqa_prefill_ex(const void* q, int num_tokens, const int32_t* cu_q,
+                                    const void* kv_pool, int num_pages, const int32_t* block_tables,
+                                    int bt_row_stride, int max_blocks, const int32_t* seq_lens,
+                                    int num_seqs, int max_q_len, void* out, float scale, int* d_err,
+                                    void* stream, int compute) {
+  if (compute != PKV_COMPUTE_TENSOR && compute != PKV_PREFILL_MMA_SYNC) return PKV_ERR_INVALID_ARGUMENT;
   if (num_seqs < 0 || num_tokens < 0 || num_pages < 1 || max_blocks < 1 ||
       bt_row_stride < max_blocks || max_q_len < 0)
     return PKV_ERR_INVALID_ARGUMENT;
@@ -313,7 +606,8 @@ extern "C" int paged_gqa_prefill(const void* q, int num_tokens, const int32_t* c
   int rc = bind_stream_device(stream, &dev);
   if (rc != PKV_OK) return rc;
   CUtensorMap map;
-  rc = make_pool_map(&map, kv_pool, num_pages);
+  rc = compute == PKV_COMPUTE_TENSOR ? make_pool_tile_map(&map, kv_pool, num_pages)
+                                     : make_pool_map(&map, kv_pool, num_pages);
   if (rc != PKV_OK) return rc;
 
   PrefillParams prm;
@@ -336,11 +630,36 @@ extern "C" int paged_gqa_prefill(const void* q, int num_tokens, const int32_t* c
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks_x, PKV_NUM_KV_HEADS, (unsigned)num_seqs);
-  cfg.blockDim = dim3(kPfThreads);
-  cfg.dynamicSmemBytes = 0;
   cfg.stream = static_cast<cudaStream_t>(stream);
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_status(cudaLaunchKernelEx(&cfg, paged_prefill_kernel, map, prm),
-                     "cudaLaunchKernelEx(prefill)");
+  if (compute == PKV_PREFILL_MMA_SYNC) {
+    cfg.blockDim = dim3(kPfThreads);
+    cfg.dynamicSmemBytes = 0;
+    return cuda_status(cudaLaunchKernelEx(&cfg, paged_prefill_kernel, map, prm),
+                       "cudaLaunchKernelEx(prefill mma.sync)");
+  }
+  static bool attr_set[64] = {false};
+  const size_t smem = (size_t)TcSmem::kBytes + 1024;
+  if (dev < 0 || dev >= 64) return PKV_ERR_CUDA;
+  if (!attr_set[dev]) {  // benign race: every caller sets the same value
+    const cudaError_t e = cudaFuncSetAttribute(paged_prefill_tc_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(prefill)");
+    attr_set[dev] = true;
+  }
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  return cuda_status(cudaLaunchKernelEx(&cfg, paged_prefill_tc_kernel, map, prm),
+                     "cudaLaunchKernelEx(prefill tcgen05)");
+}
+
+extern "C" int paged_gqa_prefill(const void* q, int num_tokens, const int32_t* cu_q,
+                                 const void* kv_pool, int num_pages, const int32_t* block_tables,
+                                 int bt_row_stride, int max_blocks, const int32_t* seq_lens,
+                                 int num_seqs, int max_q_len, void* out, float scale, int* d_err,
+                                 void* stream) {
+  return paged_gqa_prefill_ex(q, num_tokens, cu_q, kv_pool, num_pages, block_tables, bt_row_stride,
+                              max_blocks, seq_lens, num_seqs, max_q_len, out, scale, d_err, stream,
+                              PKV_COMPUTE_TENSOR);
 }

@@ -70,4 +70,44 @@ int make_pool_map(CUtensorMap* map, const void* pool, int num_pages) {
   return PKV_OK;
 }
 
+// The same view with a one-tile box {64, 16, 1, 1}: the K tile (kv = 0) or
+// the V tile (kv = 1) of one (page, head) alone, so that the tiles of
+// consecutive pages can be placed back to back in shared memory.
+int make_pool_tile_map(CUtensorMap* map, const void* pool, int num_pages) {
+  struct Cached {
+    const void* ptr = nullptr;
+    int pages = 0;
+    CUtensorMap map;
+  };
+  static thread_local Cached cache;
+  if (cache.ptr == pool && cache.pages == num_pages) {
+    *map = cache.map;
+    return PKV_OK;
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) {
+    set_last_error("cudaGetDriverEntryPointByVersion", "cuTensorMapEncodeTiled unavailable");
+    return PKV_ERR_CUDA;
+  }
+  // (dim, token, head, 2 page + K/V): one box {64, 16, 1, 2} is the K tile and
+  // then the V tile of one (page, head), 4 KiB, in a single copy
+  const cuuint64_t dims[4] = {64, 16, PKV_NUM_KV_HEADS, (cuuint64_t)num_pages * 2};
+  const cuuint64_t strides[3] = {128, 2048, 2048 * PKV_NUM_KV_HEADS};
+  const cuuint32_t box[4] = {64, 16, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char msg[64];
+    snprintf(msg, sizeof(msg), "CUresult %d", (int)r);
+    set_last_error("cuTensorMapEncodeTiled", msg);
+    return PKV_ERR_CUDA;
+  }
+  cache.ptr = pool;
+  cache.pages = num_pages;
+  cache.map = *map;
+  return PKV_OK;
+}
+
 }  // namespace pkv
