@@ -302,29 +302,46 @@ __global__ void __launch_bounds__(kPfThreads, 2)
 
 // ---------------------------------------------------------------------------
 // tcgen05 prefill.
+//
+// Pipeline per 64-key block b (buffers alternate with b):
+//   producer lane 0: K(b) -> K stage      (after S(b - 2) has read that stage)
+//   producer lane 1: V(b) -> V stage      (after P V(b - 2) has read it)
+//   MMA thread:      S(b + 1) = Q K^T -> S buffer, while the softmax works on
+//                    S(b); then, once P(b) is written, O += P(b) V(b)
+//   softmax:         S(b) -> row max -> P(b) (bf16) in its own buffer
+// so the tensor cores compute the next scores and the last P V while the
+// warpgroup turns the current scores into weights.  Every barrier is used
+// per buffer, so a waiter is never two phases behind its barrier.
 // ---------------------------------------------------------------------------
 constexpr int kTcRows = 128;                   // 32 tokens x 4 query heads
 constexpr int kTcKeys = 64;                    // keys per block (4 pages)
 constexpr int kTcPages = kTcKeys / PKV_PAGE_TOKENS;
-constexpr int kTcStages = 2;
 constexpr int kTcThreads = 256;                // w0 TMA, w1 MMA, w2-3 Q, w4-7 softmax
-constexpr uint32_t kTmemCols = 128;            // S: [0, 64), O: [64, 128)
-constexpr uint32_t kTmemO = 64;
+constexpr uint32_t kTmemCols = 256;            // S0: [0, 64), S1: [64, 128), O: [128, 192)
+constexpr uint32_t kTmemO = 128;
 constexpr float kLazyRescale = 8.f;            // log2 units
 
 struct TcSmem {
-  static constexpr int kQ = 0;                          // [128][64] bf16, swizzled
-  static constexpr int kP = kQ + kTcRows * 128;         // [128][64 keys] bf16, swizzled
-  static constexpr int kK = kP + kTcRows * 128;         // [stage][64 keys][64] bf16
-  static constexpr int kV = kK + kTcStages * kTcKeys * 128;
-  static constexpr int kBars = kV + kTcStages * kTcKeys * 128;
-  // barriers: kv_full[2], kv_empty[2], s_full, p_full, o_done, q_ready
-  static constexpr int kTmemSlot = kBars + 8 * 8;
-  static constexpr int kBytes = kTmemSlot + 16;
+  static constexpr int kTile = kTcRows * 128;            // 16 KB: 128 rows of 128 B
+  static constexpr int kKV = kTcKeys * 128;              // 8 KB: 64 keys of 128 B
+  static constexpr int kQ = 0;
+  static constexpr int kP = kQ + kTile;                  // [2] P buffers
+  static constexpr int kK = kP + 2 * kTile;              // [2] K stages
+  static constexpr int kV = kK + 2 * kKV;                // [2] V stages
+  static constexpr int kBars = kV + 2 * kKV;
+  // kfull[2] kempty[2] vfull[2] vempty[2] sfull[2] sfree[2] pfull[2] odone[2] qready
+  static constexpr int kTmemSlot = kBars + 17 * 8;
+  static constexpr int kBytes = kTmemSlot + 8;
 };
 
 __device__ __forceinline__ uint32_t sw128_chunk(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __global__ void __launch_bounds__(kTcThreads, 2)
@@ -372,21 +389,25 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const int nb = p_last / kTcKeys + 1;           // key blocks [0, nb)
 
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase + TcSmem::kQ, sP = sbase + TcSmem::kP;
+  const uint32_t sQ = sbase + TcSmem::kQ;
   const uint32_t bars = sbase + TcSmem::kBars;
-  const uint32_t kv_full = bars, kv_empty = bars + 16, s_full = bars + 32, p_full = bars + 40,
-                 o_done = bars + 48, q_ready = bars + 56;
+  const uint32_t kfull = bars, kempty = bars + 16, vfull = bars + 32, vempty = bars + 48,
+                 sfull = bars + 64, sfree = bars + 80, pfull = bars + 96, odone = bars + 112,
+                 qready = bars + 128;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TcSmem::kTmemSlot);
 
   if (threadIdx.x == 0) {
-    for (int st = 0; st < kTcStages; ++st) {
-      mbar_init(kv_full + 8 * st, 1);
-      mbar_init(kv_empty + 8 * st, 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(kfull + 8 * k, 1);
+      mbar_init(kempty + 8 * k, 1);
+      mbar_init(vfull + 8 * k, 1);
+      mbar_init(vempty + 8 * k, 1);
+      mbar_init(sfull + 8 * k, 1);
+      mbar_init(sfree + 8 * k, kTcRows);
+      mbar_init(pfull + 8 * k, kTcRows);
+      mbar_init(odone + 8 * k, 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_full, kTcRows);
-    mbar_init(o_done, 1);
-    mbar_init(q_ready, 64);
+    mbar_init(qready, 64);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -397,26 +418,23 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   bool failed = false;
 
   if (warp == 0) {
-    // ---------------- K / V producer --------------------------------------
-    if (lane == 0) {
+    // ---------------- producers: lane 0 K tiles, lane 1 V tiles ----------
+    if (lane < 2) {
+      const int kv = lane;
+      const uint32_t full = kv ? vfull : kfull, empty = kv ? vempty : kempty;
+      const uint32_t dst0 = sbase + (kv ? TcSmem::kV : TcSmem::kK);
       const int32_t* row = p.block_tables + (size_t)s * p.bt_stride;
-      for (int b = 0; b < nb && !failed; ++b) {
+      for (int b = 0; b < nb; ++b) {
         const int st = b & 1;
-        if (b >= kTcStages &&
-            !mbar_wait_bounded(kv_empty + 8 * st, (uint32_t)((b / kTcStages - 1) & 1), kPfWaitNs)) {
+        if (b >= 2 && !mbar_wait_bounded(empty + 8 * st, (uint32_t)((b / 2 - 1) & 1), kPfWaitNs)) {
           report_error(p.d_err, PKV_ERR_TIMEOUT);
-          failed = true;
           break;
         }
         const int j0 = b * kTcPages, jn = min(kTcPages, n_pages_seq - j0);
-        mbar_arrive_expect_tx(kv_full + 8 * st, (uint32_t)(jn * 2 * 2048));
-        const uint32_t dK = sbase + TcSmem::kK + st * kTcKeys * 128;
-        const uint32_t dV = sbase + TcSmem::kV + st * kTcKeys * 128;
-        for (int pg = 0; pg < jn; ++pg) {
-          const int pid = __ldg(row + j0 + pg);
-          tma_load_4d(dK + pg * 2048, &tmap, 0, 0, g, pid * 2, kv_full + 8 * st);
-          tma_load_4d(dV + pg * 2048, &tmap, 0, 0, g, pid * 2 + 1, kv_full + 8 * st);
-        }
+        mbar_arrive_expect_tx(full + 8 * st, (uint32_t)(jn * 2048));
+        for (int pg = 0; pg < jn; ++pg)
+          tma_load_4d(dst0 + st * TcSmem::kKV + pg * 2048, &tmap, 0, 0, g,
+                      __ldg(row + j0 + pg) * 2 + kv, full + 8 * st);
       }
     }
   } else if (warp == 1) {
@@ -424,34 +442,43 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (lane == 0) {
       const uint32_t id_s = umma_idesc_bf16(kTcRows, kTcKeys, 0);
       const uint32_t id_o = umma_idesc_bf16(kTcRows, 64, 1);
-      if (!mbar_wait_bounded(q_ready, 0, kPfWaitNs)) failed = true;
-      for (int b = 0; b < nb && !failed; ++b) {
+      auto issue_s = [&](int b) -> bool {  // S(b) into S buffer b & 1
         const int st = b & 1;
-        if (!mbar_wait_bounded(kv_full + 8 * st, (uint32_t)((b / kTcStages) & 1), kPfWaitNs)) {
-          failed = true;
+        if (!mbar_wait_bounded(kfull + 8 * st, (uint32_t)((b / 2) & 1), kPfWaitNs)) return false;
+        if (b >= 2 && !mbar_wait_bounded(sfree + 8 * st, (uint32_t)((b / 2 - 1) & 1), kPfWaitNs)) return false;
+        tc_fence_after();
+        const uint32_t sK = sbase + TcSmem::kK + st * TcSmem::kKV;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // 16 dims per step
+          umma_bf16(tmem + 64 * st, umma_desc_sw128(sQ + 32 * k, 16, 1024),
+                    umma_desc_sw128(sK + 32 * k, 16, 1024), id_s, k > 0);
+        umma_commit(sfull + 8 * st);
+        umma_commit(kempty + 8 * st);  // the K stage may be refilled once S(b) is done
+        return true;
+      };
+      bool ok = mbar_wait_bounded(qready, 0, kPfWaitNs) && issue_s(0);
+      for (int b = 0; b < nb && ok; ++b) {
+        const int st = b & 1;
+        if (b + 1 < nb && !issue_s(b + 1)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait_bounded(pfull + 8 * st, (uint32_t)((b / 2) & 1), kPfWaitNs) ||
+            !mbar_wait_bounded(vfull + 8 * st, (uint32_t)((b / 2) & 1), kPfWaitNs)) {
+          ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t sK = sbase + TcSmem::kK + st * kTcKeys * 128;
-        const uint32_t sV = sbase + TcSmem::kV + st * kTcKeys * 128;
+        const uint32_t sP = sbase + TcSmem::kP + st * TcSmem::kTile;
+        const uint32_t sV = sbase + TcSmem::kV + st * TcSmem::kKV;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)  // S = Q K^T, 16 dims per step
-          umma_bf16(tmem, umma_desc_sw128(sQ + 32 * k, 16, 1024), umma_desc_sw128(sK + 32 * k, 16, 1024),
-                    id_s, k > 0);
-        umma_commit(s_full);
-        if (!mbar_wait_bounded(p_full, (uint32_t)(b & 1), kPfWaitNs)) {
-          failed = true;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 4; ++k)  // O += P V, 16 keys per step (V is MN-major: 16 rows = 2048 B)
+        for (int k = 0; k < 4; ++k)  // 16 keys per step; V is MN-major (16 rows = 2048 B)
           umma_bf16(tmem + kTmemO, umma_desc_sw128(sP + 32 * k, 16, 1024),
                     umma_desc_sw128(sV + 2048 * k, 8192, 1024), id_o, (b > 0 || k > 0));
-        umma_commit(o_done);
-        umma_commit(kv_empty + 8 * st);
+        umma_commit(odone + 8 * st);
+        umma_commit(vempty + 8 * st);
       }
-      if (failed) report_error(p.d_err, PKV_ERR_TIMEOUT);
+      if (!ok) report_error(p.d_err, PKV_ERR_TIMEOUT);
     }
   } else if (warp < 4) {
     // ---------------- Q tile (row i = token i / 4, head 4 g + i % 4) -------
@@ -466,7 +493,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       *reinterpret_cast<uint4*>(smem + TcSmem::kQ + sw128_chunk(row, c)) = v;
     }
     fence_proxy_async_smem();
-    mbar_arrive(q_ready);
+    mbar_arrive(qready);
   } else {
     // ---------------- softmax: thread = row ------------------------------
     const int i = threadIdx.x - 128;               // TMEM lane = query row
@@ -475,81 +502,94 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const bool valid = tok < t_end;
     const int p_i = valid ? pos0 + tok : -1;
     float m_used = -INFINITY, l = 0.f;
-    // every wait is decided warp-wide: the tensor-memory loads below are
-    // warp-collective
+    // every wait is decided warp-wide: the tensor-memory loads are warp-collective
     auto wait_all = [&](uint32_t bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, kPfWaitNs));
     };
     for (int b = 0; b < nb; ++b) {
-      if (!wait_all(s_full, (uint32_t)(b & 1))) {
+      const int st = b & 1;
+      const uint32_t sS = tmem + lane_base + 64 * st;
+      if (!wait_all(sfull + 8 * st, (uint32_t)((b / 2) & 1))) {
         failed = true;
         break;
       }
       tc_fence_after();
       const int k0 = b * kTcKeys;
-      // pass 1: row max of the block's scores (masked keys excluded)
-      float mx = -INFINITY;
+      float mx = -INFINITY;  // pass 1: the block's row max (masked keys excluded)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float v[32];
-        tmem_ld32(tmem + lane_base + 32 * h, v);
+        tmem_ld32(sS + 32 * h, v);
 #pragma unroll
         for (int c = 0; c < 32; ++c)
           if (k0 + 32 * h + c <= p_i) mx = fmaxf(mx, v[c] * p.sl2);
       }
-      // the previous block's P V must be done before P and O are touched
-      if (b > 0 && !wait_all(o_done, (uint32_t)((b - 1) & 1))) {
+      // P buffer st was last read by P V(b - 2)
+      if (b >= 2 && !wait_all(odone + 8 * st, (uint32_t)((b / 2 - 1) & 1))) {
         failed = true;
         break;
       }
-      tc_fence_after();
-      if (mx > m_used + kLazyRescale || (m_used == -INFINITY && mx > -INFINITY)) {
-        if (m_used > -INFINITY) {  // rescale O (and l) to the new reference
-          const float alpha = exp2f(m_used - mx);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float v[32];
-            tmem_ld32(tmem + lane_base + kTmemO + 32 * h, v);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) v[c] *= alpha;
-            tmem_st32(tmem + lane_base + kTmemO + 32 * h, v);
-          }
-          l *= alpha;
+      const bool grow = mx > m_used + kLazyRescale || (m_used == -INFINITY && mx > -INFINITY);
+      if (__any_sync(0xffffffffu, grow && m_used > -INFINITY)) {
+        // O is rescaled: every P V so far (the last is P V(b - 1)) must be done
+        if (b >= 1 && !wait_all(odone + 8 * ((b - 1) & 1), (uint32_t)(((b - 1) / 2) & 1))) {
+          failed = true;
+          break;
         }
-        m_used = mx;
+        tc_fence_after();
+        const float alpha = (grow && m_used > -INFINITY) ? exp2f(m_used - mx) : 1.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float v[32];
+          tmem_ld32(tmem + lane_base + kTmemO + 32 * h, v);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] *= alpha;
+          tmem_st32(tmem + lane_base + kTmemO + 32 * h, v);
+        }
+        l *= alpha;
       }
-      // pass 2: weights, rounded to bf16 (the denominator sums the same values)
+      if (grow) m_used = mx;
+      // pass 2: weights rounded to bf16 (the denominator sums the same values)
+      uint8_t* Pst = smem + TcSmem::kP + st * TcSmem::kTile;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float v[32];
-        tmem_ld32(tmem + lane_base + 32 * h, v);
+        tmem_ld32(sS + 32 * h, v);
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           const int k = k0 + 32 * h + c;
-          const float w0 = (k <= p_i && m_used > -INFINITY) ? exp2f(v[c] * p.sl2 - m_used) : 0.f;
-          const float w1 = (k + 1 <= p_i && m_used > -INFINITY) ? exp2f(v[c + 1] * p.sl2 - m_used) : 0.f;
+          const float w0 = (k <= p_i) ? ex2_approx(v[c] * p.sl2 - m_used) : 0.f;
+          const float w1 = (k + 1 <= p_i) ? ex2_approx(v[c + 1] * p.sl2 - m_used) : 0.f;
           pk[c / 2] = pack_bf16x2(w0, w1);
           l += bf16lo_to_f32(pk[c / 2]) + bf16hi_to_f32(pk[c / 2]);
         }
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8)
-          *reinterpret_cast<uint4*>(smem + TcSmem::kP + sw128_chunk(i, 4 * h + c8)) =
+          *reinterpret_cast<uint4*>(Pst + sw128_chunk(i, 4 * h + c8)) =
               make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
       }
-      // keys past the sequence's end: their V rows may hold any bits; zero them
+      tc_fence_before();
+      mbar_arrive(sfree + 8 * st);  // S buffer st is read
+      // keys past the sequence's end: their V rows may hold any bits; zero
+      // them once this block's V tiles have landed
       const int zero_from = max(0, n - k0);
       if (zero_from < kTcKeys) {
-        uint8_t* vst = smem + TcSmem::kV + (b & 1) * kTcKeys * 128;
+        if (!wait_all(vfull + 8 * st, (uint32_t)((b / 2) & 1))) {
+          failed = true;
+          break;
+        }
+        uint8_t* vst = smem + TcSmem::kV + st * TcSmem::kKV;
         for (int idx = i; idx < (kTcKeys - zero_from) * 8; idx += kTcRows)
           *reinterpret_cast<uint4*>(vst + (zero_from + idx / 8) * 128 + (idx & 7) * 16) =
               make_uint4(0u, 0u, 0u, 0u);
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(pfull + 8 * st);
     }
-    if (!failed && wait_all(o_done, (uint32_t)((nb - 1) & 1))) {
+    const int lb = nb - 1;
+    if (!failed && wait_all(odone + 8 * (lb & 1), (uint32_t)((lb / 2) & 1))) {
       tc_fence_after();
       uint32_t* dst = reinterpret_cast<uint32_t*>(
           p.out + ((size_t)(r0 + (valid ? tok : 0)) * PKV_NUM_Q_HEADS + g * 4 + (i & 3)) * 64);
