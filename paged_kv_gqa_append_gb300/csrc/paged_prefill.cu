@@ -317,8 +317,9 @@ constexpr int kTcRows = 128;                   // 32 tokens x 4 query heads
 constexpr int kTcKeys = 64;                    // keys per block (4 pages)
 constexpr int kTcPages = kTcKeys / PKV_PAGE_TOKENS;
 constexpr int kTcThreads = 256;                // w0 TMA, w1 MMA, w2-3 Q, w4-7 softmax
-constexpr uint32_t kTmemCols = 256;            // S0: [0, 64), S1: [64, 128), O: [128, 192)
+constexpr uint32_t kTmemCols = 256;            // S0 [0, 64), S1 [64, 128), O [128, 192), L [192, 208)
 constexpr uint32_t kTmemO = 128;
+constexpr uint32_t kTmemL = 192;               // row sums of P: P times a tile of ones
 constexpr float kLazyRescale = 8.f;            // log2 units
 
 struct TcSmem {
@@ -328,7 +329,8 @@ struct TcSmem {
   static constexpr int kP = kQ + kTile;                  // [2] P buffers
   static constexpr int kK = kP + 2 * kTile;              // [2] K stages
   static constexpr int kV = kK + 2 * kKV;                // [2] V stages
-  static constexpr int kBars = kV + 2 * kKV;
+  static constexpr int kOnes = kV + 2 * kKV;              // [16][64] bf16 ones (2 KB)
+  static constexpr int kBars = kOnes + 16 * 128;
   // kfull[2] kempty[2] vfull[2] vempty[2] sfull[2] sfree[2] pfull[2] odone[2] qready
   static constexpr int kTmemSlot = kBars + 17 * 8;
   static constexpr int kBytes = kTmemSlot + 8;
@@ -442,6 +444,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (lane == 0) {
       const uint32_t id_s = umma_idesc_bf16(kTcRows, kTcKeys, 0);
       const uint32_t id_o = umma_idesc_bf16(kTcRows, 64, 1);
+      const uint32_t id_l = umma_idesc_bf16(kTcRows, 16, 0);
+      const uint32_t sOnes = sbase + TcSmem::kOnes;
       auto issue_s = [&](int b) -> bool {  // S(b) into S buffer b & 1
         const int st = b & 1;
         if (!mbar_wait_bounded(kfull + 8 * st, (uint32_t)((b / 2) & 1), kPfWaitNs)) return false;
@@ -475,6 +479,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         for (int k = 0; k < 4; ++k)  // 16 keys per step; V is MN-major (16 rows = 2048 B)
           umma_bf16(tmem + kTmemO, umma_desc_sw128(sP + 32 * k, 16, 1024),
                     umma_desc_sw128(sV + 2048 * k, 8192, 1024), id_o, (b > 0 || k > 0));
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // L += P 1: the row sums of the same bf16 weights
+          umma_bf16(tmem + kTmemL, umma_desc_sw128(sP + 32 * k, 16, 1024),
+                    umma_desc_sw128(sOnes + 32 * k, 16, 1024), id_l, (b > 0 || k > 0));
         umma_commit(odone + 8 * st);
         umma_commit(vempty + 8 * st);
       }
@@ -492,6 +500,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                       p.q + ((size_t)(r0 + tok) * PKV_NUM_Q_HEADS + g * 4 + (row & 3)) * 64) + c);
       *reinterpret_cast<uint4*>(smem + TcSmem::kQ + sw128_chunk(row, c)) = v;
     }
+    for (int idx = t; idx < 16 * 8; idx += 64)  // bf16 1.0 = 0x3F80
+      *reinterpret_cast<uint4*>(smem + TcSmem::kOnes + idx * 16) =
+          make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     fence_proxy_async_smem();
     mbar_arrive(qready);
   } else {
@@ -501,7 +512,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const int tok = t0 + (i >> 2);
     const bool valid = tok < t_end;
     const int p_i = valid ? pos0 + tok : -1;
-    float m_used = -INFINITY, l = 0.f;
+    float m_used = -INFINITY;
     // every wait is decided warp-wide: the tensor-memory loads are warp-collective
     auto wait_all = [&](uint32_t bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, kPfWaitNs));
@@ -546,10 +557,16 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           for (int c = 0; c < 32; ++c) v[c] *= alpha;
           tmem_st32(tmem + lane_base + kTmemO + 32 * h, v);
         }
-        l *= alpha;
+        {  // the row sums live in columns [kTmemL, kTmemL + 16) of the same 32-column group
+          float v[32];
+          tmem_ld32(tmem + lane_base + kTmemL, v);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] *= alpha;
+          tmem_st32(tmem + lane_base + kTmemL, v);
+        }
       }
       if (grow) m_used = mx;
-      // pass 2: weights rounded to bf16 (the denominator sums the same values)
+      // pass 2: weights rounded to bf16 (L sums the same values on the tensor cores)
       uint8_t* Pst = smem + TcSmem::kP + st * TcSmem::kTile;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -562,7 +579,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           const float w0 = (k <= p_i) ? ex2_approx(v[c] * p.sl2 - m_used) : 0.f;
           const float w1 = (k + 1 <= p_i) ? ex2_approx(v[c + 1] * p.sl2 - m_used) : 0.f;
           pk[c / 2] = pack_bf16x2(w0, w1);
-          l += bf16lo_to_f32(pk[c / 2]) + bf16hi_to_f32(pk[c / 2]);
         }
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8)
@@ -591,6 +607,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const int lb = nb - 1;
     if (!failed && wait_all(odone + 8 * (lb & 1), (uint32_t)((lb / 2) & 1))) {
       tc_fence_after();
+      float lv[32];
+      tmem_ld32(tmem + lane_base + kTmemL, lv);
+      const float l = lv[0];
       uint32_t* dst = reinterpret_cast<uint32_t*>(
           p.out + ((size_t)(r0 + (valid ? tok : 0)) * PKV_NUM_Q_HEADS + g * 4 + (i & 3)) * 64);
 #pragma unroll
