@@ -526,15 +526,25 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       }
       tc_fence_after();
       const int k0 = b * kTcKeys;
-      float mx = -INFINITY;  // pass 1: the block's row max (masked keys excluded)
+      // every key of the block visible to every row of the warp: no masks
+      const bool full = __all_sync(0xffffffffu, k0 + kTcKeys - 1 <= p_i);
+      // pass 1: the block's row max of the raw scores (scale * log2 e > 0,
+      // so it is applied once to the max)
+      float rmx = -INFINITY;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float v[32];
         tmem_ld32(sS + 32 * h, v);
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (k0 + 32 * h + c <= p_i) mx = fmaxf(mx, v[c] * p.sl2);
+          for (int c = 0; c < 32; ++c) rmx = fmaxf(rmx, v[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (k0 + 32 * h + c <= p_i) rmx = fmaxf(rmx, v[c]);
+        }
       }
+      const float mx = rmx * p.sl2;
       // P buffer st was last read by P V(b - 2)
       if (b >= 2 && !wait_all(odone + 8 * st, (uint32_t)((b / 2 - 1) & 1))) {
         failed = true;
@@ -573,12 +583,19 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         float v[32];
         tmem_ld32(sS + 32 * h, v);
         uint32_t pk[16];
+        const float nm = -m_used;
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const int k = k0 + 32 * h + c;
-          const float w0 = (k <= p_i) ? ex2_approx(v[c] * p.sl2 - m_used) : 0.f;
-          const float w1 = (k + 1 <= p_i) ? ex2_approx(v[c + 1] * p.sl2 - m_used) : 0.f;
-          pk[c / 2] = pack_bf16x2(w0, w1);
+          for (int c = 0; c < 32; c += 2)
+            pk[c / 2] = pack_bf16x2(ex2_approx(fmaf(v[c], p.sl2, nm)), ex2_approx(fmaf(v[c + 1], p.sl2, nm)));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const int k = k0 + 32 * h + c;
+            const float w0 = (k <= p_i) ? ex2_approx(fmaf(v[c], p.sl2, nm)) : 0.f;
+            const float w1 = (k + 1 <= p_i) ? ex2_approx(fmaf(v[c + 1], p.sl2, nm)) : 0.f;
+            pk[c / 2] = pack_bf16x2(w0, w1);
+          }
         }
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8)
