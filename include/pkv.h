@@ -310,6 +310,8 @@ int paged_gqa_decode_append(const void* q, const void* k_new, const void* v_new,
  *   block_tables, bt_row_stride, max_blocks, seq_lens: as paged_gqa_decode
  *   max_q_len   host upper bound of every q_len (sizes the grid)
  *   out         device bf16 [num_tokens][32][64]
+ *   scale       positive and finite (the kernel takes the row max of the
+ *               unscaled scores), else PKV_ERR_INVALID_ARGUMENT
  * tcgen05 MMAs (bf16 operands, fp32 accumulation in tensor memory) and an
  * online softmax, one CTA per (32 query tokens, KV head, sequence);
  * deterministic.  A sequence whose

@@ -303,42 +303,46 @@ __global__ void __launch_bounds__(kPfThreads, 2)
 // ---------------------------------------------------------------------------
 // tcgen05 prefill.
 //
-// Pipeline per 64-key block b (buffers alternate with b):
-//   producer lane 0: K(b) -> K stage      (after S(b - 2) has read that stage)
-//   producer lane 1: V(b) -> V stage      (after P V(b - 2) has read it)
+// Pipeline per 64-key block b (S and P buffers alternate with b & 1, K stages
+// rotate with b % 4, V stages with b % 3):
+//   producer warp 0: Q once, then K(b) -> K stage (after S(b - 4) read it)
+//   producer warp 2: V(b) -> V stage                (after P V(b - 3) read it)
 //   MMA thread:      S(b + 1) = Q K^T -> S buffer, while the softmax works on
 //                    S(b); then, once P(b) is written, O += P(b) V(b)
-//   softmax:         S(b) -> row max -> P(b) (bf16) in its own buffer
+//   softmax:         S(b) -> row max -> P(b) (bf16) in its own tensor-memory
+//                    buffer, row sums in registers
 // so the tensor cores compute the next scores and the last P V while the
-// warpgroup turns the current scores into weights.  Every barrier is used
-// per buffer, so a waiter is never two phases behind its barrier.
+// warpgroup turns the current scores into weights, and each K copy has three
+// blocks of time to land (copies take microseconds when every SM streams).
+// P V takes P from tensor memory: shared memory only feeds Q, K and V to the
+// tensor cores (its bandwidth, not the MMA rate, bounds small-N MMAs).
+// Page ids are read one block ahead.  Every barrier is used per buffer, so a
+// waiter is never two phases behind its barrier.
 // ---------------------------------------------------------------------------
 constexpr int kTcRows = 128;                   // 32 tokens x 4 query heads
 constexpr int kTcKeys = 64;                    // keys per block (4 pages)
 constexpr int kTcPages = kTcKeys / PKV_PAGE_TOKENS;
-constexpr int kTcThreads = 256;                // w0 TMA, w1 MMA, w2-3 Q, w4-7 softmax
-constexpr uint32_t kTmemCols = 256;            // S0 [0, 64), S1 [64, 128), O [128, 192), L [192, 208)
+constexpr int kTcKStages = 4;
+constexpr int kTcVStages = 4;
+constexpr int kTcThreads = 256;                // w0 Q/K TMA, w1 MMA, w2 V TMA, w4-7 softmax
+constexpr uint32_t kTmemCols = 256;            // S0 [0, 64), S1 [64, 128), O [128, 192), P0, P1 [192, 256)
 constexpr uint32_t kTmemO = 128;
-constexpr uint32_t kTmemL = 192;               // row sums of P: P times a tile of ones
+constexpr uint32_t kTmemP = 192;               // P buffers: 64 bf16 weights per row = 32 columns
 constexpr float kLazyRescale = 8.f;            // log2 units
 
 struct TcSmem {
   static constexpr int kTile = kTcRows * 128;            // 16 KB: 128 rows of 128 B
   static constexpr int kKV = kTcKeys * 128;              // 8 KB: 64 keys of 128 B
   static constexpr int kQ = 0;
-  static constexpr int kP = kQ + kTile;                  // [2] P buffers
-  static constexpr int kK = kP + 2 * kTile;              // [2] K stages
-  static constexpr int kV = kK + 2 * kKV;                // [2] V stages
-  static constexpr int kOnes = kV + 2 * kKV;              // [16][64] bf16 ones (2 KB)
-  static constexpr int kBars = kOnes + 16 * 128;
-  // kfull[2] kempty[2] vfull[2] vempty[2] sfull[2] sfree[2] pfull[2] odone[2] qready
-  static constexpr int kTmemSlot = kBars + 17 * 8;
+  static constexpr int kK = kQ + kTile;                  // [kTcKStages] K stages
+  static constexpr int kV = kK + kTcKStages * kKV;       // [kTcVStages] V stages
+  static constexpr int kBars = kV + kTcVStages * kKV;
+  // kfull, kempty [kTcKStages]; vfull, vempty [kTcVStages]; sfull, sfree, pfull,
+  // odone [2] each; qready; drain (the MMA thread's last commit)
+  static constexpr int kNumBars = 2 * kTcKStages + 2 * kTcVStages + 4 * 2 + 2;
+  static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kBytes = kTmemSlot + 8;
 };
-
-__device__ __forceinline__ uint32_t sw128_chunk(int row, int chunk) {
-  return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
-}
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -346,8 +350,18 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Page ids of key block b (4 pages; 0 past the sequence's last page).
+__device__ __forceinline__ void block_page_ids(const int32_t* row, int b, int n_pages, int (&ids)[kTcPages]) {
+#pragma unroll
+  for (int k = 0; k < kTcPages; ++k) {
+    const int j = b * kTcPages + k;
+    ids[k] = j < n_pages ? __ldg(row + j) : 0;
+  }
+}
+
 __global__ void __launch_bounds__(kTcThreads, 2)
-    paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap, const PrefillParams p) {
+    paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap,
+                            const __grid_constant__ CUtensorMap qmap, const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -356,20 +370,52 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const int s = blockIdx.z, g = blockIdx.y;
   const int qb = (int)gridDim.x - 1 - (int)blockIdx.x;  // latest (longest) blocks first
 
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + TcSmem::kQ;
+  const uint32_t bars = sbase + TcSmem::kBars;
+  const uint32_t kfull = bars, kempty = kfull + 8 * kTcKStages, vfull = kempty + 8 * kTcKStages,
+                 vempty = vfull + 8 * kTcVStages;
+  const uint32_t sfull = vempty + 8 * kTcVStages, sfree = sfull + 16, pfull = sfull + 32, odone = sfull + 48,
+                 qready = sfull + 64, drain = sfull + 72;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TcSmem::kTmemSlot);
+
+  // set-up that reads no global memory runs before the dependency wait
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < kTcKStages; ++k) {
+      mbar_init(kfull + 8 * k, 1);
+      mbar_init(kempty + 8 * k, 1);
+    }
+    for (int k = 0; k < kTcVStages; ++k) {
+      mbar_init(vfull + 8 * k, 1);
+      mbar_init(vempty + 8 * k, 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(sfull + 8 * k, 1);
+      mbar_init(sfree + 8 * k, kTcRows);
+      mbar_init(pfull + 8 * k, kTcRows);
+      mbar_init(odone + 8 * k, 1);
+    }
+    mbar_init(qready, 1);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    bad_flag = 0;
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
   pdl_wait();
   pdl_launch_dependents();
   const int r0 = __ldg(p.cu_q + s), r1 = __ldg(p.cu_q + s + 1), q_len = r1 - r0;
   const int n = __ldg(p.seq_lens + s);
-  if (r0 < 0 || r1 > p.num_tokens || q_len < 0) {  // rows outside q/out: touch nothing
-    if (blockIdx.x == 0 && g == 0 && threadIdx.x == 0) report_error(p.d_err, PKV_ERR_DEVICE_INDEX);
-    return;
-  }
-  if (q_len == 0) return;
   const int n_pages_seq = (n + PKV_PAGE_TOKENS - 1) / PKV_PAGE_TOKENS;
-  bool bad = q_len > n || n > PKV_PAGE_TOKENS * p.max_blocks || q_len > (int)gridDim.x * kPfTokens;
-  if (threadIdx.x == 0) bad_flag = 0;
-  __syncthreads();
-  if (!bad && warp == 0) {
+  const bool rows_ok = r0 >= 0 && r1 <= p.num_tokens && q_len >= 0;  // else touch no rows
+  const bool some = rows_ok && q_len > 0;
+  bool bad = some && (q_len > n || n > PKV_PAGE_TOKENS * p.max_blocks ||
+                      q_len > (int)gridDim.x * kPfTokens);
+  if (some && !bad && warp == 0) {
     int any = 0;
     for (int j = lane; j < n_pages_seq; j += 32) {
       const int pid = __ldg(p.block_tables + (size_t)s * p.bt_stride + j);
@@ -378,134 +424,108 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (__any_sync(0xffffffffu, any) && lane == 0) bad_flag = 1;
   }
   __syncthreads();
-  if (bad || bad_flag) {
-    if (blockIdx.x == 0 && g == 0 && threadIdx.x == 0) report_error(p.d_err, PKV_ERR_DEVICE_INDEX);
-    zero_rows(p, r0, q_len, g);
-    return;
-  }
+  bad = bad || bad_flag;
+  if ((!rows_ok || bad) && blockIdx.x == 0 && g == 0 && threadIdx.x == 0)
+    report_error(p.d_err, PKV_ERR_DEVICE_INDEX);
+  if (some && bad) zero_rows(p, r0, q_len, g);
   const int t0 = qb * kPfTokens;
-  if (t0 >= q_len) return;
+  const bool run = some && !bad && t0 < q_len;
   const int t_end = min(t0 + kPfTokens, q_len);
   const int pos0 = n - q_len;
-  const int p_last = pos0 + t_end - 1;
-  const int nb = p_last / kTcKeys + 1;           // key blocks [0, nb)
-
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase + TcSmem::kQ;
-  const uint32_t bars = sbase + TcSmem::kBars;
-  const uint32_t kfull = bars, kempty = bars + 16, vfull = bars + 32, vempty = bars + 48,
-                 sfull = bars + 64, sfree = bars + 80, pfull = bars + 96, odone = bars + 112,
-                 qready = bars + 128;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TcSmem::kTmemSlot);
-
-  if (threadIdx.x == 0) {
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(kfull + 8 * k, 1);
-      mbar_init(kempty + 8 * k, 1);
-      mbar_init(vfull + 8 * k, 1);
-      mbar_init(vempty + 8 * k, 1);
-      mbar_init(sfull + 8 * k, 1);
-      mbar_init(sfree + 8 * k, kTcRows);
-      mbar_init(pfull + 8 * k, kTcRows);
-      mbar_init(odone + 8 * k, 1);
-    }
-    mbar_init(qready, 64);
-    fence_mbar_init();
-  }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const int nb = run ? (pos0 + t_end - 1) / kTcKeys + 1 : 0;  // key blocks [0, nb)
   bool failed = false;
 
-  if (warp == 0) {
-    // ---------------- producers: lane 0 K tiles, lane 1 V tiles ----------
-    if (lane < 2) {
-      const int kv = lane;
+  if (!run) {
+  } else if (warp == 0 || warp == 2) {
+    // ---------------- producers: warp 0 Q then K tiles, warp 2 V tiles ----
+    // (one lane each, in separate warps: two lanes of one warp would
+    // reconverge after every wait, tying each K copy to a V stage)
+    if (lane == 0) {
+      const int kv = warp == 2;
       const uint32_t full = kv ? vfull : kfull, empty = kv ? vempty : kempty;
       const uint32_t dst0 = sbase + (kv ? TcSmem::kV : TcSmem::kK);
+      const int nst = kv ? kTcVStages : kTcKStages;
       const int32_t* row = p.block_tables + (size_t)s * p.bt_stride;
+      if (kv == 0) {  // rows of tokens past this sequence's chunk are never stored
+        mbar_arrive_expect_tx(qready, (uint32_t)TcSmem::kTile);
+        tma_load_4d(sQ, &qmap, 0, 0, g, r0 + t0, qready);
+      }
+      int ids[kTcPages];
+      block_page_ids(row, 0, n_pages_seq, ids);
+      int issued = 0;
       for (int b = 0; b < nb; ++b) {
-        const int st = b & 1;
-        if (b >= 2 && !mbar_wait_bounded(empty + 8 * st, (uint32_t)((b / 2 - 1) & 1), kPfWaitNs)) {
+        const int st = b % nst;
+        int next[kTcPages];
+        block_page_ids(row, b + 1, n_pages_seq, next);
+        if (b >= nst && !mbar_wait_bounded(empty + 8 * st, (uint32_t)((b / nst - 1) & 1), kPfWaitNs)) {
           report_error(p.d_err, PKV_ERR_TIMEOUT);
           break;
         }
-        const int j0 = b * kTcPages, jn = min(kTcPages, n_pages_seq - j0);
+        const int jn = min(kTcPages, n_pages_seq - b * kTcPages);
         mbar_arrive_expect_tx(full + 8 * st, (uint32_t)(jn * 2048));
-        for (int pg = 0; pg < jn; ++pg)
-          tma_load_4d(dst0 + st * TcSmem::kKV + pg * 2048, &tmap, 0, 0, g,
-                      __ldg(row + j0 + pg) * 2 + kv, full + 8 * st);
+#pragma unroll
+        for (int pg = 0; pg < kTcPages; ++pg)
+          if (pg < jn)
+            tma_load_4d(dst0 + st * TcSmem::kKV + pg * 2048, &tmap, 0, 0, g, ids[pg] * 2 + kv,
+                        full + 8 * st);
+#pragma unroll
+        for (int pg = 0; pg < kTcPages; ++pg) ids[pg] = next[pg];
+        issued = b + 1;
       }
+      // no copy may still be landing when the CTA exits (its consumers
+      // normally saw every one; after a timeout they may not have)
+      bool landed = kv != 0 || mbar_wait_bounded(qready, 0, kPfWaitNs);
+      for (int b = max(0, issued - nst); b < issued; ++b)
+        landed = landed && mbar_wait_bounded(full + 8 * (b % nst), (uint32_t)((b / nst) & 1), kPfWaitNs);
+      if (!landed) report_error(p.d_err, PKV_ERR_TIMEOUT);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ------------------------------------------
     if (lane == 0) {
       const uint32_t id_s = umma_idesc_bf16(kTcRows, kTcKeys, 0);
       const uint32_t id_o = umma_idesc_bf16(kTcRows, 64, 1);
-      const uint32_t id_l = umma_idesc_bf16(kTcRows, 16, 0);
-      const uint32_t sOnes = sbase + TcSmem::kOnes;
-      auto issue_s = [&](int b) -> bool {  // S(b) into S buffer b & 1
-        const int st = b & 1;
-        if (!mbar_wait_bounded(kfull + 8 * st, (uint32_t)((b / 2) & 1), kPfWaitNs)) return false;
-        if (b >= 2 && !mbar_wait_bounded(sfree + 8 * st, (uint32_t)((b / 2 - 1) & 1), kPfWaitNs)) return false;
+      auto issue_s = [&](int j) -> bool {  // S(j) into S buffer j & 1
+        const int st = j % kTcKStages, sb = j & 1;
+        if (!mbar_wait_bounded(kfull + 8 * st, (uint32_t)((j / kTcKStages) & 1), kPfWaitNs)) return false;
+        if (j >= 2 && !mbar_wait_bounded(sfree + 8 * sb, (uint32_t)((j / 2 - 1) & 1), kPfWaitNs)) return false;
         tc_fence_after();
         const uint32_t sK = sbase + TcSmem::kK + st * TcSmem::kKV;
 #pragma unroll
         for (int k = 0; k < 4; ++k)  // 16 dims per step
-          umma_bf16(tmem + 64 * st, umma_desc_sw128(sQ + 32 * k, 16, 1024),
+          umma_bf16(tmem + 64 * sb, umma_desc_sw128(sQ + 32 * k, 16, 1024),
                     umma_desc_sw128(sK + 32 * k, 16, 1024), id_s, k > 0);
-        umma_commit(sfull + 8 * st);
-        umma_commit(kempty + 8 * st);  // the K stage may be refilled once S(b) is done
+        umma_commit(sfull + 8 * sb);
+        umma_commit(kempty + 8 * st);  // the K stage may be refilled once S(j) is done
         return true;
       };
       bool ok = mbar_wait_bounded(qready, 0, kPfWaitNs) && issue_s(0);
       for (int b = 0; b < nb && ok; ++b) {
-        const int st = b & 1;
+        const int st = b % kTcVStages, sb = b & 1;
         if (b + 1 < nb && !issue_s(b + 1)) {
           ok = false;
           break;
         }
-        if (!mbar_wait_bounded(pfull + 8 * st, (uint32_t)((b / 2) & 1), kPfWaitNs) ||
-            !mbar_wait_bounded(vfull + 8 * st, (uint32_t)((b / 2) & 1), kPfWaitNs)) {
+        if (!mbar_wait_bounded(pfull + 8 * sb, (uint32_t)((b / 2) & 1), kPfWaitNs) ||
+            !mbar_wait_bounded(vfull + 8 * st, (uint32_t)((b / kTcVStages) & 1), kPfWaitNs)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t sP = sbase + TcSmem::kP + st * TcSmem::kTile;
+        const uint32_t tP = tmem + kTmemP + 32 * sb;
         const uint32_t sV = sbase + TcSmem::kV + st * TcSmem::kKV;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)  // 16 keys per step; V is MN-major (16 rows = 2048 B)
-          umma_bf16(tmem + kTmemO, umma_desc_sw128(sP + 32 * k, 16, 1024),
-                    umma_desc_sw128(sV + 2048 * k, 8192, 1024), id_o, (b > 0 || k > 0));
-#pragma unroll
-        for (int k = 0; k < 4; ++k)  // L += P 1: the row sums of the same bf16 weights
-          umma_bf16(tmem + kTmemL, umma_desc_sw128(sP + 32 * k, 16, 1024),
-                    umma_desc_sw128(sOnes + 32 * k, 16, 1024), id_l, (b > 0 || k > 0));
-        umma_commit(odone + 8 * st);
+        for (int k = 0; k < 4; ++k)  // 16 keys (8 columns of P) per step; V is MN-major (16 rows = 2048 B)
+          umma_bf16_ta(tmem + kTmemO, tP + 8 * k, umma_desc_sw128(sV + 2048 * k, 8192, 1024), id_o,
+                       (b > 0 || k > 0));
+        umma_commit(odone + 8 * sb);
         umma_commit(vempty + 8 * st);
       }
+      // every MMA issued here is complete before tensor memory is freed
+      umma_commit(drain);
+      if (!mbar_wait_bounded(drain, 0, kPfWaitNs)) ok = false;
       if (!ok) report_error(p.d_err, PKV_ERR_TIMEOUT);
     }
-  } else if (warp < 4) {
-    // ---------------- Q tile (row i = token i / 4, head 4 g + i % 4) -------
-    const int t = threadIdx.x - 64;
-    for (int idx = t; idx < kTcRows * 8; idx += 64) {
-      const int row = idx >> 3, c = idx & 7;
-      const int tok = t0 + (row >> 2);
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (tok < t_end)
-        v = __ldg(reinterpret_cast<const uint4*>(
-                      p.q + ((size_t)(r0 + tok) * PKV_NUM_Q_HEADS + g * 4 + (row & 3)) * 64) + c);
-      *reinterpret_cast<uint4*>(smem + TcSmem::kQ + sw128_chunk(row, c)) = v;
-    }
-    for (int idx = t; idx < 16 * 8; idx += 64)  // bf16 1.0 = 0x3F80
-      *reinterpret_cast<uint4*>(smem + TcSmem::kOnes + idx * 16) =
-          make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-    fence_proxy_async_smem();
-    mbar_arrive(qready);
-  } else {
+  } else if (warp >= 4) {
     // ---------------- softmax: thread = row ------------------------------
     const int i = threadIdx.x - 128;               // TMEM lane = query row
     const uint32_t lane_base = (uint32_t)(32 * (warp - 4)) << 16;
@@ -513,40 +533,41 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const bool valid = tok < t_end;
     const int p_i = valid ? pos0 + tok : -1;
     float m_used = -INFINITY;
+    float l_run = 0.f;  // row sum of the bf16 weights, relative to m_used
     // every wait is decided warp-wide: the tensor-memory loads are warp-collective
     auto wait_all = [&](uint32_t bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, kPfWaitNs));
     };
     for (int b = 0; b < nb; ++b) {
-      const int st = b & 1;
-      const uint32_t sS = tmem + lane_base + 64 * st;
-      if (!wait_all(sfull + 8 * st, (uint32_t)((b / 2) & 1))) {
+      const int st = b % kTcVStages, sb = b & 1;
+      if (!wait_all(sfull + 8 * sb, (uint32_t)((b / 2) & 1))) {
         failed = true;
         break;
       }
       tc_fence_after();
-      const int k0 = b * kTcKeys;
-      // every key of the block visible to every row of the warp: no masks
-      const bool full = __all_sync(0xffffffffu, k0 + kTcKeys - 1 <= p_i);
-      // pass 1: the block's row max of the raw scores (scale * log2 e > 0,
-      // so it is applied once to the max)
-      float rmx = -INFINITY;
+      float v[64];
+      tmem_ld64(tmem + lane_base + 64 * sb, v);
+      tc_fence_before();
+      mbar_arrive(sfree + 8 * sb);  // S buffer sb is in registers
+      // keys k0 + c with c > lim are after this row's position (or past the
+      // sequence): their scores become -inf, their weights 0
+      const int k0 = b * kTcKeys, lim = p_i - k0;
+      if (!__all_sync(0xffffffffu, lim >= kTcKeys - 1)) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float v[32];
-        tmem_ld32(sS + 32 * h, v);
-        if (full) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) rmx = fmaxf(rmx, v[c]);
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (k0 + 32 * h + c <= p_i) rmx = fmaxf(rmx, v[c]);
-        }
+        for (int c = 0; c < 64; ++c) v[c] = c <= lim ? v[c] : -INFINITY;
       }
+      // the block's row max of the raw scores (scale * log2 e > 0, so it is
+      // applied once to the max)
+      float t[22];
+#pragma unroll
+      for (int c = 0; c < 21; ++c) t[c] = fmax3(v[3 * c], v[3 * c + 1], v[3 * c + 2]);
+      t[21] = v[63];
+#pragma unroll
+      for (int c = 0; c < 7; ++c) t[c] = fmax3(t[3 * c], t[3 * c + 1], t[3 * c + 2]);
+      const float rmx = fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmaxf(t[6], t[21]));
       const float mx = rmx * p.sl2;
-      // P buffer st was last read by P V(b - 2)
-      if (b >= 2 && !wait_all(odone + 8 * st, (uint32_t)((b / 2 - 1) & 1))) {
+      // P buffer sb was last read by P V(b - 2)
+      if (b >= 2 && !wait_all(odone + 8 * sb, (uint32_t)((b / 2 - 1) & 1))) {
         failed = true;
         break;
       }
@@ -559,56 +580,30 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         }
         tc_fence_after();
         const float alpha = (grow && m_used > -INFINITY) ? exp2f(m_used - mx) : 1.f;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float v[32];
-          tmem_ld32(tmem + lane_base + kTmemO + 32 * h, v);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] *= alpha;
-          tmem_st32(tmem + lane_base + kTmemO + 32 * h, v);
-        }
-        {  // the row sums live in columns [kTmemL, kTmemL + 16) of the same 32-column group
-          float v[32];
-          tmem_ld32(tmem + lane_base + kTmemL, v);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] *= alpha;
-          tmem_st32(tmem + lane_base + kTmemL, v);
-        }
+#pragma unroll 1
+        for (int c = 0; c < 64; c += 8) tmem_scale8(tmem + lane_base + kTmemO + c, alpha);
+        l_run *= alpha;
       }
       if (grow) m_used = mx;
-      // pass 2: weights rounded to bf16 (L sums the same values on the tensor cores)
-      uint8_t* Pst = smem + TcSmem::kP + st * TcSmem::kTile;
+      // weights rounded to bf16, packed two per column (even key low), and
+      // their sum as rounded; a row with nothing visible yet keeps
+      // m_used = -inf and gets zeros
+      const float nm = m_used == -INFINITY ? 0.f : -m_used;
+      uint32_t pk[32];
+      float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float v[32];
-        tmem_ld32(sS + 32 * h, v);
-        uint32_t pk[16];
-        const float nm = -m_used;
-        if (full) {
-#pragma unroll
-          for (int c = 0; c < 32; c += 2)
-            pk[c / 2] = pack_bf16x2(ex2_approx(fmaf(v[c], p.sl2, nm)), ex2_approx(fmaf(v[c + 1], p.sl2, nm)));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const int k = k0 + 32 * h + c;
-            const float w0 = (k <= p_i) ? ex2_approx(fmaf(v[c], p.sl2, nm)) : 0.f;
-            const float w1 = (k + 1 <= p_i) ? ex2_approx(fmaf(v[c + 1], p.sl2, nm)) : 0.f;
-            pk[c / 2] = pack_bf16x2(w0, w1);
-          }
-        }
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8)
-          *reinterpret_cast<uint4*>(Pst + sw128_chunk(i, 4 * h + c8)) =
-              make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+      for (int c = 0; c < 32; ++c) {
+        pk[c] = pack_bf16x2(ex2_approx(fmaf(v[2 * c], p.sl2, nm)), ex2_approx(fmaf(v[2 * c + 1], p.sl2, nm)));
+        ls0 += __uint_as_float(pk[c] << 16);
+        ls1 += __uint_as_float(pk[c] & 0xFFFF0000u);
       }
-      tc_fence_before();
-      mbar_arrive(sfree + 8 * st);  // S buffer st is read
+      l_run += ls0 + ls1;
+      tmem_st32_nowait(tmem + lane_base + kTmemP + 32 * sb, pk);
       // keys past the sequence's end: their V rows may hold any bits; zero
       // them once this block's V tiles have landed
       const int zero_from = max(0, n - k0);
       if (zero_from < kTcKeys) {
-        if (!wait_all(vfull + 8 * st, (uint32_t)((b / 2) & 1))) {
+        if (!wait_all(vfull + 8 * st, (uint32_t)((b / kTcVStages) & 1))) {
           failed = true;
           break;
         }
@@ -617,26 +612,29 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           *reinterpret_cast<uint4*>(vst + (zero_from + idx / 8) * 128 + (idx & 7) * 16) =
               make_uint4(0u, 0u, 0u, 0u);
       }
+      tmem_wait_st();
       fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(pfull + 8 * st);
+      tc_fence_before();  // P and any rescale of O are in tensor memory
+      mbar_arrive(pfull + 8 * sb);
     }
     const int lb = nb - 1;
     if (!failed && wait_all(odone + 8 * (lb & 1), (uint32_t)((lb / 2) & 1))) {
       tc_fence_after();
-      float lv[32];
-      tmem_ld32(tmem + lane_base + kTmemL, lv);
-      const float l = lv[0];
-      uint32_t* dst = reinterpret_cast<uint32_t*>(
+      const float l = l_run;
+      uint4* dst = reinterpret_cast<uint4*>(
           p.out + ((size_t)(r0 + (valid ? tok : 0)) * PKV_NUM_Q_HEADS + g * 4 + (i & 3)) * 64);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        float v[32];
-        tmem_ld32(tmem + lane_base + kTmemO + 32 * h, v);  // every lane: warp-collective
+        float o[32];
+        tmem_ld32(tmem + lane_base + kTmemO + 32 * h, o);  // every lane: warp-collective
         if (valid) {
 #pragma unroll
-          for (int c = 0; c < 32; c += 2)
-            dst[16 * h + c / 2] = pack_bf16x2(__fdiv_rn(v[c], l), __fdiv_rn(v[c + 1], l));
+          for (int c8 = 0; c8 < 4; ++c8)
+            dst[4 * h + c8] =
+                make_uint4(pack_bf16x2(__fdiv_rn(o[8 * c8], l), __fdiv_rn(o[8 * c8 + 1], l)),
+                           pack_bf16x2(__fdiv_rn(o[8 * c8 + 2], l), __fdiv_rn(o[8 * c8 + 3], l)),
+                           pack_bf16x2(__fdiv_rn(o[8 * c8 + 4], l), __fdiv_rn(o[8 * c8 + 5], l)),
+                           pack_bf16x2(__fdiv_rn(o[8 * c8 + 6], l), __fdiv_rn(o[8 * c8 + 7], l)));
         }
       }
     } else if (!failed) {
@@ -669,7 +667,7 @@ extern "C" int paged_gqa_prefill_ex(const void* q, int num_tokens, const int32_t
     return PKV_ERR_INVALID_ARGUMENT;
   if (num_seqs == 0 || max_q_len == 0 || num_tokens == 0) return PKV_OK;
   if (!q || !cu_q || !kv_pool || !block_tables || !seq_lens || !out) return PKV_ERR_INVALID_ARGUMENT;
-  if (!isfinite(scale)) return PKV_ERR_INVALID_ARGUMENT;
+  if (!isfinite(scale) || !(scale > 0.f)) return PKV_ERR_INVALID_ARGUMENT;
   if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
       (reinterpret_cast<uintptr_t>(cu_q) & 3u))
@@ -681,9 +679,10 @@ extern "C" int paged_gqa_prefill_ex(const void* q, int num_tokens, const int32_t
   int dev = 0;
   int rc = bind_stream_device(stream, &dev);
   if (rc != PKV_OK) return rc;
-  CUtensorMap map;
+  CUtensorMap map, qmap;
   rc = compute == PKV_COMPUTE_TENSOR ? make_pool_tile_map(&map, kv_pool, num_pages)
                                      : make_pool_map(&map, kv_pool, num_pages);
+  if (rc == PKV_OK && compute == PKV_COMPUTE_TENSOR) rc = make_q_group_map(&qmap, q, num_tokens);
   if (rc != PKV_OK) return rc;
 
   PrefillParams prm;
@@ -726,7 +725,7 @@ extern "C" int paged_gqa_prefill_ex(const void* q, int num_tokens, const int32_t
   }
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = smem;
-  return cuda_status(cudaLaunchKernelEx(&cfg, paged_prefill_tc_kernel, map, prm),
+  return cuda_status(cudaLaunchKernelEx(&cfg, paged_prefill_tc_kernel, map, qmap, prm),
                      "cudaLaunchKernelEx(prefill tcgen05)");
 }
 

@@ -1,4 +1,4 @@
-// The pool's TMA tensor map, shared by the decode and prefill kernels.
+// TMA tensor maps of the pool (decode and prefill) and of the query rows (prefill).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <mutex>
@@ -29,18 +29,18 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Pool viewed as a 4-D tensor: dim (64), token slot (16), head (8),
-// page * 2 + kv.  One box {64, 16, 1, 2} = the K and V tiles of one (page,
-// head), 2 x 2 KiB, stored in shared memory with the 128-byte swizzle (16
-// rows of 128 bytes each, so the V tile starts a fresh swizzle period).
-int make_pool_map(CUtensorMap* map, const void* pool, int num_pages) {
-  struct Cached {
-    const void* ptr = nullptr;
-    int pages = 0;
-    CUtensorMap map;
-  };
-  static thread_local Cached cache;
-  if (cache.ptr == pool && cache.pages == num_pages) {
+// One encoded map per (base pointer, extent) and kind, cached per thread:
+// the encode is a host-side driver call of a few microseconds.
+struct MapCache {
+  const void* ptr = nullptr;
+  long long extent = -1;
+  CUtensorMap map;
+};
+
+static int encode_bf16_4d(MapCache& cache, CUtensorMap* map, const void* base, long long extent,
+                          const cuuint64_t (&dims)[4], const cuuint64_t (&strides)[3],
+                          const cuuint32_t (&box)[4]) {
+  if (cache.ptr == base && cache.extent == extent) {
     *map = cache.map;
     return PKV_OK;
   }
@@ -49,13 +49,8 @@ int make_pool_map(CUtensorMap* map, const void* pool, int num_pages) {
     set_last_error("cudaGetDriverEntryPointByVersion", "cuTensorMapEncodeTiled unavailable");
     return PKV_ERR_CUDA;
   }
-  // (dim, token, head, 2 page + K/V): one box {64, 16, 1, 2} is the K tile and
-  // then the V tile of one (page, head), 4 KiB, in a single copy
-  const cuuint64_t dims[4] = {64, 16, PKV_NUM_KV_HEADS, (cuuint64_t)num_pages * 2};
-  const cuuint64_t strides[3] = {128, 2048, 2048 * PKV_NUM_KV_HEADS};
-  const cuuint32_t box[4] = {64, 16, 1, 2};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims, strides,
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -64,50 +59,45 @@ int make_pool_map(CUtensorMap* map, const void* pool, int num_pages) {
     set_last_error("cuTensorMapEncodeTiled", msg);
     return PKV_ERR_CUDA;
   }
-  cache.ptr = pool;
-  cache.pages = num_pages;
+  cache.ptr = base;
+  cache.extent = extent;
   cache.map = *map;
   return PKV_OK;
+}
+
+// Pool viewed as a 4-D tensor: dim (64), token slot (16), head (8),
+// page * 2 + kv.  One box {64, 16, 1, 2} = the K and V tiles of one (page,
+// head), 2 x 2 KiB, stored in shared memory with the 128-byte swizzle (16
+// rows of 128 bytes each, so the V tile starts a fresh swizzle period).
+int make_pool_map(CUtensorMap* map, const void* pool, int num_pages) {
+  static thread_local MapCache cache;
+  const cuuint64_t dims[4] = {64, 16, PKV_NUM_KV_HEADS, (cuuint64_t)num_pages * 2};
+  const cuuint64_t strides[3] = {128, 2048, 2048 * PKV_NUM_KV_HEADS};
+  const cuuint32_t box[4] = {64, 16, 1, 2};
+  return encode_bf16_4d(cache, map, pool, num_pages, dims, strides, box);
 }
 
 // The same view with a one-tile box {64, 16, 1, 1}: the K tile (kv = 0) or
 // the V tile (kv = 1) of one (page, head) alone, so that the tiles of
 // consecutive pages can be placed back to back in shared memory.
 int make_pool_tile_map(CUtensorMap* map, const void* pool, int num_pages) {
-  struct Cached {
-    const void* ptr = nullptr;
-    int pages = 0;
-    CUtensorMap map;
-  };
-  static thread_local Cached cache;
-  if (cache.ptr == pool && cache.pages == num_pages) {
-    *map = cache.map;
-    return PKV_OK;
-  }
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) {
-    set_last_error("cudaGetDriverEntryPointByVersion", "cuTensorMapEncodeTiled unavailable");
-    return PKV_ERR_CUDA;
-  }
-  // (dim, token, head, 2 page + K/V): one box {64, 16, 1, 2} is the K tile and
-  // then the V tile of one (page, head), 4 KiB, in a single copy
+  static thread_local MapCache cache;
   const cuuint64_t dims[4] = {64, 16, PKV_NUM_KV_HEADS, (cuuint64_t)num_pages * 2};
   const cuuint64_t strides[3] = {128, 2048, 2048 * PKV_NUM_KV_HEADS};
   const cuuint32_t box[4] = {64, 16, 1, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    char msg[64];
-    snprintf(msg, sizeof(msg), "CUresult %d", (int)r);
-    set_last_error("cuTensorMapEncodeTiled", msg);
-    return PKV_ERR_CUDA;
-  }
-  cache.ptr = pool;
-  cache.pages = num_pages;
-  cache.map = *map;
-  return PKV_OK;
+  return encode_bf16_4d(cache, map, pool, num_pages, dims, strides, box);
+}
+
+// Query rows [T][32][64] viewed as (dim 64, head in group 4, group 8, token
+// T).  One box {64, 4, 1, 32} = the 4 query heads of one group for 32
+// consecutive tokens: 128 rows of 128 bytes, token-major, swizzled like the
+// pool tiles; tokens past T read as zeros.
+int make_q_group_map(CUtensorMap* map, const void* q, int num_tokens) {
+  static thread_local MapCache cache;
+  const cuuint64_t dims[4] = {64, 4, PKV_NUM_KV_HEADS, (cuuint64_t)num_tokens};
+  const cuuint64_t strides[3] = {128, 512, 512 * PKV_NUM_KV_HEADS};
+  const cuuint32_t box[4] = {64, 4, 1, 32};
+  return encode_bf16_4d(cache, map, q, num_tokens, dims, strides, box);
 }
 
 }  // namespace pkv
