@@ -307,8 +307,12 @@ __global__ void __launch_bounds__(kPfThreads, 2)
 // rotate with b % 4, V stages with b % 3):
 //   producer warp 0: Q once, then K(b) -> K stage (after S(b - 4) read it)
 //   producer warp 2: V(b) -> V stage                (after P V(b - 3) read it)
-//   MMA thread:      S(b + 1) = Q K^T -> S buffer, while the softmax works on
-//                    S(b); then, once P(b) is written, O += P(b) V(b)
+//   S thread:        S(b) = Q K^T -> S buffer b & 1 once K(b) has landed and
+//                    the softmax has read S(b - 2)
+//   P V thread:      O += P(b) V(b) once P(b) is written
+// (S and P V are issued by threads of different warps: one thread issues an
+// MMA every ~100 cycles whatever its N, so a single issuer of both would
+// bound a 64-key block at 8 issue slots)
 //   softmax:         S(b) -> row max -> P(b) (bf16) in its own tensor-memory
 //                    buffer, row sums in registers
 // so the tensor cores compute the next scores and the last P V while the
@@ -324,7 +328,7 @@ constexpr int kTcKeys = 64;                    // keys per block (4 pages)
 constexpr int kTcPages = kTcKeys / PKV_PAGE_TOKENS;
 constexpr int kTcKStages = 4;
 constexpr int kTcVStages = 4;
-constexpr int kTcThreads = 256;                // w0 Q/K TMA, w1 MMA, w2 V TMA, w4-7 softmax
+constexpr int kTcThreads = 256;                // w0 Q/K TMA, w1 S MMA, w2 V TMA, w3 P V MMA, w4-7 softmax
 constexpr uint32_t kTmemCols = 256;            // S0 [0, 64), S1 [64, 128), O [128, 192), P0, P1 [192, 256)
 constexpr uint32_t kTmemO = 128;
 constexpr uint32_t kTmemP = 192;               // P buffers: 64 bf16 weights per row = 32 columns
@@ -338,8 +342,8 @@ struct TcSmem {
   static constexpr int kV = kK + kTcKStages * kKV;       // [kTcVStages] V stages
   static constexpr int kBars = kV + kTcVStages * kKV;
   // kfull, kempty [kTcKStages]; vfull, vempty [kTcVStages]; sfull, sfree, pfull,
-  // odone [2] each; qready; drain (the MMA thread's last commit)
-  static constexpr int kNumBars = 2 * kTcKStages + 2 * kTcVStages + 4 * 2 + 2;
+  // odone [2] each; qready; drain [2] (each MMA thread's last commit)
+  static constexpr int kNumBars = 2 * kTcKStages + 2 * kTcVStages + 4 * 2 + 3;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kBytes = kTmemSlot + 8;
 };
@@ -397,6 +401,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
     mbar_init(qready, 1);
     mbar_init(drain, 1);
+    mbar_init(drain + 8, 1);
     fence_mbar_init();
     bad_flag = 0;
   }
@@ -480,14 +485,17 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       if (!landed) report_error(p.d_err, PKV_ERR_TIMEOUT);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ------------------------------------------
+    // ---------------- S = Q K^T issuer ------------------------------------
     if (lane == 0) {
       const uint32_t id_s = umma_idesc_bf16(kTcRows, kTcKeys, 0);
-      const uint32_t id_o = umma_idesc_bf16(kTcRows, 64, 1);
-      auto issue_s = [&](int j) -> bool {  // S(j) into S buffer j & 1
-        const int st = j % kTcKStages, sb = j & 1;
-        if (!mbar_wait_bounded(kfull + 8 * st, (uint32_t)((j / kTcKStages) & 1), kPfWaitNs)) return false;
-        if (j >= 2 && !mbar_wait_bounded(sfree + 8 * sb, (uint32_t)((j / 2 - 1) & 1), kPfWaitNs)) return false;
+      bool ok = mbar_wait_bounded(qready, 0, kPfWaitNs);
+      for (int b = 0; b < nb && ok; ++b) {
+        const int st = b % kTcKStages, sb = b & 1;
+        if (!mbar_wait_bounded(kfull + 8 * st, (uint32_t)((b / kTcKStages) & 1), kPfWaitNs) ||
+            (b >= 2 && !mbar_wait_bounded(sfree + 8 * sb, (uint32_t)((b / 2 - 1) & 1), kPfWaitNs))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t sK = sbase + TcSmem::kK + st * TcSmem::kKV;
 #pragma unroll
@@ -495,16 +503,20 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           umma_bf16(tmem + 64 * sb, umma_desc_sw128(sQ + 32 * k, 16, 1024),
                     umma_desc_sw128(sK + 32 * k, 16, 1024), id_s, k > 0);
         umma_commit(sfull + 8 * sb);
-        umma_commit(kempty + 8 * st);  // the K stage may be refilled once S(j) is done
-        return true;
-      };
-      bool ok = mbar_wait_bounded(qready, 0, kPfWaitNs) && issue_s(0);
-      for (int b = 0; b < nb && ok; ++b) {
+        umma_commit(kempty + 8 * st);  // the K stage may be refilled once S(b) is done
+      }
+      // every MMA issued here is complete before tensor memory is freed
+      umma_commit(drain);
+      if (!mbar_wait_bounded(drain, 0, kPfWaitNs)) ok = false;
+      if (!ok) report_error(p.d_err, PKV_ERR_TIMEOUT);
+    }
+  } else if (warp == 3) {
+    // ---------------- O += P V issuer -------------------------------------
+    if (lane == 0) {
+      const uint32_t id_o = umma_idesc_bf16(kTcRows, 64, 1);
+      bool ok = true;
+      for (int b = 0; b < nb; ++b) {
         const int st = b % kTcVStages, sb = b & 1;
-        if (b + 1 < nb && !issue_s(b + 1)) {
-          ok = false;
-          break;
-        }
         if (!mbar_wait_bounded(pfull + 8 * sb, (uint32_t)((b / 2) & 1), kPfWaitNs) ||
             !mbar_wait_bounded(vfull + 8 * st, (uint32_t)((b / kTcVStages) & 1), kPfWaitNs)) {
           ok = false;
@@ -520,9 +532,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         umma_commit(odone + 8 * sb);
         umma_commit(vempty + 8 * st);
       }
-      // every MMA issued here is complete before tensor memory is freed
-      umma_commit(drain);
-      if (!mbar_wait_bounded(drain, 0, kPfWaitNs)) ok = false;
+      umma_commit(drain + 8);
+      if (!mbar_wait_bounded(drain + 8, 0, kPfWaitNs)) ok = false;
       if (!ok) report_error(p.d_err, PKV_ERR_TIMEOUT);
     }
   } else if (warp >= 4) {
