@@ -37,7 +37,6 @@ inline int cuda_status(cudaError_t e, const char* where = "cuda") {
 int make_pool_map(CUtensorMap* map, const void* pool, int num_pages);
 // The same view with a one-tile box {64, 16, 1, 1}.
 int make_pool_tile_map(CUtensorMap* map, const void* pool, int num_pages);
-// q [T][32][64] bf16 with box {64, 4, 1, 32}: 4 heads of one group x 32 tokens.
-int make_q_group_map(CUtensorMap* map, const void* q, int num_tokens);
+
 
 }  // namespace pkv

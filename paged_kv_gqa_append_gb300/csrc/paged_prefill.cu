@@ -303,47 +303,43 @@ __global__ void __launch_bounds__(kPfThreads, 2)
 // ---------------------------------------------------------------------------
 // tcgen05 prefill.
 //
-// Pipeline per 64-key block b (S and P buffers alternate with b & 1, K stages
-// rotate with b % 4, V stages with b % 3):
-//   producer warp 0: Q once, then K(b) -> K stage (after S(b - 4) read it)
-//   producer warp 2: V(b) -> V stage                (after P V(b - 3) read it)
+// Pipeline per 64-key block b (S buffers alternate with b & 1, K and V stages
+// rotate with b % 4):
+//   producer warp 0: K(b) -> K stage               (after S(b - 4) read it)
+//   producer warp 2: V(b) -> V stage               (after P V(b - 4) read it)
 //   S thread:        S(b) = Q K^T -> S buffer b & 1 once K(b) has landed and
-//                    the softmax has read S(b - 2)
+//                    P V(b - 2) has read that buffer's P
 //   P V thread:      O += P(b) V(b) once P(b) is written
-// (S and P V are issued by threads of different warps: one thread issues an
-// MMA every ~100 cycles whatever its N, so a single issuer of both would
-// bound a 64-key block at 8 issue slots)
-//   softmax:         S(b) -> row max -> P(b) (bf16) in its own tensor-memory
-//                    buffer, row sums in registers
-// so the tensor cores compute the next scores and the last P V while the
-// warpgroup turns the current scores into weights, and each K copy has three
-// blocks of time to land (copies take microseconds when every SM streams).
-// P V takes P from tensor memory: shared memory only feeds Q, K and V to the
-// tensor cores (its bandwidth, not the MMA rate, bounds small-N MMAs).
-// Page ids are read one block ahead.  Every barrier is used per buffer, so a
-// waiter is never two phases behind its barrier.
+//   softmax:         S(b) -> row max -> P(b) (bf16) over the first half of
+//                    S buffer b & 1, row sums in registers
+// Q, S, P and O live in tensor memory; shared memory only feeds K and V to
+// the tensor cores (its bandwidth bounds small-N MMAs reading it).  S and P V
+// are issued by threads of different warps: one thread issues an MMA every
+// ~100 cycles whatever its N, so a single issuer of both would bound a
+// 64-key block at 8 issue slots.  Each K copy has three blocks of time to
+// land (copies take microseconds when every SM streams); page ids are read
+// one block ahead.  Every barrier is used per buffer, so a waiter is never
+// two phases behind its barrier.
 // ---------------------------------------------------------------------------
 constexpr int kTcRows = 128;                   // 32 tokens x 4 query heads
 constexpr int kTcKeys = 64;                    // keys per block (4 pages)
 constexpr int kTcPages = kTcKeys / PKV_PAGE_TOKENS;
 constexpr int kTcKStages = 4;
 constexpr int kTcVStages = 4;
-constexpr int kTcThreads = 256;                // w0 Q/K TMA, w1 S MMA, w2 V TMA, w3 P V MMA, w4-7 softmax
-constexpr uint32_t kTmemCols = 256;            // S0 [0, 64), S1 [64, 128), O [128, 192), P0, P1 [192, 256)
+constexpr int kTcThreads = 256;                // w0 K TMA, w1 S MMA, w2 V TMA, w3 P V MMA, w4-7 softmax
+constexpr uint32_t kTmemCols = 256;            // S0 [0, 64), S1 [64, 128), O [128, 192), Q [192, 224)
 constexpr uint32_t kTmemO = 128;
-constexpr uint32_t kTmemP = 192;               // P buffers: 64 bf16 weights per row = 32 columns
+constexpr uint32_t kTmemQ = 192;               // 64 bf16 per row = 32 columns (P likewise, over S)
 constexpr float kLazyRescale = 8.f;            // log2 units
 
 struct TcSmem {
-  static constexpr int kTile = kTcRows * 128;            // 16 KB: 128 rows of 128 B
   static constexpr int kKV = kTcKeys * 128;              // 8 KB: 64 keys of 128 B
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;                  // [kTcKStages] K stages
+  static constexpr int kK = 0;                           // [kTcKStages] K stages
   static constexpr int kV = kK + kTcKStages * kKV;       // [kTcVStages] V stages
   static constexpr int kBars = kV + kTcVStages * kKV;
-  // kfull, kempty [kTcKStages]; vfull, vempty [kTcVStages]; sfull, sfree, pfull,
-  // odone [2] each; qready; drain [2] (each MMA thread's last commit)
-  static constexpr int kNumBars = 2 * kTcKStages + 2 * kTcVStages + 4 * 2 + 3;
+  // kfull, kempty [kTcKStages]; vfull, vempty [kTcVStages]; sfull, pfull, odone
+  // [2] each; qready; drain [2] (each MMA thread's last commit)
+  static constexpr int kNumBars = 2 * kTcKStages + 2 * kTcVStages + 3 * 2 + 3;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kBytes = kTmemSlot + 8;
 };
@@ -364,8 +360,7 @@ __device__ __forceinline__ void block_page_ids(const int32_t* row, int b, int n_
 }
 
 __global__ void __launch_bounds__(kTcThreads, 2)
-    paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap,
-                            const __grid_constant__ CUtensorMap qmap, const PrefillParams p) {
+    paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap, const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -375,12 +370,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const int qb = (int)gridDim.x - 1 - (int)blockIdx.x;  // latest (longest) blocks first
 
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase + TcSmem::kQ;
   const uint32_t bars = sbase + TcSmem::kBars;
   const uint32_t kfull = bars, kempty = kfull + 8 * kTcKStages, vfull = kempty + 8 * kTcKStages,
                  vempty = vfull + 8 * kTcVStages;
-  const uint32_t sfull = vempty + 8 * kTcVStages, sfree = sfull + 16, pfull = sfull + 32, odone = sfull + 48,
-                 qready = sfull + 64, drain = sfull + 72;
+  const uint32_t sfull = vempty + 8 * kTcVStages, pfull = sfull + 16, odone = sfull + 32,
+                 qready = sfull + 48, drain = sfull + 56;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TcSmem::kTmemSlot);
 
   // set-up that reads no global memory runs before the dependency wait
@@ -395,11 +389,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(sfull + 8 * k, 1);
-      mbar_init(sfree + 8 * k, kTcRows);
       mbar_init(pfull + 8 * k, kTcRows);
       mbar_init(odone + 8 * k, 1);
     }
-    mbar_init(qready, 1);
+    mbar_init(qready, kTcRows);
     mbar_init(drain, 1);
     mbar_init(drain + 8, 1);
     fence_mbar_init();
@@ -442,7 +435,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
   if (!run) {
   } else if (warp == 0 || warp == 2) {
-    // ---------------- producers: warp 0 Q then K tiles, warp 2 V tiles ----
+    // ---------------- producers: warp 0 K tiles, warp 2 V tiles ----------
     // (one lane each, in separate warps: two lanes of one warp would
     // reconverge after every wait, tying each K copy to a V stage)
     if (lane == 0) {
@@ -451,10 +444,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       const uint32_t dst0 = sbase + (kv ? TcSmem::kV : TcSmem::kK);
       const int nst = kv ? kTcVStages : kTcKStages;
       const int32_t* row = p.block_tables + (size_t)s * p.bt_stride;
-      if (kv == 0) {  // rows of tokens past this sequence's chunk are never stored
-        mbar_arrive_expect_tx(qready, (uint32_t)TcSmem::kTile);
-        tma_load_4d(sQ, &qmap, 0, 0, g, r0 + t0, qready);
-      }
       int ids[kTcPages];
       block_page_ids(row, 0, n_pages_seq, ids);
       int issued = 0;
@@ -479,7 +468,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       }
       // no copy may still be landing when the CTA exits (its consumers
       // normally saw every one; after a timeout they may not have)
-      bool landed = kv != 0 || mbar_wait_bounded(qready, 0, kPfWaitNs);
+      bool landed = true;
       for (int b = max(0, issued - nst); b < issued; ++b)
         landed = landed && mbar_wait_bounded(full + 8 * (b % nst), (uint32_t)((b / nst) & 1), kPfWaitNs);
       if (!landed) report_error(p.d_err, PKV_ERR_TIMEOUT);
@@ -491,17 +480,18 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       bool ok = mbar_wait_bounded(qready, 0, kPfWaitNs);
       for (int b = 0; b < nb && ok; ++b) {
         const int st = b % kTcKStages, sb = b & 1;
+        // S buffer sb holds P(b - 2) until P V(b - 2) is done
         if (!mbar_wait_bounded(kfull + 8 * st, (uint32_t)((b / kTcKStages) & 1), kPfWaitNs) ||
-            (b >= 2 && !mbar_wait_bounded(sfree + 8 * sb, (uint32_t)((b / 2 - 1) & 1), kPfWaitNs))) {
+            (b >= 2 && !mbar_wait_bounded(odone + 8 * sb, (uint32_t)((b / 2 - 1) & 1), kPfWaitNs))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t sK = sbase + TcSmem::kK + st * TcSmem::kKV;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)  // 16 dims per step
-          umma_bf16(tmem + 64 * sb, umma_desc_sw128(sQ + 32 * k, 16, 1024),
-                    umma_desc_sw128(sK + 32 * k, 16, 1024), id_s, k > 0);
+        for (int k = 0; k < 4; ++k)  // 16 dims (8 columns of Q) per step
+          umma_bf16_ta(tmem + 64 * sb, tmem + kTmemQ + 8 * k, umma_desc_sw128(sK + 32 * k, 16, 1024),
+                       id_s, k > 0);
         umma_commit(sfull + 8 * sb);
         umma_commit(kempty + 8 * st);  // the K stage may be refilled once S(b) is done
       }
@@ -523,7 +513,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           break;
         }
         tc_fence_after();
-        const uint32_t tP = tmem + kTmemP + 32 * sb;
+        const uint32_t tP = tmem + 64 * sb;  // P(b) over the first half of S buffer sb
         const uint32_t sV = sbase + TcSmem::kV + st * TcSmem::kKV;
 #pragma unroll
         for (int k = 0; k < 4; ++k)  // 16 keys (8 columns of P) per step; V is MN-major (16 rows = 2048 B)
@@ -549,6 +539,20 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     auto wait_all = [&](uint32_t bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, kPfWaitNs));
     };
+    {  // this row of Q (zeros past the chunk) into tensor memory: the A operand of S
+      uint32_t w[32];
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + ((size_t)(r0 + (valid ? tok : 0)) * PKV_NUM_Q_HEADS + g * 4 + (i & 3)) * 64);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 x = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+        w[4 * c] = x.x, w[4 * c + 1] = x.y, w[4 * c + 2] = x.z, w[4 * c + 3] = x.w;
+      }
+      tmem_st32_nowait(tmem + lane_base + kTmemQ, w);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(qready);
+    }
     for (int b = 0; b < nb; ++b) {
       const int st = b % kTcVStages, sb = b & 1;
       if (!wait_all(sfull + 8 * sb, (uint32_t)((b / 2) & 1))) {
@@ -558,8 +562,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       tc_fence_after();
       float v[64];
       tmem_ld64(tmem + lane_base + 64 * sb, v);
-      tc_fence_before();
-      mbar_arrive(sfree + 8 * sb);  // S buffer sb is in registers
       // keys k0 + c with c > lim are after this row's position (or past the
       // sequence): their scores become -inf, their weights 0
       const int k0 = b * kTcKeys, lim = p_i - k0;
@@ -577,11 +579,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       for (int c = 0; c < 7; ++c) t[c] = fmax3(t[3 * c], t[3 * c + 1], t[3 * c + 2]);
       const float rmx = fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmaxf(t[6], t[21]));
       const float mx = rmx * p.sl2;
-      // P buffer sb was last read by P V(b - 2)
-      if (b >= 2 && !wait_all(odone + 8 * sb, (uint32_t)((b / 2 - 1) & 1))) {
-        failed = true;
-        break;
-      }
+      // (P V(b - 2), the last reader of S buffer sb, finished before S(b) was issued)
       const bool grow = mx > m_used + kLazyRescale || (m_used == -INFINITY && mx > -INFINITY);
       if (__any_sync(0xffffffffu, grow && m_used > -INFINITY)) {
         // O is rescaled: every P V so far (the last is P V(b - 1)) must be done
@@ -609,7 +607,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         ls1 += __uint_as_float(pk[c] & 0xFFFF0000u);
       }
       l_run += ls0 + ls1;
-      tmem_st32_nowait(tmem + lane_base + kTmemP + 32 * sb, pk);
+      tmem_st32_nowait(tmem + lane_base + 64 * sb, pk);
       // keys past the sequence's end: their V rows may hold any bits; zero
       // them once this block's V tiles have landed
       const int zero_from = max(0, n - k0);
@@ -690,10 +688,9 @@ extern "C" int paged_gqa_prefill_ex(const void* q, int num_tokens, const int32_t
   int dev = 0;
   int rc = bind_stream_device(stream, &dev);
   if (rc != PKV_OK) return rc;
-  CUtensorMap map, qmap;
+  CUtensorMap map;
   rc = compute == PKV_COMPUTE_TENSOR ? make_pool_tile_map(&map, kv_pool, num_pages)
                                      : make_pool_map(&map, kv_pool, num_pages);
-  if (rc == PKV_OK && compute == PKV_COMPUTE_TENSOR) rc = make_q_group_map(&qmap, q, num_tokens);
   if (rc != PKV_OK) return rc;
 
   PrefillParams prm;
@@ -736,7 +733,7 @@ extern "C" int paged_gqa_prefill_ex(const void* q, int num_tokens, const int32_t
   }
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = smem;
-  return cuda_status(cudaLaunchKernelEx(&cfg, paged_prefill_tc_kernel, map, qmap, prm),
+  return cuda_status(cudaLaunchKernelEx(&cfg, paged_prefill_tc_kernel, map, prm),
                      "cudaLaunchKernelEx(prefill tcgen05)");
 }
 

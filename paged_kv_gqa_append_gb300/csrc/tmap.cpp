@@ -1,4 +1,4 @@
-// TMA tensor maps of the pool (decode and prefill) and of the query rows (prefill).
+// The pool's TMA tensor maps, shared by the decode and prefill kernels.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <mutex>
@@ -86,18 +86,6 @@ int make_pool_tile_map(CUtensorMap* map, const void* pool, int num_pages) {
   const cuuint64_t strides[3] = {128, 2048, 2048 * PKV_NUM_KV_HEADS};
   const cuuint32_t box[4] = {64, 16, 1, 1};
   return encode_bf16_4d(cache, map, pool, num_pages, dims, strides, box);
-}
-
-// Query rows [T][32][64] viewed as (dim 64, head in group 4, group 8, token
-// T).  One box {64, 4, 1, 32} = the 4 query heads of one group for 32
-// consecutive tokens: 128 rows of 128 bytes, token-major, swizzled like the
-// pool tiles; tokens past T read as zeros.
-int make_q_group_map(CUtensorMap* map, const void* q, int num_tokens) {
-  static thread_local MapCache cache;
-  const cuuint64_t dims[4] = {64, 4, PKV_NUM_KV_HEADS, (cuuint64_t)num_tokens};
-  const cuuint64_t strides[3] = {128, 512, 512 * PKV_NUM_KV_HEADS};
-  const cuuint32_t box[4] = {64, 4, 1, 32};
-  return encode_bf16_4d(cache, map, q, num_tokens, dims, strides, box);
 }
 
 }  // namespace pkv
