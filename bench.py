@@ -600,7 +600,7 @@ def run_prefill_line(args, world, rank, local):
             "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"prefill_b{S}_p{P}", "prompts": S, "prompt_tokens": P,
-                       "l2": "pool 240 MiB > 129 MB L2 and every page read by 32 query blocks",
+                       "l2": "q (63 MB), out (63 MB) and pool (31.5 MB) together exceed the 129 MB L2; each page is read by up to 60 query blocks",
                        "parallelism": f"replicas x{world}"},
             "clocks": clk, "gpu_launches": steps,
             "e2e": {"value": flops * k_e2e * world / e2e_s / 1e12, "unit": "TFLOP/s",
@@ -608,7 +608,7 @@ def run_prefill_line(args, world, rank, local):
                     "steps": k_e2e},
             "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak,
                          "unit": "TFLOP/s", "frac": value / world / peak, "traffic": None,
-                         "peak_source": kind, "kernel": "paged_prefill_kernel (mma.sync bf16)",
+                         "peak_source": kind, "kernel": "paged_prefill_tc_kernel (tcgen05 bf16, S and O in tensor memory)",
                          "avg_launch_us": avg_us, "algorithmic_flops_per_launch": flops},
             "cpu_baseline": cpu}), flush=True)
 
