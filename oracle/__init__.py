@@ -15,6 +15,9 @@ to check by eye, in FP64 NumPy with per-element loops where that is clearer:
 * ``paged_kv``   append into 16-token pages through per-sequence block tables,
                  and decode attention over a sequence's own pages (the softmax
                  definition, plus a split/log-sum-exp-combine restatement).
+* ``int8_kv``    INT8 K/V pages: per-row symmetric 8-bit codes with fp32
+                 scales, the quantised append, and decode over the
+                 dequantised pages.
 * ``admission``  the admission-credit rule and a FIFO continuous-batching
                  simulation with on-demand page allocation.
 
@@ -25,6 +28,8 @@ Sources (titles of the pages that define the path):
     de batching" (16-token pages, per-sequence per-layer block tables, append at
     the absolute RoPE position, paged attention over the sequence's own pages,
     admission credit, rejection of oversize requests).
+  - "Lifecycle and Memory Model" (TinyLoop C++ API), section "Per-request /
+    handle-owned memory" (a request's KV cache stored as FP16 or INT8 K/V).
   - tiny-vllm chapter "2. Weight Loading and GPU Buffer Design", sections
     "Preallocating the 16 compute buffers" (model constants) and "What else is
     set up in the initialization block" (block table initialised to -1).
@@ -32,4 +37,4 @@ Sources (titles of the pages that define the path):
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 (closed forms, invariants, brute force, library routines); none is unpinned.
 """
-from . import admission, bf16, paged_kv, rope  # noqa: F401
+from . import admission, bf16, int8_kv, paged_kv, rope  # noqa: F401

@@ -1,0 +1,182 @@
+"""INT8 K/V pages: quantised paged append and paged GQA decode over them.
+
+TEST INFRASTRUCTURE ONLY (like the rest of ``oracle/``).
+
+Source: "Lifecycle and Memory Model" (TinyLoop C++ API), section
+"Per-request / handle-owned memory": a request's RuntimeKVCache keeps its
+layers as FP16 K/V or as INT8 K/V, among other storage modes.  The page does
+not say how the 8-bit values are formed.  Reading taken here (the plainest
+one for a cache that grows one token at a time, where a row, once written,
+never changes):
+
+  * every (token, KV head) row of K and every such row of V -- 64 values --
+    is quantised on its own, symmetrically, with one fp32 scale:
+        amax    = max_d |x_d|
+        scale   = fp32(amax / 127)
+        code_d  = round-half-even(fp32(x_d / scale)), kept in [-127, 127]
+    and a row with amax == 0 gets scale 0 and codes 0;
+  * x is the row the bf16 cache would hold: K rotated at its position and
+    rounded to bf16 exactly as ``paged_kv.append_rope`` does, V as given;
+  * the value a code stands for is code * scale (exact in FP64);
+  * decode is the bf16 definition (``paged_kv.attend``) applied to those
+    values: nothing else about attention changes.
+
+Storage (the page geometry of the bf16 pool, one byte per element):
+  codes   int8    [num_pages][2 (K, V)][8 heads][16 slots][64 dims]  16 KiB/page
+  scales  float32 [num_pages][2 (K, V)][8 heads][16 slots]            1 KiB/page
+
+fp32 emulation: each division is done in FP64 and rounded once to fp32.  For
++, -, *, / a binary64 intermediate followed by rounding to binary32 gives the
+correctly rounded binary32 result (53 >= 2*24 + 2; Figueroa, "When is double
+rounding innocuous?", 1995), so these are the IEEE fp32 divisions.
+
+Parity status: pinned by ``tests/test_oracle_int8.py`` (integer rows,
+power-of-two scaling, the half-step error bound, ties, brute-force nearest
+code, a sentinel scan of the append, and the decode against a float64
+library attention over the dequantised pages).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import bf16, rope
+from .paged_kv import GROUP, HEAD_DIM, NUM_KV_HEADS, NUM_Q_HEADS, PAGE_TOKENS, attend, locate
+
+QMAX = 127
+
+
+def quantize_rows(x) -> tuple[np.ndarray, np.ndarray]:
+    """Symmetric 8-bit codes and fp32 scales of rows of 64 values (last axis).
+
+    x: values exactly representable in fp32 (here: bf16 values), [..., 64].
+    Returns (codes int8 [..., 64], scales float32 [...]).  Each row is
+    quantised on its own, by the steps of the module docstring.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    amax = np.max(np.abs(x), axis=-1)
+    scale = (amax / QMAX).astype(np.float32)                       # fp32(amax / 127)
+    zero = scale == 0                                              # amax == 0 (see below)
+    den = np.where(zero, 1.0, scale.astype(np.float64))[..., None]
+    q = (x / den).astype(np.float32)                               # fp32(x_d / scale)
+    codes = np.clip(np.rint(q), -QMAX, QMAX)                       # ties to even
+    codes = np.where(zero[..., None], 0.0, codes)
+    return codes.astype(np.int8), scale
+
+
+def quantize_row(x) -> tuple[np.ndarray, np.float32]:
+    """``quantize_rows`` of a single row: (codes int8 [64], scale float32)."""
+    codes, scale = quantize_rows(np.asarray(x, dtype=np.float64)[None, :])
+    return codes[0], np.float32(scale[0])
+
+
+def dequantize(codes, scales) -> np.ndarray:
+    """code * scale in FP64; scales broadcast over the last (dim) axis."""
+    return np.asarray(codes, np.float64) * np.asarray(scales, np.float64)[..., None]
+
+
+def new_pools(num_pages: int, code_fill: int = 0, scale_fill: float = 0.0):
+    """(codes int8 [N][2][8][16][64], scales float32 [N][2][8][16])."""
+    codes = np.full((num_pages, 2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM), code_fill, dtype=np.int8)
+    scales = np.full((num_pages, 2, NUM_KV_HEADS, PAGE_TOKENS), scale_fill, dtype=np.float32)
+    return codes, scales
+
+
+def append_rope_int8(codes, scales, k_bits, v_bits, positions, token_seq, block_tables, cos, sin,
+                     q_bits=None, inplace=False):
+    """Write T new tokens into the INT8 pools.  Returns (codes', scales', q_rot or None, err).
+
+    Arguments as ``paged_kv.append_rope``; the pools are those of
+    ``new_pools``.  The K row of each head is rotated and rounded to bf16 as
+    in the bf16 cache, then quantised; the V row is quantised from its bf16
+    values.  q (when given) is rotated as in the bf16 append and not
+    quantised.  A token with a bad row, position or page id writes nothing,
+    gets a zero q row and raises the flag.
+    """
+    c_out = codes if inplace else np.array(codes, copy=True)
+    s_out = scales if inplace else np.array(scales, copy=True)
+    num_pages = c_out.shape[0]
+    S, max_blocks = block_tables.shape
+    max_pos = cos.shape[0]
+    T = k_bits.shape[0]
+    q_rot = None if q_bits is None else np.zeros_like(q_bits)
+    err = False
+    for t in range(T):
+        s = t if token_seq is None else int(token_seq[t])
+        p = int(positions[t])
+        if s < 0 or s >= S or p < 0 or p >= max_pos:
+            err = True
+            continue
+        where = locate(block_tables[s], p, num_pages, max_blocks)
+        if where is None:
+            err = True
+            continue
+        page, slot = where
+        k_rot = rope.rotate_bf16(k_bits[t], cos[p], sin[p])          # [8][64] bf16 bits
+        for g in range(NUM_KV_HEADS):
+            c_out[page, 0, g, slot], s_out[page, 0, g, slot] = quantize_row(bf16.to_f64(k_rot[g]))
+            c_out[page, 1, g, slot], s_out[page, 1, g, slot] = quantize_row(bf16.to_f64(v_bits[t, g]))
+        if q_bits is not None:
+            for h in range(NUM_Q_HEADS):
+                q_rot[t, h] = rope.rotate_bf16(q_bits[t, h], cos[p], sin[p])
+    return c_out, s_out, q_rot, err
+
+
+def gather_int8(codes, scales, block_table_row, n: int):
+    """Dequantised K, V of positions [0, n) as float64 [n][8][64]; None on a bad page id."""
+    num_pages = codes.shape[0]
+    K = np.empty((n, NUM_KV_HEADS, HEAD_DIM))
+    V = np.empty((n, NUM_KV_HEADS, HEAD_DIM))
+    for j in range((n + PAGE_TOKENS - 1) // PAGE_TOKENS):
+        page = int(block_table_row[j])
+        if page < 0 or page >= num_pages:
+            return None
+        lo, hi = j * PAGE_TOKENS, min(n, (j + 1) * PAGE_TOKENS)
+        k = dequantize(codes[page, 0, :, :hi - lo, :], scales[page, 0, :, :hi - lo])   # [8][slot][64]
+        v = dequantize(codes[page, 1, :, :hi - lo, :], scales[page, 1, :, :hi - lo])
+        K[lo:hi] = k.transpose(1, 0, 2)
+        V[lo:hi] = v.transpose(1, 0, 2)
+    return K, V
+
+
+def decode_int8(q_bits, codes, scales, block_tables, seq_lens, scale: float):
+    """Decode-step GQA attention over INT8 pages; the rules of ``paged_kv.decode``.
+
+    Returns (out float64 [S][32][64], error_flag).
+    """
+    S = q_bits.shape[0]
+    max_blocks = block_tables.shape[1]
+    out = np.zeros((S, NUM_Q_HEADS, HEAD_DIM))
+    err = False
+    q = bf16.to_f64(q_bits)
+    for s in range(S):
+        n = int(seq_lens[s])
+        if n < 0 or n > PAGE_TOKENS * max_blocks:
+            err = True
+            continue
+        if n == 0:
+            continue
+        kv = gather_int8(codes, scales, block_tables[s], n)
+        if kv is None:
+            err = True
+            continue
+        K, V = kv
+        for h in range(NUM_Q_HEADS):
+            g = h // GROUP
+            out[s, h] = attend(q[s, h], K[:, g, :], V[:, g, :], scale)
+    return out, err
+
+
+def decode_one_int8(q_bits_sh, codes, scales, block_table_row, n: int, scale: float, h: int):
+    """One (sequence, query head) output, for sampled checks at full size."""
+    kv = gather_int8(codes, scales, block_table_row, n)
+    if kv is None:
+        raise ValueError("bad page id")
+    K, V = kv
+    g = h // GROUP
+    return attend(bf16.to_f64(q_bits_sh), K[:, g, :], V[:, g, :], scale)
+
+
+def quantize_pool(pool_bits):
+    """INT8 pools holding what ``append_rope_int8`` would store for every row of
+    a bf16 pool (pool bits [N][2][8][16][64]); for building test inputs."""
+    return quantize_rows(bf16.to_f64(pool_bits))
