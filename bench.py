@@ -48,10 +48,12 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--workload", choices=["batch32", "stress256", "prefill", "argmax"],
+    ap.add_argument("--workload", choices=["batch32", "stress256", "int8", "int8_stress256",
+                                           "prefill", "argmax"],
                     default="batch32",
-                    help="batch32 / stress256: the decode step; prefill: causal prefill of 8 "
-                         "prompts x 1920 tokens; argmax: next-token argmax of 32 x 128256 logits")
+                    help="batch32 / stress256: the decode step; int8 / int8_stress256: the same "
+                         "step on INT8 K/V pages; prefill: causal prefill of 8 prompts x 1920 "
+                         "tokens; argmax: next-token argmax of 32 x 128256 logits")
     ap.add_argument("--compute", choices=["tensor", "fma"], default="tensor")
     ap.add_argument("--layers", type=int, default=0,
                     help="layers of the workload (0 = its own: 16); fewer layers shrink the pool "
@@ -66,7 +68,7 @@ def parse():
 
 
 def make_case(name, layers=0):
-    case = W.case_batch32() if name == "batch32" else W.case_stress()
+    case = W.case_batch32() if name in ("batch32", "int8") else W.case_stress()
     if layers and layers != case.num_layers:  # same batch, context and seed, fewer layers
         case = W.case_uniform(case.seed, case.num_seqs, layers, int(case.seq_lens[0]),
                               outlier_frac=case.outlier_frac,
@@ -231,6 +233,32 @@ class OracleSample:
                 return done * self.kv_bytes / el / 1e9, done, el
 
 
+class OracleSampleInt8(OracleSample):
+    """The same (layer, sequence) pair on INT8 pages: append the new token
+    (K rotated and quantised, V quantised, q rotated), then decode."""
+
+    def __init__(self, case):
+        super().__init__(case)
+        import dataclasses
+        from oracle import int8_kv as OI
+        self.OI = OI
+        pages_per = self.pool.shape[0]
+        small = dataclasses.replace(case, num_pages=pages_per, outlier_frac=0.0)
+        codes, scales = W.fill_pool_int8(small)
+        self.codes, self.scales = codes.numpy(), scales.numpy()
+        self.kv_bytes = self.n * W.NUM_KV_HEADS * INT8_ROW_BYTES
+
+    def run_one(self):
+        c2, s2, qr, _ = self.OI.append_rope_int8(self.codes, self.scales, self.k, self.v,
+                                                 np.array([self.n - 1]), None, self.bt, self.cos,
+                                                 self.sin, self.q)
+        self.OI.decode_int8(qr, c2, s2, self.bt, np.array([self.n]), self.case.scale)
+
+
+# K and V of one (token, KV head) on INT8 pages: 64 + 64 code bytes, 4 + 4 scale bytes
+INT8_ROW_BYTES = 2 * (W.HEAD_DIM + 4)
+
+
 def cpu_cores_used():
     return 1  # the oracle is single-threaded NumPy (BLAS pinned to one thread)
 
@@ -282,7 +310,8 @@ def run_reference(args, world, rank):
         run_reference_other(args)
         return
     case = make_case(args.workload, args.layers)
-    ora = OracleSample(case)
+    int8 = args.workload.startswith("int8")
+    ora = OracleSampleInt8(case) if int8 else OracleSample(case)
     # warm-up steps, then K timed steps; each step = one (layer, seq) pair
     for _ in range(args.warmup):
         ora.run_one()
@@ -293,15 +322,15 @@ def run_reference(args, world, rank):
     pairs = args.steps
     n_tok = ora.n
     value = pairs * ora.kv_bytes / el / 1e9
-    sample = (f"{pairs} (layer, sequence) pairs of {case.name}: append 1 token + decode 32 heads "
-              f"over {n_tok} tokens each")
+    sample = (f"{pairs} (layer, sequence) pairs of {case.name}{' on INT8 pages' if int8 else ''}: "
+              f"append 1 token + decode 32 heads over {n_tok} tokens each")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": case.name, "batch": case.num_seqs, "layers": case.num_layers,
-                   "ctx": n_tok, "sample": "one (layer, seq) pair per step"},
+        "config": {"workload": ("int8_" if int8 else "") + case.name, "batch": case.num_seqs,
+                   "layers": case.num_layers, "ctx": n_tok, "sample": "one (layer, seq) pair per step"},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cpu_cores_used(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -486,6 +515,129 @@ def run_gb300(args, world, rank, local):
             "roofline": roof, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------- INT8 pages ----
+
+def run_int8_line(args, world, rank, local):
+    """The decode step on INT8 K/V pages: per layer kv_append_rope_int8 (new
+    token quantised into its page, q rotated) then paged_gqa_decode_int8, one
+    CUDA graph per step.  KV bytes per (token, head): 136 (codes and scales)."""
+    import paged_kv_gqa_append_gb300 as pkv
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    case = make_case(args.workload, args.layers)
+    L, S = case.num_layers, case.num_seqs
+    codes, scales = W.fill_pool_int8(case, device=dev)
+    q_raw = W.fill_queries(case, device=dev)
+    k_new, v_new = W.fill_new_kv(case, device=dev)
+    bt = torch.from_numpy(case.block_tables).to(dev)
+    lens = torch.from_numpy(case.seq_lens).to(dev)
+    pos = torch.from_numpy(W.new_positions(case)).to(dev)
+    cos, sin = pkv.rope_tables_device(dev, W.MAX_CONTEXT)
+    out = torch.empty_like(q_raw)
+    kv_bytes_layer = int(case.seq_lens.sum()) * W.NUM_KV_HEADS * INT8_ROW_BYTES
+    step = pkv.Int8DecodeStep(codes, scales, bt, lens, pos, k_new, v_new, q_raw, out, cos, sin,
+                              case.scale, max_seq_len=case.max_seq_len)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        step.run()
+    if step.error() != 0:
+        raise RuntimeError("device error during the INT8 warm-up")
+
+    def timed(run, k):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(k):
+            run()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.5 if clocks else 0)
+    barrier(world)
+    t_wall0 = time.time()
+    ms = max_over_ranks(timed(step.run, args.steps), world, dev)
+    barrier(world)
+    if step.error() != 0:
+        raise RuntimeError("device error in the INT8 timed region")
+    # the decode kernel alone (dominant) and the append kernel alone
+    g_dec, g_app = step.partial_graph(False, True), step.partial_graph(True, False)
+    for _ in range(3):
+        g_dec.replay()
+        g_app.replay()
+    k_part = max(10, args.steps // 4)
+    dec_avg_ms = timed(g_dec.replay, k_part) / (k_part * L)
+    append_us = timed(g_app.replay, k_part) * 1e3 / (k_part * L)
+    if step.error() != 0:
+        raise RuntimeError("device error in the INT8 kernel timings")
+    clk = clocks.summary(t_wall0, time.time()) if clocks else None
+    if clocks:
+        clocks.stop()
+    steps = args.steps
+    sec = ms / 1e3
+    value = kv_bytes_layer * L * steps * world / sec / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        hs = [t.cpu().pin_memory() for t in (q_raw, k_new, v_new, pos, lens, bt)]
+        devs = (q_raw, k_new, v_new, pos, lens, bt)
+        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in hs)
+        k_e2e = max(1, min(steps, 500))
+
+        def e2e_step():
+            for d, h in zip(devs, hs):
+                d.copy_(h, non_blocking=True)
+            step.run()
+            out_h.copy_(out, non_blocking=True)
+        barrier(world)
+        t0 = time.perf_counter()
+        dev_ms = timed(e2e_step, k_e2e)
+        e2e_s = max_over_ranks(max(dev_ms / 1e3, time.perf_counter() - t0), world, dev)
+        e2e = {"value": kv_bytes_layer * L * k_e2e * world / e2e_s / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_h.numel() * out_h.element_size(),
+               "steps": k_e2e, "tokens_per_s": S * k_e2e * world / e2e_s,
+               "path": "Int8DecodeStep graph replay + pinned H2D/D2H copies"}
+        if step.error() != 0:
+            raise RuntimeError("device error in the INT8 e2e region")
+
+    peak, peak_kind = hbm_peak()
+    achieved = kv_bytes_layer / (dec_avg_ms / 1e3) / 1e9
+    tag = "paged_decode_int8"
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": ncu_traffic(f"{tag}:{case.name}"),
+            "peak_source": peak_kind,
+            "kernel": f"{tag} (paged_gqa_decode_int8: decode-only graph, one launch per layer)",
+            "launches_timed": k_part * L, "algorithmic_bytes_per_launch": kv_bytes_layer,
+            "avg_launch_us": dec_avg_ms * 1e3}
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, pairs, el = OracleSampleInt8(case).timed(10.0)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": cpu_cores_used(), "kind": "oracle",
+               "sample": f"{pairs} (layer, sequence) pairs of {case.name} on INT8 pages (append "
+                         f"1 token + decode 32 heads over {int(case.seq_lens[0])} tokens), {el:.1f} s"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": ms / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic",
+            "config": {"workload": "int8_" + case.name, "batch": S, "layers": L,
+                       "ctx": int(case.seq_lens[0]), "pool_pages": case.num_pages,
+                       "pool_bytes": case.num_pages * (W.PAGE_ELEMS + 2 * 8 * 16 * 4),
+                       "kv_format": "int8 codes + fp32 scale per (token, KV head) row of K and V; "
+                                    "fp16 tensor-core MMAs, fp32 accumulation",
+                       "l2": "inputs larger than L2 (pool read per step exceeds 129 MB L2)",
+                       "parallelism": f"replicas x{world}",
+                       "launch": "CUDA graph of the step: INT8 append kernel + INT8 decode kernel per layer"},
+            "tokens_per_s": S * steps * world / sec, "us_per_layer": ms * 1e3 / (steps * L),
+            "decode_us_per_layer": dec_avg_ms * 1e3, "append_us_per_layer": append_us,
+            "kv_bytes_per_step": kv_bytes_layer * L, "hbm_frac_step": value / world / peak,
+            "clocks": clk, "e2e": e2e, "gpu_launches": step.launches_per_step * steps,
+            "roofline": roof, "cpu_baseline": cpu}), flush=True)
 
 
 # ------------------------------------------------ prefill and argmax lines --
@@ -703,6 +855,8 @@ def main():
             run_prefill_line(args, world, rank, local)
         elif args.workload == "argmax":
             run_argmax_line(args, world, rank, local)
+        elif args.workload.startswith("int8"):
+            run_int8_line(args, world, rank, local)
         else:
             run_gb300(args, world, rank, local)
     finally:

@@ -292,6 +292,59 @@ int paged_gqa_decode_append(const void* q, const void* k_new, const void* v_new,
                             int* d_err, void* stream, const pkv_decode_opts* opts);
 
 /* ------------------------------------------------------------------------
+ * INT8 K/V pages - the "INT8 K/V" storage mode of a request's KV cache
+ * ("Lifecycle and Memory Model", TinyLoop C++ API, section "Per-request /
+ * handle-owned memory", RuntimeKVCache).  The page names the mode only; the
+ * scheme here is the library's reading of it for a cache written one token
+ * at a time: every (token, KV head) row of K and of V -- 64 values -- is
+ * quantised on its own, symmetrically, with one fp32 scale:
+ *     amax = max_d |x_d|,  scale = amax / 127,
+ *     code_d = round-half-even(x_d / scale) in [-127, 127]
+ * (both divisions IEEE fp32; amax == 0 gives scale 0 and zero codes), where
+ * x is the row the bf16 cache would hold (K rotated and rounded to bf16 as in
+ * kv_append_rope, V as given).  A code stands for code * scale.  Rows must be
+ * finite.  Pages keep the bf16 pool's geometry and block tables:
+ *   kv_codes   device int8  [num_pages][2 (K,V)][8][16][64], 16 KiB/page
+ *   kv_scales  device float [num_pages][2 (K,V)][8][16],      1 KiB/page
+ * both 16-byte aligned, caller-owned.
+ * ---------------------------------------------------------------------- */
+
+/* kv_append_rope into INT8 pages: the arguments, ordering and error rules of
+ * kv_append_rope, with the bf16 pool replaced by (kv_codes, kv_scales).  The
+ * rotated q (when q_in is given) stays bf16.  k, v, kv_codes and kv_scales
+ * must be 16-byte aligned, q_in/q_out 4-byte aligned. */
+int kv_append_rope_int8(const void* k, const void* v, const int32_t* positions,
+                        const int32_t* token_seq, int T,
+                        const int32_t* block_tables, int num_seqs, int bt_row_stride,
+                        int max_blocks, void* kv_codes, float* kv_scales, int num_pages,
+                        const float* rope_cos, const float* rope_sin, int max_pos,
+                        const void* q_in, void* q_out, int* d_err, void* stream);
+
+/* paged_gqa_decode over INT8 pages: the same contract (arguments, workspace
+ * of paged_gqa_decode_workspace_bytes, error rules), with the bf16 pool
+ * replaced by (kv_codes, kv_scales).  Attention is over the dequantised
+ * values: scores scale * q . (code_K * scale_K), weights applied to
+ * code_V * scale_V.  Codes enter bf16 tensor-core MMAs exactly; the K scale
+ * multiplies each fp32 score, and each probability times its V scale is
+ * rounded to bf16 for the P V product (fp32 accumulation).  Output bf16. */
+int paged_gqa_decode_int8(const void* q, const void* kv_codes, const float* kv_scales,
+                          int num_pages, const int32_t* block_tables, int bt_row_stride,
+                          int max_blocks, const int32_t* seq_lens, int num_seqs,
+                          int max_seq_len, void* out, float scale,
+                          void* workspace, size_t workspace_bytes,
+                          int* d_err, void* stream);
+
+/* paged_gqa_decode_int8 with tuning options: compute must be
+ * PKV_COMPUTE_TENSOR, schedule 0; (warps_per_cta, stages) one of (16, 4)
+ * (the default), (16, 2) or (8, 4); other fields as paged_gqa_decode_ex. */
+int paged_gqa_decode_int8_ex(const void* q, const void* kv_codes, const float* kv_scales,
+                             int num_pages, const int32_t* block_tables, int bt_row_stride,
+                             int max_blocks, const int32_t* seq_lens, int num_seqs,
+                             int max_seq_len, void* out, float scale,
+                             void* workspace, size_t workspace_bytes,
+                             int* d_err, void* stream, const pkv_decode_opts* opts);
+
+/* ------------------------------------------------------------------------
  * paged_gqa_prefill - causal GQA attention of each sequence's newest tokens
  * over its own pages: a whole prompt, or a chunk of one after a cached
  * prefix ("Gestion de la KV cache et strategies de batching": attention

@@ -76,6 +76,11 @@ _SIGS = {
     "paged_gqa_decode_append": (_i, [_p, _p, _p, _p, _p, _i, _p, _i, _p, _i, _i, _p, _i, _i, _p, _p,
                                      _f, _p, _sz, _p, _p, ctypes.POINTER(DecodeOpts)]),
     "paged_gqa_decode_noalloc": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _p]),
+    "kv_append_rope_int8": (_i, [_p, _p, _p, _p, _i, _p, _i, _i, _i, _p, _p, _i, _p, _p, _i, _p, _p,
+                                 _p, _p]),
+    "paged_gqa_decode_int8": (_i, [_p, _p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p, _p]),
+    "paged_gqa_decode_int8_ex": (_i, [_p, _p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p,
+                                      _p, ctypes.POINTER(DecodeOpts)]),
     "pkv_read_device_error": (_i, [_p, _p, _i, _ip]),
     "pkv_credit_pages": (_i, [_i, _i, _i]),
     "pkv_sched_create": (_p, [_i, _i, _i, _i]),
@@ -288,6 +293,105 @@ def paged_gqa_decode(q, kv_pool, block_tables, seq_lens, out, scale, workspace=N
                           schedule, early_kv)
         st = _L().paged_gqa_decode_ex(*args, ctypes.byref(opts))
     _check(st, "paged_gqa_decode")
+
+
+# --------------------------------------------------------------- INT8 pages --
+
+def new_int8_pools(num_pages: int, device):
+    """(codes int8 [N, 2, 8, 16, 64], scales float32 [N, 2, 8, 16]), zero-filled."""
+    codes = torch.zeros((num_pages, 2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM), dtype=torch.int8,
+                        device=device)
+    scales = torch.zeros((num_pages, 2, NUM_KV_HEADS, PAGE_TOKENS), dtype=torch.float32,
+                         device=device)
+    return codes, scales
+
+
+def kv_append_rope_int8(k, v, positions, block_tables, kv_codes, kv_scales, rope_cos, rope_sin,
+                        token_seq=None, q_in=None, q_out=None, d_err=None, max_blocks=None,
+                        stream=None):
+    """kv_append_rope into INT8 pages: each (token, head) row of the rotated K
+    and of V is stored as 64 int8 codes and one fp32 scale."""
+    dev = kv_codes.device
+    _need(kv_codes, "kv_codes", torch.int8, dev, (2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM))
+    _need(kv_scales, "kv_scales", torch.float32, dev, (2, NUM_KV_HEADS, PAGE_TOKENS))
+    if kv_scales.shape[0] != kv_codes.shape[0]:
+        raise ValueError("kv_scales must have one row of scales per page of kv_codes")
+    _need(k, "k", torch.bfloat16, dev, (NUM_KV_HEADS, HEAD_DIM))
+    _need(v, "v", torch.bfloat16, dev, (NUM_KV_HEADS, HEAD_DIM))
+    T = k.numel() // (NUM_KV_HEADS * HEAD_DIM)
+    if v.numel() != k.numel():
+        raise ValueError("k and v must have the same shape")
+    _need(positions, "positions", torch.int32, dev)
+    if positions.numel() != T:
+        raise ValueError("positions must have one entry per token")
+    if token_seq is not None:
+        _need(token_seq, "token_seq", torch.int32, dev)
+        if token_seq.numel() != T:
+            raise ValueError("token_seq must have one entry per token")
+    _need(block_tables, "block_tables", torch.int32, dev)
+    if block_tables.dim() != 2:
+        raise ValueError("block_tables must be [num_seqs, row_stride]")
+    _need(rope_cos, "rope_cos", torch.float32, dev, (ROPE_PAIRS,))
+    _need(rope_sin, "rope_sin", torch.float32, dev, (ROPE_PAIRS,))
+    if (q_in is None) != (q_out is None):
+        raise ValueError("q_in and q_out go together")
+    if q_in is not None:
+        _need(q_in, "q_in", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
+        _need(q_out, "q_out", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
+        if q_in.numel() != T * NUM_Q_HEADS * HEAD_DIM or q_out.numel() != q_in.numel():
+            raise ValueError("q_in/q_out must be [T, 32, 64]")
+    if d_err is not None:
+        _need(d_err, "d_err", torch.int32, dev)
+    S, stride = block_tables.shape
+    mb = stride if max_blocks is None else max_blocks
+    st = _L().kv_append_rope_int8(_ptr(k), _ptr(v), _ptr(positions), _ptr(token_seq), T,
+                                 _ptr(block_tables), S, stride, mb, _ptr(kv_codes),
+                                 _ptr(kv_scales), kv_codes.shape[0], _ptr(rope_cos),
+                                 _ptr(rope_sin), rope_cos.shape[0], _ptr(q_in), _ptr(q_out),
+                                 _ptr(d_err), _stream(stream))
+    _check(st, "kv_append_rope_int8")
+
+
+def paged_gqa_decode_int8(q, kv_codes, kv_scales, block_tables, seq_lens, out, scale,
+                          workspace=None, max_seq_len=None, d_err=None, max_blocks=None,
+                          min_units_per_warp=0, ctas_per_sm=0, stages=0, warps_per_cta=0,
+                          stream=None):
+    """paged_gqa_decode over INT8 pages (codes and per-row scales)."""
+    dev = kv_codes.device
+    _need(kv_codes, "kv_codes", torch.int8, dev, (2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM))
+    _need(kv_scales, "kv_scales", torch.float32, dev, (2, NUM_KV_HEADS, PAGE_TOKENS))
+    if kv_scales.shape[0] != kv_codes.shape[0]:
+        raise ValueError("kv_scales must have one row of scales per page of kv_codes")
+    _need(q, "q", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
+    _need(out, "out", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
+    S = q.numel() // (NUM_Q_HEADS * HEAD_DIM)
+    if out.numel() != q.numel():
+        raise ValueError("out must match q")
+    _need(block_tables, "block_tables", torch.int32, dev)
+    if block_tables.dim() != 2 or block_tables.shape[0] < S:
+        raise ValueError("block_tables must be [>= num_seqs, row_stride]")
+    _need(seq_lens, "seq_lens", torch.int32, dev)
+    if seq_lens.numel() != S:
+        raise ValueError("seq_lens must have num_seqs entries")
+    stride = block_tables.shape[1]
+    mb = stride if max_blocks is None else max_blocks
+    if max_seq_len is None:
+        max_seq_len = PAGE_TOKENS * mb
+    if workspace is None:
+        workspace = alloc_workspace(S, dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    if d_err is not None:
+        _need(d_err, "d_err", torch.int32, dev)
+    args = (_ptr(q), _ptr(kv_codes), _ptr(kv_scales), kv_codes.shape[0], _ptr(block_tables),
+            stride, mb, _ptr(seq_lens), S, int(max_seq_len), _ptr(out), float(scale),
+            _ptr(workspace), workspace.numel(), _ptr(d_err), _stream(stream))
+    if not (min_units_per_warp or ctas_per_sm or stages or warps_per_cta):
+        st = _L().paged_gqa_decode_int8(*args)
+    else:
+        opts = DecodeOpts(COMPUTE_TENSOR, min_units_per_warp, ctas_per_sm, stages, warps_per_cta,
+                          0, 0, 0)
+        st = _L().paged_gqa_decode_int8_ex(*args, ctypes.byref(opts))
+    _check(st, "paged_gqa_decode_int8")
 
 
 def paged_gqa_decode_append(q, k_new, v_new, kv_pool, block_tables, seq_lens, out, rope_cos,
@@ -575,6 +679,73 @@ class DecodeStep:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             self._launch(decode_only=True)
+        return g
+
+    def error(self) -> int:
+        """Synchronise and return (and clear) the device error word."""
+        return pkv_read_device_error(self.d_err)
+
+
+class Int8DecodeStep:
+    """One decode step over every layer on INT8 pages, captured into a CUDA graph.
+
+    Per layer l:
+        kv_append_rope_int8(k[l], v[l], positions, block_tables[l], codes, scales,
+                            cos, sin, q_in=q[l], q_out=q_rot[l])
+        paged_gqa_decode_int8(q_rot[l], codes, scales, block_tables[l], seq_lens,
+                              out[l], scale)
+    Tensors are bound at construction (refresh their contents in place and
+    call run()), as for DecodeStep.
+
+        codes   [num_pages, 2, 8, 16, 64] int8;  scales [num_pages, 2, 8, 16] float32
+        block_tables [L, S, max_blocks] int32;  seq_lens, positions [S] int32
+        k, v [L, S, 8, 64] bf16;  q, out [L, S, 32, 64] bf16
+    """
+
+    def __init__(self, codes, scales, block_tables, seq_lens, positions, k, v, q, out, rope_cos,
+                 rope_sin, scale, max_seq_len=None, workspace=None, d_err=None, q_rot=None,
+                 use_graph=True, stream=None):
+        self.L, self.S = block_tables.shape[0], block_tables.shape[1]
+        self.t = dict(codes=codes, scales=scales, bt=block_tables, lens=seq_lens, pos=positions,
+                      k=k, v=v, q=q, out=out, cos=rope_cos, sin=rope_sin)
+        dev = codes.device
+        self.q_rot = torch.empty_like(q) if q_rot is None else q_rot
+        self.workspace = alloc_workspace(self.S, dev) if workspace is None else workspace
+        self.d_err = torch.zeros(1, dtype=torch.int32, device=dev) if d_err is None else d_err
+        self.scale = float(scale)
+        self.max_seq_len = max_seq_len
+        self.launches_per_step = 2 * self.L
+        self._launch()                      # eager run: sets up kernels and descriptors
+        torch.cuda.synchronize(dev)
+        self.graph = None
+        if use_graph:
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph, stream=stream):
+                self._launch()
+
+    def _launch(self, append=True, decode=True):
+        t = self.t
+        for l in range(self.L):
+            if append:
+                kv_append_rope_int8(t["k"][l], t["v"][l], t["pos"], t["bt"][l], t["codes"],
+                                    t["scales"], t["cos"], t["sin"], q_in=t["q"][l],
+                                    q_out=self.q_rot[l], d_err=self.d_err)
+            if decode:
+                paged_gqa_decode_int8(self.q_rot[l], t["codes"], t["scales"], t["bt"][l],
+                                      t["lens"], t["out"][l], self.scale, workspace=self.workspace,
+                                      max_seq_len=self.max_seq_len, d_err=self.d_err)
+
+    def run(self):
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self._launch()
+
+    def partial_graph(self, append: bool, decode: bool):
+        """A graph of only the append calls or only the decode calls (for timing)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self._launch(append=append, decode=decode)
         return g
 
     def error(self) -> int:

@@ -94,6 +94,114 @@ __global__ void __launch_bounds__(256) kv_append_rope_kernel(const AppendParams 
   }
 }
 
+// ---------------------------------------------------------------------------
+// INT8 K/V pages (the "INT8 K/V" storage mode of a request's KV cache in
+// "Lifecycle and Memory Model", section "Per-request / handle-owned memory").
+// Each (token, head) row of K (rotated and rounded to bf16 exactly as above)
+// and of V is quantised on its own: amax = max |x|, scale = amax / 127 and
+// code = round-half-even(x / scale) in [-127, 127], both divisions IEEE fp32;
+// amax == 0 gives scale 0 and zero codes.  Same grid as the bf16 append: one
+// CTA per token, one warp per KV head, lane i holding dims i and i + 32.
+// ---------------------------------------------------------------------------
+struct AppendI8Params {
+  const uint16_t* k;          // [T][8][64] bf16
+  const uint16_t* v;          // [T][8][64] bf16
+  const int32_t* positions;   // [T]
+  const int32_t* token_seq;   // [T] or null
+  const int32_t* block_tables;
+  const float* cos;           // [max_pos][32]
+  const float* sin;
+  const uint16_t* q_in;       // [T][32][64] or null
+  uint16_t* q_out;
+  int8_t* codes;              // [num_pages][2][8][16][64]
+  float* scales;              // [num_pages][2][8][16]
+  int T, num_seqs, bt_stride, max_blocks, num_pages, max_pos;
+  int* d_err;
+};
+
+// Codes of the two values x0 (dim lane) and x1 (dim lane + 32) of a row held
+// across the warp, and the row's scale.
+__device__ __forceinline__ float quantize_pair(float x0, float x1, int8_t& c0, int8_t& c1) {
+  const uint32_t a = max(__float_as_uint(x0) & 0x7FFFFFFFu, __float_as_uint(x1) & 0x7FFFFFFFu);
+  const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, a));  // |x| bits order as |x|
+  const float scale = __fdiv_rn(amax, 127.f);
+  if (amax == 0.f) {
+    c0 = c1 = 0;
+    return 0.f;
+  }
+  c0 = (int8_t)max(-127, min(127, __float2int_rn(__fdiv_rn(x0, scale))));
+  c1 = (int8_t)max(-127, min(127, __float2int_rn(__fdiv_rn(x1, scale))));
+  return scale;
+}
+
+__global__ void __launch_bounds__(256) kv_append_rope_int8_kernel(const AppendI8Params p) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t = blockIdx.x;
+  const int g = threadIdx.x >> 5;  // KV head
+  const int lane = threadIdx.x & 31;
+  const int s = p.token_seq ? __ldg(p.token_seq + t) : t;
+  const int pos = __ldg(p.positions + t);
+  bool ok = s >= 0 && s < p.num_seqs && pos >= 0 && pos < p.max_pos &&
+            (pos / PKV_PAGE_TOKENS) < p.max_blocks;
+  int page = -1;
+  if (ok) {
+    page = __ldg(p.block_tables + (size_t)s * p.bt_stride + pos / PKV_PAGE_TOKENS);
+    ok = page >= 0 && page < p.num_pages;
+  }
+  if (!ok) {
+    if (threadIdx.x == 0) report_error(p.d_err, PKV_ERR_DEVICE_INDEX);
+    if (p.q_out) {
+      for (int hh = 0; hh < 4; ++hh) {
+        uint16_t* qo = p.q_out + ((size_t)t * PKV_NUM_Q_HEADS + g * 4 + hh) * 64;
+        qo[lane] = 0;
+        qo[lane + 32] = 0;
+      }
+    }
+    return;
+  }
+  const int slot = pos % PKV_PAGE_TOKENS;
+  const float c = __ldg(p.cos + (size_t)pos * PKV_ROPE_PAIRS + lane);
+  const float sn = __ldg(p.sin + (size_t)pos * PKV_ROPE_PAIRS + lane);
+  const size_t krow = (((size_t)page * 2 + 0) * PKV_NUM_KV_HEADS + g) * PKV_PAGE_TOKENS + slot;
+  const size_t vrow = (((size_t)page * 2 + 1) * PKV_NUM_KV_HEADS + g) * PKV_PAGE_TOKENS + slot;
+
+  // K: rotate (bf16 result, as in the bf16 cache), quantise, store
+  const uint16_t* kr = p.k + ((size_t)t * PKV_NUM_KV_HEADS + g) * 64;
+  uint16_t r0, r1;
+  rope_pair(kr[lane], kr[lane + 32], c, sn, r0, r1);
+  int8_t k0, k1;
+  const float ks = quantize_pair(__uint_as_float((uint32_t)r0 << 16), __uint_as_float((uint32_t)r1 << 16),
+                                 k0, k1);
+  p.codes[krow * 64 + lane] = k0;
+  p.codes[krow * 64 + lane + 32] = k1;
+
+  // V: quantise the bf16 row
+  const uint16_t* vr = p.v + ((size_t)t * PKV_NUM_KV_HEADS + g) * 64;
+  int8_t v0, v1;
+  const float vs = quantize_pair(__uint_as_float((uint32_t)vr[lane] << 16),
+                                 __uint_as_float((uint32_t)vr[lane + 32] << 16), v0, v1);
+  p.codes[vrow * 64 + lane] = v0;
+  p.codes[vrow * 64 + lane + 32] = v1;
+  if (lane == 0) {
+    p.scales[krow] = ks;
+    p.scales[vrow] = vs;
+  }
+
+  // q: the 4 query heads of this group, rotated as in the bf16 append
+  if (p.q_in) {
+    for (int hh = 0; hh < 4; ++hh) {
+      const size_t row = ((size_t)t * PKV_NUM_Q_HEADS + g * 4 + hh) * 64;
+      const uint16_t* qi = p.q_in + row;
+      uint16_t q0, q1;
+      rope_pair(qi[lane], qi[lane + 32], c, sn, q0, q1);
+      __syncwarp();
+      p.q_out[row + lane] = q0;
+      p.q_out[row + lane + 32] = q1;
+    }
+  }
+}
+
 }  // namespace pkv
 
 using namespace pkv;
@@ -150,4 +258,59 @@ extern "C" int kv_append_rope(const void* k, const void* v, const int32_t* posit
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cuda_status(cudaLaunchKernelEx(&cfg, kv_append_rope_kernel, p), "cudaLaunchKernelEx(append)");
+}
+
+extern "C" int kv_append_rope_int8(const void* k, const void* v, const int32_t* positions,
+                                   const int32_t* token_seq, int T, const int32_t* block_tables,
+                                   int num_seqs, int bt_row_stride, int max_blocks,
+                                   void* kv_codes, float* kv_scales, int num_pages,
+                                   const float* rope_cos, const float* rope_sin, int max_pos,
+                                   const void* q_in, void* q_out, int* d_err, void* stream) {
+  if (T < 0 || num_seqs < 1 || max_blocks < 1 || bt_row_stride < max_blocks || num_pages < 1 ||
+      max_pos < 1)
+    return PKV_ERR_INVALID_ARGUMENT;
+  if (T == 0) return PKV_OK;
+  if (!k || !v || !positions || !block_tables || !kv_codes || !kv_scales || !rope_cos || !rope_sin)
+    return PKV_ERR_INVALID_ARGUMENT;
+  if ((q_in == nullptr) != (q_out == nullptr)) return PKV_ERR_INVALID_ARGUMENT;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(kv_codes) || !aligned16(kv_scales) ||
+      ((reinterpret_cast<uintptr_t>(q_in) | reinterpret_cast<uintptr_t>(q_out)) & 3u))
+    return PKV_ERR_MISALIGNED;
+  if (T > (1 << 30) || (long long)num_pages * PKV_PAGE_ELEMS >= (1ll << 40))
+    return PKV_ERR_UNSUPPORTED_SHAPE;
+  int dev = 0;
+  int rc = bind_stream_device(stream, &dev);
+  if (rc != PKV_OK) return rc;
+
+  AppendI8Params p;
+  p.k = static_cast<const uint16_t*>(k);
+  p.v = static_cast<const uint16_t*>(v);
+  p.positions = positions;
+  p.token_seq = token_seq;
+  p.block_tables = block_tables;
+  p.cos = rope_cos;
+  p.sin = rope_sin;
+  p.q_in = static_cast<const uint16_t*>(q_in);
+  p.q_out = static_cast<uint16_t*>(q_out);
+  p.codes = static_cast<int8_t*>(kv_codes);
+  p.scales = kv_scales;
+  p.T = T;
+  p.num_seqs = num_seqs;
+  p.bt_stride = bt_row_stride;
+  p.max_blocks = max_blocks;
+  p.num_pages = num_pages;
+  p.max_pos = max_pos;
+  p.d_err = d_err;
+
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(T);
+  cfg.blockDim = dim3(256);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kv_append_rope_int8_kernel, p),
+                     "cudaLaunchKernelEx(append int8)");
 }

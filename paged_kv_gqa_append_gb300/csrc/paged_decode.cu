@@ -57,6 +57,7 @@ struct DecodeParams {
   const uint16_t* q;              // [S][32][64] bf16
   const int32_t* block_tables;    // [S][bt_stride]
   const int32_t* seq_lens;        // [S]
+  const float* kv_scales;         // INT8 pages: [num_pages][2][8][16] fp32, else null
   uint16_t* out;                  // [S][32][64] bf16
   int bt_stride, max_blocks, num_pages, num_seqs;
   float sl2;                      // scale * log2(e)
@@ -88,9 +89,10 @@ struct Record {
   float2* ml;
 };
 
-template <int kWarps, int kStages>
+template <int kWarps, int kStages, int kStageB = kStageBytes>
 struct SmemLayout {
-  static constexpr int kTiles = kWarps * kStages * kStageBytes;
+  static_assert(kStages * kStageB >= kRecordBytes, "slot 1 lives in the warp's own stages");
+  static constexpr int kTiles = kWarps * kStages * kStageB;
   static constexpr int kBars = kTiles;                                 // u64 [kWarps][kStages]
   static constexpr int kPid = kBars + kWarps * kStages * 8;            // int [kWarps][kStages]
   static constexpr int kCnt = kPid + kWarps * kStages * 4;             // int [kWarps + 1]
@@ -102,7 +104,7 @@ struct SmemLayout {
   // its range, written after the warp's last page, in its own idle tiles.
   __device__ static Record slot(uint8_t* smem, int warp, int which) {
     uint8_t* base = which == 0 ? smem + kSlots + warp * kRecordBytes
-                               : smem + warp * kStages * kStageBytes;
+                               : smem + warp * kStages * kStageB;
     return Record{reinterpret_cast<float*>(base), reinterpret_cast<float2*>(base + 1024)};
   }
 };
@@ -344,7 +346,20 @@ struct MergeAcc {
 // (8 tiles), K = 16 tokens.  The C layout of S is the A layout of P, so the
 // probabilities never leave registers.
 // ---------------------------------------------------------------------------
-struct MmaState {
+// Stage contents of a bf16 page unit: the K tile then the V tile of one
+// (page, head), one 4-D TMA box with the 128-byte swizzle.
+struct Bf16Pages {
+  static constexpr bool kBf16Pages = true;
+  static constexpr int kStageBytes = pkv::kStageBytes;
+  static constexpr int kVOffset = kTileBytes;
+  __device__ static __forceinline__ void copy(uint32_t dst, const CUtensorMap* map,
+                                              const DecodeParams&, int g, int pid, uint32_t bar) {
+    mbar_arrive_expect_tx(bar, kStageBytes);
+    tma_load_4d(dst, map, 0, 0, g, pid * 2, bar);  // K tile, then V tile
+  }
+};
+
+struct MmaState : Bf16Pages {
   // at most 128 registers per thread: 16 warps of work per SM
   __host__ __device__ static constexpr int min_blocks(int warps) { return warps >= 16 ? 1 : 16 / warps; }
   uint32_t qa[4][2];  // Q A-fragments per 16-dim chunk: (row gq, k 2tig..) and (k 8+2tig..)
@@ -519,7 +534,7 @@ struct MmaState {
 // [16 qd, 16 qd + 16).  Scores are reduced over the 4 lanes of a quad; the
 // output accumulates per lane and is reduced over t8 once per segment.
 // ---------------------------------------------------------------------------
-struct FmaState {
+struct FmaState : Bf16Pages {
   __host__ __device__ static constexpr int min_blocks(int) { return 1; }
   float qf[4][16];
   float o[4][16];
@@ -675,6 +690,273 @@ struct FmaState {
 };
 
 // ---------------------------------------------------------------------------
+// INT8 pages (kv_append_rope_int8).  Per unit, the K and V code tiles of one
+// (page, head) -- 16 rows of 64 bytes each -- land by one 4-D TMA box with the
+// 64-byte swizzle (byte b of row r at r*64 + (((b/16) ^ (r/2)) % 4)*16 + b%16)
+// and the 16 K and 16 V scales by two 64-byte bulk copies behind them.
+//
+// Codes enter fp16 m16n8k16 MMAs (fp32 accumulation) exactly: with u = code +
+// 128 in a byte, the fp16 with bits 0x64uu is 1024 + u, and subtracting 1152
+// leaves the code (one byte permute makes two such fp16, one f16x2
+// subtraction finishes them).  fp16 operands need ranges kept in check:
+//   * q is multiplied by a power of two per segment so that its largest
+//     |value| lies in [2^14, 2^15) (exact: a bf16 value times a power of two
+//     fits fp16's 11 significant bits), and the score scale divided by it;
+//   * the V scale of token j multiplies its probability, and the product is
+//     divided by 2^E, E the exponent of the largest V scale of the page, so
+//     P' = p_j s_j 2^-E < 2 before its rounding to fp16; O is kept in units
+//     of 2^E of the latest page and rescaled with the softmax factor when E
+//     changes.
+// Scores: x_j = (q' . code_j) s_K,j scale log2(e) / 2^e_q, online softmax in
+// base 2 as for bf16 pages; the denominator sums the fp32 probabilities.
+//
+// Lane (g8 = lane/4, c = lane%4).  A page's 16 tokens are dealt out as
+// T(c, i) = ((c ^ i) & 1) + 2 (i & 1) + 4 (c >> 1) + 8 (i >> 1), i = 0..3:
+// column j of S tile 0 is token T(j/2, j%2) and of S tile 1 token
+// T(j/2, 2 + j%2), so lane (g8, c) holds the scores -- and the P V
+// A-fragment -- of tokens T(c, 0..3).  The MMA k indices {2c, 2c+1, 2c+8,
+// 2c+9} of step kt are dims 16c + 4kt + {0, 1, 2, 3} (q's dims permuted the
+// same way, which leaves q.k unchanged), so a lane's B fragments of a K row
+// are bytes 16c .. 16c+15 of it.  Column g8 of P V tile nb is dim 8 g8 + nb:
+// a lane reads bytes 8 g8 .. 8 g8 + 7 of the V rows of its four tokens, and
+// its O fragment of tile nb holds dims 16c + nb and 16c + 8 + nb.  With the
+// 64-byte swizzle every shared-memory load of a page is conflict-free: each
+// quarter-warp's 16-byte K loads cover two rows of opposite parity, and each
+// half-warp's 8-byte V loads cover four rows whose 32-byte pieces fall on
+// distinct banks.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int i8_token(int c, int i) {
+  return ((c ^ i) & 1) + 2 * (i & 1) + 4 * (c >> 1) + 8 * (i >> 1);
+}
+// Offset of byte b (a multiple of 8) of row r of a 16 x 64-byte tile stored
+// with the 64-byte swizzle (the tile starts on a 512-byte boundary).
+__device__ __forceinline__ uint32_t sw64(int r, int b) {
+  return (uint32_t)(r * 64 + ((((b >> 4) ^ (r >> 1)) & 3) << 4) + (b & 15));
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float lds32f(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+// f16x2 (h - 1152, h - 1152): exact for the 1024 + (code + 128) values here.
+__device__ __forceinline__ uint32_t hsub1152(uint32_t h) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+  return r;
+}
+// D(16x8, fp32) += A(16x16, fp16, row) * B(16x8, fp16, col); rows 8..15 of A
+// and C are zero, as in mma_bf16_16816.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0,
+                                              uint32_t b1) {
+  float t[4] = {d[0], d[1], 0.f, 0.f};
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(t[0]), "+f"(t[1]), "+f"(t[2]), "+f"(t[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+  d[0] = t[0];
+  d[1] = t[1];
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// 2^k as a float for a biased exponent k clamped to the normal range.
+__device__ __forceinline__ float pow2_biased(int k) {
+  return __int_as_float(min(max(k, 1), 254) << 23);
+}
+
+struct MmaI8State {
+  static constexpr bool kBf16Pages = false;
+  static constexpr int kCodeTile = 1024;                 // 16 x 64 int8
+  static constexpr int kStageBytes = 2560;               // K, V code tiles, 2 x 64 B scales; 512-aligned
+  static constexpr int kVOffset = kCodeTile;
+  static constexpr int kScaleOffset = 2 * kCodeTile;
+  __host__ __device__ static constexpr int min_blocks(int warps) { return warps >= 16 ? 1 : 16 / warps; }
+  uint32_t qa[4][2];  // q' A-fragments (fp16) per MMA step, dims permuted as above
+  float o[8][2];      // O in units of 2^(ev - 127): tile nb holds dims 16c + nb, 16c + 8 + nb
+  float m, l;         // running max (log2 units) and per-lane partial denominator
+  float sl2q;         // scale * log2(e) / (q's power-of-two factor)
+  int ev;             // biased exponent of O's unit
+
+  __device__ static __forceinline__ void copy(uint32_t dst, const CUtensorMap* map,
+                                              const DecodeParams& p, int g, int pid, uint32_t bar) {
+    mbar_arrive_expect_tx(bar, 2 * kCodeTile + 128);
+    tma_load_4d(dst, map, 0, 0, g, pid * 2, bar);  // K codes, then V codes
+    const float* sc = p.kv_scales + ((size_t)pid * 2 * PKV_NUM_KV_HEADS + g) * PKV_PAGE_TOKENS;
+    bulk_load(dst + kScaleOffset, sc, 64, bar);
+    bulk_load(dst + kScaleOffset + 64, sc + PKV_NUM_KV_HEADS * PKV_PAGE_TOKENS, 64, bar);
+  }
+
+  template <bool kAppend>
+  __device__ __forceinline__ void load_q(const DecodeParams& p, int s, int g, int, bool, int lane) {
+    const int gq = lane >> 2, c = lane & 3;
+    uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    if (gq < 4) {  // words 8c .. 8c+7 of the row: dims 16c .. 16c+15
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + gq) * 64 + 16 * c);
+      const uint4 a = __ldg(src), b = __ldg(src + 1);
+      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+      w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    }
+    // largest |q| of the group (4 heads) -> factor 2^(14 - e), 2^e <= max < 2^(e+1)
+    uint32_t amax = 0u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) amax = max(amax, max((w[k] << 16) & 0x7FFFFFFFu, w[k] & 0x7FFF0000u));
+    amax = __reduce_max_sync(0xffffffffu, amax);
+    // biased exponent of the largest |q|, clamped so that both factors stay normal
+    const int eb = min(max((int)(amax >> 23), 15), 267);
+    const float f = amax ? pow2_biased(268 - eb) : 1.f;
+    sl2q = p.sl2 * (amax ? pow2_biased(eb - 14) : 1.f);
+#pragma unroll
+    for (int kt = 0; kt < 4; ++kt) {
+      qa[kt][0] = pack_f16x2(bf16lo_to_f32(w[2 * kt]) * f, bf16hi_to_f32(w[2 * kt]) * f);
+      qa[kt][1] = pack_f16x2(bf16lo_to_f32(w[2 * kt + 1]) * f, bf16hi_to_f32(w[2 * kt + 1]) * f);
+    }
+  }
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int n = 0; n < 8; ++n) o[n][0] = o[n][1] = 0.f;
+    m = -INFINITY;
+    l = 0.f;
+    ev = 127;
+  }
+
+  __device__ __forceinline__ void page(uint32_t sK, uint32_t sV, int valid, float, int lane) {
+    const int g8 = lane >> 2, c = lane & 3;
+    const uint32_t sSc = sK + kScaleOffset;  // K scales [16], V scales [16]
+    // ---- S = q' K^T ------------------------------------------------------
+    const int ra = i8_token(g8 >> 1, g8 & 1), rb = i8_token(g8 >> 1, 2 + (g8 & 1));
+    const uint4 ka = lds128(sK + sw64(ra, 16 * c)), kb = lds128(sK + sw64(rb, 16 * c));
+    const uint32_t kaw[4] = {ka.x, ka.y, ka.z, ka.w}, kbw[4] = {kb.x, kb.y, kb.z, kb.w};
+    float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
+#pragma unroll
+    for (int kt = 0; kt < 4; ++kt) {
+      const uint32_t ua = kaw[kt] ^ 0x80808080u, ub = kbw[kt] ^ 0x80808080u;
+      mma_f16_16816(s0, qa[kt][0], qa[kt][1], hsub1152(__byte_perm(ua, 0x64646464u, 0x7150)),
+                    hsub1152(__byte_perm(ua, 0x64646464u, 0x7352)));
+      mma_f16_16816(s1, qa[kt][0], qa[kt][1], hsub1152(__byte_perm(ub, 0x64646464u, 0x7150)),
+                    hsub1152(__byte_perm(ub, 0x64646464u, 0x7352)));
+    }
+    // ---- online softmax (base 2) over tokens T(c, 0..3) ---------------------
+    int tk[4];
+    float x[4], sv[4];
+    const float sraw[4] = {s0[0], s0[1], s1[0], s1[1]};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      tk[i] = i8_token(c, i);
+      x[i] = sraw[i] * (lds32f(sSc + 4 * tk[i]) * sl2q);
+      sv[i] = lds32f(sSc + 64 + 4 * tk[i]);
+    }
+    if (valid < PKV_PAGE_TOKENS) {  // tokens past the end: no score, and their scales may hold any bits
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[i] = tk[i] < valid ? x[i] : -INFINITY;
+        sv[i] = tk[i] < valid ? sv[i] : 0.f;
+      }
+    }
+    float pm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    float vm = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
+    vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 1));
+    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
+    vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 2));
+    const float mn = fmaxf(m, pm);
+    const int evn = vm > 0.f ? (__float_as_int(vm) >> 23) : ev;  // O's unit from this page on
+    const float a_soft = (m == mn) ? 1.f : exp2f(m - mn);
+    const float alpha = a_soft * pow2_biased(127 + ev - evn);
+    const float vinv = pow2_biased(254 - evn);  // 2^-(evn - 127)
+    float pr[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pr[i] = (x[i] == mn) ? 1.f : exp2f(x[i] - mn);
+    l = l * a_soft + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+    m = mn;
+    ev = evn;
+    const uint32_t pa0 = pack_f16x2(pr[0] * (sv[0] * vinv), pr[1] * (sv[1] * vinv));  // P'[g8][2c, 2c+1]
+    const uint32_t pa2 = pack_f16x2(pr[2] * (sv[2] * vinv), pr[3] * (sv[3] * vinv));  // P'[g8][2c+8, 2c+9]
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+      o[n][0] *= alpha;
+      o[n][1] *= alpha;
+    }
+    // ---- O += P' V ---------------------------------------------------------
+    uint32_t vw[4][2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint2 t = lds64(sV + sw64(tk[i], 8 * g8));
+      vw[i][0] = t.x ^ 0x80808080u;
+      vw[i][1] = t.y ^ 0x80808080u;
+    }
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      // rows (0, 1) and (2, 3) interleaved per dim: [r0.b, r1.b, r0.b', r1.b']
+      const uint32_t t01[2] = {__byte_perm(vw[0][w], vw[1][w], 0x5140), __byte_perm(vw[0][w], vw[1][w], 0x7362)};
+      const uint32_t t23[2] = {__byte_perm(vw[2][w], vw[3][w], 0x5140), __byte_perm(vw[2][w], vw[3][w], 0x7362)};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t sel = (k & 1) ? 0x4342u : 0x4140u;
+        mma_f16_16816(o[4 * w + k], pa0, pa2, hsub1152(__byte_perm(t01[k >> 1], 0x64646464u, sel)),
+                      hsub1152(__byte_perm(t23[k >> 1], 0x64646464u, sel)));
+      }
+    }
+  }
+
+  __device__ __forceinline__ float total_l() const {
+    float lt = l;
+    lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+    return lt;
+  }
+
+  __device__ __forceinline__ void write_record(const Record& r, bool bad, int lane) {
+    const int gq = lane >> 2, c = lane & 3;
+    const float lt = total_l();
+    if (gq < 4) {
+      const float u = pow2_biased(ev);  // O's unit
+      float4* dst = reinterpret_cast<float4*>(r.o + gq * 64 + 16 * c);
+      dst[0] = make_float4(o[0][0] * u, o[1][0] * u, o[2][0] * u, o[3][0] * u);
+      dst[1] = make_float4(o[4][0] * u, o[5][0] * u, o[6][0] * u, o[7][0] * u);
+      dst[2] = make_float4(o[0][1] * u, o[1][1] * u, o[2][1] * u, o[3][1] * u);
+      dst[3] = make_float4(o[4][1] * u, o[5][1] * u, o[6][1] * u, o[7][1] * u);
+      if (c == 0) r.ml[gq] = make_float2(m, bad ? -1.f : lt);
+    }
+  }
+
+  __device__ __forceinline__ void write_output(const DecodeParams& p, int s, int g, bool bad,
+                                               int lane) {
+    const int gq = lane >> 2, c = lane & 3;
+    const float lt = total_l();
+    if (gq < 4) {
+      const bool ok = !bad && lt > 0.f;
+      const float u = pow2_biased(ev);
+      float v[2][8];
+#pragma unroll
+      for (int nb = 0; nb < 8; ++nb) {
+        v[0][nb] = ok ? __fdiv_rn(o[nb][0] * u, lt) : 0.f;
+        v[1][nb] = ok ? __fdiv_rn(o[nb][1] * u, lt) : 0.f;
+      }
+      uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + gq) * 64 + 16 * c);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        dst[h] = make_uint4(pack_bf16x2(v[h][0], v[h][1]), pack_bf16x2(v[h][2], v[h][3]),
+                            pack_bf16x2(v[h][4], v[h][5]), pack_bf16x2(v[h][6], v[h][7]));
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
 // Fused append: the warp that owns a sequence's last page writes the new
 // token's rotated K row and its V row into the staged tiles (so its own
 // attention sees them) and into the pool.  Lane l rotates the pair
@@ -766,7 +1048,9 @@ __device__ __forceinline__ void cross_cta_merge(const DecodeParams& p, const Mer
 template <class State, int kWarps, int kStages, bool kAppend>
 __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
-  using Smem = SmemLayout<kWarps, kStages>;
+  static_assert(!kAppend || State::kBf16Pages, "the fused append writes bf16 pages");
+  constexpr int kStageB = State::kStageBytes;
+  using Smem = SmemLayout<kWarps, kStages, kStageB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -794,7 +1078,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
   const int n_units = (int)(u1 - u0);
 
   if (n_units > 0) {
-    const uint32_t tiles = smem_u32(smem) + warp * kStages * kStageBytes;
+    const uint32_t tiles = smem_u32(smem) + warp * kStages * kStageB;
     const uint32_t bars = smem_u32(smem + Smem::kBars) + warp * kStages * 8;
     int* my_pid = spid + warp * kStages;
     if (lane == 0) {
@@ -820,9 +1104,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
         const uint32_t bar = bars + 8 * stage;
         if (pid >= 0) {
           fence_proxy_async_smem();
-          mbar_arrive_expect_tx(bar, kStageBytes);
-          const uint32_t dst = tiles + stage * kStageBytes;
-          tma_load_4d(dst, &tmap, 0, 0, ci.g, pid * 2, bar);  // K tile, then V tile
+          State::copy(tiles + stage * kStageB, &tmap, p, ci.g, pid, bar);
         } else {
           mbar_arrive(bar);  // keep the phase sequence of this stage intact
         }
@@ -922,12 +1204,12 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
         seg_bad = true;
       } else if (pid >= 0) {
         const int valid = min(PKV_PAGE_TOKENS, seg_len - PKV_PAGE_TOKENS * cc.j);
-        const uint32_t sK = tiles + stage * kStageBytes;
+        const uint32_t sK = tiles + stage * kStageB;
         if (kAppend && cc.j == cc.np - 1) {  // the page that receives the new token
           tok.insert(p, sK, sK + kTileBytes, pid, cc.g, (seg_len - 1) % PKV_PAGE_TOKENS, lane);
           __syncwarp();
         }
-        st.page(sK, sK + kTileBytes, valid, p.sl2, lane);
+        st.page(sK, sK + State::kVOffset, valid, p.sl2, lane);
       } else {
         seg_bad = true;
         if (lane == 0) report_error(p.d_err, PKV_ERR_DEVICE_INDEX);
@@ -1556,7 +1838,7 @@ static long long whole_segment_grid(long long nc, int num_seqs, long long pages_
 template <class State, int kWarps, int kStages, bool kAppend = false>
 static int launch_decode(const DecodeParams& prm, const CUtensorMap& map, int device, int num_sms,
                          int max_seq_len, int min_units, int ctas_per_sm, cudaStream_t stream) {
-  const size_t smem = SmemLayout<kWarps, kStages>::bytes(prm.num_seqs);
+  const size_t smem = SmemLayout<kWarps, kStages, State::kStageBytes>::bytes(prm.num_seqs);
   int occ = 0;
   int rc = setup_kernel<State, kWarps, kStages, kAppend>(device, smem, &occ);
   if (rc != PKV_OK) return rc;
@@ -1673,7 +1955,8 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
                         const int32_t* block_tables, int bt_row_stride, int max_blocks,
                         const int32_t* seq_lens, int num_seqs, int max_seq_len, void* out,
                         float scale, void* workspace, size_t workspace_bytes, int* d_err,
-                        void* stream, const pkv_decode_opts* opts, const AppendArgs* app) {
+                        void* stream, const pkv_decode_opts* opts, const AppendArgs* app,
+                        const float* kv_scales = nullptr) {
   if (num_seqs < 0 || num_pages < 1 || max_blocks < 1 || bt_row_stride < max_blocks)
     return PKV_ERR_INVALID_ARGUMENT;
   if (num_seqs == 0) return PKV_OK;
@@ -1681,6 +1964,7 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
     return PKV_ERR_INVALID_ARGUMENT;
   if (!isfinite(scale)) return PKV_ERR_INVALID_ARGUMENT;
   if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out) || !aligned16(workspace) ||
+      !aligned16(kv_scales) ||
       (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
     return PKV_ERR_MISALIGNED;
   if (app) {
@@ -1701,8 +1985,14 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   if (compute != PKV_COMPUTE_TENSOR && compute != PKV_COMPUTE_FMA) return PKV_ERR_INVALID_ARGUMENT;
   if (app && compute != PKV_COMPUTE_TENSOR) return PKV_ERR_INVALID_ARGUMENT;
   const int cfg = warps * 100 + stages;
-  if (compute == PKV_COMPUTE_TENSOR && cfg != 1602 && cfg != 1603 && cfg != 802 && cfg != 804 &&
-      cfg != 402 && cfg != 404)
+  // INT8 pages: static schedule, tensor cores, 4 stages by default
+  const bool int8 = kv_scales != nullptr;
+  const int cfg8 = warps * 100 + ((opts && opts->stages > 0) ? opts->stages : 4);
+  if (int8 && (app || compute != PKV_COMPUTE_TENSOR || (opts && opts->schedule == 1) ||
+               (cfg8 != 1604 && cfg8 != 1602 && cfg8 != 804)))
+    return PKV_ERR_INVALID_ARGUMENT;
+  if (!int8 && compute == PKV_COMPUTE_TENSOR && cfg != 1602 && cfg != 1603 && cfg != 802 &&
+      cfg != 804 && cfg != 402 && cfg != 404)
     return PKV_ERR_INVALID_ARGUMENT;
   if (app && cfg != 1602 && cfg != 802 && cfg != 402) return PKV_ERR_INVALID_ARGUMENT;
 
@@ -1715,7 +2005,7 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   if (workspace_bytes < wl.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
 
   CUtensorMap map;
-  rc = make_pool_map(&map, kv_pool, num_pages);
+  rc = int8 ? make_pool_map_i8(&map, kv_pool, num_pages) : make_pool_map(&map, kv_pool, num_pages);
   if (rc != PKV_OK) return rc;
 
   DecodeParams prm;
@@ -1723,6 +2013,7 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   prm.q = static_cast<const uint16_t*>(q);
   prm.block_tables = block_tables;
   prm.seq_lens = seq_lens;
+  prm.kv_scales = kv_scales;
   prm.out = static_cast<uint16_t*>(out);
   prm.bt_stride = bt_row_stride;
   prm.max_blocks = max_blocks;
@@ -1749,6 +2040,13 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int ms = max_seq_len;
+  if (int8) {
+    switch (cfg8) {
+      case 1602: return launch_decode<MmaI8State, 16, 2>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
+      case 804: return launch_decode<MmaI8State, 8, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
+      default: return launch_decode<MmaI8State, 16, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
+    }
+  }
   const int schedule = opts ? opts->schedule : 0;
   if (schedule == 1 && compute == PKV_COMPUTE_TENSOR) {
     const int rc2 = app ? launch_decode_dyn<true>(prm, map, dev, sms, ms, min_units, st)
@@ -1808,4 +2106,26 @@ extern "C" int paged_gqa_decode(const void* q, const void* kv_pool, int num_page
   return paged_gqa_decode_ex(q, kv_pool, num_pages, block_tables, bt_row_stride, max_blocks,
                              seq_lens, num_seqs, max_seq_len, out, scale, workspace,
                              workspace_bytes, d_err, stream, nullptr);
+}
+
+extern "C" int paged_gqa_decode_int8_ex(const void* q, const void* kv_codes, const float* kv_scales,
+                                        int num_pages, const int32_t* block_tables,
+                                        int bt_row_stride, int max_blocks, const int32_t* seq_lens,
+                                        int num_seqs, int max_seq_len, void* out, float scale,
+                                        void* workspace, size_t workspace_bytes, int* d_err,
+                                        void* stream, const pkv_decode_opts* opts) {
+  if (kv_scales == nullptr && num_seqs > 0) return PKV_ERR_INVALID_ARGUMENT;
+  return decode_entry(q, kv_codes, num_pages, block_tables, bt_row_stride, max_blocks, seq_lens,
+                      num_seqs, max_seq_len, out, scale, workspace, workspace_bytes, d_err, stream,
+                      opts, nullptr, kv_scales);
+}
+
+extern "C" int paged_gqa_decode_int8(const void* q, const void* kv_codes, const float* kv_scales,
+                                     int num_pages, const int32_t* block_tables, int bt_row_stride,
+                                     int max_blocks, const int32_t* seq_lens, int num_seqs,
+                                     int max_seq_len, void* out, float scale, void* workspace,
+                                     size_t workspace_bytes, int* d_err, void* stream) {
+  return paged_gqa_decode_int8_ex(q, kv_codes, kv_scales, num_pages, block_tables, bt_row_stride,
+                                  max_blocks, seq_lens, num_seqs, max_seq_len, out, scale,
+                                  workspace, workspace_bytes, d_err, stream, nullptr);
 }

@@ -1,4 +1,5 @@
-// The pool's TMA tensor maps, shared by the decode and prefill kernels.
+// The pools' TMA tensor maps (bf16 pages for decode and prefill, INT8 code
+// pages for decode).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <mutex>
@@ -37,9 +38,10 @@ struct MapCache {
   CUtensorMap map;
 };
 
-static int encode_bf16_4d(MapCache& cache, CUtensorMap* map, const void* base, long long extent,
-                          const cuuint64_t (&dims)[4], const cuuint64_t (&strides)[3],
-                          const cuuint32_t (&box)[4]) {
+static int encode_4d(MapCache& cache, CUtensorMap* map, const void* base, long long extent,
+                     const cuuint64_t (&dims)[4], const cuuint64_t (&strides)[3],
+                     const cuuint32_t (&box)[4], CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   if (cache.ptr == base && cache.extent == extent) {
     *map = cache.map;
     return PKV_OK;
@@ -50,8 +52,8 @@ static int encode_bf16_4d(MapCache& cache, CUtensorMap* map, const void* base, l
     return PKV_ERR_CUDA;
   }
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(map, dtype, 4, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char msg[64];
@@ -74,7 +76,7 @@ int make_pool_map(CUtensorMap* map, const void* pool, int num_pages) {
   const cuuint64_t dims[4] = {64, 16, PKV_NUM_KV_HEADS, (cuuint64_t)num_pages * 2};
   const cuuint64_t strides[3] = {128, 2048, 2048 * PKV_NUM_KV_HEADS};
   const cuuint32_t box[4] = {64, 16, 1, 2};
-  return encode_bf16_4d(cache, map, pool, num_pages, dims, strides, box);
+  return encode_4d(cache, map, pool, num_pages, dims, strides, box);
 }
 
 // The same view with a one-tile box {64, 16, 1, 1}: the K tile (kv = 0) or
@@ -85,7 +87,19 @@ int make_pool_tile_map(CUtensorMap* map, const void* pool, int num_pages) {
   const cuuint64_t dims[4] = {64, 16, PKV_NUM_KV_HEADS, (cuuint64_t)num_pages * 2};
   const cuuint64_t strides[3] = {128, 2048, 2048 * PKV_NUM_KV_HEADS};
   const cuuint32_t box[4] = {64, 16, 1, 1};
-  return encode_bf16_4d(cache, map, pool, num_pages, dims, strides, box);
+  return encode_4d(cache, map, pool, num_pages, dims, strides, box);
+}
+
+// INT8 code pool [num_pages][2][8][16][64] viewed as (byte 64, slot 16,
+// head 8, page * 2 + kv); one box {64, 16, 1, 2} = the K and V code tiles of
+// one (page, head), 2 x 1 KiB, with the 64-byte swizzle (rows are 64 bytes).
+int make_pool_map_i8(CUtensorMap* map, const void* codes, int num_pages) {
+  static thread_local MapCache cache;
+  const cuuint64_t dims[4] = {64, 16, PKV_NUM_KV_HEADS, (cuuint64_t)num_pages * 2};
+  const cuuint64_t strides[3] = {64, 1024, 1024 * PKV_NUM_KV_HEADS};
+  const cuuint32_t box[4] = {64, 16, 1, 2};
+  return encode_4d(cache, map, codes, num_pages, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                   CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 }  // namespace pkv

@@ -1,0 +1,343 @@
+"""GPU parity of the INT8 K/V pages: kv_append_rope_int8 and
+paged_gqa_decode_int8 through the C ABI against the FP64 oracle.
+
+The append (codes, scales, rotated q) is compared bit for bit.  Decode outputs
+(bf16) are compared with the oracle's FP64 attention over the dequantised
+pages by the bf16 bar (max |err| <= 1.5e-2, mean |err| <= 1e-3) applied
+beyond the bf16 output format's own rounding (see check_close_int8).  Inputs
+come from workloads.py and the oracle; nothing the CUDA path computes is fed
+to the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import bf16 as OB, int8_kv as OI, rope as OR
+from tests._util import MAX_ABS_TOL, MEAN_ABS_TOL, bf16_to_f64, bits, to_dev_bf16, to_dev_i32
+from tests.test_gpu_parity import edge_case, make_case, rand_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib(cuda_device):
+    from paged_kv_gqa_append_gb300 import build
+    build.build()
+    import paged_kv_gqa_append_gb300 as m
+    return m
+
+
+@pytest.fixture(scope="module")
+def tables(lib, cuda_device):
+    cos_d, sin_d = lib.rope_tables_device(cuda_device, 2048)
+    cos_o, sin_o = OR.table(OR.inv_freq_llama3(), 2048)
+    return cos_d, sin_d, cos_o, sin_o
+
+
+def check_close_int8(gpu, ref, what=""):
+    """The bf16 bar applied to the error beyond the output format's own
+    rounding: max |err| <= 1.5e-2 + 2^-8 |ref| where |ref| >= 4 (a bf16 half
+    step there exceeds 1.5e-2), and mean |err| <= 1e-3 + the mean distance of
+    the FP64 values to their nearest bf16 (the dequantised values, unlike bf16
+    pages, are not bf16 numbers, so an output dominated by one token carries
+    the full rounding of the bf16 result)."""
+    gpu = gpu.astype(np.float64)
+    err = np.abs(gpu - ref)
+    assert np.all(np.isfinite(gpu)), f"{what}: non-finite GPU output"
+    allowed = MAX_ABS_TOL + np.where(np.abs(ref) >= 4.0, 2.0 ** -8 * np.abs(ref), 0.0)
+    worst = int(np.argmax(err - allowed))
+    assert np.all(err <= allowed), f"{what}: |err| {err.flat[worst]:.3e} at |ref| {abs(ref.flat[worst]):.3f}"
+    rounding = np.abs(ref - OB.to_f64(OB.from_f64_via_f32(ref))).mean()
+    assert err.mean() <= MEAN_ABS_TOL + rounding, \
+        f"{what}: mean |err| {err.mean():.3e} (output rounding alone {rounding:.3e})"
+    return float(err.max()), float(err.mean())
+
+
+def dev_pools(codes, scales, dev):
+    return (torch.from_numpy(np.ascontiguousarray(codes)).to(dev),
+            torch.from_numpy(np.ascontiguousarray(scales)).to(dev))
+
+
+def run_decode8(lib, dev, q_bits, codes, scales, bt, lens, scale=0.125, **kw):
+    q = to_dev_bf16(q_bits, dev)
+    c, s = dev_pools(codes, scales, dev)
+    out = torch.empty_like(q)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lib.paged_gqa_decode_int8(q, c, s, to_dev_i32(bt, dev), to_dev_i32(lens, dev), out, scale,
+                              d_err=err, **kw)
+    return out, lib.pkv_read_device_error(err)
+
+
+def f32_bits(a):
+    return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+
+
+# ---------------------------------------------------------------- append ----
+
+def test_int8_append_bit_exact(lib, cuda_device, tables):
+    """40 tokens of 3 sequences at shuffled positions, q rotated in the same call."""
+    cos_d, sin_d, cos_o, sin_o = tables
+    dev = cuda_device
+    rng = np.random.default_rng(40)
+    S, N, T = 3, 12, 40
+    codes0, scales0 = OI.new_pools(N, code_fill=-128, scale_fill=-1.0)
+    perm = rng.permutation(N)
+    bt = np.full((S, 8), -1, np.int32)
+    bt[0, :3], bt[1, :2], bt[2, :4] = perm[:3], perm[3:5], perm[5:9]
+    caps = [48, 32, 64]
+    pairs = set()
+    while len(pairs) < T:
+        s = int(rng.integers(0, S))
+        pairs.add((s, int(rng.integers(0, caps[s]))))
+    pairs = sorted(pairs, key=lambda _: rng.random())
+    seqs = np.array([p[0] for p in pairs], np.int32)
+    pos = np.array([p[1] for p in pairs], np.int32)
+    k, v, q = rand_bits(4000, (T, 8, 64)), rand_bits(4001, (T, 8, 64)), rand_bits(4002, (T, 32, 64))
+    c_d, s_d = dev_pools(codes0, scales0, dev)
+    q_out = torch.empty((T, 32, 64), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lib.kv_append_rope_int8(to_dev_bf16(k, dev), to_dev_bf16(v, dev), to_dev_i32(pos, dev),
+                            to_dev_i32(bt, dev), c_d, s_d, cos_d, sin_d, token_seq=to_dev_i32(seqs, dev),
+                            q_in=to_dev_bf16(q, dev), q_out=q_out, d_err=err)
+    assert lib.pkv_read_device_error(err) == 0
+    want_c, want_s, want_q, e = OI.append_rope_int8(codes0, scales0, k, v, pos, seqs, bt, cos_o, sin_o, q)
+    assert not e
+    assert np.array_equal(c_d.cpu().numpy(), want_c)
+    assert np.array_equal(f32_bits(s_d.cpu().numpy()), f32_bits(want_s))
+    assert np.array_equal(bits(q_out), want_q)
+
+
+def test_int8_append_special_rows(lib, cuda_device, tables):
+    """Position 0 (RoPE is the identity): an integer K row with halves (ties to
+    even), a zero V row (scale 0), a tiny row, and an all-negative row."""
+    cos_d, sin_d, cos_o, sin_o = tables
+    dev = cuda_device
+    k = np.zeros((4, 8, 64), np.float32)
+    v = np.zeros((4, 8, 64), np.float32)
+    k[0, :, 0] = 127.0
+    k[0, :, 1:9] = [2.5, 3.5, -2.5, -3.5, 0.5, 1.5, 126.5, -0.5]
+    k[1] = np.random.default_rng(1).standard_normal((8, 64)) * 2.0 ** -100
+    k[2] = -np.abs(np.random.default_rng(2).standard_normal((8, 64))) - 0.25
+    v[1] = 1.0
+    v[3] = np.random.default_rng(3).standard_normal((8, 64))
+    kb = OB.from_f32_rne(k)
+    vb = OB.from_f32_rne(v)
+    pos = np.array([0, 16, 32, 48], np.int32)      # slot 0 of four pages, position 0 first
+    bt = np.array([[0, 1, 2, 3]], np.int32)
+    codes0, scales0 = OI.new_pools(4, code_fill=5, scale_fill=7.0)
+    c_d, s_d = dev_pools(codes0, scales0, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lib.kv_append_rope_int8(to_dev_bf16(kb, dev), to_dev_bf16(vb, dev), to_dev_i32(pos, dev),
+                            to_dev_i32(bt, dev), c_d, s_d, cos_d, sin_d,
+                            token_seq=to_dev_i32(np.zeros(4, np.int32), dev), d_err=err)
+    assert lib.pkv_read_device_error(err) == 0
+    want_c, want_s, _, e = OI.append_rope_int8(codes0, scales0, kb, vb, pos, np.zeros(4, np.int32),
+                                               bt, cos_o, sin_o)
+    assert not e
+    got_c = c_d.cpu().numpy()
+    assert np.array_equal(got_c, want_c)
+    assert np.array_equal(f32_bits(s_d.cpu().numpy()), f32_bits(want_s))
+    assert list(got_c[0, 0, 0, 0, 1:9]) == [2, 4, -2, -4, 0, 2, 126, 0]
+    assert np.all(got_c[0, 1, :, 0] == 0) and np.all(s_d.cpu().numpy()[0, 1, :, 0] == 0)
+
+
+def test_int8_append_error_contract(lib, cuda_device, tables):
+    cos_d, sin_d, cos_o, sin_o = tables
+    dev = cuda_device
+    codes0, scales0 = OI.new_pools(4, code_fill=7, scale_fill=3.0)
+    bt = np.array([[0, 1], [2, 9]], np.int32)      # page 9 does not exist
+    k, v, q = rand_bits(4010, (4, 8, 64)), rand_bits(4011, (4, 8, 64)), rand_bits(4012, (4, 32, 64))
+    pos, seqs = np.array([3, 20, 0, 40], np.int32), np.array([0, 1, 5, 0], np.int32)
+    c_d, s_d = dev_pools(codes0, scales0, dev)
+    q_out = torch.full((4, 32, 64), 1.0, dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lib.kv_append_rope_int8(to_dev_bf16(k, dev), to_dev_bf16(v, dev), to_dev_i32(pos, dev),
+                            to_dev_i32(bt, dev), c_d, s_d, cos_d[:32], sin_d[:32],
+                            token_seq=to_dev_i32(seqs, dev), q_in=to_dev_bf16(q, dev), q_out=q_out,
+                            d_err=err)
+    assert lib.pkv_read_device_error(err) == lib.ERR_DEVICE_INDEX
+    want_c, want_s, want_q, e = OI.append_rope_int8(codes0, scales0, k, v, pos, seqs, bt,
+                                                    cos_o[:32], sin_o[:32], q)
+    assert e
+    assert np.array_equal(c_d.cpu().numpy(), want_c)
+    assert np.array_equal(f32_bits(s_d.cpu().numpy()), f32_bits(want_s))
+    assert np.array_equal(bits(q_out), want_q)
+
+
+# ---------------------------------------------------------------- decode ----
+
+def edge_case_int8():
+    """The bf16 edge case's lengths and pages, quantised by the oracle, with
+    NaN / +Inf scales in every unused tail slot."""
+    case, _, q = edge_case()
+    codes, scales = OI.quantize_pool(W.bf16_bits(W.fill_pool(case)))
+    st = torch.from_numpy(scales)
+    W.garbage_fill_unused_int8(st, case, 0)
+    return case, codes, st.numpy(), q
+
+
+def test_int8_decode_edge_lengths_and_tail_garbage(lib, cuda_device):
+    case, codes, scales, q = edge_case_int8()
+    bt = case.block_tables[0]
+    out, code = run_decode8(lib, cuda_device, q, codes, scales, bt, case.seq_lens)
+    ref, err = OI.decode_int8(q, codes, scales, bt, case.seq_lens, case.scale)
+    assert code == 0 and not err
+    got = bf16_to_f64(out)
+    check_close_int8(got, ref, "int8 edge lengths")
+    assert np.all(got[8] == 0)                      # seq_len 0 -> zeros
+
+
+def test_int8_decode_permutation_invariant_and_deterministic(lib, cuda_device):
+    case, codes, scales, q = edge_case_int8()
+    bt = case.block_tables[0]
+    out1, _ = run_decode8(lib, cuda_device, q, codes, scales, bt, case.seq_lens)
+    out1b, _ = run_decode8(lib, cuda_device, q, codes, scales, bt, case.seq_lens)
+    assert torch.equal(out1.view(torch.int16), out1b.view(torch.int16))
+    perm = np.random.default_rng(6).permutation(case.num_pages)
+    c2, s2 = np.empty_like(codes), np.empty_like(scales)
+    c2[perm], s2[perm] = codes, scales
+    bt2 = np.where(bt >= 0, perm[np.maximum(bt, 0)], -1).astype(np.int32)
+    out2, _ = run_decode8(lib, cuda_device, q, c2, s2, bt2, case.seq_lens)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_int8_decode_error_contract(lib, cuda_device):
+    case, codes, scales, q = edge_case_int8()
+    bt = case.block_tables[0].copy()
+    good, code = run_decode8(lib, cuda_device, q, codes, scales, bt, case.seq_lens)
+    assert code == 0
+    bad_bt = bt.copy()
+    bad_bt[6, 50] = case.num_pages + 3
+    out, code = run_decode8(lib, cuda_device, q, codes, scales, bad_bt, case.seq_lens)
+    assert code == lib.ERR_DEVICE_INDEX
+    got = bits(out)
+    assert np.all(got[6] == 0)
+    keep = [s for s in range(len(case.seq_lens)) if s != 6]
+    assert np.array_equal(got[keep], bits(good)[keep])
+    lens = case.seq_lens.copy()
+    lens[3], lens[4] = -1, 16 * 128 + 1
+    out, code = run_decode8(lib, cuda_device, q, codes, scales, bt, lens)
+    assert code == lib.ERR_DEVICE_INDEX
+    ref, err = OI.decode_int8(q, codes, scales, bt, lens, case.scale)
+    assert err
+    got = bf16_to_f64(out)
+    assert np.all(got[3] == 0) and np.all(got[4] == 0)
+    check_close_int8(got, ref, "int8 sequences next to invalid lengths")
+
+
+def test_int8_decode_mixed_batch8(lib, cuda_device):
+    case = W.case_mixed()
+    pool = W.bf16_bits(W.fill_pool(case))
+    codes, scales = OI.quantize_pool(pool)
+    q = W.bf16_bits(W.fill_queries(case))[0]
+    bt = case.block_tables[0]
+    out, code = run_decode8(lib, cuda_device, q, codes, scales, bt, case.seq_lens)
+    ref, _ = OI.decode_int8(q, codes, scales, bt, case.seq_lens, case.scale)
+    assert code == 0
+    check_close_int8(bf16_to_f64(out), ref, "int8 mixed batch 8")
+
+
+@pytest.mark.parametrize("opts", [dict(), dict(stages=2), dict(warps_per_cta=8, stages=4),
+                                  dict(min_units_per_warp=1), dict(min_units_per_warp=64),
+                                  dict(ctas_per_sm=1), dict(max_seq_len=2048),
+                                  dict(warps_per_cta=8, stages=4, min_units_per_warp=1)])
+def test_int8_decode_work_split_variants(lib, cuda_device, opts):
+    case = make_case([3, 40, 17, 700, 1, 129, 2048, 16], seed=9, extra_pages=5)
+    pool = W.bf16_bits(W.fill_pool(case))
+    codes, scales = OI.quantize_pool(pool)
+    q = W.bf16_bits(W.fill_queries(case))[0]
+    bt = case.block_tables[0]
+    out, code = run_decode8(lib, cuda_device, q, codes, scales, bt, case.seq_lens, **opts)
+    ref, _ = OI.decode_int8(q, codes, scales, bt, case.seq_lens, case.scale)
+    assert code == 0
+    check_close_int8(bf16_to_f64(out), ref, f"int8 split variant {opts}")
+
+
+def test_int8_append_then_decode_matches_oracle(lib, cuda_device, tables):
+    """Prompt K/V of five sequences appended into INT8 pages (one call), then
+    decoded: the pages equal the oracle's bit for bit and so does nothing else
+    need to (decode within tolerance)."""
+    cos_d, sin_d, cos_o, sin_o = tables
+    dev = cuda_device
+    lens = np.array([1, 16, 33, 200, 517], np.int32)
+    case = make_case(lens, seed=31, extra_pages=3)
+    bt = case.block_tables[0]
+    T = int(lens.sum())
+    seqs = np.repeat(np.arange(len(lens), dtype=np.int32), lens)
+    pos = np.concatenate([np.arange(n, dtype=np.int32) for n in lens])
+    k, v = rand_bits(4020, (T, 8, 64)), rand_bits(4021, (T, 8, 64))
+    q = rand_bits(4022, (len(lens), 32, 64))
+    codes0, scales0 = OI.new_pools(case.num_pages)
+    c_d, s_d = dev_pools(codes0, scales0, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lib.kv_append_rope_int8(to_dev_bf16(k, dev), to_dev_bf16(v, dev), to_dev_i32(pos, dev),
+                            to_dev_i32(bt, dev), c_d, s_d, cos_d, sin_d,
+                            token_seq=to_dev_i32(seqs, dev), d_err=err)
+    want_c, want_s, _, e = OI.append_rope_int8(codes0, scales0, k, v, pos, seqs, bt, cos_o, sin_o)
+    assert not e and lib.pkv_read_device_error(err) == 0
+    assert np.array_equal(c_d.cpu().numpy(), want_c)
+    assert np.array_equal(f32_bits(s_d.cpu().numpy()), f32_bits(want_s))
+    out = torch.empty((len(lens), 32, 64), dtype=torch.bfloat16, device=dev)
+    lib.paged_gqa_decode_int8(to_dev_bf16(q, dev), c_d, s_d, to_dev_i32(bt, dev),
+                              to_dev_i32(lens, dev), out, 0.125, d_err=err)
+    assert lib.pkv_read_device_error(err) == 0
+    ref, _ = OI.decode_int8(q, want_c, want_s, bt, lens, 0.125)
+    check_close_int8(bf16_to_f64(out), ref, "int8 append then decode")
+
+
+# ------------------------------------------------- full-size, sampled -------
+
+def full_size_int8_check(lib, dev, case, samples, tables):
+    """One bench-shaped INT8 step on every layer (append of the new token with q
+    rotation, then decode) and sampled (layer, seq) outputs against the oracle."""
+    cos_d, sin_d, cos_o, sin_o = tables
+    codes, scales = W.fill_pool_int8(case, device=dev)
+    q_raw = W.fill_queries(case, device=dev)
+    k_new, v_new = W.fill_new_kv(case, device=dev)
+    pos = W.new_positions(case)
+    bt_all = to_dev_i32(case.block_tables, dev)
+    lens = to_dev_i32(case.seq_lens, dev)
+    posd = to_dev_i32(pos, dev)
+    pre = {}
+    for (l, s) in samples:
+        ids = case.block_tables[l, s][case.block_tables[l, s] >= 0]
+        idx = torch.from_numpy(ids).to(dev).long()
+        pre[(l, s)] = (ids, codes[idx].cpu().numpy(), scales[idx].cpu().numpy())
+    q_rot = torch.empty_like(q_raw)
+    out = torch.empty_like(q_raw)
+    ws = lib.alloc_workspace(case.num_seqs, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    for l in range(case.num_layers):
+        lib.kv_append_rope_int8(k_new[l], v_new[l], posd, bt_all[l], codes, scales, cos_d, sin_d,
+                                q_in=q_raw[l], q_out=q_rot[l], d_err=err)
+        lib.paged_gqa_decode_int8(q_rot[l], codes, scales, bt_all[l], lens, out[l], case.scale,
+                                  workspace=ws, max_seq_len=case.max_seq_len, d_err=err)
+    assert lib.pkv_read_device_error(err) == 0
+    for (l, s) in samples:
+        ids, c_pages, s_pages = pre[(l, s)]
+        bt_local = np.full((1, 128), -1, np.int32)
+        bt_local[0, :len(ids)] = np.arange(len(ids))
+        kb, vb = bits(k_new[l, s:s + 1]), bits(v_new[l, s:s + 1])
+        qb = bits(q_raw[l, s:s + 1])
+        want_c, want_s, want_q, e = OI.append_rope_int8(c_pages, s_pages, kb, vb, pos[s:s + 1], None,
+                                                        bt_local, cos_o, sin_o, qb)
+        assert not e
+        idx = torch.from_numpy(ids).to(dev).long()
+        assert np.array_equal(codes[idx].cpu().numpy(), want_c), f"codes of layer {l} seq {s}"
+        assert np.array_equal(f32_bits(scales[idx].cpu().numpy()), f32_bits(want_s))
+        assert np.array_equal(bits(q_rot[l, s:s + 1]), want_q)
+        ref, _ = OI.decode_int8(want_q, want_c, want_s, bt_local, case.seq_lens[s:s + 1], case.scale)
+        check_close_int8(bf16_to_f64(out[l, s:s + 1]), ref, f"int8 layer {l} seq {s}")
+
+
+def test_int8_full_size_batch32_sampled(lib, cuda_device, tables):
+    case = W.case_batch32()
+    full_size_int8_check(lib, cuda_device, case, [(0, 0), (0, 31), (7, 13), (15, 5)], tables)
+    torch.cuda.empty_cache()
+
+
+def test_int8_full_size_stress256_sampled(lib, cuda_device, tables):
+    case = W.case_stress()
+    full_size_int8_check(lib, cuda_device, case, [(0, 0), (9, 77), (15, 255)], tables)
+    torch.cuda.empty_cache()

@@ -158,6 +158,51 @@ def fill_pool(case: DecodeCase, device="cpu", chunk_pages: int = 8192) -> torch.
     return pool
 
 
+def fill_pool_int8(case: DecodeCase, device="cpu", chunk_pages: int = 8192):
+    """INT8 pages for the same geometry: (codes int8 [N][2][8][16][64],
+    scales float32 [N][2][8][16]).
+
+    Codes are N(0, 42^2) samples rounded and clipped to [-127, 127] and
+    scales uniform on [0.015, 0.025) -- about max|x| / 127 for rows of 64
+    N(0,1) values, so that code * scale is close to N(0,1) -- drawn in chunks
+    from one generator seeded with the case seed.  The case's outlier
+    fraction of key rows (page, head, slot) get 8x their scale: the INT8
+    image of a key row scaled by 8.
+    """
+    gen = torch.Generator(device=device).manual_seed(case.seed + 5000)
+    N = case.num_pages
+    codes = torch.empty((N, 2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM), dtype=torch.int8, device=device)
+    scales = torch.empty((N, 2, NUM_KV_HEADS, PAGE_TOKENS), dtype=torch.float32, device=device)
+    for p0 in range(0, N, chunk_pages):
+        p1 = min(N, p0 + chunk_pages)
+        g = torch.randn((p1 - p0, 2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM), generator=gen,
+                        device=device)
+        codes[p0:p1] = (g * 42.0).round().clamp(-127, 127).to(torch.int8)
+        scales[p0:p1] = 0.015 + 0.01 * torch.rand((p1 - p0, 2, NUM_KV_HEADS, PAGE_TOKENS),
+                                                  generator=gen, device=device)
+    if case.outlier_frac > 0:
+        n_vec = N * NUM_KV_HEADS * PAGE_TOKENS
+        n_out = int(round(case.outlier_frac * n_vec))
+        idx = torch.randperm(n_vec, generator=gen, device=device)[:n_out]
+        page, vec = idx // (NUM_KV_HEADS * PAGE_TOKENS), idx % (NUM_KV_HEADS * PAGE_TOKENS)
+        sv = scales.view(N, 2, NUM_KV_HEADS * PAGE_TOKENS)
+        sv[page, 0, vec] = sv[page, 0, vec] * 8
+    return codes, scales
+
+
+def garbage_fill_unused_int8(scales: torch.Tensor, case: DecodeCase, layer: int) -> None:
+    """Overwrite the scales of the unused tail slots of each sequence's last
+    page with NaN / +Inf bits (codes are finite whatever their bits)."""
+    bits = scales.view(torch.int32)
+    for s in range(case.num_seqs):
+        n = int(case.seq_lens[s])
+        if n % PAGE_TOKENS == 0 or n == 0:
+            continue
+        page = int(case.block_tables[layer, s, n // PAGE_TOKENS])
+        bits[page, 0, :, n % PAGE_TOKENS:] = 0x7FC00000   # NaN
+        bits[page, 1, :, n % PAGE_TOKENS:] = 0x7F800000   # +Inf
+
+
 def fill_queries(case: DecodeCase, device="cpu") -> torch.Tensor:
     """q[L][S][32][64] bf16 ~ N(0,1) (already rotated; rotation-invariant law)."""
     gen = torch.Generator(device=device).manual_seed(case.seed + 1000)
