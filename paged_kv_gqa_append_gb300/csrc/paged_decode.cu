@@ -147,31 +147,43 @@ __device__ __forceinline__ uint32_t seg_base(const Cursor& c, const int32_t* pre
   return 8u * (uint32_t)prefix[c.s] + (uint32_t)c.g * (uint32_t)c.np;
 }
 
-// Page id of unit u (or -1 if the table entry is outside the pool, -2 if u is
-// past the end of this warp's range).
-__device__ __forceinline__ int unit_page(uint32_t u, uint32_t u_end, const int32_t* prefix,
-                                         const DecodeParams& p) {
-  if (u >= u_end) return -2;
+// Page ids of unit u, which covers logical pages kP*j .. kP*j + kP - 1 of its
+// (sequence, head): .x the first, .y the second when kP == 2.  -1: an entry
+// outside the pool (in .x, for the unit); -2: u is past the end of this
+// warp's range; -3 (.y only): the sequence ends before the second page.
+template <int kP>
+__device__ __forceinline__ int2 unit_pages(uint32_t u, uint32_t u_end, const int32_t* prefix,
+                                           const int32_t* lens, const DecodeParams& p) {
+  if (u >= u_end) return make_int2(-2, -2);
   Cursor c;
   cursor_seek(c, u, prefix, p.num_seqs);
-  const int pid = __ldg(p.block_tables + (size_t)c.s * p.bt_stride + c.j);
-  return (pid >= 0 && pid < p.num_pages) ? pid : -1;
+  const int32_t* row = p.block_tables + (size_t)c.s * p.bt_stride + kP * c.j;
+  const int a = __ldg(row);
+  bool ok = a >= 0 && a < p.num_pages;
+  int b = -3;
+  if (kP == 2 && 2 * c.j + 1 < (lens[c.s] + PKV_PAGE_TOKENS - 1) / PKV_PAGE_TOKENS) {
+    b = __ldg(row + 1);
+    ok = ok && b >= 0 && b < p.num_pages;
+  }
+  return ok ? make_int2(a, b) : make_int2(-1, -1);
 }
 
-// Pages of a sequence, or 0 (and an error) for a length outside [0, max_len].
+// Units of a sequence (kP pages each), or 0 (and an error) for a length
+// outside [0, max_len].
+template <int kP = 1>
 __device__ __forceinline__ int seq_pages(int n, int max_len, bool* bad) {
   if (n < 0 || n > max_len) {
     *bad = true;
     return 0;
   }
-  return (n + PKV_PAGE_TOKENS - 1) / PKV_PAGE_TOKENS;
+  return (n + kP * PKV_PAGE_TOKENS - 1) / (kP * PKV_PAGE_TOKENS);
 }
 
 // Block-wide exclusive prefix of pages over all sequences into prefix[0..S],
 // if `nz` is given of non-empty sequences into nz[0..S], and if `lens` is
 // given a copy of seq_lens[0..S); returns the number of sequences without
 // pages (empty or invalid length).
-template <int kWarps, bool kAppend>
+template <int kWarps, bool kAppend, int kP = 1>
 __device__ int build_prefix(const DecodeParams& p, int32_t* prefix, int32_t* nz = nullptr,
                             int32_t* lens = nullptr) {
   // with a fused append the new token's position must also lie in the table
@@ -189,7 +201,7 @@ __device__ int build_prefix(const DecodeParams& p, int32_t* prefix, int32_t* nz 
   for (int s = lo; s < hi; ++s) {
     const int len = __ldg(p.seq_lens + s);
     if (lens) lens[s] = len;
-    const int np = seq_pages(len, max_len, &bad);
+    const int np = seq_pages<kP>(len, max_len, &bad);
     sum += np;
     cnt += (np > 0);
   }
@@ -220,7 +232,7 @@ __device__ int build_prefix(const DecodeParams& p, int32_t* prefix, int32_t* nz 
   for (int s = lo; s < hi; ++s) {
     prefix[s] = run;
     if (nz) nz[s] = run_nz;
-    const int np = seq_pages(lens ? lens[s] : __ldg(p.seq_lens + s), max_len, &bad);
+    const int np = seq_pages<kP>(lens ? lens[s] : __ldg(p.seq_lens + s), max_len, &bad);
     empties += (np == 0);
     run += np;
     run_nz += (np > 0);
@@ -350,12 +362,13 @@ struct MergeAcc {
 // (page, head), one 4-D TMA box with the 128-byte swizzle.
 struct Bf16Pages {
   static constexpr bool kBf16Pages = true;
+  static constexpr int kPagesPerUnit = 1;
   static constexpr int kStageBytes = pkv::kStageBytes;
   static constexpr int kVOffset = kTileBytes;
   __device__ static __forceinline__ void copy(uint32_t dst, const CUtensorMap* map,
-                                              const DecodeParams&, int g, int pid, uint32_t bar) {
+                                              const DecodeParams&, int g, int2 pid, uint32_t bar) {
     mbar_arrive_expect_tx(bar, kStageBytes);
-    tma_load_4d(dst, map, 0, 0, g, pid * 2, bar);  // K tile, then V tile
+    tma_load_4d(dst, map, 0, 0, g, pid.x * 2, bar);  // K tile, then V tile
   }
 };
 
@@ -777,12 +790,17 @@ __device__ __forceinline__ float pow2_biased(int k) {
   return __int_as_float(min(max(k, 1), 254) << 23);
 }
 
+template <int kP>
 struct MmaI8State {
+  static_assert(kP == 1 || kP == 2, "one or two pages per unit");
   static constexpr bool kBf16Pages = false;
-  static constexpr int kCodeTile = 1024;                 // 16 x 64 int8
-  static constexpr int kStageBytes = 2560;               // K, V code tiles, 2 x 64 B scales; 512-aligned
+  static constexpr int kPagesPerUnit = kP;
+  static constexpr int kCodeTile = 1024;                  // 16 x 64 int8
+  // per page: K and V code tiles (2 KiB); then per page 64 B of K and 64 B of
+  // V scales; rounded up to 512 bytes (the 64-byte swizzle's period)
+  static constexpr int kScaleOffset = 2 * kCodeTile * kP;
+  static constexpr int kStageBytes = (kScaleOffset + 128 * kP + 511) / 512 * 512;
   static constexpr int kVOffset = kCodeTile;
-  static constexpr int kScaleOffset = 2 * kCodeTile;
   __host__ __device__ static constexpr int min_blocks(int warps) { return warps >= 16 ? 1 : 16 / warps; }
   uint32_t qa[4][2];  // q' A-fragments (fp16) per MMA step, dims permuted as above
   float o[8][2];      // O in units of 2^(ev - 127): tile nb holds dims 16c + nb, 16c + 8 + nb
@@ -790,13 +808,20 @@ struct MmaI8State {
   float sl2q;         // scale * log2(e) / (q's power-of-two factor)
   int ev;             // biased exponent of O's unit
 
+  // The unit's pages: pid.x, and pid.y when kP == 2 and the sequence has it.
   __device__ static __forceinline__ void copy(uint32_t dst, const CUtensorMap* map,
-                                              const DecodeParams& p, int g, int pid, uint32_t bar) {
-    mbar_arrive_expect_tx(bar, 2 * kCodeTile + 128);
-    tma_load_4d(dst, map, 0, 0, g, pid * 2, bar);  // K codes, then V codes
-    const float* sc = p.kv_scales + ((size_t)pid * 2 * PKV_NUM_KV_HEADS + g) * PKV_PAGE_TOKENS;
-    bulk_load(dst + kScaleOffset, sc, 64, bar);
-    bulk_load(dst + kScaleOffset + 64, sc + PKV_NUM_KV_HEADS * PKV_PAGE_TOKENS, 64, bar);
+                                              const DecodeParams& p, int g, int2 pid, uint32_t bar) {
+    const bool two = kP == 2 && pid.y >= 0;
+    mbar_arrive_expect_tx(bar, (two ? 2 : 1) * (2 * kCodeTile + 128));
+#pragma unroll
+    for (int k = 0; k < kP; ++k) {
+      if (k == 1 && !two) break;
+      const int page = k == 0 ? pid.x : pid.y;
+      tma_load_4d(dst + 2 * kCodeTile * k, map, 0, 0, g, page * 2, bar);  // K codes, V codes
+      const float* sc = p.kv_scales + ((size_t)page * 2 * PKV_NUM_KV_HEADS + g) * PKV_PAGE_TOKENS;
+      bulk_load(dst + kScaleOffset + 128 * k, sc, 64, bar);
+      bulk_load(dst + kScaleOffset + 128 * k + 64, sc + PKV_NUM_KV_HEADS * PKV_PAGE_TOKENS, 64, bar);
+    }
   }
 
   template <bool kAppend>
@@ -834,81 +859,108 @@ struct MmaI8State {
     ev = 127;
   }
 
-  __device__ __forceinline__ void page(uint32_t sK, uint32_t sV, int valid, float, int lane) {
+  // One unit: kP pages at `base` (stage layout above), `valid` tokens (1 ..
+  // 16 kP) counted from the unit's first token.
+  __device__ __forceinline__ void page(uint32_t base, uint32_t, int valid, float, int lane) {
     const int g8 = lane >> 2, c = lane & 3;
-    const uint32_t sSc = sK + kScaleOffset;  // K scales [16], V scales [16]
-    // ---- S = q' K^T ------------------------------------------------------
-    const int ra = i8_token(g8 >> 1, g8 & 1), rb = i8_token(g8 >> 1, 2 + (g8 & 1));
-    const uint4 ka = lds128(sK + sw64(ra, 16 * c)), kb = lds128(sK + sw64(rb, 16 * c));
-    const uint32_t kaw[4] = {ka.x, ka.y, ka.z, ka.w}, kbw[4] = {kb.x, kb.y, kb.z, kb.w};
-    float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
-#pragma unroll
-    for (int kt = 0; kt < 4; ++kt) {
-      const uint32_t ua = kaw[kt] ^ 0x80808080u, ub = kbw[kt] ^ 0x80808080u;
-      mma_f16_16816(s0, qa[kt][0], qa[kt][1], hsub1152(__byte_perm(ua, 0x64646464u, 0x7150)),
-                    hsub1152(__byte_perm(ua, 0x64646464u, 0x7352)));
-      mma_f16_16816(s1, qa[kt][0], qa[kt][1], hsub1152(__byte_perm(ub, 0x64646464u, 0x7150)),
-                    hsub1152(__byte_perm(ub, 0x64646464u, 0x7352)));
-    }
-    // ---- online softmax (base 2) over tokens T(c, 0..3) ---------------------
+    const uint32_t sSc = base + kScaleOffset;
+    const bool hasB = kP == 2 && valid > PKV_PAGE_TOKENS;  // warp-uniform
     int tk[4];
-    float x[4], sv[4];
-    const float sraw[4] = {s0[0], s0[1], s1[0], s1[1]};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      tk[i] = i8_token(c, i);
-      x[i] = sraw[i] * (lds32f(sSc + 4 * tk[i]) * sl2q);
-      sv[i] = lds32f(sSc + 64 + 4 * tk[i]);
-    }
-    if (valid < PKV_PAGE_TOKENS) {  // tokens past the end: no score, and their scales may hold any bits
+    for (int i = 0; i < 4; ++i) tk[i] = i8_token(c, i);
+    // ---- S = q' K^T, per page ----------------------------------------------
+    const int ra = i8_token(g8 >> 1, g8 & 1), rb = i8_token(g8 >> 1, 2 + (g8 & 1));
+    float x[4 * kP], sv[4 * kP];
+#pragma unroll
+    for (int pg = 0; pg < kP; ++pg) {
+      float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
+      if (pg == 0 || hasB) {
+        const uint32_t sK = base + 2 * kCodeTile * pg;
+        const uint4 ka = lds128(sK + sw64(ra, 16 * c)), kb = lds128(sK + sw64(rb, 16 * c));
+        const uint32_t kaw[4] = {ka.x, ka.y, ka.z, ka.w}, kbw[4] = {kb.x, kb.y, kb.z, kb.w};
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) {
+          const uint32_t ua = kaw[kt] ^ 0x80808080u, ub = kbw[kt] ^ 0x80808080u;
+          mma_f16_16816(s0, qa[kt][0], qa[kt][1], hsub1152(__byte_perm(ua, 0x64646464u, 0x7150)),
+                        hsub1152(__byte_perm(ua, 0x64646464u, 0x7352)));
+          mma_f16_16816(s1, qa[kt][0], qa[kt][1], hsub1152(__byte_perm(ub, 0x64646464u, 0x7150)),
+                        hsub1152(__byte_perm(ub, 0x64646464u, 0x7352)));
+        }
+      }
+      const float sraw[4] = {s0[0], s0[1], s1[0], s1[1]};
+      const uint32_t sc = sSc + 128 * pg;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        x[i] = tk[i] < valid ? x[i] : -INFINITY;
-        sv[i] = tk[i] < valid ? sv[i] : 0.f;
+        x[4 * pg + i] = sraw[i] * (lds32f(sc + 4 * tk[i]) * sl2q);
+        sv[4 * pg + i] = lds32f(sc + 64 + 4 * tk[i]);
       }
     }
-    float pm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-    float vm = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+    // tokens past the end: no score, and their scales may hold any bits
+    if (valid < kP * PKV_PAGE_TOKENS) {
+#pragma unroll
+      for (int i = 0; i < 4 * kP; ++i) {
+        const bool live = (i >> 2) * PKV_PAGE_TOKENS + tk[i & 3] < valid;
+        x[i] = live ? x[i] : -INFINITY;
+        sv[i] = live ? sv[i] : 0.f;
+      }
+    }
+    // ---- online softmax (base 2) over the lane's tokens ---------------------
+    float pm = x[0], vm = sv[0];
+#pragma unroll
+    for (int i = 1; i < 4 * kP; ++i) {
+      pm = fmaxf(pm, x[i]);
+      vm = fmaxf(vm, sv[i]);
+    }
     pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
     vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 1));
     pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
     vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 2));
     const float mn = fmaxf(m, pm);
-    const int evn = vm > 0.f ? (__float_as_int(vm) >> 23) : ev;  // O's unit from this page on
+    const int evn = vm > 0.f ? (__float_as_int(vm) >> 23) : ev;  // O's unit from this unit on
     const float a_soft = (m == mn) ? 1.f : exp2f(m - mn);
     const float alpha = a_soft * pow2_biased(127 + ev - evn);
     const float vinv = pow2_biased(254 - evn);  // 2^-(evn - 127)
-    float pr[4];
+    float pr[4 * kP];
+    float lsum = 0.f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) pr[i] = (x[i] == mn) ? 1.f : exp2f(x[i] - mn);
-    l = l * a_soft + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+    for (int i = 0; i < 4 * kP; ++i) {
+      pr[i] = (x[i] == mn) ? 1.f : exp2f(x[i] - mn);
+      lsum += pr[i];
+    }
+    l = l * a_soft + lsum;
     m = mn;
     ev = evn;
-    const uint32_t pa0 = pack_f16x2(pr[0] * (sv[0] * vinv), pr[1] * (sv[1] * vinv));  // P'[g8][2c, 2c+1]
-    const uint32_t pa2 = pack_f16x2(pr[2] * (sv[2] * vinv), pr[3] * (sv[3] * vinv));  // P'[g8][2c+8, 2c+9]
 #pragma unroll
     for (int n = 0; n < 8; ++n) {
       o[n][0] *= alpha;
       o[n][1] *= alpha;
     }
-    // ---- O += P' V ---------------------------------------------------------
-    uint32_t vw[4][2];
+    // ---- O += P' V, per page ---------------------------------------------
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint2 t = lds64(sV + sw64(tk[i], 8 * g8));
-      vw[i][0] = t.x ^ 0x80808080u;
-      vw[i][1] = t.y ^ 0x80808080u;
-    }
+    for (int pg = 0; pg < kP; ++pg) {
+      if (pg == 1 && !hasB) break;
+      // P'[g8][2c, 2c+1] and P'[g8][2c+8, 2c+9] of this page
+      const uint32_t pa0 = pack_f16x2(pr[4 * pg] * (sv[4 * pg] * vinv), pr[4 * pg + 1] * (sv[4 * pg + 1] * vinv));
+      const uint32_t pa2 = pack_f16x2(pr[4 * pg + 2] * (sv[4 * pg + 2] * vinv), pr[4 * pg + 3] * (sv[4 * pg + 3] * vinv));
+      const uint32_t sV = base + 2 * kCodeTile * pg + kCodeTile;
+      uint32_t vw[4][2];
 #pragma unroll
-    for (int w = 0; w < 2; ++w) {
-      // rows (0, 1) and (2, 3) interleaved per dim: [r0.b, r1.b, r0.b', r1.b']
-      const uint32_t t01[2] = {__byte_perm(vw[0][w], vw[1][w], 0x5140), __byte_perm(vw[0][w], vw[1][w], 0x7362)};
-      const uint32_t t23[2] = {__byte_perm(vw[2][w], vw[3][w], 0x5140), __byte_perm(vw[2][w], vw[3][w], 0x7362)};
+      for (int i = 0; i < 4; ++i) {
+        const uint2 t = lds64(sV + sw64(tk[i], 8 * g8));
+        vw[i][0] = t.x ^ 0x80808080u;
+        vw[i][1] = t.y ^ 0x80808080u;
+      }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t sel = (k & 1) ? 0x4342u : 0x4140u;
-        mma_f16_16816(o[4 * w + k], pa0, pa2, hsub1152(__byte_perm(t01[k >> 1], 0x64646464u, sel)),
-                      hsub1152(__byte_perm(t23[k >> 1], 0x64646464u, sel)));
+      for (int w = 0; w < 2; ++w) {
+        // rows (0, 1) and (2, 3) interleaved per dim: [r0.b, r1.b, r0.b', r1.b']
+        const uint32_t t01[2] = {__byte_perm(vw[0][w], vw[1][w], 0x5140), __byte_perm(vw[0][w], vw[1][w], 0x7362)};
+        const uint32_t t23[2] = {__byte_perm(vw[2][w], vw[3][w], 0x5140), __byte_perm(vw[2][w], vw[3][w], 0x7362)};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t sel = (k & 1) ? 0x4342u : 0x4140u;
+          mma_f16_16816(o[4 * w + k], pa0, pa2, hsub1152(__byte_perm(t01[k >> 1], 0x64646464u, sel)),
+                        hsub1152(__byte_perm(t23[k >> 1], 0x64646464u, sel)));
+        }
       }
     }
   }
@@ -1050,6 +1102,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
   static_assert(!kAppend || State::kBf16Pages, "the fused append writes bf16 pages");
   constexpr int kStageB = State::kStageBytes;
+  constexpr int kP = State::kPagesPerUnit;  // pages per unit (and per pipeline stage)
   using Smem = SmemLayout<kWarps, kStages, kStageB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1067,7 +1120,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
   // Without `early` everything waits for the previous kernel here.  With it,
   // only reads of q and the new token, and every global write, wait (below).
   if (!p.early) pdl_wait();
-  const int n_empty = build_prefix<kWarps, kAppend>(p, prefix, nullptr, slen);
+  const int n_empty = build_prefix<kWarps, kAppend, kP>(p, prefix, nullptr, slen);
   pdl_launch_dependents();
 
   const uint32_t U = 8u * (uint32_t)prefix[S];
@@ -1088,8 +1141,8 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
     __syncwarp();
 
     // Page ids of the next 64 units, one per lane in two chunks.
-    int pidA = unit_page(u0 + lane, u1, prefix, p);
-    int pidB = unit_page(u0 + 32 + lane, u1, prefix, p);
+    int2 pidA = unit_pages<kP>(u0 + lane, u1, prefix, slen, p);
+    int2 pidB = unit_pages<kP>(u0 + 32 + lane, u1, prefix, slen, p);
     int chunk_base = 0;
     Cursor ci;
     cursor_seek(ci, u0, prefix, S);
@@ -1098,11 +1151,14 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
 
     auto issue = [&](int stage) {
       const int rel = iv - chunk_base;
-      const int pid = __shfl_sync(0xffffffffu, rel < 32 ? pidA : pidB, rel & 31);
+      const int2 mine = rel < 32 ? pidA : pidB;
+      int2 pid;
+      pid.x = __shfl_sync(0xffffffffu, mine.x, rel & 31);
+      pid.y = kP == 2 ? __shfl_sync(0xffffffffu, mine.y, rel & 31) : -3;
       if (lane == 0) {
-        my_pid[stage] = pid;
+        my_pid[stage] = pid.x;
         const uint32_t bar = bars + 8 * stage;
-        if (pid >= 0) {
+        if (pid.x >= 0) {
           fence_proxy_async_smem();
           State::copy(tiles + stage * kStageB, &tmap, p, ci.g, pid, bar);
         } else {
@@ -1114,7 +1170,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
       if (iv - chunk_base == 32) {
         pidA = pidB;
         chunk_base += 32;
-        pidB = unit_page(u0 + chunk_base + 32 + lane, u1, prefix, p);
+        pidB = unit_pages<kP>(u0 + chunk_base + 32 + lane, u1, prefix, slen, p);
       }
     };
 
@@ -1203,7 +1259,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
       if (timed_out) {
         seg_bad = true;
       } else if (pid >= 0) {
-        const int valid = min(PKV_PAGE_TOKENS, seg_len - PKV_PAGE_TOKENS * cc.j);
+        const int valid = min(kP * PKV_PAGE_TOKENS, seg_len - kP * PKV_PAGE_TOKENS * cc.j);
         const uint32_t sK = tiles + stage * kStageB;
         if (kAppend && cc.j == cc.np - 1) {  // the page that receives the new token
           tok.insert(p, sK, sK + kTileBytes, pid, cc.g, (seg_len - 1) % PKV_PAGE_TOKENS, lane);
@@ -1839,14 +1895,15 @@ template <class State, int kWarps, int kStages, bool kAppend = false>
 static int launch_decode(const DecodeParams& prm, const CUtensorMap& map, int device, int num_sms,
                          int max_seq_len, int min_units, int ctas_per_sm, cudaStream_t stream) {
   const size_t smem = SmemLayout<kWarps, kStages, State::kStageBytes>::bytes(prm.num_seqs);
+  constexpr int kP = State::kPagesPerUnit;
   int occ = 0;
   int rc = setup_kernel<State, kWarps, kStages, kAppend>(device, smem, &occ);
   if (rc != PKV_OK) return rc;
   if (occ < 1) return PKV_ERR_UNSUPPORTED_SHAPE;
   occ = min(occ, kMaxCtasPerSm);
   if (ctas_per_sm > 0) occ = min(occ, ctas_per_sm);
-  const long long pages_bound = max_seq_len > 0 ? (max_seq_len + 15) / 16 : 0;
-  const long long u_bound = 8ll * prm.num_seqs * pages_bound;
+  const long long pages_bound = max_seq_len > 0 ? (max_seq_len + 16 * kP - 1) / (16 * kP) : 0;
+  const long long u_bound = 8ll * prm.num_seqs * pages_bound;  // (units of kP pages)
   long long nc = (long long)num_sms * occ;
   const long long want = (u_bound + (long long)kWarps * min_units - 1) / ((long long)kWarps * min_units);
   if (want < nc) nc = want;
@@ -1987,8 +2044,8 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   const int cfg = warps * 100 + stages;
   // INT8 pages: static schedule, tensor cores, 4 stages by default
   const bool int8 = kv_scales != nullptr;
-  const int cfg8 = warps * 100 + ((opts && opts->stages > 0) ? opts->stages : 4);
-  if (int8 && (app || compute != PKV_COMPUTE_TENSOR || (opts && opts->schedule == 1) ||
+  const int cfg8 = warps * 100 + ((opts && opts->stages > 0) ? opts->stages : 2);
+  if (int8 && (app || compute != PKV_COMPUTE_TENSOR || (opts && (opts->schedule == 1 || opts->combine == 1)) ||
                (cfg8 != 1604 && cfg8 != 1602 && cfg8 != 804)))
     return PKV_ERR_INVALID_ARGUMENT;
   if (!int8 && compute == PKV_COMPUTE_TENSOR && cfg != 1602 && cfg != 1603 && cfg != 802 &&
@@ -2040,11 +2097,11 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int ms = max_seq_len;
-  if (int8) {
+  if (int8) {  // stages 2: two pages per stage; stages 4: one page per stage
     switch (cfg8) {
-      case 1602: return launch_decode<MmaI8State, 16, 2>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
-      case 804: return launch_decode<MmaI8State, 8, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
-      default: return launch_decode<MmaI8State, 16, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
+      case 1604: return launch_decode<MmaI8State<1>, 16, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
+      case 804: return launch_decode<MmaI8State<1>, 8, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
+      default: return launch_decode<MmaI8State<2>, 16, 2>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
     }
   }
   const int schedule = opts ? opts->schedule : 0;

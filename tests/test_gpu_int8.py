@@ -238,9 +238,10 @@ def test_int8_decode_mixed_batch8(lib, cuda_device):
     check_close_int8(bf16_to_f64(out), ref, "int8 mixed batch 8")
 
 
-@pytest.mark.parametrize("opts", [dict(), dict(stages=2), dict(warps_per_cta=8, stages=4),
+@pytest.mark.parametrize("opts", [dict(), dict(stages=4), dict(warps_per_cta=8, stages=4),
                                   dict(min_units_per_warp=1), dict(min_units_per_warp=64),
                                   dict(ctas_per_sm=1), dict(max_seq_len=2048),
+                                  dict(stages=4, min_units_per_warp=1, max_seq_len=2048),
                                   dict(warps_per_cta=8, stages=4, min_units_per_warp=1)])
 def test_int8_decode_work_split_variants(lib, cuda_device, opts):
     case = make_case([3, 40, 17, 700, 1, 129, 2048, 16], seed=9, extra_pages=5)
