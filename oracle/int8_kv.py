@@ -21,9 +21,13 @@ never changes):
   * decode is the bf16 definition (``paged_kv.attend``) applied to those
     values: nothing else about attention changes.
 
-Storage (the page geometry of the bf16 pool, one byte per element):
-  codes   int8    [num_pages][2 (K, V)][8 heads][16 slots][64 dims]  16 KiB/page
-  scales  float32 [num_pages][2 (K, V)][8 heads][16 slots]            1 KiB/page
+Logical arrays (the page geometry of the bf16 pool, one byte per element):
+  codes   int8    [num_pages][2 (K, V)][8 heads][16 slots][64 dims]
+  scales  float32 [num_pages][2 (K, V)][8 heads][16 slots]
+The pool the library reads and writes holds them as bytes, one 2176-byte
+block per (page, head) -- K codes [16][64], V codes [16][64], K scales [16],
+V scales [16] (little-endian fp32) -- so a page is 8 x 2176 = 17408 bytes
+(``pack_pages`` / ``unpack_pages``).
 
 fp32 emulation: each division is done in FP64 and rounded once to fp32.  For
 +, -, *, / a binary64 intermediate followed by rounding to binary32 gives the
@@ -43,6 +47,7 @@ from . import bf16, rope
 from .paged_kv import GROUP, HEAD_DIM, NUM_KV_HEADS, NUM_Q_HEADS, PAGE_TOKENS, attend, locate
 
 QMAX = 127
+BLOCK_BYTES = 2 * PAGE_TOKENS * HEAD_DIM + 2 * PAGE_TOKENS * 4   # 2176 per (page, head)
 
 
 def quantize_rows(x) -> tuple[np.ndarray, np.ndarray]:
@@ -180,3 +185,32 @@ def quantize_pool(pool_bits):
     """INT8 pools holding what ``append_rope_int8`` would store for every row of
     a bf16 pool (pool bits [N][2][8][16][64]); for building test inputs."""
     return quantize_rows(bf16.to_f64(pool_bits))
+
+
+def pack_pages(codes, scales) -> np.ndarray:
+    """Logical (codes, scales) -> the pool's bytes, uint8 [N][8][2176]: per
+    (page, head) the K codes, the V codes, the K scales, the V scales."""
+    codes = np.asarray(codes, np.int8)
+    scales = np.asarray(scales, np.float32)
+    N = codes.shape[0]
+    out = np.empty((N, NUM_KV_HEADS, BLOCK_BYTES), np.uint8)
+    for kv in range(2):
+        c = codes[:, kv].reshape(N, NUM_KV_HEADS, PAGE_TOKENS * HEAD_DIM)
+        out[:, :, kv * 1024:(kv + 1) * 1024] = c.view(np.uint8)
+        sc = np.ascontiguousarray(scales[:, kv].astype('<f4'))
+        out[:, :, 2048 + 64 * kv:2048 + 64 * (kv + 1)] = sc.view(np.uint8).reshape(N, NUM_KV_HEADS, 64)
+    return out
+
+
+def unpack_pages(pool_bytes):
+    """The pool's bytes uint8 [N][8][2176] -> logical (codes, scales)."""
+    b = np.ascontiguousarray(np.asarray(pool_bytes, np.uint8))
+    N = b.shape[0]
+    codes = np.empty((N, 2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM), np.int8)
+    scales = np.empty((N, 2, NUM_KV_HEADS, PAGE_TOKENS), np.float32)
+    for kv in range(2):
+        codes[:, kv] = b[:, :, kv * 1024:(kv + 1) * 1024].copy().view(np.int8).reshape(
+            N, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM)
+        scales[:, kv] = b[:, :, 2048 + 64 * kv:2048 + 64 * (kv + 1)].copy().view('<f4').reshape(
+            N, NUM_KV_HEADS, PAGE_TOKENS)
+    return codes, scales

@@ -273,3 +273,28 @@ def test_close_to_the_bf16_cache():
     d = np.abs(o8 - o16)
     assert d.max() < 0.05 and d.mean() < 0.01
     assert d.max() > 0          # the two caches do differ
+
+
+# ------------------------------------------------------------ byte layout ---
+
+def test_pack_pages_layout_by_hand():
+    codes, scales = I.new_pools(3)
+    codes[2, 0, 5, 7, 9] = -3          # K code: page 2, head 5, slot 7, dim 9
+    codes[1, 1, 0, 15, 63] = 127       # V code: page 1, head 0, slot 15, dim 63
+    scales[2, 1, 5, 4] = 0.5           # V scale: page 2, head 5, slot 4
+    scales[0, 0, 7, 0] = -2.0          # K scale: page 0, head 7, slot 0
+    b = I.pack_pages(codes, scales)
+    assert b.shape == (3, 8, 2176) and I.BLOCK_BYTES == 2176
+    assert b[2, 5, 7 * 64 + 9] == 256 - 3
+    assert b[1, 0, 1024 + 15 * 64 + 63] == 127
+    assert bytes(b[2, 5, 2112 + 16:2112 + 20]) == np.float32(0.5).tobytes()
+    assert bytes(b[0, 7, 2048:2052]) == np.float32(-2.0).tobytes()
+    assert np.count_nonzero(b) == 4     # 0.5 = 0x3F000000 and -2.0 = 0xC0000000: one nonzero byte each
+
+
+def test_pack_unpack_round_trip():
+    rng = np.random.default_rng(30)
+    codes = rng.integers(-128, 128, (5, 2, 8, 16, 64)).astype(np.int8)
+    scales = rng.standard_normal((5, 2, 8, 16)).astype(np.float32)
+    c2, s2 = I.unpack_pages(I.pack_pages(codes, scales))
+    assert np.array_equal(c2, codes) and np.array_equal(s2.view(np.uint32), scales.view(np.uint32))
