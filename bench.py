@@ -244,8 +244,7 @@ class OracleSampleInt8(OracleSample):
         self.OI = OI
         pages_per = self.pool.shape[0]
         small = dataclasses.replace(case, num_pages=pages_per, outlier_frac=0.0)
-        codes, scales = W.fill_pool_int8(small)
-        self.codes, self.scales = codes.numpy(), scales.numpy()
+        self.codes, self.scales = OI.unpack_pages(W.fill_pool_int8(small).numpy())
         self.kv_bytes = self.n * W.NUM_KV_HEADS * INT8_ROW_BYTES
 
     def run_one(self):
@@ -528,7 +527,7 @@ def run_int8_line(args, world, rank, local):
     torch.cuda.set_device(dev)
     case = make_case(args.workload, args.layers)
     L, S = case.num_layers, case.num_seqs
-    codes, scales = W.fill_pool_int8(case, device=dev)
+    pool = W.fill_pool_int8(case, device=dev)
     q_raw = W.fill_queries(case, device=dev)
     k_new, v_new = W.fill_new_kv(case, device=dev)
     bt = torch.from_numpy(case.block_tables).to(dev)
@@ -537,7 +536,7 @@ def run_int8_line(args, world, rank, local):
     cos, sin = pkv.rope_tables_device(dev, W.MAX_CONTEXT)
     out = torch.empty_like(q_raw)
     kv_bytes_layer = int(case.seq_lens.sum()) * W.NUM_KV_HEADS * INT8_ROW_BYTES
-    step = pkv.Int8DecodeStep(codes, scales, bt, lens, pos, k_new, v_new, q_raw, out, cos, sin,
+    step = pkv.Int8DecodeStep(pool, bt, lens, pos, k_new, v_new, q_raw, out, cos, sin,
                               case.scale, max_seq_len=case.max_seq_len)
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
@@ -627,9 +626,10 @@ def run_int8_line(args, world, rank, local):
             "data": "synthetic",
             "config": {"workload": "int8_" + case.name, "batch": S, "layers": L,
                        "ctx": int(case.seq_lens[0]), "pool_pages": case.num_pages,
-                       "pool_bytes": case.num_pages * (W.PAGE_ELEMS + 2 * 8 * 16 * 4),
-                       "kv_format": "int8 codes + fp32 scale per (token, KV head) row of K and V; "
-                                    "fp16 tensor-core MMAs, fp32 accumulation",
+                       "pool_bytes": case.num_pages * W.NUM_KV_HEADS * W.I8_BLOCK_BYTES,
+                       "kv_format": "int8 codes + fp32 scale per (token, KV head) row of K and V, "
+                                    "one 2176-byte block per (page, KV head); fp16 tensor-core "
+                                    "MMAs, fp32 accumulation",
                        "l2": "inputs larger than L2 (pool read per step exceeds 129 MB L2)",
                        "parallelism": f"replicas x{world}",
                        "launch": "CUDA graph of the step: INT8 append kernel + INT8 decode kernel per layer"},

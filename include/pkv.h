@@ -64,6 +64,10 @@ extern "C" {
 #define PKV_PAGE_TOKENS 16
 #define PKV_PAGE_ELEMS (2 * PKV_NUM_KV_HEADS * PKV_PAGE_TOKENS * PKV_HEAD_DIM)
 #define PKV_PAGE_BYTES (2 * PKV_PAGE_ELEMS) /* 32768 */
+/* INT8 pages: one block per (page, KV head) = K codes [16][64] int8, V codes
+ * [16][64] int8, K scales [16] float, V scales [16] float. */
+#define PKV_I8_BLOCK_BYTES (2 * PKV_PAGE_TOKENS * PKV_HEAD_DIM + 2 * PKV_PAGE_TOKENS * 4) /* 2176 */
+#define PKV_I8_PAGE_BYTES (PKV_NUM_KV_HEADS * PKV_I8_BLOCK_BYTES)                       /* 17408 */
 
 typedef enum pkv_status {
   PKV_OK = 0,
@@ -303,44 +307,50 @@ int paged_gqa_decode_append(const void* q, const void* k_new, const void* v_new,
  * (both divisions IEEE fp32; amax == 0 gives scale 0 and zero codes), where
  * x is the row the bf16 cache would hold (K rotated and rounded to bf16 as in
  * kv_append_rope, V as given).  A code stands for code * scale.  Rows must be
- * finite.  Pages keep the bf16 pool's geometry and block tables:
- *   kv_codes   device int8  [num_pages][2 (K,V)][8][16][64], 16 KiB/page
- *   kv_scales  device float [num_pages][2 (K,V)][8][16],      1 KiB/page
- * both 16-byte aligned, caller-owned.
+ * finite.  Pages keep the bf16 pool's block tables and 16 tokens; a page of
+ * the INT8 pool is 8 blocks of PKV_I8_BLOCK_BYTES, one per KV head:
+ *   kv_pool  device bytes [num_pages][8][2176], 17408 bytes/page, 16-byte
+ *            aligned, caller-owned; block (page, head) = K codes [16 slots][64]
+ *            int8, V codes [16][64] int8, K scales [16] float, V scales [16]
+ *            float (little-endian), so one contiguous copy brings a unit.
  * ---------------------------------------------------------------------- */
 
 /* kv_append_rope into INT8 pages: the arguments, ordering and error rules of
- * kv_append_rope, with the bf16 pool replaced by (kv_codes, kv_scales).  The
- * rotated q (when q_in is given) stays bf16.  k, v, kv_codes and kv_scales
- * must be 16-byte aligned, q_in/q_out 4-byte aligned. */
+ * kv_append_rope, with kv_pool the INT8 pool.  The rotated q (when q_in is
+ * given) stays bf16.  k, v and kv_pool must be 16-byte aligned, q_in/q_out
+ * 4-byte aligned. */
 int kv_append_rope_int8(const void* k, const void* v, const int32_t* positions,
                         const int32_t* token_seq, int T,
                         const int32_t* block_tables, int num_seqs, int bt_row_stride,
-                        int max_blocks, void* kv_codes, float* kv_scales, int num_pages,
+                        int max_blocks, void* kv_pool, int num_pages,
                         const float* rope_cos, const float* rope_sin, int max_pos,
                         const void* q_in, void* q_out, int* d_err, void* stream);
 
-/* paged_gqa_decode over INT8 pages: the same contract (arguments, workspace
- * of paged_gqa_decode_workspace_bytes, error rules), with the bf16 pool
- * replaced by (kv_codes, kv_scales).  Attention is over the dequantised
- * values: scores scale * q . (code_K * scale_K), weights applied to
- * code_V * scale_V.  Codes enter bf16 tensor-core MMAs exactly; the K scale
- * multiplies each fp32 score, and each probability times its V scale is
- * rounded to bf16 for the P V product (fp32 accumulation).  Output bf16. */
-int paged_gqa_decode_int8(const void* q, const void* kv_codes, const float* kv_scales,
-                          int num_pages, const int32_t* block_tables, int bt_row_stride,
-                          int max_blocks, const int32_t* seq_lens, int num_seqs,
-                          int max_seq_len, void* out, float scale,
+/* paged_gqa_decode over INT8 pages: the same arguments, workspace
+ * (paged_gqa_decode_workspace_bytes) and error rules, with kv_pool the INT8
+ * pool.  Attention is over the dequantised values: scores
+ * scale * q . (code_K * scale_K), weights applied to code_V * scale_V.
+ * Codes enter fp16 tensor-core MMAs exactly (fp32 accumulation); q is scaled
+ * by a power of two per (sequence, KV head) so that its largest |value| lies
+ * in [2^14, 2^15) (exact), the K scale multiplies each fp32 score, and each
+ * probability times its V scale, divided by a power of two that puts the
+ * largest V scale of its two-page block in [1, 2), is rounded to fp16 for
+ * the P V product.  Output bf16. */
+int paged_gqa_decode_int8(const void* q, const void* kv_pool, int num_pages,
+                          const int32_t* block_tables, int bt_row_stride, int max_blocks,
+                          const int32_t* seq_lens, int num_seqs, int max_seq_len,
+                          void* out, float scale,
                           void* workspace, size_t workspace_bytes,
                           int* d_err, void* stream);
 
 /* paged_gqa_decode_int8 with tuning options: compute must be
- * PKV_COMPUTE_TENSOR, schedule 0; (warps_per_cta, stages) one of (16, 4)
- * (the default), (16, 2) or (8, 4); other fields as paged_gqa_decode_ex. */
-int paged_gqa_decode_int8_ex(const void* q, const void* kv_codes, const float* kv_scales,
-                             int num_pages, const int32_t* block_tables, int bt_row_stride,
-                             int max_blocks, const int32_t* seq_lens, int num_seqs,
-                             int max_seq_len, void* out, float scale,
+ * PKV_COMPUTE_TENSOR, schedule and combine 0; (warps_per_cta, stages) one of
+ * (16, 2) (the default: two pages per stage), (16, 4) or (8, 4) (one page
+ * per stage); other fields as paged_gqa_decode_ex. */
+int paged_gqa_decode_int8_ex(const void* q, const void* kv_pool, int num_pages,
+                             const int32_t* block_tables, int bt_row_stride, int max_blocks,
+                             const int32_t* seq_lens, int num_seqs, int max_seq_len,
+                             void* out, float scale,
                              void* workspace, size_t workspace_bytes,
                              int* d_err, void* stream, const pkv_decode_opts* opts);
 

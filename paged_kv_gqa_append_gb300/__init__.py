@@ -76,11 +76,11 @@ _SIGS = {
     "paged_gqa_decode_append": (_i, [_p, _p, _p, _p, _p, _i, _p, _i, _p, _i, _i, _p, _i, _i, _p, _p,
                                      _f, _p, _sz, _p, _p, ctypes.POINTER(DecodeOpts)]),
     "paged_gqa_decode_noalloc": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _p]),
-    "kv_append_rope_int8": (_i, [_p, _p, _p, _p, _i, _p, _i, _i, _i, _p, _p, _i, _p, _p, _i, _p, _p,
-                                 _p, _p]),
-    "paged_gqa_decode_int8": (_i, [_p, _p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p, _p]),
-    "paged_gqa_decode_int8_ex": (_i, [_p, _p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p,
-                                      _p, ctypes.POINTER(DecodeOpts)]),
+    "kv_append_rope_int8": (_i, [_p, _p, _p, _p, _i, _p, _i, _i, _i, _p, _i, _p, _p, _i, _p, _p, _p,
+                                 _p]),
+    "paged_gqa_decode_int8": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p, _p]),
+    "paged_gqa_decode_int8_ex": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p, _p,
+                                      ctypes.POINTER(DecodeOpts)]),
     "pkv_read_device_error": (_i, [_p, _p, _i, _ip]),
     "pkv_credit_pages": (_i, [_i, _i, _i]),
     "pkv_sched_create": (_p, [_i, _i, _i, _i]),
@@ -297,25 +297,28 @@ def paged_gqa_decode(q, kv_pool, block_tables, seq_lens, out, scale, workspace=N
 
 # --------------------------------------------------------------- INT8 pages --
 
-def new_int8_pools(num_pages: int, device):
-    """(codes int8 [N, 2, 8, 16, 64], scales float32 [N, 2, 8, 16]), zero-filled."""
-    codes = torch.zeros((num_pages, 2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM), dtype=torch.int8,
-                        device=device)
-    scales = torch.zeros((num_pages, 2, NUM_KV_HEADS, PAGE_TOKENS), dtype=torch.float32,
-                         device=device)
-    return codes, scales
+I8_BLOCK_BYTES = 2 * PAGE_TOKENS * HEAD_DIM + 2 * PAGE_TOKENS * 4   # 2176 per (page, KV head)
 
 
-def kv_append_rope_int8(k, v, positions, block_tables, kv_codes, kv_scales, rope_cos, rope_sin,
+def new_int8_pool(num_pages: int, device) -> torch.Tensor:
+    """A zero-filled INT8 pool: uint8 [num_pages, 8, 2176], per (page, KV head)
+    K codes [16][64], V codes [16][64], K scales [16], V scales [16] (fp32)."""
+    return torch.zeros((num_pages, NUM_KV_HEADS, I8_BLOCK_BYTES), dtype=torch.uint8, device=device)
+
+
+def _need_i8_pool(kv_pool, dev):
+    _need(kv_pool, "kv_pool", torch.uint8, dev, (NUM_KV_HEADS, I8_BLOCK_BYTES))
+    if kv_pool.dim() != 3:
+        raise ValueError("the INT8 pool must be [num_pages, 8, 2176] uint8")
+
+
+def kv_append_rope_int8(k, v, positions, block_tables, kv_pool, rope_cos, rope_sin,
                         token_seq=None, q_in=None, q_out=None, d_err=None, max_blocks=None,
                         stream=None):
     """kv_append_rope into INT8 pages: each (token, head) row of the rotated K
     and of V is stored as 64 int8 codes and one fp32 scale."""
-    dev = kv_codes.device
-    _need(kv_codes, "kv_codes", torch.int8, dev, (2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM))
-    _need(kv_scales, "kv_scales", torch.float32, dev, (2, NUM_KV_HEADS, PAGE_TOKENS))
-    if kv_scales.shape[0] != kv_codes.shape[0]:
-        raise ValueError("kv_scales must have one row of scales per page of kv_codes")
+    dev = kv_pool.device
+    _need_i8_pool(kv_pool, dev)
     _need(k, "k", torch.bfloat16, dev, (NUM_KV_HEADS, HEAD_DIM))
     _need(v, "v", torch.bfloat16, dev, (NUM_KV_HEADS, HEAD_DIM))
     T = k.numel() // (NUM_KV_HEADS * HEAD_DIM)
@@ -345,23 +348,18 @@ def kv_append_rope_int8(k, v, positions, block_tables, kv_codes, kv_scales, rope
     S, stride = block_tables.shape
     mb = stride if max_blocks is None else max_blocks
     st = _L().kv_append_rope_int8(_ptr(k), _ptr(v), _ptr(positions), _ptr(token_seq), T,
-                                 _ptr(block_tables), S, stride, mb, _ptr(kv_codes),
-                                 _ptr(kv_scales), kv_codes.shape[0], _ptr(rope_cos),
-                                 _ptr(rope_sin), rope_cos.shape[0], _ptr(q_in), _ptr(q_out),
-                                 _ptr(d_err), _stream(stream))
+                                 _ptr(block_tables), S, stride, mb, _ptr(kv_pool), kv_pool.shape[0],
+                                 _ptr(rope_cos), _ptr(rope_sin), rope_cos.shape[0], _ptr(q_in),
+                                 _ptr(q_out), _ptr(d_err), _stream(stream))
     _check(st, "kv_append_rope_int8")
 
 
-def paged_gqa_decode_int8(q, kv_codes, kv_scales, block_tables, seq_lens, out, scale,
-                          workspace=None, max_seq_len=None, d_err=None, max_blocks=None,
-                          min_units_per_warp=0, ctas_per_sm=0, stages=0, warps_per_cta=0,
-                          stream=None):
-    """paged_gqa_decode over INT8 pages (codes and per-row scales)."""
-    dev = kv_codes.device
-    _need(kv_codes, "kv_codes", torch.int8, dev, (2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM))
-    _need(kv_scales, "kv_scales", torch.float32, dev, (2, NUM_KV_HEADS, PAGE_TOKENS))
-    if kv_scales.shape[0] != kv_codes.shape[0]:
-        raise ValueError("kv_scales must have one row of scales per page of kv_codes")
+def paged_gqa_decode_int8(q, kv_pool, block_tables, seq_lens, out, scale, workspace=None,
+                          max_seq_len=None, d_err=None, max_blocks=None, min_units_per_warp=0,
+                          ctas_per_sm=0, stages=0, warps_per_cta=0, stream=None):
+    """paged_gqa_decode over INT8 pages."""
+    dev = kv_pool.device
+    _need_i8_pool(kv_pool, dev)
     _need(q, "q", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
     _need(out, "out", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
     S = q.numel() // (NUM_Q_HEADS * HEAD_DIM)
@@ -382,9 +380,9 @@ def paged_gqa_decode_int8(q, kv_codes, kv_scales, block_tables, seq_lens, out, s
     _need(workspace, "workspace", torch.uint8, dev)
     if d_err is not None:
         _need(d_err, "d_err", torch.int32, dev)
-    args = (_ptr(q), _ptr(kv_codes), _ptr(kv_scales), kv_codes.shape[0], _ptr(block_tables),
-            stride, mb, _ptr(seq_lens), S, int(max_seq_len), _ptr(out), float(scale),
-            _ptr(workspace), workspace.numel(), _ptr(d_err), _stream(stream))
+    args = (_ptr(q), _ptr(kv_pool), kv_pool.shape[0], _ptr(block_tables), stride, mb,
+            _ptr(seq_lens), S, int(max_seq_len), _ptr(out), float(scale), _ptr(workspace),
+            workspace.numel(), _ptr(d_err), _stream(stream))
     if not (min_units_per_warp or ctas_per_sm or stages or warps_per_cta):
         st = _L().paged_gqa_decode_int8(*args)
     else:
@@ -690,25 +688,24 @@ class Int8DecodeStep:
     """One decode step over every layer on INT8 pages, captured into a CUDA graph.
 
     Per layer l:
-        kv_append_rope_int8(k[l], v[l], positions, block_tables[l], codes, scales,
-                            cos, sin, q_in=q[l], q_out=q_rot[l])
-        paged_gqa_decode_int8(q_rot[l], codes, scales, block_tables[l], seq_lens,
-                              out[l], scale)
+        kv_append_rope_int8(k[l], v[l], positions, block_tables[l], kv_pool, cos, sin,
+                            q_in=q[l], q_out=q_rot[l])
+        paged_gqa_decode_int8(q_rot[l], kv_pool, block_tables[l], seq_lens, out[l], scale)
     Tensors are bound at construction (refresh their contents in place and
     call run()), as for DecodeStep.
 
-        codes   [num_pages, 2, 8, 16, 64] int8;  scales [num_pages, 2, 8, 16] float32
+        kv_pool [num_pages, 8, 2176] uint8 (see new_int8_pool)
         block_tables [L, S, max_blocks] int32;  seq_lens, positions [S] int32
         k, v [L, S, 8, 64] bf16;  q, out [L, S, 32, 64] bf16
     """
 
-    def __init__(self, codes, scales, block_tables, seq_lens, positions, k, v, q, out, rope_cos,
+    def __init__(self, kv_pool, block_tables, seq_lens, positions, k, v, q, out, rope_cos,
                  rope_sin, scale, max_seq_len=None, workspace=None, d_err=None, q_rot=None,
                  use_graph=True, stream=None):
         self.L, self.S = block_tables.shape[0], block_tables.shape[1]
-        self.t = dict(codes=codes, scales=scales, bt=block_tables, lens=seq_lens, pos=positions,
+        self.t = dict(pool=kv_pool, bt=block_tables, lens=seq_lens, pos=positions,
                       k=k, v=v, q=q, out=out, cos=rope_cos, sin=rope_sin)
-        dev = codes.device
+        dev = kv_pool.device
         self.q_rot = torch.empty_like(q) if q_rot is None else q_rot
         self.workspace = alloc_workspace(self.S, dev) if workspace is None else workspace
         self.d_err = torch.zeros(1, dtype=torch.int32, device=dev) if d_err is None else d_err
@@ -727,12 +724,12 @@ class Int8DecodeStep:
         t = self.t
         for l in range(self.L):
             if append:
-                kv_append_rope_int8(t["k"][l], t["v"][l], t["pos"], t["bt"][l], t["codes"],
-                                    t["scales"], t["cos"], t["sin"], q_in=t["q"][l],
-                                    q_out=self.q_rot[l], d_err=self.d_err)
+                kv_append_rope_int8(t["k"][l], t["v"][l], t["pos"], t["bt"][l], t["pool"],
+                                    t["cos"], t["sin"], q_in=t["q"][l], q_out=self.q_rot[l],
+                                    d_err=self.d_err)
             if decode:
-                paged_gqa_decode_int8(self.q_rot[l], t["codes"], t["scales"], t["bt"][l],
-                                      t["lens"], t["out"][l], self.scale, workspace=self.workspace,
+                paged_gqa_decode_int8(self.q_rot[l], t["pool"], t["bt"][l], t["lens"], t["out"][l],
+                                      self.scale, workspace=self.workspace,
                                       max_seq_len=self.max_seq_len, d_err=self.d_err)
 
     def run(self):

@@ -100,8 +100,10 @@ __global__ void __launch_bounds__(256) kv_append_rope_kernel(const AppendParams 
 // Each (token, head) row of K (rotated and rounded to bf16 exactly as above)
 // and of V is quantised on its own: amax = max |x|, scale = amax / 127 and
 // code = round-half-even(x / scale) in [-127, 127], both divisions IEEE fp32;
-// amax == 0 gives scale 0 and zero codes.  Same grid as the bf16 append: one
-// CTA per token, one warp per KV head, lane i holding dims i and i + 32.
+// amax == 0 gives scale 0 and zero codes.  A (page, head) is one 2176-byte
+// block of the pool: K codes [16][64], V codes [16][64], K scales [16], V
+// scales [16].  Same grid as the bf16 append: one CTA per token, one warp per
+// KV head, lane i holding dims i and i + 32.
 // ---------------------------------------------------------------------------
 struct AppendI8Params {
   const uint16_t* k;          // [T][8][64] bf16
@@ -113,8 +115,7 @@ struct AppendI8Params {
   const float* sin;
   const uint16_t* q_in;       // [T][32][64] or null
   uint16_t* q_out;
-  int8_t* codes;              // [num_pages][2][8][16][64]
-  float* scales;              // [num_pages][2][8][16]
+  uint8_t* pool;              // [num_pages][8][2176]
   int T, num_seqs, bt_stride, max_blocks, num_pages, max_pos;
   int* d_err;
 };
@@ -163,8 +164,9 @@ __global__ void __launch_bounds__(256) kv_append_rope_int8_kernel(const AppendI8
   const int slot = pos % PKV_PAGE_TOKENS;
   const float c = __ldg(p.cos + (size_t)pos * PKV_ROPE_PAIRS + lane);
   const float sn = __ldg(p.sin + (size_t)pos * PKV_ROPE_PAIRS + lane);
-  const size_t krow = (((size_t)page * 2 + 0) * PKV_NUM_KV_HEADS + g) * PKV_PAGE_TOKENS + slot;
-  const size_t vrow = (((size_t)page * 2 + 1) * PKV_NUM_KV_HEADS + g) * PKV_PAGE_TOKENS + slot;
+  uint8_t* blk = p.pool + ((size_t)page * PKV_NUM_KV_HEADS + g) * PKV_I8_BLOCK_BYTES;
+  int8_t* kcode = reinterpret_cast<int8_t*>(blk) + slot * 64;
+  int8_t* vcode = reinterpret_cast<int8_t*>(blk) + 1024 + slot * 64;
 
   // K: rotate (bf16 result, as in the bf16 cache), quantise, store
   const uint16_t* kr = p.k + ((size_t)t * PKV_NUM_KV_HEADS + g) * 64;
@@ -173,19 +175,19 @@ __global__ void __launch_bounds__(256) kv_append_rope_int8_kernel(const AppendI8
   int8_t k0, k1;
   const float ks = quantize_pair(__uint_as_float((uint32_t)r0 << 16), __uint_as_float((uint32_t)r1 << 16),
                                  k0, k1);
-  p.codes[krow * 64 + lane] = k0;
-  p.codes[krow * 64 + lane + 32] = k1;
+  kcode[lane] = k0;
+  kcode[lane + 32] = k1;
 
   // V: quantise the bf16 row
   const uint16_t* vr = p.v + ((size_t)t * PKV_NUM_KV_HEADS + g) * 64;
   int8_t v0, v1;
   const float vs = quantize_pair(__uint_as_float((uint32_t)vr[lane] << 16),
                                  __uint_as_float((uint32_t)vr[lane + 32] << 16), v0, v1);
-  p.codes[vrow * 64 + lane] = v0;
-  p.codes[vrow * 64 + lane + 32] = v1;
+  vcode[lane] = v0;
+  vcode[lane + 32] = v1;
   if (lane == 0) {
-    p.scales[krow] = ks;
-    p.scales[vrow] = vs;
+    reinterpret_cast<float*>(blk + 2048)[slot] = ks;
+    reinterpret_cast<float*>(blk + 2112)[slot] = vs;
   }
 
   // q: the 4 query heads of this group, rotated as in the bf16 append
@@ -263,17 +265,17 @@ extern "C" int kv_append_rope(const void* k, const void* v, const int32_t* posit
 extern "C" int kv_append_rope_int8(const void* k, const void* v, const int32_t* positions,
                                    const int32_t* token_seq, int T, const int32_t* block_tables,
                                    int num_seqs, int bt_row_stride, int max_blocks,
-                                   void* kv_codes, float* kv_scales, int num_pages,
+                                   void* kv_pool, int num_pages,
                                    const float* rope_cos, const float* rope_sin, int max_pos,
                                    const void* q_in, void* q_out, int* d_err, void* stream) {
   if (T < 0 || num_seqs < 1 || max_blocks < 1 || bt_row_stride < max_blocks || num_pages < 1 ||
       max_pos < 1)
     return PKV_ERR_INVALID_ARGUMENT;
   if (T == 0) return PKV_OK;
-  if (!k || !v || !positions || !block_tables || !kv_codes || !kv_scales || !rope_cos || !rope_sin)
+  if (!k || !v || !positions || !block_tables || !kv_pool || !rope_cos || !rope_sin)
     return PKV_ERR_INVALID_ARGUMENT;
   if ((q_in == nullptr) != (q_out == nullptr)) return PKV_ERR_INVALID_ARGUMENT;
-  if (!aligned16(k) || !aligned16(v) || !aligned16(kv_codes) || !aligned16(kv_scales) ||
+  if (!aligned16(k) || !aligned16(v) || !aligned16(kv_pool) ||
       ((reinterpret_cast<uintptr_t>(q_in) | reinterpret_cast<uintptr_t>(q_out)) & 3u))
     return PKV_ERR_MISALIGNED;
   if (T > (1 << 30) || (long long)num_pages * PKV_PAGE_ELEMS >= (1ll << 40))
@@ -292,8 +294,7 @@ extern "C" int kv_append_rope_int8(const void* k, const void* v, const int32_t* 
   p.sin = rope_sin;
   p.q_in = static_cast<const uint16_t*>(q_in);
   p.q_out = static_cast<uint16_t*>(q_out);
-  p.codes = static_cast<int8_t*>(kv_codes);
-  p.scales = kv_scales;
+  p.pool = static_cast<uint8_t*>(kv_pool);
   p.T = T;
   p.num_seqs = num_seqs;
   p.bt_stride = bt_row_stride;

@@ -37,7 +37,4 @@ inline int cuda_status(cudaError_t e, const char* where = "cuda") {
 int make_pool_map(CUtensorMap* map, const void* pool, int num_pages);
 // The same view with a one-tile box {64, 16, 1, 1}.
 int make_pool_tile_map(CUtensorMap* map, const void* pool, int num_pages);
-// INT8 code pool [num_pages][2][8][16][64] viewed as (byte 64, slot 16,
-// head 8, page * 2 + kv), box {64, 16, 1, 2}, 64-byte swizzle.
-int make_pool_map_i8(CUtensorMap* map, const void* codes, int num_pages);
 }  // namespace pkv

@@ -57,7 +57,7 @@ struct DecodeParams {
   const uint16_t* q;              // [S][32][64] bf16
   const int32_t* block_tables;    // [S][bt_stride]
   const int32_t* seq_lens;        // [S]
-  const float* kv_scales;         // INT8 pages: [num_pages][2][8][16] fp32, else null
+  const uint8_t* pool_i8;         // INT8 pages: [num_pages][8][2176] bytes, else null
   uint16_t* out;                  // [S][32][64] bf16
   int bt_stride, max_blocks, num_pages, num_seqs;
   float sl2;                      // scale * log2(e)
@@ -703,10 +703,10 @@ struct FmaState : Bf16Pages {
 };
 
 // ---------------------------------------------------------------------------
-// INT8 pages (kv_append_rope_int8).  Per unit, the K and V code tiles of one
-// (page, head) -- 16 rows of 64 bytes each -- land by one 4-D TMA box with the
-// 64-byte swizzle (byte b of row r at r*64 + (((b/16) ^ (r/2)) % 4)*16 + b%16)
-// and the 16 K and 16 V scales by two 64-byte bulk copies behind them.
+// INT8 pages (kv_append_rope_int8).  A (page, head) is one contiguous
+// 2176-byte block of the pool -- K codes [16][64], V codes [16][64], K scales
+// [16], V scales [16] -- so one bulk copy per page brings everything a unit
+// needs (a unit is two consecutive pages of a (sequence, head)).
 //
 // Codes enter fp16 m16n8k16 MMAs (fp32 accumulation) exactly: with u = code +
 // 128 in a byte, the fp16 with bits 0x64uu is 1024 + u, and subtracting 1152
@@ -732,19 +732,13 @@ struct FmaState : Bf16Pages {
 // same way, which leaves q.k unchanged), so a lane's B fragments of a K row
 // are bytes 16c .. 16c+15 of it.  Column g8 of P V tile nb is dim 8 g8 + nb:
 // a lane reads bytes 8 g8 .. 8 g8 + 7 of the V rows of its four tokens, and
-// its O fragment of tile nb holds dims 16c + nb and 16c + 8 + nb.  With the
-// 64-byte swizzle every shared-memory load of a page is conflict-free: each
-// quarter-warp's 16-byte K loads cover two rows of opposite parity, and each
-// half-warp's 8-byte V loads cover four rows whose 32-byte pieces fall on
-// distinct banks.
+// its O fragment of tile nb holds dims 16c + nb and 16c + 8 + nb.  Each
+// quarter-warp's 16-byte K loads cover two rows of opposite parity
+// (conflict-free); each half-warp's 8-byte V loads cover four rows, two per
+// 64-byte half of the bank window (two-way).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int i8_token(int c, int i) {
   return ((c ^ i) & 1) + 2 * (i & 1) + 4 * (c >> 1) + 8 * (i >> 1);
-}
-// Offset of byte b (a multiple of 8) of row r of a 16 x 64-byte tile stored
-// with the 64-byte swizzle (the tile starts on a 512-byte boundary).
-__device__ __forceinline__ uint32_t sw64(int r, int b) {
-  return (uint32_t)(r * 64 + ((((b >> 4) ^ (r >> 1)) & 3) << 4) + (b & 15));
 }
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
   uint4 v;
@@ -795,12 +789,9 @@ struct MmaI8State {
   static_assert(kP == 1 || kP == 2, "one or two pages per unit");
   static constexpr bool kBf16Pages = false;
   static constexpr int kPagesPerUnit = kP;
-  static constexpr int kCodeTile = 1024;                  // 16 x 64 int8
-  // per page: K and V code tiles (2 KiB); then per page 64 B of K and 64 B of
-  // V scales; rounded up to 512 bytes (the 64-byte swizzle's period)
-  static constexpr int kScaleOffset = 2 * kCodeTile * kP;
-  static constexpr int kStageBytes = (kScaleOffset + 128 * kP + 511) / 512 * 512;
-  static constexpr int kVOffset = kCodeTile;
+  static constexpr int kBlock = PKV_I8_BLOCK_BYTES;     // one (page, head): 2176 bytes
+  static constexpr int kStageBytes = kBlock * kP;        // a multiple of 16
+  static constexpr int kVOffset = 1024;                  // V codes; K scales at 2048, V scales at 2112
   __host__ __device__ static constexpr int min_blocks(int warps) { return warps >= 16 ? 1 : 16 / warps; }
   uint32_t qa[4][2];  // q' A-fragments (fp16) per MMA step, dims permuted as above
   float o[8][2];      // O in units of 2^(ev - 127): tile nb holds dims 16c + nb, 16c + 8 + nb
@@ -812,16 +803,9 @@ struct MmaI8State {
   __device__ static __forceinline__ void copy(uint32_t dst, const CUtensorMap* map,
                                               const DecodeParams& p, int g, int2 pid, uint32_t bar) {
     const bool two = kP == 2 && pid.y >= 0;
-    mbar_arrive_expect_tx(bar, (two ? 2 : 1) * (2 * kCodeTile + 128));
-#pragma unroll
-    for (int k = 0; k < kP; ++k) {
-      if (k == 1 && !two) break;
-      const int page = k == 0 ? pid.x : pid.y;
-      tma_load_4d(dst + 2 * kCodeTile * k, map, 0, 0, g, page * 2, bar);  // K codes, V codes
-      const float* sc = p.kv_scales + ((size_t)page * 2 * PKV_NUM_KV_HEADS + g) * PKV_PAGE_TOKENS;
-      bulk_load(dst + kScaleOffset + 128 * k, sc, 64, bar);
-      bulk_load(dst + kScaleOffset + 128 * k + 64, sc + PKV_NUM_KV_HEADS * PKV_PAGE_TOKENS, 64, bar);
-    }
+    mbar_arrive_expect_tx(bar, (two ? 2 : 1) * kBlock);
+    bulk_load(dst, p.pool_i8 + ((size_t)pid.x * PKV_NUM_KV_HEADS + g) * kBlock, kBlock, bar);
+    if (two) bulk_load(dst + kBlock, p.pool_i8 + ((size_t)pid.y * PKV_NUM_KV_HEADS + g) * kBlock, kBlock, bar);
   }
 
   template <bool kAppend>
@@ -859,11 +843,10 @@ struct MmaI8State {
     ev = 127;
   }
 
-  // One unit: kP pages at `base` (stage layout above), `valid` tokens (1 ..
-  // 16 kP) counted from the unit's first token.
+  // One unit: kP page blocks at `base`, `valid` tokens (1 .. 16 kP) counted
+  // from the unit's first token.
   __device__ __forceinline__ void page(uint32_t base, uint32_t, int valid, float, int lane) {
     const int g8 = lane >> 2, c = lane & 3;
-    const uint32_t sSc = base + kScaleOffset;
     const bool hasB = kP == 2 && valid > PKV_PAGE_TOKENS;  // warp-uniform
     int tk[4];
 #pragma unroll
@@ -875,8 +858,8 @@ struct MmaI8State {
     for (int pg = 0; pg < kP; ++pg) {
       float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
       if (pg == 0 || hasB) {
-        const uint32_t sK = base + 2 * kCodeTile * pg;
-        const uint4 ka = lds128(sK + sw64(ra, 16 * c)), kb = lds128(sK + sw64(rb, 16 * c));
+        const uint32_t sK = base + kBlock * pg;
+        const uint4 ka = lds128(sK + ra * 64 + 16 * c), kb = lds128(sK + rb * 64 + 16 * c);
         const uint32_t kaw[4] = {ka.x, ka.y, ka.z, ka.w}, kbw[4] = {kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
         for (int kt = 0; kt < 4; ++kt) {
@@ -888,7 +871,7 @@ struct MmaI8State {
         }
       }
       const float sraw[4] = {s0[0], s0[1], s1[0], s1[1]};
-      const uint32_t sc = sSc + 128 * pg;
+      const uint32_t sc = base + kBlock * pg + 2048;  // K scales, then V scales
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         x[4 * pg + i] = sraw[i] * (lds32f(sc + 4 * tk[i]) * sl2q);
@@ -942,11 +925,11 @@ struct MmaI8State {
       // P'[g8][2c, 2c+1] and P'[g8][2c+8, 2c+9] of this page
       const uint32_t pa0 = pack_f16x2(pr[4 * pg] * (sv[4 * pg] * vinv), pr[4 * pg + 1] * (sv[4 * pg + 1] * vinv));
       const uint32_t pa2 = pack_f16x2(pr[4 * pg + 2] * (sv[4 * pg + 2] * vinv), pr[4 * pg + 3] * (sv[4 * pg + 3] * vinv));
-      const uint32_t sV = base + 2 * kCodeTile * pg + kCodeTile;
+      const uint32_t sV = base + kBlock * pg + kVOffset;
       uint32_t vw[4][2];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint2 t = lds64(sV + sw64(tk[i], 8 * g8));
+        const uint2 t = lds64(sV + tk[i] * 64 + 8 * g8);
         vw[i][0] = t.x ^ 0x80808080u;
         vw[i][1] = t.y ^ 0x80808080u;
       }
@@ -2013,7 +1996,7 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
                         const int32_t* seq_lens, int num_seqs, int max_seq_len, void* out,
                         float scale, void* workspace, size_t workspace_bytes, int* d_err,
                         void* stream, const pkv_decode_opts* opts, const AppendArgs* app,
-                        const float* kv_scales = nullptr) {
+                        bool int8 = false) {
   if (num_seqs < 0 || num_pages < 1 || max_blocks < 1 || bt_row_stride < max_blocks)
     return PKV_ERR_INVALID_ARGUMENT;
   if (num_seqs == 0) return PKV_OK;
@@ -2021,7 +2004,6 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
     return PKV_ERR_INVALID_ARGUMENT;
   if (!isfinite(scale)) return PKV_ERR_INVALID_ARGUMENT;
   if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out) || !aligned16(workspace) ||
-      !aligned16(kv_scales) ||
       (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
     return PKV_ERR_MISALIGNED;
   if (app) {
@@ -2042,8 +2024,7 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   if (compute != PKV_COMPUTE_TENSOR && compute != PKV_COMPUTE_FMA) return PKV_ERR_INVALID_ARGUMENT;
   if (app && compute != PKV_COMPUTE_TENSOR) return PKV_ERR_INVALID_ARGUMENT;
   const int cfg = warps * 100 + stages;
-  // INT8 pages: static schedule, tensor cores, 4 stages by default
-  const bool int8 = kv_scales != nullptr;
+  // INT8 pages: static schedule, tensor cores, two pages per stage by default
   const int cfg8 = warps * 100 + ((opts && opts->stages > 0) ? opts->stages : 2);
   if (int8 && (app || compute != PKV_COMPUTE_TENSOR || (opts && (opts->schedule == 1 || opts->combine == 1)) ||
                (cfg8 != 1604 && cfg8 != 1602 && cfg8 != 804)))
@@ -2061,8 +2042,11 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   const WorkspaceLayout wl = workspace_layout(num_seqs, sms);
   if (workspace_bytes < wl.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
 
-  CUtensorMap map;
-  rc = int8 ? make_pool_map_i8(&map, kv_pool, num_pages) : make_pool_map(&map, kv_pool, num_pages);
+  CUtensorMap map;  // INT8 pages are copied by plain bulk copies: no map
+  if (int8)
+    memset(&map, 0, sizeof(map));
+  else
+    rc = make_pool_map(&map, kv_pool, num_pages);
   if (rc != PKV_OK) return rc;
 
   DecodeParams prm;
@@ -2070,7 +2054,7 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   prm.q = static_cast<const uint16_t*>(q);
   prm.block_tables = block_tables;
   prm.seq_lens = seq_lens;
-  prm.kv_scales = kv_scales;
+  prm.pool_i8 = int8 ? static_cast<const uint8_t*>(kv_pool) : nullptr;
   prm.out = static_cast<uint16_t*>(out);
   prm.bt_stride = bt_row_stride;
   prm.max_blocks = max_blocks;
@@ -2165,24 +2149,23 @@ extern "C" int paged_gqa_decode(const void* q, const void* kv_pool, int num_page
                              workspace_bytes, d_err, stream, nullptr);
 }
 
-extern "C" int paged_gqa_decode_int8_ex(const void* q, const void* kv_codes, const float* kv_scales,
-                                        int num_pages, const int32_t* block_tables,
-                                        int bt_row_stride, int max_blocks, const int32_t* seq_lens,
-                                        int num_seqs, int max_seq_len, void* out, float scale,
-                                        void* workspace, size_t workspace_bytes, int* d_err,
-                                        void* stream, const pkv_decode_opts* opts) {
-  if (kv_scales == nullptr && num_seqs > 0) return PKV_ERR_INVALID_ARGUMENT;
-  return decode_entry(q, kv_codes, num_pages, block_tables, bt_row_stride, max_blocks, seq_lens,
+extern "C" int paged_gqa_decode_int8_ex(const void* q, const void* kv_pool, int num_pages,
+                                        const int32_t* block_tables, int bt_row_stride,
+                                        int max_blocks, const int32_t* seq_lens, int num_seqs,
+                                        int max_seq_len, void* out, float scale, void* workspace,
+                                        size_t workspace_bytes, int* d_err, void* stream,
+                                        const pkv_decode_opts* opts) {
+  return decode_entry(q, kv_pool, num_pages, block_tables, bt_row_stride, max_blocks, seq_lens,
                       num_seqs, max_seq_len, out, scale, workspace, workspace_bytes, d_err, stream,
-                      opts, nullptr, kv_scales);
+                      opts, nullptr, true);
 }
 
-extern "C" int paged_gqa_decode_int8(const void* q, const void* kv_codes, const float* kv_scales,
-                                     int num_pages, const int32_t* block_tables, int bt_row_stride,
-                                     int max_blocks, const int32_t* seq_lens, int num_seqs,
-                                     int max_seq_len, void* out, float scale, void* workspace,
+extern "C" int paged_gqa_decode_int8(const void* q, const void* kv_pool, int num_pages,
+                                     const int32_t* block_tables, int bt_row_stride, int max_blocks,
+                                     const int32_t* seq_lens, int num_seqs, int max_seq_len,
+                                     void* out, float scale, void* workspace,
                                      size_t workspace_bytes, int* d_err, void* stream) {
-  return paged_gqa_decode_int8_ex(q, kv_codes, kv_scales, num_pages, block_tables, bt_row_stride,
-                                  max_blocks, seq_lens, num_seqs, max_seq_len, out, scale,
-                                  workspace, workspace_bytes, d_err, stream, nullptr);
+  return paged_gqa_decode_int8_ex(q, kv_pool, num_pages, block_tables, bt_row_stride, max_blocks,
+                                  seq_lens, num_seqs, max_seq_len, out, scale, workspace,
+                                  workspace_bytes, d_err, stream, nullptr);
 }

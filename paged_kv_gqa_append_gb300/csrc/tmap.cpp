@@ -1,5 +1,4 @@
-// The pools' TMA tensor maps (bf16 pages for decode and prefill, INT8 code
-// pages for decode).
+// The pool's TMA tensor maps, shared by the decode and prefill kernels.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <mutex>
@@ -88,18 +87,6 @@ int make_pool_tile_map(CUtensorMap* map, const void* pool, int num_pages) {
   const cuuint64_t strides[3] = {128, 2048, 2048 * PKV_NUM_KV_HEADS};
   const cuuint32_t box[4] = {64, 16, 1, 1};
   return encode_4d(cache, map, pool, num_pages, dims, strides, box);
-}
-
-// INT8 code pool [num_pages][2][8][16][64] viewed as (byte 64, slot 16,
-// head 8, page * 2 + kv); one box {64, 16, 1, 2} = the K and V code tiles of
-// one (page, head), 2 x 1 KiB, with the 64-byte swizzle (rows are 64 bytes).
-int make_pool_map_i8(CUtensorMap* map, const void* codes, int num_pages) {
-  static thread_local MapCache cache;
-  const cuuint64_t dims[4] = {64, 16, PKV_NUM_KV_HEADS, (cuuint64_t)num_pages * 2};
-  const cuuint64_t strides[3] = {64, 1024, 1024 * PKV_NUM_KV_HEADS};
-  const cuuint32_t box[4] = {64, 16, 1, 2};
-  return encode_4d(cache, map, codes, num_pages, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                   CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 }  // namespace pkv

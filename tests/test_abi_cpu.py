@@ -107,27 +107,27 @@ def test_host_side_validation_returns_before_launch():
     assert AM(fake, 4, 10, 9, fake, null) == 1
     assert AM(null, 4, 10, 10, fake, null) == 1
     assert AM(ctypes.c_void_p(0x10001), 4, 10, 10, fake, null) == 2
-    # INT8 append: nothing to do; nulls (scales missing); misaligned scales
+    # INT8 append: nothing to do; null pool; misaligned pool
     A8 = L.kv_append_rope_int8
-    assert A8(null, null, null, null, 0, null, 1, 128, 128, null, null, 8, null, null, 2048, null,
-              null, null, null) == 0
-    assert A8(fake, fake, fake, null, 1, fake, 1, 128, 128, fake, null, 8, fake, fake, 2048, null,
-              null, null, null) == 1
-    assert A8(fake, fake, fake, null, 1, fake, 1, 128, 128, fake, ctypes.c_void_p(0x10004), 8, fake,
-              fake, 2048, null, null, null, null) == 2
-    # INT8 decode: nothing to do; missing scales; misaligned scales; bad option set
+    assert A8(null, null, null, null, 0, null, 1, 128, 128, null, 8, null, null, 2048, null, null,
+              null, null) == 0
+    assert A8(fake, fake, fake, null, 1, fake, 1, 128, 128, null, 8, fake, fake, 2048, null, null,
+              null, null) == 1
+    assert A8(fake, fake, fake, null, 1, fake, 1, 128, 128, ctypes.c_void_p(0x10004), 8, fake, fake,
+              2048, null, null, null, null) == 2
+    # INT8 decode: nothing to do; null pool; misaligned pool; bad option sets
     D8 = L.paged_gqa_decode_int8
-    assert D8(null, null, null, 8, null, 128, 128, null, 0, 0, null, 0.125, null, 0, null, null) == 0
-    assert D8(fake, fake, null, 8, fake, 128, 128, fake, 1, 16, fake, 0.125, fake, 1 << 20, null,
+    assert D8(null, null, 8, null, 128, 128, null, 0, 0, null, 0.125, null, 0, null, null) == 0
+    assert D8(fake, null, 8, fake, 128, 128, fake, 1, 16, fake, 0.125, fake, 1 << 20, null,
               null) == 1
-    assert D8(fake, fake, ctypes.c_void_p(0x10008), 8, fake, 128, 128, fake, 1, 16, fake, 0.125,
-              fake, 1 << 20, null, null) == 2
-    opts = pkv.DecodeOpts(pkv.COMPUTE_FMA, 0, 0, 0, 0, 0, 0, 0)
-    assert L.paged_gqa_decode_int8_ex(fake, fake, fake, 8, fake, 128, 128, fake, 1, 16, fake, 0.125,
-                                      fake, 1 << 20, null, null, ctypes.byref(opts)) == 1
-    opts = pkv.DecodeOpts(pkv.COMPUTE_TENSOR, 0, 0, 3, 16, 0, 0, 0)
-    assert L.paged_gqa_decode_int8_ex(fake, fake, fake, 8, fake, 128, 128, fake, 1, 16, fake, 0.125,
-                                      fake, 1 << 20, null, null, ctypes.byref(opts)) == 1
+    assert D8(fake, ctypes.c_void_p(0x10008), 8, fake, 128, 128, fake, 1, 16, fake, 0.125, fake,
+              1 << 20, null, null) == 2
+    for bad in (pkv.DecodeOpts(pkv.COMPUTE_FMA, 0, 0, 0, 0, 0, 0, 0),
+                pkv.DecodeOpts(pkv.COMPUTE_TENSOR, 0, 0, 3, 16, 0, 0, 0),
+                pkv.DecodeOpts(pkv.COMPUTE_TENSOR, 0, 0, 0, 0, 1, 0, 0),
+                pkv.DecodeOpts(pkv.COMPUTE_TENSOR, 0, 0, 0, 0, 0, 1, 0)):
+        assert L.paged_gqa_decode_int8_ex(fake, fake, 8, fake, 128, 128, fake, 1, 16, fake, 0.125,
+                                          fake, 1 << 20, null, null, ctypes.byref(bad)) == 1
 
 
 def _run_cpp_schedule(case, static=False):

@@ -54,23 +54,28 @@ def check_close_int8(gpu, ref, what=""):
     return float(err.max()), float(err.mean())
 
 
-def dev_pools(codes, scales, dev):
-    return (torch.from_numpy(np.ascontiguousarray(codes)).to(dev),
-            torch.from_numpy(np.ascontiguousarray(scales)).to(dev))
+def dev_pool(codes, scales, dev):
+    """The library's INT8 pool (bytes) holding the oracle's logical arrays."""
+    return torch.from_numpy(OI.pack_pages(codes, scales)).to(dev)
+
+
+def host_pool(pool):
+    """Logical (codes, scales) of a device INT8 pool."""
+    return OI.unpack_pages(pool.cpu().numpy())
+
+
+def same_pool(pool, codes, scales):
+    """The device pool's bytes equal the oracle's arrays packed (bit for bit)."""
+    return np.array_equal(pool.cpu().numpy(), OI.pack_pages(codes, scales))
 
 
 def run_decode8(lib, dev, q_bits, codes, scales, bt, lens, scale=0.125, **kw):
     q = to_dev_bf16(q_bits, dev)
-    c, s = dev_pools(codes, scales, dev)
     out = torch.empty_like(q)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    lib.paged_gqa_decode_int8(q, c, s, to_dev_i32(bt, dev), to_dev_i32(lens, dev), out, scale,
-                              d_err=err, **kw)
+    lib.paged_gqa_decode_int8(q, dev_pool(codes, scales, dev), to_dev_i32(bt, dev),
+                              to_dev_i32(lens, dev), out, scale, d_err=err, **kw)
     return out, lib.pkv_read_device_error(err)
-
-
-def f32_bits(a):
-    return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
 
 
 # ---------------------------------------------------------------- append ----
@@ -94,17 +99,16 @@ def test_int8_append_bit_exact(lib, cuda_device, tables):
     seqs = np.array([p[0] for p in pairs], np.int32)
     pos = np.array([p[1] for p in pairs], np.int32)
     k, v, q = rand_bits(4000, (T, 8, 64)), rand_bits(4001, (T, 8, 64)), rand_bits(4002, (T, 32, 64))
-    c_d, s_d = dev_pools(codes0, scales0, dev)
+    pool_d = dev_pool(codes0, scales0, dev)
     q_out = torch.empty((T, 32, 64), dtype=torch.bfloat16, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     lib.kv_append_rope_int8(to_dev_bf16(k, dev), to_dev_bf16(v, dev), to_dev_i32(pos, dev),
-                            to_dev_i32(bt, dev), c_d, s_d, cos_d, sin_d, token_seq=to_dev_i32(seqs, dev),
+                            to_dev_i32(bt, dev), pool_d, cos_d, sin_d, token_seq=to_dev_i32(seqs, dev),
                             q_in=to_dev_bf16(q, dev), q_out=q_out, d_err=err)
     assert lib.pkv_read_device_error(err) == 0
     want_c, want_s, want_q, e = OI.append_rope_int8(codes0, scales0, k, v, pos, seqs, bt, cos_o, sin_o, q)
     assert not e
-    assert np.array_equal(c_d.cpu().numpy(), want_c)
-    assert np.array_equal(f32_bits(s_d.cpu().numpy()), f32_bits(want_s))
+    assert same_pool(pool_d, want_c, want_s)
     assert np.array_equal(bits(q_out), want_q)
 
 
@@ -126,20 +130,19 @@ def test_int8_append_special_rows(lib, cuda_device, tables):
     pos = np.array([0, 16, 32, 48], np.int32)      # slot 0 of four pages, position 0 first
     bt = np.array([[0, 1, 2, 3]], np.int32)
     codes0, scales0 = OI.new_pools(4, code_fill=5, scale_fill=7.0)
-    c_d, s_d = dev_pools(codes0, scales0, dev)
+    pool_d = dev_pool(codes0, scales0, dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     lib.kv_append_rope_int8(to_dev_bf16(kb, dev), to_dev_bf16(vb, dev), to_dev_i32(pos, dev),
-                            to_dev_i32(bt, dev), c_d, s_d, cos_d, sin_d,
+                            to_dev_i32(bt, dev), pool_d, cos_d, sin_d,
                             token_seq=to_dev_i32(np.zeros(4, np.int32), dev), d_err=err)
     assert lib.pkv_read_device_error(err) == 0
     want_c, want_s, _, e = OI.append_rope_int8(codes0, scales0, kb, vb, pos, np.zeros(4, np.int32),
                                                bt, cos_o, sin_o)
     assert not e
-    got_c = c_d.cpu().numpy()
-    assert np.array_equal(got_c, want_c)
-    assert np.array_equal(f32_bits(s_d.cpu().numpy()), f32_bits(want_s))
+    assert same_pool(pool_d, want_c, want_s)
+    got_c, got_s = host_pool(pool_d)
     assert list(got_c[0, 0, 0, 0, 1:9]) == [2, 4, -2, -4, 0, 2, 126, 0]
-    assert np.all(got_c[0, 1, :, 0] == 0) and np.all(s_d.cpu().numpy()[0, 1, :, 0] == 0)
+    assert np.all(got_c[0, 1, :, 0] == 0) and np.all(got_s[0, 1, :, 0] == 0)
 
 
 def test_int8_append_error_contract(lib, cuda_device, tables):
@@ -149,19 +152,18 @@ def test_int8_append_error_contract(lib, cuda_device, tables):
     bt = np.array([[0, 1], [2, 9]], np.int32)      # page 9 does not exist
     k, v, q = rand_bits(4010, (4, 8, 64)), rand_bits(4011, (4, 8, 64)), rand_bits(4012, (4, 32, 64))
     pos, seqs = np.array([3, 20, 0, 40], np.int32), np.array([0, 1, 5, 0], np.int32)
-    c_d, s_d = dev_pools(codes0, scales0, dev)
+    pool_d = dev_pool(codes0, scales0, dev)
     q_out = torch.full((4, 32, 64), 1.0, dtype=torch.bfloat16, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     lib.kv_append_rope_int8(to_dev_bf16(k, dev), to_dev_bf16(v, dev), to_dev_i32(pos, dev),
-                            to_dev_i32(bt, dev), c_d, s_d, cos_d[:32], sin_d[:32],
+                            to_dev_i32(bt, dev), pool_d, cos_d[:32], sin_d[:32],
                             token_seq=to_dev_i32(seqs, dev), q_in=to_dev_bf16(q, dev), q_out=q_out,
                             d_err=err)
     assert lib.pkv_read_device_error(err) == lib.ERR_DEVICE_INDEX
     want_c, want_s, want_q, e = OI.append_rope_int8(codes0, scales0, k, v, pos, seqs, bt,
                                                     cos_o[:32], sin_o[:32], q)
     assert e
-    assert np.array_equal(c_d.cpu().numpy(), want_c)
-    assert np.array_equal(f32_bits(s_d.cpu().numpy()), f32_bits(want_s))
+    assert same_pool(pool_d, want_c, want_s)
     assert np.array_equal(bits(q_out), want_q)
 
 
@@ -172,9 +174,10 @@ def edge_case_int8():
     NaN / +Inf scales in every unused tail slot."""
     case, _, q = edge_case()
     codes, scales = OI.quantize_pool(W.bf16_bits(W.fill_pool(case)))
-    st = torch.from_numpy(scales)
-    W.garbage_fill_unused_int8(st, case, 0)
-    return case, codes, st.numpy(), q
+    pool = torch.from_numpy(OI.pack_pages(codes, scales))
+    W.garbage_fill_unused_int8(pool, case, 0)
+    codes, scales = OI.unpack_pages(pool.numpy())
+    return case, codes, scales, q
 
 
 def test_int8_decode_edge_lengths_and_tail_garbage(lib, cuda_device):
@@ -270,17 +273,16 @@ def test_int8_append_then_decode_matches_oracle(lib, cuda_device, tables):
     k, v = rand_bits(4020, (T, 8, 64)), rand_bits(4021, (T, 8, 64))
     q = rand_bits(4022, (len(lens), 32, 64))
     codes0, scales0 = OI.new_pools(case.num_pages)
-    c_d, s_d = dev_pools(codes0, scales0, dev)
+    pool_d = dev_pool(codes0, scales0, dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     lib.kv_append_rope_int8(to_dev_bf16(k, dev), to_dev_bf16(v, dev), to_dev_i32(pos, dev),
-                            to_dev_i32(bt, dev), c_d, s_d, cos_d, sin_d,
+                            to_dev_i32(bt, dev), pool_d, cos_d, sin_d,
                             token_seq=to_dev_i32(seqs, dev), d_err=err)
     want_c, want_s, _, e = OI.append_rope_int8(codes0, scales0, k, v, pos, seqs, bt, cos_o, sin_o)
     assert not e and lib.pkv_read_device_error(err) == 0
-    assert np.array_equal(c_d.cpu().numpy(), want_c)
-    assert np.array_equal(f32_bits(s_d.cpu().numpy()), f32_bits(want_s))
+    assert same_pool(pool_d, want_c, want_s)
     out = torch.empty((len(lens), 32, 64), dtype=torch.bfloat16, device=dev)
-    lib.paged_gqa_decode_int8(to_dev_bf16(q, dev), c_d, s_d, to_dev_i32(bt, dev),
+    lib.paged_gqa_decode_int8(to_dev_bf16(q, dev), pool_d, to_dev_i32(bt, dev),
                               to_dev_i32(lens, dev), out, 0.125, d_err=err)
     assert lib.pkv_read_device_error(err) == 0
     ref, _ = OI.decode_int8(q, want_c, want_s, bt, lens, 0.125)
@@ -293,7 +295,7 @@ def full_size_int8_check(lib, dev, case, samples, tables):
     """One bench-shaped INT8 step on every layer (append of the new token with q
     rotation, then decode) and sampled (layer, seq) outputs against the oracle."""
     cos_d, sin_d, cos_o, sin_o = tables
-    codes, scales = W.fill_pool_int8(case, device=dev)
+    pool = W.fill_pool_int8(case, device=dev)
     q_raw = W.fill_queries(case, device=dev)
     k_new, v_new = W.fill_new_kv(case, device=dev)
     pos = W.new_positions(case)
@@ -304,15 +306,15 @@ def full_size_int8_check(lib, dev, case, samples, tables):
     for (l, s) in samples:
         ids = case.block_tables[l, s][case.block_tables[l, s] >= 0]
         idx = torch.from_numpy(ids).to(dev).long()
-        pre[(l, s)] = (ids, codes[idx].cpu().numpy(), scales[idx].cpu().numpy())
+        pre[(l, s)] = (ids,) + OI.unpack_pages(pool[idx].cpu().numpy())
     q_rot = torch.empty_like(q_raw)
     out = torch.empty_like(q_raw)
     ws = lib.alloc_workspace(case.num_seqs, dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     for l in range(case.num_layers):
-        lib.kv_append_rope_int8(k_new[l], v_new[l], posd, bt_all[l], codes, scales, cos_d, sin_d,
+        lib.kv_append_rope_int8(k_new[l], v_new[l], posd, bt_all[l], pool, cos_d, sin_d,
                                 q_in=q_raw[l], q_out=q_rot[l], d_err=err)
-        lib.paged_gqa_decode_int8(q_rot[l], codes, scales, bt_all[l], lens, out[l], case.scale,
+        lib.paged_gqa_decode_int8(q_rot[l], pool, bt_all[l], lens, out[l], case.scale,
                                   workspace=ws, max_seq_len=case.max_seq_len, d_err=err)
     assert lib.pkv_read_device_error(err) == 0
     for (l, s) in samples:
@@ -325,8 +327,7 @@ def full_size_int8_check(lib, dev, case, samples, tables):
                                                         bt_local, cos_o, sin_o, qb)
         assert not e
         idx = torch.from_numpy(ids).to(dev).long()
-        assert np.array_equal(codes[idx].cpu().numpy(), want_c), f"codes of layer {l} seq {s}"
-        assert np.array_equal(f32_bits(scales[idx].cpu().numpy()), f32_bits(want_s))
+        assert same_pool(pool[idx], want_c, want_s), f"pages of layer {l} seq {s}"
         assert np.array_equal(bits(q_rot[l, s:s + 1]), want_q)
         ref, _ = OI.decode_int8(want_q, want_c, want_s, bt_local, case.seq_lens[s:s + 1], case.scale)
         check_close_int8(bf16_to_f64(out[l, s:s + 1]), ref, f"int8 layer {l} seq {s}")

@@ -158,9 +158,12 @@ def fill_pool(case: DecodeCase, device="cpu", chunk_pages: int = 8192) -> torch.
     return pool
 
 
-def fill_pool_int8(case: DecodeCase, device="cpu", chunk_pages: int = 8192):
-    """INT8 pages for the same geometry: (codes int8 [N][2][8][16][64],
-    scales float32 [N][2][8][16]).
+I8_BLOCK_BYTES = 2 * PAGE_TOKENS * HEAD_DIM + 2 * PAGE_TOKENS * 4   # 2176
+
+
+def fill_pool_int8(case: DecodeCase, device="cpu", chunk_pages: int = 8192) -> torch.Tensor:
+    """An INT8 pool for the same geometry: uint8 [N][8][2176], per (page, KV
+    head) K codes [16][64], V codes [16][64], K scales [16], V scales [16].
 
     Codes are N(0, 42^2) samples rounded and clipped to [-127, 127] and
     scales uniform on [0.015, 0.025) -- about max|x| / 127 for rows of 64
@@ -171,15 +174,8 @@ def fill_pool_int8(case: DecodeCase, device="cpu", chunk_pages: int = 8192):
     """
     gen = torch.Generator(device=device).manual_seed(case.seed + 5000)
     N = case.num_pages
-    codes = torch.empty((N, 2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM), dtype=torch.int8, device=device)
-    scales = torch.empty((N, 2, NUM_KV_HEADS, PAGE_TOKENS), dtype=torch.float32, device=device)
-    for p0 in range(0, N, chunk_pages):
-        p1 = min(N, p0 + chunk_pages)
-        g = torch.randn((p1 - p0, 2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM), generator=gen,
-                        device=device)
-        codes[p0:p1] = (g * 42.0).round().clamp(-127, 127).to(torch.int8)
-        scales[p0:p1] = 0.015 + 0.01 * torch.rand((p1 - p0, 2, NUM_KV_HEADS, PAGE_TOKENS),
-                                                  generator=gen, device=device)
+    scales = 0.015 + 0.01 * torch.rand((N, 2, NUM_KV_HEADS, PAGE_TOKENS), generator=gen,
+                                       device=device)
     if case.outlier_frac > 0:
         n_vec = N * NUM_KV_HEADS * PAGE_TOKENS
         n_out = int(round(case.outlier_frac * n_vec))
@@ -187,20 +183,31 @@ def fill_pool_int8(case: DecodeCase, device="cpu", chunk_pages: int = 8192):
         page, vec = idx // (NUM_KV_HEADS * PAGE_TOKENS), idx % (NUM_KV_HEADS * PAGE_TOKENS)
         sv = scales.view(N, 2, NUM_KV_HEADS * PAGE_TOKENS)
         sv[page, 0, vec] = sv[page, 0, vec] * 8
-    return codes, scales
+    pool = torch.empty((N, NUM_KV_HEADS, I8_BLOCK_BYTES), dtype=torch.uint8, device=device)
+    for p0 in range(0, N, chunk_pages):
+        p1 = min(N, p0 + chunk_pages)
+        g = torch.randn((p1 - p0, 2, NUM_KV_HEADS, PAGE_TOKENS * HEAD_DIM), generator=gen,
+                        device=device)
+        codes = (g * 42.0).round().clamp(-127, 127).to(torch.int8).view(torch.uint8)
+        pool[p0:p1, :, 0:1024] = codes[:, 0]
+        pool[p0:p1, :, 1024:2048] = codes[:, 1]
+        sc = scales[p0:p1].contiguous().view(torch.uint8)          # [n][2][8][64] bytes
+        pool[p0:p1, :, 2048:2112] = sc[:, 0]
+        pool[p0:p1, :, 2112:2176] = sc[:, 1]
+    return pool
 
 
-def garbage_fill_unused_int8(scales: torch.Tensor, case: DecodeCase, layer: int) -> None:
+def garbage_fill_unused_int8(pool: torch.Tensor, case: DecodeCase, layer: int) -> None:
     """Overwrite the scales of the unused tail slots of each sequence's last
     page with NaN / +Inf bits (codes are finite whatever their bits)."""
-    bits = scales.view(torch.int32)
     for s in range(case.num_seqs):
         n = int(case.seq_lens[s])
         if n % PAGE_TOKENS == 0 or n == 0:
             continue
         page = int(case.block_tables[layer, s, n // PAGE_TOKENS])
-        bits[page, 0, :, n % PAGE_TOKENS:] = 0x7FC00000   # NaN
-        bits[page, 1, :, n % PAGE_TOKENS:] = 0x7F800000   # +Inf
+        words = pool[page].view(torch.int32)                      # [8][544]
+        words[:, 512 + n % PAGE_TOKENS:512 + PAGE_TOKENS] = 0x7FC00000   # K scales: NaN
+        words[:, 528 + n % PAGE_TOKENS:528 + PAGE_TOKENS] = 0x7F800000   # V scales: +Inf
 
 
 def fill_queries(case: DecodeCase, device="cpu") -> torch.Tensor:
