@@ -779,6 +779,13 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// 2^x by the hardware approximation (results below 2^-126 flush to zero):
+// ex2(0) is 1 and ex2(-inf) is 0, so no special cases are needed here.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 // 2^k as a float for a biased exponent k clamped to the normal range.
 __device__ __forceinline__ float pow2_biased(int k) {
   return __int_as_float(min(max(k, 1), 254) << 23);
@@ -900,23 +907,26 @@ struct MmaI8State {
     vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 2));
     const float mn = fmaxf(m, pm);
     const int evn = vm > 0.f ? (__float_as_int(vm) >> 23) : ev;  // O's unit from this unit on
-    const float a_soft = (m == mn) ? 1.f : exp2f(m - mn);
+    // (mn is finite: every unit has a live token; m - mn is -inf on the first unit)
+    const float a_soft = ex2_approx(m - mn);
     const float alpha = a_soft * pow2_biased(127 + ev - evn);
     const float vinv = pow2_biased(254 - evn);  // 2^-(evn - 127)
     float pr[4 * kP];
     float lsum = 0.f;
 #pragma unroll
     for (int i = 0; i < 4 * kP; ++i) {
-      pr[i] = (x[i] == mn) ? 1.f : exp2f(x[i] - mn);
+      pr[i] = ex2_approx(x[i] - mn);
       lsum += pr[i];
     }
     l = l * a_soft + lsum;
     m = mn;
     ev = evn;
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {  // most units change neither max nor unit
 #pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      o[n][0] *= alpha;
-      o[n][1] *= alpha;
+      for (int n = 0; n < 8; ++n) {
+        o[n][0] *= alpha;
+        o[n][1] *= alpha;
+      }
     }
     // ---- O += P' V, per page ---------------------------------------------
 #pragma unroll
