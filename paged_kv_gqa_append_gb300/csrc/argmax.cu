@@ -7,8 +7,9 @@
 // each reducing one contiguous part; the parts' results meet in the first
 // CTA's shared memory (distributed shared memory) after a cluster barrier.
 // Many rows: one CTA per row.  Inside a CTA each thread keeps the best
-// (value, index) of a strided share (16-byte streaming loads when the part is
-// 16-byte aligned); warp shuffles, then one shared-memory round, reduce the
+// (value, index) of a strided share (16-byte streaming loads, four in flight,
+// when the part is 16-byte aligned); warp shuffles, then one shared-memory
+// round, reduce the
 // pairs under the same total order (larger value first, then lower index,
 // NaN last), which is associative and commutative, so the result does not
 // depend on the reduction order.
@@ -23,7 +24,8 @@
 namespace pkv {
 namespace {
 
-constexpr int kArgThreads = 256;
+constexpr int kArgThreads = 512;
+static_assert(kArgThreads % 64 == 0 && kArgThreads <= 1024, "warps reduced by one warp");
 constexpr int kClusterCtas = 8;
 
 // (v, i) before (bv, bi)?  bi < 0 marks "nothing yet"; a NaN never wins.
@@ -40,8 +42,22 @@ __device__ __forceinline__ void take(float v, int i, float& bv, int& bi) {
   }
 }
 
+// Four consecutive elements starting at index `base`, later in this thread's
+// share than everything it has seen: their largest non-NaN value m (fmaxf
+// ignores a NaN operand) replaces the best only if it is strictly larger --
+// an equal value seen before has the lower index -- or if nothing non-NaN
+// was seen yet; then the first of the four equal to m is the index.
+__device__ __forceinline__ void take4(const float4& v, int base, float& bv, int& bi) {
+  const float m = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+  if (bi < 0 ? m == m : m > bv) {
+    bi = base + (v.x == m ? 0 : v.y == m ? 1 : v.z == m ? 2 : 3);
+    bv = m;
+  }
+}
+
 // Best (value, index) of elements [lo, hi) of `row`, reduced over the CTA;
-// valid in thread 0.
+// valid in thread 0.  Each thread walks its share in increasing index order,
+// four 16-byte loads in flight at a time.
 __device__ void cta_best(const float* __restrict__ row, int lo, int hi, float& bv, int& bi) {
   bv = 0.f;
   bi = -1;
@@ -49,15 +65,15 @@ __device__ void cta_best(const float* __restrict__ row, int lo, int hi, float& b
   if (((reinterpret_cast<uintptr_t>(row + lo)) & 15u) == 0) {
     const int n4 = (hi - lo) / 4;
     const float4* r4 = reinterpret_cast<const float4*>(row + lo);
-#pragma unroll 4
-    for (int k = threadIdx.x; k < n4; k += kArgThreads) {
-      const float4 v = __ldcs(r4 + k);
-      const int base = lo + 4 * k;
-      take(v.x, base, bv, bi);
-      take(v.y, base + 1, bv, bi);
-      take(v.z, base + 2, bv, bi);
-      take(v.w, base + 3, bv, bi);
+    int k = threadIdx.x;
+    for (; k + 3 * kArgThreads < n4; k += 4 * kArgThreads) {
+      float4 a[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a[u] = __ldcs(r4 + k + u * kArgThreads);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) take4(a[u], lo + 4 * (k + u * kArgThreads), bv, bi);
     }
+    for (; k < n4; k += kArgThreads) take4(__ldcs(r4 + k), lo + 4 * k, bv, bi);
     i = lo + 4 * n4 + threadIdx.x;
   }
   for (; i < hi; i += kArgThreads) take(__ldcs(row + i), i, bv, bi);
@@ -79,7 +95,7 @@ __device__ void cta_best(const float* __restrict__ row, int lo, int hi, float& b
     bv = lane < kArgThreads / 32 ? sv[lane] : 0.f;
     bi = lane < kArgThreads / 32 ? si[lane] : -1;
 #pragma unroll
-    for (int o = 4; o > 0; o >>= 1) {
+    for (int o = kArgThreads / 64; o > 0; o >>= 1) {
       const float ov = __shfl_down_sync(0xffffffffu, bv, o);
       const int oi = __shfl_down_sync(0xffffffffu, bi, o);
       take(ov, oi, bv, bi);
