@@ -344,6 +344,27 @@ struct TcSmem {
   static constexpr int kBytes = kTmemSlot + 8;
 };
 
+// (y0, y1) = (a0 * b + c, a1 * b + c) by one packed fp32 FMA, each rounded once.
+__device__ __forceinline__ void fma2(float a0, float a1, float b, float c, float& y0, float& y1) {
+  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 b, {%4, %4};\n\t"
+      "mov.b64 c, {%5, %5};\n\t"
+      "fma.rn.f32x2 d, a, b, c;\n\t"
+      "mov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// (s0, s1) += (e0, e1) by one packed fp32 add.
+__device__ __forceinline__ void add2(float& s0, float& s1, float e0, float e1) {
+  asm("{\n\t.reg .b64 s, e;\n\t"
+      "mov.b64 s, {%0, %1};\n\t"
+      "mov.b64 e, {%2, %3};\n\t"
+      "add.rn.f32x2 s, s, e;\n\t"
+      "mov.b64 {%0, %1}, s;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(e0), "f"(e1));
+}
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -594,17 +615,20 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         l_run *= alpha;
       }
       if (grow) m_used = mx;
-      // weights rounded to bf16, packed two per column (even key low), and
-      // their sum as rounded; a row with nothing visible yet keeps
-      // m_used = -inf and gets zeros
+      // weights 2^(x sl2 - m_used) (two per packed fp32 FMA), rounded to bf16
+      // and packed two per column (even key low); their fp32 sum (two per
+      // packed add); a row with nothing visible yet keeps m_used = -inf and
+      // gets zeros
       const float nm = m_used == -INFINITY ? 0.f : -m_used;
       uint32_t pk[32];
       float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        pk[c] = pack_bf16x2(ex2_approx(fmaf(v[2 * c], p.sl2, nm)), ex2_approx(fmaf(v[2 * c + 1], p.sl2, nm)));
-        ls0 += __uint_as_float(pk[c] << 16);
-        ls1 += __uint_as_float(pk[c] & 0xFFFF0000u);
+        float y0, y1;
+        fma2(v[2 * c], v[2 * c + 1], p.sl2, nm, y0, y1);
+        const float e0 = ex2_approx(y0), e1 = ex2_approx(y1);
+        pk[c] = pack_bf16x2(e0, e1);
+        add2(ls0, ls1, e0, e1);
       }
       l_run += ls0 + ls1;
       tmem_st32_nowait(tmem + lane_base + 64 * sb, pk);
