@@ -18,6 +18,8 @@ to check by eye, in FP64 NumPy with per-element loops where that is clearer:
 * ``int8_kv``    INT8 K/V pages: per-row symmetric 8-bit codes with fp32
                  scales, the quantised append, and decode over the
                  dequantised pages.
+* ``argmax``     next-token selection over FP32 logits (first index of the
+                 largest non-NaN value).
 * ``admission``  the admission-credit rule and a FIFO continuous-batching
                  simulation with on-demand page allocation.
 
@@ -37,4 +39,4 @@ Sources (titles of the pages that define the path):
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 (closed forms, invariants, brute force, library routines); none is unpinned.
 """
-from . import admission, bf16, int8_kv, paged_kv, rope  # noqa: F401
+from . import admission, argmax, bf16, int8_kv, paged_kv, rope  # noqa: F401
