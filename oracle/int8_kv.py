@@ -214,3 +214,43 @@ def unpack_pages(pool_bytes):
         scales[:, kv] = b[:, :, 2048 + 64 * kv:2048 + 64 * (kv + 1)].copy().view('<f4').reshape(
             N, NUM_KV_HEADS, PAGE_TOKENS)
     return codes, scales
+
+
+def decode_step_int8(codes, scales, q_bits, k_bits, v_bits, block_tables, seq_lens, cos, sin,
+                     scale: float):
+    """One decode step on INT8 pages: append each sequence's new token, then attend.
+
+    The rules of ``paged_kv.decode_step`` with the INT8 append and decode: for
+    sequence s with n = seq_lens[s], n == 0 does nothing (zero output and
+    rotated query); n < 0 or n beyond the RoPE table or 16 * max_blocks
+    raises the flag and does nothing; otherwise q is rotated at n - 1, the
+    token (k, v) is appended at n - 1 by ``append_rope_int8`` (nothing written
+    and the flag raised if that page is outside the pool), and attention
+    covers [0, n) (zero output and the flag for a bad needed page).
+    Returns (codes', scales', q_rot bits [S][32][64], out float64 [S][32][64], err).
+    """
+    S = q_bits.shape[0]
+    lens = np.asarray(seq_lens)
+    max_len = min(cos.shape[0], PAGE_TOKENS * block_tables.shape[1])
+    q_rot = np.zeros_like(q_bits)
+    out = np.zeros((S, NUM_Q_HEADS, HEAD_DIM))
+    err = False
+    valid = []
+    for s in range(S):
+        n = int(lens[s])
+        if n == 0:
+            continue
+        if n < 0 or n > max_len:
+            err = True
+            continue
+        valid.append(s)
+        for h in range(NUM_Q_HEADS):
+            q_rot[s, h] = rope.rotate_bf16(q_bits[s, h], cos[n - 1], sin[n - 1])
+        codes, scales, _, e = append_rope_int8(codes, scales, k_bits[s:s + 1], v_bits[s:s + 1],
+                                               [n - 1], [s], block_tables, cos, sin)
+        err |= e
+    for s in valid:
+        o, e = decode_int8(q_rot[s:s + 1], codes, scales, block_tables[s:s + 1], [int(lens[s])], scale)
+        err |= e
+        out[s] = o[0]
+    return codes, scales, q_rot, out, err

@@ -298,3 +298,44 @@ def test_pack_unpack_round_trip():
     scales = rng.standard_normal((5, 2, 8, 16)).astype(np.float32)
     c2, s2 = I.unpack_pages(I.pack_pages(codes, scales))
     assert np.array_equal(c2, codes) and np.array_equal(s2.view(np.uint32), scales.view(np.uint32))
+
+
+def test_decode_step_int8_is_append_then_decode():
+    """The INT8 step equals the two-call composition when every index is
+    valid, and isolates a bad sequence (zero output, flag) when one is not."""
+    rng = np.random.default_rng(31)
+    lens = np.array([1, 16, 17, 0, 50], np.int32)
+    pool, bt, q = random_paged(rng, lens, extra_pages=4)
+    codes, scales = I.quantize_pool(pool)
+    k, v = rand_bits(rng, (5, 8, 64)), rand_bits(rng, (5, 8, 64))
+    cos, sin = rope.table(rope.inv_freq_llama3(), 64)
+    c1, s1, qr, out, err = I.decode_step_int8(codes, scales, q, k, v, bt, lens, cos, sin, 0.125)
+    assert not err
+    live = np.nonzero(lens)[0]
+    c2, s2, qr2, e2 = I.append_rope_int8(codes, scales, k[live], v[live], lens[live] - 1, live, bt,
+                                         cos, sin, q[live])
+    assert not e2 and np.array_equal(c1, c2) and np.array_equal(s1, s2)
+    assert np.array_equal(qr[live], qr2)
+    assert np.all(qr[3] == 0) and np.all(out[3] == 0)
+    qf = np.zeros_like(q)
+    qf[live] = qr2
+    ref, _ = I.decode_int8(qf, c2, s2, bt, lens, 0.125)
+    assert np.array_equal(out, ref)
+    # the rotated query is the bf16 step's, and the new token's row is the
+    # quantised image of the bf16 step's row
+    p1, qb, _, _ = P.decode_step(pool, q, k, v, bt, lens, cos, sin, 0.125)
+    assert np.array_equal(qb, qr)
+    cq, sq = I.quantize_pool(p1)
+    for s in live:
+        page, slot = bt[s, (lens[s] - 1) // 16], (lens[s] - 1) % 16
+        assert np.array_equal(c1[page, :, :, slot], cq[page, :, :, slot])
+        assert np.array_equal(s1[page, :, :, slot], sq[page, :, :, slot])
+    # a length past the 64-entry table: that sequence only is rejected
+    lens_bad = lens.copy()
+    lens_bad[4] = 65
+    bt_big = bt.copy()
+    bt_big[4, 4] = bt[4, 3]
+    _, _, qr3, out3, err3 = I.decode_step_int8(codes, scales, q, k, v, bt_big, lens_bad, cos, sin,
+                                               0.125)
+    assert err3 and np.all(out3[4] == 0) and np.all(qr3[4] == 0)
+    assert np.array_equal(out3[:3], out[:3])
