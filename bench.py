@@ -519,9 +519,11 @@ def run_gb300(args, world, rank, local):
 # ---------------------------------------------------------- INT8 pages ----
 
 def run_int8_line(args, world, rank, local):
-    """The decode step on INT8 K/V pages: per layer kv_append_rope_int8 (new
-    token quantised into its page, q rotated) then paged_gqa_decode_int8, one
-    CUDA graph per step.  KV bytes per (token, head): 136 (codes and scales)."""
+    """The decode step on INT8 K/V pages: per layer one fused kernel
+    (paged_gqa_decode_append_int8: new token quantised into its page, q
+    rotated, attention), or with --unfused kv_append_rope_int8 then
+    paged_gqa_decode_int8; one CUDA graph per step.  KV bytes per (token,
+    head): 136 (codes and scales)."""
     import paged_kv_gqa_append_gb300 as pkv
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
@@ -537,7 +539,7 @@ def run_int8_line(args, world, rank, local):
     out = torch.empty_like(q_raw)
     kv_bytes_layer = int(case.seq_lens.sum()) * W.NUM_KV_HEADS * INT8_ROW_BYTES
     step = pkv.Int8DecodeStep(pool, bt, lens, pos, k_new, v_new, q_raw, out, cos, sin,
-                              case.scale, max_seq_len=case.max_seq_len)
+                              case.scale, max_seq_len=case.max_seq_len, fused=not args.unfused)
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
         step.run()
@@ -562,13 +564,16 @@ def run_int8_line(args, world, rank, local):
     barrier(world)
     if step.error() != 0:
         raise RuntimeError("device error in the INT8 timed region")
-    # the decode kernel alone (dominant) and the append kernel alone
+    # the dominant kernel: the fused kernel is the step's only kernel (timed
+    # over the headline region); else the decode kernel alone.  And the
+    # append kernel alone.
     g_dec, g_app = step.partial_graph(False, True), step.partial_graph(True, False)
     for _ in range(3):
         g_dec.replay()
         g_app.replay()
     k_part = max(10, args.steps // 4)
-    dec_avg_ms = timed(g_dec.replay, k_part) / (k_part * L)
+    dec_only_ms = timed(g_dec.replay, k_part) / (k_part * L)
+    dec_avg_ms = ms / (args.steps * L) if step.fused else dec_only_ms
     append_us = timed(g_app.replay, k_part) * 1e3 / (k_part * L)
     if step.error() != 0:
         raise RuntimeError("device error in the INT8 kernel timings")
@@ -605,12 +610,15 @@ def run_int8_line(args, world, rank, local):
 
     peak, peak_kind = hbm_peak()
     achieved = kv_bytes_layer / (dec_avg_ms / 1e3) / 1e9
-    tag = "paged_decode_int8"
+    tag = "paged_decode_append_int8" if step.fused else "paged_decode_int8"
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "traffic": ncu_traffic(f"{tag}:{case.name}"),
             "peak_source": peak_kind,
-            "kernel": f"{tag} (paged_gqa_decode_int8: decode-only graph, one launch per layer)",
-            "launches_timed": k_part * L, "algorithmic_bytes_per_launch": kv_bytes_layer,
+            "kernel": (f"{tag} (paged_gqa_decode_append_int8: the step's only kernel, one launch "
+                       "per layer, timed over the headline region)" if step.fused else
+                       f"{tag} (paged_gqa_decode_int8: decode-only graph, one launch per layer)"),
+            "launches_timed": (args.steps if step.fused else k_part) * L,
+            "algorithmic_bytes_per_launch": kv_bytes_layer,
             "avg_launch_us": dec_avg_ms * 1e3}
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -632,9 +640,11 @@ def run_int8_line(args, world, rank, local):
                                     "MMAs, fp32 accumulation",
                        "l2": "inputs larger than L2 (pool read per step exceeds 129 MB L2)",
                        "parallelism": f"replicas x{world}",
-                       "launch": "CUDA graph of the step: INT8 append kernel + INT8 decode kernel per layer"},
+                       "launch": ("CUDA graph of the step: one fused INT8 append+decode kernel per layer"
+                                  if step.fused else
+                                  "CUDA graph of the step: INT8 append kernel + INT8 decode kernel per layer")},
             "tokens_per_s": S * steps * world / sec, "us_per_layer": ms * 1e3 / (steps * L),
-            "decode_us_per_layer": dec_avg_ms * 1e3, "append_us_per_layer": append_us,
+            "decode_only_us_per_layer": dec_only_ms * 1e3, "append_us_per_layer": append_us,
             "kv_bytes_per_step": kv_bytes_layer * L, "hbm_frac_step": value / world / peak,
             "clocks": clk, "e2e": e2e, "gpu_launches": step.launches_per_step * steps,
             "roofline": roof, "cpu_baseline": cpu}), flush=True)

@@ -354,6 +354,23 @@ int paged_gqa_decode_int8_ex(const void* q, const void* kv_pool, int num_pages,
                              void* workspace, size_t workspace_bytes,
                              int* d_err, void* stream, const pkv_decode_opts* opts);
 
+/* paged_gqa_decode_append on INT8 pages: for sequence s with n = seq_lens[s]
+ * its new token (k_new[s], v_new[s]) is rotated and quantised exactly as
+ * kv_append_rope_int8 does and written at position n - 1, q is rotated there
+ * (into q_out when given), and attention covers [0, n) including the new
+ * token -- one kernel.  Arguments, error rules and the early_kv option as
+ * paged_gqa_decode_append, with kv_pool the INT8 pool; opts may be NULL, and
+ * otherwise must select the default configuration (warps 0 or 16, stages 0
+ * or 2, compute PKV_COMPUTE_TENSOR, schedule and combine 0). */
+int paged_gqa_decode_append_int8(const void* q, const void* k_new, const void* v_new,
+                                 const float* rope_cos, const float* rope_sin, int max_pos,
+                                 void* kv_pool, int num_pages,
+                                 const int32_t* block_tables, int bt_row_stride, int max_blocks,
+                                 const int32_t* seq_lens, int num_seqs, int max_seq_len,
+                                 void* q_out, void* out, float scale,
+                                 void* workspace, size_t workspace_bytes,
+                                 int* d_err, void* stream, const pkv_decode_opts* opts);
+
 /* ------------------------------------------------------------------------
  * paged_gqa_prefill - causal GQA attention of each sequence's newest tokens
  * over its own pages: a whole prompt, or a chunk of one after a cached

@@ -81,6 +81,8 @@ _SIGS = {
     "paged_gqa_decode_int8": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p, _p]),
     "paged_gqa_decode_int8_ex": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p, _p,
                                       ctypes.POINTER(DecodeOpts)]),
+    "paged_gqa_decode_append_int8": (_i, [_p, _p, _p, _p, _p, _i, _p, _i, _p, _i, _i, _p, _i, _i, _p,
+                                          _p, _f, _p, _sz, _p, _p, ctypes.POINTER(DecodeOpts)]),
     "pkv_read_device_error": (_i, [_p, _p, _i, _ip]),
     "pkv_credit_pages": (_i, [_i, _i, _i]),
     "pkv_sched_create": (_p, [_i, _i, _i, _i]),
@@ -392,6 +394,54 @@ def paged_gqa_decode_int8(q, kv_pool, block_tables, seq_lens, out, scale, worksp
     _check(st, "paged_gqa_decode_int8")
 
 
+def paged_gqa_decode_append_int8(q, k_new, v_new, kv_pool, block_tables, seq_lens, out, rope_cos,
+                                 rope_sin, scale, q_out=None, workspace=None, max_seq_len=None,
+                                 d_err=None, max_blocks=None, min_units_per_warp=0, early_kv=0,
+                                 stream=None):
+    """paged_gqa_decode_append on INT8 pages: sequence s's new token (k_new[s],
+    v_new[s]) is quantised into its page at seq_lens[s] - 1 and q rotated
+    there, then attention over seq_lens[s] tokens -- one kernel."""
+    dev = kv_pool.device
+    _need_i8_pool(kv_pool, dev)
+    _need(q, "q", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
+    _need(out, "out", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
+    S = q.numel() // (NUM_Q_HEADS * HEAD_DIM)
+    if out.numel() != q.numel():
+        raise ValueError("out must match q")
+    _need(k_new, "k_new", torch.bfloat16, dev, (NUM_KV_HEADS, HEAD_DIM))
+    _need(v_new, "v_new", torch.bfloat16, dev, (NUM_KV_HEADS, HEAD_DIM))
+    if k_new.numel() != S * NUM_KV_HEADS * HEAD_DIM or v_new.numel() != k_new.numel():
+        raise ValueError("k_new/v_new must be [num_seqs, 8, 64]")
+    if q_out is not None:
+        _need(q_out, "q_out", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
+        if q_out.numel() != q.numel():
+            raise ValueError("q_out must match q")
+    _need(block_tables, "block_tables", torch.int32, dev)
+    if block_tables.dim() != 2 or block_tables.shape[0] < S:
+        raise ValueError("block_tables must be [>= num_seqs, row_stride]")
+    _need(seq_lens, "seq_lens", torch.int32, dev)
+    if seq_lens.numel() != S:
+        raise ValueError("seq_lens must have num_seqs entries")
+    _need(rope_cos, "rope_cos", torch.float32, dev, (ROPE_PAIRS,))
+    _need(rope_sin, "rope_sin", torch.float32, dev, (ROPE_PAIRS,))
+    stride = block_tables.shape[1]
+    mb = stride if max_blocks is None else max_blocks
+    if max_seq_len is None:
+        max_seq_len = PAGE_TOKENS * mb
+    if workspace is None:
+        workspace = alloc_workspace(S, dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    if d_err is not None:
+        _need(d_err, "d_err", torch.int32, dev)
+    opts = DecodeOpts(COMPUTE_TENSOR, min_units_per_warp, 0, 0, 0, 0, 0, early_kv)
+    st = _L().paged_gqa_decode_append_int8(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(rope_cos), _ptr(rope_sin), rope_cos.shape[0],
+        _ptr(kv_pool), kv_pool.shape[0], _ptr(block_tables), stride, mb, _ptr(seq_lens), S,
+        int(max_seq_len), _ptr(q_out), _ptr(out), float(scale), _ptr(workspace), workspace.numel(),
+        _ptr(d_err), _stream(stream), ctypes.byref(opts))
+    _check(st, "paged_gqa_decode_append_int8")
+
+
 def paged_gqa_decode_append(q, k_new, v_new, kv_pool, block_tables, seq_lens, out, rope_cos,
                             rope_sin, scale, q_out=None, workspace=None, max_seq_len=None,
                             d_err=None, max_blocks=None, warps_per_cta=0, min_units_per_warp=0,
@@ -691,8 +741,15 @@ class Int8DecodeStep:
         kv_append_rope_int8(k[l], v[l], positions, block_tables[l], kv_pool, cos, sin,
                             q_in=q[l], q_out=q_rot[l])
         paged_gqa_decode_int8(q_rot[l], kv_pool, block_tables[l], seq_lens, out[l], scale)
-    Tensors are bound at construction (refresh their contents in place and
-    call run()), as for DecodeStep.
+    By default (fused=True) each layer is one call
+        paged_gqa_decode_append_int8(q[l], k[l], v[l], kv_pool, block_tables[l],
+                                     seq_lens, out[l], cos, sin, q_out=q_rot[l])
+    which places token s at seq_lens[s] - 1 (positions unused); with
+    overlap_layers (the default) layer l >= 1 reads its tables and stages its
+    first pages before layer l - 1's kernel has finished, which requires the
+    layers' block tables to name disjoint pages.  Tensors are bound at
+    construction (refresh their contents in place and call run()), as for
+    DecodeStep.
 
         kv_pool [num_pages, 8, 2176] uint8 (see new_int8_pool)
         block_tables [L, S, max_blocks] int32;  seq_lens, positions [S] int32
@@ -701,8 +758,10 @@ class Int8DecodeStep:
 
     def __init__(self, kv_pool, block_tables, seq_lens, positions, k, v, q, out, rope_cos,
                  rope_sin, scale, max_seq_len=None, workspace=None, d_err=None, q_rot=None,
-                 use_graph=True, stream=None):
+                 use_graph=True, stream=None, fused=True, overlap_layers=True):
         self.L, self.S = block_tables.shape[0], block_tables.shape[1]
+        self.fused = bool(fused)
+        self.overlap = bool(overlap_layers)
         self.t = dict(pool=kv_pool, bt=block_tables, lens=seq_lens, pos=positions,
                       k=k, v=v, q=q, out=out, cos=rope_cos, sin=rope_sin)
         dev = kv_pool.device
@@ -711,7 +770,7 @@ class Int8DecodeStep:
         self.d_err = torch.zeros(1, dtype=torch.int32, device=dev) if d_err is None else d_err
         self.scale = float(scale)
         self.max_seq_len = max_seq_len
-        self.launches_per_step = 2 * self.L
+        self.launches_per_step = (1 if self.fused else 2) * self.L
         self._launch()                      # eager run: sets up kernels and descriptors
         torch.cuda.synchronize(dev)
         self.graph = None
@@ -722,6 +781,14 @@ class Int8DecodeStep:
 
     def _launch(self, append=True, decode=True):
         t = self.t
+        if self.fused and append and decode:
+            for l in range(self.L):
+                paged_gqa_decode_append_int8(t["q"][l], t["k"][l], t["v"][l], t["pool"], t["bt"][l],
+                                             t["lens"], t["out"][l], t["cos"], t["sin"], self.scale,
+                                             q_out=self.q_rot[l], workspace=self.workspace,
+                                             max_seq_len=self.max_seq_len, d_err=self.d_err,
+                                             early_kv=int(self.overlap and l > 0))
+            return
         for l in range(self.L):
             if append:
                 kv_append_rope_int8(t["k"][l], t["v"][l], t["pos"], t["bt"][l], t["pool"],

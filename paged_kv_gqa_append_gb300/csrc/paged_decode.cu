@@ -41,6 +41,7 @@
 #include "internal.h"
 #include "pkv.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 #include "rope.cuh"
 
 namespace pkv {
@@ -57,7 +58,7 @@ struct DecodeParams {
   const uint16_t* q;              // [S][32][64] bf16
   const int32_t* block_tables;    // [S][bt_stride]
   const int32_t* seq_lens;        // [S]
-  const uint8_t* pool_i8;         // INT8 pages: [num_pages][8][2176] bytes, else null
+  uint8_t* pool_i8;               // INT8 pages: [num_pages][8][2176] bytes, else null
   uint16_t* out;                  // [S][32][64] bf16
   int bt_stride, max_blocks, num_pages, num_seqs;
   float sl2;                      // scale * log2(e)
@@ -89,7 +90,7 @@ struct Record {
   float2* ml;
 };
 
-template <int kWarps, int kStages, int kStageB = kStageBytes>
+template <int kWarps, int kStages, int kStageB = kStageBytes, int kTokB = 0>
 struct SmemLayout {
   static_assert(kStages * kStageB >= kRecordBytes, "slot 1 lives in the warp's own stages");
   static constexpr int kTiles = kWarps * kStages * kStageB;
@@ -97,7 +98,8 @@ struct SmemLayout {
   static constexpr int kPid = kBars + kWarps * kStages * 8;            // int [kWarps][kStages]
   static constexpr int kCnt = kPid + kWarps * kStages * 4;             // int [kWarps + 1]
   static constexpr int kSlots = kCnt + (((kWarps + 1) * 4 + 15) / 16) * 16;  // Record [kWarps]
-  static constexpr int kPrefix = kSlots + kWarps * kRecordBytes;       // int [S + 1], then len [S]
+  static constexpr int kTok = kSlots + kWarps * kRecordBytes;          // per-warp new-token area
+  static constexpr int kPrefix = kTok + kWarps * kTokB;                 // int [S + 1], then len [S]
   static size_t bytes(int num_seqs) { return 1024 + kPrefix + 4 * (size_t)(2 * num_seqs + 1); }
   // Slot 0 (dedicated) holds the warp's record for a segment that began
   // before its range; slot 1 holds the record for a segment that runs past
@@ -358,9 +360,15 @@ struct MergeAcc {
 // (8 tiles), K = 16 tokens.  The C layout of S is the A layout of P, so the
 // probabilities never leave registers.
 // ---------------------------------------------------------------------------
+struct NewToken;
+template <int kP>
+struct NewTokenI8;
+
 // Stage contents of a bf16 page unit: the K tile then the V tile of one
 // (page, head), one 4-D TMA box with the 128-byte swizzle.
 struct Bf16Pages {
+  using Token = NewToken;
+  static constexpr int kTokenBytes = 0;  // the new token lives in registers
   static constexpr bool kBf16Pages = true;
   static constexpr int kPagesPerUnit = 1;
   static constexpr int kStageBytes = pkv::kStageBytes;
@@ -791,9 +799,40 @@ __device__ __forceinline__ float pow2_biased(int k) {
   return __int_as_float(min(max(k, 1), 254) << 23);
 }
 
+// Rotation of the q words of an INT8-page decode lane at position pos (dims d
+// and d + 32 sit in lanes c and c ^ 2 of a row), and their store to q_out
+// when `write_q`.  Kept out of line: it runs once per segment, and inlined
+// its temporaries would crowd the page loop's registers.
+__device__ __forceinline__ void rotate_q_i8(const DecodeParams& p, uint32_t (&w)[8], size_t row, int pos,
+                                         bool write_q, int lane) {
+  const int gq = lane >> 2, c = lane & 3;
+  const float* cr = p.rope_cos + (size_t)pos * PKV_ROPE_PAIRS + 16 * (c & 1);
+  const float* sr = p.rope_sin + (size_t)pos * PKV_ROPE_PAIRS + 16 * (c & 1);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t o = __shfl_xor_sync(0xffffffffu, w[k], 2);  // the partner dims (d +- 32)
+    if (gq < 4) {
+      const uint32_t x0 = c < 2 ? w[k] : o, x1 = c < 2 ? o : w[k];
+      const float2 cs = __ldg(reinterpret_cast<const float2*>(cr) + k);
+      const float2 sn = __ldg(reinterpret_cast<const float2*>(sr) + k);
+      uint16_t a0, b0, a1, b1;
+      rope_pair((uint16_t)(x0 & 0xFFFFu), (uint16_t)(x1 & 0xFFFFu), cs.x, sn.x, a0, b0);
+      rope_pair((uint16_t)(x0 >> 16), (uint16_t)(x1 >> 16), cs.y, sn.y, a1, b1);
+      w[k] = c < 2 ? ((uint32_t)a0 | ((uint32_t)a1 << 16)) : ((uint32_t)b0 | ((uint32_t)b1 << 16));
+    }
+  }
+  if (write_q && p.q_out != nullptr && gq < 4) {
+    uint4* dst = reinterpret_cast<uint4*>(p.q_out + row);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
 template <int kP>
 struct MmaI8State {
   static_assert(kP == 1 || kP == 2, "one or two pages per unit");
+  using Token = NewTokenI8<kP>;
+  static constexpr int kTokenBytes = 3 * 32 * 4;  // the new token's codes and scales, per warp
   static constexpr bool kBf16Pages = false;
   static constexpr int kPagesPerUnit = kP;
   static constexpr int kBlock = PKV_I8_BLOCK_BYTES;     // one (page, head): 2176 bytes
@@ -815,17 +854,22 @@ struct MmaI8State {
     if (two) bulk_load(dst + kBlock, p.pool_i8 + ((size_t)pid.y * PKV_NUM_KV_HEADS + g) * kBlock, kBlock, bar);
   }
 
+  // q rows of heads 4g..4g+3; with kAppend rotated at position `pos` first
+  // (dims d and d + 32 sit in lanes c and c ^ 2 of a row) and, when
+  // `write_q`, stored to q_out.
   template <bool kAppend>
-  __device__ __forceinline__ void load_q(const DecodeParams& p, int s, int g, int, bool, int lane) {
+  __device__ __forceinline__ void load_q(const DecodeParams& p, int s, int g, int pos, bool write_q,
+                                         int lane) {
     const int gq = lane >> 2, c = lane & 3;
     uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    const size_t row = ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + gq) * 64 + 16 * c;
     if (gq < 4) {  // words 8c .. 8c+7 of the row: dims 16c .. 16c+15
-      const uint4* src = reinterpret_cast<const uint4*>(
-          p.q + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + gq) * 64 + 16 * c);
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + row);
       const uint4 a = __ldg(src), b = __ldg(src + 1);
       w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
       w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
     }
+    if (kAppend) rotate_q_i8(p, w, row, pos, write_q, lane);
     // largest |q| of the group (4 heads) -> factor 2^(14 - e), 2^e <= max < 2^(e+1)
     uint32_t amax = 0u;
 #pragma unroll
@@ -1013,7 +1057,8 @@ struct NewToken {
   uint32_t v;
   float c, s;
 
-  __device__ __forceinline__ void load(const DecodeParams& p, int seq, int g, int pos, int lane) {
+  __device__ __forceinline__ void load(const DecodeParams& p, int seq, int g, int pos, int lane,
+                                       uint32_t = 0) {
     const uint16_t* kr = p.k_new + ((size_t)seq * PKV_NUM_KV_HEADS + g) * 64;
     k0 = __ldg(kr + lane);
     k1 = __ldg(kr + lane + 32);
@@ -1021,6 +1066,12 @@ struct NewToken {
               lane);
     c = __ldg(p.rope_cos + (size_t)pos * PKV_ROPE_PAIRS + lane);
     s = __ldg(p.rope_sin + (size_t)pos * PKV_ROPE_PAIRS + lane);
+  }
+
+  // The unit staged at sK holds the token's page: insert at position pos.
+  __device__ __forceinline__ void insert_at(const DecodeParams& p, uint32_t sK, int pid, int,
+                                            int g, int pos, int lane, uint32_t) const {
+    insert(p, sK, sK + kTileBytes, pid, g, pos % PKV_PAGE_TOKENS, lane);
   }
 
   __device__ __forceinline__ void insert(const DecodeParams& p, uint32_t sK, uint32_t sV, int pid,
@@ -1043,6 +1094,72 @@ struct NewToken {
     uint32_t* vg = reinterpret_cast<uint32_t*>(
         p.pool + ((((size_t)pid * 2 + 1) * PKV_NUM_KV_HEADS + g) * PKV_PAGE_TOKENS + slot) * 64);
     vg[lane] = v;
+  }
+};
+
+// Fused append on INT8 pages: the warp that owns a sequence's last unit
+// rotates the new token's K (rounded to bf16), quantises its K and V rows as
+// kv_append_rope_int8 does (lane l holds dims l and l + 32), and writes codes
+// and scales into the staged block of the token's page -- so its own
+// attention sees them -- and into the pool.
+template <int kP>
+struct NewTokenI8 {
+  // Nothing is held in registers, which the page loop needs: the token goes
+  // to the warp's area in shared memory, per lane the codes (K dims lane,
+  // lane + 32, V dims lane, lane + 32, one byte each), then the K scale, then
+  // the V scale.
+
+  __device__ __forceinline__ void load(const DecodeParams& p, int s, int g, int pos, int lane,
+                                    uint32_t area) {
+    const uint16_t* kr = p.k_new + ((size_t)s * PKV_NUM_KV_HEADS + g) * 64;
+    const uint16_t* vr = p.v_new + ((size_t)s * PKV_NUM_KV_HEADS + g) * 64;
+    const float c = __ldg(p.rope_cos + (size_t)pos * PKV_ROPE_PAIRS + lane);
+    const float sn = __ldg(p.rope_sin + (size_t)pos * PKV_ROPE_PAIRS + lane);
+    uint16_t r0, r1;
+    rope_pair(__ldg(kr + lane), __ldg(kr + lane + 32), c, sn, r0, r1);
+    int8_t k0, k1, v0, v1;
+    const float ks = quantize_pair(__uint_as_float((uint32_t)r0 << 16),
+                                   __uint_as_float((uint32_t)r1 << 16), k0, k1);
+    const float vs = quantize_pair(__uint_as_float((uint32_t)__ldg(vr + lane) << 16),
+                                   __uint_as_float((uint32_t)__ldg(vr + lane + 32) << 16), v0, v1);
+    const uint32_t codes = (uint32_t)(uint8_t)k0 | ((uint32_t)(uint8_t)k1 << 8) |
+                           ((uint32_t)(uint8_t)v0 << 16) | ((uint32_t)(uint8_t)v1 << 24);
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(area + 4u * lane), "r"(codes) : "memory");
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(area + 128u + 4u * lane), "f"(ks) : "memory");
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(area + 256u + 4u * lane), "f"(vs) : "memory");
+  }
+
+  // The unit staged at `base` (first page id `pid`) of sequence `seq` holds
+  // position pos.
+  __device__ __forceinline__ void insert_at(const DecodeParams& p, uint32_t base, int pid, int seq,
+                                            int g, int pos, int lane, uint32_t area) const {
+    const int lp = pos / PKV_PAGE_TOKENS, slot = pos % PKV_PAGE_TOKENS;
+    const int pg = kP == 2 ? (lp & 1) : 0;  // the token's page within the unit
+    const int page = pg == 0 ? pid : __ldg(p.block_tables + (size_t)seq * p.bt_stride + lp);
+    const uint32_t blk = base + (uint32_t)(PKV_I8_BLOCK_BYTES * pg);
+    uint8_t* gblk = p.pool_i8 + ((size_t)page * PKV_NUM_KV_HEADS + g) * PKV_I8_BLOCK_BYTES;
+    const uint32_t rk = (uint32_t)slot * 64, rv = 1024u + (uint32_t)slot * 64;
+    uint32_t codes;
+    float ks, vs;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(codes) : "r"(area + 4u * lane) : "memory");
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(ks) : "r"(area + 128u + 4u * lane) : "memory");
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(vs) : "r"(area + 256u + 4u * lane) : "memory");
+    const uint16_t k0 = codes & 0xFFu, k1 = (codes >> 8) & 0xFFu, v0 = (codes >> 16) & 0xFFu,
+                   v1 = codes >> 24;
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + rk + lane), "h"(k0) : "memory");
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + rk + lane + 32), "h"(k1) : "memory");
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + rv + lane), "h"(v0) : "memory");
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + rv + lane + 32), "h"(v1) : "memory");
+    gblk[rk + lane] = (uint8_t)k0;
+    gblk[rk + lane + 32] = (uint8_t)k1;
+    gblk[rv + lane] = (uint8_t)v0;
+    gblk[rv + lane + 32] = (uint8_t)v1;
+    if (lane == 0) {
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(blk + 2048u + 4u * slot), "f"(ks) : "memory");
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(blk + 2112u + 4u * slot), "f"(vs) : "memory");
+      reinterpret_cast<float*>(gblk + 2048)[slot] = ks;
+      reinterpret_cast<float*>(gblk + 2112)[slot] = vs;
+    }
   }
 };
 
@@ -1093,10 +1210,9 @@ __device__ __forceinline__ void cross_cta_merge(const DecodeParams& p, const Mer
 template <class State, int kWarps, int kStages, bool kAppend>
 __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
-  static_assert(!kAppend || State::kBf16Pages, "the fused append writes bf16 pages");
   constexpr int kStageB = State::kStageBytes;
   constexpr int kP = State::kPagesPerUnit;  // pages per unit (and per pipeline stage)
-  using Smem = SmemLayout<kWarps, kStages, kStageB>;
+  using Smem = SmemLayout<kWarps, kStages, kStageB, State::kTokenBytes>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -1176,13 +1292,15 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
     cursor_seek(cc, u0, prefix, S);
     st.reset();
     int seg_len = slen[cc.s];
-    NewToken tok;
+    typename State::Token tok;
+    // this warp's new-token area in shared memory (states that keep the token there)
+    auto tok_area = [&]() { return smem_u32(smem + Smem::kTok) + (uint32_t)(warp * State::kTokenBytes); };
     auto enter_segment = [&]() {
       const uint32_t base = seg_base(cc, prefix);
       // this warp rotates q (and stores it if it owns the segment's first
       // page) and, if it owns the last page, brings in the new token
       st.template load_q<kAppend>(p, cc.s, cc.g, seg_len - 1, base >= u0, lane);
-      if (kAppend && base + (uint32_t)cc.np - 1 < u1) tok.load(p, cc.s, cc.g, seg_len - 1, lane);
+      if (kAppend && base + (uint32_t)cc.np - 1 < u1) tok.load(p, cc.s, cc.g, seg_len - 1, lane, tok_area());
     };
     enter_segment();
     bool seg_bad = false;
@@ -1255,7 +1373,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
         const int valid = min(kP * PKV_PAGE_TOKENS, seg_len - kP * PKV_PAGE_TOKENS * cc.j);
         const uint32_t sK = tiles + stage * kStageB;
         if (kAppend && cc.j == cc.np - 1) {  // the page that receives the new token
-          tok.insert(p, sK, sK + kTileBytes, pid, cc.g, (seg_len - 1) % PKV_PAGE_TOKENS, lane);
+          tok.insert_at(p, sK, pid, cc.s, cc.g, seg_len - 1, lane, tok_area());
           __syncwarp();
         }
         st.page(sK, sK + State::kVOffset, valid, p.sl2, lane);
@@ -1887,7 +2005,8 @@ static long long whole_segment_grid(long long nc, int num_seqs, long long pages_
 template <class State, int kWarps, int kStages, bool kAppend = false>
 static int launch_decode(const DecodeParams& prm, const CUtensorMap& map, int device, int num_sms,
                          int max_seq_len, int min_units, int ctas_per_sm, cudaStream_t stream) {
-  const size_t smem = SmemLayout<kWarps, kStages, State::kStageBytes>::bytes(prm.num_seqs);
+  const size_t smem =
+      SmemLayout<kWarps, kStages, State::kStageBytes, State::kTokenBytes>::bytes(prm.num_seqs);
   constexpr int kP = State::kPagesPerUnit;
   int occ = 0;
   int rc = setup_kernel<State, kWarps, kStages, kAppend>(device, smem, &occ);
@@ -2036,13 +2155,13 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   const int cfg = warps * 100 + stages;
   // INT8 pages: static schedule, tensor cores, two pages per stage by default
   const int cfg8 = warps * 100 + ((opts && opts->stages > 0) ? opts->stages : 2);
-  if (int8 && (app || compute != PKV_COMPUTE_TENSOR || (opts && (opts->schedule == 1 || opts->combine == 1)) ||
-               (cfg8 != 1604 && cfg8 != 1602 && cfg8 != 804)))
+  if (int8 && (compute != PKV_COMPUTE_TENSOR || (opts && (opts->schedule == 1 || opts->combine == 1)) ||
+               (cfg8 != 1604 && cfg8 != 1602 && cfg8 != 804) || (app && cfg8 != 1602)))
     return PKV_ERR_INVALID_ARGUMENT;
   if (!int8 && compute == PKV_COMPUTE_TENSOR && cfg != 1602 && cfg != 1603 && cfg != 802 &&
       cfg != 804 && cfg != 402 && cfg != 404)
     return PKV_ERR_INVALID_ARGUMENT;
-  if (app && cfg != 1602 && cfg != 802 && cfg != 402) return PKV_ERR_INVALID_ARGUMENT;
+  if (!int8 && app && cfg != 1602 && cfg != 802 && cfg != 402) return PKV_ERR_INVALID_ARGUMENT;
 
   int dev = 0;
   int rc = bind_stream_device(stream, &dev);
@@ -2064,7 +2183,7 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   prm.q = static_cast<const uint16_t*>(q);
   prm.block_tables = block_tables;
   prm.seq_lens = seq_lens;
-  prm.pool_i8 = int8 ? static_cast<const uint8_t*>(kv_pool) : nullptr;
+  prm.pool_i8 = int8 ? static_cast<uint8_t*>(const_cast<void*>(kv_pool)) : nullptr;
   prm.out = static_cast<uint16_t*>(out);
   prm.bt_stride = bt_row_stride;
   prm.max_blocks = max_blocks;
@@ -2092,6 +2211,7 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int ms = max_seq_len;
   if (int8) {  // stages 2: two pages per stage; stages 4: one page per stage
+    if (app) return launch_decode<MmaI8State<2>, 16, 2, true>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
     switch (cfg8) {
       case 1604: return launch_decode<MmaI8State<1>, 16, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
       case 804: return launch_decode<MmaI8State<1>, 8, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
@@ -2157,6 +2277,20 @@ extern "C" int paged_gqa_decode(const void* q, const void* kv_pool, int num_page
   return paged_gqa_decode_ex(q, kv_pool, num_pages, block_tables, bt_row_stride, max_blocks,
                              seq_lens, num_seqs, max_seq_len, out, scale, workspace,
                              workspace_bytes, d_err, stream, nullptr);
+}
+
+extern "C" int paged_gqa_decode_append_int8(const void* q, const void* k_new, const void* v_new,
+                                            const float* rope_cos, const float* rope_sin,
+                                            int max_pos, void* kv_pool, int num_pages,
+                                            const int32_t* block_tables, int bt_row_stride,
+                                            int max_blocks, const int32_t* seq_lens, int num_seqs,
+                                            int max_seq_len, void* q_out, void* out, float scale,
+                                            void* workspace, size_t workspace_bytes, int* d_err,
+                                            void* stream, const pkv_decode_opts* opts) {
+  const AppendArgs app{k_new, v_new, rope_cos, rope_sin, max_pos, q_out};
+  return decode_entry(q, kv_pool, num_pages, block_tables, bt_row_stride, max_blocks, seq_lens,
+                      num_seqs, max_seq_len, out, scale, workspace, workspace_bytes, d_err, stream,
+                      opts, &app, true);
 }
 
 extern "C" int paged_gqa_decode_int8_ex(const void* q, const void* kv_pool, int num_pages,

@@ -128,6 +128,15 @@ def test_host_side_validation_returns_before_launch():
                 pkv.DecodeOpts(pkv.COMPUTE_TENSOR, 0, 0, 0, 0, 0, 1, 0)):
         assert L.paged_gqa_decode_int8_ex(fake, fake, 8, fake, 128, 128, fake, 1, 16, fake, 0.125,
                                           fake, 1 << 20, null, null, ctypes.byref(bad)) == 1
+    # fused INT8 step: null new token; misaligned pool; a non-default configuration
+    F8 = L.paged_gqa_decode_append_int8
+    assert F8(fake, null, fake, fake, fake, 2048, fake, 8, fake, 128, 128, fake, 1, 16, null, fake,
+              0.125, fake, 1 << 20, null, null, null) == 1
+    assert F8(fake, fake, fake, fake, fake, 2048, ctypes.c_void_p(0x10008), 8, fake, 128, 128, fake, 1,
+              16, null, fake, 0.125, fake, 1 << 20, null, null, null) == 2
+    four = pkv.DecodeOpts(pkv.COMPUTE_TENSOR, 0, 0, 4, 16, 0, 0, 0)
+    assert F8(fake, fake, fake, fake, fake, 2048, fake, 8, fake, 128, 128, fake, 1, 16, null, fake,
+              0.125, fake, 1 << 20, null, null, ctypes.byref(four)) == 1
 
 
 def _run_cpp_schedule(case, static=False):

@@ -343,3 +343,105 @@ def test_int8_full_size_stress256_sampled(lib, cuda_device, tables):
     case = W.case_stress()
     full_size_int8_check(lib, cuda_device, case, [(0, 0), (9, 77), (15, 255)], tables)
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------ fused decode step ---
+
+def fused_case_int8(lens, seed):
+    """One layer: the oracle's INT8 image of random pages holding seq_lens - 1
+    tokens, room for the new token, new K/V and un-rotated q."""
+    lens = np.asarray(lens, np.int32)
+    case = make_case(lens, seed=seed, extra_pages=3)
+    codes, scales = OI.quantize_pool(W.bf16_bits(W.fill_pool(case)))
+    k = rand_bits(seed + 1, (len(lens), 8, 64))
+    v = rand_bits(seed + 2, (len(lens), 8, 64))
+    q = rand_bits(seed + 3, (len(lens), 32, 64))
+    return case, codes, scales, q, k, v
+
+
+def run_fused8(lib, dev, tables, case, codes, scales, q, k, v, lens=None, bt=None):
+    cos_d, sin_d, _, _ = tables
+    lens = case.seq_lens if lens is None else lens
+    bt = case.block_tables[0] if bt is None else bt
+    pool = dev_pool(codes, scales, dev)
+    out = torch.empty((len(lens), 32, 64), dtype=torch.bfloat16, device=dev)
+    q_out = torch.empty_like(out)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lib.paged_gqa_decode_append_int8(to_dev_bf16(q, dev), to_dev_bf16(k, dev), to_dev_bf16(v, dev),
+                                     pool, to_dev_i32(bt, dev), to_dev_i32(lens, dev), out, cos_d,
+                                     sin_d, 0.125, q_out=q_out, d_err=err)
+    return pool, q_out, out, lib.pkv_read_device_error(err)
+
+
+def test_int8_fused_step_matches_oracle(lib, cuda_device, tables):
+    """The new token lands in the first or the second page of a two-page unit,
+    on page boundaries, in one-page sequences and in full contexts."""
+    _, _, cos_o, sin_o = tables
+    lens = [1, 16, 17, 32, 33, 48, 49, 0, 700, 2048, 5, 1023]
+    case, codes, scales, q, k, v = fused_case_int8(lens, 50)
+    pool, q_out, out, code = run_fused8(lib, cuda_device, tables, case, codes, scales, q, k, v)
+    wc, ws, wq, ref, e = OI.decode_step_int8(codes, scales, q, k, v, case.block_tables[0],
+                                             case.seq_lens, cos_o, sin_o, 0.125)
+    assert code == 0 and not e
+    assert same_pool(pool, wc, ws), "appended pages differ from the oracle's"
+    assert np.array_equal(bits(q_out), wq), "rotated q differs from the oracle's"
+    got = bf16_to_f64(out)
+    check_close_int8(got, ref, "fused INT8 step")
+    assert np.all(got[7] == 0) and np.all(bits(q_out)[7] == 0)
+
+
+@pytest.mark.parametrize("bad", ["last_page", "middle_page", "past_table"])
+def test_int8_fused_step_error_contract(lib, cuda_device, tables, bad):
+    _, _, cos_o, sin_o = tables
+    lens = np.array([40, 17, 300, 1], np.int32)
+    case, codes, scales, q, k, v = fused_case_int8(lens, 60)
+    bt = case.block_tables[0].copy()
+    if bad == "last_page":
+        bt[2, (lens[2] - 1) // 16] = case.num_pages + 5     # the new token's page
+    elif bad == "middle_page":
+        bt[2, 3] = -1
+    else:
+        lens[2] = 16 * 128 + 1
+    pool, q_out, out, code = run_fused8(lib, cuda_device, tables, case, codes, scales, q, k, v,
+                                        lens=lens, bt=bt)
+    wc, ws, wq, ref, e = OI.decode_step_int8(codes, scales, q, k, v, bt, lens, cos_o, sin_o, 0.125)
+    assert e and code == lib.ERR_DEVICE_INDEX
+    assert same_pool(pool, wc, ws)
+    assert np.array_equal(bits(q_out), wq)
+    got = bf16_to_f64(out)
+    assert np.all(got[2] == 0)
+    check_close_int8(got, ref, f"fused INT8 step next to a bad sequence ({bad})")
+
+
+def test_int8_fused_full_size_batch32_sampled(lib, cuda_device, tables):
+    """The bench's INT8 step (16 fused launches) at batch 32 x 2048, sampled."""
+    cos_d, sin_d, cos_o, sin_o = tables
+    dev = cuda_device
+    case = W.case_batch32()
+    pool = W.fill_pool_int8(case, device=dev)
+    q_raw = W.fill_queries(case, device=dev)
+    k_new, v_new = W.fill_new_kv(case, device=dev)
+    bt_all = to_dev_i32(case.block_tables, dev)
+    lens = to_dev_i32(case.seq_lens, dev)
+    pos = to_dev_i32(W.new_positions(case), dev)
+    out = torch.empty_like(q_raw)
+    samples = [(0, 0), (5, 31), (15, 7)]
+    pre = {}
+    for (l, s) in samples:
+        ids = case.block_tables[l, s][case.block_tables[l, s] >= 0]
+        pre[(l, s)] = (ids,) + OI.unpack_pages(pool[torch.from_numpy(ids).to(dev).long()].cpu().numpy())
+    step = lib.Int8DecodeStep(pool, bt_all, lens, pos, k_new, v_new, q_raw, out, cos_d, sin_d,
+                              case.scale, max_seq_len=case.max_seq_len, use_graph=False)
+    assert step.error() == 0
+    for (l, s) in samples:
+        ids, c_pages, s_pages = pre[(l, s)]
+        bt_local = np.full((1, 128), -1, np.int32)
+        bt_local[0, :len(ids)] = np.arange(len(ids))
+        wc, ws, wq, ref, e = OI.decode_step_int8(
+            c_pages, s_pages, bits(q_raw[l, s:s + 1]), bits(k_new[l, s:s + 1]),
+            bits(v_new[l, s:s + 1]), bt_local, case.seq_lens[s:s + 1], cos_o, sin_o, case.scale)
+        assert not e
+        assert same_pool(pool[torch.from_numpy(ids).to(dev).long()], wc, ws), f"layer {l} seq {s}"
+        assert np.array_equal(bits(step.q_rot[l, s:s + 1]), wq)
+        check_close_int8(bf16_to_f64(out[l, s:s + 1]), ref, f"fused INT8 layer {l} seq {s}")
+    torch.cuda.empty_cache()
