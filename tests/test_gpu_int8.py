@@ -445,3 +445,40 @@ def test_int8_fused_full_size_batch32_sampled(lib, cuda_device, tables):
         assert np.array_equal(bits(step.q_rot[l, s:s + 1]), wq)
         check_close_int8(bf16_to_f64(out[l, s:s + 1]), ref, f"fused INT8 layer {l} seq {s}")
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_int8_step_graph_matches_eager_and_oracle(lib, cuda_device, tables, fused):
+    """Int8DecodeStep over 3 layers (fused: with the layer overlap), replayed
+    from its CUDA graph and run eagerly: identical bits, and equal to the
+    oracle's INT8 step layer by layer."""
+    cos_d, sin_d, cos_o, sin_o = tables
+    case = W.case_uniform(7, batch=4, layers=3, ctx=300, name="i8_step_small")
+    case.seq_lens[:] = [300, 17, 129, 256]
+    dev = cuda_device
+    pool0 = W.fill_pool_int8(case, device=dev)
+    q = W.fill_queries(case, device=dev)
+    k, v = W.fill_new_kv(case, device=dev)
+    pos = torch.from_numpy(W.new_positions(case)).to(dev)
+    bt = torch.from_numpy(case.block_tables).to(dev)
+    lens = torch.from_numpy(case.seq_lens).to(dev)
+    outs = []
+    for use_graph in (False, True):
+        pool = pool0.clone()
+        out = torch.empty_like(q)
+        step = lib.Int8DecodeStep(pool, bt, lens, pos, k, v, q, out, cos_d, sin_d, case.scale,
+                                  max_seq_len=300, use_graph=use_graph, fused=fused)
+        step.run()
+        assert step.error() == 0
+        outs.append((bits(out), pool.cpu().numpy(), bits(step.q_rot)))
+    assert all(np.array_equal(a, b) for a, b in zip(outs[0], outs[1]))
+    out_b, pool_b, qrot_b = outs[1]
+    codes, scales = OI.unpack_pages(pool0.cpu().numpy())
+    for l in range(case.num_layers):
+        codes, scales, want_q, ref, e = OI.decode_step_int8(
+            codes, scales, bits(q[l]), bits(k[l]), bits(v[l]), case.block_tables[l], case.seq_lens,
+            cos_o, sin_o, case.scale)
+        assert not e
+        assert np.array_equal(qrot_b[l], want_q)
+        check_close_int8(OB.to_f64(out_b[l]), ref, f"INT8 step layer {l}")
+    assert np.array_equal(pool_b, OI.pack_pages(codes, scales))
