@@ -13,7 +13,8 @@ on the device per slot ([L][max_slots][max_blocks]), and each step gathers
 the running sequences' rows into a packed batch table.  The caller supplies
 the new K/V/q values through callbacks, so any model (or a synthetic source)
 can drive it.  Nothing here computes attention: every token goes through
-kv_append_rope / paged_gqa_decode(_append).
+kv_append_rope / paged_gqa_decode(_append), or their INT8-page forms when the
+pool is an INT8 pool.
 """
 from __future__ import annotations
 
@@ -21,14 +22,16 @@ import numpy as np
 import torch
 
 from . import (OK, PAGE_TOKENS, PkvError, Scheduler, alloc_workspace, kv_append_rope,
-               paged_gqa_decode, paged_gqa_decode_append, pkv_read_device_error,
+               kv_append_rope_int8, paged_gqa_decode, paged_gqa_decode_append,
+               paged_gqa_decode_append_int8, paged_gqa_decode_int8, pkv_read_device_error,
                ERR_REQUEST_TOO_LARGE)
 
 
 class ContinuousBatcher:
     """FIFO continuous batching of decode requests on one device.
 
-    pool:        [num_pages, 2, 8, 16, 64] bf16 (one layer per page)
+    pool:        [num_pages, 2, 8, 16, 64] bf16 (one layer per page), or an
+                 INT8 pool [num_pages, 8, 2176] uint8 (see new_int8_pool)
     rope_cos/sin [max_pos, 32] fp32 device tables
     fused:       decode steps as one fused append+decode kernel per layer
                  (else kv_append_rope followed by paged_gqa_decode)
@@ -39,6 +42,7 @@ class ContinuousBatcher:
     def __init__(self, pool, num_layers, rope_cos, rope_sin, scale, max_blocks=128,
                  max_slots=256, fused=True, static=False):
         self.pool = pool
+        self.int8 = pool.dtype == torch.uint8
         self.dev = pool.device
         self.L = num_layers
         self.M = max_blocks
@@ -92,10 +96,11 @@ class ContinuousBatcher:
             self._sync_rows(rid)
             pos = torch.arange(P, dtype=torch.int32, device=self.dev)
             rows = torch.full((P,), self.slot[rid], dtype=torch.int32, device=self.dev)
+            append = kv_append_rope_int8 if self.int8 else kv_append_rope
             for l in range(self.L):
                 k, v = prompt_kv(rid, l)
-                kv_append_rope(k.to(self.dev), v.to(self.dev), pos, self.tables[l], self.pool,
-                               self.cos, self.sin, token_seq=rows, d_err=self.d_err)
+                append(k.to(self.dev), v.to(self.dev), pos, self.tables[l], self.pool,
+                       self.cos, self.sin, token_seq=rows, d_err=self.d_err)
             self.length[rid] = P
             self.steps_done[rid] = 0
         self.running += admitted
@@ -128,14 +133,17 @@ class ContinuousBatcher:
             v = torch.stack([b for _, b in kv]).to(self.dev)
             bt = self.tables[l].index_select(0, slots).contiguous()
             if self.fused:
-                paged_gqa_decode_append(q, k, v, self.pool, bt, lens, out[l], self.cos, self.sin,
-                                        self.scale, workspace=ws, d_err=self.d_err)
+                step = paged_gqa_decode_append_int8 if self.int8 else paged_gqa_decode_append
+                step(q, k, v, self.pool, bt, lens, out[l], self.cos, self.sin, self.scale,
+                     workspace=ws, d_err=self.d_err)
             else:
                 q_rot = torch.empty_like(q)
-                kv_append_rope(k, v, pos, bt, self.pool, self.cos, self.sin, q_in=q,
-                               q_out=q_rot, d_err=self.d_err)
-                paged_gqa_decode(q_rot, self.pool, bt, lens, out[l], self.scale, workspace=ws,
-                                 d_err=self.d_err)
+                append = kv_append_rope_int8 if self.int8 else kv_append_rope
+                decode = paged_gqa_decode_int8 if self.int8 else paged_gqa_decode
+                append(k, v, pos, bt, self.pool, self.cos, self.sin, q_in=q, q_out=q_rot,
+                       d_err=self.d_err)
+                decode(q_rot, self.pool, bt, lens, out[l], self.scale, workspace=ws,
+                       d_err=self.d_err)
         for rid in ids:
             self.length[rid] += 1
             self.steps_done[rid] += 1

@@ -6,15 +6,17 @@ admission-credit rule.  The C++ scheduler (driving the kernels) and the
 oracle's scheduler must take identical decisions; every decode output of
 layers 0 and 15 at every 16th step must match the FP64 oracle; the final pool
 must equal the oracle's bit for bit.  The same run is made with the fused
-decode step and with kv_append_rope followed by paged_gqa_decode.
+decode step and with kv_append_rope followed by paged_gqa_decode, and on INT8
+pages (the oracle's INT8 append and decode).
 """
 import numpy as np
 import pytest
 import torch
 
 import workloads as W
-from oracle import admission as OA, paged_kv as OP, rope as OR
+from oracle import admission as OA, int8_kv as OI, paged_kv as OP, rope as OR
 from tests._util import bf16_to_f64, bits, check_close
+from tests.test_gpu_int8 import check_close_int8
 
 pytestmark = pytest.mark.gpu
 
@@ -55,10 +57,14 @@ class Source:
         return self.q_cache[key]
 
 
-def run_mix(lib, dev, case, fused, cos_d, sin_d, static=False):
+def run_mix(lib, dev, case, fused, cos_d, sin_d, static=False, int8=False):
     from paged_kv_gqa_append_gb300.serving import ContinuousBatcher
     src = Source(case)
-    pool = torch.zeros((case.num_pages, 2, 8, 16, 64), dtype=torch.bfloat16, device=dev)
+    if int8:
+        pool = lib.new_int8_pool(case.num_pages, dev)
+        ocodes, oscales = OI.new_pools(case.num_pages)
+    else:
+        pool = torch.zeros((case.num_pages, 2, 8, 16, 64), dtype=torch.bfloat16, device=dev)
     cb = ContinuousBatcher(pool, case.num_layers, cos_d, sin_d, W.DEFAULT_SCALE,
                            max_slots=64, fused=fused, static=static)
     for p in case.prompt_lens:
@@ -83,8 +89,13 @@ def run_mix(lib, dev, case, fused, cos_d, sin_d, static=False):
             for l in range(case.num_layers):
                 k, v = src.prompt_kv(rid, l)
                 row = np.array([osch.block_table_row(rid, l)], np.int32)
-                _, _, e = OP.append_rope(opool, bits(k), bits(v), np.arange(P), np.zeros(P, np.int32),
-                                         row, cos_o, sin_o, inplace=True)
+                if int8:
+                    _, _, _, e = OI.append_rope_int8(ocodes, oscales, bits(k), bits(v), np.arange(P),
+                                                     np.zeros(P, np.int32), row, cos_o, sin_o,
+                                                     inplace=True)
+                else:
+                    _, _, e = OP.append_rope(opool, bits(k), bits(v), np.arange(P),
+                                             np.zeros(P, np.int32), row, cos_o, sin_o, inplace=True)
                 assert not e
             olen[rid], odone[rid] = P, 0
         orun += oadm
@@ -100,14 +111,23 @@ def run_mix(lib, dev, case, fused, cos_d, sin_d, static=False):
                 k, v = src.token_kv(rid, l, pos)
                 row = np.array([osch.block_table_row(rid, l)], np.int32)
                 q = src.token_q(rid, l, pos)
-                _, qr, e = OP.append_rope(opool, bits(k[None]), bits(v[None]), [pos], [0], row,
-                                          cos_o, sin_o, bits(q[None]), inplace=True)
+                if int8:
+                    _, _, qr, e = OI.append_rope_int8(ocodes, oscales, bits(k[None]), bits(v[None]),
+                                                      [pos], [0], row, cos_o, sin_o, bits(q[None]),
+                                                      inplace=True)
+                else:
+                    _, qr, e = OP.append_rope(opool, bits(k[None]), bits(v[None]), [pos], [0], row,
+                                              cos_o, sin_o, bits(q[None]), inplace=True)
                 assert not e
                 if sample and l in SAMPLE_LAYERS:
-                    ref, e2 = OP.decode(qr, opool, row, [pos + 1], W.DEFAULT_SCALE)
-                    assert not e2
                     got = bf16_to_f64(outs[SAMPLE_LAYERS.index(l), b])[None]
-                    check_close(got, ref, f"step {step} layer {l} request {rid}")
+                    if int8:
+                        ref, e2 = OI.decode_int8(qr, ocodes, oscales, row, [pos + 1], W.DEFAULT_SCALE)
+                        check_close_int8(got, ref, f"INT8 step {step} layer {l} request {rid}")
+                    else:
+                        ref, e2 = OP.decode(qr, opool, row, [pos + 1], W.DEFAULT_SCALE)
+                        check_close(got, ref, f"step {step} layer {l} request {rid}")
+                    assert not e2
                     checked += 1
         for rid in orun:
             olen[rid] += 1
@@ -121,7 +141,10 @@ def run_mix(lib, dev, case, fused, cos_d, sin_d, static=False):
         step += 1
     assert cb.error() == 0
     assert cb.sched.events() == osch.events
-    assert np.array_equal(bits(pool), opool)
+    if int8:
+        assert np.array_equal(pool.cpu().numpy(), OI.pack_pages(ocodes, oscales))
+    else:
+        assert np.array_equal(bits(pool), opool)
     assert checked >= len(case.prompt_lens)     # every request sampled at least once
     return step
 
@@ -134,3 +157,13 @@ def test_continuous_batching_mix_matches_oracle(lib, cuda_device, fused, static)
     cos_d, sin_d = lib.rope_tables_device(cuda_device, W.MAX_CONTEXT)
     steps = run_mix(lib, cuda_device, case, fused, cos_d, sin_d, static)
     assert steps > case.decode_steps          # requests really overlapped in time
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_continuous_batching_mix_int8_pages(lib, cuda_device, fused):
+    # the first 16 requests of the mix on INT8 pages (same scheduler, same
+    # page count): pages bit-exact at the end, outputs sampled as above
+    case = W.case_continuous(requests=16)
+    cos_d, sin_d = lib.rope_tables_device(cuda_device, W.MAX_CONTEXT)
+    steps = run_mix(lib, cuda_device, case, fused, cos_d, sin_d, int8=True)
+    assert steps > case.decode_steps
