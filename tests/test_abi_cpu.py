@@ -33,6 +33,15 @@ def test_every_declared_symbol_is_exported():
     assert not missing, missing
 
 
+def test_int8_page_format_agrees_with_the_oracle():
+    # the header's INT8 block, the binding's and the oracle's byte layout
+    text = open(HEADER).read()
+    m = re.search(r"#define PKV_I8_BLOCK_BYTES .*?/\* (\d+) \*/", text)
+    assert m and int(m.group(1)) == 2176
+    from oracle import int8_kv as OI
+    assert pkv.I8_BLOCK_BYTES == OI.BLOCK_BYTES == W.I8_BLOCK_BYTES == 2176
+
+
 def test_status_strings():
     assert pkv.status_string(0) == "PKV_OK"
     assert pkv.status_string(6) == "PKV_ERR_DEVICE_INDEX"
