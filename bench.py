@@ -49,11 +49,13 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", choices=["batch32", "stress256", "int8", "int8_stress256",
-                                           "prefill", "argmax"],
+                                           "mixed8", "single37", "prefill", "argmax"],
                     default="batch32",
                     help="batch32 / stress256: the decode step; int8 / int8_stress256: the same "
-                         "step on INT8 K/V pages; prefill: causal prefill of 8 prompts x 1920 "
-                         "tokens; argmax: next-token argmax of 32 x 128256 logits")
+                         "step on INT8 K/V pages; mixed8 / single37: one decode launch on the "
+                         "batch of 8 mixed lengths (L2 flushed before each launch, warm beside it) "
+                         "or the one 37-token sequence (latency); prefill: causal prefill of 8 "
+                         "prompts x 1920 tokens; argmax: next-token argmax of 32 x 128256 logits")
     ap.add_argument("--compute", choices=["tensor", "fma"], default="tensor")
     ap.add_argument("--layers", type=int, default=0,
                     help="layers of the workload (0 = its own: 16); fewer layers shrink the pool "
@@ -307,6 +309,31 @@ def run_reference(args, world, rank):
         return
     if args.workload in ("prefill", "argmax"):
         run_reference_other(args)
+        return
+    if args.workload in ("mixed8", "single37"):
+        from oracle import paged_kv as OP
+        case = W.case_mixed() if args.workload == "mixed8" else W.case_single()
+        pool_b = W.bf16_bits(W.fill_pool(case))
+        q_b = W.bf16_bits(W.fill_queries(case))[0]
+        one = lambda: OP.decode(q_b, pool_b, case.block_tables[0], case.seq_lens, case.scale)
+        for _ in range(args.warmup):
+            one()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            one()
+        el = time.perf_counter() - t0
+        value = case.kv_bytes_per_layer() * args.steps / el / 1e9
+        sample = f"{args.steps} whole decodes of {case.name}"
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": case.name, "batch": case.num_seqs, "layers": 1},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cpu_cores_used(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}), flush=True)
         return
     case = make_case(args.workload, args.layers)
     int8 = args.workload.startswith("int8")
@@ -650,6 +677,118 @@ def run_int8_line(args, world, rank, local):
             "roofline": roof, "cpu_baseline": cpu}), flush=True)
 
 
+# ------------------------------------------- the small decode cases ------
+
+def run_small_line(args, world, rank, local):
+    """One paged_gqa_decode launch on a small case: the batch of 8 mixed
+    lengths (16.8 MB of K/V, which fits in L2: timed with a 2 x L2 buffer
+    written before each launch, and warm, back to back, beside it) or the one
+    37-token sequence (latency: microseconds per call)."""
+    import paged_kv_gqa_append_gb300 as pkv
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    case = W.case_mixed() if args.workload == "mixed8" else W.case_single()
+    pool = W.fill_pool(case, device=dev)
+    q = W.fill_queries(case, device=dev)[0]
+    bt = torch.from_numpy(case.block_tables[0]).to(dev)
+    lens = torch.from_numpy(case.seq_lens).to(dev)
+    out = torch.empty_like(q)
+    ws = pkv.alloc_workspace(case.num_seqs, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    kv_bytes = case.kv_bytes_per_layer()
+    stream = torch.cuda.current_stream(dev)
+    launch = lambda: pkv.paged_gqa_decode(q, pool, bt, lens, out, case.scale, workspace=ws,
+                                          max_seq_len=case.max_seq_len, d_err=err)
+    launch()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        launch()
+    for _ in range(max(3, args.warmup)):
+        g.replay()
+    if pkv.pkv_read_device_error(err):
+        raise RuntimeError("device error in the warm-up")
+    steps = max(1, min(args.steps, 500))
+    flush = torch.empty(2 * 129 * 2 ** 20 // 4, dtype=torch.float32, device=dev)  # 2 x L2
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.5 if clocks else 0)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    # flushed: events around each launch, the L2 flush outside them
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        flush.fill_(1.0)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    flushed_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), world, dev)
+    # warm: back to back
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    warm_ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    clk = clocks.summary(t_wall0, time.time()) if clocks else None
+    if clocks:
+        clocks.stop()
+    if pkv.pkv_read_device_error(err):
+        raise RuntimeError("device error in the timed region")
+    us_flushed, us_warm = flushed_ms * 1e3 / steps, warm_ms * 1e3 / steps
+    value = kv_bytes * steps * world / (flushed_ms / 1e3) / 1e9
+    # e2e: q uploaded from pinned memory, the output read back, per launch
+    q_h, out_h = q.cpu().pin_memory(), torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    k_e2e = max(1, min(steps, 200))
+    torch.cuda.synchronize()
+    a.record(stream)
+    t0 = time.perf_counter()
+    for _ in range(k_e2e):
+        q.copy_(q_h, non_blocking=True)
+        g.replay()
+        out_h.copy_(out, non_blocking=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(max(a.elapsed_time(b) / 1e3, time.perf_counter() - t0), world, dev)
+    peak, peak_kind = hbm_peak()
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle import paged_kv as OP
+        pool_b, q_b = W.bf16_bits(pool), W.bf16_bits(q)
+        done, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < 5.0:
+            OP.decode(q_b, pool_b, case.block_tables[0], case.seq_lens, case.scale)
+            done += 1
+        el = time.perf_counter() - t0
+        cpu = {"value": kv_bytes * done / el / 1e9, "unit": "GB/s", "cores": cpu_cores_used(),
+               "kind": "oracle", "sample": f"{done} whole decodes of {case.name}, {el:.1f} s"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": flushed_ms / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": case.name, "batch": case.num_seqs, "layers": 1,
+                       "seq_lens": [int(x) for x in case.seq_lens], "pool_pages": case.num_pages,
+                       "l2": "flushed: a 2 x L2 buffer written before each timed launch (outside "
+                             "its events); `warm_us_per_call` times back-to-back launches",
+                       "parallelism": f"replicas x{world}",
+                       "launch": "one paged_gqa_decode launch (CUDA graph replay) per step"},
+            "us_per_call": us_flushed, "warm_us_per_call": us_warm,
+            "warm_gbs": kv_bytes * steps * world / (warm_ms / 1e3) / 1e9,
+            "kv_bytes_per_step": kv_bytes, "clocks": clk, "gpu_launches": steps,
+            "e2e": {"value": kv_bytes * k_e2e * world / e2e_s / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": q_h.numel() * 2, "d2h_bytes_per_step": out_h.numel() * 2,
+                    "steps": k_e2e},
+            "roofline": {"bound": "hbm", "achieved": value / world, "peak": peak, "unit": "GB/s",
+                         "frac": value / world / peak, "traffic": None, "peak_source": peak_kind,
+                         "kernel": "paged_decode_kernel (paged_gqa_decode, L2 flushed before each launch)",
+                         "avg_launch_us": us_flushed, "algorithmic_bytes_per_launch": kv_bytes},
+            "cpu_baseline": cpu}), flush=True)
+
+
 # ------------------------------------------------ prefill and argmax lines --
 
 def tensor_peak():
@@ -867,6 +1006,8 @@ def main():
             run_argmax_line(args, world, rank, local)
         elif args.workload.startswith("int8"):
             run_int8_line(args, world, rank, local)
+        elif args.workload in ("mixed8", "single37"):
+            run_small_line(args, world, rank, local)
         else:
             run_gb300(args, world, rank, local)
     finally:
