@@ -85,7 +85,7 @@ extern "C" const char* pkv_status_string(int status) {
 
 extern "C" const char* pkv_last_error(void) { return g_last_error; }
 
-extern "C" int pkv_version(void) { return 10000 * 0 + 100 * 1 + 0; }
+extern "C" int pkv_version(void) { return 10000 * 0 + 100 * 2 + 0; }
 
 extern "C" int pkv_rope_inv_freq_plain(double* inv_freq, double theta) {
   if (!inv_freq || !(theta > 1.0)) return PKV_ERR_INVALID_ARGUMENT;
