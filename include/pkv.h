@@ -202,7 +202,9 @@ typedef struct pkv_decode_opts {
   int min_units_per_warp; /* 0 = default (2): fewer CTAs for small batches           */
   int ctas_per_sm;        /* 0 = as many as fit (at most 8)                          */
   int stages;             /* pages in flight per warp: 0 = default (2), 2 or 4       */
-  int warps_per_cta;      /* 0 = default (16); 16 (2 or 3 stages), 8 or 4            */
+  int warps_per_cta;      /* 0 = default: 16, or 8 on bf16 pages when max_seq_len
+                             bounds the problem to at most 128 (sequence, head,
+                             page) units; else 16 (2 or 3 stages), 8 or 4      */
   int combine;            /* segments split across CTAs: 0 = the last CTA merges
                              them in the same kernel, 1 = a second kernel merges
                              them after the first (programmatic dependent launch) */
