@@ -49,12 +49,14 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", choices=["batch32", "stress256", "int8", "int8_stress256",
-                                           "mixed8", "single37", "prefill", "argmax"],
+                                           "mixed8", "single37", "continuous", "prefill",
+                                           "argmax"],
                     default="batch32",
                     help="batch32 / stress256: the decode step; int8 / int8_stress256: the same "
                          "step on INT8 K/V pages; mixed8 / single37: one decode launch on the "
                          "batch of 8 mixed lengths (L2 flushed before each launch, warm beside it) "
-                         "or the one 37-token sequence (latency); prefill: causal prefill of 8 "
+                         "or the one 37-token sequence (latency); continuous: the 64-request "
+                         "continuous-batching mix run to completion; prefill: causal prefill of 8 "
                          "prompts x 1920 tokens; argmax: next-token argmax of 32 x 128256 logits")
     ap.add_argument("--compute", choices=["tensor", "fma"], default="tensor")
     ap.add_argument("--layers", type=int, default=0,
@@ -309,6 +311,35 @@ def run_reference(args, world, rank):
         return
     if args.workload in ("prefill", "argmax"):
         run_reference_other(args)
+        return
+    if args.workload == "continuous":
+        from oracle import admission as OA
+        case = W.case_continuous()
+        _, log, _ = OA.simulate(case.prompt_lens, case.decode_steps, case.num_pages,
+                                case.num_layers)
+        tokens = sum(len(e["lens"]) for e in log)
+        ora = mix_sample(round(sum(sum(e["lens"]) for e in log) / tokens))
+        for _ in range(args.warmup):
+            ora.run_one()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            ora.run_one()
+        el = time.perf_counter() - t0
+        value = args.steps * ora.kv_bytes / el / 1e9
+        sample = (f"{args.steps} (layer, sequence) pairs at the mix's mean decode length "
+                  f"({ora.n} tokens): append 1 token + decode 32 heads each")
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": case.name, "requests": len(case.prompt_lens),
+                       "layers": case.num_layers, "mean_len": ora.n,
+                       "sample": "one (layer, seq) pair per step"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cpu_cores_used(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}), flush=True)
         return
     if args.workload in ("mixed8", "single37"):
         from oracle import paged_kv as OP
@@ -789,6 +820,185 @@ def run_small_line(args, world, rank, local):
             "cpu_baseline": cpu}), flush=True)
 
 
+# ------------------------------------------------ continuous-batching line --
+
+SLEEP_CYCLES = 20_000_000  # ~10 ms at 2 GHz: covers the host's enqueue of one step
+
+
+def mix_sample(mean_len):
+    """The oracle on one (layer, sequence) pair at the mix's mean decode length."""
+    n = int(mean_len)
+    case = W.DecodeCase("continuous_r64_geo300", 3, 16, np.array([n], np.int32), 0,
+                        np.zeros((1, 1, W.MAX_BLOCKS), np.int32))
+    return OracleSample(case)
+
+
+def run_continuous_line(args, world, rank, local):
+    """The continuous-batching mix run to completion through
+    serving.ContinuousBatcher: 64 requests (prompts geometric, mean 300,
+    clipped to [1, 1920]) of 128 decode steps each, 16 layers, a 128 MiB pool
+    of 4096 pages, admission by page credit, one fused append + decode kernel
+    per layer and step.
+
+    Device time: each step's host work (scheduler, table rows, the batch's
+    table gather, that step's q / k / v drawn on the device) is queued first,
+    then a 2 x L2 buffer is written and a device sleep queued so that the
+    step's 16 launches are all queued before the GPU reaches them; CUDA
+    events bracket those launches alone.  (The host's enqueue time also
+    counts waits on a full launch queue, when it has run ahead of the
+    device; the measured step times were the same with a 3 ms sleep.)  value = K/V bytes the steps read
+    (sum over steps, layers and sequences of length x 2048) / the summed step
+    time.  e2e: the same mix again, wall clock from the first admission to
+    the last output read back, prompts and every step's q / k / v copied from
+    pinned host memory and every step's output copied to pinned host memory.
+    """
+    import paged_kv_gqa_append_gb300 as pkv
+    from paged_kv_gqa_append_gb300.serving import ContinuousBatcher
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    case = W.case_continuous()
+    L = case.num_layers
+    cos, sin = pkv.rope_tables_device(dev, W.MAX_CONTEXT)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(2 * 129 * 2 ** 20 // 4, dtype=torch.float32, device=dev)  # 2 x L2
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(case.seed)
+    pmax = int(case.prompt_lens.max())
+    prompt_d = W.normal_bf16((2, pmax, W.NUM_KV_HEADS, W.HEAD_DIM), gen)
+
+    def batcher():
+        pool = torch.zeros((case.num_pages, 2, 8, 16, 64), dtype=torch.bfloat16, device=dev)
+        cb = ContinuousBatcher(pool, L, cos, sin, W.DEFAULT_SCALE, max_slots=64)
+        for p in case.prompt_lens:
+            if cb.submit(int(p), case.allowed_new_tokens) < 0:
+                raise RuntimeError("request rejected")
+        return cb
+
+    def device_run(max_steps):
+        cb = batcher()
+        P = lambda rid, l: (prompt_d[0, :cb.prompt[rid]], prompt_d[1, :cb.prompt[rid]])
+        evs, host_s, tokens, kv_bytes, step = [], [], 0, 0, 0
+        while (cb.sched.stats()["queued"] or cb.running) and step < max_steps:
+            cb.admit(P)
+            batch = cb.prepare_step()
+            B = len(batch.ids)
+            q = W.normal_bf16((L, B, W.NUM_Q_HEADS, W.HEAD_DIM), gen)
+            k = W.normal_bf16((L, B, W.NUM_KV_HEADS, W.HEAD_DIM), gen)
+            v = W.normal_bf16((L, B, W.NUM_KV_HEADS, W.HEAD_DIM), gen)
+            flush.fill_(1.0)
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+            torch.cuda._sleep(SLEEP_CYCLES)
+            t0 = time.perf_counter()
+            e1.record(stream)
+            cb.launch_step(batch, q, k, v)
+            e2.record(stream)
+            host_s.append(time.perf_counter() - t0)
+            evs.append((e0, e1, e2))
+            tokens += B
+            kv_bytes += int(batch.lens_h.sum()) * W.NUM_KV_HEADS * W.HEAD_DIM * 2 * 2 * L
+            cb.retire(case.decode_steps)
+            step += 1
+        torch.cuda.synchronize()
+        if cb.error():
+            raise RuntimeError("device error in the continuous mix")
+        step_ms = [a.elapsed_time(b) for _, a, b in evs]
+        sleep_ms = [s.elapsed_time(a) for s, a, _ in evs]
+        return step, tokens, kv_bytes, step_ms, sleep_ms, host_s
+
+    def e2e_run():
+        cb = batcher()
+        bmax = 64
+        prompt_h = prompt_d.cpu().pin_memory()
+        q_h = W.normal_bf16((L * bmax * W.NUM_Q_HEADS * W.HEAD_DIM,), gen).cpu().pin_memory()
+        kv_h = W.normal_bf16((2, L * bmax * W.NUM_KV_HEADS * W.HEAD_DIM), gen).cpu().pin_memory()
+        out_h = torch.empty(L * bmax * W.NUM_Q_HEADS * W.HEAD_DIM, dtype=torch.bfloat16,
+                            pin_memory=True)
+        P = lambda rid, l: (prompt_h[0, :cb.prompt[rid]], prompt_h[1, :cb.prompt[rid]])
+        h2d = d2h = steps = 0
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        while cb.sched.stats()["queued"] or cb.running:
+            for rid in cb.admit(P):
+                h2d += 2 * L * cb.prompt[rid] * W.NUM_KV_HEADS * W.HEAD_DIM * 2
+            batch = cb.prepare_step()
+            B = len(batch.ids)
+            nq, nkv = L * B * W.NUM_Q_HEADS * W.HEAD_DIM, L * B * W.NUM_KV_HEADS * W.HEAD_DIM
+            q = q_h[:nq].view(L, B, W.NUM_Q_HEADS, W.HEAD_DIM).to(dev, non_blocking=True)
+            k = kv_h[0, :nkv].view(L, B, W.NUM_KV_HEADS, W.HEAD_DIM).to(dev, non_blocking=True)
+            v = kv_h[1, :nkv].view(L, B, W.NUM_KV_HEADS, W.HEAD_DIM).to(dev, non_blocking=True)
+            out = cb.launch_step(batch, q, k, v)
+            out_h[:nq].copy_(out.view(-1), non_blocking=True)
+            h2d += (nq + 2 * nkv) * 2
+            d2h += nq * 2
+            cb.retire(case.decode_steps)
+            steps += 1
+        torch.cuda.synchronize()
+        el = time.perf_counter() - t0
+        if cb.error():
+            raise RuntimeError("device error in the continuous mix (e2e)")
+        return el, steps, h2d + cb.uploaded_bytes, d2h
+
+    device_run(max(3, args.warmup))          # warm-up: the first steps of the mix
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.5 if clocks else 0)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    steps, tokens, kv_bytes, step_ms, sleep_ms, host_s = device_run(1 << 30)
+    clk = clocks.summary(t_wall0, time.time()) if clocks else None
+    if clocks:
+        clocks.stop()
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    value = kv_bytes * world / (total_ms / 1e3) / 1e9
+    e2e_s, e2e_steps, h2d, d2h = e2e_run()
+    if e2e_steps != steps:
+        raise RuntimeError("the e2e run took another schedule")
+    e2e_s = max_over_ranks(e2e_s, world, dev)
+    peak, peak_kind = hbm_peak()
+    mean_len = kv_bytes / (tokens * W.NUM_KV_HEADS * W.HEAD_DIM * 4 * L)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        ora = mix_sample(round(mean_len))
+        gbs, done, el = ora.timed(10.0)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": cpu_cores_used(), "kind": "oracle",
+               "sample": f"{done} (layer, sequence) pairs at the mix's mean decode length "
+                         f"({ora.n} tokens): append 1 token + decode 32 heads, {el:.1f} s"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
+            "warmup": max(3, args.warmup), "ms_per_step": total_ms / steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": case.name, "requests": len(case.prompt_lens),
+                       "decode_steps_per_request": case.decode_steps, "layers": L,
+                       "pool_pages": case.num_pages, "mean_batch": tokens / steps,
+                       "mean_len": mean_len,
+                       "l2": "flushed: a 2 x L2 buffer written before each step (outside its events)",
+                       "parallelism": f"replicas x{world}",
+                       "launch": "ContinuousBatcher.launch_step: one fused append+decode kernel "
+                                 "per layer; events around each step's launches"},
+            "tokens_per_s": tokens * world / (total_ms / 1e3),
+            "us_per_layer": total_ms * 1e3 / (steps * L),
+            "kv_bytes_total": kv_bytes,
+            "host_enqueue_us_max": max(host_s) * 1e6,
+            "host_enqueue_us_mean": sum(host_s) / len(host_s) * 1e6,
+            "device_sleep_us_min": min(sleep_ms) * 1e3,
+            "clocks": clk, "gpu_launches": steps * L,
+            "e2e": {"value": kv_bytes * world / e2e_s / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d // e2e_steps, "d2h_bytes_per_step": d2h // e2e_steps,
+                    "steps": e2e_steps, "tokens_per_s": tokens * world / e2e_s,
+                    "path": "ContinuousBatcher admit / prepare_step / launch_step / retire, "
+                            "inputs from and outputs to pinned host memory, host scheduling "
+                            "included"},
+            "roofline": {"bound": "hbm", "achieved": value / world, "peak": peak, "unit": "GB/s",
+                         "frac": value / world / peak, "traffic": None, "peak_source": peak_kind,
+                         "kernel": "paged_decode_append (one launch per layer and step)",
+                         "launches_timed": steps * L, "avg_launch_us": total_ms * 1e3 / (steps * L),
+                         "algorithmic_bytes_per_launch": kv_bytes / (steps * L)},
+            "cpu_baseline": cpu}), flush=True)
+
+
 # ------------------------------------------------ prefill and argmax lines --
 
 def tensor_peak():
@@ -1008,6 +1218,8 @@ def main():
             run_int8_line(args, world, rank, local)
         elif args.workload in ("mixed8", "single37"):
             run_small_line(args, world, rank, local)
+        elif args.workload == "continuous":
+            run_continuous_line(args, world, rank, local)
         else:
             run_gb300(args, world, rank, local)
     finally:

@@ -18,13 +18,25 @@ pool is an INT8 pool.
 """
 from __future__ import annotations
 
+from typing import NamedTuple
+
 import numpy as np
 import torch
 
-from . import (OK, PAGE_TOKENS, PkvError, Scheduler, alloc_workspace, kv_append_rope,
+from . import (HEAD_DIM, NUM_KV_HEADS, NUM_Q_HEADS, OK, PAGE_TOKENS, PkvError, Scheduler,
+               alloc_workspace, kv_append_rope,
                kv_append_rope_int8, paged_gqa_decode, paged_gqa_decode_append,
                paged_gqa_decode_append_int8, paged_gqa_decode_int8, pkv_read_device_error,
                ERR_REQUEST_TOO_LARGE)
+
+
+class StepBatch(NamedTuple):
+    """One decode step's batch, from ContinuousBatcher.prepare_step."""
+    ids: list                 # running request ids, in batch-row order
+    lens_h: np.ndarray        # [B] int32 lengths after the step (host)
+    lens: torch.Tensor        # the same on the device
+    positions: torch.Tensor   # [B] int32 positions of the new tokens (lens - 1)
+    tables: torch.Tensor      # [L, B, max_blocks] int32 block tables
 
 
 class ContinuousBatcher:
@@ -62,6 +74,7 @@ class ContinuousBatcher:
         self.steps_done = {}
         self.slot = {}
         self.rejected = []
+        self.uploaded_bytes = 0    # scheduler state copied host -> device so far
 
     # -- requests -------------------------------------------------------------
     def submit(self, prompt_tokens: int, new_tokens: int):
@@ -73,19 +86,30 @@ class ContinuousBatcher:
         self.prompt[rid] = int(prompt_tokens)
         return rid
 
+    def _upload(self, a: np.ndarray) -> torch.Tensor:
+        """Host array -> device tensor without waiting for the device (pinned
+        staging; the host allocator keeps the staging block until the copy
+        has run)."""
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        self.uploaded_bytes += t.numel() * t.element_size()
+        if self.dev.type == "cuda":
+            t = t.pin_memory()
+        return t.to(self.dev, non_blocking=True)
+
     def _sync_rows(self, rid):
         """Copy a request's block-table rows (all layers) to the device."""
         s = self.slot[rid]
         for l in range(self.L):
             row, _ = self.sched.block_table(rid, l)
             self.host_tables[l, s] = row
-        self.tables[:, s].copy_(torch.from_numpy(self.host_tables[:, s]))
+        self.tables[:, s].copy_(self._upload(self.host_tables[:, s]))
 
     def admit(self, prompt_kv):
         """Admit what fits and write the prompts' K/V.
 
-        prompt_kv(rid, layer) -> (k [P, 8, 64], v [P, 8, 64]) bf16 tensors.
-        Returns the admitted request ids.
+        prompt_kv(rid, layer) -> (k [P, 8, 64], v [P, 8, 64]) bf16 tensors
+        (host tensors are copied without waiting: a pinned one must stay
+        unchanged until the copy has run).  Returns the admitted request ids.
         """
         admitted = self.sched.admit()
         for rid in admitted:
@@ -99,55 +123,95 @@ class ContinuousBatcher:
             append = kv_append_rope_int8 if self.int8 else kv_append_rope
             for l in range(self.L):
                 k, v = prompt_kv(rid, l)
-                append(k.to(self.dev), v.to(self.dev), pos, self.tables[l], self.pool,
+                append(k.to(self.dev, non_blocking=True), v.to(self.dev, non_blocking=True),
+                       pos, self.tables[l], self.pool,
                        self.cos, self.sin, token_seq=rows, d_err=self.d_err)
             self.length[rid] = P
             self.steps_done[rid] = 0
         self.running += admitted
         return admitted
 
-    def step(self, token_kv, token_q, out_layers=None):
-        """One decode step for every running request.
+    def prepare_step(self) -> "StepBatch":
+        """Host side of one decode step for every running request.
+
+        Grows each request by one token (a new page in every layer where its
+        position starts one), copies changed block-table rows to the device
+        and gathers the batch's tables [L, B, max_blocks] and lengths (after
+        the step) on the device.  The returned batch is consumed by exactly
+        one launch_step; nothing here launches an attention kernel.
+        """
+        ids = list(self.running)
+        for rid in ids:
+            if self.sched.grow(rid, self.length[rid] + 1) != OK:
+                raise PkvError(7, "ContinuousBatcher.prepare_step")
+            if self.length[rid] % PAGE_TOKENS == 0:      # a new page in every layer
+                self._sync_rows(rid)
+        lens_h = np.array([self.length[r] + 1 for r in ids], np.int32)
+        slots = self._upload(np.array([self.slot[r] for r in ids], np.int64))
+        lens = self._upload(lens_h)
+        tables = self.tables.index_select(1, slots)       # [L, B, M], contiguous
+        for rid in ids:
+            self.length[rid] += 1
+            self.steps_done[rid] += 1
+        return StepBatch(ids, lens_h, lens, lens - 1, tables)
+
+    def launch_step(self, batch: "StepBatch", q, k, v, out=None):
+        """Device side of one decode step: every layer appends each request's
+        new token at its position and attends over the request's pages.
+
+        q [L, B, 32, 64] (un-rotated), k / v [L, B, 8, 64] bf16 device
+        tensors, rows in batch.ids order.  Returns out [L, B, 32, 64] bf16.
+        Launches kernels only (one fused kernel per layer, or an append and
+        a decode): no host synchronisation.
+        """
+        B = len(batch.ids)
+        shapes = ((q, NUM_Q_HEADS), (k, NUM_KV_HEADS), (v, NUM_KV_HEADS))
+        for t, h in shapes:
+            if tuple(t.shape) != (self.L, B, h, HEAD_DIM):
+                raise ValueError(f"expected [{self.L}, {B}, {h}, {HEAD_DIM}], got {tuple(t.shape)}")
+        if out is None:
+            out = torch.empty((self.L, B, NUM_Q_HEADS, HEAD_DIM), dtype=torch.bfloat16,
+                              device=self.dev)
+        if B == 0:
+            return out
+        ms = int(batch.lens_h.max())
+        ws = self.workspace
+        for l in range(self.L):
+            bt = batch.tables[l]
+            if self.fused:
+                step = paged_gqa_decode_append_int8 if self.int8 else paged_gqa_decode_append
+                step(q[l], k[l], v[l], self.pool, bt, batch.lens, out[l], self.cos, self.sin,
+                     self.scale, workspace=ws, max_seq_len=ms, d_err=self.d_err)
+            else:
+                q_rot = torch.empty_like(q[l])
+                append = kv_append_rope_int8 if self.int8 else kv_append_rope
+                decode = paged_gqa_decode_int8 if self.int8 else paged_gqa_decode
+                append(k[l], v[l], batch.positions, bt, self.pool, self.cos, self.sin, q_in=q[l],
+                       q_out=q_rot, d_err=self.d_err)
+                decode(q_rot, self.pool, bt, batch.lens, out[l], self.scale, workspace=ws,
+                       max_seq_len=ms, d_err=self.d_err)
+        return out
+
+    def step(self, token_kv, token_q):
+        """One decode step for every running request, inputs from callbacks.
 
         token_kv(rid, layer, pos) -> (k [8, 64], v [8, 64]); token_q(rid, layer,
         pos) -> q [32, 64] (un-rotated).  Returns (running ids, lengths after
         the step, outputs [L, B, 32, 64] bf16 on the device).
         """
-        ids = list(self.running)
-        B = len(ids)
-        for rid in ids:
-            if self.sched.grow(rid, self.length[rid] + 1) != OK:
-                raise PkvError(7, "ContinuousBatcher.step")
-            if self.length[rid] % PAGE_TOKENS == 0:      # a new page in every layer
-                self._sync_rows(rid)
-        lens_h = np.array([self.length[r] + 1 for r in ids], np.int32)
-        slots = torch.tensor([self.slot[r] for r in ids], dtype=torch.long, device=self.dev)
-        lens = torch.from_numpy(lens_h).to(self.dev)
-        pos = lens - 1
-        out = torch.empty((self.L, B, 32, 64), dtype=torch.bfloat16, device=self.dev)
-        ws = self.workspace
+        batch = self.prepare_step()
+        if not batch.ids:
+            return [], batch.lens_h, torch.empty((self.L, 0, NUM_Q_HEADS, HEAD_DIM),
+                                                 dtype=torch.bfloat16, device=self.dev)
+        pos = [int(p) for p in batch.lens_h - 1]
+        qs, ks, vs = [], [], []
         for l in range(self.L):
-            q = torch.stack([token_q(r, l, self.length[r]) for r in ids]).to(self.dev)
-            kv = [token_kv(r, l, self.length[r]) for r in ids]
-            k = torch.stack([a for a, _ in kv]).to(self.dev)
-            v = torch.stack([b for _, b in kv]).to(self.dev)
-            bt = self.tables[l].index_select(0, slots).contiguous()
-            if self.fused:
-                step = paged_gqa_decode_append_int8 if self.int8 else paged_gqa_decode_append
-                step(q, k, v, self.pool, bt, lens, out[l], self.cos, self.sin, self.scale,
-                     workspace=ws, d_err=self.d_err)
-            else:
-                q_rot = torch.empty_like(q)
-                append = kv_append_rope_int8 if self.int8 else kv_append_rope
-                decode = paged_gqa_decode_int8 if self.int8 else paged_gqa_decode
-                append(k, v, pos, bt, self.pool, self.cos, self.sin, q_in=q, q_out=q_rot,
-                       d_err=self.d_err)
-                decode(q_rot, self.pool, bt, lens, out[l], self.scale, workspace=ws,
-                       d_err=self.d_err)
-        for rid in ids:
-            self.length[rid] += 1
-            self.steps_done[rid] += 1
-        return ids, lens_h, out
+            qs.append(torch.stack([token_q(r, l, p) for r, p in zip(batch.ids, pos)]))
+            kv = [token_kv(r, l, p) for r, p in zip(batch.ids, pos)]
+            ks.append(torch.stack([a for a, _ in kv]))
+            vs.append(torch.stack([b for _, b in kv]))
+        q, k, v = (torch.stack(x).to(self.dev) for x in (qs, ks, vs))
+        return batch.ids, batch.lens_h, self.launch_step(batch, q, k, v)
 
     def retire(self, decode_steps: int):
         """Finish requests that have done `decode_steps` steps; frees their pages."""
