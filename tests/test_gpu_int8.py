@@ -14,7 +14,8 @@ import torch
 
 import workloads as W
 from oracle import bf16 as OB, int8_kv as OI, rope as OR
-from tests._util import MAX_ABS_TOL, MEAN_ABS_TOL, bf16_to_f64, bits, to_dev_bf16, to_dev_i32
+from tests._util import (bf16_to_f64, bits, check_close_int8,
+                         to_dev_bf16, to_dev_i32)
 from tests.test_gpu_parity import edge_case, make_case, rand_bits
 
 pytestmark = pytest.mark.gpu
@@ -33,25 +34,6 @@ def tables(lib, cuda_device):
     cos_d, sin_d = lib.rope_tables_device(cuda_device, 2048)
     cos_o, sin_o = OR.table(OR.inv_freq_llama3(), 2048)
     return cos_d, sin_d, cos_o, sin_o
-
-
-def check_close_int8(gpu, ref, what=""):
-    """The bf16 bar applied to the error beyond the output format's own
-    rounding: max |err| <= 1.5e-2 + 2^-8 |ref| where |ref| >= 4 (a bf16 half
-    step there exceeds 1.5e-2), and mean |err| <= 1e-3 + the mean distance of
-    the FP64 values to their nearest bf16 (the dequantised values, unlike bf16
-    pages, are not bf16 numbers, so an output dominated by one token carries
-    the full rounding of the bf16 result)."""
-    gpu = gpu.astype(np.float64)
-    err = np.abs(gpu - ref)
-    assert np.all(np.isfinite(gpu)), f"{what}: non-finite GPU output"
-    allowed = MAX_ABS_TOL + np.where(np.abs(ref) >= 4.0, 2.0 ** -8 * np.abs(ref), 0.0)
-    worst = int(np.argmax(err - allowed))
-    assert np.all(err <= allowed), f"{what}: |err| {err.flat[worst]:.3e} at |ref| {abs(ref.flat[worst]):.3f}"
-    rounding = np.abs(ref - OB.to_f64(OB.from_f64_via_f32(ref))).mean()
-    assert err.mean() <= MEAN_ABS_TOL + rounding, \
-        f"{what}: mean |err| {err.mean():.3e} (output rounding alone {rounding:.3e})"
-    return float(err.max()), float(err.mean())
 
 
 def dev_pool(codes, scales, dev):
