@@ -493,6 +493,67 @@ def paged_gqa_decode_append(q, k_new, v_new, kv_pool, block_tables, seq_lens, ou
     _check(st, "paged_gqa_decode_append")
 
 
+def paged_gqa_decode_append_layers(q, k_new, v_new, kv_pool, block_tables, seq_lens, out,
+                                   rope_cos, rope_sin, scale, workspace, max_seq_len=None,
+                                   d_err=None, stream=None):
+    """A whole decode step: for every layer l, the fused append + decode of
+    q[l], k_new[l], v_new[l] over block_tables[l] into out[l] on a bf16 pool
+    (paged_gqa_decode_append) or an INT8 pool (paged_gqa_decode_append_int8),
+    in layer order on one stream.
+
+    q, out: [L, S, 32, 64] bf16; k_new, v_new: [L, S, 8, 64] bf16;
+    block_tables: [L, S', row_stride] int32 with S' >= S; seq_lens: [S] int32,
+    shared by the layers.  The C calls and their arguments are exactly those
+    of L calls of the per-layer binding with default options; the arguments
+    are checked once, which is what a serving loop saves per step.
+    """
+    dev = kv_pool.device
+    int8 = kv_pool.dtype == torch.uint8
+    if int8:
+        _need_i8_pool(kv_pool, dev)
+    else:
+        _need(kv_pool, "kv_pool", torch.bfloat16, dev, (2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM))
+    for t, name, heads in ((q, "q", NUM_Q_HEADS), (out, "out", NUM_Q_HEADS),
+                           (k_new, "k_new", NUM_KV_HEADS), (v_new, "v_new", NUM_KV_HEADS)):
+        _need(t, name, torch.bfloat16, dev, (heads, HEAD_DIM))
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [layers, num_seqs, {heads}, {HEAD_DIM}]")
+    L, S = q.shape[0], q.shape[1]
+    if out.shape != q.shape or k_new.shape[:2] != (L, S) or v_new.shape != k_new.shape:
+        raise ValueError("q/out [L, S, 32, 64] and k_new/v_new [L, S, 8, 64] must agree")
+    if L == 0:
+        return
+    _need(block_tables, "block_tables", torch.int32, dev)
+    if block_tables.dim() != 3 or block_tables.shape[0] != L or block_tables.shape[1] < S:
+        raise ValueError("block_tables must be [layers, >= num_seqs, row_stride]")
+    _need(seq_lens, "seq_lens", torch.int32, dev)
+    if seq_lens.numel() != S:
+        raise ValueError("seq_lens must have num_seqs entries")
+    _need(rope_cos, "rope_cos", torch.float32, dev, (ROPE_PAIRS,))
+    _need(rope_sin, "rope_sin", torch.float32, dev, (ROPE_PAIRS,))
+    _need(workspace, "workspace", torch.uint8, dev)
+    if d_err is not None:
+        _need(d_err, "d_err", torch.int32, dev)
+    stride = block_tables.shape[2]
+    if max_seq_len is None:
+        max_seq_len = PAGE_TOKENS * stride
+    opts = DecodeOpts(COMPUTE_TENSOR, 0, 0, 0, 0, 0, 0, 0)
+    fn = _L().paged_gqa_decode_append_int8 if int8 else _L().paged_gqa_decode_append
+    where = "paged_gqa_decode_append_int8" if int8 else "paged_gqa_decode_append"
+    # contiguous [L, ...] tensors: layer l starts l x (bytes per layer) in
+    steps = [t.data_ptr() for t in (q, k_new, v_new, block_tables, out)]
+    sizes = [t[0].numel() * t.element_size() for t in (q, k_new, v_new, block_tables, out)]
+    common = (_ptr(rope_cos), _ptr(rope_sin), rope_cos.shape[0], _ptr(kv_pool), kv_pool.shape[0])
+    tail = (_ptr(seq_lens), S, int(max_seq_len), None)
+    ws = (float(scale), _ptr(workspace), workspace.numel(), _ptr(d_err), _stream(stream),
+          ctypes.byref(opts))
+    for l in range(L):
+        pq, pk, pv, pbt, po = (b + l * n for b, n in zip(steps, sizes))
+        st = fn(ctypes.c_void_p(pq), ctypes.c_void_p(pk), ctypes.c_void_p(pv), *common,
+                ctypes.c_void_p(pbt), stride, stride, *tail, ctypes.c_void_p(po), *ws)
+        _check(st, where)
+
+
 PREFILL_MMA_SYNC = 2  # comparison arm of paged_gqa_prefill (legacy bf16 mma.sync)
 
 

@@ -13,8 +13,8 @@ on the device per slot ([L][max_slots][max_blocks]), and each step gathers
 the running sequences' rows into a packed batch table.  The caller supplies
 the new K/V/q values through callbacks, so any model (or a synthetic source)
 can drive it.  Nothing here computes attention: every token goes through
-kv_append_rope / paged_gqa_decode(_append), or their INT8-page forms when the
-pool is an INT8 pool.
+kv_append_rope / paged_gqa_decode / paged_gqa_decode_append(_layers), or
+their INT8-page forms when the pool is an INT8 pool.
 """
 from __future__ import annotations
 
@@ -24,9 +24,8 @@ import numpy as np
 import torch
 
 from . import (HEAD_DIM, NUM_KV_HEADS, NUM_Q_HEADS, OK, PAGE_TOKENS, PkvError, Scheduler,
-               alloc_workspace, kv_append_rope,
-               kv_append_rope_int8, paged_gqa_decode, paged_gqa_decode_append,
-               paged_gqa_decode_append_int8, paged_gqa_decode_int8, pkv_read_device_error,
+               alloc_workspace, kv_append_rope, kv_append_rope_int8, paged_gqa_decode,
+               paged_gqa_decode_append_layers, paged_gqa_decode_int8, pkv_read_device_error,
                ERR_REQUEST_TOO_LARGE)
 
 
@@ -176,20 +175,20 @@ class ContinuousBatcher:
             return out
         ms = int(batch.lens_h.max())
         ws = self.workspace
+        if self.fused:        # one checked call issues the L per-layer launches
+            paged_gqa_decode_append_layers(q, k, v, self.pool, batch.tables, batch.lens, out,
+                                           self.cos, self.sin, self.scale, ws, max_seq_len=ms,
+                                           d_err=self.d_err)
+            return out
+        append = kv_append_rope_int8 if self.int8 else kv_append_rope
+        decode = paged_gqa_decode_int8 if self.int8 else paged_gqa_decode
         for l in range(self.L):
             bt = batch.tables[l]
-            if self.fused:
-                step = paged_gqa_decode_append_int8 if self.int8 else paged_gqa_decode_append
-                step(q[l], k[l], v[l], self.pool, bt, batch.lens, out[l], self.cos, self.sin,
-                     self.scale, workspace=ws, max_seq_len=ms, d_err=self.d_err)
-            else:
-                q_rot = torch.empty_like(q[l])
-                append = kv_append_rope_int8 if self.int8 else kv_append_rope
-                decode = paged_gqa_decode_int8 if self.int8 else paged_gqa_decode
-                append(k[l], v[l], batch.positions, bt, self.pool, self.cos, self.sin, q_in=q[l],
-                       q_out=q_rot, d_err=self.d_err)
-                decode(q_rot, self.pool, bt, batch.lens, out[l], self.scale, workspace=ws,
-                       max_seq_len=ms, d_err=self.d_err)
+            q_rot = torch.empty_like(q[l])
+            append(k[l], v[l], batch.positions, bt, self.pool, self.cos, self.sin, q_in=q[l],
+                   q_out=q_rot, d_err=self.d_err)
+            decode(q_rot, self.pool, bt, batch.lens, out[l], self.scale, workspace=ws,
+                   max_seq_len=ms, d_err=self.d_err)
         return out
 
     def step(self, token_kv, token_q):

@@ -132,6 +132,16 @@ def paged_gqa_decode_append_int8(q, k_new, v_new, kv_pool, block_tables, seq_len
     _flag(err, d_err)
 
 
+def paged_gqa_decode_append_layers(q, k_new, v_new, kv_pool, block_tables, seq_lens, out,
+                                   rope_cos, rope_sin, scale, workspace, max_seq_len=None,
+                                   d_err=None, stream=None):
+    assert q.dim() == 4 and block_tables.dim() == 3 and block_tables.shape[0] == q.shape[0]
+    step = paged_gqa_decode_append_int8 if kv_pool.dtype == torch.uint8 else paged_gqa_decode_append
+    for l in range(q.shape[0]):
+        step(q[l], k_new[l], v_new[l], kv_pool, block_tables[l], seq_lens, out[l], rope_cos,
+             rope_sin, scale, workspace=workspace, max_seq_len=max_seq_len, d_err=d_err)
+
+
 def alloc_workspace(num_seqs, device):
     return torch.zeros(16, dtype=torch.uint8)
 
@@ -144,13 +154,16 @@ def pkv_read_device_error(d_err, clear=True, stream=None):
 
 
 NAMES = ("kv_append_rope", "kv_append_rope_int8", "paged_gqa_decode", "paged_gqa_decode_int8",
-         "paged_gqa_decode_append", "paged_gqa_decode_append_int8", "alloc_workspace",
+         "paged_gqa_decode_append", "paged_gqa_decode_append_int8",
+         "paged_gqa_decode_append_layers", "alloc_workspace",
          "pkv_read_device_error")
 
 
 def patch_serving(monkeypatch):
-    """Point serving's kernel calls at the stand-ins above."""
+    """Point serving's kernel calls (the ones it imports) at the stand-ins above."""
     import paged_kv_gqa_append_gb300.serving as S
     g = globals()
-    for n in NAMES:
+    patched = [n for n in NAMES if hasattr(S, n)]
+    for n in patched:
         monkeypatch.setattr(S, n, g[n])
+    assert "paged_gqa_decode_append_layers" in patched and "paged_gqa_decode" in patched

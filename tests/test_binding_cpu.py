@@ -1,0 +1,111 @@
+"""Binding-level checks that need no GPU: the C calls the Python binding
+makes, recorded by a stand-in for the loaded library.
+
+paged_gqa_decode_append_layers must make exactly the C calls (same entry
+point, same arguments, same order) that L calls of the per-layer binding
+make, so that the per-layer path's GPU parity carries over to it.
+"""
+import ctypes
+import types
+
+import pytest
+import torch
+
+import paged_kv_gqa_append_gb300 as pkv
+
+BF16, I32 = torch.bfloat16, torch.int32
+
+
+class Recorder:
+    """Stands in for libpkv.so: records each call's entry point and arguments
+    (pointers as integers, option structs as field tuples) and returns OK."""
+
+    def __init__(self):
+        self.calls = []
+
+    def __getattr__(self, name):
+        def call(*args):
+            self.calls.append((name, tuple(self._norm(a) for a in args)))
+            return pkv.OK
+        return call
+
+    @staticmethod
+    def _norm(a):
+        if isinstance(a, ctypes.c_void_p):
+            return a.value
+        if type(a).__name__ == "CArgObject":
+            obj = a._obj
+            return tuple(getattr(obj, f) for f, _ in obj._fields_)
+        return a
+
+    def take(self):
+        out, self.calls = self.calls, []
+        return out
+
+
+def tensors(int8, L=3, S=5, S_rows=7, row_stride=128):
+    pool = (pkv.new_int8_pool(11, "cpu") if int8
+            else torch.zeros((11, 2, 8, 16, 64), dtype=BF16))
+    return dict(
+        q=torch.zeros((L, S, 32, 64), dtype=BF16), k=torch.zeros((L, S, 8, 64), dtype=BF16),
+        v=torch.zeros((L, S, 8, 64), dtype=BF16), out=torch.zeros((L, S, 32, 64), dtype=BF16),
+        bt=torch.zeros((L, S_rows, row_stride), dtype=I32), lens=torch.zeros(S, dtype=I32),
+        cos=torch.zeros((64, 32)), sin=torch.zeros((64, 32)),
+        ws=torch.zeros(4096, dtype=torch.uint8), err=torch.zeros(1, dtype=I32), pool=pool)
+
+
+@pytest.fixture
+def rec(monkeypatch):
+    r = Recorder()
+    monkeypatch.setattr(pkv, "_L", lambda: r)
+    return r
+
+
+STREAM = types.SimpleNamespace(cuda_stream=0x1234)
+
+
+@pytest.mark.parametrize("int8", [False, True])
+@pytest.mark.parametrize("max_seq_len", [None, 77])
+def test_layers_call_makes_the_per_layer_calls(rec, int8, max_seq_len):
+    t = tensors(int8)
+    per_layer = pkv.paged_gqa_decode_append_int8 if int8 else pkv.paged_gqa_decode_append
+    for l in range(t["q"].shape[0]):
+        per_layer(t["q"][l], t["k"][l], t["v"][l], t["pool"], t["bt"][l], t["lens"], t["out"][l],
+                  t["cos"], t["sin"], 0.125, workspace=t["ws"], max_seq_len=max_seq_len,
+                  d_err=t["err"], stream=STREAM)
+    want = rec.take()
+    pkv.paged_gqa_decode_append_layers(t["q"], t["k"], t["v"], t["pool"], t["bt"], t["lens"],
+                                       t["out"], t["cos"], t["sin"], 0.125, t["ws"],
+                                       max_seq_len=max_seq_len, d_err=t["err"], stream=STREAM)
+    got = rec.take()
+    assert len(got) == 3 and got == want
+    name = "paged_gqa_decode_append_int8" if int8 else "paged_gqa_decode_append"
+    assert {c[0] for c in got} == {name}
+    # the per-layer pointers step through the layers
+    assert [c[1][0] for c in got] == [t["q"][l].data_ptr() for l in range(3)]
+    assert [c[1][8] for c in got] == [t["bt"][l].data_ptr() for l in range(3)]
+
+
+@pytest.mark.parametrize("bad", ["out_shape", "kv_layers", "tables_layers", "tables_rows",
+                                 "lens", "not_4d", "strided"])
+def test_layers_call_rejects_bad_shapes_before_any_call(rec, bad):
+    t = tensors(False)
+    if bad == "out_shape":
+        t["out"] = t["out"][:, :4].contiguous()
+    elif bad == "kv_layers":
+        t["k"] = t["k"][:2].contiguous()
+    elif bad == "tables_layers":
+        t["bt"] = t["bt"][:2].contiguous()
+    elif bad == "tables_rows":
+        t["bt"] = t["bt"][:, :4].contiguous()
+    elif bad == "lens":
+        t["lens"] = t["lens"][:4].contiguous()
+    elif bad == "not_4d":
+        t["q"] = t["q"].reshape(15, 32, 64)
+    elif bad == "strided":
+        t["q"] = torch.zeros((5, 3, 32, 64), dtype=BF16).transpose(0, 1)
+    with pytest.raises((ValueError, TypeError)):
+        pkv.paged_gqa_decode_append_layers(t["q"], t["k"], t["v"], t["pool"], t["bt"], t["lens"],
+                                           t["out"], t["cos"], t["sin"], 0.125, t["ws"],
+                                           d_err=t["err"], stream=STREAM)
+    assert rec.calls == []
