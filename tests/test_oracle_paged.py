@@ -3,9 +3,12 @@
 The decode definition is checked against closed forms (one token, identical
 keys, two tokens, constant V), linearity, page-permutation invariance, torch's
 scaled_dot_product_attention on a contiguous FP64 copy, and a 50-digit mpmath
-brute force; the append is checked by a brute-force scan of a sentinel pool.
+brute force; the append is checked by a brute-force scan of a sentinel pool;
+the page geometry against the sizes the pages print (tests/golden/).
 """
+import json
 import math
+import os
 
 import numpy as np
 import pytest
@@ -330,3 +333,18 @@ def test_decode_step_is_append_then_decode():
     _, qr3, out3, err3 = P.decode_step(pool, q, k, v, bt_big, lens_bad, cos, sin, 0.125)
     assert err3 and np.all(out3[4] == 0) and np.all(qr3[4] == 0)
     assert np.array_equal(out3[:3], out[:3])
+
+
+def test_page_geometry_matches_the_printed_sizes():
+    # sizes the pages print (tests/golden/page_geometry.json, cited there)
+    with open(os.path.join(os.path.dirname(__file__), "golden", "page_geometry.json")) as f:
+        g = json.load(f)
+    pool1 = P.new_pool(1)
+    page_bytes = pool1.nbytes
+    assert page_bytes * g["kv_cache_pages"] == g["kv_cache_bytes"]     # 65536 pages fill 2 GiB
+    k_row = pool1[0, 0, :, 0, :].nbytes            # one token's K over every KV head
+    assert k_row == g["kv_dim"] * 2
+    assert g["max_prompt_len"] * k_row == g["prefill_k_temp_bytes"]
+    assert g["decode_batch_slots"] * k_row == g["decode_k_batch_bytes"]
+    assert P.PAGE_TOKENS == g["page_tokens"] == pool1.shape[3]
+    assert g["default_pool_mib"] * 2 ** 20 // page_bytes == W.case_continuous().num_pages == 4096
