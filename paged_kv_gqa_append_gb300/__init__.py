@@ -39,7 +39,8 @@ STATUS = {
     6: "PKV_ERR_DEVICE_INDEX", 7: "PKV_ERR_POOL_EXHAUSTED", 8: "PKV_ERR_REQUEST_TOO_LARGE",
     9: "PKV_ERR_TIMEOUT",
 }
-OK, ERR_DEVICE_INDEX, ERR_POOL_EXHAUSTED, ERR_REQUEST_TOO_LARGE, ERR_TIMEOUT = 0, 6, 7, 8, 9
+OK, ERR_INVALID_ARGUMENT, ERR_DEVICE_INDEX, ERR_POOL_EXHAUSTED = 0, 1, 6, 7
+ERR_REQUEST_TOO_LARGE, ERR_TIMEOUT = 8, 9
 
 
 class PkvError(RuntimeError):

@@ -208,3 +208,50 @@ def test_scheduler_rejects_and_blocks():
     row, slot = s.block_table(1, 1)
     assert list(row[:3]) == [2, 3, -1] and slot == 0
     assert s.stats() == dict(free=16, reserved=16, queued=1, running=1)
+
+
+def test_scheduler_misuse_is_refused_without_state_change():
+    # the C scheduler's contract for calls out of order or out of range:
+    # PKV_ERR_INVALID_ARGUMENT, and nothing allocated or released
+    lib, INV = pkv.lib, pkv.ERR_INVALID_ARGUMENT
+    i = ctypes.c_int
+    assert not lib.pkv_sched_create(0, 2, 8, 4) and not lib.pkv_sched_create(16, 2, 8, 0)
+    assert lib.pkv_sched_set_mode(None, 0) == INV
+    assert lib.pkv_sched_grow(None, 0, 1) == INV and lib.pkv_sched_finish(None, 0) == INV
+    assert lib.pkv_sched_event_count(None) == -1
+    s = lib.pkv_sched_create(16, 2, 4, 2)
+    assert s
+    try:
+        rid, n, adm = i(-7), i(-1), (i * 4)()
+        assert lib.pkv_sched_set_mode(s, 2) == INV
+        assert lib.pkv_sched_submit(s, 0, 5, ctypes.byref(rid)) == INV
+        assert lib.pkv_sched_submit(s, 5, 0, ctypes.byref(rid)) == INV
+        assert lib.pkv_sched_submit(s, 5, 5, None) == INV
+        # 62 + 5 - 1 tokens need 5 pages a layer, past max_blocks 4
+        assert lib.pkv_sched_submit(s, 62, 5, ctypes.byref(rid)) == pkv.ERR_REQUEST_TOO_LARGE
+        assert rid.value == -1
+        assert lib.pkv_sched_submit(s, 20, 5, ctypes.byref(rid)) == pkv.OK and rid.value == 0
+        assert lib.pkv_sched_grow(s, 0, 1) == INV      # still queued
+        assert lib.pkv_sched_finish(s, 0) == INV       # still queued
+        assert lib.pkv_sched_admit(s, None, 4, ctypes.byref(n)) == INV
+        assert lib.pkv_sched_admit(s, adm, -1, ctypes.byref(n)) == INV
+        assert lib.pkv_sched_admit(s, adm, 4, ctypes.byref(n)) == pkv.OK and n.value == 1
+        assert lib.pkv_sched_grow(s, 1, 1) == INV      # unknown id
+        assert lib.pkv_sched_grow(s, 0, -1) == INV
+        assert lib.pkv_sched_grow(s, 0, 4 * 16 + 1) == INV      # past max_blocks
+        assert lib.pkv_sched_grow(s, 0, 20) == pkv.OK
+        assert lib.pkv_sched_grow(s, 0, 33) == pkv.ERR_POOL_EXHAUSTED   # past its credit
+        row = (ctypes.c_int32 * 4)()
+        assert lib.pkv_sched_block_table(s, 0, 2, row, None) == INV     # layer out of range
+        assert lib.pkv_sched_block_table(s, 0, 1, None, None) == INV
+        assert lib.pkv_sched_event(s, lib.pkv_sched_event_count(s), None, None, None, None) == INV
+        free = i(0)
+        assert lib.pkv_sched_stats(s, ctypes.byref(free), None, None, None) == pkv.OK
+        assert free.value == 16 - 4                    # 2 layers x 2 pages taken
+        assert lib.pkv_sched_finish(s, 0) == pkv.OK
+        assert lib.pkv_sched_finish(s, 0) == INV       # finished twice
+        assert lib.pkv_sched_grow(s, 0, 1) == INV      # finished
+        assert lib.pkv_sched_stats(s, ctypes.byref(free), None, None, None) == pkv.OK
+        assert free.value == 16
+    finally:
+        lib.pkv_sched_destroy(s)
