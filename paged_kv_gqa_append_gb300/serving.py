@@ -77,7 +77,9 @@ class ContinuousBatcher:
 
     # -- requests -------------------------------------------------------------
     def submit(self, prompt_tokens: int, new_tokens: int):
-        """Queue a request; returns its id, or -1 when it can never fit."""
+        """Queue a request; returns its id, or -1 when it can never fit.
+        Raises PkvError for an invalid request (fewer than one prompt or new
+        token)."""
         st, rid = self.sched.submit(prompt_tokens, new_tokens)
         if st == ERR_REQUEST_TOO_LARGE:
             self.rejected.append((prompt_tokens, new_tokens))

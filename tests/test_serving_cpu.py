@@ -101,3 +101,6 @@ def test_oversize_request_is_rejected(serving_on_oracle):
     assert cb.submit(64, 33) == -1
     assert cb.rejected == [(64, 33)]
     assert cb.submit(16, 17) >= 0          # 2 x 2 pages fits
+    with pytest.raises(pkv.PkvError):
+        cb.submit(0, 5)                    # no prompt token
+    assert list(cb.prompt) == [0]
