@@ -171,6 +171,24 @@ class ClockSampler:
 
 # ------------------------------------------------------------- roofline ----
 
+def env_info(dev):
+    """The device and software a line was measured on (never raises)."""
+    info = {"gpu": None, "sms": None, "cuda": torch.version.cuda, "torch": torch.__version__,
+            "pkv_version": None}
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        info["gpu"], info["sms"] = props.name, props.multi_processor_count
+    except Exception:
+        pass
+    try:
+        import paged_kv_gqa_append_gb300 as pkv
+        v = int(pkv.lib.pkv_version())
+        info["pkv_version"] = f"{v // 10000}.{v // 100 % 100}.{v % 100}"
+    except Exception:
+        pass
+    return info
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -569,7 +587,7 @@ def run_gb300(args, world, rank, local):
             "kv_bytes_per_step": kv_bytes_layer * L,
             "hbm_frac_step": value / world / peak,
             "clocks": clk, "e2e": e2e, "gpu_launches": step.launches_per_step * steps,
-            "roofline": roof, "cpu_baseline": cpu,
+            "roofline": roof, "env": env_info(dev), "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
 
@@ -705,7 +723,7 @@ def run_int8_line(args, world, rank, local):
             "decode_only_us_per_layer": dec_only_ms * 1e3, "append_us_per_layer": append_us,
             "kv_bytes_per_step": kv_bytes_layer * L, "hbm_frac_step": value / world / peak,
             "clocks": clk, "e2e": e2e, "gpu_launches": step.launches_per_step * steps,
-            "roofline": roof, "cpu_baseline": cpu}), flush=True)
+            "roofline": roof, "env": env_info(dev), "cpu_baseline": cpu}), flush=True)
 
 
 # ------------------------------------------- the small decode cases ------
@@ -817,7 +835,7 @@ def run_small_line(args, world, rank, local):
                          "frac": value / world / peak, "traffic": None, "peak_source": peak_kind,
                          "kernel": "paged_decode_kernel (paged_gqa_decode, L2 flushed before each launch)",
                          "avg_launch_us": us_flushed, "algorithmic_bytes_per_launch": kv_bytes},
-            "cpu_baseline": cpu}), flush=True)
+            "env": env_info(dev), "cpu_baseline": cpu}), flush=True)
 
 
 # ------------------------------------------------ continuous-batching line --
@@ -996,7 +1014,7 @@ def run_continuous_line(args, world, rank, local):
                          "kernel": "paged_decode_append (one launch per layer and step)",
                          "launches_timed": steps * L, "avg_launch_us": total_ms * 1e3 / (steps * L),
                          "algorithmic_bytes_per_launch": kv_bytes / (steps * L)},
-            "cpu_baseline": cpu}), flush=True)
+            "env": env_info(dev), "cpu_baseline": cpu}), flush=True)
 
 
 # ------------------------------------------------ prefill and argmax lines --
@@ -1121,7 +1139,7 @@ def run_prefill_line(args, world, rank, local):
                          "unit": "TFLOP/s", "frac": value / world / peak, "traffic": None,
                          "peak_source": kind, "kernel": "paged_prefill_tc_kernel (tcgen05 bf16, S and O in tensor memory)",
                          "avg_launch_us": avg_us, "algorithmic_flops_per_launch": flops},
-            "cpu_baseline": cpu}), flush=True)
+            "env": env_info(dev), "cpu_baseline": cpu}), flush=True)
 
 
 ARGMAX_ROWS, ARGMAX_VOCAB, ARGMAX_BUFS = 32, 128256, 12   # 12 x 16.4 MB > L2
@@ -1201,7 +1219,7 @@ def run_argmax_line(args, world, rank, local):
                          "frac": value / world / peak, "traffic": None, "peak_source": kind,
                          "kernel": "argmax_kernel", "avg_launch_us": ms * 1e3 / steps,
                          "algorithmic_bytes_per_launch": nbytes},
-            "cpu_baseline": cpu}), flush=True)
+            "env": env_info(dev), "cpu_baseline": cpu}), flush=True)
 
 
 def main():
