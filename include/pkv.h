@@ -247,9 +247,15 @@ int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_pages,
  *     array (on a 152-SM GB300: up to 343 sequences per call); larger
  *     batches return PKV_ERR_WORKSPACE_TOO_SMALL and pkv_last_error() says
  *     why.
- *   - The first call on each device looks up the array's device address
- *     (with that device current); make that first call before any stream
- *     capture.
+ *   - Arguments are checked (as paged_gqa_decode checks them) before
+ *     anything touches the device or the array.
+ *   - Each call made outside stream capture looks up the array's device
+ *     address (with the stream's device current), so a device reset does not
+ *     leave a stale address behind.  A call made while `stream` is being
+ *     captured reuses the address of the last uncaptured call on the current
+ *     device: make the first call on each device before any capture (a first
+ *     call under capture returns PKV_ERR_CUDA), and make the captured
+ *     stream's device current.
  *   - Every call on a device shares the array: calls whose kernels may run
  *     at the same time on the GPU race with each other.  Each call clears the
  *     part that must start at zero (on `stream`) before its kernel runs.

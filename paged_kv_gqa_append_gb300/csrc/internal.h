@@ -37,4 +37,11 @@ inline int cuda_status(cudaError_t e, const char* where = "cuda") {
 int make_pool_map(CUtensorMap* map, const void* pool, int num_pages);
 // The same view with a one-tile box {64, 16, 1, 1}.
 int make_pool_tile_map(CUtensorMap* map, const void* pool, int num_pages);
+
+// The host-side argument checks of paged_gqa_decode that need no workspace
+// and no CUDA call (sizes, null pointers, alignment, the scale): PKV_OK or
+// the status the decode call would return for these arguments.
+int decode_check_args(const void* q, const void* kv_pool, int num_pages,
+                      const int32_t* block_tables, int bt_row_stride, int max_blocks,
+                      const int32_t* seq_lens, int num_seqs, const void* out, float scale);
 }  // namespace pkv

@@ -258,15 +258,20 @@ __device__ __forceinline__ uint32_t range_start(uint32_t k, uint32_t U, uint32_t
 }
 
 // ---------------------------------------------------------------------------
-// Merging records.  Lane (hh = lane/8, dims d0 = 8*(lane%8) .. d0+8) keeps an
-// online log-sum-exp merge of the records it is given:
-//   M' = max(M, m_k);  acc = acc e^(M - M') + o_k e^(m_k - M');
-//   L = L e^(M - M') + l_k e^(m_k - M').
+// Merging records.  Lane (hh = lane/8, r = lane%8) keeps head hh, dims
+// 4r .. 4r+3 (acc[0..3]) and 32+4r .. 32+4r+3 (acc[4..7]): a quarter-warp's
+// 16-byte reads of a record row then cover 128 contiguous bytes, free of
+// bank conflicts.  Records are combined by the log-sum-exp rule
+//   M = max_k m_k,  o = sum_k 2^(m_k - M) o_k,  l = sum_k 2^(m_k - M) l_k.
 // ---------------------------------------------------------------------------
 struct MergeAcc {
   float acc[8];
   float M, L;
   bool bad;
+
+  // byte offsets of this lane's two dim groups in a record's o[4][64]
+  __device__ static __forceinline__ uint32_t off0(int lane) { return (uint32_t)((lane >> 3) * 256 + (lane & 7) * 16); }
+  static constexpr uint32_t kOff1 = 128;  // + 32 dims
 
   __device__ __forceinline__ void init() {
 #pragma unroll
@@ -276,6 +281,8 @@ struct MergeAcc {
     bad = false;
   }
 
+  // Online form, one record at a time (the dynamic schedule's merges):
+  //   M' = max(M, m);  acc = acc 2^(M - M') + o 2^(m - M');  L likewise.
   __device__ __forceinline__ void add(float2 ml, float4 o0, float4 o1) {
     if (ml.y < 0.f) {
       bad = true;
@@ -293,62 +300,129 @@ struct MergeAcc {
 
   // record in shared memory
   __device__ __forceinline__ void add_shared(const Record& r, int lane) {
-    const int hh = lane >> 3, d0 = (lane & 7) * 8;
-    const float4* src = reinterpret_cast<const float4*>(r.o + hh * 64 + d0);
-    add(r.ml[hh], src[0], src[1]);
+    const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const uint8_t*>(r.o) + off0(lane));
+    add(r.ml[lane >> 3], src[0], src[kOff1 / 16]);
   }
 
-  // Merge of records in shared memory in two passes: the largest m first, then
-  // the sum of the rescaled records (independent terms, no rescale chain).
-  // `each(f)` calls f(record) for every record to merge.
-  template <class Each>
-  __device__ __forceinline__ void merge_shared(Each each, int lane) {
-    const int hh = lane >> 3, d0 = (lane & 7) * 8;
-    float Mx = -INFINITY;
-    each([&](const Record& r) {
-      const float2 ml = r.ml[hh];
-      if (ml.y < 0.f) bad = true;
-      else Mx = fmaxf(Mx, ml.x);
-    });
-    each([&](const Record& r) {
-      const float2 ml = r.ml[hh];
-      if (ml.y >= 0.f) {
-        const float w = (ml.x == Mx) ? 1.f : exp2f(ml.x - Mx);
-        const float4* src = reinterpret_cast<const float4*>(r.o + hh * 64 + d0);
-        const float4 o0 = src[0], o1 = src[1];
+  // Merge of records 0 .. n-1 (n <= kN; record k at addr(k), skipped when
+  // !live(k)) in two passes, every load of a pass in flight at once: lane
+  // (hh, r) reads (m, l) of head hh of records r, r + 8, ..., the 8 lanes of
+  // a head reduce the largest m, each lane turns its (m, l) into weights
+  // 2^(m - M), and every lane then adds w o over all records for its dims,
+  // the weight of record k coming from lane (hh, k % 8) by a shuffle.  The
+  // sums run in a fixed order, so the result does not depend on timing.
+  // Shared-memory records (kGlobal false) are addressed by 32-bit shared
+  // addresses; records of other CTAs (kGlobal) by pointers, read through L2.
+  template <int kN, bool kGlobal, class Addr, class Live>
+  __device__ __forceinline__ void merge_records(int n, Addr addr, Live live, int lane) {
+    static_assert(kN % 8 == 0 && kN <= 32, "records in groups of 8, at most 32");
+    constexpr int kG = kN / 8;
+    const int hh = lane >> 3, r8 = lane & 7;
+    float mk[kG], lk[kG];
+    bool bd = false;
+#pragma unroll
+    for (int i = 0; i < kG; ++i) {
+      const int k = r8 + 8 * i;
+      mk[i] = -INFINITY;
+      lk[i] = 0.f;
+      if (k < n && live(k)) {
+        const float2 ml = ld_ml(addr(k), hh);
+        if (ml.y < 0.f) {
+          bd = true;
+        } else {
+          mk[i] = ml.x;
+          lk[i] = ml.y;
+        }
+      }
+    }
+    float Mx = mk[0];
+#pragma unroll
+    for (int i = 1; i < kG; ++i) Mx = fmaxf(Mx, mk[i]);
+    Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, 1));
+    Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, 2));
+    Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, 4));
+    bad = bad || __any_sync(0xffffffffu, bd);
+    float wk[kG], Ls = 0.f;
+#pragma unroll
+    for (int i = 0; i < kG; ++i) {
+      wk[i] = mk[i] == -INFINITY ? 0.f : (mk[i] == Mx ? 1.f : exp2f(mk[i] - Mx));
+      Ls += wk[i] * lk[i];
+    }
+#pragma unroll
+    for (int k = 0; k < kN; ++k) {
+      const float w = __shfl_sync(0xffffffffu, wk[k >> 3], (lane & ~7) | (k & 7));
+      if (k < n && live(k)) {  // a bad or vanishing record has weight 0 and finite o
+        float4 o0, o1;
+        ld_o(addr(k), lane, o0, o1);
         acc[0] += w * o0.x; acc[1] += w * o0.y; acc[2] += w * o0.z; acc[3] += w * o0.w;
         acc[4] += w * o1.x; acc[5] += w * o1.y; acc[6] += w * o1.z; acc[7] += w * o1.w;
-        L += w * ml.y;
       }
-    });
+    }
+    Ls += __shfl_xor_sync(0xffffffffu, Ls, 1);
+    Ls += __shfl_xor_sync(0xffffffffu, Ls, 2);
+    Ls += __shfl_xor_sync(0xffffffffu, Ls, 4);
+    L = Ls;
     M = Mx;
   }
 
-  // record in global memory written by another CTA: read through L2 only
-  __device__ __forceinline__ void add_global(const Record& r, int lane) {
-    const int hh = lane >> 3, d0 = (lane & 7) * 8;
-    const float4* src = reinterpret_cast<const float4*>(r.o + hh * 64 + d0);
-    add(__ldcg(r.ml + hh), __ldcg(src), __ldcg(src + 1));
+  // (m, l) of head hh and this lane's o groups of a record: in shared memory
+  // (32-bit address of the record) or written by another CTA (read via L2).
+  __device__ static __forceinline__ float2 ld_ml(uint32_t rec, int hh) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(rec + 1024u + 8u * hh));
+    return v;
+  }
+  __device__ static __forceinline__ float2 ld_ml(const Record& r, int hh) { return __ldcg(r.ml + hh); }
+  __device__ static __forceinline__ void ld_o(uint32_t rec, int lane, float4& o0, float4& o1) {
+    const uint32_t a = rec + off0(lane);
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(o0.x), "=f"(o0.y), "=f"(o0.z), "=f"(o0.w) : "r"(a));
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(o1.x), "=f"(o1.y), "=f"(o1.z), "=f"(o1.w) : "r"(a + kOff1));
+  }
+  __device__ static __forceinline__ void ld_o(const Record& r, int lane, float4& o0, float4& o1) {
+    const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const uint8_t*>(r.o) + off0(lane));
+    o0 = __ldcg(src);
+    o1 = __ldcg(src + kOff1 / 16);
+  }
+
+  // Merge of any number of records written by other CTAs, eight at a time
+  // with merge_records, and the groups combined by the log-sum-exp rule.
+  template <class Rec>
+  __device__ __forceinline__ void merge_global(int n, Rec rec, int lane) {
+    if (n <= 8) {
+      merge_records<8, true>(n, rec, [](int) { return true; }, lane);
+      return;
+    }
+    for (int k0 = 0; k0 < n; k0 += 8) {
+      MergeAcc part;
+      part.init();
+      part.merge_records<8, true>(min(8, n - k0), [&](int k) { return rec(k0 + k); },
+                                  [](int) { return true; }, lane);
+      bad = bad || part.bad;
+      if (part.L > 0.f) {
+        add(make_float2(part.M, part.L), make_float4(part.acc[0], part.acc[1], part.acc[2], part.acc[3]),
+            make_float4(part.acc[4], part.acc[5], part.acc[6], part.acc[7]));
+      }
+    }
   }
 
   __device__ __forceinline__ void store_record(const Record& r, int lane) const {
-    const int hh = lane >> 3, d0 = (lane & 7) * 8;
-    float4* dst = reinterpret_cast<float4*>(r.o + hh * 64 + d0);
+    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(r.o) + off0(lane));
     dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-    if ((lane & 7) == 0) r.ml[hh] = make_float2(M, bad ? -1.f : L);
+    dst[kOff1 / 16] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if ((lane & 7) == 0) r.ml[lane >> 3] = make_float2(M, bad ? -1.f : L);
   }
 
   __device__ __forceinline__ void store_output(const DecodeParams& p, int s, int g, int lane) const {
-    const int hh = lane >> 3, d0 = (lane & 7) * 8;
+    const int hh = lane >> 3, r8 = lane & 7;
     const bool ok = !bad && L > 0.f;
     uint32_t packed[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      packed[i] = pack_bf16x2(ok ? __fdiv_rn(acc[2 * i], L) : 0.f,
-                              ok ? __fdiv_rn(acc[2 * i + 1], L) : 0.f);
-    uint16_t* dst = p.out + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + hh) * 64 + d0;
-    *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      packed[i] = pack_bf16x2(ok ? __fdiv_rn(acc[2 * i], L) : 0.f, ok ? __fdiv_rn(acc[2 * i + 1], L) : 0.f);
+    uint16_t* dst = p.out + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + hh) * 64 + 4 * r8;
+    *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+    *reinterpret_cast<uint2*>(dst + 32) = make_uint2(packed[2], packed[3]);
   }
 };
 
@@ -360,6 +434,14 @@ struct MergeAcc {
 // (8 tiles), K = 16 tokens.  The C layout of S is the A layout of P, so the
 // probabilities never leave registers.
 // ---------------------------------------------------------------------------
+// 2^x by the hardware approximation (results below 2^-126 flush to zero):
+// ex2(0) is 1 and ex2(-inf) is 0, so no special cases are needed here.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 struct NewToken;
 template <int kP>
 struct NewTokenI8;
@@ -478,21 +560,25 @@ struct MmaState : Bf16Pages {
     pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
     pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
     const float mn = fmaxf(m, pm);
-    const float alpha = (m == mn) ? 1.f : exp2f(m - mn);
-    const float p0 = (x0 == mn) ? 1.f : exp2f(x0 - mn);
-    const float p1 = (x1 == mn) ? 1.f : exp2f(x1 - mn);
-    const float p2 = (x2 == mn) ? 1.f : exp2f(x2 - mn);
-    const float p3 = (x3 == mn) ? 1.f : exp2f(x3 - mn);
+    // hardware 2^x: exact at 0 (the row maximum weighs exactly 1, and a
+    // one-token context returns V exactly), 0 at -inf (masked tokens)
+    const float alpha = ex2_approx(m - mn);
+    const float p0 = ex2_approx(x0 - mn);
+    const float p1 = ex2_approx(x1 - mn);
+    const float p2 = ex2_approx(x2 - mn);
+    const float p3 = ex2_approx(x3 - mn);
     m = mn;
     const uint32_t pa0 = pack_bf16x2(p0, p1);  // P[gq][2tig, 2tig+1]
     const uint32_t pa2 = pack_bf16x2(p2, p3);  // P[gq][8+2tig, 9+2tig]
     // the denominator uses the same bf16-rounded weights as the PV product
     l = l * alpha + ((bf16lo_to_f32(pa0) + bf16hi_to_f32(pa0)) +
                      (bf16lo_to_f32(pa2) + bf16hi_to_f32(pa2)));
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {  // the running max rarely moves
 #pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      o[n][0] *= alpha;
-      o[n][1] *= alpha;
+      for (int n = 0; n < 8; ++n) {
+        o[n][0] *= alpha;
+        o[n][1] *= alpha;
+      }
     }
     // ---- O += P V ----------------------------------------------------------
     uint32_t m01 = 0xFFFFFFFFu, m89 = 0xFFFFFFFFu;
@@ -786,13 +872,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
-}
-// 2^x by the hardware approximation (results below 2^-126 flush to zero):
-// ex2(0) is 1 and ex2(-inf) is 0, so no special cases are needed here.
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
 }
 // 2^k as a float for a biased exponent k clamped to the normal range.
 __device__ __forceinline__ float pow2_biased(int k) {
@@ -1188,11 +1267,13 @@ __device__ __noinline__ void cross_cta_arrive(const DecodeParams& p, int s, int 
   __threadfence();  // every other record of this segment is now visible
   MergeAcc t;
   t.init();
-#pragma unroll 4
-  for (uint32_t k = 0; k < P; ++k) {
-    const uint32_t ck = dense ? c0 + k : owner_of(base + k, U, NC);
-    t.add_global(global_record(p, sg + ck), lane);
-  }
+  t.merge_global(
+      (int)P,
+      [&](int k) {
+        const uint32_t ck = dense ? c0 + (uint32_t)k : owner_of(base + (uint32_t)k, U, NC);
+        return global_record(p, sg + ck);
+      },
+      lane);
   t.store_output(p, s, g, lane);
   if (lane == 0) p.ws_cnt[sg] = 0u;  // ready for the next call
 }
@@ -1204,12 +1285,42 @@ __device__ __forceinline__ void cross_cta_merge(const DecodeParams& p, const Mer
   cross_cta_arrive(p, s, g, base, np, U, NC, lane);
 }
 
+// A segment that several warps of this CTA cover, once every covering warp
+// has written its record to shared memory: merge the records and store the
+// output, or hand the CTA's record on to the cross-CTA merge.  CTA c owns
+// units [a, b), split evenly over kWarps warps.  Out of line: it runs once
+// per such segment, and inlined its temporaries would crowd the page loop's
+// registers.
+template <class Smem, int kWarps>
+__device__ __noinline__ void finalise_segment(const DecodeParams& p, uint8_t* smem, int s, int g,
+                                              uint32_t base, uint32_t np, uint32_t a, uint32_t b,
+                                              uint32_t U, uint32_t NC, uint32_t c, int lane) {
+  const uint32_t last = base + np - 1;
+  const uint32_t lo = max(base, a), hi = min(last, b - 1), n_cta = b - a;
+  const int j0 = (int)owner_of(lo - a, n_cta, kWarps), j1 = (int)owner_of(hi - a, n_cta, kWarps);
+  // the records of the covering warps j0 .. j1 with non-empty ranges: warp
+  // j0's is in slot 1 if the segment starts in its range, every other one in
+  // slot 0 (the segment began before the warp's range)
+  const bool first_own = base >= a + range_start(j0, n_cta, kWarps);
+  MergeAcc m;
+  m.init();
+  m.merge_records<(kWarps + 7) / 8 * 8, false>(
+      j1 - j0 + 1,
+      [&](int k) { return smem_u32(Smem::slot(smem, j0 + k, (k == 0 && first_own) ? 1 : 0).o); },
+      [&](int k) { return range_start(j0 + k + 1, n_cta, kWarps) > range_start(j0 + k, n_cta, kWarps); },
+      lane);
+  if (base >= a && last < b)
+    m.store_output(p, s, g, lane);
+  else
+    cross_cta_merge(p, m, s, g, base, np, U, NC, c, lane);
+}
+
 // ---------------------------------------------------------------------------
 // The decode kernel.
 // ---------------------------------------------------------------------------
 template <class State, int kWarps, int kStages, bool kAppend>
 __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
-    paged_decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ DecodeParams p) {
   constexpr int kStageB = State::kStageBytes;
   constexpr int kP = State::kPagesPerUnit;  // pages per unit (and per pipeline stage)
   using Smem = SmemLayout<kWarps, kStages, kStageB, State::kTokenBytes>;
@@ -1312,25 +1423,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
     int fin_s = -1, fin_g = 0;
     uint32_t fin_base = 0, fin_np = 0;
     auto finalise = [&](int s, int g, uint32_t base, uint32_t np) {
-      const uint32_t last = base + np - 1;
-      const uint32_t lo = max(base, a), hi = min(last, b - 1), n_cta = b - a;
-      const int j0 = (int)owner_of(lo - a, n_cta, kWarps), j1 = (int)owner_of(hi - a, n_cta, kWarps);
-      // the records of the covering warps with non-empty ranges
-      auto each = [&](auto f) {
-        uint32_t v0 = range_start(j0, n_cta, kWarps);
-        for (int j = j0; j <= j1; ++j) {
-          const uint32_t v1 = range_start(j + 1, n_cta, kWarps);
-          if (v1 > v0) f(Smem::slot(smem, j, base < a + v0 ? 0 : 1));
-          v0 = v1;
-        }
-      };
-      MergeAcc m;
-      m.init();
-      m.merge_shared(each, lane);
-      if (base >= a && last < b)
-        m.store_output(p, s, g, lane);
-      else
-        cross_cta_merge(p, m, s, g, base, np, U, NC, c, lane);
+      finalise_segment<Smem, kWarps>(p, smem, s, g, base, np, a, b, U, NC, c, lane);
     };
     auto count_in = [&](int s, int g, uint32_t base, uint32_t np, bool more) {
       const uint32_t last = base + np - 1;
@@ -1517,7 +1610,7 @@ __device__ __forceinline__ bool spin_until(Pred pred) {
 
 template <bool kAppend>
 __global__ void __launch_bounds__(DynSmem::kThreads, 1)
-    paged_decode_dyn_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p,
+    paged_decode_dyn_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ DecodeParams p,
                             int n_cap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1894,7 +1987,7 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
 // Separate-combine mode: one warp per CTA boundary c (1 <= c < NC) merges the
 // segment that first crosses it, after the decode grid has finished.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) paged_decode_boundary_kernel(const DecodeParams p,
+__global__ void __launch_bounds__(256) paged_decode_boundary_kernel(const __grid_constant__ DecodeParams p,
                                                                     uint32_t NC) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
@@ -1916,11 +2009,13 @@ __global__ void __launch_bounds__(256) paged_decode_boundary_kernel(const Decode
   const uint32_t P = dense ? owner_of(base + np - 1, U, NC) - c0 + 1 : np;
   MergeAcc t;
   t.init();
-#pragma unroll 4
-  for (uint32_t k = 0; k < P; ++k) {
-    const uint32_t ck = dense ? c0 + k : owner_of(base + k, U, NC);
-    t.add_global(global_record(p, sg + ck), lane);
-  }
+  t.merge_global(
+      (int)P,
+      [&](int k) {
+        const uint32_t ck = dense ? c0 + (uint32_t)k : owner_of(base + (uint32_t)k, U, NC);
+        return global_record(p, sg + ck);
+      },
+      lane);
   t.store_output(p, cs.s, cs.g, lane);
 }
 
@@ -2119,6 +2214,23 @@ struct AppendArgs {
   int max_pos;
   void* q_out;
 };
+
+int decode_check_args(const void* q, const void* kv_pool, int num_pages,
+                      const int32_t* block_tables, int bt_row_stride, int max_blocks,
+                      const int32_t* seq_lens, int num_seqs, const void* out, float scale) {
+  if (num_seqs < 0 || num_pages < 1 || max_blocks < 1 || bt_row_stride < max_blocks)
+    return PKV_ERR_INVALID_ARGUMENT;
+  if (num_seqs == 0) return PKV_OK;
+  if (!q || !kv_pool || !block_tables || !seq_lens || !out) return PKV_ERR_INVALID_ARGUMENT;
+  if (!isfinite(scale)) return PKV_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return PKV_ERR_MISALIGNED;
+  if (num_seqs > kMaxSeqs || (long long)num_pages * 16 * 8 * 2 >= (1ll << 31) ||
+      (long long)max_blocks * PKV_PAGE_TOKENS >= (1ll << 24))
+    return PKV_ERR_UNSUPPORTED_SHAPE;
+  return PKV_OK;
+}
 
 static int decode_entry(const void* q, const void* kv_pool, int num_pages,
                         const int32_t* block_tables, int bt_row_stride, int max_blocks,

@@ -21,10 +21,14 @@ namespace pkv {
 // Workspace of the allocation-free entry point (see PKV_NOALLOC_WORKSPACE_BYTES).
 static __device__ __align__(256) uint8_t g_noalloc_workspace[PKV_NOALLOC_WORKSPACE_BYTES];
 
-// Device address of g_noalloc_workspace for `device`, looked up once per
-// device with that device current (host code must not use the symbol itself:
-// on the host it names a stand-in, not device memory).
-static int noalloc_workspace_address(int device, uint8_t** out) {
+// Device address of g_noalloc_workspace on `device`, which is current.  Host
+// code must not use the symbol itself: on the host it names a stand-in, not
+// device memory.  Outside stream capture the address is looked up on every
+// call (a host-side lookup, no stream work), so a device reset that reloads
+// the library's module cannot leave a stale address behind; while `stream`
+// is being captured the address from the last uncaptured call on the device
+// is used, and a first call under capture is refused.
+static int noalloc_workspace_address(int device, bool capturing, uint8_t** out) {
   static std::mutex mu;
   static uint8_t* addr[64] = {nullptr};
   if (device < 0 || device >= 64) {
@@ -32,7 +36,13 @@ static int noalloc_workspace_address(int device, uint8_t** out) {
     return PKV_ERR_CUDA;
   }
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[device] == nullptr) {
+  if (capturing) {
+    if (addr[device] == nullptr) {
+      set_last_error("paged_gqa_decode_noalloc",
+                     "first call on this device made during stream capture; call it once before capturing");
+      return PKV_ERR_CUDA;
+    }
+  } else {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_workspace);
     if (e != cudaSuccess) return cuda_status(e, "cudaGetSymbolAddress(noalloc workspace)");
@@ -51,10 +61,20 @@ extern "C" int paged_gqa_decode_noalloc(const void* q, const void* kv_pool, int 
                                         int max_blocks, const int32_t* seq_lens, int num_seqs,
                                         int max_seq_len, void* out, float scale, int* d_err,
                                         void* stream) {
-  if (num_seqs < 0) return PKV_ERR_INVALID_ARGUMENT;
-  if (num_seqs == 0) return PKV_OK;
+  // every check that needs no device comes first: a rejected call touches
+  // neither the GPU nor the shared array
+  int rc = decode_check_args(q, kv_pool, num_pages, block_tables, bt_row_stride, max_blocks,
+                             seq_lens, num_seqs, out, scale);
+  if (rc != PKV_OK || num_seqs == 0) return rc;
+  bool capturing = false;
+  if (stream != nullptr) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cap);
+    if (e != cudaSuccess) return cuda_status(e, "cudaStreamIsCapturing");
+    capturing = cap != cudaStreamCaptureStatusNone;
+  }
   int dev = 0;
-  int rc = bind_stream_device(stream, &dev);
+  rc = bind_stream_device(stream, &dev);
   if (rc != PKV_OK) return rc;
   const size_t need = paged_gqa_decode_workspace_bytes(num_seqs);
   if (need == 0) {
@@ -70,7 +90,7 @@ extern "C" int paged_gqa_decode_noalloc(const void* q, const void* kv_pool, int 
     return PKV_ERR_WORKSPACE_TOO_SMALL;
   }
   uint8_t* ws = nullptr;
-  rc = noalloc_workspace_address(dev, &ws);
+  rc = noalloc_workspace_address(dev, capturing, &ws);
   if (rc != PKV_OK) return rc;
   // The per-segment arrival counters at the front of the workspace must be
   // zero when a call starts; clear them on the caller's stream every time.

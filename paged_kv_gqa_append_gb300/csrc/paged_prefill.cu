@@ -12,15 +12,17 @@
 //  * tcgen05 (default): one CTA per (32 query tokens, KV head, sequence) =
 //    an M = 128 tile of query rows (token-major, the 4 query heads of the
 //    group inside); keys in blocks of 64 (4 pages).  S = Q K^T and O += P V
-//    run on the 5th-generation tensor cores with S and O in tensor memory,
-//    operands in 128-byte-swizzled shared memory (Q and P written by
-//    threads, K and V tiles by TMA; V is the MN-major B operand as stored).
-//    A producer warp streams K and V through two stages, one thread issues
-//    the MMAs, and a warpgroup runs the softmax with one thread per row
-//    (the row max and sum need no shuffles); O is rescaled in tensor memory
-//    only when a row's running max grows by more than 8 (in log2 units) --
-//    softmax does not depend on the subtracted constant, and the weights
-//    stay below 2^8.
+//    run on the 5th-generation tensor cores with Q, S, P and O in tensor
+//    memory (Q loaded once by the softmax warps as the A operand of S; P
+//    written over the first half of its own S buffer as the A operand of
+//    P V); K and V tiles arrive by TMA in 128-byte-swizzled shared memory
+//    (V is the MN-major B operand as stored).  Two producer warps stream K
+//    and V through their own 4-stage rings; S = Q K^T (into one of two S
+//    buffers) and O += P V are issued by threads of two different warps; a
+//    warpgroup runs the softmax with one thread per row (the row max and
+//    sum need no shuffles).  O is rescaled in tensor memory only when a
+//    row's running max grows by more than 8 (in log2 units) -- softmax does
+//    not depend on the subtracted constant, and the weights stay below 2^8.
 //  * mma.sync (comparison arm, below): the same units on the legacy tensor path.
 //
 // mma.sync arm: work unit = (query block of 32 tokens, KV head g, sequence s), one CTA.

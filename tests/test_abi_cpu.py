@@ -4,6 +4,8 @@ its host-side RoPE tables and scheduler agree with the FP64 oracle exactly."""
 import ctypes
 import os
 import re
+import subprocess
+import sys
 
 import numpy as np
 import pytest
@@ -69,6 +71,19 @@ def test_credit_matches_oracle():
 
 
 def test_host_side_validation_returns_before_launch():
+    """The checks below pass made-up device addresses: they run in a child
+    process that sees no GPU (CUDA_VISIBLE_DEVICES empty), so even a check
+    that let one through could never launch a kernel on them."""
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    code = "import tests.test_abi_cpu as t; t._host_validation_checks()"
+    r = subprocess.run([sys.executable, "-c", code], cwd=B.ROOT, env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+
+
+def _host_validation_checks():
+    import torch
+    assert not torch.cuda.is_available()
     L = pkv.lib
     null = None
     # append: null pointers, bad sizes
@@ -99,6 +114,14 @@ def test_host_side_validation_returns_before_launch():
                               1 << 30, null, null) == 3
     assert L.paged_gqa_decode(fake, fake, 8, fake, 128, 128, fake, 1, 16, fake, float("nan"), fake,
                               1 << 20, null, null) == 1
+    # allocation-free decode: the same checks, all before any device work
+    NA = L.paged_gqa_decode_noalloc
+    assert NA(null, null, 8, null, 128, 128, null, 0, 0, null, 0.125, null, null) == 0
+    assert NA(null, fake, 8, fake, 128, 128, fake, 1, 16, fake, 0.125, null, null) == 1
+    assert NA(fake, fake, 8, fake, 64, 128, fake, 1, 16, fake, 0.125, null, null) == 1
+    assert NA(fake, odd, 8, fake, 128, 128, fake, 1, 16, fake, 0.125, null, null) == 2
+    assert NA(fake, fake, 8, fake, 128, 128, fake, 1, 16, fake, float("nan"), null, null) == 1
+    assert NA(fake, fake, 8, fake, 128, 128, fake, 5000, 16, fake, 0.125, null, null) == 3
     # prefill: nothing to do; nulls; stride < max_blocks; misaligned q; NaN scale; too many seqs
     PF = L.paged_gqa_prefill
     assert PF(null, 0, null, null, 8, null, 128, 128, null, 0, 16, null, 0.125, null, null) == 0
