@@ -62,13 +62,24 @@ def parse():
     ap.add_argument("--layers", type=int, default=0,
                     help="layers of the workload (0 = its own: 16); fewer layers shrink the pool "
                          "for a profiler capture of the same kernel shape")
-    ap.add_argument("--schedule", choices=["static", "dynamic"], default="static",
-                    help="decode schedule (opts.schedule 0 or 1)")
+    ap.add_argument("--schedule", choices=["auto", "static", "dynamic"], default="auto",
+                    help="decode schedule (opts.schedule 2, 0 or 1; auto: dynamic when every SM "
+                         "gets at least 512 units of work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--unfused", action="store_true",
                     help="run append and decode as two kernels per layer")
     return ap.parse_args()
+
+
+def effective_schedule(schedule, case, dev):
+    """The schedule a decode launch of `case` runs with (include/pkv.h: the
+    automatic one is dynamic from PKV_DYNAMIC_MIN_UNITS = 512 units per SM)."""
+    if schedule != "auto":
+        return schedule
+    units = 8 * case.num_seqs * ((int(case.max_seq_len) + 15) // 16)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    return "dynamic" if units >= 512 * sms else "static"
 
 
 def make_case(name, layers=0):
@@ -167,6 +178,70 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(r[1] for r in inside),
                 "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
                 "samples": len(inside)}
+
+
+class NvmlClocks:
+    """Dense clock samples from NVML (read-only queries through ctypes): a
+    thread polls the SM clock and the clock-event reasons every `period_s`
+    while running.  Falls back to nothing (available False) when the NVML
+    library cannot be loaded."""
+    # nvmlClocksEventReasons bits of the public NVML API
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index, period_s=0.0005):
+        import ctypes
+        import threading
+        self.samples, self.available, self._stop = [], False, threading.Event()
+        self.period = period_s
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+                return
+            self._nv, self._h, self._ct = nv, h, ctypes
+            mx = ctypes.c_uint(0)
+            nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))   # NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+            self.available = True
+        except Exception:
+            return
+        self._thread = threading.Thread(target=self._run, daemon=True)
+
+    def _run(self):
+        ct, nv, h = self._ct, self._nv, self._h
+        mhz, rs = ct.c_uint(0), ct.c_ulonglong(0)
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(mhz)) == 0:
+                r = nv.nvmlDeviceGetCurrentClocksEventReasons(h, ct.byref(rs))
+                self.samples.append((time.time(), float(mhz.value), rs.value if r == 0 else 0))
+            time.sleep(self.period)
+
+    def start(self):
+        if self.available:
+            self._thread.start()
+        return self
+
+    def stop(self):
+        if self.available:
+            self._stop.set()
+            self._thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        if not self.available:
+            return None
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"],
+                    "samples": 0, "source": "nvml"}
+        reasons = sorted({n for _, _, r in inside for b, n in self.REASONS.items() if r & b})
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": min(s[1] for s in inside), "reasons": reasons,
+                "samples": len(inside), "source": "nvml, every 0.5 ms"}
 
 
 # ------------------------------------------------------------- roofline ----
@@ -422,11 +497,23 @@ def run_gb300(args, world, rank, local):
     compute = pkv.COMPUTE_TENSOR if args.compute == "tensor" else pkv.COMPUTE_FMA
 
     pool = W.fill_pool(case, device=dev)
-    q_raw = W.fill_queries(case, device=dev)
-    k_new, v_new = W.fill_new_kv(case, device=dev)
-    bt = torch.from_numpy(case.block_tables).to(dev)
-    lens = torch.from_numpy(case.seq_lens).to(dev)
-    pos = torch.from_numpy(W.new_positions(case)).to(dev)
+    # the step's inputs (q, new K/V, positions, lengths, tables) are views of
+    # one device buffer, so that the end-to-end run uploads them in one copy
+    parts = [W.fill_queries(case, device=dev), *W.fill_new_kv(case, device=dev),
+             torch.from_numpy(W.new_positions(case)).to(dev),
+             torch.from_numpy(case.seq_lens).to(dev), torch.from_numpy(case.block_tables).to(dev)]
+    offs, total = [], 0
+    for x in parts:
+        offs.append(total)
+        total += (x.numel() * x.element_size() + 255) // 256 * 256
+    inbuf = torch.empty(total, dtype=torch.uint8, device=dev)
+    views = []
+    for x, o in zip(parts, offs):
+        v = inbuf[o:o + x.numel() * x.element_size()].view(x.dtype).view(x.shape)
+        v.copy_(x)
+        views.append(v)
+    q_raw, k_new, v_new, pos, lens, bt = views
+    del parts
     cos, sin = pkv.rope_tables_device(dev, W.MAX_CONTEXT)
     out = torch.empty_like(q_raw)
     kv_bytes_layer = case.kv_bytes_per_layer()
@@ -434,7 +521,7 @@ def run_gb300(args, world, rank, local):
                           max_seq_len=case.max_seq_len,
                           compute=None if compute == pkv.COMPUTE_TENSOR else compute,
                           fused=not args.unfused,
-                          schedule=1 if args.schedule == "dynamic" else 0)
+                          schedule={"auto": 2, "static": 0, "dynamic": 1}[args.schedule])
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(args.warmup):
@@ -445,6 +532,7 @@ def run_gb300(args, world, rank, local):
 
     # ---- headline: K graph replays of the step, inputs resident in HBM -----
     clocks = ClockSampler(dev.index) if rank == 0 else None
+    dense = NvmlClocks(dev.index).start() if rank == 0 else None
     time.sleep(0.5 if clocks else 0)
     barrier(world)
     torch.cuda.synchronize()
@@ -458,6 +546,20 @@ def run_gb300(args, world, rank, local):
     t_wall1 = time.time()
     barrier(world)
     ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    # ---- the same step graph over a sustained window of >= 2 s, clocks sampled
+    n_sus = max(1, int(2.0 / max(ms / args.steps / 1e3, 1e-6)) + 1)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_sus0 = time.time()
+    s0.record(stream)
+    for _ in range(n_sus):
+        step.run()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    t_sus1 = time.time()
+    sus_ms = s0.elapsed_time(s1)
+    if dense:
+        dense.stop()
     code = step.error()
     if code != 0:
         raise RuntimeError(f"device error {pkv.status_string(code)} in the timed region")
@@ -500,6 +602,18 @@ def run_gb300(args, world, rank, local):
     clk = clocks.summary(t_wall0, t_wall2) if clocks else None
     if clocks:
         clocks.stop()
+    if dense and dense.available:
+        # the headline's own clocks come from the dense samples of its region
+        clk = dict(dense.summary(t_wall0, t_wall1), smi=clk)
+    sustained = None
+    if rank == 0:
+        sus_clk = dense.summary(t_sus0, t_sus1) if dense and dense.available else None
+        sustained = {"steps": n_sus, "ms_per_step": sus_ms / n_sus,
+                     "value": kv_bytes_layer * L * n_sus / (sus_ms / 1e3) / 1e9, "unit": "GB/s",
+                     "window_s": sus_ms / 1e3, "clocks": sus_clk}
+        if sus_clk and sus_clk.get("sm_mhz"):
+            # time x clock: the step's cost in SM cycles, comparable across clocks
+            sustained["us_x_mhz_per_layer"] = sus_ms * 1e3 / (n_sus * L) * sus_clk["sm_mhz"]
 
     steps = args.steps
     sec = ms / 1e3
@@ -511,12 +625,9 @@ def run_gb300(args, world, rank, local):
     # ---- e2e: the same step with its inputs uploaded and output read back --
     e2e = None
     if not args.no_e2e:
-        q_h = q_raw.cpu().pin_memory()
-        k_h, v_h = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
-        pos_h, lens_h = pos.cpu().pin_memory(), lens.cpu().pin_memory()
-        bt_h = bt.cpu().pin_memory()
+        in_h = inbuf.cpu().pin_memory()      # q, new K/V, positions, lengths, tables
         out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, pos_h, lens_h, bt_h))
+        h2d = in_h.numel()
         d2h = out_h.numel() * out_h.element_size()
         k_e2e = max(1, min(steps, 500))
         barrier(world)
@@ -525,12 +636,7 @@ def run_gb300(args, world, rank, local):
         t0 = time.perf_counter()
         a.record(stream)
         for _ in range(k_e2e):
-            q_raw.copy_(q_h, non_blocking=True)
-            k_new.copy_(k_h, non_blocking=True)
-            v_new.copy_(v_h, non_blocking=True)
-            pos.copy_(pos_h, non_blocking=True)
-            lens.copy_(lens_h, non_blocking=True)
-            bt.copy_(bt_h, non_blocking=True)
+            inbuf.copy_(in_h, non_blocking=True)     # the step's inputs: one upload
             step.run()
             out_h.copy_(out, non_blocking=True)
         b.record(stream)
@@ -540,7 +646,8 @@ def run_gb300(args, world, rank, local):
         e2e = {"value": kv_bytes_layer * L * k_e2e * world / e2e_s / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": k_e2e, "tokens_per_s": S * k_e2e * world / e2e_s,
-               "path": "DecodeStep graph replay + pinned H2D/D2H copies"}
+               "path": "DecodeStep graph replay; the step's inputs (q, new K/V, positions, "
+                       "lengths, tables) uploaded as one pinned copy, the output read back"}
         if step.error() != 0:
             raise RuntimeError("device error in the e2e region")
 
@@ -549,7 +656,7 @@ def run_gb300(args, world, rank, local):
     achieved = kv_bytes_layer / (dec_avg_ms / 1e3) / 1e9
     tag = ("paged_decode_append" if step.fused else
            "paged_decode_" + ("mma" if compute == pkv.COMPUTE_TENSOR else "fma"))
-    if args.schedule == "dynamic":
+    if effective_schedule(args.schedule, case, dev) == "dynamic":
         tag += "_dyn"
     traffic = ncu_traffic(f"{tag}:{case.name}")
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -578,7 +685,7 @@ def run_gb300(args, world, rank, local):
                        "pool_bytes": case.num_pages * W.PAGE_ELEMS * 2,
                        "l2": "inputs larger than L2 (pool read per step exceeds 129 MB L2)",
                        "parallelism": f"replicas x{world}", "compute": args.compute,
-                       "schedule": args.schedule,
+                       "schedule": f"{args.schedule} ({effective_schedule(args.schedule, case, dev)})",
                        "launch": ("CUDA graph of the step: one fused append+decode kernel per layer"
                                   if step.fused else
                                   "CUDA graph of the step: append kernel + decode kernel per layer")},
@@ -586,7 +693,8 @@ def run_gb300(args, world, rank, local):
             "append_us_per_layer": append_us,
             "kv_bytes_per_step": kv_bytes_layer * L,
             "hbm_frac_step": value / world / peak,
-            "clocks": clk, "e2e": e2e, "gpu_launches": step.launches_per_step * steps,
+            "clocks": clk, "sustained": sustained, "e2e": e2e,
+            "gpu_launches": step.launches_per_step * steps,
             "roofline": roof, "env": env_info(dev), "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -615,7 +723,8 @@ def run_int8_line(args, world, rank, local):
     out = torch.empty_like(q_raw)
     kv_bytes_layer = int(case.seq_lens.sum()) * W.NUM_KV_HEADS * INT8_ROW_BYTES
     step = pkv.Int8DecodeStep(pool, bt, lens, pos, k_new, v_new, q_raw, out, cos, sin,
-                              case.scale, max_seq_len=case.max_seq_len, fused=not args.unfused)
+                              case.scale, max_seq_len=case.max_seq_len,
+                              fused=False if args.unfused else None)   # None: by batch size
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
         step.run()

@@ -213,7 +213,12 @@ typedef struct pkv_decode_opts {
                              from a shared counter (large first, single pages at
                              the end) and the CTA's shared segments go first.
                              Falls back to 0 when its page table does not fit in
-                             shared memory (tensor path only)                   */
+                             shared memory (tensor path only);
+                             2 = automatic: dynamic when the length bound gives
+                             every SM at least PKV_DYNAMIC_MIN_UNITS units of
+                             (sequence, KV head, page) -- long ranges, where
+                             evening out the warps pays for the claims -- else
+                             static.  Calls without options use 2.             */
   int early_kv;           /* 1 = the caller guarantees that block_tables, seq_lens
                              and the K/V pages this call reads are not written by
                              the kernel enqueued just before it on the stream:
@@ -221,7 +226,26 @@ typedef struct pkv_decode_opts {
                              while that kernel is still finishing (programmatic
                              dependent launch); q, the new token and all writes
                              still wait for it.  0 = everything waits (default). */
+  long long wait_limit_ns; /* limit of every bounded wait inside the kernel (a page's
+                             copy, a shared-memory turn): 0 = the default of 2 s;
+                             when one runs out the kernel sets *d_err =
+                             PKV_ERR_TIMEOUT, waits (2 s at most) for its own copies
+                             still in flight and returns; the outputs are then
+                             undefined and the workspace must be zeroed again      */
+  int expire_first_wait;  /* test of that path: 1 = the first warp of the first CTA
+                             waits on a barrier nothing completes instead of its
+                             first page, so its wait runs out after wait_limit_ns
+                             (no fault, no hang: the bounded-wait contract above) */
 } pkv_decode_opts;
+
+/* Work per SM from which the automatic schedule is the dynamic one (on
+ * GB300 the dynamic schedule is 3-4 % faster from 96 sequences of 2048 tokens
+ * on, 512 units per SM and more; at 32 sequences the static one is 13 %
+ * faster). */
+#define PKV_DYNAMIC_MIN_UNITS 512
+#define PKV_SCHEDULE_STATIC 0
+#define PKV_SCHEDULE_DYNAMIC 1
+#define PKV_SCHEDULE_AUTO 2
 
 /* paged_gqa_decode with explicit options; same contract otherwise. */
 int paged_gqa_decode_ex(const void* q, const void* kv_pool, int num_pages,
@@ -380,6 +404,45 @@ int paged_gqa_decode_append_int8(const void* q, const void* k_new, const void* v
                                  int* d_err, void* stream, const pkv_decode_opts* opts);
 
 /* ------------------------------------------------------------------------
+ * paged_gqa_decode_append_layers - one decode step of every layer in one
+ * call: the batched decode of the samir-vllm article ("Gestion de la KV
+ * cache et strategies de batching": each step appends every active
+ * sequence's token at its absolute position and attends over its pages),
+ * for all layers of the model in layer order.
+ *
+ * If host_stage is given, first one host->device copy of stage_bytes from
+ * host_stage (pinned host memory, caller-owned; it must stay unchanged until
+ * the copy has run on `stream`) to dev_stage (device) is enqueued: the block
+ * tables and lengths of the step may live there (pkv_sched_pack_step).  Then
+ * for l = 0 .. num_layers-1 exactly the call
+ *   paged_gqa_decode_append(q + l Q, k_new + l K, v_new + l K, rope_cos,
+ *       rope_sin, max_pos, kv_pool, num_pages,
+ *       block_tables + l * bt_layer_stride, bt_row_stride, max_blocks,
+ *       seq_lens, num_seqs, max_seq_len, q_out ? q_out + l Q : NULL,
+ *       out + l Q, scale, workspace, workspace_bytes, d_err, stream, &opts)
+ * (paged_gqa_decode_append_int8 when int8 = 1) with Q = num_seqs*32*64 and
+ * K = num_seqs*8*64 bf16 elements and default options, except that with
+ * early_kv = 1 the layers l >= 1 take opts.early_kv = 1: the layers' block
+ * tables must then name disjoint pages, as the layers of a paged cache do.
+ *   q, out, q_out   device bf16 [num_layers][num_seqs][32][64] (q_out or NULL)
+ *   k_new, v_new    device bf16 [num_layers][num_seqs][8][64]
+ *   block_tables    device int32, layer l at + l * bt_layer_stride elements
+ *                   (bt_layer_stride >= num_seqs * bt_row_stride)
+ * Returns the first non-zero status of a layer's call (later layers are then
+ * not launched) or of the copy; PKV_OK otherwise.
+ * ---------------------------------------------------------------------- */
+int paged_gqa_decode_append_layers(const void* q, const void* k_new, const void* v_new,
+                                   void* q_out, void* out, int num_layers, int num_seqs,
+                                   const float* rope_cos, const float* rope_sin, int max_pos,
+                                   void* kv_pool, int num_pages, int int8,
+                                   const int32_t* block_tables, long long bt_layer_stride,
+                                   int bt_row_stride, int max_blocks, const int32_t* seq_lens,
+                                   int max_seq_len, float scale, void* workspace,
+                                   size_t workspace_bytes, int* d_err, void* stream,
+                                   int early_kv, const void* host_stage, void* dev_stage,
+                                   size_t stage_bytes);
+
+/* ------------------------------------------------------------------------
  * paged_gqa_prefill - causal GQA attention of each sequence's newest tokens
  * over its own pages: a whole prompt, or a chunk of one after a cached
  * prefix ("Gestion de la KV cache et strategies de batching": attention
@@ -487,6 +550,30 @@ int pkv_sched_grow(pkv_sched* s, int req_id, int new_len);
 
 /* Release a running request's pages and slot. */
 int pkv_sched_finish(pkv_sched* s, int req_id);
+
+/* Host side of one decode step of the continuous batch: every running
+ * request, in admission order (= id order), grows by one token as
+ * pkv_sched_grow(id, length + 1) would, where length is the largest length
+ * it was grown to.  ids (host int32[max_out], out) gets the batch's request
+ * ids in that order, lens (host int32[max_out], out) their lengths after the
+ * step, *batch their count.  All or nothing: if any request cannot take its
+ * token (PKV_ERR_POOL_EXHAUSTED) nothing changes; PKV_ERR_INVALID_ARGUMENT
+ * if more than max_out requests run. */
+int pkv_sched_begin_step(pkv_sched* s, int32_t* ids, int32_t* lens, int max_out, int* batch);
+
+/* Bytes of a step block for `batch` rows of lengths at most max_len: the
+ * lengths [batch] int32, then at the next 16-byte boundary the block tables
+ * [num_layers][batch][P] int32 with P = max(1, ceil(max_len / 16)). */
+size_t pkv_sched_step_bytes(const pkv_sched* s, int batch, int max_len);
+
+/* Write the step block of requests ids[0 .. batch) (running, lengths at most
+ * max_len) into `block` (host memory of at least pkv_sched_step_bytes
+ * bytes): their current lengths and, per layer, their page ids padded with
+ * -1.  Layer l's tables then start at element offset l * batch * P of the
+ * tables part, rows of P entries: the block_tables / seq_lens arguments of
+ * paged_gqa_decode_append_layers once the block is on the device. */
+int pkv_sched_pack_step(const pkv_sched* s, const int32_t* ids, int batch, int max_len,
+                        void* block, size_t bytes);
 
 /* Copy one request's block table for `layer` (host int32[max_blocks], -1
  * padded) and report its slot (may be NULL). */

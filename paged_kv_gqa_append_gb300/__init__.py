@@ -32,6 +32,7 @@ ROPE_PAIRS = 32
 
 COMPUTE_TENSOR = 0
 COMPUTE_FMA = 1
+SCHEDULE_STATIC, SCHEDULE_DYNAMIC, SCHEDULE_AUTO = 0, 1, 2
 
 STATUS = {
     0: "PKV_OK", 1: "PKV_ERR_INVALID_ARGUMENT", 2: "PKV_ERR_MISALIGNED",
@@ -56,7 +57,8 @@ _ip = ctypes.POINTER(ctypes.c_int)
 
 class DecodeOpts(ctypes.Structure):
     _fields_ = [("compute", _i), ("min_units_per_warp", _i), ("ctas_per_sm", _i), ("stages", _i),
-                ("warps_per_cta", _i), ("combine", _i), ("schedule", _i), ("early_kv", _i)]
+                ("warps_per_cta", _i), ("combine", _i), ("schedule", _i), ("early_kv", _i),
+                ("wait_limit_ns", ctypes.c_longlong), ("expire_first_wait", _i)]
 
 
 _SIGS = {
@@ -84,6 +86,9 @@ _SIGS = {
                                       ctypes.POINTER(DecodeOpts)]),
     "paged_gqa_decode_append_int8": (_i, [_p, _p, _p, _p, _p, _i, _p, _i, _p, _i, _i, _p, _i, _i, _p,
                                           _p, _f, _p, _sz, _p, _p, ctypes.POINTER(DecodeOpts)]),
+    "paged_gqa_decode_append_layers": (_i, [_p, _p, _p, _p, _p, _i, _i, _p, _p, _i, _p, _i, _i, _p,
+                                            ctypes.c_longlong, _i, _i, _p, _i, _f, _p, _sz, _p, _p,
+                                            _i, _p, _p, _sz]),
     "pkv_read_device_error": (_i, [_p, _p, _i, _ip]),
     "pkv_credit_pages": (_i, [_i, _i, _i]),
     "pkv_sched_create": (_p, [_i, _i, _i, _i]),
@@ -97,6 +102,9 @@ _SIGS = {
     "pkv_sched_stats": (_i, [_p, _ip, _ip, _ip, _ip]),
     "pkv_sched_event_count": (_i, [_p]),
     "pkv_sched_event": (_i, [_p, _i, _ip, _ip, _ip, _ip]),
+    "pkv_sched_begin_step": (_i, [_p, _p, _p, _i, _ip]),
+    "pkv_sched_step_bytes": (_sz, [_p, _i, _i]),
+    "pkv_sched_pack_step": (_i, [_p, _p, _i, _i, _p, _sz]),
 }
 
 _LIB = None
@@ -255,12 +263,16 @@ def alloc_workspace(num_seqs: int, device) -> torch.Tensor:
 def paged_gqa_decode(q, kv_pool, block_tables, seq_lens, out, scale, workspace=None,
                      max_seq_len=None, d_err=None, max_blocks=None, compute=None,
                      min_units_per_warp=0, ctas_per_sm=0, stages=0, warps_per_cta=0,
-                     combine=0, schedule=0, early_kv=0, stream=None):
+                     combine=0, schedule=None, early_kv=0, stream=None, wait_limit_ns=0,
+                     expire_first_wait=0):
     """out[s, h] = softmax(scale * q[s, h] . K) V over sequence s's own pages.
 
     early_kv=1 promises that the kernel enqueued just before this call on the
     stream writes neither block_tables, seq_lens nor the pages read here; the
-    call then starts on them while that kernel finishes.
+    call then starts on them while that kernel finishes.  schedule: None or
+    SCHEDULE_AUTO (by work per SM), SCHEDULE_STATIC or SCHEDULE_DYNAMIC.
+    wait_limit_ns and expire_first_wait: the bounded-wait limit and its test
+    (pkv_decode_opts).
     """
     dev = kv_pool.device
     _need(kv_pool, "kv_pool", torch.bfloat16, dev, (2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM))
@@ -288,12 +300,14 @@ def paged_gqa_decode(q, kv_pool, block_tables, seq_lens, out, scale, workspace=N
             _ptr(seq_lens), S, int(max_seq_len), _ptr(out), float(scale), _ptr(workspace),
             workspace.numel(), _ptr(d_err), _stream(stream))
     if compute is None and not (min_units_per_warp or ctas_per_sm or stages or warps_per_cta
-                                or combine or schedule or early_kv):
+                                or combine or schedule is not None or early_kv
+                                or wait_limit_ns or expire_first_wait):
         st = _L().paged_gqa_decode(*args)
     else:
         opts = DecodeOpts(COMPUTE_TENSOR if compute is None else compute,
                           min_units_per_warp, ctas_per_sm, stages, warps_per_cta, combine,
-                          schedule, early_kv)
+                          SCHEDULE_AUTO if schedule is None else schedule, early_kv,
+                          wait_limit_ns, expire_first_wait)
         st = _L().paged_gqa_decode_ex(*args, ctypes.byref(opts))
     _check(st, "paged_gqa_decode")
 
@@ -434,7 +448,7 @@ def paged_gqa_decode_append_int8(q, k_new, v_new, kv_pool, block_tables, seq_len
     _need(workspace, "workspace", torch.uint8, dev)
     if d_err is not None:
         _need(d_err, "d_err", torch.int32, dev)
-    opts = DecodeOpts(COMPUTE_TENSOR, min_units_per_warp, 0, 0, 0, 0, 0, early_kv)
+    opts = DecodeOpts(COMPUTE_TENSOR, min_units_per_warp, 0, 0, 0, 0, SCHEDULE_AUTO, early_kv)
     st = _L().paged_gqa_decode_append_int8(
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(rope_cos), _ptr(rope_sin), rope_cos.shape[0],
         _ptr(kv_pool), kv_pool.shape[0], _ptr(block_tables), stride, mb, _ptr(seq_lens), S,
@@ -446,7 +460,7 @@ def paged_gqa_decode_append_int8(q, k_new, v_new, kv_pool, block_tables, seq_len
 def paged_gqa_decode_append(q, k_new, v_new, kv_pool, block_tables, seq_lens, out, rope_cos,
                             rope_sin, scale, q_out=None, workspace=None, max_seq_len=None,
                             d_err=None, max_blocks=None, warps_per_cta=0, min_units_per_warp=0,
-                            ctas_per_sm=0, schedule=0, early_kv=0, stream=None):
+                            ctas_per_sm=0, schedule=None, early_kv=0, stream=None):
     """One decode step: append each sequence's new token at seq_lens-1, then attend.
 
     early_kv as for paged_gqa_decode (the pages meant are the ones this call
@@ -485,7 +499,7 @@ def paged_gqa_decode_append(q, k_new, v_new, kv_pool, block_tables, seq_lens, ou
     if d_err is not None:
         _need(d_err, "d_err", torch.int32, dev)
     opts = DecodeOpts(COMPUTE_TENSOR, min_units_per_warp, ctas_per_sm, 0, warps_per_cta, 0,
-                      schedule, early_kv)
+                      SCHEDULE_AUTO if schedule is None else schedule, early_kv)
     st = _L().paged_gqa_decode_append(
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(rope_cos), _ptr(rope_sin), rope_cos.shape[0],
         _ptr(kv_pool), kv_pool.shape[0], _ptr(block_tables), stride, mb, _ptr(seq_lens), S,
@@ -496,17 +510,22 @@ def paged_gqa_decode_append(q, k_new, v_new, kv_pool, block_tables, seq_lens, ou
 
 def paged_gqa_decode_append_layers(q, k_new, v_new, kv_pool, block_tables, seq_lens, out,
                                    rope_cos, rope_sin, scale, workspace, max_seq_len=None,
-                                   d_err=None, stream=None):
+                                   d_err=None, stream=None, q_out=None, early_kv=1,
+                                   host_stage=None, dev_stage=None):
     """A whole decode step: for every layer l, the fused append + decode of
     q[l], k_new[l], v_new[l] over block_tables[l] into out[l] on a bf16 pool
     (paged_gqa_decode_append) or an INT8 pool (paged_gqa_decode_append_int8),
-    in layer order on one stream.
+    in layer order on one stream -- one call of the C function of the same
+    name, which makes those per-layer calls.
 
-    q, out: [L, S, 32, 64] bf16; k_new, v_new: [L, S, 8, 64] bf16;
+    q, out (and q_out): [L, S, 32, 64] bf16; k_new, v_new: [L, S, 8, 64] bf16;
     block_tables: [L, S', row_stride] int32 with S' >= S; seq_lens: [S] int32,
-    shared by the layers.  The C calls and their arguments are exactly those
-    of L calls of the per-layer binding with default options; the arguments
-    are checked once, which is what a serving loop saves per step.
+    shared by the layers.  early_kv=1 lets layers >= 1 read their tables and
+    stage their first pages while the previous layer's kernel finishes (the
+    layers' pages must be disjoint).  host_stage (pinned uint8 host tensor) and
+    dev_stage (uint8 device tensor of at least its size): one copy of the
+    first into the second runs on the stream before the launches, e.g. the
+    block of pkv_sched_pack_step that block_tables / seq_lens are views of.
     """
     dev = kv_pool.device
     int8 = kv_pool.dtype == torch.uint8
@@ -522,6 +541,10 @@ def paged_gqa_decode_append_layers(q, k_new, v_new, kv_pool, block_tables, seq_l
     L, S = q.shape[0], q.shape[1]
     if out.shape != q.shape or k_new.shape[:2] != (L, S) or v_new.shape != k_new.shape:
         raise ValueError("q/out [L, S, 32, 64] and k_new/v_new [L, S, 8, 64] must agree")
+    if q_out is not None:
+        _need(q_out, "q_out", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
+        if q_out.shape != q.shape:
+            raise ValueError("q_out must match q")
     if L == 0:
         return
     _need(block_tables, "block_tables", torch.int32, dev)
@@ -535,24 +558,26 @@ def paged_gqa_decode_append_layers(q, k_new, v_new, kv_pool, block_tables, seq_l
     _need(workspace, "workspace", torch.uint8, dev)
     if d_err is not None:
         _need(d_err, "d_err", torch.int32, dev)
+    if (host_stage is None) != (dev_stage is None):
+        raise ValueError("host_stage and dev_stage go together")
+    stage = 0
+    if host_stage is not None:
+        if host_stage.dtype != torch.uint8 or not host_stage.is_contiguous():
+            raise TypeError("host_stage must be a contiguous uint8 host tensor")
+        _need(dev_stage, "dev_stage", torch.uint8, dev)
+        stage = host_stage.numel()
+        if dev_stage.numel() < stage:
+            raise ValueError("dev_stage is smaller than host_stage")
     stride = block_tables.shape[2]
     if max_seq_len is None:
         max_seq_len = PAGE_TOKENS * stride
-    opts = DecodeOpts(COMPUTE_TENSOR, 0, 0, 0, 0, 0, 0, 0)
-    fn = _L().paged_gqa_decode_append_int8 if int8 else _L().paged_gqa_decode_append
-    where = "paged_gqa_decode_append_int8" if int8 else "paged_gqa_decode_append"
-    # contiguous [L, ...] tensors: layer l starts l x (bytes per layer) in
-    steps = [t.data_ptr() for t in (q, k_new, v_new, block_tables, out)]
-    sizes = [t[0].numel() * t.element_size() for t in (q, k_new, v_new, block_tables, out)]
-    common = (_ptr(rope_cos), _ptr(rope_sin), rope_cos.shape[0], _ptr(kv_pool), kv_pool.shape[0])
-    tail = (_ptr(seq_lens), S, int(max_seq_len), None)
-    ws = (float(scale), _ptr(workspace), workspace.numel(), _ptr(d_err), _stream(stream),
-          ctypes.byref(opts))
-    for l in range(L):
-        pq, pk, pv, pbt, po = (b + l * n for b, n in zip(steps, sizes))
-        st = fn(ctypes.c_void_p(pq), ctypes.c_void_p(pk), ctypes.c_void_p(pv), *common,
-                ctypes.c_void_p(pbt), stride, stride, *tail, ctypes.c_void_p(po), *ws)
-        _check(st, where)
+    st = _L().paged_gqa_decode_append_layers(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(q_out), _ptr(out), L, S, _ptr(rope_cos),
+        _ptr(rope_sin), rope_cos.shape[0], _ptr(kv_pool), kv_pool.shape[0], int(int8),
+        _ptr(block_tables), block_tables.shape[1] * stride, stride, stride, _ptr(seq_lens),
+        int(max_seq_len), float(scale), _ptr(workspace), workspace.numel(), _ptr(d_err),
+        _stream(stream), int(early_kv), _ptr(host_stage), _ptr(dev_stage), stage)
+    _check(st, "paged_gqa_decode_append_layers")
 
 
 PREFILL_MMA_SYNC = 2  # comparison arm of paged_gqa_prefill (legacy bf16 mma.sync)
@@ -680,6 +705,30 @@ class Scheduler:
         _check(_L().pkv_sched_stats(self._h, *[ctypes.byref(x) for x in v]), "pkv_sched_stats")
         return dict(free=v[0].value, reserved=v[1].value, queued=v[2].value, running=v[3].value)
 
+    def begin_step(self):
+        """Grow every running request by one token (admission order); returns
+        (ids, lengths after the step) as int32 arrays."""
+        ids = np.empty(self.max_slots, np.int32)
+        lens = np.empty(self.max_slots, np.int32)
+        n = ctypes.c_int(0)
+        st = _L().pkv_sched_begin_step(self._h, ids.ctypes.data, lens.ctypes.data, self.max_slots,
+                                       ctypes.byref(n))
+        _check(st, "pkv_sched_begin_step")
+        return ids[:n.value].copy(), lens[:n.value].copy()
+
+    def step_bytes(self, batch: int, max_len: int) -> int:
+        return int(_L().pkv_sched_step_bytes(self._h, batch, max_len))
+
+    def pack_step(self, ids, max_len: int, block) -> int:
+        """Write the step block (lengths, then tables [L][B][P]) of requests
+        `ids` into `block` (a contiguous uint8 host tensor or array); returns P."""
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        ptr = block.data_ptr() if isinstance(block, torch.Tensor) else block.ctypes.data
+        nbytes = block.numel() if isinstance(block, torch.Tensor) else block.nbytes
+        _check(_L().pkv_sched_pack_step(self._h, ids.ctypes.data, len(ids), int(max_len), ptr,
+                                        nbytes), "pkv_sched_pack_step")
+        return max(1, (int(max_len) + PAGE_TOKENS - 1) // PAGE_TOKENS)
+
     def events(self):
         n = _L().pkv_sched_event_count(self._h)
         out = []
@@ -721,7 +770,7 @@ class DecodeStep:
 
     def __init__(self, pool, block_tables, seq_lens, positions, k, v, q, out, rope_cos, rope_sin,
                  scale, max_seq_len=None, workspace=None, d_err=None, q_rot=None, compute=None,
-                 use_graph=True, stream=None, fused=True, overlap_layers=True, schedule=0):
+                 use_graph=True, stream=None, fused=True, overlap_layers=True, schedule=None):
         self.L, self.S = block_tables.shape[0], block_tables.shape[1]
         self.t = dict(pool=pool, bt=block_tables, lens=seq_lens, pos=positions, k=k, v=v, q=q,
                       out=out, cos=rope_cos, sin=rope_sin)
@@ -733,7 +782,7 @@ class DecodeStep:
         self.max_seq_len = max_seq_len
         self.compute = compute
         self.overlap = bool(overlap_layers)
-        self.schedule = int(schedule)
+        self.schedule = None if schedule is None else int(schedule)   # None: automatic
         # the fused kernel places each new token at seq_lens - 1 (positions unused)
         self.fused = fused and compute in (None, COMPUTE_TENSOR)
         self.launches_per_step = (1 if self.fused else 2) * self.L
@@ -803,10 +852,15 @@ class Int8DecodeStep:
         kv_append_rope_int8(k[l], v[l], positions, block_tables[l], kv_pool, cos, sin,
                             q_in=q[l], q_out=q_rot[l])
         paged_gqa_decode_int8(q_rot[l], kv_pool, block_tables[l], seq_lens, out[l], scale)
-    By default (fused=True) each layer is one call
+    With fused=True each layer is one call
         paged_gqa_decode_append_int8(q[l], k[l], v[l], kv_pool, block_tables[l],
                                      seq_lens, out[l], cos, sin, q_out=q_rot[l])
-    which places token s at seq_lens[s] - 1 (positions unused); with
+    which places token s at seq_lens[s] - 1 (positions unused).  The default
+    (fused=None) takes the faster form for the batch: fused up to
+    FUSED_INT8_MAX_BATCH sequences, the two kernels above it (on GB300 at 2048
+    tokens a sequence the fused kernel, at the 128-register cap, loses from
+    about 192 sequences on: 100.8 vs 99.5 us/layer at 192, 128.3 vs 125.6 at
+    256; it wins 70.0 vs 72.2 at 128 and 26.1 vs 30.0 at 32).  With
     overlap_layers (the default) layer l >= 1 reads its tables and stages its
     first pages before layer l - 1's kernel has finished, which requires the
     layers' block tables to name disjoint pages.  Tensors are bound at
@@ -818,11 +872,13 @@ class Int8DecodeStep:
         k, v [L, S, 8, 64] bf16;  q, out [L, S, 32, 64] bf16
     """
 
+    FUSED_INT8_MAX_BATCH = 160
+
     def __init__(self, kv_pool, block_tables, seq_lens, positions, k, v, q, out, rope_cos,
                  rope_sin, scale, max_seq_len=None, workspace=None, d_err=None, q_rot=None,
-                 use_graph=True, stream=None, fused=True, overlap_layers=True):
+                 use_graph=True, stream=None, fused=None, overlap_layers=True):
         self.L, self.S = block_tables.shape[0], block_tables.shape[1]
-        self.fused = bool(fused)
+        self.fused = (self.S <= self.FUSED_INT8_MAX_BATCH) if fused is None else bool(fused)
         self.overlap = bool(overlap_layers)
         self.t = dict(pool=kv_pool, bt=block_tables, lens=seq_lens, pos=positions,
                       k=k, v=v, q=q, out=out, cos=rope_cos, sin=rope_sin)

@@ -81,6 +81,8 @@ struct DecodeParams {
   // kernel in the stream, so they are read (and the first pages staged)
   // before waiting for it; everything else still waits.
   int early;
+  uint64_t wait_ns;  // limit of each bounded wait (drains of copies in flight keep kWaitLimitNs)
+  int expire_first;  // 1: warp 0 of CTA 0 waits on a barrier nothing completes (timeout test)
 };
 
 // One (o, m, l) record: unnormalised o[4][64] and (m, l) for the 4 heads of a
@@ -255,6 +257,16 @@ __device__ __forceinline__ uint32_t owner_of(uint32_t u, uint32_t U, uint32_t N)
 }
 __device__ __forceinline__ uint32_t range_start(uint32_t k, uint32_t U, uint32_t N) {
   return (uint32_t)(((uint64_t)k * U) / N);
+}
+// The same owner for the kN warp ranges of a CTA (kN a compile-time count):
+// the number of k in 1 .. kN-1 whose range starts at or before u -- the
+// starts never decrease -- with no division by the runtime size U.
+template <int kN>
+__device__ __forceinline__ int warp_owner(uint32_t u, uint32_t U) {
+  int j = 0;
+#pragma unroll
+  for (int k = 1; k < kN; ++k) j += range_start(k, U, kN) <= u;
+  return j;
 }
 
 // ---------------------------------------------------------------------------
@@ -573,12 +585,10 @@ struct MmaState : Bf16Pages {
     // the denominator uses the same bf16-rounded weights as the PV product
     l = l * alpha + ((bf16lo_to_f32(pa0) + bf16hi_to_f32(pa0)) +
                      (bf16lo_to_f32(pa2) + bf16hi_to_f32(pa2)));
-    if (__any_sync(0xffffffffu, alpha != 1.f)) {  // the running max rarely moves
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        o[n][0] *= alpha;
-        o[n][1] *= alpha;
-      }
+    for (int n = 0; n < 8; ++n) {
+      o[n][0] *= alpha;
+      o[n][1] *= alpha;
     }
     // ---- O += P V ----------------------------------------------------------
     uint32_t m01 = 0xFFFFFFFFu, m89 = 0xFFFFFFFFu;
@@ -1297,7 +1307,7 @@ __device__ __noinline__ void finalise_segment(const DecodeParams& p, uint8_t* sm
                                               uint32_t U, uint32_t NC, uint32_t c, int lane) {
   const uint32_t last = base + np - 1;
   const uint32_t lo = max(base, a), hi = min(last, b - 1), n_cta = b - a;
-  const int j0 = (int)owner_of(lo - a, n_cta, kWarps), j1 = (int)owner_of(hi - a, n_cta, kWarps);
+  const int j0 = warp_owner<kWarps>(lo - a, n_cta), j1 = warp_owner<kWarps>(hi - a, n_cta);
   // the records of the covering warps j0 .. j1 with non-empty ranges: warp
   // j0's is in slot 1 if the segment starts in its range, every other one in
   // slot 0 (the segment began before the warp's range)
@@ -1428,7 +1438,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
     auto count_in = [&](int s, int g, uint32_t base, uint32_t np, bool more) {
       const uint32_t last = base + np - 1;
       const uint32_t lo = max(base, a), hi = min(last, b - 1), n_cta = b - a;
-      const int j0 = (int)owner_of(lo - a, n_cta, kWarps), j1 = (int)owner_of(hi - a, n_cta, kWarps);
+      const int j0 = warp_owner<kWarps>(lo - a, n_cta), j1 = warp_owner<kWarps>(hi - a, n_cta);
       int total = 0;
       for (int j = j0; j <= j1; ++j) total += range_start(j + 1, n_cta, kWarps) > range_start(j, n_cta, kWarps);
       int old = 0;
@@ -1450,12 +1460,24 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
       }
     };
 
+    // the timeout test: a barrier that nothing arrives on stands in for the
+    // first page's (whose copy is still drained below)
+    __shared__ __align__(8) uint64_t never_bar;
+    const bool expire = p.expire_first && blockIdx.x == 0 && warp == 0;
+    if (expire) {
+      if (lane == 0) {
+        mbar_init(smem_u32(&never_bar), 1);
+        fence_mbar_init();
+      }
+      __syncwarp();
+    }
     for (int uc = 0; uc < n_units; ++uc) {
       const int stage = uc % kStages;
       const uint32_t parity = (uint32_t)(uc / kStages) & 1u;
       const int pid = my_pid[stage];
       if (!timed_out) {
-        if (!mbar_wait_bounded(bars + 8 * stage, parity, kWaitLimitNs)) {
+        const uint32_t bar = (expire && uc == 0) ? smem_u32(&never_bar) : bars + 8 * stage;
+        if (!mbar_wait_bounded(bar, (expire && uc == 0) ? 0u : parity, p.wait_ns)) {
           timed_out = true;
           if (lane == 0) report_error(p.d_err, PKV_ERR_TIMEOUT);
         }
@@ -1594,16 +1616,16 @@ struct DynSmem {
 static_assert(DynSmem::kRecs % 16 == 0 && kRecordBytes % 16 == 0 && DynSmem::kSegs % 16 == 0,
               "aligned records");
 
-// Spin (one lane, bounded) until `pred()`; false on timeout.
+// Spin (one lane, bounded) until `pred()`; false after about limit_ns.
 template <class Pred>
-__device__ __forceinline__ bool spin_until(Pred pred) {
+__device__ __forceinline__ bool spin_until(Pred pred, uint64_t limit_ns) {
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
     if (pred()) return true;
     if ((it & 255u) == 255u) {
       const uint64_t now = global_timer_ns();
       if (t0 == 0) t0 = now;
-      else if (now - t0 > kWaitLimitNs) return false;
+      else if (now - t0 > limit_ns) return false;
     }
   }
 }
@@ -1816,7 +1838,7 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
       // this warp took every unit the CTA has of the segment: no record, but
       // the word still passes through this segment's turn, in order
       if (lane == 0) {
-        got = spin_until([&] { return *tag == lorder; });
+        got = spin_until([&] { return *tag == lorder; }, p.wait_ns);
         if (got) *tag = lorder + kSeg;
       }
       got = __shfl_sync(0xffffffffu, got, 0);
@@ -1834,7 +1856,7 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
     // a record slot of this warp whose last record has been merged
     const int bit = warp + kDynWarps * next_slot;
     next_slot ^= 1;
-    if (lane == 0) got = spin_until([&] { return busy[bit] == 0; });
+    if (lane == 0) got = spin_until([&] { return busy[bit] == 0; }, p.wait_ns);
     got = __shfl_sync(0xffffffffu, got, 0);
     if (!got) {
       st.reset();
@@ -1846,7 +1868,7 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
     uint32_t lo = 0, hi = 0;
     if (lane == 0) {
       busy[bit] = 1;
-      got = spin_until([&] { return *tag == lorder; });
+      got = spin_until([&] { return *tag == lorder; }, p.wait_ns);
       if (got) {
         __threadfence_block();  // the record before the count
         const unsigned long long old = atom_add_shared_u64(
@@ -1894,6 +1916,7 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
     __syncwarp();
   }
 
+  __shared__ __align__(8) uint64_t never_bar;
   for (int k = 0;; ++k) {
     const int stage = k % kDynStages;
     const int4 mt = my_meta[stage];
@@ -1902,7 +1925,18 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
     // new chunk is claimed only after it, so claims do not run ahead)
     const bool in_chunk = cq < ce;
     const Ahead nxt = look_ahead(in_chunk ? cq++ : n);
-    if (!mbar_wait_bounded(bars0 + 8 * stage, ((ph >> stage) & 1u) ^ 1u, kWaitLimitNs)) {
+    // the timeout test: warp 0 of CTA 0 waits on a barrier nothing completes
+    // instead of its first unit's (whose copy is drained below)
+    const bool expire = p.expire_first && k == 0 && blockIdx.x == 0 && warp == 0;
+    if (expire) {
+      if (lane == 0) {
+        mbar_init(smem_u32(&never_bar), 1);
+        fence_mbar_init();
+      }
+      __syncwarp();
+    }
+    if (!mbar_wait_bounded(expire ? smem_u32(&never_bar) : bars0 + 8 * stage,
+                           expire ? 0u : ((ph >> stage) & 1u) ^ 1u, p.wait_ns)) {
       failed = true;
       if (lane == 0) {
         atomicOr(ctl + 1, 1);
@@ -2269,10 +2303,13 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   const bool tiny = units_hint >= 0 && units_hint <= 4ll * 16 * 2 && !int8;
   const int warps = (opts && opts->warps_per_cta > 0) ? opts->warps_per_cta : (tiny ? 8 : 16);
   if (compute != PKV_COMPUTE_TENSOR && compute != PKV_COMPUTE_FMA) return PKV_ERR_INVALID_ARGUMENT;
+  if (opts && (opts->wait_limit_ns < 0 || (opts->expire_first_wait != 0 && opts->expire_first_wait != 1)))
+    return PKV_ERR_INVALID_ARGUMENT;
   if (app && compute != PKV_COMPUTE_TENSOR) return PKV_ERR_INVALID_ARGUMENT;
   const int cfg = warps * 100 + stages;
   // INT8 pages: static schedule, tensor cores, two pages per stage by default
   const int cfg8 = warps * 100 + ((opts && opts->stages > 0) ? opts->stages : 2);
+  if (opts && (opts->schedule < 0 || opts->schedule > 2)) return PKV_ERR_INVALID_ARGUMENT;
   if (int8 && (compute != PKV_COMPUTE_TENSOR || (opts && (opts->schedule == 1 || opts->combine == 1)) ||
                (cfg8 != 1604 && cfg8 != 1602 && cfg8 != 804) || (app && cfg8 != 1602)))
     return PKV_ERR_INVALID_ARGUMENT;
@@ -2314,6 +2351,8 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   prm.ws_prefix = reinterpret_cast<int32_t*>(ws + wl.prefix);
   prm.combine_mode = (opts && opts->combine == 1) ? 1 : 0;
   prm.early = (opts && opts->early_kv == 1) ? 1 : 0;
+  prm.wait_ns = (opts && opts->wait_limit_ns > 0) ? (uint64_t)opts->wait_limit_ns : kWaitLimitNs;
+  prm.expire_first = (opts && opts->expire_first_wait == 1) ? 1 : 0;
   prm.ws_ml = reinterpret_cast<float2*>(ws + wl.ml);
   prm.ws_o = reinterpret_cast<float*>(ws + wl.o);
   if (app) {
@@ -2336,8 +2375,16 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
       default: return launch_decode<MmaI8State<2>, 16, 2>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
     }
   }
-  const int schedule = opts ? opts->schedule : 0;
-  if (schedule == 1 && compute == PKV_COMPUTE_TENSOR) {
+  int schedule = opts ? opts->schedule : PKV_SCHEDULE_AUTO;
+  if (schedule == PKV_SCHEDULE_AUTO) {
+    // long per-SM ranges: the dynamic schedule evens out the warps' ends
+    const long long pages_bound = ms > 0 ? (ms + 15) / 16 : 0;
+    const long long units = 8ll * num_seqs * pages_bound;
+    schedule = (units >= (long long)PKV_DYNAMIC_MIN_UNITS * sms && min_units == 2 &&
+                (!opts || (opts->warps_per_cta == 0 && opts->stages == 0 && opts->ctas_per_sm == 0)))
+                   ? PKV_SCHEDULE_DYNAMIC : PKV_SCHEDULE_STATIC;
+  }
+  if (schedule == PKV_SCHEDULE_DYNAMIC && compute == PKV_COMPUTE_TENSOR) {
     const int rc2 = app ? launch_decode_dyn<true>(prm, map, dev, sms, ms, min_units, st)
                         : launch_decode_dyn<false>(prm, map, dev, sms, ms, min_units, st);
     if (rc2 != PKV_ERR_UNSUPPORTED_SHAPE) return rc2;  // too many sequences: static schedule
@@ -2430,4 +2477,53 @@ extern "C" int paged_gqa_decode_int8(const void* q, const void* kv_pool, int num
   return paged_gqa_decode_int8_ex(q, kv_pool, num_pages, block_tables, bt_row_stride, max_blocks,
                                   seq_lens, num_seqs, max_seq_len, out, scale, workspace,
                                   workspace_bytes, d_err, stream, nullptr);
+}
+
+extern "C" int paged_gqa_decode_append_layers(
+    const void* q, const void* k_new, const void* v_new, void* q_out, void* out, int num_layers,
+    int num_seqs, const float* rope_cos, const float* rope_sin, int max_pos, void* kv_pool,
+    int num_pages, int int8, const int32_t* block_tables, long long bt_layer_stride,
+    int bt_row_stride, int max_blocks, const int32_t* seq_lens, int max_seq_len, float scale,
+    void* workspace, size_t workspace_bytes, int* d_err, void* stream, int early_kv,
+    const void* host_stage, void* dev_stage, size_t stage_bytes) {
+  if (num_layers < 0 || num_seqs < 0 || bt_layer_stride < 0 || (int8 != 0 && int8 != 1) ||
+      (early_kv != 0 && early_kv != 1))
+    return PKV_ERR_INVALID_ARGUMENT;
+  if ((host_stage == nullptr) != (dev_stage == nullptr) || (host_stage && stage_bytes == 0))
+    return PKV_ERR_INVALID_ARGUMENT;
+  if (num_layers == 0 || num_seqs == 0) return PKV_OK;
+  if (!q || !k_new || !v_new || !out || !block_tables) return PKV_ERR_INVALID_ARGUMENT;
+  if (bt_layer_stride < (long long)num_seqs * bt_row_stride) return PKV_ERR_INVALID_ARGUMENT;
+  int rc = decode_check_args(q, kv_pool, num_pages, block_tables, bt_row_stride, max_blocks,
+                             seq_lens, num_seqs, out, scale);
+  if (rc != PKV_OK) return rc;
+  if (host_stage) {
+    int dev = 0;
+    rc = bind_stream_device(stream, &dev);
+    if (rc != PKV_OK) return rc;
+    rc = cuda_status(cudaMemcpyAsync(dev_stage, host_stage, stage_bytes, cudaMemcpyHostToDevice,
+                                     static_cast<cudaStream_t>(stream)),
+                     "cudaMemcpyAsync(step block)");
+    if (rc != PKV_OK) return rc;
+  }
+  const size_t qb = (size_t)num_seqs * PKV_NUM_Q_HEADS * PKV_HEAD_DIM * 2;
+  const size_t kb = (size_t)num_seqs * PKV_NUM_KV_HEADS * PKV_HEAD_DIM * 2;
+  const uint8_t* q8 = static_cast<const uint8_t*>(q);
+  const uint8_t* k8 = static_cast<const uint8_t*>(k_new);
+  const uint8_t* v8 = static_cast<const uint8_t*>(v_new);
+  uint8_t* o8 = static_cast<uint8_t*>(out);
+  uint8_t* qo8 = static_cast<uint8_t*>(q_out);
+  for (int l = 0; l < num_layers; ++l) {
+    pkv_decode_opts opts;
+    memset(&opts, 0, sizeof(opts));
+    opts.schedule = PKV_SCHEDULE_AUTO;
+    opts.early_kv = (early_kv && l > 0) ? 1 : 0;
+    const AppendArgs app{k8 + l * kb, v8 + l * kb, rope_cos, rope_sin, max_pos,
+                         qo8 ? qo8 + l * qb : nullptr};
+    rc = decode_entry(q8 + l * qb, kv_pool, num_pages, block_tables + l * bt_layer_stride,
+                      bt_row_stride, max_blocks, seq_lens, num_seqs, max_seq_len, o8 + l * qb,
+                      scale, workspace, workspace_bytes, d_err, stream, &opts, &app, int8 != 0);
+    if (rc != PKV_OK) return rc;
+  }
+  return PKV_OK;
 }

@@ -27,6 +27,7 @@ namespace {
 
 struct Request {
   int prompt = 0, allowed_new = 0, credit = 0, held = 0, slot = -1;
+  int len = 0;    // KV tokens the request's pages cover (the largest length grown to)
   int state = 0;  // 0 queued, 1 running, 2 done
   std::vector<std::vector<int32_t>> pages;  // [layer][logical page]
 };
@@ -50,6 +51,7 @@ struct pkv_sched {
   std::vector<Event> events;
   long long reserved = 0;  // sum over running requests of credit - held
   int running = 0;
+  std::vector<int> run_list;  // running requests in admission order (= id order)
   int mode = 0;            // 0 continuous, 1 static (admit only when nothing runs)
 };
 
@@ -132,10 +134,23 @@ extern "C" int pkv_sched_admit(pkv_sched* s, int* admitted, int max_out, int* n_
     r.state = 1;
     s->reserved += r.credit - r.held;
     ++s->running;
+    s->run_list.push_back(id);
     admitted[n++] = id;
   }
   *n_admitted = n;
   return PKV_OK;
+}
+
+// Pages request r still needs in all layers to cover new_len tokens, or -1
+// when that is not allowed (beyond max_blocks, its credit or the free pages).
+static long long grow_need(const pkv_sched* s, const Request& r, int new_len) {
+  const int need = ceil_pages(new_len);
+  if (need > s->max_blocks) return -1;
+  long long extra = 0;
+  for (int l = 0; l < s->num_layers; ++l)
+    if ((int)r.pages[l].size() < need) extra += need - (int)r.pages[l].size();
+  if (r.held + extra > r.credit || extra > (long long)s->free_stack.size()) return -1;
+  return extra;
 }
 
 extern "C" int pkv_sched_grow(pkv_sched* s, int req_id, int new_len) {
@@ -144,11 +159,8 @@ extern "C" int pkv_sched_grow(pkv_sched* s, int req_id, int new_len) {
   Request& r = s->reqs[req_id];
   const int need = ceil_pages(new_len);
   if (r.state != 1 || need > s->max_blocks) return PKV_ERR_INVALID_ARGUMENT;
-  long long extra = 0;
-  for (int l = 0; l < s->num_layers; ++l)
-    if ((int)r.pages[l].size() < need) extra += need - (int)r.pages[l].size();
-  if (r.held + extra > r.credit || extra > (long long)s->free_stack.size())
-    return PKV_ERR_POOL_EXHAUSTED;
+  if (grow_need(s, r, new_len) < 0) return PKV_ERR_POOL_EXHAUSTED;
+  if (new_len > r.len) r.len = new_len;
   for (int l = 0; l < s->num_layers; ++l) {
     while ((int)r.pages[l].size() < need) {
       const int32_t page = s->free_stack.back();
@@ -176,6 +188,70 @@ extern "C" int pkv_sched_finish(pkv_sched* s, int req_id) {
   r.slot = -1;
   r.state = 2;
   --s->running;
+  for (size_t i = 0; i < s->run_list.size(); ++i)
+    if (s->run_list[i] == req_id) {
+      s->run_list.erase(s->run_list.begin() + (long)i);
+      break;
+    }
+  return PKV_OK;
+}
+
+extern "C" int pkv_sched_begin_step(pkv_sched* s, int32_t* ids, int32_t* lens, int max_out,
+                                    int* batch) {
+  if (!s || !batch || max_out < 0 || (max_out > 0 && (!ids || !lens))) return PKV_ERR_INVALID_ARGUMENT;
+  const int B = (int)s->run_list.size();
+  if (B > max_out) return PKV_ERR_INVALID_ARGUMENT;
+  // every request must be able to take its token before any grows (all or nothing)
+  long long extra = 0;
+  for (int id : s->run_list) {
+    const Request& r = s->reqs[id];
+    const long long e = grow_need(s, r, r.len + 1);
+    if (e < 0) return PKV_ERR_POOL_EXHAUSTED;
+    extra += e;
+  }
+  if (extra > (long long)s->free_stack.size()) return PKV_ERR_POOL_EXHAUSTED;
+  for (int b = 0; b < B; ++b) {
+    const int id = s->run_list[b];
+    const int rc = pkv_sched_grow(s, id, s->reqs[id].len + 1);
+    if (rc != PKV_OK) return rc;  // cannot happen after the check above
+    ids[b] = id;
+    lens[b] = s->reqs[id].len;
+  }
+  *batch = B;
+  return PKV_OK;
+}
+
+// lens [batch] int32, then (16-byte aligned) tables [L][batch][pages] int32
+static size_t step_tables_offset(int batch) { return ((size_t)4 * batch + 15) & ~(size_t)15; }
+
+extern "C" size_t pkv_sched_step_bytes(const pkv_sched* s, int batch, int max_len) {
+  if (!s || batch < 0 || max_len < 0) return 0;
+  const int pages = ceil_pages(max_len) > 0 ? ceil_pages(max_len) : 1;
+  return step_tables_offset(batch) + (size_t)4 * s->num_layers * batch * pages;
+}
+
+extern "C" int pkv_sched_pack_step(const pkv_sched* s, const int32_t* ids, int batch, int max_len,
+                                   void* block, size_t bytes) {
+  if (!s || batch < 0 || max_len < 0 || (batch > 0 && (!ids || !block)))
+    return PKV_ERR_INVALID_ARGUMENT;
+  if (bytes < pkv_sched_step_bytes(s, batch, max_len)) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  const int pages = ceil_pages(max_len) > 0 ? ceil_pages(max_len) : 1;
+  int32_t* lens = static_cast<int32_t*>(block);
+  int32_t* tab = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(block) + step_tables_offset(batch));
+  for (int b = 0; b < batch; ++b) {
+    if (ids[b] < 0 || ids[b] >= (int)s->reqs.size() || s->reqs[ids[b]].state != 1)
+      return PKV_ERR_INVALID_ARGUMENT;
+    if (s->reqs[ids[b]].len > max_len) return PKV_ERR_INVALID_ARGUMENT;
+    lens[b] = s->reqs[ids[b]].len;
+  }
+  for (int l = 0; l < s->num_layers; ++l)
+    for (int b = 0; b < batch; ++b) {
+      const std::vector<int32_t>& pg = s->reqs[ids[b]].pages[l];
+      int32_t* row = tab + ((size_t)l * batch + b) * pages;
+      const int have = (int)pg.size() < pages ? (int)pg.size() : pages;
+      for (int j = 0; j < have; ++j) row[j] = pg[j];
+      for (int j = have; j < pages; ++j) row[j] = -1;
+    }
   return PKV_OK;
 }
 

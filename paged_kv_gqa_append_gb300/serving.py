@@ -8,9 +8,11 @@ layer), oversize requests are rejected, the prompt fills its pages at
 admission and every decode step appends one token per running sequence at its
 absolute position and attends over the sequence's own pages.
 
-The scheduler decides admissions and page ids (host C++); block tables live
-on the device per slot ([L][max_slots][max_blocks]), and each step gathers
-the running sequences' rows into a packed batch table.  The caller supplies
+The scheduler decides admissions and page ids (host C++).  Prompt appends
+use per-slot block tables on the device ([L][max_slots][max_blocks]); a decode
+step's lengths and tables are packed by the scheduler into one pinned host
+block and reach the device in one copy, issued together with the step's
+launches by one native call (paged_gqa_decode_append_layers).  The caller supplies
 the new K/V/q values through callbacks, so any model (or a synthetic source)
 can drive it.  Nothing here computes attention: every token goes through
 kv_append_rope / paged_gqa_decode / paged_gqa_decode_append(_layers), or
@@ -33,9 +35,11 @@ class StepBatch(NamedTuple):
     """One decode step's batch, from ContinuousBatcher.prepare_step."""
     ids: list                 # running request ids, in batch-row order
     lens_h: np.ndarray        # [B] int32 lengths after the step (host)
-    lens: torch.Tensor        # the same on the device
-    positions: torch.Tensor   # [B] int32 positions of the new tokens (lens - 1)
-    tables: torch.Tensor      # [L, B, max_blocks] int32 block tables
+    lens: torch.Tensor        # the same on the device (a view of dev_block)
+    tables: torch.Tensor      # [L, B, P] int32 block tables (a view of dev_block)
+    host_block: torch.Tensor  # the packed step block (pinned host memory)
+    dev_block: torch.Tensor   # its device copy, written by launch_step
+    turn: int                 # which of the two host blocks it is
 
 
 class ContinuousBatcher:
@@ -67,6 +71,15 @@ class ContinuousBatcher:
         self.host_tables = np.full((num_layers, max_slots, max_blocks), -1, np.int32)
         self.d_err = torch.zeros(1, dtype=torch.int32, device=self.dev)
         self.workspace = alloc_workspace(max_slots, self.dev)   # serves any batch <= max_slots
+        # step blocks (lengths + tables of a step, pkv_sched_pack_step): two
+        # pinned host blocks used in turn, each reused only once the copy made
+        # from it two steps earlier has run, and one device block
+        nmax = self.sched.step_bytes(max_slots, PAGE_TOKENS * max_blocks)
+        pin = self.dev.type == "cuda"
+        self._host_blocks = [torch.empty(nmax, dtype=torch.uint8, pin_memory=pin) for _ in range(2)]
+        self._block_done = [None, None]
+        self._turn = 0
+        self._dev_block = torch.empty(nmax, dtype=torch.uint8, device=self.dev)
         self.prompt = {}           # request id -> prompt tokens
         self.running = []          # request ids in admission order
         self.length = {}           # request id -> KV tokens held
@@ -135,26 +148,42 @@ class ContinuousBatcher:
     def prepare_step(self) -> "StepBatch":
         """Host side of one decode step for every running request.
 
-        Grows each request by one token (a new page in every layer where its
-        position starts one), copies changed block-table rows to the device
-        and gathers the batch's tables [L, B, max_blocks] and lengths (after
-        the step) on the device.  The returned batch is consumed by exactly
-        one launch_step; nothing here launches an attention kernel.
+        The scheduler grows each request by one token (a new page in every
+        layer where its position starts one) and packs the batch's lengths
+        (after the step) and block tables [L, B, P] into a pinned host block
+        (two C calls); launch_step copies it to the device.  The returned
+        batch is consumed by exactly one launch_step; nothing here launches a
+        kernel.
         """
-        ids = list(self.running)
-        for rid in ids:
-            if self.sched.grow(rid, self.length[rid] + 1) != OK:
-                raise PkvError(7, "ContinuousBatcher.prepare_step")
-            if self.length[rid] % PAGE_TOKENS == 0:      # a new page in every layer
-                self._sync_rows(rid)
-        lens_h = np.array([self.length[r] + 1 for r in ids], np.int32)
-        slots = self._upload(np.array([self.slot[r] for r in ids], np.int64))
-        lens = self._upload(lens_h)
-        tables = self.tables.index_select(1, slots)       # [L, B, M], contiguous
-        for rid in ids:
-            self.length[rid] += 1
+        ids_a, lens_h = self.sched.begin_step()
+        ids = [int(r) for r in ids_a]
+        if ids != self.running:
+            raise PkvError(1, "ContinuousBatcher.prepare_step")   # scheduler and batcher disagree
+        B = len(ids)
+        max_len = int(lens_h.max()) if B else 0
+        nbytes = self.sched.step_bytes(B, max_len)
+        turn = self._turn
+        self._turn ^= 1
+        if self._block_done[turn] is not None:
+            self._block_done[turn].synchronize()   # its copy from two steps ago has run
+        host = self._host_blocks[turn][:nbytes]
+        P = self.sched.pack_step(ids_a, max_len, host)
+        dev = self._dev_block[:nbytes]
+        off = (4 * B + 15) // 16 * 16
+        lens = dev[:4 * B].view(torch.int32)
+        tables = dev[off:off + 4 * self.L * B * P].view(torch.int32).view(self.L, B, P)
+        self.uploaded_bytes += nbytes
+        for rid, n in zip(ids, lens_h):
+            self.length[rid] = int(n)
             self.steps_done[rid] += 1
-        return StepBatch(ids, lens_h, lens, lens - 1, tables)
+        return StepBatch(ids, lens_h, lens, tables, host, dev, turn)
+
+    def _block_sent(self, batch):
+        """Mark (on the stream) the point after which the batch's host block may be reused."""
+        if self.dev.type == "cuda":
+            ev = torch.cuda.Event()
+            ev.record()
+            self._block_done[batch.turn] = ev
 
     def launch_step(self, batch: "StepBatch", q, k, v, out=None):
         """Device side of one decode step: every layer appends each request's
@@ -177,17 +206,24 @@ class ContinuousBatcher:
             return out
         ms = int(batch.lens_h.max())
         ws = self.workspace
-        if self.fused:        # one checked call issues the L per-layer launches
+        if self.fused:
+            # one C call: the step block's copy, then the L fused launches
+            # (layers >= 1 stage their pages while the previous layer ends)
             paged_gqa_decode_append_layers(q, k, v, self.pool, batch.tables, batch.lens, out,
                                            self.cos, self.sin, self.scale, ws, max_seq_len=ms,
-                                           d_err=self.d_err)
+                                           d_err=self.d_err, early_kv=1,
+                                           host_stage=batch.host_block, dev_stage=batch.dev_block)
+            self._block_sent(batch)
             return out
+        batch.dev_block.copy_(batch.host_block, non_blocking=True)
+        self._block_sent(batch)
+        positions = batch.lens - 1
         append = kv_append_rope_int8 if self.int8 else kv_append_rope
         decode = paged_gqa_decode_int8 if self.int8 else paged_gqa_decode
         for l in range(self.L):
             bt = batch.tables[l]
             q_rot = torch.empty_like(q[l])
-            append(k[l], v[l], batch.positions, bt, self.pool, self.cos, self.sin, q_in=q[l],
+            append(k[l], v[l], positions, bt, self.pool, self.cos, self.sin, q_in=q[l],
                    q_out=q_rot, d_err=self.d_err)
             decode(q_rot, self.pool, bt, batch.lens, out[l], self.scale, workspace=ws,
                    max_seq_len=ms, d_err=self.d_err)

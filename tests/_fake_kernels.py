@@ -134,12 +134,18 @@ def paged_gqa_decode_append_int8(q, k_new, v_new, kv_pool, block_tables, seq_len
 
 def paged_gqa_decode_append_layers(q, k_new, v_new, kv_pool, block_tables, seq_lens, out,
                                    rope_cos, rope_sin, scale, workspace, max_seq_len=None,
-                                   d_err=None, stream=None):
+                                   d_err=None, stream=None, q_out=None, early_kv=1,
+                                   host_stage=None, dev_stage=None):
     assert q.dim() == 4 and block_tables.dim() == 3 and block_tables.shape[0] == q.shape[0]
+    assert (host_stage is None) == (dev_stage is None) and early_kv in (0, 1)
+    if host_stage is not None:       # the step block's copy comes first
+        assert host_stage.dtype == torch.uint8 and dev_stage.numel() >= host_stage.numel()
+        dev_stage[:host_stage.numel()].copy_(host_stage)
     step = paged_gqa_decode_append_int8 if kv_pool.dtype == torch.uint8 else paged_gqa_decode_append
     for l in range(q.shape[0]):
         step(q[l], k_new[l], v_new[l], kv_pool, block_tables[l], seq_lens, out[l], rope_cos,
-             rope_sin, scale, workspace=workspace, max_seq_len=max_seq_len, d_err=d_err)
+             rope_sin, scale, q_out=None if q_out is None else q_out[l], workspace=workspace,
+             max_seq_len=max_seq_len, d_err=d_err)
 
 
 def alloc_workspace(num_seqs, device):

@@ -171,8 +171,11 @@ def _host_validation_checks():
               0.125, fake, 1 << 20, null, null, ctypes.byref(four)) == 1
 
 
-def _run_cpp_schedule(case, static=False):
-    """Drive the C++ scheduler with the oracle's step loop; return its log."""
+def _run_cpp_schedule(case, static=False, begin_step=False):
+    """Drive the C++ scheduler with the oracle's step loop; return its log.
+    With begin_step, each decode step is one pkv_sched_begin_step call (and
+    its packed block is checked against the scheduler's tables) instead of
+    one grow per request."""
     s = pkv.Scheduler(case.num_pages, case.num_layers, W.MAX_BLOCKS, 256, static=static)
     ids = [s.submit(int(p), case.allowed_new_tokens) for p in case.prompt_lens]
     running, length, done, log = [], {}, {}, []
@@ -183,8 +186,15 @@ def _run_cpp_schedule(case, static=False):
             length[rid], done[rid] = int(case.prompt_lens[rid]), 0
         running += admitted
         lens = []
+        if begin_step:
+            b_ids, b_lens = s.begin_step()
+            assert b_ids.tolist() == running
+            for rid, n in zip(running, b_lens.tolist()):
+                assert n == length[rid] + 1
+            _check_packed_block(s, b_ids, b_lens, case.num_layers)
         for rid in running:
-            assert s.grow(rid, length[rid] + 1) == pkv.OK
+            if not begin_step:
+                assert s.grow(rid, length[rid] + 1) == pkv.OK
             length[rid] += 1
             done[rid] += 1
             lens.append(length[rid])
@@ -196,13 +206,37 @@ def _run_cpp_schedule(case, static=False):
     return ids, log, s
 
 
+def _check_packed_block(s, ids, lens, L):
+    """The step block pkv_sched_pack_step writes: lengths, then per layer the
+    requests' page ids padded with -1 to P = ceil(max length / 16) entries."""
+    B = len(ids)
+    max_len = int(lens.max()) if B else 0
+    n = s.step_bytes(B, max_len)
+    block = np.full(n + 16, 0x55, np.uint8)            # 16 guard bytes that must stay untouched
+    P = s.pack_step(ids, max_len, block[:n])
+    assert P == max(1, -(-max_len // 16)) and (block[n:] == 0x55).all()
+    assert block[:4 * B].view(np.int32).tolist() == lens.tolist()
+    off = (4 * B + 15) // 16 * 16
+    tab = block[off:off + 4 * L * B * P].view(np.int32).reshape(L, B, P)
+    for l in range(L):
+        for b, rid in enumerate(ids.tolist()):
+            row, _ = s.block_table(rid, l)
+            assert tab[l, b].tolist() == row[:P].tolist()
+    if B:
+        with pytest.raises(pkv.PkvError):            # a length above max_len
+            s.pack_step(ids, max_len - 1, block[:n])
+        with pytest.raises(pkv.PkvError):            # a block too small
+            s.pack_step(ids, max_len, block[:n - 4])
+
+
 @pytest.mark.parametrize("static", [False, True])
-def test_scheduler_matches_oracle_on_continuous_mix(static):
+@pytest.mark.parametrize("begin_step", [False, True])
+def test_scheduler_matches_oracle_on_continuous_mix(static, begin_step):
     case = W.case_continuous()
     ids_o, log_o, sch_o = A.simulate(case.prompt_lens, case.decode_steps, case.num_pages,
                                      case.num_layers,
                                      mode=A.Scheduler.STATIC if static else A.Scheduler.CONTINUOUS)
-    ids_c, log_c, sch_c = _run_cpp_schedule(case, static)
+    ids_c, log_c, sch_c = _run_cpp_schedule(case, static, begin_step)
     assert [r for _, r in ids_c] == [r for _, r in ids_o]
     assert len(log_c) == len(log_o)
     for a, b in zip(log_c, log_o):
@@ -264,13 +298,24 @@ def test_scheduler_misuse_is_refused_without_state_change():
         assert lib.pkv_sched_grow(s, 0, 4 * 16 + 1) == INV      # past max_blocks
         assert lib.pkv_sched_grow(s, 0, 20) == pkv.OK
         assert lib.pkv_sched_grow(s, 0, 33) == pkv.ERR_POOL_EXHAUSTED   # past its credit
+        # begin_step: room for the batch, then all or nothing at the credit's edge
+        bid, blen, nb = (ctypes.c_int32 * 4)(), (ctypes.c_int32 * 4)(), i(-1)
+        assert lib.pkv_sched_begin_step(s, bid, blen, 0, ctypes.byref(nb)) == INV
+        assert lib.pkv_sched_begin_step(None, bid, blen, 4, ctypes.byref(nb)) == INV
+        assert lib.pkv_sched_begin_step(s, bid, blen, 4, ctypes.byref(nb)) == pkv.OK
+        assert nb.value == 1 and bid[0] == 0 and blen[0] == 21
+        assert lib.pkv_sched_grow(s, 0, 32) == pkv.OK  # the credit's last token
+        ev = lib.pkv_sched_event_count(s)
+        assert lib.pkv_sched_begin_step(s, bid, blen, 4, ctypes.byref(nb)) == pkv.ERR_POOL_EXHAUSTED
+        assert lib.pkv_sched_event_count(s) == ev      # nothing taken
+        assert lib.pkv_sched_pack_step(s, bid, 1, 16, None, 0) == INV   # null block
         row = (ctypes.c_int32 * 4)()
         assert lib.pkv_sched_block_table(s, 0, 2, row, None) == INV     # layer out of range
         assert lib.pkv_sched_block_table(s, 0, 1, None, None) == INV
         assert lib.pkv_sched_event(s, lib.pkv_sched_event_count(s), None, None, None, None) == INV
         free = i(0)
         assert lib.pkv_sched_stats(s, ctypes.byref(free), None, None, None) == pkv.OK
-        assert free.value == 16 - 4                    # 2 layers x 2 pages taken
+        assert free.value == 16 - 4                    # 2 layers x 2 pages taken (the credit)
         assert lib.pkv_sched_finish(s, 0) == pkv.OK
         assert lib.pkv_sched_finish(s, 0) == INV       # finished twice
         assert lib.pkv_sched_grow(s, 0, 1) == INV      # finished

@@ -1,9 +1,11 @@
 """Binding-level checks that need no GPU: the C calls the Python binding
 makes, recorded by a stand-in for the loaded library.
 
-paged_gqa_decode_append_layers must make exactly the C calls (same entry
-point, same arguments, same order) that L calls of the per-layer binding
-make, so that the per-layer path's GPU parity carries over to it.
+paged_gqa_decode_append_layers makes one call of the C function of the same
+name; the per-layer pointers that function derives (base + l x the layer's
+bytes, tables base + l x bt_layer_stride) must be exactly the arguments that
+L calls of the per-layer binding pass, so that the per-layer path's GPU
+parity carries over (the GPU tests also compare the two bit for bit).
 """
 import ctypes
 import types
@@ -66,10 +68,11 @@ STREAM = types.SimpleNamespace(cuda_stream=0x1234)
 
 @pytest.mark.parametrize("int8", [False, True])
 @pytest.mark.parametrize("max_seq_len", [None, 77])
-def test_layers_call_makes_the_per_layer_calls(rec, int8, max_seq_len):
+def test_layers_call_derives_the_per_layer_calls(rec, int8, max_seq_len):
     t = tensors(int8)
+    L, S = t["q"].shape[:2]
     per_layer = pkv.paged_gqa_decode_append_int8 if int8 else pkv.paged_gqa_decode_append
-    for l in range(t["q"].shape[0]):
+    for l in range(L):
         per_layer(t["q"][l], t["k"][l], t["v"][l], t["pool"], t["bt"][l], t["lens"], t["out"][l],
                   t["cos"], t["sin"], 0.125, workspace=t["ws"], max_seq_len=max_seq_len,
                   d_err=t["err"], stream=STREAM)
@@ -78,12 +81,25 @@ def test_layers_call_makes_the_per_layer_calls(rec, int8, max_seq_len):
                                        t["out"], t["cos"], t["sin"], 0.125, t["ws"],
                                        max_seq_len=max_seq_len, d_err=t["err"], stream=STREAM)
     got = rec.take()
-    assert len(got) == 3 and got == want
+    assert len(got) == 1 and got[0][0] == "paged_gqa_decode_append_layers"
+    (q, k, v, q_out, out, nl, ns, cos, sin, max_pos, pool, npages, i8, bt, bt_ls, bt_rs, mb, lens,
+     msl, scale, ws, wsb, err, stream, early, hst, dst, sb) = got[0][1]
+    assert (nl, ns, i8, early, hst, dst, sb, q_out) == (L, S, int(int8), 1, None, None, 0, None)
+    qb, kb = S * 32 * 64 * 2, S * 8 * 64 * 2
     name = "paged_gqa_decode_append_int8" if int8 else "paged_gqa_decode_append"
-    assert {c[0] for c in got} == {name}
-    # the per-layer pointers step through the layers
-    assert [c[1][0] for c in got] == [t["q"][l].data_ptr() for l in range(3)]
-    assert [c[1][8] for c in got] == [t["bt"][l].data_ptr() for l in range(3)]
+    for l, (fn, a) in enumerate(want):
+        assert fn == name
+        # per-layer arguments: q, k, v, cos, sin, max_pos, pool, pages, bt, stride, max_blocks,
+        # lens, S, max_seq_len, q_out, out, scale, ws, ws bytes, d_err, stream, opts
+        assert a[0] == q + l * qb and a[1] == k + l * kb and a[2] == v + l * kb
+        assert a[3:8] == (cos, sin, max_pos, pool, npages)
+        assert a[8] == bt + 4 * l * bt_ls and (a[9], a[10]) == (bt_rs, mb)
+        assert (a[11], a[12], a[13], a[14]) == (lens, S, msl, None)
+        assert a[15] == out + l * qb
+        assert a[16:21] == (scale, ws, wsb, err, stream)
+        # default options, automatic schedule (the native call sets early_kv on
+        # layers >= 1 itself)
+        assert a[21] == (pkv.COMPUTE_TENSOR, 0, 0, 0, 0, 0, pkv.SCHEDULE_AUTO, 0, 0, 0)
 
 
 @pytest.mark.parametrize("bad", ["out_shape", "kv_layers", "tables_layers", "tables_rows",

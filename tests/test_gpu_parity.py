@@ -460,3 +460,33 @@ def test_fused_append_decode_error_contract(lib, cuda_device, tables, bad, sched
     assert np.array_equal(bits(q_out), want_q)
     assert np.all(bits(out)[1] == 0)
     check_close(bf16_to_f64(out), ref, f"fused with a bad sequence ({bad})")
+
+
+# ------------------------------------------------------- bounded waits ----
+
+@pytest.mark.parametrize("schedule", [0, 1])
+def test_bounded_wait_runs_out_and_reports_timeout(lib, cuda_device, schedule):
+    """A wait that nothing completes (expire_first_wait) runs out after
+    wait_limit_ns: the call reports PKV_ERR_TIMEOUT in the device error word,
+    drains its copies and returns; after the workspace is zeroed again the
+    same decode is exact (the context and the library stay usable)."""
+    dev = cuda_device
+    case = W.case_mixed(seed=95)
+    pool = W.fill_pool(case, device=dev)
+    q = W.fill_queries(case, device=dev)[0].contiguous()
+    bt = torch.from_numpy(case.block_tables[0]).to(dev)
+    lens = torch.from_numpy(case.seq_lens).to(dev)
+    out = torch.empty_like(q)
+    ws = lib.alloc_workspace(case.num_seqs, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lib.paged_gqa_decode(q, pool, bt, lens, out, case.scale, workspace=ws, d_err=err,
+                         max_seq_len=case.max_seq_len, schedule=schedule,
+                         wait_limit_ns=20000, expire_first_wait=1)
+    assert lib.pkv_read_device_error(err) == lib.ERR_TIMEOUT
+    ws.zero_()
+    lib.paged_gqa_decode(q, pool, bt, lens, out, case.scale, workspace=ws, d_err=err,
+                         max_seq_len=case.max_seq_len, schedule=schedule)
+    assert lib.pkv_read_device_error(err) == 0
+    want, _ = OP.decode(W.bf16_bits(q), W.bf16_bits(pool), case.block_tables[0], case.seq_lens,
+                        case.scale)
+    check_close(bf16_to_f64(out), want, "decode after a timeout")

@@ -71,15 +71,20 @@ def test_prepare_and_launch_step_are_one_step(serving_on_oracle):
     src = lambda rid, l: W.request_kv(case.seed, rid, l, 0, cb.prompt[rid])
     assert cb.admit(src) == [0, 1]
     batch = cb.prepare_step()
+    L, B = case.num_layers, 2
     assert batch.ids == [0, 1]
     assert list(batch.lens_h) == [int(p) + 1 for p in case.prompt_lens]
-    assert batch.positions.tolist() == [int(p) for p in case.prompt_lens]
-    assert tuple(batch.tables.shape) == (case.num_layers, 2, W.MAX_BLOCKS)
-    for l in range(case.num_layers):
+    # the packed host block: the lengths, then tables [L, B, P] padded with -1
+    P = -(-int(batch.lens_h.max()) // W.PAGE_TOKENS)
+    host = batch.host_block
+    assert host.view(torch.int32)[:B].tolist() == list(batch.lens_h)
+    off = (4 * B + 15) // 16 * 16
+    tab = host[off:off + 4 * L * B * P].view(torch.int32).view(L, B, P)
+    assert tuple(batch.tables.shape) == (L, B, P)
+    for l in range(L):
         for b, rid in enumerate(batch.ids):
             row, _ = cb.sched.block_table(rid, l)
-            assert batch.tables[l, b].tolist() == list(row)
-    L = case.num_layers
+            assert tab[l, b].tolist() == list(row[:P])
     q = torch.zeros((L, 2, 32, 64), dtype=torch.bfloat16)
     kv = torch.zeros((L, 2, 8, 64), dtype=torch.bfloat16)
     with pytest.raises(ValueError):
@@ -89,6 +94,8 @@ def test_prepare_and_launch_step_are_one_step(serving_on_oracle):
     out = cb.launch_step(batch, q, kv, kv)
     assert tuple(out.shape) == (L, 2, 32, 64)
     assert cb.error() == 0
+    # launch_step copied the block: the device views now hold it
+    assert torch.equal(batch.tables.cpu(), tab) and batch.lens.tolist() == list(batch.lens_h)
     assert cb.uploaded_bytes > 0
 
 
