@@ -2133,7 +2133,8 @@ static long long whole_segment_grid(long long nc, int num_seqs, long long pages_
 
 template <class State, int kWarps, int kStages, bool kAppend = false>
 static int launch_decode(const DecodeParams& prm, const CUtensorMap& map, int device, int num_sms,
-                         int max_seq_len, int min_units, int ctas_per_sm, cudaStream_t stream) {
+                         int max_seq_len, int min_units, int ctas_per_sm, cudaStream_t stream,
+                         bool one_segment = false) {
   const size_t smem =
       SmemLayout<kWarps, kStages, State::kStageBytes, State::kTokenBytes>::bytes(prm.num_seqs);
   constexpr int kP = State::kPagesPerUnit;
@@ -2150,6 +2151,7 @@ static int launch_decode(const DecodeParams& prm, const CUtensorMap& map, int de
   if (want < nc) nc = want;
   if (nc < 1) nc = 1;
   if (occ == 1) nc = whole_segment_grid(nc, prm.num_seqs, pages_bound);
+  else if (one_segment && 8ll * prm.num_seqs <= (long long)num_sms * occ) nc = 8ll * prm.num_seqs;
 
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -2301,7 +2303,23 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   // 10.3 -> 8.2 us).  INT8 pages keep their own default.
   const long long units_hint = max_seq_len > 0 ? 8ll * num_seqs * ((max_seq_len + 15) / 16) : -1;
   const bool tiny = units_hint >= 0 && units_hint <= 4ll * 16 * 2 && !int8;
-  const int warps = (opts && opts->warps_per_cta > 0) ? opts->warps_per_cta : (tiny ? 8 : 16);
+  // Between one and two (sequence, KV head) segments per SM at the length
+  // bound (19 .. 38 sequences on a 152-SM GB300): 8-warp CTAs, two to an SM,
+  // one segment each -- no segment is split between CTAs, and the next
+  // launch's CTAs find free slots while this one's last CTAs finish (batch
+  // 32 x 2048 fused step: 26.8 -> 26.1 us/layer).
+  const long long pages_hint = max_seq_len > 0 ? (max_seq_len + 15) / 16 : 0;
+  const int sms_hint = [&] {
+    int d = 0;
+    return cudaGetDevice(&d) == cudaSuccess ? sm_count(d) : 0;
+  }();
+  const bool seg_pairs = !int8 && !tiny && compute == PKV_COMPUTE_TENSOR && sms_hint > 0 &&
+                         !(opts && (opts->warps_per_cta > 0 || opts->stages > 0 ||
+                                    opts->ctas_per_sm > 0 || opts->min_units_per_warp > 0 ||
+                                    opts->combine == 1)) &&
+                         8ll * num_seqs >= sms_hint && 8ll * num_seqs <= 2ll * sms_hint &&
+                         pages_hint >= 16;
+  const int warps = (opts && opts->warps_per_cta > 0) ? opts->warps_per_cta : ((tiny || seg_pairs) ? 8 : 16);
   if (compute != PKV_COMPUTE_TENSOR && compute != PKV_COMPUTE_FMA) return PKV_ERR_INVALID_ARGUMENT;
   if (opts && (opts->wait_limit_ns < 0 || (opts->expire_first_wait != 0 && opts->expire_first_wait != 1)))
     return PKV_ERR_INVALID_ARGUMENT;
@@ -2391,7 +2409,7 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   }
   if (app) {
     switch (cfg) {
-      case 802: return launch_decode<MmaState, 8, 2, true>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
+      case 802: return launch_decode<MmaState, 8, 2, true>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st, seg_pairs);
       case 402: return launch_decode<MmaState, 4, 2, true>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
       default: return launch_decode<MmaState, 16, 2, true>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
     }
@@ -2400,7 +2418,7 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
     return launch_decode<FmaState, 4, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
   switch (cfg) {
     case 1603: return launch_decode<MmaState, 16, 3>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
-    case 802: return launch_decode<MmaState, 8, 2>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
+    case 802: return launch_decode<MmaState, 8, 2>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st, seg_pairs);
     case 804: return launch_decode<MmaState, 8, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
     case 402: return launch_decode<MmaState, 4, 2>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
     case 404: return launch_decode<MmaState, 4, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
