@@ -858,9 +858,9 @@ class Int8DecodeStep:
     which places token s at seq_lens[s] - 1 (positions unused).  The default
     (fused=None) takes the faster form for the batch: fused up to
     FUSED_INT8_MAX_BATCH sequences, the two kernels above it (on GB300 at 2048
-    tokens a sequence the fused kernel, at the 128-register cap, loses from
-    about 192 sequences on: 100.8 vs 99.5 us/layer at 192, 128.3 vs 125.6 at
-    256; it wins 70.0 vs 72.2 at 128 and 26.1 vs 30.0 at 32).  With
+    tokens a sequence the fused kernel, at the 128-register cap, wins at 32
+    sequences, 26.3 vs 29.4 us/layer, and loses at 128, 72.8 vs 71.0, and at
+    256, 133.6 vs 122.4).  With
     overlap_layers (the default) layer l >= 1 reads its tables and stages its
     first pages before layer l - 1's kernel has finished, which requires the
     layers' block tables to name disjoint pages.  Tensors are bound at
@@ -872,7 +872,7 @@ class Int8DecodeStep:
         k, v [L, S, 8, 64] bf16;  q, out [L, S, 32, 64] bf16
     """
 
-    FUSED_INT8_MAX_BATCH = 160
+    FUSED_INT8_MAX_BATCH = 80
 
     def __init__(self, kv_pool, block_tables, seq_lens, positions, k, v, q, out, rope_cos,
                  rope_sin, scale, max_seq_len=None, workspace=None, d_err=None, q_rot=None,

@@ -52,6 +52,7 @@ constexpr int kRecordBytes = 4 * 64 * 4 + 4 * 8;  // o[4][64] fp32 + (m, l)[4]
 constexpr int kMaxCtasPerSm = 8;     // workspace is sized for this many CTAs per SM
 constexpr int kMaxSeqs = 4096;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per stage wait
+constexpr uint32_t kWaitLimitUs = 2000000u;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeParams {
@@ -81,7 +82,7 @@ struct DecodeParams {
   // kernel in the stream, so they are read (and the first pages staged)
   // before waiting for it; everything else still waits.
   int early;
-  uint64_t wait_ns;  // limit of each bounded wait (drains of copies in flight keep kWaitLimitNs)
+  uint32_t wait_us;  // limit of each bounded wait in us (drains of copies in flight keep kWaitLimitUs)
   int expire_first;  // 1: warp 0 of CTA 0 waits on a barrier nothing completes (timeout test)
 };
 
@@ -1298,13 +1299,13 @@ __device__ __forceinline__ void cross_cta_merge(const DecodeParams& p, const Mer
 // A segment that several warps of this CTA cover, once every covering warp
 // has written its record to shared memory: merge the records and store the
 // output, or hand the CTA's record on to the cross-CTA merge.  CTA c owns
-// units [a, b), split evenly over kWarps warps.  Out of line: it runs once
-// per such segment, and inlined its temporaries would crowd the page loop's
-// registers.
+// units [a, b), split evenly over kWarps warps.  (Called out of line from the
+// bf16-page kernels, whose page loop needs the registers, and inline from
+// the INT8-page ones, where the call's saved registers spill instead.)
 template <class Smem, int kWarps>
-__device__ __noinline__ void finalise_segment(const DecodeParams& p, uint8_t* smem, int s, int g,
-                                              uint32_t base, uint32_t np, uint32_t a, uint32_t b,
-                                              uint32_t U, uint32_t NC, uint32_t c, int lane) {
+__device__ __forceinline__ void finalise_segment(const DecodeParams& p, uint8_t* smem, int s, int g,
+                                                 uint32_t base, uint32_t np, uint32_t a, uint32_t b,
+                                                 uint32_t U, uint32_t NC, uint32_t c, int lane) {
   const uint32_t last = base + np - 1;
   const uint32_t lo = max(base, a), hi = min(last, b - 1), n_cta = b - a;
   const int j0 = warp_owner<kWarps>(lo - a, n_cta), j1 = warp_owner<kWarps>(hi - a, n_cta);
@@ -1323,6 +1324,13 @@ __device__ __noinline__ void finalise_segment(const DecodeParams& p, uint8_t* sm
     m.store_output(p, s, g, lane);
   else
     cross_cta_merge(p, m, s, g, base, np, U, NC, c, lane);
+}
+
+template <class Smem, int kWarps>
+__device__ __noinline__ void finalise_segment_call(const DecodeParams& p, uint8_t* smem, int s, int g,
+                                                   uint32_t base, uint32_t np, uint32_t a, uint32_t b,
+                                                   uint32_t U, uint32_t NC, uint32_t c, int lane) {
+  finalise_segment<Smem, kWarps>(p, smem, s, g, base, np, a, b, U, NC, c, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -1433,7 +1441,10 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
     int fin_s = -1, fin_g = 0;
     uint32_t fin_base = 0, fin_np = 0;
     auto finalise = [&](int s, int g, uint32_t base, uint32_t np) {
-      finalise_segment<Smem, kWarps>(p, smem, s, g, base, np, a, b, U, NC, c, lane);
+      if constexpr (State::kBf16Pages)
+        finalise_segment_call<Smem, kWarps>(p, smem, s, g, base, np, a, b, U, NC, c, lane);
+      else
+        finalise_segment<Smem, kWarps>(p, smem, s, g, base, np, a, b, U, NC, c, lane);
     };
     auto count_in = [&](int s, int g, uint32_t base, uint32_t np, bool more) {
       const uint32_t last = base + np - 1;
@@ -1460,24 +1471,26 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
       }
     };
 
-    // the timeout test: a barrier that nothing arrives on stands in for the
-    // first page's (whose copy is still drained below)
-    __shared__ __align__(8) uint64_t never_bar;
-    const bool expire = p.expire_first && blockIdx.x == 0 && warp == 0;
-    if (expire) {
+    // the timeout test: the first warp waits on a barrier that nothing
+    // arrives on instead of its first page (whose copy is drained below)
+    if (p.expire_first && blockIdx.x == 0 && warp == 0) {
+      __shared__ __align__(8) uint64_t never_bar;
       if (lane == 0) {
         mbar_init(smem_u32(&never_bar), 1);
         fence_mbar_init();
       }
       __syncwarp();
+      if (!mbar_wait_bounded(smem_u32(&never_bar), 0u, p.wait_us)) {
+        timed_out = true;
+        if (lane == 0) report_error(p.d_err, PKV_ERR_TIMEOUT);
+      }
     }
     for (int uc = 0; uc < n_units; ++uc) {
       const int stage = uc % kStages;
       const uint32_t parity = (uint32_t)(uc / kStages) & 1u;
       const int pid = my_pid[stage];
       if (!timed_out) {
-        const uint32_t bar = (expire && uc == 0) ? smem_u32(&never_bar) : bars + 8 * stage;
-        if (!mbar_wait_bounded(bar, (expire && uc == 0) ? 0u : parity, p.wait_ns)) {
+        if (!mbar_wait_bounded(bars + 8 * stage, parity, p.wait_us)) {
           timed_out = true;
           if (lane == 0) report_error(p.d_err, PKV_ERR_TIMEOUT);
         }
@@ -1523,7 +1536,7 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
       // Drain whatever this warp still has in flight before leaving (bounded).
       for (int u = max(0, iv - kStages); u < iv; ++u) {
         const int stage = u % kStages;
-        (void)mbar_wait_bounded(bars + 8 * stage, (uint32_t)(u / kStages) & 1u, kWaitLimitNs);
+        (void)mbar_wait_bounded(bars + 8 * stage, (uint32_t)(u / kStages) & 1u, kWaitLimitUs);
       }
     }
   } else if (p.early) {
@@ -1618,14 +1631,14 @@ static_assert(DynSmem::kRecs % 16 == 0 && kRecordBytes % 16 == 0 && DynSmem::kSe
 
 // Spin (one lane, bounded) until `pred()`; false after about limit_ns.
 template <class Pred>
-__device__ __forceinline__ bool spin_until(Pred pred, uint64_t limit_ns) {
+__device__ __forceinline__ bool spin_until(Pred pred, uint32_t limit_us) {
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
     if (pred()) return true;
     if ((it & 255u) == 255u) {
       const uint64_t now = global_timer_ns();
       if (t0 == 0) t0 = now;
-      else if (now - t0 > limit_ns) return false;
+      else if (now - t0 > (uint64_t)limit_us * 1000ull) return false;
     }
   }
 }
@@ -1838,7 +1851,7 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
       // this warp took every unit the CTA has of the segment: no record, but
       // the word still passes through this segment's turn, in order
       if (lane == 0) {
-        got = spin_until([&] { return *tag == lorder; }, p.wait_ns);
+        got = spin_until([&] { return *tag == lorder; }, p.wait_us);
         if (got) *tag = lorder + kSeg;
       }
       got = __shfl_sync(0xffffffffu, got, 0);
@@ -1856,7 +1869,7 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
     // a record slot of this warp whose last record has been merged
     const int bit = warp + kDynWarps * next_slot;
     next_slot ^= 1;
-    if (lane == 0) got = spin_until([&] { return busy[bit] == 0; }, p.wait_ns);
+    if (lane == 0) got = spin_until([&] { return busy[bit] == 0; }, p.wait_us);
     got = __shfl_sync(0xffffffffu, got, 0);
     if (!got) {
       st.reset();
@@ -1868,7 +1881,7 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
     uint32_t lo = 0, hi = 0;
     if (lane == 0) {
       busy[bit] = 1;
-      got = spin_until([&] { return *tag == lorder; }, p.wait_ns);
+      got = spin_until([&] { return *tag == lorder; }, p.wait_us);
       if (got) {
         __threadfence_block();  // the record before the count
         const unsigned long long old = atom_add_shared_u64(
@@ -1916,8 +1929,23 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
     __syncwarp();
   }
 
-  __shared__ __align__(8) uint64_t never_bar;
-  for (int k = 0;; ++k) {
+  if (p.expire_first && blockIdx.x == 0 && warp == 0 && my_meta[0].x >= 0) {
+    // the timeout test: a barrier nothing arrives on, in place of the first unit's
+    __shared__ __align__(8) uint64_t never_bar;
+    if (lane == 0) {
+      mbar_init(smem_u32(&never_bar), 1);
+      fence_mbar_init();
+    }
+    __syncwarp();
+    if (!mbar_wait_bounded(smem_u32(&never_bar), 0u, p.wait_us)) {
+      failed = true;
+      if (lane == 0) {
+        atomicOr(ctl + 1, 1);
+        report_error(p.d_err, PKV_ERR_TIMEOUT);
+      }
+    }
+  }
+  for (int k = 0; !failed; ++k) {
     const int stage = k % kDynStages;
     const int4 mt = my_meta[stage];
     if (mt.x < 0 || vctl[1] != 0) break;
@@ -1925,18 +1953,7 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
     // new chunk is claimed only after it, so claims do not run ahead)
     const bool in_chunk = cq < ce;
     const Ahead nxt = look_ahead(in_chunk ? cq++ : n);
-    // the timeout test: warp 0 of CTA 0 waits on a barrier nothing completes
-    // instead of its first unit's (whose copy is drained below)
-    const bool expire = p.expire_first && k == 0 && blockIdx.x == 0 && warp == 0;
-    if (expire) {
-      if (lane == 0) {
-        mbar_init(smem_u32(&never_bar), 1);
-        fence_mbar_init();
-      }
-      __syncwarp();
-    }
-    if (!mbar_wait_bounded(expire ? smem_u32(&never_bar) : bars0 + 8 * stage,
-                           expire ? 0u : ((ph >> stage) & 1u) ^ 1u, p.wait_ns)) {
+    if (!mbar_wait_bounded(bars0 + 8 * stage, ((ph >> stage) & 1u) ^ 1u, p.wait_us)) {
       failed = true;
       if (lane == 0) {
         atomicOr(ctl + 1, 1);
@@ -1997,7 +2014,7 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
     // after a timeout: wait (bounded) for this warp's copies still in flight
     for (int stg = 0; stg < kDynStages; ++stg)
       if ((armed >> stg) & 1u)
-        (void)mbar_wait_bounded(bars0 + 8 * stg, ((ph >> stg) & 1u) ^ 1u, kWaitLimitNs);
+        (void)mbar_wait_bounded(bars0 + 8 * stg, ((ph >> stg) & 1u) ^ 1u, kWaitLimitUs);
   }
 
   if (p.combine_mode == 1 && blockIdx.x == 0)
@@ -2369,7 +2386,8 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   prm.ws_prefix = reinterpret_cast<int32_t*>(ws + wl.prefix);
   prm.combine_mode = (opts && opts->combine == 1) ? 1 : 0;
   prm.early = (opts && opts->early_kv == 1) ? 1 : 0;
-  prm.wait_ns = (opts && opts->wait_limit_ns > 0) ? (uint64_t)opts->wait_limit_ns : kWaitLimitNs;
+  const uint64_t wait_ns = (opts && opts->wait_limit_ns > 0) ? (uint64_t)opts->wait_limit_ns : kWaitLimitNs;
+  prm.wait_us = (uint32_t)std::min<uint64_t>(std::max<uint64_t>(wait_ns / 1000ull, 1ull), 0xFFFFFFFFull);
   prm.expire_first = (opts && opts->expire_first_wait == 1) ? 1 : 0;
   prm.ws_ml = reinterpret_cast<float2*>(ws + wl.ml);
   prm.ws_o = reinterpret_cast<float*>(ws + wl.o);

@@ -51,7 +51,7 @@ constexpr int kPfTokens = 4 * kPfWarps;        // query tokens per CTA
 constexpr int kPfStages = 4;
 constexpr int kPfStageBytes = 4096;            // K tile + V tile of one (page, head)
 constexpr int kPfThreads = (kPfWarps + 1) * 32;
-constexpr uint64_t kPfWaitNs = 2000000000ull;  // 2 s per wait
+constexpr uint32_t kPfWaitUs = 2000000u;  // 2 s per wait (in us)
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct PrefillParams {
@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       const int st = j % kPfStages;
       bool ok = true;
       if (lane == 0 && j >= kPfStages)
-        ok = mbar_wait_bounded(smem_u32(&empty[st]), (uint32_t)((j / kPfStages - 1) & 1), kPfWaitNs);
+        ok = mbar_wait_bounded(smem_u32(&empty[st]), (uint32_t)((j / kPfStages - 1) & 1), kPfWaitUs);
       if (!__shfl_sync(0xffffffffu, (int)ok, 0)) {
         if (lane == 0) report_error(p.d_err, PKV_ERR_TIMEOUT);
         return;  // consumers time out on the pages never issued
@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     // wait (bounded) for the last copies to land before the CTA may exit
     if (lane == 0)
       for (int j = max(0, n_pages - kPfStages); j < n_pages; ++j)
-        (void)mbar_wait_bounded(smem_u32(&full[j % kPfStages]), (uint32_t)((j / kPfStages) & 1), kPfWaitNs);
+        (void)mbar_wait_bounded(smem_u32(&full[j % kPfStages]), (uint32_t)((j / kPfStages) & 1), kPfWaitUs);
     return;
   }
   if (warp >= n_active) return;
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
 
   for (int j = 0; j < n_pages; ++j) {
     const int st = j % kPfStages;
-    if (!mbar_wait_bounded(smem_u32(&full[st]), (uint32_t)((j / kPfStages) & 1), kPfWaitNs)) {
+    if (!mbar_wait_bounded(smem_u32(&full[st]), (uint32_t)((j / kPfStages) & 1), kPfWaitUs)) {
       if (lane == 0) report_error(p.d_err, PKV_ERR_TIMEOUT);
       timed_out = true;
       break;
@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         const int st = b % nst;
         int next[kTcPages];
         block_page_ids(row, b + 1, n_pages_seq, next);
-        if (b >= nst && !mbar_wait_bounded(empty + 8 * st, (uint32_t)((b / nst - 1) & 1), kPfWaitNs)) {
+        if (b >= nst && !mbar_wait_bounded(empty + 8 * st, (uint32_t)((b / nst - 1) & 1), kPfWaitUs)) {
           report_error(p.d_err, PKV_ERR_TIMEOUT);
           break;
         }
@@ -493,19 +493,19 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       // normally saw every one; after a timeout they may not have)
       bool landed = true;
       for (int b = max(0, issued - nst); b < issued; ++b)
-        landed = landed && mbar_wait_bounded(full + 8 * (b % nst), (uint32_t)((b / nst) & 1), kPfWaitNs);
+        landed = landed && mbar_wait_bounded(full + 8 * (b % nst), (uint32_t)((b / nst) & 1), kPfWaitUs);
       if (!landed) report_error(p.d_err, PKV_ERR_TIMEOUT);
     }
   } else if (warp == 1) {
     // ---------------- S = Q K^T issuer ------------------------------------
     if (lane == 0) {
       const uint32_t id_s = umma_idesc_bf16(kTcRows, kTcKeys, 0);
-      bool ok = mbar_wait_bounded(qready, 0, kPfWaitNs);
+      bool ok = mbar_wait_bounded(qready, 0, kPfWaitUs);
       for (int b = 0; b < nb && ok; ++b) {
         const int st = b % kTcKStages, sb = b & 1;
         // S buffer sb holds P(b - 2) until P V(b - 2) is done
-        if (!mbar_wait_bounded(kfull + 8 * st, (uint32_t)((b / kTcKStages) & 1), kPfWaitNs) ||
-            (b >= 2 && !mbar_wait_bounded(odone + 8 * sb, (uint32_t)((b / 2 - 1) & 1), kPfWaitNs))) {
+        if (!mbar_wait_bounded(kfull + 8 * st, (uint32_t)((b / kTcKStages) & 1), kPfWaitUs) ||
+            (b >= 2 && !mbar_wait_bounded(odone + 8 * sb, (uint32_t)((b / 2 - 1) & 1), kPfWaitUs))) {
           ok = false;
           break;
         }
@@ -520,7 +520,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       }
       // every MMA issued here is complete before tensor memory is freed
       umma_commit(drain);
-      if (!mbar_wait_bounded(drain, 0, kPfWaitNs)) ok = false;
+      if (!mbar_wait_bounded(drain, 0, kPfWaitUs)) ok = false;
       if (!ok) report_error(p.d_err, PKV_ERR_TIMEOUT);
     }
   } else if (warp == 3) {
@@ -530,8 +530,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       bool ok = true;
       for (int b = 0; b < nb; ++b) {
         const int st = b % kTcVStages, sb = b & 1;
-        if (!mbar_wait_bounded(pfull + 8 * sb, (uint32_t)((b / 2) & 1), kPfWaitNs) ||
-            !mbar_wait_bounded(vfull + 8 * st, (uint32_t)((b / kTcVStages) & 1), kPfWaitNs)) {
+        if (!mbar_wait_bounded(pfull + 8 * sb, (uint32_t)((b / 2) & 1), kPfWaitUs) ||
+            !mbar_wait_bounded(vfull + 8 * st, (uint32_t)((b / kTcVStages) & 1), kPfWaitUs)) {
           ok = false;
           break;
         }
@@ -546,7 +546,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         umma_commit(vempty + 8 * st);
       }
       umma_commit(drain + 8);
-      if (!mbar_wait_bounded(drain + 8, 0, kPfWaitNs)) ok = false;
+      if (!mbar_wait_bounded(drain + 8, 0, kPfWaitUs)) ok = false;
       if (!ok) report_error(p.d_err, PKV_ERR_TIMEOUT);
     }
   } else if (warp >= 4) {
@@ -560,7 +560,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     float l_run = 0.f;  // row sum of the bf16 weights, relative to m_used
     // every wait is decided warp-wide: the tensor-memory loads are warp-collective
     auto wait_all = [&](uint32_t bar, uint32_t parity) {
-      return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, kPfWaitNs));
+      return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, kPfWaitUs));
     };
     {  // this row of Q (zeros past the chunk) into tensor memory: the A operand of S
       uint32_t w[32];
