@@ -1039,8 +1039,9 @@ def run_continuous_line(args, world, rank, local):
         cb = batcher()
         bmax = 64
         prompt_h = prompt_d.cpu().pin_memory()
-        q_h = W.normal_bf16((L * bmax * W.NUM_Q_HEADS * W.HEAD_DIM,), gen).cpu().pin_memory()
-        kv_h = W.normal_bf16((2, L * bmax * W.NUM_KV_HEADS * W.HEAD_DIM), gen).cpu().pin_memory()
+        # a step's q, k and v packed in one pinned block: one upload per step
+        qkv_h = W.normal_bf16((L * bmax * (W.NUM_Q_HEADS + 2 * W.NUM_KV_HEADS) * W.HEAD_DIM,),
+                              gen).cpu().pin_memory()
         out_h = torch.empty(L * bmax * W.NUM_Q_HEADS * W.HEAD_DIM, dtype=torch.bfloat16,
                             pin_memory=True)
         P = lambda rid, l: (prompt_h[0, :cb.prompt[rid]], prompt_h[1, :cb.prompt[rid]])
@@ -1053,9 +1054,10 @@ def run_continuous_line(args, world, rank, local):
             batch = cb.prepare_step()
             B = len(batch.ids)
             nq, nkv = L * B * W.NUM_Q_HEADS * W.HEAD_DIM, L * B * W.NUM_KV_HEADS * W.HEAD_DIM
-            q = q_h[:nq].view(L, B, W.NUM_Q_HEADS, W.HEAD_DIM).to(dev, non_blocking=True)
-            k = kv_h[0, :nkv].view(L, B, W.NUM_KV_HEADS, W.HEAD_DIM).to(dev, non_blocking=True)
-            v = kv_h[1, :nkv].view(L, B, W.NUM_KV_HEADS, W.HEAD_DIM).to(dev, non_blocking=True)
+            qkv = qkv_h[:nq + 2 * nkv].to(dev, non_blocking=True)
+            q = qkv[:nq].view(L, B, W.NUM_Q_HEADS, W.HEAD_DIM)
+            k = qkv[nq:nq + nkv].view(L, B, W.NUM_KV_HEADS, W.HEAD_DIM)
+            v = qkv[nq + nkv:].view(L, B, W.NUM_KV_HEADS, W.HEAD_DIM)
             out = cb.launch_step(batch, q, k, v)
             out_h[:nq].copy_(out.view(-1), non_blocking=True)
             h2d += (nq + 2 * nkv) * 2

@@ -511,7 +511,7 @@ def paged_gqa_decode_append(q, k_new, v_new, kv_pool, block_tables, seq_lens, ou
 def paged_gqa_decode_append_layers(q, k_new, v_new, kv_pool, block_tables, seq_lens, out,
                                    rope_cos, rope_sin, scale, workspace, max_seq_len=None,
                                    d_err=None, stream=None, q_out=None, early_kv=1,
-                                   host_stage=None, dev_stage=None):
+                                   host_stage=None, dev_stage=None, check=True):
     """A whole decode step: for every layer l, the fused append + decode of
     q[l], k_new[l], v_new[l] over block_tables[l] into out[l] on a bf16 pool
     (paged_gqa_decode_append) or an INT8 pool (paged_gqa_decode_append_int8),
@@ -526,9 +526,33 @@ def paged_gqa_decode_append_layers(q, k_new, v_new, kv_pool, block_tables, seq_l
     dev_stage (uint8 device tensor of at least its size): one copy of the
     first into the second runs on the stream before the launches, e.g. the
     block of pkv_sched_pack_step that block_tables / seq_lens are views of.
+    check=False skips the tensor checks below (the C call still checks sizes,
+    pointers and alignment): for a caller that built the tensors itself and
+    checked their shapes once, as ContinuousBatcher does every step.
     """
     dev = kv_pool.device
     int8 = kv_pool.dtype == torch.uint8
+    if check:
+        _check_layers_args(q, k_new, v_new, kv_pool, block_tables, seq_lens, out, rope_cos,
+                           rope_sin, workspace, d_err, q_out, host_stage, dev_stage, int8, dev)
+    L, S = q.shape[0], q.shape[1]
+    if L == 0:
+        return
+    stage = 0 if host_stage is None else host_stage.numel()
+    stride = block_tables.shape[2]
+    if max_seq_len is None:
+        max_seq_len = PAGE_TOKENS * stride
+    st = _L().paged_gqa_decode_append_layers(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(q_out), _ptr(out), L, S, _ptr(rope_cos),
+        _ptr(rope_sin), rope_cos.shape[0], _ptr(kv_pool), kv_pool.shape[0], int(int8),
+        _ptr(block_tables), block_tables.shape[1] * stride, stride, stride, _ptr(seq_lens),
+        int(max_seq_len), float(scale), _ptr(workspace), workspace.numel(), _ptr(d_err),
+        _stream(stream), int(early_kv), _ptr(host_stage), _ptr(dev_stage), stage)
+    _check(st, "paged_gqa_decode_append_layers")
+
+
+def _check_layers_args(q, k_new, v_new, kv_pool, block_tables, seq_lens, out, rope_cos, rope_sin,
+                       workspace, d_err, q_out, host_stage, dev_stage, int8, dev):
     if int8:
         _need_i8_pool(kv_pool, dev)
     else:
@@ -560,24 +584,12 @@ def paged_gqa_decode_append_layers(q, k_new, v_new, kv_pool, block_tables, seq_l
         _need(d_err, "d_err", torch.int32, dev)
     if (host_stage is None) != (dev_stage is None):
         raise ValueError("host_stage and dev_stage go together")
-    stage = 0
     if host_stage is not None:
         if host_stage.dtype != torch.uint8 or not host_stage.is_contiguous():
             raise TypeError("host_stage must be a contiguous uint8 host tensor")
         _need(dev_stage, "dev_stage", torch.uint8, dev)
-        stage = host_stage.numel()
-        if dev_stage.numel() < stage:
+        if dev_stage.numel() < host_stage.numel():
             raise ValueError("dev_stage is smaller than host_stage")
-    stride = block_tables.shape[2]
-    if max_seq_len is None:
-        max_seq_len = PAGE_TOKENS * stride
-    st = _L().paged_gqa_decode_append_layers(
-        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(q_out), _ptr(out), L, S, _ptr(rope_cos),
-        _ptr(rope_sin), rope_cos.shape[0], _ptr(kv_pool), kv_pool.shape[0], int(int8),
-        _ptr(block_tables), block_tables.shape[1] * stride, stride, stride, _ptr(seq_lens),
-        int(max_seq_len), float(scale), _ptr(workspace), workspace.numel(), _ptr(d_err),
-        _stream(stream), int(early_kv), _ptr(host_stage), _ptr(dev_stage), stage)
-    _check(st, "paged_gqa_decode_append_layers")
 
 
 PREFILL_MMA_SYNC = 2  # comparison arm of paged_gqa_prefill (legacy bf16 mma.sync)

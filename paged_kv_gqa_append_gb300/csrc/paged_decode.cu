@@ -1929,8 +1929,10 @@ __global__ void __launch_bounds__(DynSmem::kThreads, 1)
     __syncwarp();
   }
 
-  if (p.expire_first && blockIdx.x == 0 && warp == 0 && my_meta[0].x >= 0) {
-    // the timeout test: a barrier nothing arrives on, in place of the first unit's
+  if (p.expire_first && blockIdx.x == 0 && warp == 0) {
+    // the timeout test: a barrier nothing arrives on, before the first unit
+    // (whether or not this warp claimed one; the drain below waits only for
+    // the stages it armed)
     __shared__ __align__(8) uint64_t never_bar;
     if (lane == 0) {
       mbar_init(smem_u32(&never_bar), 1);

@@ -78,6 +78,7 @@ class ContinuousBatcher:
         pin = self.dev.type == "cuda"
         self._host_blocks = [torch.empty(nmax, dtype=torch.uint8, pin_memory=pin) for _ in range(2)]
         self._block_done = [None, None]
+        self._block_events = [torch.cuda.Event(), torch.cuda.Event()] if pin else None
         self._turn = 0
         self._dev_block = torch.empty(nmax, dtype=torch.uint8, device=self.dev)
         self.prompt = {}           # request id -> prompt tokens
@@ -180,8 +181,8 @@ class ContinuousBatcher:
 
     def _block_sent(self, batch):
         """Mark (on the stream) the point after which the batch's host block may be reused."""
-        if self.dev.type == "cuda":
-            ev = torch.cuda.Event()
+        if self._block_events is not None:
+            ev = self._block_events[batch.turn]
             ev.record()
             self._block_done[batch.turn] = ev
 
@@ -199,20 +200,28 @@ class ContinuousBatcher:
         for t, h in shapes:
             if tuple(t.shape) != (self.L, B, h, HEAD_DIM):
                 raise ValueError(f"expected [{self.L}, {B}, {h}, {HEAD_DIM}], got {tuple(t.shape)}")
+            if t.dtype != torch.bfloat16 or t.device != self.dev or not t.is_contiguous():
+                raise TypeError("q / k / v must be contiguous bf16 tensors on the pool's device")
         if out is None:
             out = torch.empty((self.L, B, NUM_Q_HEADS, HEAD_DIM), dtype=torch.bfloat16,
                               device=self.dev)
+        elif (tuple(out.shape) != (self.L, B, NUM_Q_HEADS, HEAD_DIM) or out.dtype != torch.bfloat16
+              or out.device != self.dev or not out.is_contiguous()):
+            raise ValueError("out must be a contiguous bf16 [L, B, 32, 64] tensor on the pool's device")
         if B == 0:
             return out
         ms = int(batch.lens_h.max())
         ws = self.workspace
         if self.fused:
             # one C call: the step block's copy, then the L fused launches
-            # (layers >= 1 stage their pages while the previous layer ends)
+            # (layers >= 1 stage their pages while the previous layer ends);
+            # the shapes were checked above and the other tensors are the
+            # batcher's own, so the binding's per-call checks are skipped
             paged_gqa_decode_append_layers(q, k, v, self.pool, batch.tables, batch.lens, out,
                                            self.cos, self.sin, self.scale, ws, max_seq_len=ms,
                                            d_err=self.d_err, early_kv=1,
-                                           host_stage=batch.host_block, dev_stage=batch.dev_block)
+                                           host_stage=batch.host_block, dev_stage=batch.dev_block,
+                                           check=False)
             self._block_sent(batch)
             return out
         batch.dev_block.copy_(batch.host_block, non_blocking=True)

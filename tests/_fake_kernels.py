@@ -135,7 +135,7 @@ def paged_gqa_decode_append_int8(q, k_new, v_new, kv_pool, block_tables, seq_len
 def paged_gqa_decode_append_layers(q, k_new, v_new, kv_pool, block_tables, seq_lens, out,
                                    rope_cos, rope_sin, scale, workspace, max_seq_len=None,
                                    d_err=None, stream=None, q_out=None, early_kv=1,
-                                   host_stage=None, dev_stage=None):
+                                   host_stage=None, dev_stage=None, check=True):
     assert q.dim() == 4 and block_tables.dim() == 3 and block_tables.shape[0] == q.shape[0]
     assert (host_stage is None) == (dev_stage is None) and early_kv in (0, 1)
     if host_stage is not None:       # the step block's copy comes first
