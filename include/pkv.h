@@ -342,9 +342,21 @@ int paged_gqa_decode_append(const void* q, const void* k_new, const void* v_new,
  * finite.  Pages keep the bf16 pool's block tables and 16 tokens; a page of
  * the INT8 pool is 8 blocks of PKV_I8_BLOCK_BYTES, one per KV head:
  *   kv_pool  device bytes [num_pages][8][2176], 17408 bytes/page, 16-byte
- *            aligned, caller-owned; block (page, head) = K codes [16 slots][64]
- *            int8, V codes [16][64] int8, K scales [16] float, V scales [16]
- *            float (little-endian), so one contiguous copy brings a unit.
+ *            aligned, caller-owned; one contiguous copy brings a unit.  The
+ *            block of (page, head), in this library's format:
+ *            - a code c is stored as the byte c + 128 (an all-0x80 block
+ *              holds zero codes);
+ *            - bytes 0..1023, K codes: slot t, dim d at 64 t + d;
+ *            - bytes 1024..2047, V codes by slot pairs: slot t is member
+ *              t % 2 of pair p = t / 2, and dim d of a pair is the byte
+ *              pair at 1024 + 128 p + 16 ((d % 8) ^ (2 (p % 4)))
+ *              + 2 (d / 8) + member;
+ *            - bytes 2048..2175, float scales (little-endian) in groups of
+ *              four: group j = 0..7 at 2048 + 16 j holds the K scales of
+ *              slots j and j + 8, then their V scales.
+ *            (So each shared-memory read of the decode is one
+ *            conflict-free 16-byte load: two K rows, one scale group, and
+ *            eight dims of a slot pair.)
  * ---------------------------------------------------------------------- */
 
 /* kv_append_rope into INT8 pages: the arguments, ordering and error rules of

@@ -25,9 +25,18 @@ Logical arrays (the page geometry of the bf16 pool, one byte per element):
   codes   int8    [num_pages][2 (K, V)][8 heads][16 slots][64 dims]
   scales  float32 [num_pages][2 (K, V)][8 heads][16 slots]
 The pool the library reads and writes holds them as bytes, one 2176-byte
-block per (page, head) -- K codes [16][64], V codes [16][64], K scales [16],
-V scales [16] (little-endian fp32) -- so a page is 8 x 2176 = 17408 bytes
-(``pack_pages`` / ``unpack_pages``).
+block per (page, head), so a page is 8 x 2176 = 17408 bytes (``pack_pages``
+/ ``unpack_pages``).  This byte format is the library's own (the page says
+nothing of storage); it is defined here by ``block_positions``:
+  * a code is stored as the byte code + 128 (1 .. 255 for codes in
+    [-127, 127]);
+  * K codes, bytes 0 .. 1023: slot t, dim d at 64 t + d;
+  * V codes, bytes 1024 .. 2047, by slot pairs: slot t is member t % 2 of
+    pair p = t // 2, and dim d of a pair is the byte pair at
+        1024 + 128 p + 16 ((d % 8) ^ (2 (p % 4))) + 2 (d // 8) + member;
+  * scales, bytes 2048 .. 2175, little-endian fp32 in groups of four:
+    group j = 0..7 at 2048 + 16 j holds the K scales of slots j and j + 8,
+    then their V scales.
 
 fp32 emulation: each division is done in FP64 and rounded once to fp32.  For
 +, -, *, / a binary64 intermediate followed by rounding to binary32 gives the
@@ -187,18 +196,40 @@ def quantize_pool(pool_bits):
     return quantize_rows(bf16.to_f64(pool_bits))
 
 
+def block_positions():
+    """Byte positions inside a (page, head) block, from the rules of the module
+    docstring: (k [16][64], v [16][64], k_scale [16], v_scale [16]) -- the
+    byte of each code, and the first byte of each fp32 scale."""
+    k = np.empty((PAGE_TOKENS, HEAD_DIM), np.int64)
+    v = np.empty((PAGE_TOKENS, HEAD_DIM), np.int64)
+    ks = np.empty(PAGE_TOKENS, np.int64)
+    vs = np.empty(PAGE_TOKENS, np.int64)
+    for t in range(PAGE_TOKENS):
+        pair, member = t // 2, t % 2
+        ks[t] = 2048 + 16 * (t % 8) + 4 * (t // 8)
+        vs[t] = ks[t] + 8
+        for d in range(HEAD_DIM):
+            k[t, d] = 64 * t + d
+            v[t, d] = 1024 + 128 * pair + 16 * ((d % 8) ^ (2 * (pair % 4))) + 2 * (d // 8) + member
+    return k, v, ks, vs
+
+
 def pack_pages(codes, scales) -> np.ndarray:
-    """Logical (codes, scales) -> the pool's bytes, uint8 [N][8][2176]: per
-    (page, head) the K codes, the V codes, the K scales, the V scales."""
+    """Logical (codes, scales) -> the pool's bytes, uint8 [N][8][2176], in the
+    block format of the module docstring."""
     codes = np.asarray(codes, np.int8)
     scales = np.asarray(scales, np.float32)
     N = codes.shape[0]
-    out = np.empty((N, NUM_KV_HEADS, BLOCK_BYTES), np.uint8)
-    for kv in range(2):
-        c = codes[:, kv].reshape(N, NUM_KV_HEADS, PAGE_TOKENS * HEAD_DIM)
-        out[:, :, kv * 1024:(kv + 1) * 1024] = c.view(np.uint8)
-        sc = np.ascontiguousarray(scales[:, kv].astype('<f4'))
-        out[:, :, 2048 + 64 * kv:2048 + 64 * (kv + 1)] = sc.view(np.uint8).reshape(N, NUM_KV_HEADS, 64)
+    kpos, vpos, kspos, vspos = block_positions()
+    out = np.zeros((N, NUM_KV_HEADS, BLOCK_BYTES), np.uint8)
+    biased = (codes.astype(np.int16) + 128).astype(np.uint8)       # code + 128
+    out[:, :, kpos] = biased[:, 0]
+    out[:, :, vpos] = biased[:, 1]
+    for kv, pos in ((0, kspos), (1, vspos)):
+        sb = np.ascontiguousarray(scales[:, kv].astype('<f4')).view(np.uint8).reshape(
+            N, NUM_KV_HEADS, PAGE_TOKENS, 4)
+        for j in range(4):
+            out[:, :, pos + j] = sb[..., j]
     return out
 
 
@@ -206,13 +237,14 @@ def unpack_pages(pool_bytes):
     """The pool's bytes uint8 [N][8][2176] -> logical (codes, scales)."""
     b = np.ascontiguousarray(np.asarray(pool_bytes, np.uint8))
     N = b.shape[0]
+    kpos, vpos, kspos, vspos = block_positions()
     codes = np.empty((N, 2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM), np.int8)
     scales = np.empty((N, 2, NUM_KV_HEADS, PAGE_TOKENS), np.float32)
-    for kv in range(2):
-        codes[:, kv] = b[:, :, kv * 1024:(kv + 1) * 1024].copy().view(np.int8).reshape(
-            N, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM)
-        scales[:, kv] = b[:, :, 2048 + 64 * kv:2048 + 64 * (kv + 1)].copy().view('<f4').reshape(
-            N, NUM_KV_HEADS, PAGE_TOKENS)
+    codes[:, 0] = (b[:, :, kpos].astype(np.int16) - 128).astype(np.int8)
+    codes[:, 1] = (b[:, :, vpos].astype(np.int16) - 128).astype(np.int8)
+    for kv, pos in ((0, kspos), (1, vspos)):
+        sb = np.stack([b[:, :, pos + j] for j in range(4)], axis=-1)  # [N][8][16][4]
+        scales[:, kv] = np.ascontiguousarray(sb).view('<f4')[..., 0]
     return codes, scales
 
 

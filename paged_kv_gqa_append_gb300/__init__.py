@@ -318,9 +318,11 @@ I8_BLOCK_BYTES = 2 * PAGE_TOKENS * HEAD_DIM + 2 * PAGE_TOKENS * 4   # 2176 per (
 
 
 def new_int8_pool(num_pages: int, device) -> torch.Tensor:
-    """A zero-filled INT8 pool: uint8 [num_pages, 8, 2176], per (page, KV head)
-    K codes [16][64], V codes [16][64], K scales [16], V scales [16] (fp32)."""
-    return torch.zeros((num_pages, NUM_KV_HEADS, I8_BLOCK_BYTES), dtype=torch.uint8, device=device)
+    """An empty INT8 pool, uint8 [num_pages, 8, 2176]: every code 0 (stored as
+    the byte 0x80) and every scale 0.  The block format is in pkv.h."""
+    pool = torch.zeros((num_pages, NUM_KV_HEADS, I8_BLOCK_BYTES), dtype=torch.uint8, device=device)
+    pool[:, :, :2 * 16 * 64] = 0x80
+    return pool
 
 
 def _need_i8_pool(kv_pool, dev):

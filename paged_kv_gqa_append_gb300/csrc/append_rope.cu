@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "i8_layout.cuh"
 #include "internal.h"
 #include "pkv.h"
 #include "ptx.cuh"
@@ -102,9 +103,10 @@ __global__ void __launch_bounds__(256) kv_append_rope_kernel(const AppendParams 
 // and of V is quantised on its own: amax = max |x|, scale = amax / 127 and
 // code = round-half-even(x / scale) in [-127, 127], both divisions IEEE fp32;
 // amax == 0 gives scale 0 and zero codes.  A (page, head) is one 2176-byte
-// block of the pool: K codes [16][64], V codes [16][64], K scales [16], V
-// scales [16].  Same grid as the bf16 append: one CTA per token, one warp per
-// KV head, lane i holding dims i and i + 32.
+// block of the pool in the format of i8_layout.cuh (codes as code + 128; K
+// codes row-major; V codes in slot pairs; scales in the decode's lane
+// order).  Same grid as the bf16 append: one CTA per token, one warp per KV
+// head, lane i holding dims i and i + 32.
 // ---------------------------------------------------------------------------
 struct AppendI8Params {
   const uint16_t* k;          // [T][8][64] bf16
@@ -151,8 +153,6 @@ __global__ void __launch_bounds__(256) kv_append_rope_int8_kernel(const AppendI8
   const float c = __ldg(p.cos + (size_t)pos * PKV_ROPE_PAIRS + lane);
   const float sn = __ldg(p.sin + (size_t)pos * PKV_ROPE_PAIRS + lane);
   uint8_t* blk = p.pool + ((size_t)page * PKV_NUM_KV_HEADS + g) * PKV_I8_BLOCK_BYTES;
-  int8_t* kcode = reinterpret_cast<int8_t*>(blk) + slot * 64;
-  int8_t* vcode = reinterpret_cast<int8_t*>(blk) + 1024 + slot * 64;
 
   // K: rotate (bf16 result, as in the bf16 cache), quantise, store
   const uint16_t* kr = p.k + ((size_t)t * PKV_NUM_KV_HEADS + g) * 64;
@@ -161,19 +161,19 @@ __global__ void __launch_bounds__(256) kv_append_rope_int8_kernel(const AppendI8
   int8_t k0, k1;
   const float ks = quantize_pair(__uint_as_float((uint32_t)r0 << 16), __uint_as_float((uint32_t)r1 << 16),
                                  k0, k1);
-  kcode[lane] = k0;
-  kcode[lane + 32] = k1;
+  blk[i8_k_byte(slot, lane)] = i8_code_byte(k0);
+  blk[i8_k_byte(slot, lane + 32)] = i8_code_byte(k1);
 
   // V: quantise the bf16 row
   const uint16_t* vr = p.v + ((size_t)t * PKV_NUM_KV_HEADS + g) * 64;
   int8_t v0, v1;
   const float vs = quantize_pair(__uint_as_float((uint32_t)vr[lane] << 16),
                                  __uint_as_float((uint32_t)vr[lane + 32] << 16), v0, v1);
-  vcode[lane] = v0;
-  vcode[lane + 32] = v1;
+  blk[i8_v_byte(slot, lane)] = i8_code_byte(v0);
+  blk[i8_v_byte(slot, lane + 32)] = i8_code_byte(v1);
   if (lane == 0) {
-    reinterpret_cast<float*>(blk + 2048)[slot] = ks;
-    reinterpret_cast<float*>(blk + 2112)[slot] = vs;
+    *reinterpret_cast<float*>(blk + i8_k_scale_byte(slot)) = ks;
+    *reinterpret_cast<float*>(blk + i8_v_scale_byte(slot)) = vs;
   }
 
   // q: the 4 query heads of this group, rotated as in the bf16 append

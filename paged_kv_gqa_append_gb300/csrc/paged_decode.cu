@@ -38,6 +38,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include "i8_layout.cuh"
 #include "internal.h"
 #include "pkv.h"
 #include "ptx.cuh"
@@ -809,75 +810,68 @@ struct FmaState : Bf16Pages {
 
 // ---------------------------------------------------------------------------
 // INT8 pages (kv_append_rope_int8).  A (page, head) is one contiguous
-// 2176-byte block of the pool -- K codes [16][64], V codes [16][64], K scales
-// [16], V scales [16] -- so one bulk copy per page brings everything a unit
-// needs (a unit is two consecutive pages of a (sequence, head)).
+// 2176-byte block of the pool in the format of i8_layout.cuh, so one bulk
+// copy per page brings everything a unit needs (a unit is two consecutive
+// pages of a (sequence, head)).
 //
-// Codes enter fp16 m16n8k16 MMAs (fp32 accumulation) exactly: with u = code +
-// 128 in a byte, the fp16 with bits 0x64uu is 1024 + u, and subtracting 1152
-// leaves the code (one byte permute makes two such fp16, one f16x2
-// subtraction finishes them).  fp16 operands need ranges kept in check:
+// The page's 16 tokens are the M of the MMAs (m16n8k16, fp16 operands, fp32
+// accumulation) and the group's 4 query heads the N (of 8): S^T = K q'^T and
+// O^T += V^T P'^T, four MMAs each per page, every accumulator a full
+// four-register fragment updated in place.  P' leaves S^T in accumulator
+// layout (lane (g8, c) holds tokens g8 and g8 + 8 of heads 2c and 2c + 1);
+// one movmatrix transpose per 8 x 8 half turns it into the B fragment of
+// P'^T.  Lanes with c >= 2 carry the 4 padding heads (zero rows of q).
+//
+// Codes enter the MMAs as h = 1024 + byte = code + 1152: one byte permute
+// makes two such fp16 (bits 0x64bb) of stored bytes, and the constant is
+// taken out of the results instead of out of every operand.  Every score of
+// head r carries 1152 sum_d q'_rd, so the S accumulators start at minus
+// that; every element of O^T's column r carries 1152 sum_j P'_rj, which one
+// more MMA per page (A = ones) accumulates beside O (rescaled with it), and
+// O - 1152 * that is the result.  The cancellation costs about ten of fp32's
+// 24 bits in the worst case here (2048 near-uniform weights), far below the
+// bf16 output's rounding.  fp16 operands need ranges kept in check:
 //   * q is multiplied by a power of two per segment so that its largest
 //     |value| lies in [2^14, 2^15) (exact: a bf16 value times a power of two
 //     fits fp16's 11 significant bits), and the score scale divided by it;
 //   * the V scale of token j multiplies its probability, and the product is
-//     divided by 2^E, E the exponent of the largest V scale of the page, so
+//     divided by 2^E, E the exponent of the largest V scale of the unit, so
 //     P' = p_j s_j 2^-E < 2 before its rounding to fp16; O is kept in units
-//     of 2^E of the latest page and rescaled with the softmax factor when E
+//     of 2^E of the latest unit and rescaled with the softmax factors when E
 //     changes.
 // Scores: x_j = (q' . code_j) s_K,j scale log2(e) / 2^e_q, online softmax in
-// base 2 as for bf16 pages; the denominator sums the fp32 probabilities.
+// base 2 per head as for bf16 pages; the denominator sums the fp32
+// probabilities.
 //
-// Lane (g8 = lane/4, c = lane%4).  A page's 16 tokens are dealt out as
-// T(c, i) = ((c ^ i) & 1) + 2 (i & 1) + 4 (c >> 1) + 8 (i >> 1), i = 0..3:
-// column j of S tile 0 is token T(j/2, j%2) and of S tile 1 token
-// T(j/2, 2 + j%2), so lane (g8, c) holds the scores -- and the P V
-// A-fragment -- of tokens T(c, 0..3).  The MMA k indices {2c, 2c+1, 2c+8,
-// 2c+9} of step kt are dims 16c + 4kt + {0, 1, 2, 3} (q's dims permuted the
-// same way, which leaves q.k unchanged), so a lane's B fragments of a K row
-// are bytes 16c .. 16c+15 of it.  Column g8 of P V tile nb is dim 8 g8 + nb:
-// a lane reads bytes 8 g8 .. 8 g8 + 7 of the V rows of its four tokens, and
-// its O fragment of tile nb holds dims 16c + nb and 16c + 8 + nb.  Each
-// quarter-warp's 16-byte K loads cover two rows of opposite parity
-// (conflict-free); each half-warp's 8-byte V loads cover four rows, two per
-// 64-byte half of the bank window (two-way).
+// Fragments, lane (g8 = lane / 4, c = lane % 4): in S^T's k step kt the MMA
+// k indices {2c, 2c+1, 2c+8, 2c+9} are dims 16c + 4kt + {0, 1, 2, 3} (q's
+// dims permuted the same way, which leaves q.k unchanged), so the lane's A
+// fragments are bytes 16c .. 16c+15 of K rows g8 and g8 + 8; its B
+// fragments are q' of head g8.  In O^T's m-tile m the rows are dims 16m + g8
+// and 16m + g8 + 8 and the k indices tokens, so the A fragments are dims
+// g8 + 8j of the token pairs (2c, 2c+1) and (2c+8, 2c+9), one 16-byte chunk
+// each.  O^T's fragment of tile m holds dims 16m + g8 (elements 0, 1) and
+// 16m + g8 + 8 (2, 3) of heads 2c (0, 2) and 2c + 1 (1, 3).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int i8_token(int c, int i) {
-  return ((c ^ i) & 1) + 2 * (i & 1) + 4 * (c >> 1) + 8 * (i >> 1);
-}
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
   return v;
 }
-__device__ __forceinline__ uint2 lds64(uint32_t a) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ float lds32f(uint32_t a) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
-  return v;
-}
-// f16x2 (h - 1152, h - 1152): exact for the 1024 + (code + 128) values here.
-__device__ __forceinline__ uint32_t hsub1152(uint32_t h) {
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
-  return r;
-}
-// D(16x8, fp32) += A(16x16, fp16, row) * B(16x8, fp16, col); rows 8..15 of A
-// and C are zero, as in mma_bf16_16816.
-__device__ __forceinline__ void mma_f16_16816(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0,
-                                              uint32_t b1) {
-  float t[4] = {d[0], d[1], 0.f, 0.f};
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+// D += A B (m16n8k16, fp16 operands, fp32 accumulation), all four fragments.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
       "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(t[0]), "+f"(t[1]), "+f"(t[2]), "+f"(t[3])
-      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
-  d[0] = t[0];
-  d[1] = t[1];
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// The transpose of an 8 x 8 matrix of 16-bit values held in the warp's
+// fragment layout (lane l: row l / 4, columns 2 (l % 4) and + 1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
 }
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
@@ -891,8 +885,7 @@ __device__ __forceinline__ float pow2_biased(int k) {
 
 // Rotation of the q words of an INT8-page decode lane at position pos (dims d
 // and d + 32 sit in lanes c and c ^ 2 of a row), and their store to q_out
-// when `write_q`.  Kept out of line: it runs once per segment, and inlined
-// its temporaries would crowd the page loop's registers.
+// when `write_q`.
 __device__ __forceinline__ void rotate_q_i8(const DecodeParams& p, uint32_t (&w)[8], size_t row, int pos,
                                          bool write_q, int lane) {
   const int gq = lane >> 2, c = lane & 3;
@@ -927,12 +920,15 @@ struct MmaI8State {
   static constexpr int kPagesPerUnit = kP;
   static constexpr int kBlock = PKV_I8_BLOCK_BYTES;     // one (page, head): 2176 bytes
   static constexpr int kStageBytes = kBlock * kP;        // a multiple of 16
-  static constexpr int kVOffset = 1024;                  // V codes; K scales at 2048, V scales at 2112
+  static constexpr int kVOffset = 1024;                  // V codes (unused: the block is one piece)
   __host__ __device__ static constexpr int min_blocks(int warps) { return warps >= 16 ? 1 : 16 / warps; }
-  uint32_t qa[4][2];  // q' A-fragments (fp16) per MMA step, dims permuted as above
-  float o[8][2];      // O in units of 2^(ev - 127): tile nb holds dims 16c + nb, 16c + 8 + nb
-  float m, l;         // running max (log2 units) and per-lane partial denominator
+  uint32_t qb[4][2];  // B fragments of q'^T per k step: head g8, dims 16c + 4kt + {0, 1} / {2, 3}
+  float o[4][4];      // O^T + 1152 o1 in units of 2^(ev - 127) (fragment layout above)
+  float o1[4];        // sum of P' of heads 2c, 2c + 1 (twice), same units
+  float m0, m1;       // running max of heads 2c, 2c + 1 (log2 units)
+  float l0, l1;       // their partial denominators over the lane's tokens
   float sl2q;         // scale * log2(e) / (q's power-of-two factor)
+  float nc0, nc1;     // -1152 sum_d q'_d of heads 2c, 2c + 1: the S accumulators' start
   int ev;             // biased exponent of O's unit
 
   // The unit's pages: pid.x, and pid.y when kP == 2 and the sequence has it.
@@ -969,168 +965,195 @@ struct MmaI8State {
     const int eb = min(max((int)(amax >> 23), 15), 267);
     const float f = amax ? pow2_biased(268 - eb) : 1.f;
     sl2q = p.sl2 * (amax ? pow2_biased(eb - 14) : 1.f);
+    float qsum = 0.f;  // of head gq's q' (exact products; the lane's 16 dims, then the row)
 #pragma unroll
     for (int kt = 0; kt < 4; ++kt) {
-      qa[kt][0] = pack_f16x2(bf16lo_to_f32(w[2 * kt]) * f, bf16hi_to_f32(w[2 * kt]) * f);
-      qa[kt][1] = pack_f16x2(bf16lo_to_f32(w[2 * kt + 1]) * f, bf16hi_to_f32(w[2 * kt + 1]) * f);
+      const float a0 = bf16lo_to_f32(w[2 * kt]) * f, a1 = bf16hi_to_f32(w[2 * kt]) * f;
+      const float a2 = bf16lo_to_f32(w[2 * kt + 1]) * f, a3 = bf16hi_to_f32(w[2 * kt + 1]) * f;
+      qb[kt][0] = pack_f16x2(a0, a1);
+      qb[kt][1] = pack_f16x2(a2, a3);
+      qsum += (a0 + a1) + (a2 + a3);
     }
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+    // heads 2c and 2c + 1 sit in lanes 8c and 8c + 4 (zero rows for c >= 2)
+    nc0 = -1152.f * __shfl_sync(0xffffffffu, qsum, 8 * c);
+    nc1 = -1152.f * __shfl_sync(0xffffffffu, qsum, 8 * c + 4);
   }
 
   __device__ __forceinline__ void reset() {
 #pragma unroll
-    for (int n = 0; n < 8; ++n) o[n][0] = o[n][1] = 0.f;
-    m = -INFINITY;
-    l = 0.f;
+    for (int m = 0; m < 4; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
+    o1[0] = o1[1] = o1[2] = o1[3] = 0.f;
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
     ev = 127;
   }
 
   // One unit: kP page blocks at `base`, `valid` tokens (1 .. 16 kP) counted
-  // from the unit's first token.
+  // from the unit's first token.  A missing second page (valid <= 16) is
+  // computed from whatever its buffer holds, all of it masked: codes are
+  // finite whatever their bits, and its scores and V scales are replaced.
   __device__ __forceinline__ void page(uint32_t base, uint32_t, int valid, float, int lane) {
     const int g8 = lane >> 2, c = lane & 3;
-    const bool hasB = kP == 2 && valid > PKV_PAGE_TOKENS;  // warp-uniform
-    int tk[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) tk[i] = i8_token(c, i);
-    // ---- S = q' K^T, per page ----------------------------------------------
-    const int ra = i8_token(g8 >> 1, g8 & 1), rb = i8_token(g8 >> 1, 2 + (g8 & 1));
-    float x[4 * kP], sv[4 * kP];
+    constexpr uint32_t kMagic = 0x64646464u;  // high bytes of the fp16 1024 + byte
+    const uint32_t koff = 64u * g8 + 16u * c;                                 // K row g8 (g8 + 8: +512)
+    const uint32_t voff = 1024u + 128u * c + 16u * (uint32_t)(g8 ^ (2 * c));  // pair c (c + 4: +512)
+    const uint32_t soff = 2048u + 16u * g8;                                   // scales of g8, g8 + 8
+    // ---- S^T = h q'^T (accumulators start at -1152 sum q') and the scores ----
+    float x[kP][4];   // tokens g8 (0, 1) and g8 + 8 (2, 3) of heads 2c (0, 2) and 2c + 1 (1, 3)
+    float sv[kP][2];  // V scales of tokens g8, g8 + 8
 #pragma unroll
     for (int pg = 0; pg < kP; ++pg) {
-      float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
-      if (pg == 0 || hasB) {
-        const uint32_t sK = base + kBlock * pg;
-        const uint4 ka = lds128(sK + ra * 64 + 16 * c), kb = lds128(sK + rb * 64 + 16 * c);
-        const uint32_t kaw[4] = {ka.x, ka.y, ka.z, ka.w}, kbw[4] = {kb.x, kb.y, kb.z, kb.w};
+      const uint32_t blk = base + kBlock * pg;
+      float s[4] = {nc0, nc1, nc0, nc1};
+      const uint4 ka = lds128(blk + koff), kb = lds128(blk + koff + 512u);
+      const uint32_t kaw[4] = {ka.x, ka.y, ka.z, ka.w}, kbw[4] = {kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
-        for (int kt = 0; kt < 4; ++kt) {
-          const uint32_t ua = kaw[kt] ^ 0x80808080u, ub = kbw[kt] ^ 0x80808080u;
-          mma_f16_16816(s0, qa[kt][0], qa[kt][1], hsub1152(__byte_perm(ua, 0x64646464u, 0x7150)),
-                        hsub1152(__byte_perm(ua, 0x64646464u, 0x7352)));
-          mma_f16_16816(s1, qa[kt][0], qa[kt][1], hsub1152(__byte_perm(ub, 0x64646464u, 0x7150)),
-                        hsub1152(__byte_perm(ub, 0x64646464u, 0x7352)));
-        }
-      }
-      const float sraw[4] = {s0[0], s0[1], s1[0], s1[1]};
-      const uint32_t sc = base + kBlock * pg + 2048;  // K scales, then V scales
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        x[4 * pg + i] = sraw[i] * (lds32f(sc + 4 * tk[i]) * sl2q);
-        sv[4 * pg + i] = lds32f(sc + 64 + 4 * tk[i]);
-      }
+      for (int kt = 0; kt < 4; ++kt)
+        mma_f16_16816(s, __byte_perm(kaw[kt], kMagic, 0x4140), __byte_perm(kbw[kt], kMagic, 0x4140),
+                      __byte_perm(kaw[kt], kMagic, 0x4342), __byte_perm(kbw[kt], kMagic, 0x4342),
+                      qb[kt][0], qb[kt][1]);
+      const uint4 sc = lds128(blk + soff);  // K scales of g8, g8 + 8, then their V scales
+      const float fa = __uint_as_float(sc.x) * sl2q, fb = __uint_as_float(sc.y) * sl2q;
+      x[pg][0] = s[0] * fa;
+      x[pg][1] = s[1] * fa;
+      x[pg][2] = s[2] * fb;
+      x[pg][3] = s[3] * fb;
+      sv[pg][0] = __uint_as_float(sc.z);
+      sv[pg][1] = __uint_as_float(sc.w);
     }
     // tokens past the end: no score, and their scales may hold any bits
     if (valid < kP * PKV_PAGE_TOKENS) {
 #pragma unroll
-      for (int i = 0; i < 4 * kP; ++i) {
-        const bool live = (i >> 2) * PKV_PAGE_TOKENS + tk[i & 3] < valid;
-        x[i] = live ? x[i] : -INFINITY;
-        sv[i] = live ? sv[i] : 0.f;
-      }
-    }
-    // ---- online softmax (base 2) over the lane's tokens ---------------------
-    float pm = x[0], vm = sv[0];
+      for (int pg = 0; pg < kP; ++pg)
 #pragma unroll
-    for (int i = 1; i < 4 * kP; ++i) {
-      pm = fmaxf(pm, x[i]);
-      vm = fmaxf(vm, sv[i]);
+        for (int j = 0; j < 2; ++j) {
+          const bool live = pg * PKV_PAGE_TOKENS + g8 + 8 * j < valid;
+          x[pg][2 * j] = live ? x[pg][2 * j] : -INFINITY;
+          x[pg][2 * j + 1] = live ? x[pg][2 * j + 1] : -INFINITY;
+          sv[pg][j] = live ? sv[pg][j] : 0.f;
+        }
     }
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
-    vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 1));
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
-    vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 2));
-    const float mn = fmaxf(m, pm);
+    // ---- online softmax (base 2) per head over the unit's tokens -------------
+    float pm0 = fmaxf(x[0][0], x[0][2]), pm1 = fmaxf(x[0][1], x[0][3]), vm = fmaxf(sv[0][0], sv[0][1]);
+#pragma unroll
+    for (int pg = 1; pg < kP; ++pg) {
+      pm0 = fmaxf(pm0, fmaxf(x[pg][0], x[pg][2]));
+      pm1 = fmaxf(pm1, fmaxf(x[pg][1], x[pg][3]));
+      vm = fmaxf(vm, fmaxf(sv[pg][0], sv[pg][1]));
+    }
+#pragma unroll
+    for (int sh = 4; sh < 32; sh <<= 1) {  // the 8 lanes of this c hold all 16 rows
+      pm0 = fmaxf(pm0, __shfl_xor_sync(0xffffffffu, pm0, sh));
+      pm1 = fmaxf(pm1, __shfl_xor_sync(0xffffffffu, pm1, sh));
+      vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, sh));
+    }
+    const float mn0 = fmaxf(m0, pm0), mn1 = fmaxf(m1, pm1);
     const int evn = vm > 0.f ? (__float_as_int(vm) >> 23) : ev;  // O's unit from this unit on
     // (mn is finite: every unit has a live token; m - mn is -inf on the first unit)
-    const float a_soft = ex2_approx(m - mn);
-    const float alpha = a_soft * pow2_biased(127 + ev - evn);
+    const float as0 = ex2_approx(m0 - mn0), as1 = ex2_approx(m1 - mn1);
+    const float ue = pow2_biased(127 + ev - evn);
+    const float al0 = as0 * ue, al1 = as1 * ue;
     const float vinv = pow2_biased(254 - evn);  // 2^-(evn - 127)
-    float pr[4 * kP];
-    float lsum = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4 * kP; ++i) {
-      pr[i] = ex2_approx(x[i] - mn);
-      lsum += pr[i];
-    }
-    l = l * a_soft + lsum;
-    m = mn;
+    m0 = mn0;
+    m1 = mn1;
     ev = evn;
-    if (__any_sync(0xffffffffu, alpha != 1.f)) {  // most units change neither max nor unit
+    uint32_t pk[kP][2];  // P' (fp16) of tokens g8 + 8j, heads 2c (low) and 2c + 1
+    float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        o[n][0] *= alpha;
-        o[n][1] *= alpha;
+    for (int pg = 0; pg < kP; ++pg)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float p0 = ex2_approx(x[pg][2 * j] - mn0), p1 = ex2_approx(x[pg][2 * j + 1] - mn1);
+        const float wv = sv[pg][j] * vinv;
+        ls0 += p0;
+        ls1 += p1;
+        pk[pg][j] = pack_f16x2(p0 * wv, p1 * wv);
       }
+    l0 = l0 * as0 + ls0;
+    l1 = l1 * as1 + ls1;
+    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {  // most units change neither max nor unit
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        o[m][0] *= al0;
+        o[m][1] *= al1;
+        o[m][2] *= al0;
+        o[m][3] *= al1;
+      }
+      o1[0] *= al0;
+      o1[1] *= al1;
+      o1[2] *= al0;
+      o1[3] *= al1;
     }
-    // ---- O += P' V, per page ---------------------------------------------
+    // ---- O^T += h^T P'^T, per page, and the ones row -------------------------
 #pragma unroll
     for (int pg = 0; pg < kP; ++pg) {
-      if (pg == 1 && !hasB) break;
-      // P'[g8][2c, 2c+1] and P'[g8][2c+8, 2c+9] of this page
-      const uint32_t pa0 = pack_f16x2(pr[4 * pg] * (sv[4 * pg] * vinv), pr[4 * pg + 1] * (sv[4 * pg + 1] * vinv));
-      const uint32_t pa2 = pack_f16x2(pr[4 * pg + 2] * (sv[4 * pg + 2] * vinv), pr[4 * pg + 3] * (sv[4 * pg + 3] * vinv));
-      const uint32_t sV = base + kBlock * pg + kVOffset;
-      uint32_t vw[4][2];
+      const uint32_t b0 = movmatrix_trans(pk[pg][0]), b1 = movmatrix_trans(pk[pg][1]);  // tokens 0-7, 8-15
+      const uint32_t sV = base + kBlock * pg + voff;
+      const uint4 va = lds128(sV), vb = lds128(sV + 512u);  // pairs c and c + 4
+      const uint32_t vaw[4] = {va.x, va.y, va.z, va.w}, vbw[4] = {vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint2 t = lds64(sV + tk[i] * 64 + 8 * g8);
-        vw[i][0] = t.x ^ 0x80808080u;
-        vw[i][1] = t.y ^ 0x80808080u;
-      }
-#pragma unroll
-      for (int w = 0; w < 2; ++w) {
-        // rows (0, 1) and (2, 3) interleaved per dim: [r0.b, r1.b, r0.b', r1.b']
-        const uint32_t t01[2] = {__byte_perm(vw[0][w], vw[1][w], 0x5140), __byte_perm(vw[0][w], vw[1][w], 0x7362)};
-        const uint32_t t23[2] = {__byte_perm(vw[2][w], vw[3][w], 0x5140), __byte_perm(vw[2][w], vw[3][w], 0x7362)};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t sel = (k & 1) ? 0x4342u : 0x4140u;
-          mma_f16_16816(o[4 * w + k], pa0, pa2, hsub1152(__byte_perm(t01[k >> 1], 0x64646464u, sel)),
-                        hsub1152(__byte_perm(t23[k >> 1], 0x64646464u, sel)));
-        }
-      }
+      for (int m = 0; m < 4; ++m)  // word m: dims g8 + 16m and g8 + 16m + 8 of both tokens
+        mma_f16_16816(o[m], __byte_perm(vaw[m], kMagic, 0x4140), __byte_perm(vaw[m], kMagic, 0x4342),
+                      __byte_perm(vbw[m], kMagic, 0x4140), __byte_perm(vbw[m], kMagic, 0x4342), b0, b1);
+      mma_f16_16816(o1, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, b0, b1);  // A = 1
     }
   }
 
-  __device__ __forceinline__ float total_l() const {
-    float lt = l;
-    lt += __shfl_xor_sync(0xffffffffu, lt, 1);
-    lt += __shfl_xor_sync(0xffffffffu, lt, 2);
-    return lt;
+  // The denominators of heads 2c and 2c + 1 (all 16 rows of every page).
+  __device__ __forceinline__ void totals(float& lt0, float& lt1) const {
+    lt0 = l0;
+    lt1 = l1;
+#pragma unroll
+    for (int sh = 4; sh < 32; sh <<= 1) {
+      lt0 += __shfl_xor_sync(0xffffffffu, lt0, sh);
+      lt1 += __shfl_xor_sync(0xffffffffu, lt1, sh);
+    }
   }
 
   __device__ __forceinline__ void write_record(const Record& r, bool bad, int lane) {
-    const int gq = lane >> 2, c = lane & 3;
-    const float lt = total_l();
-    if (gq < 4) {
+    const int g8 = lane >> 2, c = lane & 3;
+    float lt0, lt1;
+    totals(lt0, lt1);
+    if (c < 2) {
       const float u = pow2_biased(ev);  // O's unit
-      float4* dst = reinterpret_cast<float4*>(r.o + gq * 64 + 16 * c);
-      dst[0] = make_float4(o[0][0] * u, o[1][0] * u, o[2][0] * u, o[3][0] * u);
-      dst[1] = make_float4(o[4][0] * u, o[5][0] * u, o[6][0] * u, o[7][0] * u);
-      dst[2] = make_float4(o[0][1] * u, o[1][1] * u, o[2][1] * u, o[3][1] * u);
-      dst[3] = make_float4(o[4][1] * u, o[5][1] * u, o[6][1] * u, o[7][1] * u);
-      if (c == 0) r.ml[gq] = make_float2(m, bad ? -1.f : lt);
+      const float cb0 = 1152.f * o1[0], cb1 = 1152.f * o1[1];  // the codes' offset in O
+      float* r0 = r.o + (2 * c) * 64 + g8;  // head 2c; head 2c + 1 at +64
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        r0[16 * m] = (o[m][0] - cb0) * u;
+        r0[64 + 16 * m] = (o[m][1] - cb1) * u;
+        r0[16 * m + 8] = (o[m][2] - cb0) * u;
+        r0[64 + 16 * m + 8] = (o[m][3] - cb1) * u;
+      }
+      if (g8 == 0) {
+        r.ml[2 * c] = make_float2(m0, bad ? -1.f : lt0);
+        r.ml[2 * c + 1] = make_float2(m1, bad ? -1.f : lt1);
+      }
     }
   }
 
   __device__ __forceinline__ void write_output(const DecodeParams& p, int s, int g, bool bad,
                                                int lane) {
-    const int gq = lane >> 2, c = lane & 3;
-    const float lt = total_l();
-    if (gq < 4) {
-      const bool ok = !bad && lt > 0.f;
+    const int g8 = lane >> 2, c = lane & 3;
+    float lt0, lt1;
+    totals(lt0, lt1);
+    if (c < 2) {
+      const bool ok0 = !bad && lt0 > 0.f, ok1 = !bad && lt1 > 0.f;
       const float u = pow2_biased(ev);
-      float v[2][8];
+      const float cb0 = 1152.f * o1[0], cb1 = 1152.f * o1[1];
+      uint16_t* d0 = p.out + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + 2 * c) * 64 + g8;  // head 2c + 1: +64
 #pragma unroll
-      for (int nb = 0; nb < 8; ++nb) {
-        v[0][nb] = ok ? __fdiv_rn(o[nb][0] * u, lt) : 0.f;
-        v[1][nb] = ok ? __fdiv_rn(o[nb][1] * u, lt) : 0.f;
-      }
-      uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + gq) * 64 + 16 * c);
+      for (int m = 0; m < 4; ++m)
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-        dst[h] = make_uint4(pack_bf16x2(v[h][0], v[h][1]), pack_bf16x2(v[h][2], v[h][3]),
-                            pack_bf16x2(v[h][4], v[h][5]), pack_bf16x2(v[h][6], v[h][7]));
+        for (int j = 0; j < 2; ++j) {
+          const float v0 = ok0 ? __fdiv_rn((o[m][2 * j] - cb0) * u, lt0) : 0.f;
+          const float v1 = ok1 ? __fdiv_rn((o[m][2 * j + 1] - cb1) * u, lt1) : 0.f;
+          const uint32_t b = pack_bf16x2(v0, v1);
+          d0[16 * m + 8 * j] = (uint16_t)(b & 0xFFFFu);
+          d0[64 + 16 * m + 8 * j] = (uint16_t)(b >> 16);
+        }
     }
   }
 };
@@ -1195,9 +1218,9 @@ struct NewToken {
 template <int kP>
 struct NewTokenI8 {
   // Nothing is held in registers, which the page loop needs: the token goes
-  // to the warp's area in shared memory, per lane the codes (K dims lane,
-  // lane + 32, V dims lane, lane + 32, one byte each), then the K scale, then
-  // the V scale.
+  // to the warp's area in shared memory, per lane the stored code bytes (K
+  // dims lane, lane + 32, V dims lane, lane + 32), then the K scale, then the
+  // V scale.
 
   __device__ __forceinline__ void load(const DecodeParams& p, int s, int g, int pos, int lane,
                                     uint32_t area) {
@@ -1212,8 +1235,8 @@ struct NewTokenI8 {
                                    __uint_as_float((uint32_t)r1 << 16), k0, k1);
     const float vs = quantize_pair(__uint_as_float((uint32_t)__ldg(vr + lane) << 16),
                                    __uint_as_float((uint32_t)__ldg(vr + lane + 32) << 16), v0, v1);
-    const uint32_t codes = (uint32_t)(uint8_t)k0 | ((uint32_t)(uint8_t)k1 << 8) |
-                           ((uint32_t)(uint8_t)v0 << 16) | ((uint32_t)(uint8_t)v1 << 24);
+    const uint32_t codes = (uint32_t)i8_code_byte(k0) | ((uint32_t)i8_code_byte(k1) << 8) |
+                           ((uint32_t)i8_code_byte(v0) << 16) | ((uint32_t)i8_code_byte(v1) << 24);
     asm volatile("st.shared.u32 [%0], %1;" ::"r"(area + 4u * lane), "r"(codes) : "memory");
     asm volatile("st.shared.f32 [%0], %1;" ::"r"(area + 128u + 4u * lane), "f"(ks) : "memory");
     asm volatile("st.shared.f32 [%0], %1;" ::"r"(area + 256u + 4u * lane), "f"(vs) : "memory");
@@ -1228,7 +1251,8 @@ struct NewTokenI8 {
     const int page = pg == 0 ? pid : __ldg(p.block_tables + (size_t)seq * p.bt_stride + lp);
     const uint32_t blk = base + (uint32_t)(PKV_I8_BLOCK_BYTES * pg);
     uint8_t* gblk = p.pool_i8 + ((size_t)page * PKV_NUM_KV_HEADS + g) * PKV_I8_BLOCK_BYTES;
-    const uint32_t rk = (uint32_t)slot * 64, rv = 1024u + (uint32_t)slot * 64;
+    const uint32_t k0o = i8_k_byte(slot, lane), k1o = i8_k_byte(slot, lane + 32);
+    const uint32_t v0o = i8_v_byte(slot, lane), v1o = i8_v_byte(slot, lane + 32);
     uint32_t codes;
     float ks, vs;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(codes) : "r"(area + 4u * lane) : "memory");
@@ -1236,19 +1260,20 @@ struct NewTokenI8 {
     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(vs) : "r"(area + 256u + 4u * lane) : "memory");
     const uint16_t k0 = codes & 0xFFu, k1 = (codes >> 8) & 0xFFu, v0 = (codes >> 16) & 0xFFu,
                    v1 = codes >> 24;
-    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + rk + lane), "h"(k0) : "memory");
-    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + rk + lane + 32), "h"(k1) : "memory");
-    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + rv + lane), "h"(v0) : "memory");
-    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + rv + lane + 32), "h"(v1) : "memory");
-    gblk[rk + lane] = (uint8_t)k0;
-    gblk[rk + lane + 32] = (uint8_t)k1;
-    gblk[rv + lane] = (uint8_t)v0;
-    gblk[rv + lane + 32] = (uint8_t)v1;
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + k0o), "h"(k0) : "memory");
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + k1o), "h"(k1) : "memory");
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + v0o), "h"(v0) : "memory");
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + v1o), "h"(v1) : "memory");
+    gblk[k0o] = (uint8_t)k0;
+    gblk[k1o] = (uint8_t)k1;
+    gblk[v0o] = (uint8_t)v0;
+    gblk[v1o] = (uint8_t)v1;
     if (lane == 0) {
-      asm volatile("st.shared.f32 [%0], %1;" ::"r"(blk + 2048u + 4u * slot), "f"(ks) : "memory");
-      asm volatile("st.shared.f32 [%0], %1;" ::"r"(blk + 2112u + 4u * slot), "f"(vs) : "memory");
-      reinterpret_cast<float*>(gblk + 2048)[slot] = ks;
-      reinterpret_cast<float*>(gblk + 2112)[slot] = vs;
+      const uint32_t kso = i8_k_scale_byte(slot), vso = i8_v_scale_byte(slot);
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(blk + kso), "f"(ks) : "memory");
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(blk + vso), "f"(vs) : "memory");
+      *reinterpret_cast<float*>(gblk + kso) = ks;
+      *reinterpret_cast<float*>(gblk + vso) = vs;
     }
   }
 };

@@ -278,6 +278,10 @@ def test_close_to_the_bf16_cache():
 # ------------------------------------------------------------ byte layout ---
 
 def test_pack_pages_layout_by_hand():
+    """Positions worked out by hand from the block format's rules: a code is
+    the byte code + 128; slot 15 is member 1 of pair 7, whose chunk for dims
+    7, 15, .., 63 is 7 ^ 6 = 1, dim 63 being its 8th; the V scale of slot 4 is
+    the third word of group 4; the K scale of slot 0 the first of group 0."""
     codes, scales = I.new_pools(3)
     codes[2, 0, 5, 7, 9] = -3          # K code: page 2, head 5, slot 7, dim 9
     codes[1, 1, 0, 15, 63] = 127       # V code: page 1, head 0, slot 15, dim 63
@@ -285,11 +289,27 @@ def test_pack_pages_layout_by_hand():
     scales[0, 0, 7, 0] = -2.0          # K scale: page 0, head 7, slot 0
     b = I.pack_pages(codes, scales)
     assert b.shape == (3, 8, 2176) and I.BLOCK_BYTES == 2176
-    assert b[2, 5, 7 * 64 + 9] == 256 - 3
-    assert b[1, 0, 1024 + 15 * 64 + 63] == 127
-    assert bytes(b[2, 5, 2112 + 16:2112 + 20]) == np.float32(0.5).tobytes()
+    assert b[2, 5, 7 * 64 + 9] == 125
+    assert b[1, 0, 1024 + 128 * 7 + 16 * 1 + 2 * 7 + 1] == 255
+    assert bytes(b[2, 5, 2048 + 16 * 4 + 8:2048 + 16 * 4 + 12]) == np.float32(0.5).tobytes()
     assert bytes(b[0, 7, 2048:2052]) == np.float32(-2.0).tobytes()
-    assert np.count_nonzero(b) == 4     # 0.5 = 0x3F000000 and -2.0 = 0xC0000000: one nonzero byte each
+    codes_region = b[:, :, :2048].copy()
+    codes_region[2, 5, 7 * 64 + 9] = 128
+    codes_region[1, 0, 1024 + 128 * 7 + 16 * 1 + 2 * 7 + 1] = 128
+    assert np.all(codes_region == 128)                 # every other code is 0
+    assert np.count_nonzero(b[:, :, 2048:]) == 2       # 0.5 = 0x3F000000, -2.0 = 0xC0000000
+
+
+def test_block_positions_cover_the_block_once():
+    k, v, ks, vs = I.block_positions()
+    pos = np.concatenate([k.ravel(), v.ravel()] + [ks + j for j in range(4)] + [vs + j for j in range(4)])
+    assert np.array_equal(np.sort(pos), np.arange(I.BLOCK_BYTES))
+    # the pair of a V byte pair: the two slots of a pair share every dim's 2 bytes
+    for d in (0, 9, 63):
+        pairs = {}
+        for t in range(16):
+            pairs.setdefault(int(v[t, d]) // 2, []).append(t)
+        assert sorted(len(x) for x in pairs.values()) == [2] * 8
 
 
 def test_pack_unpack_round_trip():

@@ -163,14 +163,17 @@ I8_BLOCK_BYTES = 2 * PAGE_TOKENS * HEAD_DIM + 2 * PAGE_TOKENS * 4   # 2176
 
 def fill_pool_int8(case: DecodeCase, device="cpu", chunk_pages: int = 8192) -> torch.Tensor:
     """An INT8 pool for the same geometry: uint8 [N][8][2176], per (page, KV
-    head) K codes [16][64], V codes [16][64], K scales [16], V scales [16].
+    head) 1024 K code bytes, 1024 V code bytes, 16 K scales, 16 V scales
+    (the block format of include/pkv.h).
 
-    Codes are N(0, 42^2) samples rounded and clipped to [-127, 127] and
-    scales uniform on [0.015, 0.025) -- about max|x| / 127 for rows of 64
-    N(0,1) values, so that code * scale is close to N(0,1) -- drawn in chunks
-    from one generator seeded with the case seed.  The case's outlier
-    fraction of key rows (page, head, slot) get 8x their scale: the INT8
-    image of a key row scaled by 8.
+    Codes are N(0, 42^2) samples rounded and clipped to [-127, 127], stored as
+    code + 128, and scales uniform on [0.015, 0.025) -- about max|x| / 127 for
+    rows of 64 N(0,1) values, so that code * scale is close to N(0,1) -- drawn
+    in chunks from one generator seeded with the case seed.  Every code and
+    every scale is drawn on its own, so the bytes are filled in storage order
+    (which slot and dim a byte stands for does not change the law).  The
+    case's outlier fraction of key scales get 8x their value: the INT8 image
+    of a key row scaled by 8.
     """
     gen = torch.Generator(device=device).manual_seed(case.seed + 5000)
     N = case.num_pages
@@ -188,13 +191,21 @@ def fill_pool_int8(case: DecodeCase, device="cpu", chunk_pages: int = 8192) -> t
         p1 = min(N, p0 + chunk_pages)
         g = torch.randn((p1 - p0, 2, NUM_KV_HEADS, PAGE_TOKENS * HEAD_DIM), generator=gen,
                         device=device)
-        codes = (g * 42.0).round().clamp(-127, 127).to(torch.int8).view(torch.uint8)
+        codes = ((g * 42.0).round().clamp(-127, 127) + 128).to(torch.uint8)       # code + 128
         pool[p0:p1, :, 0:1024] = codes[:, 0]
         pool[p0:p1, :, 1024:2048] = codes[:, 1]
         sc = scales[p0:p1].contiguous().view(torch.uint8)          # [n][2][8][64] bytes
         pool[p0:p1, :, 2048:2112] = sc[:, 0]
         pool[p0:p1, :, 2112:2176] = sc[:, 1]
     return pool
+
+
+def _i8_scale_words(t: int) -> tuple:
+    """Word indices (of a block's 544) of slot t's K and V scales, in the block
+    format of include/pkv.h: group t % 8 of four words at word 512 + 4 (t % 8)
+    holds the K scales of slots t % 8 and t % 8 + 8, then their V scales."""
+    k = 512 + 4 * (t % 8) + t // 8
+    return k, k + 2
 
 
 def garbage_fill_unused_int8(pool: torch.Tensor, case: DecodeCase, layer: int) -> None:
@@ -206,8 +217,10 @@ def garbage_fill_unused_int8(pool: torch.Tensor, case: DecodeCase, layer: int) -
             continue
         page = int(case.block_tables[layer, s, n // PAGE_TOKENS])
         words = pool[page].view(torch.int32)                      # [8][544]
-        words[:, 512 + n % PAGE_TOKENS:512 + PAGE_TOKENS] = 0x7FC00000   # K scales: NaN
-        words[:, 528 + n % PAGE_TOKENS:528 + PAGE_TOKENS] = 0x7F800000   # V scales: +Inf
+        for t in range(n % PAGE_TOKENS, PAGE_TOKENS):
+            kw, vw = _i8_scale_words(t)
+            words[:, kw] = 0x7FC00000                             # K scale: NaN
+            words[:, vw] = 0x7F800000                             # V scale: +Inf
 
 
 def fill_queries(case: DecodeCase, device="cpu") -> torch.Tensor:
