@@ -726,7 +726,7 @@ def run_int8_line(args, world, rank, local):
     kv_bytes_layer = int(case.seq_lens.sum()) * W.NUM_KV_HEADS * INT8_ROW_BYTES
     step = pkv.Int8DecodeStep(pool, bt, lens, pos, k_new, v_new, q_raw, out, cos, sin,
                               case.scale, max_seq_len=case.max_seq_len,
-                              fused=False if args.unfused else None)   # None: by batch size
+                              fused=False if args.unfused else None)   # None: the fused kernel
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
         step.run()

@@ -870,11 +870,9 @@ class Int8DecodeStep:
         paged_gqa_decode_append_int8(q[l], k[l], v[l], kv_pool, block_tables[l],
                                      seq_lens, out[l], cos, sin, q_out=q_rot[l])
     which places token s at seq_lens[s] - 1 (positions unused).  The default
-    (fused=None) takes the faster form for the batch: fused up to
-    FUSED_INT8_MAX_BATCH sequences, the two kernels above it (on GB300 at 2048
-    tokens a sequence the fused kernel, at the 128-register cap, wins at 32
-    sequences, 26.3 vs 29.4 us/layer, and loses at 128, 72.8 vs 71.0, and at
-    256, 133.6 vs 122.4).  With
+    (fused=None) is the fused form, the faster one at every batch measured (on
+    GB300 at 2048 tokens a sequence: 32 sequences 19.1 vs 24.4 us/layer, 256
+    sequences 100.2 vs 106.1).  With
     overlap_layers (the default) layer l >= 1 reads its tables and stages its
     first pages before layer l - 1's kernel has finished, which requires the
     layers' block tables to name disjoint pages.  Tensors are bound at
@@ -886,13 +884,11 @@ class Int8DecodeStep:
         k, v [L, S, 8, 64] bf16;  q, out [L, S, 32, 64] bf16
     """
 
-    FUSED_INT8_MAX_BATCH = 80
-
     def __init__(self, kv_pool, block_tables, seq_lens, positions, k, v, q, out, rope_cos,
                  rope_sin, scale, max_seq_len=None, workspace=None, d_err=None, q_rot=None,
                  use_graph=True, stream=None, fused=None, overlap_layers=True):
         self.L, self.S = block_tables.shape[0], block_tables.shape[1]
-        self.fused = (self.S <= self.FUSED_INT8_MAX_BATCH) if fused is None else bool(fused)
+        self.fused = True if fused is None else bool(fused)
         self.overlap = bool(overlap_layers)
         self.t = dict(pool=kv_pool, bt=block_tables, lens=seq_lens, pos=positions,
                       k=k, v=v, q=q, out=out, cos=rope_cos, sin=rope_sin)

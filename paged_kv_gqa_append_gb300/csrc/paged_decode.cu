@@ -866,13 +866,6 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-// The transpose of an 8 x 8 matrix of 16-bit values held in the warp's
-// fragment layout (lane l: row l / 4, columns 2 (l % 4) and + 1).
-__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
-  uint32_t r;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
-  return r;
-}
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -2351,13 +2344,13 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   // bound (19 .. 38 sequences on a 152-SM GB300): 8-warp CTAs, two to an SM,
   // one segment each -- no segment is split between CTAs, and the next
   // launch's CTAs find free slots while this one's last CTAs finish (batch
-  // 32 x 2048 fused step: 26.8 -> 26.1 us/layer).
+  // 32 x 2048 fused step: 26.8 -> 26.1 us/layer; on INT8 pages 20.6 -> 19.1).
   const long long pages_hint = max_seq_len > 0 ? (max_seq_len + 15) / 16 : 0;
   const int sms_hint = [&] {
     int d = 0;
     return cudaGetDevice(&d) == cudaSuccess ? sm_count(d) : 0;
   }();
-  const bool seg_pairs = !int8 && !tiny && compute == PKV_COMPUTE_TENSOR && sms_hint > 0 &&
+  const bool seg_pairs = !tiny && compute == PKV_COMPUTE_TENSOR && sms_hint > 0 &&
                          !(opts && (opts->warps_per_cta > 0 || opts->stages > 0 ||
                                     opts->ctas_per_sm > 0 || opts->min_units_per_warp > 0 ||
                                     opts->combine == 1)) &&
@@ -2373,7 +2366,7 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   const int cfg8 = warps * 100 + ((opts && opts->stages > 0) ? opts->stages : 2);
   if (opts && (opts->schedule < 0 || opts->schedule > 2)) return PKV_ERR_INVALID_ARGUMENT;
   if (int8 && (compute != PKV_COMPUTE_TENSOR || (opts && (opts->schedule == 1 || opts->combine == 1)) ||
-               (cfg8 != 1604 && cfg8 != 1602 && cfg8 != 804) || (app && cfg8 != 1602)))
+               (cfg8 != 1604 && cfg8 != 1602 && cfg8 != 804 && cfg8 != 802) || (app && cfg8 != 1602 && cfg8 != 802)))
     return PKV_ERR_INVALID_ARGUMENT;
   if (!int8 && compute == PKV_COMPUTE_TENSOR && cfg != 1602 && cfg != 1603 && cfg != 802 &&
       cfg != 804 && cfg != 402 && cfg != 404)
@@ -2431,10 +2424,12 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int ms = max_seq_len;
   if (int8) {  // stages 2: two pages per stage; stages 4: one page per stage
-    if (app) return launch_decode<MmaI8State<2>, 16, 2, true>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
+    if (app) return cfg8 == 802 ? launch_decode<MmaI8State<2>, 8, 2, true>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st, seg_pairs)
+                                : launch_decode<MmaI8State<2>, 16, 2, true>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
     switch (cfg8) {
       case 1604: return launch_decode<MmaI8State<1>, 16, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
       case 804: return launch_decode<MmaI8State<1>, 8, 4>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
+      case 802: return launch_decode<MmaI8State<2>, 8, 2>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st, seg_pairs);
       default: return launch_decode<MmaI8State<2>, 16, 2>(prm, map, dev, sms, ms, min_units, ctas_per_sm, st);
     }
   }

@@ -132,6 +132,14 @@ __device__ __forceinline__ void mma_bf16_16816_full(float (&d)[4], uint32_t a0, 
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The transpose of an 8 x 8 matrix of 16-bit values held in the warp's
+// fragment layout (lane l: row l / 4, columns 2 (l % 4) and + 1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+
 // ---- bf16 helpers ----------------------------------------------------------
 // two fp32 -> packed bf16x2 (round to nearest even); `lo` goes to bits 0..15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
