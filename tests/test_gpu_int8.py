@@ -413,7 +413,8 @@ def test_int8_fused_full_size_batch32_sampled(lib, cuda_device, tables):
         ids = case.block_tables[l, s][case.block_tables[l, s] >= 0]
         pre[(l, s)] = (ids,) + OI.unpack_pages(pool[torch.from_numpy(ids).to(dev).long()].cpu().numpy())
     step = lib.Int8DecodeStep(pool, bt_all, lens, pos, k_new, v_new, q_raw, out, cos_d, sin_d,
-                              case.scale, max_seq_len=case.max_seq_len, use_graph=False)
+                              case.scale, max_seq_len=case.max_seq_len, use_graph=False,
+                              q_rot=torch.empty_like(q_raw))
     assert step.error() == 0
     for (l, s) in samples:
         ids, c_pages, s_pages = pre[(l, s)]
@@ -449,11 +450,21 @@ def test_int8_step_graph_matches_eager_and_oracle(lib, cuda_device, tables, fuse
         pool = pool0.clone()
         out = torch.empty_like(q)
         step = lib.Int8DecodeStep(pool, bt, lens, pos, k, v, q, out, cos_d, sin_d, case.scale,
-                                  max_seq_len=300, use_graph=use_graph, fused=fused)
+                                  max_seq_len=300, use_graph=use_graph, fused=fused,
+                                  q_rot=torch.empty_like(q))
         step.run()
         assert step.error() == 0
         outs.append((bits(out), pool.cpu().numpy(), bits(step.q_rot)))
     assert all(np.array_equal(a, b) for a, b in zip(outs[0], outs[1]))
+    # without a q_rot buffer the fused step keeps no rotated queries; the rest is the same
+    pool = pool0.clone()
+    out = torch.empty_like(q)
+    step = lib.Int8DecodeStep(pool, bt, lens, pos, k, v, q, out, cos_d, sin_d, case.scale,
+                              max_seq_len=300, fused=fused)
+    assert (step.q_rot is None) == bool(fused)
+    step.run()
+    assert step.error() == 0
+    assert np.array_equal(bits(out), outs[1][0]) and np.array_equal(pool.cpu().numpy(), outs[1][1])
     out_b, pool_b, qrot_b = outs[1]
     codes, scales = OI.unpack_pages(pool0.cpu().numpy())
     for l in range(case.num_layers):

@@ -365,11 +365,21 @@ def test_decode_step_graph_matches_eager_and_oracle(lib, cuda_device, tables, fu
         pool = pool0.clone()
         out = torch.empty_like(q)
         step = lib.DecodeStep(pool, bt, lens, pos, k, v, q, out, cos_d, sin_d, case.scale,
-                              max_seq_len=300, use_graph=use_graph, fused=fused)
+                              max_seq_len=300, use_graph=use_graph, fused=fused,
+                              q_rot=torch.empty_like(q))
         step.run()
         assert step.error() == 0
         outs.append((bits(out), bits(pool), bits(step.q_rot)))
     assert all(np.array_equal(a, b) for a, b in zip(outs[0], outs[1]))
+    # without a q_rot buffer the fused step keeps no rotated queries; the rest is the same
+    pool = pool0.clone()
+    out = torch.empty_like(q)
+    step = lib.DecodeStep(pool, bt, lens, pos, k, v, q, out, cos_d, sin_d, case.scale,
+                          max_seq_len=300, fused=fused)
+    assert (step.q_rot is None) == bool(fused)
+    step.run()
+    assert step.error() == 0
+    assert np.array_equal(bits(out), outs[1][0]) and np.array_equal(bits(pool), outs[1][1])
     out_b, pool_b, qrot_b = outs[1]
     pool_in = bits(pool0)
     for l in range(case.num_layers):
