@@ -359,6 +359,36 @@ int paged_gqa_decode_append(const void* q, const void* k_new, const void* v_new,
  *            eight dims of a slot pair.)
  * ---------------------------------------------------------------------- */
 
+/* kv_append_rope_layers: the same T tokens appended into each of num_layers
+ * layers -- a newly admitted request's prompt, whose pages are written layer
+ * by layer ("Gestion de la KV cache et strategies de batching", samir-vllm
+ * article) -- in one host call: for layer l, kv_append_rope (int8 = 0; bf16
+ * pool) or kv_append_rope_int8 (int8 = 1; INT8 pool) of k[l], v[l] with the
+ * tables at block_tables + l * bt_layer_stride, no q rotation.
+ *   k, v       arrays (host memory, num_layers entries) of pointers to
+ *              [T][8][64] bf16 rows: device memory with src_host = 0; host
+ *              memory with src_host = 1, copied first into `stage` by
+ *              cudaMemcpyAsync on `stream` (pinned memory for an
+ *              asynchronous copy; other host memory works, synchronously).
+ *              The host rows must stay unchanged until those copies have run.
+ *   stage      with src_host = 1: caller-owned device memory of at least
+ *              2 * T * 1024 bytes, 16-byte aligned, reused by every layer in
+ *              stream order; unused with src_host = 0.
+ *   positions, token_seq, T, num_seqs, bt_row_stride, max_blocks, kv_pool,
+ *   num_pages, rope_cos, rope_sin, max_pos, d_err, stream: as for
+ *   kv_append_rope (every layer uses the same positions and token_seq).
+ * Errors: the host checks of kv_append_rope for each layer, and
+ * PKV_ERR_INVALID_ARGUMENT for a null array entry, num_layers < 0,
+ * bt_layer_stride < num_seqs * bt_row_stride, or a missing or short stage;
+ * a layer that fails returns at once, the layers before it stay enqueued. */
+int kv_append_rope_layers(const void* const* k, const void* const* v, int num_layers, int src_host,
+                          void* stage, size_t stage_bytes, const int32_t* positions,
+                          const int32_t* token_seq, int T, const int32_t* block_tables,
+                          long long bt_layer_stride, int num_seqs, int bt_row_stride,
+                          int max_blocks, void* kv_pool, int num_pages, int int8,
+                          const float* rope_cos, const float* rope_sin, int max_pos, int* d_err,
+                          void* stream);
+
 /* kv_append_rope into INT8 pages: the arguments, ordering and error rules of
  * kv_append_rope, with kv_pool the INT8 pool.  The rotated q (when q_in is
  * given) stays bf16.  k, v and kv_pool must be 16-byte aligned, q_in/q_out

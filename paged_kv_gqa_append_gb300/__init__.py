@@ -81,6 +81,8 @@ _SIGS = {
     "paged_gqa_decode_noalloc": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _p]),
     "kv_append_rope_int8": (_i, [_p, _p, _p, _p, _i, _p, _i, _i, _i, _p, _i, _p, _p, _i, _p, _p, _p,
                                  _p]),
+    "kv_append_rope_layers": (_i, [_p, _p, _i, _i, _p, _sz, _p, _p, _i, _p, ctypes.c_longlong, _i,
+                                   _i, _i, _p, _i, _i, _p, _p, _i, _p, _p]),
     "paged_gqa_decode_int8": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p, _p]),
     "paged_gqa_decode_int8_ex": (_i, [_p, _p, _i, _p, _i, _i, _p, _i, _i, _p, _f, _p, _sz, _p, _p,
                                       ctypes.POINTER(DecodeOpts)]),
@@ -329,6 +331,67 @@ def _need_i8_pool(kv_pool, dev):
     _need(kv_pool, "kv_pool", torch.uint8, dev, (NUM_KV_HEADS, I8_BLOCK_BYTES))
     if kv_pool.dim() != 3:
         raise ValueError("the INT8 pool must be [num_pages, 8, 2176] uint8")
+
+
+def kv_append_rope_layers(k, v, positions, block_tables, kv_pool, rope_cos, rope_sin,
+                          token_seq=None, stage=None, d_err=None, max_blocks=None, stream=None):
+    """The same T tokens appended into every layer in one native call (a new
+    request's prompt).  k, v: sequences of L tensors [T, 8, 64] bf16, all on
+    the pool's device, or all in host memory (pinned for an asynchronous
+    copy; each layer's rows then pass through `stage`, a device uint8 tensor
+    of at least 2 * T * 1024 bytes).  block_tables: [L, num_seqs, >= max_blocks]
+    int32 with unit stride in its last dimension (any layer and row strides,
+    e.g. the one-row view of a request in a larger table).  kv_pool: a bf16
+    pool or an INT8 pool (new_int8_pool).  No q rotation."""
+    dev = kv_pool.device
+    int8 = kv_pool.dtype == torch.uint8
+    if int8:
+        _need_i8_pool(kv_pool, dev)
+    else:
+        _need(kv_pool, "kv_pool", torch.bfloat16, dev, (2, NUM_KV_HEADS, PAGE_TOKENS, HEAD_DIM))
+    L = len(k)
+    if len(v) != L:
+        raise ValueError("k and v must hold one tensor per layer each")
+    if L == 0:
+        return
+    src_host = k[0].device.type == "cpu"
+    where = torch.device("cpu") if src_host else dev
+    T = k[0].numel() // (NUM_KV_HEADS * HEAD_DIM)
+    for i, t in enumerate(list(k) + list(v)):
+        _need(t, f"{'kv'[i // L]}[{i % L}]", torch.bfloat16, where, (NUM_KV_HEADS, HEAD_DIM))
+        if t.numel() != T * NUM_KV_HEADS * HEAD_DIM:
+            raise ValueError("every layer's k and v must be [T, 8, 64]")
+    _need(positions, "positions", torch.int32, dev)
+    if positions.numel() != T:
+        raise ValueError("positions must have one entry per token")
+    if token_seq is not None:
+        _need(token_seq, "token_seq", torch.int32, dev)
+        if token_seq.numel() != T:
+            raise ValueError("token_seq must have one entry per token")
+    if (not isinstance(block_tables, torch.Tensor) or block_tables.dtype != torch.int32 or
+            block_tables.device != dev or block_tables.dim() != 3 or block_tables.stride(2) != 1):
+        raise ValueError("block_tables must be an int32 [L, num_seqs, row] tensor on the pool's "
+                         "device with unit stride in its last dimension")
+    if block_tables.shape[0] < L:
+        raise ValueError("block_tables must hold one table per layer")
+    _need(rope_cos, "rope_cos", torch.float32, dev, (ROPE_PAIRS,))
+    _need(rope_sin, "rope_sin", torch.float32, dev, (ROPE_PAIRS,))
+    if src_host:
+        _need(stage, "stage", torch.uint8, dev)
+        if stage.numel() < 2 * T * NUM_KV_HEADS * HEAD_DIM * 2:
+            raise ValueError("stage must hold 2 * T * 1024 bytes")
+    if d_err is not None:
+        _need(d_err, "d_err", torch.int32, dev)
+    S, mb0 = block_tables.shape[1], block_tables.shape[2]
+    ks = (ctypes.c_void_p * L)(*[t.data_ptr() for t in k])
+    vs = (ctypes.c_void_p * L)(*[t.data_ptr() for t in v])
+    st = _L().kv_append_rope_layers(
+        ks, vs, L, int(src_host), _ptr(stage) if src_host else None,
+        stage.numel() if src_host else 0, _ptr(positions), _ptr(token_seq), T,
+        _ptr(block_tables), block_tables.stride(0), S, block_tables.stride(1),
+        mb0 if max_blocks is None else max_blocks, _ptr(kv_pool), kv_pool.shape[0], int(int8),
+        _ptr(rope_cos), _ptr(rope_sin), rope_cos.shape[0], _ptr(d_err), _stream(stream))
+    _check(st, "kv_append_rope_layers")
 
 
 def kv_append_rope_int8(k, v, positions, block_tables, kv_pool, rope_cos, rope_sin,

@@ -301,3 +301,67 @@ extern "C" int kv_append_rope_int8(const void* k, const void* v, const int32_t* 
   return cuda_status(cudaLaunchKernelEx(&cfg, kv_append_rope_int8_kernel, p),
                      "cudaLaunchKernelEx(append int8)");
 }
+
+// The same T tokens appended into every layer of a request: the prompt of a
+// newly admitted sequence ("Gestion de la KV cache et strategies de
+// batching": a request's pages are written layer by layer as it enters the
+// batch).  One host call for the L copies and L launches a serving loop
+// would otherwise make one by one.
+extern "C" int kv_append_rope_layers(const void* const* k, const void* const* v, int num_layers,
+                                     int src_host, void* stage, size_t stage_bytes,
+                                     const int32_t* positions, const int32_t* token_seq, int T,
+                                     const int32_t* block_tables, long long bt_layer_stride,
+                                     int num_seqs, int bt_row_stride, int max_blocks,
+                                     void* kv_pool, int num_pages, int int8, const float* rope_cos,
+                                     const float* rope_sin, int max_pos, int* d_err, void* stream) {
+  // every check of every layer first: a call that is refused enqueues nothing
+  if (num_layers < 0 || T < 0 || (src_host != 0 && src_host != 1) || (int8 != 0 && int8 != 1) ||
+      bt_layer_stride < 0 || num_seqs < 1 || max_blocks < 1 || bt_row_stride < max_blocks ||
+      num_pages < 1 || max_pos < 1)
+    return PKV_ERR_INVALID_ARGUMENT;
+  if (num_layers == 0 || T == 0) return PKV_OK;
+  if (!k || !v || !block_tables || !positions || !kv_pool || !rope_cos || !rope_sin)
+    return PKV_ERR_INVALID_ARGUMENT;
+  if (bt_layer_stride < (long long)num_seqs * bt_row_stride) return PKV_ERR_INVALID_ARGUMENT;
+  if (T > (1 << 30)) return PKV_ERR_UNSUPPORTED_SHAPE;
+  const uintptr_t amask = int8 ? 15u : 3u;  // the alignment each append wants of k, v and the pool
+  if (reinterpret_cast<uintptr_t>(kv_pool) & amask) return PKV_ERR_MISALIGNED;
+  const size_t rows = (size_t)T * PKV_NUM_KV_HEADS * PKV_HEAD_DIM * 2;  // bytes of k (or v) per layer
+  for (int l = 0; l < num_layers; ++l) {
+    if (!k[l] || !v[l]) return PKV_ERR_INVALID_ARGUMENT;
+    if (!src_host && ((reinterpret_cast<uintptr_t>(k[l]) | reinterpret_cast<uintptr_t>(v[l])) & amask))
+      return PKV_ERR_MISALIGNED;
+  }
+  if (src_host) {
+    if (!stage || stage_bytes < 2 * rows) return PKV_ERR_INVALID_ARGUMENT;
+    if (!aligned16(stage)) return PKV_ERR_MISALIGNED;
+    int dev = 0;  // the copies below go to the stream's device
+    const int rb = bind_stream_device(stream, &dev);
+    if (rb != PKV_OK) return rb;
+  }
+  int rc = PKV_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* sk = static_cast<uint8_t*>(stage);
+  for (int l = 0; l < num_layers; ++l) {
+    const void* kl = k[l];
+    const void* vl = v[l];
+    if (src_host) {  // the stage is reused by every layer: stream order keeps the launches apart
+      rc = cuda_status(cudaMemcpyAsync(sk, kl, rows, cudaMemcpyHostToDevice, st), "cudaMemcpyAsync(k)");
+      if (rc == PKV_OK)
+        rc = cuda_status(cudaMemcpyAsync(sk + rows, vl, rows, cudaMemcpyHostToDevice, st),
+                         "cudaMemcpyAsync(v)");
+      if (rc != PKV_OK) return rc;
+      kl = sk;
+      vl = sk + rows;
+    }
+    const int32_t* bt = block_tables + l * bt_layer_stride;
+    rc = int8 ? kv_append_rope_int8(kl, vl, positions, token_seq, T, bt, num_seqs, bt_row_stride,
+                                    max_blocks, kv_pool, num_pages, rope_cos, rope_sin, max_pos,
+                                    nullptr, nullptr, d_err, stream)
+              : kv_append_rope(kl, vl, positions, token_seq, T, bt, num_seqs, bt_row_stride,
+                               max_blocks, kv_pool, num_pages, rope_cos, rope_sin, max_pos, nullptr,
+                               nullptr, d_err, stream);
+    if (rc != PKV_OK) return rc;
+  }
+  return PKV_OK;
+}

@@ -26,7 +26,8 @@ import numpy as np
 import torch
 
 from . import (HEAD_DIM, NUM_KV_HEADS, NUM_Q_HEADS, OK, PAGE_TOKENS, PkvError, Scheduler,
-               alloc_workspace, kv_append_rope, kv_append_rope_int8, paged_gqa_decode,
+               alloc_workspace, kv_append_rope, kv_append_rope_int8, kv_append_rope_layers,
+               paged_gqa_decode,
                paged_gqa_decode_append_layers, paged_gqa_decode_int8, pkv_read_device_error,
                ERR_REQUEST_TOO_LARGE)
 
@@ -81,6 +82,12 @@ class ContinuousBatcher:
         self._block_events = [torch.cuda.Event(), torch.cuda.Event()] if pin else None
         self._turn = 0
         self._dev_block = torch.empty(nmax, dtype=torch.uint8, device=self.dev)
+        # prompt appends: positions 0.. and the row index 0 of a one-row table
+        # view, for any prompt the tables can hold; a device stage for prompt
+        # rows that come from host memory (allocated on first use)
+        self._positions = torch.arange(PAGE_TOKENS * max_blocks, dtype=torch.int32, device=self.dev)
+        self._row0 = torch.zeros(PAGE_TOKENS * max_blocks, dtype=torch.int32, device=self.dev)
+        self._stage = None
         self.prompt = {}           # request id -> prompt tokens
         self.running = []          # request ids in admission order
         self.length = {}           # request id -> KV tokens held
@@ -133,14 +140,19 @@ class ContinuousBatcher:
                 raise PkvError(7, "ContinuousBatcher.admit")
             _, self.slot[rid] = self.sched.block_table(rid, 0)
             self._sync_rows(rid)
-            pos = torch.arange(P, dtype=torch.int32, device=self.dev)
-            rows = torch.full((P,), self.slot[rid], dtype=torch.int32, device=self.dev)
-            append = kv_append_rope_int8 if self.int8 else kv_append_rope
-            for l in range(self.L):
-                k, v = prompt_kv(rid, l)
-                append(k.to(self.dev, non_blocking=True), v.to(self.dev, non_blocking=True),
-                       pos, self.tables[l], self.pool,
-                       self.cos, self.sin, token_seq=rows, d_err=self.d_err)
+            ks, vs = zip(*(prompt_kv(rid, l) for l in range(self.L)))
+            # one native call for every layer: host rows go through the stage
+            stage = None
+            if ks[0].device != self.dev:
+                need = 2 * P * NUM_KV_HEADS * HEAD_DIM * 2
+                if self._stage is None or self._stage.numel() < need:
+                    self._stage = torch.empty(2 * PAGE_TOKENS * self.M * NUM_KV_HEADS * HEAD_DIM * 2,
+                                              dtype=torch.uint8, device=self.dev)
+                stage = self._stage
+            s = self.slot[rid]
+            kv_append_rope_layers(ks, vs, self._positions[:P], self.tables[:, s:s + 1], self.pool,
+                                  self.cos, self.sin, token_seq=self._row0[:P], stage=stage,
+                                  d_err=self.d_err)
             self.length[rid] = P
             self.steps_done[rid] = 0
         self.running += admitted

@@ -75,6 +75,18 @@ def kv_append_rope_int8(k, v, positions, block_tables, kv_pool, rope_cos, rope_s
     _flag(err, d_err)
 
 
+def kv_append_rope_layers(k, v, positions, block_tables, kv_pool, rope_cos, rope_sin,
+                          token_seq=None, stage=None, d_err=None, max_blocks=None, stream=None):
+    assert len(k) == len(v) and len(k) > 0
+    assert block_tables.dtype == torch.int32 and block_tables.dim() == 3
+    assert block_tables.stride(2) == 1 and block_tables.shape[0] >= len(k)
+    assert all(t.device == k[0].device for t in list(k) + list(v))
+    append = kv_append_rope_int8 if kv_pool.dtype == torch.uint8 else kv_append_rope
+    for l in range(len(k)):
+        append(k[l], v[l], positions, block_tables[l].contiguous(), kv_pool, rope_cos, rope_sin,
+               token_seq=token_seq, d_err=d_err, max_blocks=max_blocks)
+
+
 def _write_out(out, o):
     out.copy_(torch.from_numpy(o).to(torch.bfloat16).view(out.shape))
 
@@ -159,7 +171,8 @@ def pkv_read_device_error(d_err, clear=True, stream=None):
     return code
 
 
-NAMES = ("kv_append_rope", "kv_append_rope_int8", "paged_gqa_decode", "paged_gqa_decode_int8",
+NAMES = ("kv_append_rope", "kv_append_rope_int8", "kv_append_rope_layers",
+         "paged_gqa_decode", "paged_gqa_decode_int8",
          "paged_gqa_decode_append", "paged_gqa_decode_append_int8",
          "paged_gqa_decode_append_layers", "alloc_workspace",
          "pkv_read_device_error")

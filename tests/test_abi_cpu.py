@@ -147,6 +147,26 @@ def _host_validation_checks():
               null, null) == 1
     assert A8(fake, fake, fake, null, 1, fake, 1, 128, 128, ctypes.c_void_p(0x10004), 8, fake, fake,
               2048, null, null, null, null) == 2
+    # layered append: nothing to do; a null layer entry; a missing, short or
+    # misaligned stage for host rows; a layer stride below one table; a
+    # misaligned device row; a misaligned INT8 pool -- all refused before any
+    # CUDA call (this process has no GPU, so a CUDA call would fail with 5)
+    AL = L.kv_append_rope_layers
+    arr = lambda *xs: (ctypes.c_void_p * len(xs))(*xs)
+    two = arr(fake, fake)
+    def al(k=two, v=two, n=2, host=0, stage=null, stage_bytes=0, T=4, bt_ls=1 << 16, pool=fake,
+           int8=0):
+        return AL(k, v, n, host, stage, stage_bytes, fake, null, T, fake, bt_ls, 1, 128, 128, pool,
+                  8, int8, fake, fake, 2048, null, null)
+    assert al(n=0) == 0 and al(T=0) == 0
+    assert al(k=arr(fake, null)) == 1
+    assert al(host=1) == 1
+    assert al(host=1, stage=fake, stage_bytes=2 * 4 * 1024 - 16) == 1
+    assert al(host=1, stage=ctypes.c_void_p(0x10008), stage_bytes=1 << 20) == 2
+    assert al(bt_ls=100) == 1
+    assert al(v=arr(fake, odd)) == 2
+    assert al(pool=ctypes.c_void_p(0x10004), int8=1) == 2
+    assert al(int8=2) == 1
     # INT8 decode: nothing to do; null pool; misaligned pool; bad option sets
     D8 = L.paged_gqa_decode_int8
     assert D8(null, null, 8, null, 128, 128, null, 0, 0, null, 0.125, null, 0, null, null) == 0

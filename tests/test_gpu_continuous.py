@@ -105,3 +105,55 @@ def test_native_layers_call_equals_per_layer_calls(lib, cuda_device, int8, stage
     assert torch.equal(pool_a, pool_b)
     assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
     assert torch.equal(qr_a.view(torch.int16), qr_b.view(torch.int16))
+
+
+@pytest.mark.parametrize("int8", [False, True])
+@pytest.mark.parametrize("src_host", [False, True])
+def test_layered_prompt_append_equals_per_layer_calls(lib, cuda_device, int8, src_host):
+    # kv_append_rope_layers (one C call: per layer a copy of host rows into the
+    # stage, then the append) with the batcher's one-row table view, against L
+    # kv_append_rope(_int8) calls through the full table on a copy of the same
+    # pool: the pools bit for bit, and no error
+    import numpy as np
+    import torch
+    dev = cuda_device
+    L, slots, P = 5, 6, 300
+    npg = (P + 15) // 16
+    rng = np.random.default_rng(93)
+    num_pages = L * npg + 11
+    perm = rng.permutation(num_pages).astype(np.int32)
+    slot = 4
+    tab = np.full((L, slots, 128), -1, np.int32)
+    for l in range(L):
+        tab[l, slot, :npg] = perm[l * npg:(l + 1) * npg]
+    gen = W.cpu_gen(94)
+    k = W.normal_bf16((L, P, 8, 64), gen)
+    v = W.normal_bf16((L, P, 8, 64), gen)
+    if int8:
+        pool0 = lib.new_int8_pool(num_pages, dev)
+    else:
+        pool0 = W.normal_bf16((num_pages, 2, 8, 16, 64), gen).to(dev)
+    cos_d, sin_d = lib.rope_tables_device(dev, W.MAX_CONTEXT)
+    tab_d = torch.from_numpy(tab).to(dev)
+    pos = torch.arange(P, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    per_layer = lib.kv_append_rope_int8 if int8 else lib.kv_append_rope
+    pool_a = pool0.clone()
+    rows = torch.full((P,), slot, dtype=torch.int32, device=dev)
+    kd, vd = k.to(dev), v.to(dev)
+    for l in range(L):
+        per_layer(kd[l], vd[l], pos, tab_d[l], pool_a, cos_d, sin_d, token_seq=rows, d_err=err)
+    pool_b = pool0.clone()
+    if src_host:
+        ks = [k[l].pin_memory() for l in range(L)]
+        vs = [v[l].pin_memory() for l in range(L)]
+        stage = torch.empty(2 * P * 1024, dtype=torch.uint8, device=dev)
+    else:
+        ks, vs, stage = [kd[l] for l in range(L)], [vd[l] for l in range(L)], None
+    lib.kv_append_rope_layers(ks, vs, pos, tab_d[:, slot:slot + 1], pool_b, cos_d, sin_d,
+                              token_seq=torch.zeros(P, dtype=torch.int32, device=dev), stage=stage,
+                              d_err=err)
+    torch.cuda.synchronize()
+    assert lib.pkv_read_device_error(err) == 0
+    assert torch.equal(pool_a.view(torch.uint8), pool_b.view(torch.uint8))
+    assert not torch.equal(pool_a.view(torch.uint8), pool0.view(torch.uint8))
