@@ -2310,7 +2310,8 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
                         const int32_t* seq_lens, int num_seqs, int max_seq_len, void* out,
                         float scale, void* workspace, size_t workspace_bytes, int* d_err,
                         void* stream, const pkv_decode_opts* opts, const AppendArgs* app,
-                        bool int8 = false) {
+                        bool int8 = false, int bound_dev = -1) {
+  // bound_dev >= 0: the caller has bound `stream`'s device (bind_stream_device) and passes it
   if (num_seqs < 0 || num_pages < 1 || max_blocks < 1 || bt_row_stride < max_blocks)
     return PKV_ERR_INVALID_ARGUMENT;
   if (num_seqs == 0) return PKV_OK;
@@ -2347,8 +2348,9 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
   // 32 x 2048 fused step: 26.8 -> 26.1 us/layer; on INT8 pages 20.6 -> 19.1).
   const long long pages_hint = max_seq_len > 0 ? (max_seq_len + 15) / 16 : 0;
   const int sms_hint = [&] {
-    int d = 0;
-    return cudaGetDevice(&d) == cudaSuccess ? sm_count(d) : 0;
+    int d = bound_dev;
+    if (d < 0 && cudaGetDevice(&d) != cudaSuccess) return 0;
+    return sm_count(d);
   }();
   const bool seg_pairs = !tiny && compute == PKV_COMPUTE_TENSOR && sms_hint > 0 &&
                          !(opts && (opts->warps_per_cta > 0 || opts->stages > 0 ||
@@ -2373,9 +2375,12 @@ static int decode_entry(const void* q, const void* kv_pool, int num_pages,
     return PKV_ERR_INVALID_ARGUMENT;
   if (!int8 && app && cfg != 1602 && cfg != 802 && cfg != 402) return PKV_ERR_INVALID_ARGUMENT;
 
-  int dev = 0;
-  int rc = bind_stream_device(stream, &dev);
-  if (rc != PKV_OK) return rc;
+  int dev = bound_dev;
+  int rc = PKV_OK;
+  if (dev < 0) {
+    rc = bind_stream_device(stream, &dev);
+    if (rc != PKV_OK) return rc;
+  }
   const int sms = sm_count(dev);
   if (sms <= 0) return PKV_ERR_CUDA;
   const WorkspaceLayout wl = workspace_layout(num_seqs, sms);
@@ -2555,10 +2560,10 @@ extern "C" int paged_gqa_decode_append_layers(
   int rc = decode_check_args(q, kv_pool, num_pages, block_tables, bt_row_stride, max_blocks,
                              seq_lens, num_seqs, out, scale);
   if (rc != PKV_OK) return rc;
+  int dev = 0;  // bound once for the copy and every layer's launch
+  rc = bind_stream_device(stream, &dev);
+  if (rc != PKV_OK) return rc;
   if (host_stage) {
-    int dev = 0;
-    rc = bind_stream_device(stream, &dev);
-    if (rc != PKV_OK) return rc;
     rc = cuda_status(cudaMemcpyAsync(dev_stage, host_stage, stage_bytes, cudaMemcpyHostToDevice,
                                      static_cast<cudaStream_t>(stream)),
                      "cudaMemcpyAsync(step block)");
@@ -2580,7 +2585,7 @@ extern "C" int paged_gqa_decode_append_layers(
                          qo8 ? qo8 + l * qb : nullptr};
     rc = decode_entry(q8 + l * qb, kv_pool, num_pages, block_tables + l * bt_layer_stride,
                       bt_row_stride, max_blocks, seq_lens, num_seqs, max_seq_len, o8 + l * qb,
-                      scale, workspace, workspace_bytes, d_err, stream, &opts, &app, int8 != 0);
+                      scale, workspace, workspace_bytes, d_err, stream, &opts, &app, int8 != 0, dev);
     if (rc != PKV_OK) return rc;
   }
   return PKV_OK;
