@@ -867,8 +867,7 @@ class DecodeStep:
         # the rotated queries: kept by the fused step only in a buffer of the
         # caller's; the two-kernel step needs them (its decode reads them)
         self.q_rot = q_rot if (q_rot is not None or self.fused) else torch.empty_like(q)
-        # the two-kernel graphs below, on a fused step without q_rot, rotate into this
-        self._q_scratch = None if self.q_rot is not None else q.clone()
+        self._q_scratch = None  # the two-kernel timing graphs' rotated q on a fused step without q_rot
         self.launches_per_step = (1 if self.fused else 2) * self.L
         self._launch()                      # eager run: sets up kernels and descriptors
         torch.cuda.synchronize(dev)
@@ -890,7 +889,7 @@ class DecodeStep:
                                         early_kv=int(self.overlap and l > 0),
                                         schedule=self.schedule)
             return
-        q_rot = self.q_rot if self.q_rot is not None else self._q_scratch
+        q_rot = self._rotated()
         for l in range(self.L):
             if not decode_only:
                 kv_append_rope(t["k"][l], t["v"][l], t["pos"], t["bt"][l], t["pool"], t["cos"],
@@ -908,11 +907,21 @@ class DecodeStep:
         else:
             self._launch()
 
+    def _rotated(self):
+        """The buffer the two-kernel form rotates q into: q_rot, else a
+        scratch copy of q made on first use (outside any capture: the graph
+        helpers below call this before capturing)."""
+        if self.q_rot is not None:
+            return self.q_rot
+        if self._q_scratch is None:
+            self._q_scratch = self.t["q"].clone()
+        return self._q_scratch
+
     def append_only_graph(self):
         """A graph of just the L kv_append_rope calls of the step (tokens at
         `positions`, q rotated into the step's q_rot buffer, or a scratch one)."""
         t = self.t
-        q_rot = self.q_rot if self.q_rot is not None else self._q_scratch
+        q_rot = self._rotated()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             for l in range(self.L):
@@ -922,6 +931,7 @@ class DecodeStep:
 
     def decode_only_graph(self):
         """A graph of just the L decode calls (for timing the decode kernel)."""
+        self._rotated()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             self._launch(decode_only=True)
@@ -970,7 +980,7 @@ class Int8DecodeStep:
         # the rotated queries, as for DecodeStep: kept by the fused step only
         # in a buffer of the caller's; the two-kernel step needs them
         self.q_rot = q_rot if (q_rot is not None or self.fused) else torch.empty_like(q)
-        self._q_scratch = None if self.q_rot is not None else q.clone()
+        self._q_scratch = None  # the partial graphs' rotated q on a fused step without q_rot
         self.workspace = alloc_workspace(self.S, dev) if workspace is None else workspace
         self.d_err = torch.zeros(1, dtype=torch.int32, device=dev) if d_err is None else d_err
         self.scale = float(scale)
@@ -995,7 +1005,7 @@ class Int8DecodeStep:
                                              max_seq_len=self.max_seq_len, d_err=self.d_err,
                                              early_kv=int(self.overlap and l > 0))
             return
-        q_rot = self.q_rot if self.q_rot is not None else self._q_scratch
+        q_rot = self._rotated()
         for l in range(self.L):
             if append:
                 kv_append_rope_int8(t["k"][l], t["v"][l], t["pos"], t["bt"][l], t["pool"],
@@ -1012,8 +1022,17 @@ class Int8DecodeStep:
         else:
             self._launch()
 
+    def _rotated(self):
+        """As DecodeStep._rotated."""
+        if self.q_rot is not None:
+            return self.q_rot
+        if self._q_scratch is None:
+            self._q_scratch = self.t["q"].clone()
+        return self._q_scratch
+
     def partial_graph(self, append: bool, decode: bool):
         """A graph of only the append calls or only the decode calls (for timing)."""
+        self._rotated()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             self._launch(append=append, decode=decode)
