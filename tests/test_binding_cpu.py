@@ -125,3 +125,59 @@ def test_layers_call_rejects_bad_shapes_before_any_call(rec, bad):
                                            t["out"], t["cos"], t["sin"], 0.125, t["ws"],
                                            d_err=t["err"], stream=STREAM)
     assert rec.calls == []
+
+
+def prompt_tensors(int8, L=3, P=20):
+    t = tensors(int8, L=L)
+    t["pk"] = [torch.full((P, 8, 64), float(l), dtype=BF16) for l in range(L)]
+    t["pv"] = [torch.full((P, 8, 64), -float(l), dtype=BF16) for l in range(L)]
+    t["pos"] = torch.arange(P, dtype=I32)
+    t["row0"] = torch.zeros(P, dtype=I32)
+    t["stage"] = torch.zeros(2 * P * 1024, dtype=torch.uint8)
+    return t
+
+
+@pytest.mark.parametrize("int8", [False, True])
+def test_prompt_layers_call_marshals_the_row_view(rec, int8):
+    # host rows (the pool here is on the CPU too, so the rows count as host
+    # memory): one native call with the per-layer pointer arrays, the layer
+    # stride of the full table, the one-row view's row and its row stride
+    L, P, slot = 3, 20, 4
+    t = prompt_tensors(int8, L=L, P=P)
+    view = t["bt"][:, slot:slot + 1]
+    pkv.kv_append_rope_layers(t["pk"], t["pv"], t["pos"], view, t["pool"], t["cos"], t["sin"],
+                              token_seq=t["row0"], stage=t["stage"], d_err=t["err"], stream=STREAM)
+    (name, a), = rec.take()
+    assert name == "kv_append_rope_layers"
+    ks, vs = [x for x in a[0]], [x for x in a[1]]
+    assert ks == [x.data_ptr() for x in t["pk"]] and vs == [x.data_ptr() for x in t["pv"]]
+    assert a[2:9] == (L, 1, t["stage"].data_ptr(), t["stage"].numel(), t["pos"].data_ptr(),
+                      t["row0"].data_ptr(), P)
+    assert a[9] == view.data_ptr() == t["bt"].data_ptr() + 4 * slot * 128
+    assert a[10:14] == (7 * 128, 1, 128, 128)        # layer stride, rows, row stride, max_blocks
+    assert a[14:17] == (t["pool"].data_ptr(), 11, int(int8))
+
+
+@pytest.mark.parametrize("bad", ["layers", "rows", "tables_2d", "tables_strided", "tables_layers",
+                                 "no_stage", "short_stage"])
+def test_prompt_layers_call_rejects_bad_arguments(rec, bad):
+    t = prompt_tensors(False)
+    bt, stage = t["bt"], t["stage"]
+    if bad == "layers":
+        t["pv"] = t["pv"][:2]
+    elif bad == "rows":
+        t["pk"][1] = t["pk"][1][:10].contiguous()
+    elif bad == "tables_2d":
+        bt = bt[0]
+    elif bad == "tables_strided":
+        bt = bt.transpose(1, 2)
+    elif bad == "tables_layers":
+        bt = bt[:2]
+    elif bad == "no_stage":
+        stage = None
+    elif bad == "short_stage":
+        stage = stage[:1000]
+    with pytest.raises((ValueError, TypeError)):
+        pkv.kv_append_rope_layers(t["pk"], t["pv"], t["pos"], bt, t["pool"], t["cos"], t["sin"],
+                                  token_seq=t["row0"], stage=stage, d_err=t["err"], stream=STREAM)
+    assert rec.calls == []
