@@ -341,7 +341,7 @@ def fused_case_int8(lens, seed):
     return case, codes, scales, q, k, v
 
 
-def run_fused8(lib, dev, tables, case, codes, scales, q, k, v, lens=None, bt=None):
+def run_fused8(lib, dev, tables, case, codes, scales, q, k, v, lens=None, bt=None, **kw):
     cos_d, sin_d, _, _ = tables
     lens = case.seq_lens if lens is None else lens
     bt = case.block_tables[0] if bt is None else bt
@@ -351,7 +351,7 @@ def run_fused8(lib, dev, tables, case, codes, scales, q, k, v, lens=None, bt=Non
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     lib.paged_gqa_decode_append_int8(to_dev_bf16(q, dev), to_dev_bf16(k, dev), to_dev_bf16(v, dev),
                                      pool, to_dev_i32(bt, dev), to_dev_i32(lens, dev), out, cos_d,
-                                     sin_d, 0.125, q_out=q_out, d_err=err)
+                                     sin_d, 0.125, q_out=q_out, d_err=err, **kw)
     return pool, q_out, out, lib.pkv_read_device_error(err)
 
 
@@ -475,3 +475,39 @@ def test_int8_step_graph_matches_eager_and_oracle(lib, cuda_device, tables, fuse
         assert np.array_equal(qrot_b[l], want_q)
         check_close_int8(OB.to_f64(out_b[l]), ref, f"INT8 step layer {l}")
     assert np.array_equal(pool_b, OI.pack_pages(codes, scales))
+
+
+def ragged24(seed):
+    """24 lengths in [1, 2048] with the edges 1, 16, 17 and 2048 among them."""
+    lens = np.random.default_rng(seed).integers(1, 2049, size=24).astype(np.int32)
+    lens[:4] = [1, 16, 17, 2048]
+    return lens
+
+
+def test_int8_decode_one_segment_pairs_ragged(lib, cuda_device):
+    """24 sequences at a length bound of 2048: the default launch takes 8-warp
+    CTAs, two per SM, one (sequence, KV head) segment each; ragged lengths put
+    one-page, partial and full segments side by side."""
+    case = make_case(ragged24(64), seed=64, extra_pages=9)
+    pool = W.bf16_bits(W.fill_pool(case))
+    codes, scales = OI.quantize_pool(pool)
+    q = W.bf16_bits(W.fill_queries(case))[0]
+    bt = case.block_tables[0]
+    out, code = run_decode8(lib, cuda_device, q, codes, scales, bt, case.seq_lens, max_seq_len=2048)
+    ref, _ = OI.decode_int8(q, codes, scales, bt, case.seq_lens, case.scale)
+    assert code == 0
+    check_close_int8(bf16_to_f64(out), ref, "int8, 24 ragged sequences, one segment per CTA")
+
+
+def test_int8_fused_one_segment_pairs_ragged(lib, cuda_device, tables):
+    """The fused INT8 step on the same grid: pages, rotated q and outputs."""
+    _, _, cos_o, sin_o = tables
+    case, codes, scales, q, k, v = fused_case_int8(ragged24(65), 65)
+    pool, q_out, out, code = run_fused8(lib, cuda_device, tables, case, codes, scales, q, k, v,
+                                        max_seq_len=2048)
+    wc, ws, wq, ref, e = OI.decode_step_int8(codes, scales, q, k, v, case.block_tables[0],
+                                             case.seq_lens, cos_o, sin_o, 0.125)
+    assert code == 0 and not e
+    assert same_pool(pool, wc, ws), "appended pages differ from the oracle's"
+    assert np.array_equal(bits(q_out), wq), "rotated q differs from the oracle's"
+    check_close_int8(bf16_to_f64(out), ref, "fused INT8 step, 24 ragged sequences")

@@ -500,3 +500,56 @@ def test_bounded_wait_runs_out_and_reports_timeout(lib, cuda_device, schedule):
     want, _ = OP.decode(W.bf16_bits(q), W.bf16_bits(pool), case.block_tables[0], case.seq_lens,
                         case.scale)
     check_close(bf16_to_f64(out), want, "decode after a timeout")
+
+
+def ragged24(seed):
+    """24 lengths in [1, 2048] with the edges 1, 16, 17 and 2048 among them."""
+    lens = np.random.default_rng(seed).integers(1, 2049, size=24).astype(np.int32)
+    lens[:4] = [1, 16, 17, 2048]
+    return lens
+
+
+@pytest.mark.parametrize("seed", [61, 62])
+def test_decode_one_segment_pairs_ragged(lib, cuda_device, seed):
+    """24 sequences at a length bound of 2048: the default launch takes 8-warp
+    CTAs, two per SM, one (sequence, KV head) segment each; ragged lengths put
+    one-page, partial and full segments side by side."""
+    case = make_case(ragged24(seed), seed, extra_pages=9)
+    pool = W.bf16_bits(W.fill_pool(case))
+    q = W.bf16_bits(W.fill_queries(case))[0]
+    bt = case.block_tables[0]
+    out, code = run_decode(lib, cuda_device, q, pool, bt, case.seq_lens, max_seq_len=2048)
+    ref, _ = OP.decode(q, pool, bt, case.seq_lens, case.scale)
+    assert code == 0
+    check_close(bf16_to_f64(out), ref, "24 ragged sequences, one segment per CTA")
+
+
+def test_fused_one_segment_pairs_ragged(lib, cuda_device, tables):
+    """The fused step on the same grid, two layers: pool bit for bit, rotated
+    q bit for bit, outputs against the oracle."""
+    cos_d, sin_d, cos_o, sin_o = tables
+    case = fused_case(ragged24(63), seed=63)
+    dev = cuda_device
+    pool0 = W.fill_pool(case)
+    q = W.fill_queries(case)
+    k, v = W.fill_new_kv(case)
+    pool = pool0.to(dev)
+    q_out = torch.full(q.shape, 3.0, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lens = torch.from_numpy(case.seq_lens).to(dev)
+    for l in range(case.num_layers):
+        lib.paged_gqa_decode_append(q[l].to(dev), k[l].to(dev), v[l].to(dev), pool,
+                                    torch.from_numpy(case.block_tables[l]).to(dev), lens, out[l],
+                                    cos_d, sin_d, case.scale, q_out=q_out[l], d_err=err,
+                                    max_seq_len=2048, early_kv=int(l > 0))
+    assert lib.pkv_read_device_error(err) == 0
+    want_pool = bits(pool0)
+    for l in range(case.num_layers):
+        want_pool, want_q, ref, e = OP.decode_step(want_pool, bits(q[l]), bits(k[l]), bits(v[l]),
+                                                   case.block_tables[l], case.seq_lens, cos_o,
+                                                   sin_o, case.scale)
+        assert not e
+        assert np.array_equal(bits(q_out[l]), want_q)
+        check_close(bf16_to_f64(out[l]), ref, f"fused, 24 ragged sequences, layer {l}")
+    assert np.array_equal(bits(pool), want_pool)
