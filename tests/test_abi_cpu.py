@@ -343,3 +343,36 @@ def test_scheduler_misuse_is_refused_without_state_change():
         assert free.value == 16
     finally:
         lib.pkv_sched_destroy(s)
+
+
+def test_int8_block_format_of_the_kernels_matches_the_oracle(tmp_path):
+    """The byte positions the append and decode kernels use (csrc/i8_layout.cuh,
+    compiled here for the host) against the oracle's own statement of the
+    block format (int8_kv.block_positions), for every code and scale byte, and
+    the stored byte of every code."""
+    import shutil
+    from oracle import int8_kv as OI
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None:
+        pytest.skip("no C++ compiler")
+    src = tmp_path / "layout.cpp"
+    src.write_text(
+        "#include <cstdio>\n#define __host__\n#define __device__\n"
+        f'#include "{B.CSRC}/i8_layout.cuh"\n'
+        "using namespace pkv;\nint main() {\n"
+        "  for (int t = 0; t < 16; ++t) for (int d = 0; d < 64; ++d)\n"
+        "    printf(\"%u %u\\n\", i8_k_byte(t, d), i8_v_byte(t, d));\n"
+        "  for (int t = 0; t < 16; ++t) printf(\"%u %u\\n\", i8_k_scale_byte(t), i8_v_scale_byte(t));\n"
+        "  for (int c = -128; c < 128; ++c) printf(\"%u\\n\", (unsigned)i8_code_byte((signed char)c));\n"
+        "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    r = subprocess.run([cxx, "-std=c++17", "-O0", str(src), "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    lines = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    kv = np.array([list(map(int, ln.split())) for ln in lines[:1024]])
+    sc = np.array([list(map(int, ln.split())) for ln in lines[1024:1040]])
+    cb = np.array([int(ln) for ln in lines[1040:1296]])
+    k, v, ks, vs = OI.block_positions()
+    assert np.array_equal(kv[:, 0].reshape(16, 64), k) and np.array_equal(kv[:, 1].reshape(16, 64), v)
+    assert np.array_equal(sc[:, 0], ks) and np.array_equal(sc[:, 1], vs)
+    assert np.array_equal(cb, (np.arange(-128, 128) + 128) % 256)   # code + 128 as a byte
