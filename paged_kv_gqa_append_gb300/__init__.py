@@ -438,8 +438,10 @@ def kv_append_rope_int8(k, v, positions, block_tables, kv_pool, rope_cos, rope_s
 
 def paged_gqa_decode_int8(q, kv_pool, block_tables, seq_lens, out, scale, workspace=None,
                           max_seq_len=None, d_err=None, max_blocks=None, min_units_per_warp=0,
-                          ctas_per_sm=0, stages=0, warps_per_cta=0, stream=None):
-    """paged_gqa_decode over INT8 pages."""
+                          ctas_per_sm=0, stages=0, warps_per_cta=0, early_kv=0, stream=None):
+    """paged_gqa_decode over INT8 pages (early_kv as for paged_gqa_decode: the
+    lengths, tables and first pages are read before the previous kernel on the
+    stream has finished, which must not write them)."""
     dev = kv_pool.device
     _need_i8_pool(kv_pool, dev)
     _need(q, "q", torch.bfloat16, dev, (NUM_Q_HEADS, HEAD_DIM))
@@ -465,11 +467,11 @@ def paged_gqa_decode_int8(q, kv_pool, block_tables, seq_lens, out, scale, worksp
     args = (_ptr(q), _ptr(kv_pool), kv_pool.shape[0], _ptr(block_tables), stride, mb,
             _ptr(seq_lens), S, int(max_seq_len), _ptr(out), float(scale), _ptr(workspace),
             workspace.numel(), _ptr(d_err), _stream(stream))
-    if not (min_units_per_warp or ctas_per_sm or stages or warps_per_cta):
+    if not (min_units_per_warp or ctas_per_sm or stages or warps_per_cta or early_kv):
         st = _L().paged_gqa_decode_int8(*args)
     else:
         opts = DecodeOpts(COMPUTE_TENSOR, min_units_per_warp, ctas_per_sm, stages, warps_per_cta,
-                          0, 0, 0)
+                          0, SCHEDULE_AUTO, int(bool(early_kv)))
         st = _L().paged_gqa_decode_int8_ex(*args, ctypes.byref(opts))
     _check(st, "paged_gqa_decode_int8")
 
@@ -1012,9 +1014,12 @@ class Int8DecodeStep:
                                     t["cos"], t["sin"], q_in=t["q"][l], q_out=q_rot[l],
                                     d_err=self.d_err)
             if decode:
+                # a decode-only graph (timing) has no append between the layers:
+                # layers >= 1 may stage their pages early, as in DecodeStep
                 paged_gqa_decode_int8(q_rot[l], t["pool"], t["bt"][l], t["lens"], t["out"][l],
                                       self.scale, workspace=self.workspace,
-                                      max_seq_len=self.max_seq_len, d_err=self.d_err)
+                                      max_seq_len=self.max_seq_len, d_err=self.d_err,
+                                      early_kv=int(self.overlap and not append and l > 0))
 
     def run(self):
         if self.graph is not None:

@@ -908,7 +908,7 @@ template <int kP>
 struct MmaI8State {
   static_assert(kP == 1 || kP == 2, "one or two pages per unit");
   using Token = NewTokenI8<kP>;
-  static constexpr int kTokenBytes = 3 * 32 * 4;  // the new token's codes and scales, per warp
+  static constexpr int kTokenBytes = 4 * 128;  // the new token's K, V, cos and sin rows, per warp
   static constexpr bool kBf16Pages = false;
   static constexpr int kPagesPerUnit = kP;
   static constexpr int kBlock = PKV_I8_BLOCK_BYTES;     // one (page, head): 2176 bytes
@@ -1210,35 +1210,47 @@ struct NewToken {
 // attention sees them -- and into the pool.
 template <int kP>
 struct NewTokenI8 {
-  // Nothing is held in registers, which the page loop needs: the token goes
-  // to the warp's area in shared memory, per lane the stored code bytes (K
-  // dims lane, lane + 32, V dims lane, lane + 32), then the K scale, then the
-  // V scale.
+  // Nothing is held in registers, which the page loop needs, and nothing
+  // waits at the segment's start: the token's K row, V row and the cos and
+  // sin rows of its position (128 bytes each) are copied into the warp's
+  // area in shared memory by cp.async (one 16-byte piece per lane), and are
+  // rotated and quantised at the page that receives the token.
+  static constexpr uint32_t kK = 0, kV = 128, kCos = 256, kSin = 384;
 
   __device__ __forceinline__ void load(const DecodeParams& p, int s, int g, int pos, int lane,
                                     uint32_t area) {
-    const uint16_t* kr = p.k_new + ((size_t)s * PKV_NUM_KV_HEADS + g) * 64;
-    const uint16_t* vr = p.v_new + ((size_t)s * PKV_NUM_KV_HEADS + g) * 64;
-    const float c = __ldg(p.rope_cos + (size_t)pos * PKV_ROPE_PAIRS + lane);
-    const float sn = __ldg(p.rope_sin + (size_t)pos * PKV_ROPE_PAIRS + lane);
-    uint16_t r0, r1;
-    rope_pair(__ldg(kr + lane), __ldg(kr + lane + 32), c, sn, r0, r1);
-    int8_t k0, k1, v0, v1;
-    const float ks = quantize_pair(__uint_as_float((uint32_t)r0 << 16),
-                                   __uint_as_float((uint32_t)r1 << 16), k0, k1);
-    const float vs = quantize_pair(__uint_as_float((uint32_t)__ldg(vr + lane) << 16),
-                                   __uint_as_float((uint32_t)__ldg(vr + lane + 32) << 16), v0, v1);
-    const uint32_t codes = (uint32_t)i8_code_byte(k0) | ((uint32_t)i8_code_byte(k1) << 8) |
-                           ((uint32_t)i8_code_byte(v0) << 16) | ((uint32_t)i8_code_byte(v1) << 24);
-    asm volatile("st.shared.u32 [%0], %1;" ::"r"(area + 4u * lane), "r"(codes) : "memory");
-    asm volatile("st.shared.f32 [%0], %1;" ::"r"(area + 128u + 4u * lane), "f"(ks) : "memory");
-    asm volatile("st.shared.f32 [%0], %1;" ::"r"(area + 256u + 4u * lane), "f"(vs) : "memory");
+    const int part = lane >> 3, piece = lane & 7;
+    const size_t row = ((size_t)s * PKV_NUM_KV_HEADS + g) * 64;
+    const void* src = part == 0 ? static_cast<const void*>(p.k_new + row)
+                    : part == 1 ? static_cast<const void*>(p.v_new + row)
+                    : static_cast<const void*>((part == 2 ? p.rope_cos : p.rope_sin) +
+                                               (size_t)pos * PKV_ROPE_PAIRS);
+    cp_async16(area + 128u * (uint32_t)part + 16u * (uint32_t)piece,
+               static_cast<const uint8_t*>(src) + 16 * piece);
+    cp_async_commit();
   }
 
   // The unit staged at `base` (first page id `pid`) of sequence `seq` holds
   // position pos.
   __device__ __forceinline__ void insert_at(const DecodeParams& p, uint32_t base, int pid, int seq,
                                             int g, int pos, int lane, uint32_t area) const {
+    cp_async_wait_all();
+    __syncwarp();  // every lane's piece has landed
+    uint16_t kd0, kd1, vd0, vd1;
+    float c, sn;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(kd0) : "r"(area + kK + 2u * lane) : "memory");
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(kd1) : "r"(area + kK + 2u * (lane + 32)) : "memory");
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(vd0) : "r"(area + kV + 2u * lane) : "memory");
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(vd1) : "r"(area + kV + 2u * (lane + 32)) : "memory");
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(c) : "r"(area + kCos + 4u * lane) : "memory");
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sn) : "r"(area + kSin + 4u * lane) : "memory");
+    uint16_t r0, r1;
+    rope_pair(kd0, kd1, c, sn, r0, r1);
+    int8_t k0, k1, v0, v1;
+    const float ks = quantize_pair(__uint_as_float((uint32_t)r0 << 16),
+                                   __uint_as_float((uint32_t)r1 << 16), k0, k1);
+    const float vs = quantize_pair(__uint_as_float((uint32_t)vd0 << 16),
+                                   __uint_as_float((uint32_t)vd1 << 16), v0, v1);
     const int lp = pos / PKV_PAGE_TOKENS, slot = pos % PKV_PAGE_TOKENS;
     const int pg = kP == 2 ? (lp & 1) : 0;  // the token's page within the unit
     const int page = pg == 0 ? pid : __ldg(p.block_tables + (size_t)seq * p.bt_stride + lp);
@@ -1246,21 +1258,16 @@ struct NewTokenI8 {
     uint8_t* gblk = p.pool_i8 + ((size_t)page * PKV_NUM_KV_HEADS + g) * PKV_I8_BLOCK_BYTES;
     const uint32_t k0o = i8_k_byte(slot, lane), k1o = i8_k_byte(slot, lane + 32);
     const uint32_t v0o = i8_v_byte(slot, lane), v1o = i8_v_byte(slot, lane + 32);
-    uint32_t codes;
-    float ks, vs;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(codes) : "r"(area + 4u * lane) : "memory");
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(ks) : "r"(area + 128u + 4u * lane) : "memory");
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(vs) : "r"(area + 256u + 4u * lane) : "memory");
-    const uint16_t k0 = codes & 0xFFu, k1 = (codes >> 8) & 0xFFu, v0 = (codes >> 16) & 0xFFu,
-                   v1 = codes >> 24;
-    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + k0o), "h"(k0) : "memory");
-    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + k1o), "h"(k1) : "memory");
-    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + v0o), "h"(v0) : "memory");
-    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + v1o), "h"(v1) : "memory");
-    gblk[k0o] = (uint8_t)k0;
-    gblk[k1o] = (uint8_t)k1;
-    gblk[v0o] = (uint8_t)v0;
-    gblk[v1o] = (uint8_t)v1;
+    const uint16_t b0 = i8_code_byte(k0), b1 = i8_code_byte(k1), b2 = i8_code_byte(v0),
+                   b3 = i8_code_byte(v1);
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + k0o), "h"(b0) : "memory");
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + k1o), "h"(b1) : "memory");
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + v0o), "h"(b2) : "memory");
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(blk + v1o), "h"(b3) : "memory");
+    gblk[k0o] = (uint8_t)b0;
+    gblk[k1o] = (uint8_t)b1;
+    gblk[v0o] = (uint8_t)b2;
+    gblk[v1o] = (uint8_t)b3;
     if (lane == 0) {
       const uint32_t kso = i8_k_scale_byte(slot), vso = i8_v_scale_byte(slot);
       asm volatile("st.shared.f32 [%0], %1;" ::"r"(blk + kso), "f"(ks) : "memory");
@@ -1557,6 +1564,9 @@ __global__ void __launch_bounds__(kWarps * 32, State::min_blocks(kWarps))
         (void)mbar_wait_bounded(bars + 8 * stage, (uint32_t)(u / kStages) & 1u, kWaitLimitUs);
       }
     }
+    // a new token's rows copied into shared memory for a page never reached
+    // (an error or a timeout skipped it) must land before the CTA exits
+    if (kAppend && !State::kBf16Pages) cp_async_wait_all();
   } else if (p.early) {
     pdl_wait();
   }

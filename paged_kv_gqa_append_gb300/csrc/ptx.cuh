@@ -132,6 +132,15 @@ __device__ __forceinline__ void mma_bf16_16816_full(float (&d)[4], uint32_t a0, 
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// 16 bytes global -> shared without passing through registers (both
+// addresses 16-byte aligned); complete, for this thread, after
+// cp_async_wait_all.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // The transpose of an 8 x 8 matrix of 16-bit values held in the warp's
 // fragment layout (lane l: row l / 4, columns 2 (l % 4) and + 1).
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {

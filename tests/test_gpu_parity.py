@@ -371,6 +371,14 @@ def test_decode_step_graph_matches_eager_and_oracle(lib, cuda_device, tables, fu
         assert step.error() == 0
         outs.append((bits(out), bits(pool), bits(step.q_rot)))
     assert all(np.array_equal(a, b) for a, b in zip(outs[0], outs[1]))
+    # the decode-only graph of the step (layers >= 1 staging early) over the
+    # step's pool and rotated q gives the step's output bit for bit
+    if fused:
+        out_step = out.clone()
+        g = step.decode_only_graph()
+        g.replay()
+        assert step.error() == 0
+        assert torch.equal(out.view(torch.int16), out_step.view(torch.int16))
     # without a q_rot buffer the fused step keeps no rotated queries; the rest is the same
     pool = pool0.clone()
     out = torch.empty_like(q)
