@@ -876,25 +876,31 @@ __device__ __forceinline__ float pow2_biased(int k) {
   return __int_as_float(min(max(k, 1), 254) << 23);
 }
 
-// Rotation of the q words of an INT8-page decode lane at position pos (dims d
-// and d + 32 sit in lanes c and c ^ 2 of a row), and their store to q_out
-// when `write_q`.
-__device__ __forceinline__ void rotate_q_i8(const DecodeParams& p, uint32_t (&w)[8], size_t row, int pos,
+// Rotation of the q words of an INT8-page decode lane (dims d and d + 32 sit
+// in lanes c and c ^ 2 of a row) by the cos/sin pairs `rc`, `rs` (pairs
+// 16 (c % 2) .. + 15 of the position's row), and their store to q_out when
+// `write_q`.
+__device__ __forceinline__ void rotate_q_i8(const DecodeParams& p, uint32_t (&w)[8],
+                                         const float4 (&rc)[4], const float4 (&rs)[4], size_t row,
                                          bool write_q, int lane) {
   const int gq = lane >> 2, c = lane & 3;
-  const float* cr = p.rope_cos + (size_t)pos * PKV_ROPE_PAIRS + 16 * (c & 1);
-  const float* sr = p.rope_sin + (size_t)pos * PKV_ROPE_PAIRS + 16 * (c & 1);
+  // Each lane makes only its own dims: own * cos + partner' * sin with
+  // partner' = -partner for d < 32 (x_d cos - x_(d+32) sin) and partner for
+  // d >= 32 (x_(d-32) sin + x_d cos).  The products and the sum are rounded
+  // separately, as in rope_pair (the sign is exact, the sum commutes).
+  const uint32_t pflip = c < 2 ? 0x80008000u : 0u;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const uint32_t o = __shfl_xor_sync(0xffffffffu, w[k], 2);  // the partner dims (d +- 32)
+    const uint32_t o = __shfl_xor_sync(0xffffffffu, w[k], 2) ^ pflip;  // the partner dims (d +- 32)
     if (gq < 4) {
-      const uint32_t x0 = c < 2 ? w[k] : o, x1 = c < 2 ? o : w[k];
-      const float2 cs = __ldg(reinterpret_cast<const float2*>(cr) + k);
-      const float2 sn = __ldg(reinterpret_cast<const float2*>(sr) + k);
-      uint16_t a0, b0, a1, b1;
-      rope_pair((uint16_t)(x0 & 0xFFFFu), (uint16_t)(x1 & 0xFFFFu), cs.x, sn.x, a0, b0);
-      rope_pair((uint16_t)(x0 >> 16), (uint16_t)(x1 >> 16), cs.y, sn.y, a1, b1);
-      w[k] = c < 2 ? ((uint32_t)a0 | ((uint32_t)a1 << 16)) : ((uint32_t)b0 | ((uint32_t)b1 << 16));
+      const float4 cq = rc[k >> 1], sq = rs[k >> 1];
+      const float c0 = (k & 1) ? cq.z : cq.x, c1 = (k & 1) ? cq.w : cq.y;
+      const float s0 = (k & 1) ? sq.z : sq.x, s1 = (k & 1) ? sq.w : sq.y;
+      const float r0 = __fadd_rn(__fmul_rn(__uint_as_float(w[k] << 16), c0),
+                                 __fmul_rn(__uint_as_float(o << 16), s0));
+      const float r1 = __fadd_rn(__fmul_rn(__uint_as_float(w[k] & 0xFFFF0000u), c1),
+                                 __fmul_rn(__uint_as_float(o & 0xFFFF0000u), s1));
+      w[k] = pack_bf16x2(r0, r1);
     }
   }
   if (write_q && p.q_out != nullptr && gq < 4) {
@@ -942,13 +948,22 @@ struct MmaI8State {
     const int gq = lane >> 2, c = lane & 3;
     uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
     const size_t row = ((size_t)s * PKV_NUM_Q_HEADS + g * 4 + gq) * 64 + 16 * c;
+    // the position's cos/sin pairs, requested together with q (not after it)
+    float4 rc[4], rs[4];
+    if (kAppend) {
+      const size_t t = (size_t)pos * PKV_ROPE_PAIRS + 16 * (c & 1);
+      const float4* cr = reinterpret_cast<const float4*>(p.rope_cos + t);
+      const float4* sr = reinterpret_cast<const float4*>(p.rope_sin + t);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) rc[j] = __ldg(cr + j), rs[j] = __ldg(sr + j);
+    }
     if (gq < 4) {  // words 8c .. 8c+7 of the row: dims 16c .. 16c+15
       const uint4* src = reinterpret_cast<const uint4*>(p.q + row);
       const uint4 a = __ldg(src), b = __ldg(src + 1);
       w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
       w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
     }
-    if (kAppend) rotate_q_i8(p, w, row, pos, write_q, lane);
+    if (kAppend) rotate_q_i8(p, w, rc, rs, row, write_q, lane);
     // largest |q| of the group (4 heads) -> factor 2^(14 - e), 2^e <= max < 2^(e+1)
     uint32_t amax = 0u;
 #pragma unroll

@@ -51,3 +51,25 @@ def check_close_int8(gpu, ref, what=""):
     assert err.mean() <= MEAN_ABS_TOL + rounding, \
         f"{what}: mean |err| {err.mean():.3e} (output rounding alone {rounding:.3e})"
     return float(err.max()), float(err.mean())
+
+
+def cancelling_rows(seed, positions, heads, cos_o, sin_o):
+    """bf16 bits [len(positions), heads, 64] whose rotation at the row's
+    position nearly cancels: for even pairs i, x_(i+32) ~ x_i cos / sin, so
+    x_i cos - x_(i+32) sin ~ 0; for odd pairs x_(i+32) ~ -x_i sin / cos, so
+    x_i sin + x_(i+32) cos ~ 0 (random where the ratio is out of range).
+    Near cancellation a fused multiply-add rounds differently from the two
+    rounded products and the rounded sum that the rotation prescribes, often
+    enough to show in the bf16 results."""
+    g = np.random.default_rng(seed)
+    n = len(positions)
+    pos = np.asarray(positions, np.int64)
+    x0 = OB.from_f32_rne(g.standard_normal((n, heads, 32)).astype(np.float32))
+    c = cos_o[pos][:, None, :].astype(np.float64)
+    s = sin_o[pos][:, None, :].astype(np.float64)
+    even = np.arange(32) % 2 == 0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(even, c / s, -s / c)
+    ok = np.isfinite(ratio) & (np.abs(ratio) < 64.0)
+    x1 = np.where(ok, OB.to_f64(x0) * np.where(ok, ratio, 0.0), g.standard_normal((n, heads, 32)))
+    return np.concatenate([x0, OB.from_f32_rne(x1.astype(np.float32))], axis=-1)

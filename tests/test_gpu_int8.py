@@ -14,7 +14,7 @@ import torch
 
 import workloads as W
 from oracle import bf16 as OB, int8_kv as OI, rope as OR
-from tests._util import (bf16_to_f64, bits, check_close_int8,
+from tests._util import (cancelling_rows, bf16_to_f64, bits, check_close_int8,
                          to_dev_bf16, to_dev_i32)
 from tests.test_gpu_parity import edge_case, make_case, rand_bits
 
@@ -519,3 +519,43 @@ def test_int8_fused_one_segment_pairs_ragged(lib, cuda_device, tables):
     assert same_pool(pool, wc, ws), "appended pages differ from the oracle's"
     assert np.array_equal(bits(q_out), wq), "rotated q differs from the oracle's"
     check_close_int8(bf16_to_f64(out), ref, "fused INT8 step, 24 ragged sequences")
+
+
+@pytest.mark.parametrize("shape", ["ragged24", "mixed12"])
+def test_int8_rotations_round_separately_on_cancelling_pairs(lib, cuda_device, tables, shape):
+    """q and new K rows whose pairs nearly cancel under the rotation (a fused
+    multiply-add gives other bits there): the fused INT8 step's rotated q and
+    quantised K, and the INT8 append kernel's, are the oracle's bit for bit.
+    24 ragged sequences take the one-segment 8-warp grid, 12 mixed ones the
+    default 16-warp CTAs."""
+    cos_d, sin_d, cos_o, sin_o = tables
+    dev = cuda_device
+    lens = ragged24(67) if shape == "ragged24" else \
+        np.array([2, 16, 17, 32, 33, 48, 49, 700, 2048, 5, 1023, 100], np.int32)
+    case, codes, scales, _, _, v = fused_case_int8(lens, 67)
+    S = len(lens)
+    pos = (case.seq_lens - 1).astype(np.int32)
+    q = cancelling_rows(670, pos, 32, cos_o, sin_o)
+    k = cancelling_rows(671, pos, 8, cos_o, sin_o)
+    bt = case.block_tables[0]
+    pool, q_out, out, code = run_fused8(lib, dev, tables, case, codes, scales, q, k, v,
+                                        max_seq_len=2048)
+    wc, ws, wq, ref, e = OI.decode_step_int8(codes, scales, q, k, v, bt, case.seq_lens, cos_o,
+                                             sin_o, 0.125)
+    assert code == 0 and not e
+    assert np.array_equal(bits(q_out), wq), "fused INT8 step: rotated q"
+    assert same_pool(pool, wc, ws), "fused INT8 step: appended pages"
+    check_close_int8(bf16_to_f64(out), ref, "fused INT8 step on cancelling pairs")
+    seqs = np.arange(S, dtype=np.int32)
+    want_c, want_s, want_q, e = OI.append_rope_int8(codes, scales, k, v, pos, seqs, bt, cos_o,
+                                                    sin_o, q)
+    assert not e
+    pool_d = dev_pool(codes, scales, dev)
+    q_out = torch.empty((S, 32, 64), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lib.kv_append_rope_int8(to_dev_bf16(k, dev), to_dev_bf16(v, dev), to_dev_i32(pos, dev),
+                            to_dev_i32(bt, dev), pool_d, cos_d, sin_d, token_seq=to_dev_i32(seqs, dev),
+                            q_in=to_dev_bf16(q, dev), q_out=q_out, d_err=err)
+    assert lib.pkv_read_device_error(err) == 0
+    assert np.array_equal(bits(q_out), want_q), "INT8 append kernel: rotated q"
+    assert same_pool(pool_d, want_c, want_s), "INT8 append kernel: appended pages"

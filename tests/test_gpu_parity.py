@@ -11,7 +11,7 @@ import torch
 
 import workloads as W
 from oracle import bf16 as OB, paged_kv as OP, rope as OR
-from tests._util import (bf16_to_f64, bits, check_close, to_dev_bf16, to_dev_i32)
+from tests._util import (cancelling_rows, bf16_to_f64, bits, check_close, to_dev_bf16, to_dev_i32)
 
 pytestmark = pytest.mark.gpu
 
@@ -561,3 +561,52 @@ def test_fused_one_segment_pairs_ragged(lib, cuda_device, tables):
         assert np.array_equal(bits(q_out[l]), want_q)
         check_close(bf16_to_f64(out[l]), ref, f"fused, 24 ragged sequences, layer {l}")
     assert np.array_equal(bits(pool), want_pool)
+
+
+# ------------------------------------------------ rounding of the rotations --
+
+@pytest.mark.parametrize("warps,schedule", [(0, 0), (4, 0), (0, 1)])
+def test_rotations_round_separately_on_cancelling_pairs(lib, cuda_device, tables, warps, schedule):
+    """q and new K rows whose pairs nearly cancel under the rotation, where a
+    fused multiply-add gives other bits: the fused step's rotated q and K (and,
+    on the default grid, the append kernel's) are the oracle's, bit for bit.
+    24 ragged sequences: by default the one-segment 8-warp grid; 4-warp CTAs
+    and the dynamic schedule are the other grids."""
+    cos_d, sin_d, cos_o, sin_o = tables
+    dev = cuda_device
+    case = fused_case(ragged24(66), seed=66, layers=1)
+    S = len(case.seq_lens)
+    pos = (case.seq_lens - 1).astype(np.int32)
+    q = cancelling_rows(660, pos, 32, cos_o, sin_o)
+    k = cancelling_rows(661, pos, 8, cos_o, sin_o)
+    v = rand_bits(662, (S, 8, 64))
+    pool0 = bits(W.fill_pool(case))
+    bt = case.block_tables[0]
+    want_pool, want_q, ref, e = OP.decode_step(pool0, q, k, v, bt, case.seq_lens, cos_o, sin_o,
+                                               case.scale)
+    assert not e
+    pool = to_dev_bf16(pool0, dev)
+    q_out = torch.full((S, 32, 64), 3.0, dtype=torch.bfloat16, device=dev)
+    out = torch.empty((S, 32, 64), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lib.paged_gqa_decode_append(to_dev_bf16(q, dev), to_dev_bf16(k, dev), to_dev_bf16(v, dev), pool,
+                                to_dev_i32(bt, dev), to_dev_i32(case.seq_lens, dev), out, cos_d,
+                                sin_d, case.scale, q_out=q_out, d_err=err, warps_per_cta=warps,
+                                max_seq_len=2048, schedule=schedule)
+    assert lib.pkv_read_device_error(err) == 0
+    assert np.array_equal(bits(q_out), want_q), "fused step: rotated q"
+    assert np.array_equal(bits(pool), want_pool), "fused step: appended K/V"
+    check_close(bf16_to_f64(out), ref, "fused step on cancelling pairs")
+    if warps or schedule:
+        return
+    seqs = np.arange(S, dtype=np.int32)
+    want_pool, want_q, e = OP.append_rope(pool0, k, v, pos, seqs, bt, cos_o, sin_o, q)
+    assert not e
+    pool = to_dev_bf16(pool0, dev)
+    q_out = torch.empty((S, 32, 64), dtype=torch.bfloat16, device=dev)
+    lib.kv_append_rope(to_dev_bf16(k, dev), to_dev_bf16(v, dev), to_dev_i32(pos, dev),
+                       to_dev_i32(bt, dev), pool, cos_d, sin_d, token_seq=to_dev_i32(seqs, dev),
+                       q_in=to_dev_bf16(q, dev), q_out=q_out, d_err=err)
+    assert lib.pkv_read_device_error(err) == 0
+    assert np.array_equal(bits(q_out), want_q), "append kernel: rotated q"
+    assert np.array_equal(bits(pool), want_pool), "append kernel: appended K/V"

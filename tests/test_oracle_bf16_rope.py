@@ -155,3 +155,29 @@ def test_rotate_bf16_close_to_exact():
         got = bf16.to_f64(rope.rotate_bf16(x[i], cos[p], sin[p]))
         # bf16 half-ulp of the result plus the fp32 table/op error
         assert np.all(np.abs(got - exact) <= 2.0 ** -8 * np.abs(exact) + 1e-6 * (1 + np.abs(x[i]).max()))
+
+
+def test_cancelling_rows_expose_a_fused_multiply_add():
+    """The GPU tests' near-cancelling inputs tell the prescribed rounding (two
+    rounded products, a rounded sum) from a fused multiply-add: a copy of the
+    rotation with either product fused into the sum, a planted mistake, gives
+    other bf16 bits in hundreds of the 73,728 values."""
+    from tests._util import cancelling_rows
+    cos, sin = rope.table(rope.inv_freq_llama3(), 2048)
+    pos = np.array([1, 16, 47, 100, 333, 700, 1023, 1500, 2047] * 4)
+    x = cancelling_rows(7, pos, 32, cos, sin)
+    want = np.stack([rope.rotate_bf16(x[i], cos[p], sin[p]) for i, p in enumerate(pos)])
+    f = bf16.to_f64(x)
+    x0, x1 = f[..., :32], f[..., 32:]
+    c = cos[pos][:, None, :].astype(np.float64)
+    s = sin[pos][:, None, :].astype(np.float64)
+    r32 = rope._f32
+    # near cancellation both operands of the sum have nearly one exponent, so
+    # the FP64 sum of an exact product (bf16 x fp32: 32 bits) and a rounded
+    # one is exact and one rounding to fp32 is the fused result
+    for r0, r1 in [(r32(x0 * c - r32(x1 * s)), r32(x0 * s + r32(x1 * c))),
+                   (r32(r32(x0 * c) - x1 * s), r32(r32(x0 * s) + x1 * c))]:
+        fused = np.concatenate([bf16.from_f32_rne(r0.astype(np.float32)),
+                                bf16.from_f32_rne(r1.astype(np.float32))], axis=-1)
+        differ = int(np.count_nonzero(fused != want))
+        assert differ > 200, differ
