@@ -168,7 +168,12 @@ int kv_append_rope(const void* k, const void* v, const int32_t* positions,
  *   block_tables  device int32 [num_seqs][bt_row_stride]
  *   seq_lens      device int32 [num_seqs]
  *   max_seq_len   host upper bound of seq_lens (sizes the grid; a larger
- *                 actual length is still handled correctly)
+ *                 actual length is still handled correctly; 0: none, then
+ *                 16 max_blocks).  The bound also picks the L2 policy of the
+ *                 page copies: when num_seqs x 8 heads x its pages reach
+ *                 64 MiB of K/V, half of the L2, the pages are copied under
+ *                 the evict-first policy; below that, the default policy
+ *                 leaves them in L2 for the next read
  *   out           device bf16 [num_seqs][32][64]
  *   workspace     device memory of at least
  *                 paged_gqa_decode_workspace_bytes(num_seqs) bytes, 16-byte
