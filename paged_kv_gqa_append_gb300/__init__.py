@@ -957,8 +957,8 @@ class Int8DecodeStep:
                                      seq_lens, out[l], cos, sin, q_out=q_rot[l])
     which places token s at seq_lens[s] - 1 (positions unused).  The default
     (fused=None) is the fused form, the faster one at every batch measured (on
-    GB300 at 2048 tokens a sequence: 32 sequences 19.1 vs 24.4 us/layer, 256
-    sequences 100.2 vs 106.1).  With
+    GB300 at 2048 tokens a sequence: 32 sequences 17.5 vs 23.1 us/layer, 256
+    sequences 96.6 vs 108.4).  With
     overlap_layers (the default) layer l >= 1 reads its tables and stages its
     first pages before layer l - 1's kernel has finished, which requires the
     layers' block tables to name disjoint pages.  Tensors are bound at
